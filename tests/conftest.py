@@ -1,0 +1,21 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
+
+
+@pytest.fixture(scope="session")
+def built():
+    """Build the C/CUDA artefacts once if they are missing (nvcc cross-compiles without a GPU)."""
+    import __graft_entry__ as g
+    if not g.artefacts_present():
+        g.build()
+    return True
