@@ -1,0 +1,423 @@
+"""Benchmark of the selected-token log-probability hot path on GB300.
+
+A step is one fused forward+backward call (rlk_logp_bwd with lse_in = NULL)
+over the GRPO batch: T = 65536 rows (32 x 2048) of BF16 logits
+[65536, 152576] (V_real = 151936, 64 tiles), upstream g = A_b * mask /
+active_count; it writes BF16 dlogits [65536, 152576] plus FP32 logp and LSE.
+Every row is read once and written once.  Inputs (20 GB) are larger than L2,
+so no flush is needed between steps.
+
+Prints ONE JSON line on rank 0.  ``--impl reference`` times the FP64 CPU
+oracle instead, on a bounded sample of the same workload.
+
+Multi-GPU (torchrun): token rows are independent, so each rank runs its own
+full batch with no collective on the data path (weak scaling); the time is the
+max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd logprob tokens/s and achieved HBM GB/s (% of GB300 roofline)"
+UNIT = "tokens/s"
+KERNEL_SOURCES = [
+    "vocab_selected_token_tile_gb300/csrc/logp_stream.cu",
+    "vocab_selected_token_tile_gb300/csrc/rlk_ptx.cuh",
+]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--vtp", type=int, default=2)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--extra", action="store_true", help="also time the forward-only and split paths")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1885.4)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(kernel, {}).get(workload)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# --------------------------------------------------------------------------- CPU oracle leg
+
+def time_oracle(w, budget_s=15.0, max_rows=512):
+    """The FP64 oracle, as it stands, on a seeded row sample of the workload; tokens/s."""
+    import numpy as np
+
+    import oracle
+    from synth import workloads as W
+    tgt = W.targets(w)
+    active = W.active_rows(w, tgt=tgt)
+    g = W.grad(w, active)
+    rng = np.random.default_rng(0)
+    order = rng.permutation(w.T)
+    done = 0
+    t_total = 0.0
+    chunk = 16
+    while done < max_rows and t_total < budget_s:
+        rows = np.sort(order[done:done + chunk])
+        bits = np.concatenate([W.logits_host(w, row0=int(r), nrows=1) for r in rows])
+        t0 = time.perf_counter()
+        oracle.selected_logp(bits, tgt[rows], active[rows], w.v_real)
+        oracle.dlogits(bits, tgt[rows], active[rows], g[rows], w.v_real, w.v_padded)
+        t_total += time.perf_counter() - t0
+        done += len(rows)
+    return done / t_total, done, t_total
+
+
+# --------------------------------------------------------------------------- GPU leg
+
+def run_ours(args, ws, rank, local):
+    import numpy as np
+    import torch
+
+    import vocab_selected_token_tile_gb300 as rlk
+    from synth import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.GRPO
+    T, Vr, Vp = w.T, w.v_real, w.v_padded
+    tgt = W.targets(w)
+    mask = W.active_mask(w)
+    active = mask != 0
+    g = W.grad(w, active)
+    logits = torch.empty((T, Vp), dtype=torch.int16, device=dev)
+    W.logits_device(w, logits)
+    targets = torch.from_numpy(tgt).to(dev)
+    dmask = torch.from_numpy(mask).to(dev)
+    dg = torch.from_numpy(g).to(dev)
+    dlogits = torch.empty_like(logits)
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    c = rlk.Contract(T=T, V_real=Vr, V_padded=Vp, num_tiles=w.num_tiles, virtual_tp=args.vtp,
+                     mask_mode=rlk.MASK_EXPLICIT, validate=0)
+    stream = torch.cuda.current_stream()
+    ws_buf = rlk.workspace_for(c, dev, stream)
+
+    def step():
+        rlk.check(rlk.rlk_logp_bwd(c, logits.data_ptr(), targets.data_ptr(), dmask.data_ptr(), None,
+                                   dg.data_ptr(), dlogits.data_ptr(), logp.data_ptr(), lse.data_ptr(),
+                                   ws_buf.data_ptr(), stream.cuda_stream))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = rlk.rlk_logp_workspace_status(ws_buf.data_ptr(), stream.cuda_stream)
+    if st != rlk.RLK_OK:
+        raise RuntimeError(f"device status after warm-up: {rlk.rlk_status_string(st)}")
+
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_begin.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if ws > 1:
+        torch.distributed.barrier()
+    total_ms = t_begin.elapsed_time(t_end)
+    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+
+    hbm_peak, bf16_peak, peak_kind = measured_peaks()
+    alg_bytes = T * (2 * Vr + 2 * Vp) + T * (8 + 1 + 4 + 4 + 4)
+    achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
+    result = {
+        "metric": METRIC,
+        "value": ws * T / (ms_per_step * 1e-3),
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; no dataset)",
+        "config": {
+            "workload": "grpo: fused fwd+bwd, T=65536 (32x2048) x V_padded=152576 (V_real=151936), 64 tiles, "
+                        f"virtual TP {args.vtp}, g = A_b*mask/active_count",
+            "active_tokens": int(active.sum()),
+            "parallelism": f"dp{ws} (independent rows, no collective)" if ws > 1 else "single GPU",
+            "l2": "inputs (20.0 GB logits) larger than L2; no flush",
+            "alg_bytes_per_step": alg_bytes,
+        },
+        "achieved_gbs": achieved,
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": hbm_peak,
+            "unit": "GB/s",
+            "frac": achieved / hbm_peak,
+            "traffic": recorded_traffic("stream_kernel<fused>", "grpo"),
+            "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)",
+            "kernel": "stream_kernel<kModeFused>",
+        },
+        "clocks": clk,
+        "gpu_launches": args.steps,
+    }
+    if args.extra and rank == 0:
+        result["extra"] = extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, Vp, args)
+    if not args.no_e2e:
+        result["e2e"] = e2e(rlk, c, w, logits, tgt, mask, g, dev, args)
+    return result
+
+
+def extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, Vp, args):
+    import torch
+    out = {}
+    stream = torch.cuda.current_stream()
+    for name, vtp in (("fwd_vtp1", 1), ("fwd_vtp8", 8)):
+        cf = c.replace(virtual_tp=vtp)
+        for _ in range(3):
+            rlk.logp_fwd(cf, logits, targets, dmask, out=(logp, lse))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            rlk.logp_fwd(cf, logits, targets, dmask, out=(logp, lse))
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.steps
+        out[name] = {"ms": ms, "tokens_per_s": T / ms * 1e3, "alg_gbs": T * (2 * Vr + 17) / ms / 1e6}
+    for name, vtp in (("fused_vtp1", 1), ("fused_vtp4", 4), ("fused_vtp8", 8)):
+        cf = c.replace(virtual_tp=vtp)
+        for _ in range(3):
+            rlk.logp_fwd_bwd(cf, logits, targets, dmask, dg, dlogits=dlogits, out=(logp, lse))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            rlk.logp_fwd_bwd(cf, logits, targets, dmask, dg, dlogits=dlogits, out=(logp, lse))
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.steps
+        out[name] = {"ms": ms, "tokens_per_s": T / ms * 1e3, "alg_gbs": T * (2 * Vr + 2 * Vp + 21) / ms / 1e6}
+    # split path: fwd then bwd with lse_in
+    cf = c.replace(virtual_tp=1)
+    for _ in range(3):
+        rlk.logp_fwd(cf, logits, targets, dmask, out=(logp, lse))
+        rlk.logp_bwd(cf, logits, targets, dmask, lse, dg, dlogits=dlogits)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        rlk.logp_fwd(cf, logits, targets, dmask, out=(logp, lse))
+        rlk.logp_bwd(cf, logits, targets, dmask, lse, dg, dlogits=dlogits)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    out["split_fwd_then_bwd"] = {"ms": ms, "tokens_per_s": T / ms * 1e3}
+    return out
+
+
+def e2e(rlk, c, w, logits_dev, tgt, mask, g, dev, args):
+    """Same metric through the public C ABI, inputs from pinned host memory each step."""
+    import torch
+    T, Vp = w.T, w.v_padded
+    h_logits = torch.empty((T, Vp), dtype=torch.int16, pin_memory=True)
+    h_logits.copy_(logits_dev, non_blocking=False)
+    h_tgt = torch.from_numpy(tgt).pin_memory()
+    h_mask = torch.from_numpy(mask).pin_memory()
+    h_g = torch.from_numpy(g).pin_memory()
+    h_logp = torch.empty(T, dtype=torch.float32, pin_memory=True)
+    h_lse = torch.empty(T, dtype=torch.float32, pin_memory=True)
+    d_logits = logits_dev  # the device buffers are reused; every step overwrites them from the host
+    d_tgt = torch.empty_like(h_tgt, device=dev)
+    d_mask = torch.empty_like(h_mask, device=dev)
+    d_g = torch.empty_like(h_g, device=dev)
+    d_dl = torch.empty_like(logits_dev)
+    d_logp = torch.empty(T, dtype=torch.float32, device=dev)
+    d_lse = torch.empty(T, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    ws = rlk.workspace_for(c, dev, stream)
+
+    def step():
+        d_logits.copy_(h_logits, non_blocking=True)
+        d_tgt.copy_(h_tgt, non_blocking=True)
+        d_mask.copy_(h_mask, non_blocking=True)
+        d_g.copy_(h_g, non_blocking=True)
+        rlk.check(rlk.rlk_logp_bwd(c, d_logits.data_ptr(), d_tgt.data_ptr(), d_mask.data_ptr(), None,
+                                   d_g.data_ptr(), d_dl.data_ptr(), d_logp.data_ptr(), d_lse.data_ptr(),
+                                   ws.data_ptr(), stream.cuda_stream))
+        h_logp.copy_(d_logp, non_blocking=True)
+        h_lse.copy_(d_lse, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    steps = max(2, min(args.steps, 5))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d = h_logits.numel() * 2 + h_tgt.numel() * 8 + h_mask.numel() + h_g.numel() * 4
+    return {"value": T / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": 2 * T * 4, "ms_per_step": ms, "steps": steps,
+            "note": "H2D of logits/targets/mask/g from pinned memory, fused call, D2H of logp and LSE; "
+                    "dlogits stay on the device for the model's backward"}
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from synth import workloads as W
+        t0 = time.perf_counter()
+        per_step = []
+        sample_desc = None
+        steps = max(1, args.steps)
+        budget = max(2.0, 120.0 / (steps + args.warmup))
+        for i in range(args.warmup + steps):
+            tps, rows, secs = time_oracle(W.GRPO, budget_s=budget, max_rows=256)
+            if i >= args.warmup:
+                per_step.append(tps)
+            sample_desc = f"{rows} seeded rows of the grpo workload (fwd LSE/logp + dlogits), {secs:.1f} s"
+        value = statistics.mean(per_step)
+        line = {
+            "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * 65536 / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded counter-based generator)",
+            "config": {"workload": "grpo: fused fwd+bwd, T=65536 x V_padded=152576 (V_real=151936), 64 tiles"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample_desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": time.perf_counter() - t0,
+        }
+        print(json.dumps(line))
+        return
+
+    import torch
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    result = run_ours(args, ws, rank, local)
+    if rank == 0 and not args.no_cpu:
+        from synth import workloads as W
+        tps, rows, secs = time_oracle(W.GRPO, budget_s=15.0, max_rows=512)
+        result["cpu_baseline"] = {"value": tps, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                  "sample": f"{rows} seeded rows of the grpo workload, FP64 numpy oracle "
+                                            f"(fwd LSE/logp + dlogits), {secs:.1f} s of CPU time; "
+                                            f"host has {cpu_threads()} cores"}
+    if rank == 0:
+        print(json.dumps(result))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

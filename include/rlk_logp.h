@@ -1,0 +1,171 @@
+/*
+ * rlk_logp.h -- C ABI of librlk_logp.so: deterministic selected-token
+ * log-probability over a tiled vocabulary, on one GB300 GPU (sm_103a).
+ *
+ * What the library computes (per token row r, real vocabulary V_real):
+ *
+ *   x_rc     = float(logits[r, c]) for c < V_real; columns c >= V_real are
+ *              padding and are masked to -inf before any partial is formed.
+ *   tiles    = num_tiles global tiles of width W = V_padded / num_tiles;
+ *              tile k covers columns [k*W, (k+1)*W).
+ *   partial  = (m_k, s_k) = (max over tile k, sum exp(x - m_k)) in FP32;
+ *              a padding-only or all -inf tile is the identity (-inf, 0).
+ *   merge    = left fold over k = 0..num_tiles-1 in index order:
+ *              m = max(m, m_k), s = s*exp(m_old - m) + s_k*exp(m_k - m).
+ *   LSE_r    = m + log s (FP32);  logp_r = x_{r,t_r} - LSE_r (FP32).
+ *   dlogits  = g_r * (onehot(t_r) - exp(x_r - LSE_r)) on active rows, BF16,
+ *              0 on inactive rows and on padded columns.
+ *
+ * Sources (pages on the method):
+ *   PR #289 "[WS2][PR4][Logp] feat: add distributed TP/CP logprob drift
+ *   report": PR-1 commit (typed contract: ShardingSpec with padded-vs-real
+ *   vocabulary and owner-rank resolution, MaskSpec, ReductionSpec with an
+ *   FP32 (max, sumexp) merge in fixed global index order); commit "docs:
+ *   state that cross-TP bitwise equality needs a global tile-level merge
+ *   structure" (global tiles, padded columns masked to -inf before the
+ *   partials); "typed contract" commit ((-inf, 0) identity partial,
+ *   MaskMode explicit_active_mask | ignore_index, FP32 logprob and LSE
+ *   outputs, fail-closed dispatch); review excerpt of the vocab-parallel
+ *   entry point (tile-size check, active-target validation, non-finite-LSE
+ *   error).  Issue #323 "[WS2][Logprob] H100 validation and reproduction
+ *   guide", "H100 validation matrix" (BF16 logits, FP32 accumulation,
+ *   bitwise-identical outputs across TP degrees).  The H100 matrix
+ *   document "H100 canonical TP/CP validation", "Fixes exercised" (fixed
+ *   virtual TP8 and vocabulary 152576).
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA global-memory pointers owned by the caller;
+ *     the library allocates nothing and keeps no pointer after returning.
+ *   - Work is enqueued on `stream` (NULL = the legacy default stream) and
+ *     is asynchronous, unless contract->validate == 1: then the call
+ *     synchronises the stream and turns the device status word into the
+ *     return code.
+ *   - Errors are status codes; nothing throws or exits.  A contract the
+ *     kernels do not support returns RLK_ERR_UNSUPPORTED -- there is no
+ *     fallback of any kind.  rlk_last_error_message() gives the reason
+ *     (per calling thread).
+ *   - Results do not depend on virtual_tp: outputs are bitwise identical
+ *     for virtual_tp = 1, 2, 4, 8.
+ */
+#ifndef RLK_LOGP_H
+#define RLK_LOGP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* rlk_stream_t;
+
+typedef enum {
+    RLK_OK = 0,
+    RLK_ERR_INVALID_ARG = 1,   /* null/inconsistent pointer or field */
+    RLK_ERR_UNSUPPORTED = 2,   /* well-formed but outside what the kernels do; fail closed */
+    RLK_ERR_NON_TILEABLE = 3,  /* num_tiles does not divide V_padded, or virtual_tp does not divide num_tiles */
+    RLK_ERR_MISALIGNED = 4,    /* a pointer or the row stride is not 16-byte aligned */
+    RLK_ERR_TARGET_RANGE = 5,  /* an active target outside [0, V_real) (device status) */
+    RLK_ERR_NONFINITE_LSE = 6, /* an active row's LSE is not finite (device status) */
+    RLK_ERR_TIMEOUT = 7,       /* a bounded device-side wait expired (device status) */
+    RLK_ERR_CUDA = 8           /* a CUDA runtime call failed */
+} rlk_status;
+
+typedef enum {
+    RLK_MASK_EXPLICIT = 0,     /* active_mask[r] != 0 marks an active row; targets of inactive rows are never read as indices */
+    RLK_MASK_IGNORE_INDEX = 1  /* a row is active iff targets[r] != ignore_index; active_mask must be NULL */
+} rlk_mask_mode;
+
+/*
+ * The contract (PR #289, PR-1 and "typed contract" commits: LogprobContract,
+ * ShardingSpec, MaskSpec, ReductionSpec).  64 bytes, no padding.
+ */
+typedef struct {
+    int64_t T;               /* token rows, >= 0 */
+    int64_t V_real;          /* real vocabulary, >= 1; columns >= V_real are padding */
+    int64_t V_padded;        /* padded vocabulary, >= V_real; num_tiles must divide it */
+    int64_t row_stride;      /* elements between rows of logits and of dlogits; 0 -> V_padded;
+                                must be >= V_padded and a multiple of 8 (16-byte rows) */
+    int32_t num_tiles;       /* global vocabulary tiles (64 in the pages' runs); 1..1024,
+                                tile width V_padded/num_tiles at most 16384 */
+    int32_t virtual_tp;      /* 1, 2, 4 or 8 vocabulary shards (tile-aligned, must divide num_tiles) */
+    int32_t mask_mode;       /* rlk_mask_mode */
+    int32_t validate;        /* 0: asynchronous; 1: synchronise and report device status */
+    int64_t ignore_index;    /* RLK_MASK_IGNORE_INDEX only (the pages use -100) */
+    int64_t wait_timeout_ns; /* bound of every device-side wait; 0 -> 2 s */
+} rlk_logp_contract;
+
+/*
+ * Host-only validation of a contract (PR #289 review excerpt: _tile_size and
+ * _validate_invocation run before any work).  Touches no device.
+ * Returns RLK_OK, RLK_ERR_INVALID_ARG, RLK_ERR_NON_TILEABLE,
+ * RLK_ERR_MISALIGNED or RLK_ERR_UNSUPPORTED.
+ */
+rlk_status rlk_logp_check_contract(const rlk_logp_contract* contract);
+
+/*
+ * Bytes of device workspace rlk_logp_fwd / rlk_logp_bwd need (the device
+ * status word); 0 for an invalid contract.  The workspace must be 16-byte
+ * aligned and must not be shared by calls that may run concurrently.
+ */
+size_t rlk_logp_workspace_size(const rlk_logp_contract* contract);
+
+/*
+ * Forward: LSE and selected log-probability of every row.
+ *   logits_bf16  [T, row_stride] BF16, row-major, 16-byte aligned; only
+ *                columns < V_real are read.
+ *   targets      [T] int64.  Active targets must lie in [0, V_real).
+ *   active_mask  [T] uint8 (RLK_MASK_EXPLICIT), or NULL (RLK_MASK_IGNORE_INDEX).
+ *   logp         [T] FP32 out: x_t - LSE on active rows, +0.0 on inactive rows,
+ *                NaN on an active row whose target is out of range.
+ *   lse          [T] FP32 out: LSE of every row (active or not).
+ *   partials     NULL, or [T, num_tiles, 2] FP32 out: the (m_k, s_k) partials.
+ *   workspace    rlk_logp_workspace_size() bytes.
+ * Device status: RLK_ERR_TARGET_RANGE for an active target outside
+ * [0, V_real); RLK_ERR_NONFINITE_LSE for an active row with a non-finite LSE
+ * (PR #289 review excerpt: "non-finite logsumexp on an active row").
+ */
+rlk_status rlk_logp_fwd(const rlk_logp_contract* contract, const void* logits_bf16,
+                        const int64_t* targets, const uint8_t* active_mask, float* logp,
+                        float* lse, float* partials, void* workspace, rlk_stream_t stream);
+
+/*
+ * Backward (and, with lse_in == NULL, the fused single-pass forward+backward).
+ *   grad_logp    [T] FP32: upstream gradient g_r of logp_r (used on active rows).
+ *   dlogits_bf16 [T, row_stride] BF16 out, 16-byte aligned: columns
+ *                [0, V_padded) of every row are written (padding and inactive
+ *                rows exactly 0); columns >= V_padded are not touched.
+ *   lse_in       [T] FP32 from an earlier rlk_logp_fwd, or NULL.  With
+ *                lse_in != NULL the logits are re-read and logp_out/lse_out
+ *                must be NULL.  With lse_in == NULL each logits row is read
+ *                once: LSE is formed on chip, dlogits written, and
+ *                logp_out/lse_out (both required) receive the forward
+ *                outputs, bitwise equal to rlk_logp_fwd's.
+ * dlogits are bitwise identical between the two forms.  The fused form keeps
+ * a row's slice resident in shared memory across a cluster of CTAs; a
+ * vocabulary too large for that returns RLK_ERR_UNSUPPORTED (call
+ * rlk_logp_fwd, then rlk_logp_bwd with lse_in).
+ */
+rlk_status rlk_logp_bwd(const rlk_logp_contract* contract, const void* logits_bf16,
+                        const int64_t* targets, const uint8_t* active_mask,
+                        const float* lse_in, const float* grad_logp, void* dlogits_bf16,
+                        float* logp_out, float* lse_out, void* workspace, rlk_stream_t stream);
+
+/*
+ * Synchronises `stream` and decodes the status word a previous asynchronous
+ * call left in `workspace` (RLK_OK when no device-side error was recorded).
+ */
+rlk_status rlk_logp_workspace_status(const void* workspace, rlk_stream_t stream);
+
+/* Static text of a status code. */
+const char* rlk_status_string(rlk_status status);
+
+/* Reason for the last non-OK return on the calling thread ("" if none). */
+const char* rlk_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RLK_LOGP_H */

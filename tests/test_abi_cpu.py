@@ -1,0 +1,122 @@
+"""The C ABI without a GPU: symbols, struct layout, host-side contract validation.
+
+Nothing here launches work; every call either validates on the host or
+returns before touching a device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import vocab_selected_token_tile_gb300 as rlk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "rlk_logp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rlk_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function(built):
+    lib = rlk.library()
+    names = header_functions()
+    assert "rlk_logp_fwd" in names and "rlk_logp_bwd" in names
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in rlk_logp.h but not exported"
+    assert set(names) <= set(rlk.EXPORTED) | {n for n in names if n.startswith("rlk_")}
+
+
+def test_exports_are_exactly_the_c_abi(built):
+    # the shared object exports only extern "C" rlk_* symbols (hidden visibility otherwise)
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", rlk._build.LIB], capture_output=True, text=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert syms, out
+    assert {s for s in syms if not s.startswith("rlk_")} == set(), syms
+    assert set(header_functions()) <= syms
+
+
+def test_contract_struct_layout():
+    assert ctypes.sizeof(rlk.Contract) == 64
+    assert rlk.Contract.ignore_index.offset == 48 and rlk.Contract.num_tiles.offset == 32
+
+
+def ok_contract(**kw):
+    base = dict(T=8, V_real=151936, V_padded=152576, num_tiles=64, virtual_tp=2)
+    base.update(kw)
+    return rlk.Contract(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({}, rlk.RLK_OK),
+    (dict(virtual_tp=8), rlk.RLK_OK),
+    (dict(V_padded=151936, V_real=151936), rlk.RLK_OK),
+    (dict(T=0), rlk.RLK_OK),
+    (dict(num_tiles=7), rlk.RLK_ERR_NON_TILEABLE),          # 7 does not divide 152576
+    (dict(num_tiles=2, virtual_tp=4), rlk.RLK_ERR_NON_TILEABLE),
+    (dict(virtual_tp=3), rlk.RLK_ERR_UNSUPPORTED),
+    (dict(virtual_tp=16), rlk.RLK_ERR_UNSUPPORTED),
+    (dict(num_tiles=1, virtual_tp=1), rlk.RLK_ERR_UNSUPPORTED),  # tile wider than 16384 columns
+    (dict(num_tiles=2048, V_padded=2048 * 8, V_real=2048 * 8), rlk.RLK_ERR_UNSUPPORTED),
+    (dict(V_real=0), rlk.RLK_ERR_INVALID_ARG),
+    (dict(V_padded=100, V_real=101, num_tiles=4, virtual_tp=1), rlk.RLK_ERR_INVALID_ARG),
+    (dict(T=-1), rlk.RLK_ERR_INVALID_ARG),
+    (dict(row_stride=152576 + 4), rlk.RLK_ERR_MISALIGNED),
+    (dict(row_stride=152000), rlk.RLK_ERR_INVALID_ARG),
+    (dict(mask_mode=2), rlk.RLK_ERR_INVALID_ARG),
+    (dict(validate=2), rlk.RLK_ERR_INVALID_ARG),
+    (dict(wait_timeout_ns=-5), rlk.RLK_ERR_INVALID_ARG),
+])
+def test_check_contract(built, kw, status):
+    c = ok_contract(**kw)
+    assert rlk.rlk_logp_check_contract(c) == status
+    if status != rlk.RLK_OK:
+        assert rlk.rlk_last_error_message() != ""
+        assert rlk.rlk_logp_workspace_size(c) == 0
+    else:
+        assert rlk.rlk_logp_workspace_size(c) >= 4
+
+
+def test_null_contract(built):
+    assert rlk.library().rlk_logp_check_contract(None) == rlk.RLK_ERR_INVALID_ARG
+
+
+def test_calls_fail_closed_before_any_device_work(built):
+    c = ok_contract()
+    # missing pointers are rejected on the host, before any CUDA call
+    assert rlk.rlk_logp_fwd(c, None, None, None, None, None, None, None, None) == rlk.RLK_ERR_INVALID_ARG
+    assert "logits" in rlk.rlk_last_error_message()
+    assert rlk.rlk_logp_fwd(c, 0x1008, 0x2000, 0x3000, 0x4000, 0x5000, None, 0x6000, None) == rlk.RLK_ERR_MISALIGNED
+    # ignore-index mode takes no mask, explicit mode needs one
+    ci = ok_contract(mask_mode=rlk.MASK_IGNORE_INDEX)
+    assert rlk.rlk_logp_fwd(ci, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, None, 0x6000, None) == rlk.RLK_ERR_INVALID_ARG
+    assert rlk.rlk_logp_fwd(c, 0x1000, 0x2000, None, 0x4000, 0x5000, None, 0x6000, None) == rlk.RLK_ERR_INVALID_ARG
+    # backward: lse_in excludes forward outputs; the fused form needs them
+    assert rlk.rlk_logp_bwd(c, 0x1000, 0x2000, 0x3000, 0x7000, 0x8000, 0x9000, 0xA000, None, 0x6000,
+                            None) == rlk.RLK_ERR_INVALID_ARG
+    assert rlk.rlk_logp_bwd(c, 0x1000, 0x2000, 0x3000, None, 0x8000, 0x9000, None, None, 0x6000,
+                            None) == rlk.RLK_ERR_INVALID_ARG
+    assert rlk.rlk_logp_bwd(c, 0x1000, 0x2000, 0x3000, None, 0x8000, 0x9008, 0xA000, 0xB000, 0x6000,
+                            None) == rlk.RLK_ERR_MISALIGNED
+    # an empty batch is a no-op
+    assert rlk.rlk_logp_fwd(ok_contract(T=0), None, None, None, None, None, None, None, None) == rlk.RLK_OK
+
+
+def test_status_strings(built):
+    for code in range(9):
+        assert rlk.rlk_status_string(code).startswith("RLK_")
+    assert rlk.rlk_status_string(99) == "RLK_ERR_UNKNOWN"
+
+
+def test_product_path_has_no_fallback():
+    # the package never imports the oracle or the generator
+    import inspect
+    src = inspect.getsource(rlk)
+    assert "import oracle" not in src and "import synth" not in src
+    csrc = os.path.join(ROOT, "vocab_selected_token_tile_gb300", "csrc")
+    for f in os.listdir(csrc):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            assert "oracle" not in open(os.path.join(csrc, f)).read().lower()

@@ -1,1 +1,203 @@
-"""Deterministic selected-token log-probability over a tiled vocabulary (GB300, sm_103a)."""
+"""Deterministic selected-token log-probability over a tiled vocabulary (GB300, sm_103a).
+
+A thin ctypes binding of ``librlk_logp.so`` (declared in ``include/rlk_logp.h``).
+The functions named ``rlk_*`` mirror the C entry points one to one and take
+raw device pointers; ``logp_fwd``, ``logp_bwd`` and ``logp_fwd_bwd`` only
+marshal torch tensors (allocate outputs, pass ``data_ptr()`` and the current
+stream).  Every step of the computation runs in the CUDA library: if it is
+missing or fails to load, these functions raise -- there is no fallback.
+"""
+import ctypes
+import os
+
+from . import _build
+
+RLK_OK = 0
+RLK_ERR_INVALID_ARG = 1
+RLK_ERR_UNSUPPORTED = 2
+RLK_ERR_NON_TILEABLE = 3
+RLK_ERR_MISALIGNED = 4
+RLK_ERR_TARGET_RANGE = 5
+RLK_ERR_NONFINITE_LSE = 6
+RLK_ERR_TIMEOUT = 7
+RLK_ERR_CUDA = 8
+
+MASK_EXPLICIT = 0
+MASK_IGNORE_INDEX = 1
+
+EXPORTED = (
+    "rlk_logp_check_contract",
+    "rlk_logp_workspace_size",
+    "rlk_logp_fwd",
+    "rlk_logp_bwd",
+    "rlk_logp_workspace_status",
+    "rlk_status_string",
+    "rlk_last_error_message",
+)
+
+
+class Contract(ctypes.Structure):
+    """Mirror of ``rlk_logp_contract`` (64 bytes)."""
+    _fields_ = [
+        ("T", ctypes.c_int64),
+        ("V_real", ctypes.c_int64),
+        ("V_padded", ctypes.c_int64),
+        ("row_stride", ctypes.c_int64),
+        ("num_tiles", ctypes.c_int32),
+        ("virtual_tp", ctypes.c_int32),
+        ("mask_mode", ctypes.c_int32),
+        ("validate", ctypes.c_int32),
+        ("ignore_index", ctypes.c_int64),
+        ("wait_timeout_ns", ctypes.c_int64),
+    ]
+
+    def __init__(self, T, V_real, V_padded, num_tiles=64, virtual_tp=1, mask_mode=MASK_EXPLICIT,
+                 ignore_index=-100, validate=0, row_stride=0, wait_timeout_ns=0):
+        super().__init__(T, V_real, V_padded, row_stride, num_tiles, virtual_tp, mask_mode, validate,
+                         ignore_index, wait_timeout_ns)
+
+    def replace(self, **kw):
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d.update(kw)
+        return Contract(**d)
+
+
+class RlkError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"{rlk_status_string(status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def library():
+    """Load librlk_logp.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"CUDA library not built: {_build.LIB} (run __graft_entry__.build())")
+        lib = ctypes.CDLL(_build.LIB)
+        P = ctypes.POINTER(Contract)
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        lib.rlk_logp_check_contract.argtypes = [P]
+        lib.rlk_logp_check_contract.restype = i
+        lib.rlk_logp_workspace_size.argtypes = [P]
+        lib.rlk_logp_workspace_size.restype = ctypes.c_size_t
+        lib.rlk_logp_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.rlk_logp_fwd.restype = i
+        lib.rlk_logp_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.rlk_logp_bwd.restype = i
+        lib.rlk_logp_workspace_status.argtypes = [vp, vp]
+        lib.rlk_logp_workspace_status.restype = i
+        lib.rlk_status_string.argtypes = [i]
+        lib.rlk_status_string.restype = ctypes.c_char_p
+        lib.rlk_last_error_message.argtypes = []
+        lib.rlk_last_error_message.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+# ------------------------------------------------------------------ C names
+
+def rlk_logp_check_contract(contract):
+    return library().rlk_logp_check_contract(ctypes.byref(contract))
+
+
+def rlk_logp_workspace_size(contract):
+    return library().rlk_logp_workspace_size(ctypes.byref(contract))
+
+
+def rlk_logp_fwd(contract, logits, targets, active_mask, logp, lse, partials, workspace, stream):
+    return library().rlk_logp_fwd(ctypes.byref(contract), logits, targets, active_mask, logp, lse, partials,
+                                  workspace, stream)
+
+
+def rlk_logp_bwd(contract, logits, targets, active_mask, lse_in, grad_logp, dlogits, logp_out, lse_out,
+                 workspace, stream):
+    return library().rlk_logp_bwd(ctypes.byref(contract), logits, targets, active_mask, lse_in, grad_logp,
+                                  dlogits, logp_out, lse_out, workspace, stream)
+
+
+def rlk_logp_workspace_status(workspace, stream):
+    return library().rlk_logp_workspace_status(workspace, stream)
+
+
+def rlk_status_string(status):
+    return library().rlk_status_string(status).decode()
+
+
+def rlk_last_error_message():
+    return library().rlk_last_error_message().decode()
+
+
+def check(status):
+    if status != RLK_OK:
+        raise RlkError(status, rlk_last_error_message())
+
+
+# ------------------------------------------------------------------ torch marshalling
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    return (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+
+
+_workspaces = {}
+
+
+def workspace_for(contract, device, stream=None):
+    """A per-(device, stream) status workspace; calls on one stream never overlap."""
+    import torch
+    key = (str(device), _stream(stream))
+    n = max(rlk_logp_workspace_size(contract), 256)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < n:
+        ws = torch.zeros(n, dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def logp_fwd(contract, logits, targets, mask=None, partials=False, stream=None, out=None):
+    """(logp, lse[, partials]) for BF16 ``logits`` [T, row_stride] (bf16/int16 storage) on the GPU."""
+    import torch
+    dev = logits.device
+    T = contract.T
+    logp, lse = out if out is not None else (torch.empty(T, dtype=torch.float32, device=dev),
+                                             torch.empty(T, dtype=torch.float32, device=dev))
+    part = torch.empty((T, contract.num_tiles, 2), dtype=torch.float32, device=dev) if partials else None
+    ws = workspace_for(contract, dev, stream)
+    check(rlk_logp_fwd(contract, _ptr(logits), _ptr(targets), _ptr(mask), _ptr(logp), _ptr(lse), _ptr(part),
+                       _ptr(ws), _stream(stream)))
+    return (logp, lse, part) if partials else (logp, lse)
+
+
+def logp_bwd(contract, logits, targets, mask, lse, grad, dlogits=None, stream=None):
+    """BF16 dlogits [T, row_stride] from the forward's LSE (the logits are re-read)."""
+    import torch
+    dev = logits.device
+    if dlogits is None:
+        dlogits = torch.empty_like(logits)
+    ws = workspace_for(contract, dev, stream)
+    check(rlk_logp_bwd(contract, _ptr(logits), _ptr(targets), _ptr(mask), _ptr(lse), _ptr(grad),
+                       _ptr(dlogits), None, None, _ptr(ws), _stream(stream)))
+    return dlogits
+
+
+def logp_fwd_bwd(contract, logits, targets, mask, grad, dlogits=None, stream=None, out=None):
+    """Fused single pass: (dlogits, logp, lse); each logits row is read from HBM once."""
+    import torch
+    dev = logits.device
+    T = contract.T
+    if dlogits is None:
+        dlogits = torch.empty_like(logits)
+    logp, lse = out if out is not None else (torch.empty(T, dtype=torch.float32, device=dev),
+                                             torch.empty(T, dtype=torch.float32, device=dev))
+    ws = workspace_for(contract, dev, stream)
+    check(rlk_logp_bwd(contract, _ptr(logits), _ptr(targets), _ptr(mask), None, _ptr(grad), _ptr(dlogits),
+                       _ptr(logp), _ptr(lse), _ptr(ws), _stream(stream)))
+    return dlogits, logp, lse

@@ -1,0 +1,196 @@
+// C ABI of librlk_logp.so: contract validation, argument checks, status
+// handling.  Every check that can be made on the host is made here, before
+// any launch (PR #289 review excerpt of the vocab-parallel entry point:
+// _tile_size and _validate_invocation precede any work; "typed contract"
+// commit: incompatible requests are rejected with explicit reasons and never
+// served by a silent fallback).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "rlk_internal.h"
+#include "rlk_logp.h"
+
+#define RLK_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace rlk {
+
+namespace {
+thread_local std::string g_last_error;
+}
+
+rlk_status fail(rlk_status s, const std::string& why) {
+    g_last_error = why;
+    return s;
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+rlk_status check_contract(const rlk_logp_contract* c) {
+    if (!c) return fail(RLK_ERR_INVALID_ARG, "contract is NULL");
+    if (c->T < 0) return fail(RLK_ERR_INVALID_ARG, "T must be >= 0");
+    if (c->T > ((int64_t)1 << 40)) return fail(RLK_ERR_UNSUPPORTED, "T above 2^40 rows");
+    if (c->V_real < 1) return fail(RLK_ERR_INVALID_ARG, "V_real must be >= 1");
+    if (c->V_padded < c->V_real) return fail(RLK_ERR_INVALID_ARG, "V_padded must be >= V_real");
+    if (c->V_padded > ((int64_t)1 << 31)) return fail(RLK_ERR_UNSUPPORTED, "V_padded above 2^31");
+    if (c->num_tiles < 1) return fail(RLK_ERR_INVALID_ARG, "num_tiles must be >= 1");
+    if (c->V_padded % c->num_tiles != 0)
+        return fail(RLK_ERR_NON_TILEABLE, "vocabulary is not tileable: num_tiles must divide V_padded");
+    if (c->virtual_tp != 1 && c->virtual_tp != 2 && c->virtual_tp != 4 && c->virtual_tp != 8)
+        return fail(RLK_ERR_UNSUPPORTED, "virtual_tp must be 1, 2, 4 or 8");
+    if (c->num_tiles % c->virtual_tp != 0)
+        return fail(RLK_ERR_NON_TILEABLE, "shard bounds must be tile-aligned: virtual_tp must divide num_tiles");
+    if (c->num_tiles > kMaxTiles) return fail(RLK_ERR_UNSUPPORTED, "num_tiles above 1024");
+    if (c->V_padded / c->num_tiles > kMaxTileCols)
+        return fail(RLK_ERR_UNSUPPORTED, "tile width V_padded/num_tiles above 16384 columns");
+    const int64_t stride = c->row_stride ? c->row_stride : c->V_padded;
+    if (stride < c->V_padded) return fail(RLK_ERR_INVALID_ARG, "row_stride must be >= V_padded");
+    if (stride % 8 != 0) return fail(RLK_ERR_MISALIGNED, "row_stride must be a multiple of 8 elements (16-byte rows)");
+    if (c->mask_mode != RLK_MASK_EXPLICIT && c->mask_mode != RLK_MASK_IGNORE_INDEX)
+        return fail(RLK_ERR_INVALID_ARG, "mask_mode must be RLK_MASK_EXPLICIT or RLK_MASK_IGNORE_INDEX");
+    if (c->validate != 0 && c->validate != 1) return fail(RLK_ERR_INVALID_ARG, "validate must be 0 or 1");
+    if (c->wait_timeout_ns < 0) return fail(RLK_ERR_INVALID_ARG, "wait_timeout_ns must be >= 0");
+    return RLK_OK;
+}
+
+rlk_status check_common(const rlk_logp_contract* c, const void* logits, const int64_t* targets,
+                        const uint8_t* mask, const void* workspace) {
+    if (!logits) return fail(RLK_ERR_INVALID_ARG, "logits is NULL");
+    if (!aligned16(logits)) return fail(RLK_ERR_MISALIGNED, "logits must be 16-byte aligned");
+    if (!targets) return fail(RLK_ERR_INVALID_ARG, "targets is NULL");
+    if (c->mask_mode == RLK_MASK_EXPLICIT && !mask)
+        return fail(RLK_ERR_INVALID_ARG, "explicit mask mode needs active_mask");
+    if (c->mask_mode == RLK_MASK_IGNORE_INDEX && mask)
+        return fail(RLK_ERR_INVALID_ARG, "ignore_index mode takes no active_mask (pass NULL)");
+    if (!workspace) return fail(RLK_ERR_INVALID_ARG, "workspace is NULL");
+    if (!aligned16(workspace)) return fail(RLK_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    return RLK_OK;
+}
+
+// Makes the device that owns `ptr` current for this library's runtime.
+rlk_status select_device(const void* ptr) {
+    cudaPointerAttributes attr{};
+    cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaPointerGetAttributes: ") + cudaGetErrorString(e));
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return fail(RLK_ERR_INVALID_ARG, "logits must be device memory");
+    e = cudaSetDevice(attr.device);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaSetDevice: ") + cudaGetErrorString(e));
+    return RLK_OK;
+}
+
+rlk_status decode_status(uint32_t bits) {
+    if (bits & kStatusTimeout) return fail(RLK_ERR_TIMEOUT, "a bounded device-side wait expired");
+    if (bits & kStatusTargetRange) return fail(RLK_ERR_TARGET_RANGE, "an active target lies outside [0, V_real)");
+    if (bits & kStatusNonFinite)
+        return fail(RLK_ERR_NONFINITE_LSE,
+                    "non-finite logsumexp on an active row: its real-vocabulary logits must be finite");
+    return RLK_OK;
+}
+
+rlk_status read_status(const void* workspace, cudaStream_t stream) {
+    uint32_t bits = 0;
+    cudaError_t e = cudaMemcpyAsync(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("reading the status word: ") + cudaGetErrorString(e));
+    return decode_status(bits);
+}
+
+rlk_status begin(void* workspace, cudaStream_t stream) {
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("clearing the status word: ") + cudaGetErrorString(e));
+    return RLK_OK;
+}
+
+}  // namespace
+}  // namespace rlk
+
+using namespace rlk;
+
+RLK_EXPORT rlk_status rlk_logp_check_contract(const rlk_logp_contract* contract) {
+    return check_contract(contract);
+}
+
+RLK_EXPORT size_t rlk_logp_workspace_size(const rlk_logp_contract* contract) {
+    return check_contract(contract) == RLK_OK ? kWorkspaceBytes : 0;
+}
+
+RLK_EXPORT rlk_status rlk_logp_fwd(const rlk_logp_contract* c, const void* logits_bf16, const int64_t* targets,
+                                   const uint8_t* active_mask, float* logp, float* lse, float* partials,
+                                   void* workspace, rlk_stream_t stream) {
+    rlk_status s = check_contract(c);
+    if (s != RLK_OK) return s;
+    if (c->T == 0) return RLK_OK;
+    if ((s = check_common(c, logits_bf16, targets, active_mask, workspace)) != RLK_OK) return s;
+    if (!logp || !lse) return fail(RLK_ERR_INVALID_ARG, "logp and lse outputs are required");
+    if ((s = select_device(logits_bf16)) != RLK_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = begin(workspace, st)) != RLK_OK) return s;
+    StreamArgs a{};
+    a.logits = static_cast<const uint16_t*>(logits_bf16);
+    a.targets = targets;
+    a.mask = active_mask;
+    a.logp = logp;
+    a.lse = lse;
+    a.partials = partials;
+    a.status = static_cast<uint32_t*>(workspace);
+    if ((s = launch_stream(*c, kModeFwd, a, st)) != RLK_OK) return s;
+    return c->validate ? read_status(workspace, st) : RLK_OK;
+}
+
+RLK_EXPORT rlk_status rlk_logp_bwd(const rlk_logp_contract* c, const void* logits_bf16, const int64_t* targets,
+                                   const uint8_t* active_mask, const float* lse_in, const float* grad_logp,
+                                   void* dlogits_bf16, float* logp_out, float* lse_out, void* workspace,
+                                   rlk_stream_t stream) {
+    rlk_status s = check_contract(c);
+    if (s != RLK_OK) return s;
+    if (c->T == 0) return RLK_OK;
+    if ((s = check_common(c, logits_bf16, targets, active_mask, workspace)) != RLK_OK) return s;
+    if (!grad_logp) return fail(RLK_ERR_INVALID_ARG, "grad_logp is NULL");
+    if (!dlogits_bf16) return fail(RLK_ERR_INVALID_ARG, "dlogits is NULL");
+    if (!aligned16(dlogits_bf16)) return fail(RLK_ERR_MISALIGNED, "dlogits must be 16-byte aligned");
+    if (lse_in && (logp_out || lse_out))
+        return fail(RLK_ERR_INVALID_ARG, "with lse_in the forward outputs logp_out/lse_out must be NULL");
+    if (!lse_in && (!logp_out || !lse_out))
+        return fail(RLK_ERR_INVALID_ARG, "the fused form (lse_in NULL) needs logp_out and lse_out");
+    if ((s = select_device(logits_bf16)) != RLK_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = begin(workspace, st)) != RLK_OK) return s;
+    StreamArgs a{};
+    a.logits = static_cast<const uint16_t*>(logits_bf16);
+    a.dlogits = static_cast<uint16_t*>(dlogits_bf16);
+    a.targets = targets;
+    a.mask = active_mask;
+    a.grad = grad_logp;
+    a.lse_in = lse_in;
+    a.logp = logp_out;
+    a.lse = lse_out;
+    a.status = static_cast<uint32_t*>(workspace);
+    if ((s = launch_stream(*c, lse_in ? kModeBwd : kModeFused, a, st)) != RLK_OK) return s;
+    return c->validate ? read_status(workspace, st) : RLK_OK;
+}
+
+RLK_EXPORT rlk_status rlk_logp_workspace_status(const void* workspace, rlk_stream_t stream) {
+    if (!workspace) return fail(RLK_ERR_INVALID_ARG, "workspace is NULL");
+    return read_status(workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+RLK_EXPORT const char* rlk_status_string(rlk_status s) {
+    switch (s) {
+        case RLK_OK: return "RLK_OK";
+        case RLK_ERR_INVALID_ARG: return "RLK_ERR_INVALID_ARG";
+        case RLK_ERR_UNSUPPORTED: return "RLK_ERR_UNSUPPORTED";
+        case RLK_ERR_NON_TILEABLE: return "RLK_ERR_NON_TILEABLE";
+        case RLK_ERR_MISALIGNED: return "RLK_ERR_MISALIGNED";
+        case RLK_ERR_TARGET_RANGE: return "RLK_ERR_TARGET_RANGE";
+        case RLK_ERR_NONFINITE_LSE: return "RLK_ERR_NONFINITE_LSE";
+        case RLK_ERR_TIMEOUT: return "RLK_ERR_TIMEOUT";
+        case RLK_ERR_CUDA: return "RLK_ERR_CUDA";
+    }
+    return "RLK_ERR_UNKNOWN";
+}
+
+RLK_EXPORT const char* rlk_last_error_message(void) { return g_last_error.c_str(); }

@@ -1,0 +1,49 @@
+// Internal declarations shared by the C ABI (rlk_api.cu) and the kernels'
+// launch planners.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "rlk_logp.h"
+
+namespace rlk {
+
+// Device status word bits (written by kernels with atomicOr, read by the host).
+enum : uint32_t {
+    kStatusTargetRange = 1u << 0,
+    kStatusNonFinite = 1u << 1,
+    kStatusTimeout = 1u << 2,
+};
+
+constexpr int kMaxTiles = 1024;
+constexpr int64_t kMaxTileCols = 16384;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
+constexpr size_t kWorkspaceBytes = 256;
+
+enum StreamMode : int { kModeFwd = 0, kModeBwd = 1, kModeFused = 2 };
+
+// Arguments of one streaming launch (all device pointers).
+struct StreamArgs {
+    const uint16_t* logits;
+    uint16_t* dlogits;
+    const int64_t* targets;
+    const uint8_t* mask;
+    const float* grad;
+    const float* lse_in;
+    float* logp;
+    float* lse;
+    float* partials;
+    uint32_t* status;
+};
+
+// Records a failure reason for rlk_last_error_message() and returns `s`.
+rlk_status fail(rlk_status s, const std::string& why);
+
+// Launches one streaming kernel (mode kModeFwd / kModeBwd / kModeFused) for a
+// validated contract; returns RLK_OK or an error with the message set.
+rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs& a, cudaStream_t stream);
+
+}  // namespace rlk
