@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--extra", action="store_true", help="also time the forward-only and split paths")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="profiling only: shrink the batch to this many rows (not a bench number)")
     return ap.parse_args()
 
 
@@ -175,6 +177,8 @@ def run_ours(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = W.GRPO
+    if args.rows:
+        w = w.with_(batch=max(1, args.rows // w.seq), name="grpo-profile")
     T, Vr, Vp = w.T, w.v_real, w.v_padded
     tgt = W.targets(w)
     mask = W.active_mask(w)

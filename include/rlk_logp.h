@@ -158,6 +158,17 @@ rlk_status rlk_logp_bwd(const rlk_logp_contract* contract, const void* logits_bf
  */
 rlk_status rlk_logp_workspace_status(const void* workspace, rlk_stream_t stream);
 
+/*
+ * Self-test of the kernels' bounded device-side waits: one warp waits, with
+ * the same code the kernels use, on an mbarrier that nothing arrives at.
+ * The wait expires after timeout_ns (0 < timeout_ns <= 10 s), records the
+ * timeout in the status word and the kernel returns; the call synchronises
+ * `stream` and returns RLK_ERR_TIMEOUT when the mechanism works.  Nothing
+ * faults and the context stays usable.  `workspace` as for rlk_logp_fwd.
+ * (A check of the failure-detection path; the pages have no counterpart.)
+ */
+rlk_status rlk_selftest_bounded_wait(int64_t timeout_ns, void* workspace, rlk_stream_t stream);
+
 /* Static text of a status code. */
 const char* rlk_status_string(rlk_status status);
 

@@ -1,0 +1,99 @@
+"""Full-size parity: the 65536 x 152576 rollout/GRPO batch, in bench.py's launch configuration.
+
+The oracle computes sampled rows one by one from host-generated copies of
+the same rows (first, last, inactive and seeded random rows); properties that
+hold at any size are checked over the whole batch on the device.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import vocab_selected_token_tile_gb300 as rlk
+from parity import check_dlogits, check_fwd, contract
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+BENCH_VTP = 2  # bench.py's default virtual TP for the fused step
+
+
+@pytest.fixture(scope="module")
+def batch():
+    w = W.GRPO
+    logits = torch.empty((w.T, w.v_padded), dtype=torch.int16, device="cuda")
+    W.logits_device(w, logits)
+    tgt = W.targets(w)
+    mask = W.active_mask(w)
+    active = mask != 0
+    g = W.grad(w, active)
+    rng = np.random.default_rng(99)
+    inactive = np.nonzero(~active)[0]
+    rows = np.unique(np.concatenate([[0, 1, 2, w.T - 3, w.T - 2, w.T - 1], rng.choice(w.T, 96, replace=False),
+                                     rng.choice(inactive, 16, replace=False)]))
+    bits = np.concatenate([W.logits_host(w, row0=int(r), nrows=1) for r in rows])
+    yield dict(w=w, logits=logits, tgt=tgt, mask=mask, active=active, g=g, rows=rows, bits=bits,
+               dt=torch.from_numpy(tgt).cuda(), dm=torch.from_numpy(mask).cuda(), dg=torch.from_numpy(g).cuda())
+    del logits
+    torch.cuda.empty_cache()
+
+
+def test_sampled_rows_match_the_host_generator(batch):
+    got = batch["logits"][torch.from_numpy(batch["rows"]).cuda()].cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, batch["bits"])
+
+
+def test_rollout_forward_full_size(batch):
+    w, rows = batch["w"], batch["rows"]
+    for vtp in (1, 8):
+        c = contract(w.T, w.v_real, w.v_padded, w.num_tiles, vtp)
+        logp, lse = rlk.logp_fwd(c, batch["logits"], batch["dt"], batch["dm"])
+        torch.cuda.synchronize()
+        assert torch.isfinite(lse).all()
+        act = torch.from_numpy(batch["active"]).cuda()
+        assert (logp[~act] == 0).all() and (logp[act] <= 0).all()
+        lp, ls = logp.cpu().numpy()[rows], lse.cpu().numpy()[rows]
+        check_fwd(batch["bits"], batch["tgt"][rows], batch["active"][rows], w.v_real, lp, ls)
+        if vtp == 1:
+            ref = (logp.clone(), lse.clone())
+        else:
+            assert torch.equal(ref[0], logp) and torch.equal(ref[1], lse)
+
+
+def test_grpo_fused_full_size_in_bench_configuration(batch):
+    w, rows = batch["w"], batch["rows"]
+    c = contract(w.T, w.v_real, w.v_padded, w.num_tiles, BENCH_VTP, validate=0)
+    dl, logp, lse = rlk.logp_fwd_bwd(c, batch["logits"], batch["dt"], batch["dm"], batch["dg"])
+    torch.cuda.synchronize()
+    assert rlk.rlk_logp_workspace_status(rlk.workspace_for(c, dl.device).data_ptr(),
+                                         torch.cuda.current_stream().cuda_stream) == rlk.RLK_OK
+    # sampled rows against the oracle, element by element
+    lp, ls = logp.cpu().numpy()[rows], lse.cpu().numpy()[rows]
+    check_fwd(batch["bits"], batch["tgt"][rows], batch["active"][rows], w.v_real, lp, ls)
+    dl_rows = dl[torch.from_numpy(rows).cuda()].cpu().numpy().view(np.uint16)
+    check_dlogits(batch["bits"], batch["tgt"][rows], batch["active"][rows], batch["g"][rows], w.v_real,
+                  w.v_padded, dl_rows, rows=np.arange(len(rows)))
+    # whole batch, in row blocks: inactive rows and padded columns exactly zero, and
+    # each active row's dlogits sum to ~0 (BF16 rounding of about 2|g| of mass)
+    act = torch.from_numpy(batch["active"]).cuda()
+    for r0 in range(0, w.T, 4096):
+        blk, a = dl[r0:r0 + 4096], act[r0:r0 + 4096]
+        assert not blk[~a].any()
+        assert not blk[:, w.v_real:].any()
+        sums = blk[a].view(torch.bfloat16).float().sum(dim=1)
+        gabs = batch["dg"][r0:r0 + 4096][a].abs()
+        assert (sums.abs() <= 2.0 ** -6 * gabs + 1e-12).all()
+    # the split path (fwd then bwd with lse_in) gives the same bits
+    c1 = c.replace(virtual_tp=1)
+    logp1, lse1 = rlk.logp_fwd(c1, batch["logits"], batch["dt"], batch["dm"])
+    assert torch.equal(logp1, logp) and torch.equal(lse1, lse)
+    dl1 = rlk.logp_bwd(c1, batch["logits"], batch["dt"], batch["dm"], lse1, batch["dg"])
+    torch.cuda.synchronize()
+    assert torch.equal(dl1, dl)
+    # oracle-side sanity of the sampled rows' gradient sums (pins the device property above)
+    ref = oracle.dlogits(batch["bits"][:8], batch["tgt"][rows[:8]], batch["active"][rows[:8]],
+                         batch["g"][rows[:8]], w.v_real, w.v_padded)
+    assert np.all(np.abs(ref.sum(axis=1)) <= 1e-9 * (np.abs(batch["g"][rows[:8]]) + 1e-30) * w.v_real)

@@ -31,6 +31,7 @@ EXPORTED = (
     "rlk_logp_fwd",
     "rlk_logp_bwd",
     "rlk_logp_workspace_status",
+    "rlk_selftest_bounded_wait",
     "rlk_status_string",
     "rlk_last_error_message",
 )
@@ -90,6 +91,8 @@ def library():
         lib.rlk_logp_bwd.restype = i
         lib.rlk_logp_workspace_status.argtypes = [vp, vp]
         lib.rlk_logp_workspace_status.restype = i
+        lib.rlk_selftest_bounded_wait.argtypes = [ctypes.c_int64, vp, vp]
+        lib.rlk_selftest_bounded_wait.restype = i
         lib.rlk_status_string.argtypes = [i]
         lib.rlk_status_string.restype = ctypes.c_char_p
         lib.rlk_last_error_message.argtypes = []
@@ -121,6 +124,10 @@ def rlk_logp_bwd(contract, logits, targets, active_mask, lse_in, grad_logp, dlog
 
 def rlk_logp_workspace_status(workspace, stream):
     return library().rlk_logp_workspace_status(workspace, stream)
+
+
+def rlk_selftest_bounded_wait(timeout_ns, workspace, stream):
+    return library().rlk_selftest_bounded_wait(timeout_ns, workspace, stream)
 
 
 def rlk_status_string(status):

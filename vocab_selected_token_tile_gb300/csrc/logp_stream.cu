@@ -50,7 +50,7 @@
 namespace rlk {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxSlots = 96;
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^y = 2^(y log2 e)
@@ -82,24 +82,40 @@ struct Params {
     int64_t T, Vr, Vp, stride, ignore_index;
     uint64_t wait_ns;
     int32_t NT, W, C, mask_mode, NS, slot_bytes;
+    int32_t tps;  // tiles per ring slot (consecutive tiles of one row share a slot when narrow)
     uint32_t off_full, off_empty, off_hdr, off_part, off_fold, off_rows, off_xbar, off_flag;
 };
 
 struct TileGeom {
     int64_t ts, te;  // tile columns [ts, te)
     int64_t hi;      // min(te, V_real): end of the tile's real columns
-    int64_t a, b;    // slot span [a, b): a = floor8(ts), b = min(ceil8(te), floor8(V_real))
+    int64_t a;       // floor8(ts): column of the tile's first 8-column group
+    int64_t b;       // end of the data held in shared memory (multiple of 8)
 };
 
-__device__ __forceinline__ TileGeom tile_geom(int k, const Params& p) {
+// Columns [a, b) of tiles [kf, kl) that one ring slot holds:
+// a = floor8(kf*W), b = min(ceil8(kl*W), floor8(V_real)); b <= a means nothing to copy.
+struct Span {
+    int64_t a, b;
+};
+
+__device__ __forceinline__ Span chunk_span(int kf, int kl, const Params& p) {
+    Span s;
+    s.a = ((int64_t)kf * p.W) & ~(int64_t)7;
+    const int64_t ce = ((int64_t)kl * p.W + 7) & ~(int64_t)7;
+    const int64_t fv = p.Vr & ~(int64_t)7;
+    s.b = ce < fv ? ce : fv;
+    return s;
+}
+
+// Geometry of tile k inside a slot that holds columns [sp.a, sp.b).
+__device__ __forceinline__ TileGeom tile_geom(int k, const Params& p, const Span& sp) {
     TileGeom t;
     t.ts = (int64_t)k * p.W;
     t.te = t.ts + p.W;
     t.hi = t.te < p.Vr ? t.te : p.Vr;
     t.a = t.ts & ~(int64_t)7;
-    const int64_t ce = (t.te + 7) & ~(int64_t)7;
-    const int64_t fv = p.Vr & ~(int64_t)7;
-    t.b = ce < fv ? ce : fv;
+    t.b = sp.b;
     return t;
 }
 
@@ -192,68 +208,122 @@ __device__ __forceinline__ float exp_term(float x, float neg_mL) {
     return ex2_approx(__fmaf_rn(x, kLog2e, neg_mL));
 }
 
+// Groups of one tile, indexed from floor8(ts): the "interior" groups [lo, hi)
+// lie entirely inside [ts, min(end, floor8(V_real))) -- full, real, and always
+// held in the slot -- and take a branch-free path; the others (a partial first
+// group, a partial last group, the real tail) are "edges".  The split depends
+// only on the tile and V_real, never on how tiles are grouped into slots.
+struct GroupRange {
+    int lo, hi, n;  // interior [lo, hi), all groups [0, n)
+};
+
+__device__ __forceinline__ GroupRange group_range(const TileGeom& t, int64_t end, int64_t Vr) {
+    GroupRange g;
+    g.lo = (t.ts > t.a) ? 1 : 0;
+    const int64_t fv = Vr & ~(int64_t)7;
+    const int64_t lim = end < fv ? end : fv;
+    const int64_t hi = (lim - t.a) >> 3;
+    g.n = (int)((((end + 7) & ~(int64_t)7) - t.a) >> 3);
+    g.hi = hi < g.lo ? g.lo : (int)hi;
+    if (g.hi > g.n) g.hi = g.n;
+    return g;
+}
+
+__device__ __forceinline__ int edge_group(const GroupRange& g, int e) { return e < g.lo ? 0 : g.hi + (e - g.lo); }
+
+__device__ __forceinline__ void max4(uint32_t (&acc)[4], const uint4& v) {
+    acc[0] = bf16x2_max_nan(acc[0], v.x);
+    acc[1] = bf16x2_max_nan(acc[1], v.y);
+    acc[2] = bf16x2_max_nan(acc[2], v.z);
+    acc[3] = bf16x2_max_nan(acc[3], v.w);
+}
+
+__device__ __forceinline__ void sum8(float (&s)[8], const uint4& v, float nmL) {
+    s[0] = __fadd_rn(s[0], exp_term(bf16lo_to_f32(v.x), nmL));
+    s[1] = __fadd_rn(s[1], exp_term(bf16hi_to_f32(v.x), nmL));
+    s[2] = __fadd_rn(s[2], exp_term(bf16lo_to_f32(v.y), nmL));
+    s[3] = __fadd_rn(s[3], exp_term(bf16hi_to_f32(v.y), nmL));
+    s[4] = __fadd_rn(s[4], exp_term(bf16lo_to_f32(v.z), nmL));
+    s[5] = __fadd_rn(s[5], exp_term(bf16hi_to_f32(v.z), nmL));
+    s[6] = __fadd_rn(s[6], exp_term(bf16lo_to_f32(v.w), nmL));
+    s[7] = __fadd_rn(s[7], exp_term(bf16hi_to_f32(v.w), nmL));
+}
+
 // (m_k, s_k) of one tile, computed by one warp; every lane returns the same value.
-__device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const TileGeom& t, int lane) {
+// Lane l visits interior groups lo+l, lo+l+32, ... then its edge groups; the
+// tile maximum is exact, the sum uses 8 accumulators combined pairwise, then
+// a fixed xor butterfly across lanes.
+__device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const TileGeom& t, int64_t Vr,
+                               int lane) {
     if (t.hi <= t.ts) return make_float2(-INFINITY, 0.f);  // padding-only tile: identity
-    const int ng = (int)((((t.hi + 7) & ~(int64_t)7) - t.a) >> 3);
-    uint32_t acc0 = 0xFF80FF80u, acc1 = 0xFF80FF80u;
+    const GroupRange gr = group_range(t, t.hi, Vr);
+    const int ne = gr.lo + (gr.n - gr.hi);
+    const uint4* s4 = reinterpret_cast<const uint4*>(slot);
+    uint32_t acc[4] = {0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u};
 #pragma unroll 4
-    for (int gi = lane; gi < ng; gi += 32) {
-        const uint4 v = load_group(slot, grow, t.a + 8 * (int64_t)gi, t);
-        acc0 = bf16x2_max_nan(acc0, v.x);
-        acc1 = bf16x2_max_nan(acc1, v.y);
-        acc0 = bf16x2_max_nan(acc0, v.z);
-        acc1 = bf16x2_max_nan(acc1, v.w);
-    }
-    acc0 = bf16x2_max_nan(acc0, acc1);
-    const float m = warp_max_nan(fmax_nan(bf16lo_to_f32(acc0), bf16hi_to_f32(acc0)));
+    for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) max4(acc, s4[gi]);
+    for (int e = lane; e < ne; e += 32) max4(acc, load_group(slot, grow, t.a + 8 * (int64_t)edge_group(gr, e), t));
+    acc[0] = bf16x2_max_nan(bf16x2_max_nan(acc[0], acc[1]), bf16x2_max_nan(acc[2], acc[3]));
+    const float m = warp_max_nan(fmax_nan(bf16lo_to_f32(acc[0]), bf16hi_to_f32(acc[0])));
     if (m == -INFINITY) return make_float2(-INFINITY, 0.f);  // all -inf: identity
     const float nmL = -__fmul_rn(m, kLog2e);
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-    for (int gi = lane; gi < ng; gi += 32) {
-        const uint4 v = load_group(slot, grow, t.a + 8 * (int64_t)gi, t);
-        s0 = __fadd_rn(s0, exp_term(bf16lo_to_f32(v.x), nmL));
-        s1 = __fadd_rn(s1, exp_term(bf16hi_to_f32(v.x), nmL));
-        s2 = __fadd_rn(s2, exp_term(bf16lo_to_f32(v.y), nmL));
-        s3 = __fadd_rn(s3, exp_term(bf16hi_to_f32(v.y), nmL));
-        s0 = __fadd_rn(s0, exp_term(bf16lo_to_f32(v.z), nmL));
-        s1 = __fadd_rn(s1, exp_term(bf16hi_to_f32(v.z), nmL));
-        s2 = __fadd_rn(s2, exp_term(bf16lo_to_f32(v.w), nmL));
-        s3 = __fadd_rn(s3, exp_term(bf16hi_to_f32(v.w), nmL));
-    }
-    const float s = warp_sum(__fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3)));
+    for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) sum8(sm, s4[gi], nmL);
+    for (int e = lane; e < ne; e += 32) sum8(sm, load_group(slot, grow, t.a + 8 * (int64_t)edge_group(gr, e), t), nmL);
+    const float s = warp_sum(__fadd_rn(__fadd_rn(__fadd_rn(sm[0], sm[1]), __fadd_rn(sm[2], sm[3])),
+                                       __fadd_rn(__fadd_rn(sm[4], sm[5]), __fadd_rn(sm[6], sm[7]))));
     return make_float2(m, s);
+}
+
+// dlogits of 8 columns from their exp terms: -g * p, and g * (1 - p) at the target.
+__device__ __forceinline__ uint4 grad8(const float (&pr)[8], int64_t c0, bool tgt_ok, int64_t target, float g) {
+    float d[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) d[e] = __fmul_rn(-g, pr[e]);
+    if (tgt_ok && (uint64_t)(target - c0) < 8u) {
+        const int e = (int)(target - c0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j == e) d[j] = __fmul_rn(g, __fsub_rn(1.f, pr[j]));
+    }
+    return make_uint4(pack_bf16x2_rn(d[0], d[1]), pack_bf16x2_rn(d[2], d[3]), pack_bf16x2_rn(d[4], d[5]),
+                      pack_bf16x2_rn(d[6], d[7]));
 }
 
 // dlogits of one tile's columns [ts, te) of one row, by one warp.
 __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* drow, const TileGeom& t,
                           int64_t Vr, bool active, int64_t target, float g, float lse, int lane) {
-    const int64_t ce = (t.te + 7) & ~(int64_t)7;
-    const int ng = (int)((ce - t.a) >> 3);
+    const GroupRange gr = group_range(t, t.te, Vr);
+    const int ne = gr.lo + (gr.n - gr.hi);
+    uint4* d4 = reinterpret_cast<uint4*>(drow + t.a);
     if (!active) {
-        for (int gi = lane; gi < ng; gi += 32) {
-            const int64_t c0 = t.a + 8 * (int64_t)gi;
-            if (c0 >= t.ts && c0 + 8 <= t.te) {
-                __stcs(reinterpret_cast<uint4*>(drow + c0), make_uint4(0u, 0u, 0u, 0u));
-            } else {
-                for (int e = 0; e < 8; ++e) {
-                    const int64_t c = c0 + e;
-                    if (c >= t.ts && c < t.te) drow[c] = 0;
-                }
+        for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) __stcs(d4 + gi, make_uint4(0u, 0u, 0u, 0u));
+        for (int e = lane; e < ne; e += 32) {
+            const int64_t c0 = t.a + 8 * (int64_t)edge_group(gr, e);
+            for (int j = 0; j < 8; ++j) {
+                const int64_t c = c0 + j;
+                if (c >= t.ts && c < t.te) drow[c] = 0;
             }
         }
         return;
     }
     const float nlL = -__fmul_rn(lse, kLog2e);
-    const float ng_ = -g;
     const bool tgt_ok = target >= 0 && target < Vr;
+    const uint4* s4 = reinterpret_cast<const uint4*>(slot);
 #pragma unroll 2
-    for (int gi = lane; gi < ng; gi += 32) {
-        const int64_t c0 = t.a + 8 * (int64_t)gi;
+    for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) {
+        const uint4 v = s4[gi];
+        const float pr[8] = {exp_term(bf16lo_to_f32(v.x), nlL), exp_term(bf16hi_to_f32(v.x), nlL),
+                             exp_term(bf16lo_to_f32(v.y), nlL), exp_term(bf16hi_to_f32(v.y), nlL),
+                             exp_term(bf16lo_to_f32(v.z), nlL), exp_term(bf16hi_to_f32(v.z), nlL),
+                             exp_term(bf16lo_to_f32(v.w), nlL), exp_term(bf16hi_to_f32(v.w), nlL)};
+        __stcs(d4 + gi, grad8(pr, t.a + 8 * (int64_t)gi, tgt_ok, target, g));
+    }
+    for (int e = lane; e < ne; e += 32) {
+        const int64_t c0 = t.a + 8 * (int64_t)edge_group(gr, e);
         float pr[8];
-        bool fast = c0 + 8 <= t.b;
-        if (fast) {
+        if (c0 + 8 <= t.b) {
             const uint4 v = *reinterpret_cast<const uint4*>(slot + (c0 - t.a));
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -263,36 +333,18 @@ __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* 
             }
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int64_t c = c0 + e;
-                pr[e] = (c < Vr) ? exp_term(__uint_as_float((uint32_t)ldg_bf16(grow + c) << 16), nlL) : 0.f;
+            for (int j = 0; j < 8; ++j) {
+                const int64_t c = c0 + j;
+                pr[j] = (c < Vr) ? exp_term(__uint_as_float((uint32_t)ldg_bf16(grow + c) << 16), nlL) : 0.f;
             }
         }
-        float d[8];
+        uint4 q = grad8(pr, c0, tgt_ok, target, g);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) d[e] = __fmul_rn(ng_, pr[e]);
-        if (!fast) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                if (c0 + e >= Vr) d[e] = 0.f;  // padded column: exactly +0
-        }
-        if (tgt_ok && (uint64_t)(target - c0) < 8u) {
-            const int e = (int)(target - c0);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j == e) d[j] = __fmul_rn(g, __fsub_rn(1.f, pr[j]));
-        }
-        const uint32_t w0 = pack_bf16x2_rn(d[0], d[1]), w1 = pack_bf16x2_rn(d[2], d[3]);
-        const uint32_t w2 = pack_bf16x2_rn(d[4], d[5]), w3 = pack_bf16x2_rn(d[6], d[7]);
-        if (c0 >= t.ts && c0 + 8 <= t.te) {
-            __stcs(reinterpret_cast<uint4*>(drow + c0), make_uint4(w0, w1, w2, w3));
-        } else {
-            const uint32_t w[4] = {w0, w1, w2, w3};
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int64_t c = c0 + e;
-                if (c >= t.ts && c < t.te) drow[c] = (uint16_t)((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu));
-            }
+        for (int j = 0; j < 8; ++j) {
+            const int64_t c = c0 + j;
+            if (c >= t.ts && c < t.te)
+                drow[c] = (c >= Vr) ? (uint16_t)0 : (uint16_t)((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
         }
     }
 }
@@ -303,7 +355,7 @@ struct Ctx {
     int warp, lane;
     uint32_t rank;
     int64_t q, G, nrows;
-    int k0, ntl;
+    int k0, ntl, nch;  // first tile, tiles and ring chunks of this CTA per row
     unsigned char* smem;
     uint32_t sbase, full0, empty0, xbar0;
     SlotHdr* hdr;
@@ -348,7 +400,7 @@ __device__ void producer(const Params& p, const Ctx& x) {
         const float lin = __shfl_sync(0xFFFFFFFFu, m_l, src);
         const int64_t row = x.q + n * x.G;
         const uint16_t* grow = p.a.logits + row * p.stride;
-        for (int l = 0; l < x.ntl; ++l) {
+        for (int c = 0; c < x.nch; ++c) {
             bool ok = true;
             if (lane == 0) ok = x.wt.wait(x.empty0 + 8u * slot, phase ^ 1u, false);
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -365,13 +417,15 @@ __device__ void producer(const Params& p, const Ctx& x) {
                 h.pad = 0;
                 h.row = row;
                 x.hdr[slot] = h;
-                const TileGeom tg = tile_geom(x.k0 + l, p);
+                const int kf = x.k0 + c * p.tps;
+                const int kl = min(kf + p.tps, x.k0 + x.ntl);
+                const Span sp = chunk_span(kf, kl, p);
                 const uint32_t bytes =
-                    (tg.b > tg.a && (MODE != kModeBwd || act)) ? (uint32_t)((tg.b - tg.a) * 2) : 0u;
+                    (sp.b > sp.a && (MODE != kModeBwd || act)) ? (uint32_t)((sp.b - sp.a) * 2) : 0u;
                 const uint32_t fb = x.full0 + 8u * slot;
                 if (bytes) {
                     mbar_arrive_expect_tx(fb, bytes);
-                    bulk_g2s(x.sbase + (uint32_t)slot * (uint32_t)p.slot_bytes, grow + tg.a, bytes, fb, policy);
+                    bulk_g2s(x.sbase + (uint32_t)slot * (uint32_t)p.slot_bytes, grow + sp.a, bytes, fb, policy);
                 } else {
                     mbar_arrive(fb);
                 }
@@ -478,86 +532,123 @@ __device__ void fold_row(const Params& p, const Ctx& x, int64_t n) {
     }
 }
 
+// Position of an item in the slot ring: slot index and the parity of the pass.
+struct RingPos {
+    int slot;
+    uint32_t par;
+};
+
+__device__ __forceinline__ RingPos ring_add(RingPos r, int k, int NS) {
+    const int s = r.slot + k;
+    const int q = s / NS;
+    return RingPos{s - q * NS, r.par ^ (uint32_t)(q & 1)};
+}
+
 template <int MODE>
 __device__ void consumer(const Params& p, const Ctx& x) {
-    const int W = kConsumerWarps;
+    constexpr int W = kConsumerWarps;
+    static_assert((W & (W - 1)) == 0, "consumer warp count must be a power of two");
     const int lane = x.lane;
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
     const int slot_elems = p.slot_bytes / 2;
     if constexpr (MODE == kModeBwd) {
-        const int64_t total = x.nrows * x.ntl;
+        // Items (row, chunk) in order; warp w takes items w, w+W, ...
+        const int64_t total = x.nrows * x.nch;
+        RingPos pos = ring_add(RingPos{0, 0u}, x.warp, p.NS);
+        int c = x.warp % x.nch;
         for (int64_t i = x.warp; i < total; i += W) {
-            const int slot = (int)(i % p.NS);
-            if (!x.wt.warp_wait(x.full0 + 8u * slot, (uint32_t)((i / p.NS) & 1))) continue;
+            const int slot = pos.slot;
+            const bool ok = x.wt.warp_wait(x.full0 + 8u * slot, pos.par);
+            const int cc = c;
+            pos = ring_add(pos, W, p.NS);
+            c = (c + W) % x.nch;
+            if (!ok) continue;
             const SlotHdr h = x.hdr[slot];
-            const int k = (int)(i % x.ntl);
-            const TileGeom tg = tile_geom(x.k0 + k, p);
-            if (k == 0 && lane == 0 && h.active) {
+            const int kf = x.k0 + cc * p.tps, kl = min(kf + p.tps, x.k0 + x.ntl);
+            const Span sp = chunk_span(kf, kl, p);
+            if (cc == 0 && lane == 0 && h.active) {
                 if (h.target < 0 || h.target >= p.Vr) atomicOr(p.a.status, kStatusTargetRange);
                 if (!isfinite(h.lse_in)) atomicOr(p.a.status, kStatusNonFinite);
             }
-            tile_grad(slots + (size_t)slot * slot_elems, p.a.logits + h.row * p.stride,
-                      p.a.dlogits + h.row * p.stride, tg, p.Vr, h.active != 0, h.target, h.g, h.lse_in, lane);
+            for (int k = kf; k < kl; ++k) {
+                const TileGeom tg = tile_geom(k, p, sp);
+                tile_grad(slots + (size_t)slot * slot_elems + (tg.a - sp.a), p.a.logits + h.row * p.stride,
+                          p.a.dlogits + h.row * p.stride, tg, p.Vr, h.active != 0, h.target, h.g, h.lse_in, lane);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(x.empty0 + 8u * slot);
         }
     } else {
-    for (int64_t n = 0; n < x.nrows; ++n) {
-        const int buf = (int)(n & 1);
-        const int64_t ibase = n * x.ntl;
-        const int lfirst = (int)((x.warp - (int)(ibase % W) + W) % W);
-        bool row_ok = true;  // every phase-A wait of this warp in this row succeeded
-        for (int l = lfirst; l < x.ntl; l += W) {
-            const int64_t i = ibase + l;
-            const int slot = (int)(i % p.NS);
-            if (!x.wt.warp_wait(x.full0 + 8u * slot, (uint32_t)((i / p.NS) & 1))) {
-                row_ok = false;
-                continue;
-            }
-            const SlotHdr h = x.hdr[slot];
-            const TileGeom tg = tile_geom(x.k0 + l, p);
-            const uint16_t* sl = slots + (size_t)slot * slot_elems;
-            const uint16_t* grow = p.a.logits + h.row * p.stride;
-            const float2 pr = tile_partial(sl, grow, tg, lane);
-            if (lane == 0) {
-                x.part[(size_t)buf * p.NT + x.k0 + l] = pr;
-                RowShared& rs = x.rows[buf];
-                if (l == 0) {
+        // Row n's chunks are items n*nch + c; warp w takes the chunks with
+        // (n*nch + c) mod W == w.
+        RingPos base{0, 0u};
+        for (int64_t n = 0; n < x.nrows; ++n) {
+            const RingPos rb = base;
+            base = ring_add(base, x.nch, p.NS);
+            const int buf = (int)(n & 1);
+            const int lfirst = (x.warp - (int)((n * x.nch) & (W - 1))) & (W - 1);
+            bool row_ok = true;  // every phase-A wait of this warp in this row succeeded
+            for (int c = lfirst; c < x.nch; c += W) {
+                const RingPos ps = ring_add(rb, c, p.NS);
+                const int slot = ps.slot;
+                if (!x.wt.warp_wait(x.full0 + 8u * slot, ps.par)) {
+                    row_ok = false;
+                    continue;
+                }
+                const SlotHdr h = x.hdr[slot];
+                const int kf = x.k0 + c * p.tps, kl = min(kf + p.tps, x.k0 + x.ntl);
+                const Span sp = chunk_span(kf, kl, p);
+                const uint16_t* grow = p.a.logits + h.row * p.stride;
+                if (c == 0 && lane == 0) {
+                    RowShared& rs = x.rows[buf];
                     rs.target = h.target;
                     rs.active = h.active;
                     rs.g = h.g;
                 }
-                if (h.active && h.target >= tg.ts && h.target < tg.hi) {
-                    const uint16_t bits = (h.target < tg.b) ? sl[h.target - tg.a] : ldg_bf16(grow + h.target);
-                    rs.xt = __uint_as_float((uint32_t)bits << 16);
-                    rs.has_xt = 1;
+                for (int k = kf; k < kl; ++k) {
+                    const TileGeom tg = tile_geom(k, p, sp);
+                    const uint16_t* sl = slots + (size_t)slot * slot_elems + (tg.a - sp.a);
+                    const float2 pr = tile_partial(sl, grow, tg, p.Vr, lane);
+                    if (lane == 0) {
+                        x.part[(size_t)buf * p.NT + k] = pr;
+                        if (h.active && h.target >= tg.ts && h.target < tg.hi) {
+                            const uint16_t bits =
+                                (h.target < tg.b) ? sl[h.target - tg.a] : ldg_bf16(grow + h.target);
+                            RowShared& rs = x.rows[buf];
+                            rs.xt = __uint_as_float((uint32_t)bits << 16);
+                            rs.has_xt = 1;
+                        }
+                    }
+                }
+                if (MODE == kModeFwd) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(x.empty0 + 8u * slot);
                 }
             }
-            if (MODE == kModeFwd) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(x.empty0 + 8u * slot);
+            named_bar_sync(1, W * 32);
+            if (x.warp == 0) fold_row<MODE>(p, x, n);
+            if (MODE == kModeFused) {
+                named_bar_sync(2, W * 32);
+                // After an expired wait the slot headers may be stale: skip the
+                // writes (the status word already says RLK_ERR_TIMEOUT).
+                if (!row_ok || *x.wt.abort_flag) continue;
+                const float lse_v = x.rows[buf].lse;
+                for (int c = lfirst; c < x.nch; c += W) {
+                    const int slot = ring_add(rb, c, p.NS).slot;
+                    const SlotHdr h = x.hdr[slot];
+                    const int kf = x.k0 + c * p.tps, kl = min(kf + p.tps, x.k0 + x.ntl);
+                    const Span sp = chunk_span(kf, kl, p);
+                    for (int k = kf; k < kl; ++k) {
+                        const TileGeom tg = tile_geom(k, p, sp);
+                        tile_grad(slots + (size_t)slot * slot_elems + (tg.a - sp.a), p.a.logits + h.row * p.stride,
+                                  p.a.dlogits + h.row * p.stride, tg, p.Vr, h.active != 0, h.target, h.g, lse_v,
+                                  lane);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(x.empty0 + 8u * slot);
+                }
             }
         }
-        named_bar_sync(1, W * 32);
-        if (x.warp == 0) fold_row<MODE>(p, x, n);
-        if (MODE == kModeFused) {
-            named_bar_sync(2, W * 32);
-            // After an expired wait the slot headers may be stale: skip the
-            // writes (the status word already says RLK_ERR_TIMEOUT).
-            if (!row_ok || *x.wt.abort_flag) continue;
-            const float lse_v = x.rows[buf].lse;
-            for (int l = lfirst; l < x.ntl; l += W) {
-                const int64_t i = ibase + l;
-                const int slot = (int)(i % p.NS);
-                const SlotHdr h = x.hdr[slot];
-                const TileGeom tg = tile_geom(x.k0 + l, p);
-                tile_grad(slots + (size_t)slot * slot_elems, p.a.logits + h.row * p.stride,
-                          p.a.dlogits + h.row * p.stride, tg, p.Vr, h.active != 0, h.target, h.g, lse_v, lane);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(x.empty0 + 8u * slot);
-            }
-        }
-    }
     }
 }
 
@@ -573,6 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     x.nrows = (x.q < p.T) ? (p.T - 1 - x.q) / x.G + 1 : 0;
     x.k0 = (int)(((int64_t)x.rank * p.NT) / p.C);
     x.ntl = (int)(((int64_t)(x.rank + 1) * p.NT) / p.C) - x.k0;
+    x.nch = (x.ntl + p.tps - 1) / p.tps;
     x.smem = smem;
     x.sbase = smem_u32(smem);
     x.full0 = x.sbase + p.off_full;
@@ -608,6 +700,22 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
 
     __syncthreads();
     if (p.C > 1) cluster_sync_all();  // no CTA leaves while a peer may still write into it
+}
+
+// One warp waits, with the kernels' bounded wait, on an mbarrier that nothing
+// arrives at; the wait must expire and record RLK_ERR_TIMEOUT.
+__global__ void selftest_wait_kernel(uint32_t* status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    Waiter wt{&abort_flag, status, limit_ns};
+    wt.warp_wait(smem_u32(&bar), 0u);
+    __syncthreads();
 }
 
 // ----------------------------------------------------------------- host planning
@@ -660,6 +768,13 @@ uint32_t layout(Params& p, int NS) {
 
 }  // namespace
 
+rlk_status launch_selftest_wait(uint64_t limit_ns, uint32_t* status, cudaStream_t stream) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(e));
+    return RLK_OK;
+}
+
 rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs& a, cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return fail(RLK_ERR_CUDA, "cudaGetDevice failed");
@@ -677,7 +792,12 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     p.NT = c.num_tiles;
     p.W = (int32_t)(c.V_padded / c.num_tiles);
     p.mask_mode = c.mask_mode;
-    p.slot_bytes = (int32_t)align_up((uint32_t)((((p.W + 7) & ~7) + 8) * 2), 16);
+    // Narrow tiles share a slot: about 4096 columns per slot.
+    p.tps = p.W >= 4096 ? 1 : 4096 / p.W;
+    {
+        const int64_t cols = (int64_t)p.tps * p.W;
+        p.slot_bytes = (int32_t)align_up((uint32_t)((((cols + 7) & ~(int64_t)7) + 8) * 2), 16);
+    }
 
     const int ctas_per_sm = env_int("RLK_CTAS_PER_SM", 1) >= 2 ? 2 : 1;
     const uint32_t budget = (uint32_t)di.smem_optin / (uint32_t)ctas_per_sm - 1024u;
@@ -699,7 +819,7 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
             p.C = C;
             NS = max_slots(p);
             const int ntl_max = (c.num_tiles + C - 1) / C;
-            if (NS >= ntl_max) break;
+            if (NS >= (ntl_max + p.tps - 1) / p.tps) break;
             C *= 2;
             if (C > 8 || C > c.num_tiles)
                 return fail(RLK_ERR_UNSUPPORTED,

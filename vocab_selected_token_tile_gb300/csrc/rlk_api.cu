@@ -76,7 +76,7 @@ rlk_status select_device(const void* ptr) {
     cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaPointerGetAttributes: ") + cudaGetErrorString(e));
     if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
-        return fail(RLK_ERR_INVALID_ARG, "logits must be device memory");
+        return fail(RLK_ERR_INVALID_ARG, "device buffers must be device memory");
     e = cudaSetDevice(attr.device);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaSetDevice: ") + cudaGetErrorString(e));
     return RLK_OK;
@@ -176,6 +176,19 @@ RLK_EXPORT rlk_status rlk_logp_bwd(const rlk_logp_contract* c, const void* logit
 RLK_EXPORT rlk_status rlk_logp_workspace_status(const void* workspace, rlk_stream_t stream) {
     if (!workspace) return fail(RLK_ERR_INVALID_ARG, "workspace is NULL");
     return read_status(workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+RLK_EXPORT rlk_status rlk_selftest_bounded_wait(int64_t timeout_ns, void* workspace, rlk_stream_t stream) {
+    if (timeout_ns <= 0 || timeout_ns > 10000000000ll)
+        return fail(RLK_ERR_INVALID_ARG, "timeout_ns must be in (0, 10 s]");
+    if (!workspace) return fail(RLK_ERR_INVALID_ARG, "workspace is NULL");
+    if (!aligned16(workspace)) return fail(RLK_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    rlk_status s = select_device(workspace);
+    if (s != RLK_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = begin(workspace, st)) != RLK_OK) return s;
+    if ((s = launch_selftest_wait((uint64_t)timeout_ns, static_cast<uint32_t*>(workspace), st)) != RLK_OK) return s;
+    return read_status(workspace, st);
 }
 
 RLK_EXPORT const char* rlk_status_string(rlk_status s) {

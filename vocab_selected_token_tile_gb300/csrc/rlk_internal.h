@@ -46,4 +46,8 @@ rlk_status fail(rlk_status s, const std::string& why);
 // validated contract; returns RLK_OK or an error with the message set.
 rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs& a, cudaStream_t stream);
 
+// Launches the bounded-wait self-test kernel (one warp waiting on an mbarrier
+// that nothing arrives at).
+rlk_status launch_selftest_wait(uint64_t limit_ns, uint32_t* status, cudaStream_t stream);
+
 }  // namespace rlk
