@@ -51,7 +51,9 @@ namespace rlk {
 namespace {
 
 constexpr int kConsumerWarps = 16;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kFoldWarp = kConsumerWarps;          // folds each row's partials
+constexpr int kProducerWarp = kConsumerWarps + 1;  // issues the bulk copies
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kMaxSlots = 96;
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^y = 2^(y log2 e)
 constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the final drain of own copies
@@ -83,7 +85,7 @@ struct Params {
     uint64_t wait_ns;
     int32_t NT, W, C, mask_mode, NS, slot_bytes;
     int32_t tps;  // tiles per ring slot (consecutive tiles of one row share a slot when narrow)
-    uint32_t off_full, off_empty, off_hdr, off_part, off_fold, off_rows, off_xbar, off_flag;
+    uint32_t off_full, off_empty, off_hdr, off_part, off_fold, off_rows, off_bars, off_flag;
 };
 
 struct TileGeom {
@@ -204,10 +206,6 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__device__ __forceinline__ float exp_term(float x, float neg_mL) {
-    return ex2_approx(__fmaf_rn(x, kLog2e, neg_mL));
-}
-
 // Groups of one tile, indexed from floor8(ts): the "interior" groups [lo, hi)
 // lie entirely inside [ts, min(end, floor8(V_real))) -- full, real, and always
 // held in the slot -- and take a branch-free path; the others (a partial first
@@ -238,15 +236,26 @@ __device__ __forceinline__ void max4(uint32_t (&acc)[4], const uint4& v) {
     acc[3] = bf16x2_max_nan(acc[3], v.w);
 }
 
-__device__ __forceinline__ void sum8(float (&s)[8], const uint4& v, float nmL) {
-    s[0] = __fadd_rn(s[0], exp_term(bf16lo_to_f32(v.x), nmL));
-    s[1] = __fadd_rn(s[1], exp_term(bf16hi_to_f32(v.x), nmL));
-    s[2] = __fadd_rn(s[2], exp_term(bf16lo_to_f32(v.y), nmL));
-    s[3] = __fadd_rn(s[3], exp_term(bf16hi_to_f32(v.y), nmL));
-    s[4] = __fadd_rn(s[4], exp_term(bf16lo_to_f32(v.z), nmL));
-    s[5] = __fadd_rn(s[5], exp_term(bf16hi_to_f32(v.z), nmL));
-    s[6] = __fadd_rn(s[6], exp_term(bf16lo_to_f32(v.w), nmL));
-    s[7] = __fadd_rn(s[7], exp_term(bf16hi_to_f32(v.w), nmL));
+// The two BF16 values of a packed word as an FP32 pair (lo, hi).
+__device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w) {
+    return make_float2(bf16lo_to_f32(w), bf16hi_to_f32(w));
+}
+
+// 2^(x*log2e + c) of an FP32 pair: one packed FMA (each lane rounded as a
+// scalar FMA would be) and two SFU exponentials.
+__device__ __forceinline__ float2 exp_terms2(float2 x, float2 c) {
+    const float2 t = __ffma2_rn(x, make_float2(kLog2e, kLog2e), c);
+    return make_float2(ex2_approx(t.x), ex2_approx(t.y));
+}
+
+// Accumulates the 8 exp terms of a group into 4 packed accumulators:
+// s[j] holds the running sums of elements 2j and 2j+1 of every group.
+__device__ __forceinline__ void sum8(float2 (&s)[4], const uint4& v, float nmL) {
+    const float2 c = make_float2(nmL, nmL);
+    s[0] = __fadd2_rn(s[0], exp_terms2(bf16x2_to_f32x2(v.x), c));
+    s[1] = __fadd2_rn(s[1], exp_terms2(bf16x2_to_f32x2(v.y), c));
+    s[2] = __fadd2_rn(s[2], exp_terms2(bf16x2_to_f32x2(v.z), c));
+    s[3] = __fadd2_rn(s[3], exp_terms2(bf16x2_to_f32x2(v.w), c));
 }
 
 // (m_k, s_k) of one tile, computed by one warp; every lane returns the same value.
@@ -267,20 +276,25 @@ __device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const
     const float m = warp_max_nan(fmax_nan(bf16lo_to_f32(acc[0]), bf16hi_to_f32(acc[0])));
     if (m == -INFINITY) return make_float2(-INFINITY, 0.f);  // all -inf: identity
     const float nmL = -__fmul_rn(m, kLog2e);
-    float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float2 sm[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll 4
     for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) sum8(sm, s4[gi], nmL);
     for (int e = lane; e < ne; e += 32) sum8(sm, load_group(slot, grow, t.a + 8 * (int64_t)edge_group(gr, e), t), nmL);
-    const float s = warp_sum(__fadd_rn(__fadd_rn(__fadd_rn(sm[0], sm[1]), __fadd_rn(sm[2], sm[3])),
-                                       __fadd_rn(__fadd_rn(sm[4], sm[5]), __fadd_rn(sm[6], sm[7]))));
+    const float s = warp_sum(__fadd_rn(__fadd_rn(__fadd_rn(sm[0].x, sm[0].y), __fadd_rn(sm[1].x, sm[1].y)),
+                                       __fadd_rn(__fadd_rn(sm[2].x, sm[2].y), __fadd_rn(sm[3].x, sm[3].y))));
     return make_float2(m, s);
 }
 
 // dlogits of 8 columns from their exp terms: -g * p, and g * (1 - p) at the target.
 __device__ __forceinline__ uint4 grad8(const float (&pr)[8], int64_t c0, bool tgt_ok, int64_t target, float g) {
     float d[8];
+    const float2 ng2 = make_float2(-g, -g);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) d[e] = __fmul_rn(-g, pr[e]);
+    for (int e = 0; e < 8; e += 2) {
+        const float2 q = __fmul2_rn(make_float2(pr[e], pr[e + 1]), ng2);
+        d[e] = q.x;
+        d[e + 1] = q.y;
+    }
     if (tgt_ok && (uint64_t)(target - c0) < 8u) {
         const int e = (int)(target - c0);
 #pragma unroll
@@ -314,10 +328,10 @@ __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* 
 #pragma unroll 2
     for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) {
         const uint4 v = s4[gi];
-        const float pr[8] = {exp_term(bf16lo_to_f32(v.x), nlL), exp_term(bf16hi_to_f32(v.x), nlL),
-                             exp_term(bf16lo_to_f32(v.y), nlL), exp_term(bf16hi_to_f32(v.y), nlL),
-                             exp_term(bf16lo_to_f32(v.z), nlL), exp_term(bf16hi_to_f32(v.z), nlL),
-                             exp_term(bf16lo_to_f32(v.w), nlL), exp_term(bf16hi_to_f32(v.w), nlL)};
+        const float2 c = make_float2(nlL, nlL);
+        const float2 p0 = exp_terms2(bf16x2_to_f32x2(v.x), c), p1 = exp_terms2(bf16x2_to_f32x2(v.y), c);
+        const float2 p2 = exp_terms2(bf16x2_to_f32x2(v.z), c), p3 = exp_terms2(bf16x2_to_f32x2(v.w), c);
+        const float pr[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
         __stcs(d4 + gi, grad8(pr, t.a + 8 * (int64_t)gi, tgt_ok, target, g));
     }
     for (int e = lane; e < ne; e += 32) {
@@ -328,14 +342,19 @@ __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* 
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                pr[2 * j] = exp_term(bf16lo_to_f32(w[j]), nlL);
-                pr[2 * j + 1] = exp_term(bf16hi_to_f32(w[j]), nlL);
+                const float2 q = exp_terms2(bf16x2_to_f32x2(w[j]), make_float2(nlL, nlL));
+                pr[2 * j] = q.x;
+                pr[2 * j + 1] = q.y;
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 8; j += 2) {
                 const int64_t c = c0 + j;
-                pr[j] = (c < Vr) ? exp_term(__uint_as_float((uint32_t)ldg_bf16(grow + c) << 16), nlL) : 0.f;
+                const uint32_t lo = (c < Vr) ? ldg_bf16(grow + c) : 0xFF80u;
+                const uint32_t hi = (c + 1 < Vr) ? ldg_bf16(grow + c + 1) : 0xFF80u;
+                const float2 q = exp_terms2(bf16x2_to_f32x2(lo | (hi << 16)), make_float2(nlL, nlL));
+                pr[j] = q.x;
+                pr[j + 1] = q.y;
             }
         }
         uint4 q = grad8(pr, c0, tgt_ok, target, g);
@@ -351,13 +370,21 @@ __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* 
 
 // ----------------------------------------------------------------- kernel roles
 
+// Per-row buffers of the fold: row n uses buffer n % kRowBufs.
+constexpr int kRowBufs = 2;
+
 struct Ctx {
     int warp, lane;
     uint32_t rank;
     int64_t q, G, nrows;
     int k0, ntl, nch;  // first tile, tiles and ring chunks of this CTA per row
     unsigned char* smem;
-    uint32_t sbase, full0, empty0, xbar0;
+    uint32_t sbase, full0, empty0;
+    // per row buffer b: rowdone[b] (every consumer warp arrived: partials of the
+    // row are in part[b]), lseready[b] (fold done, rows[b].lse valid),
+    // partfree[b] (part[b] and rows[b] may be reused), xbar[b] (peer CTAs'
+    // partials arrived)
+    uint32_t rowdone0, lseready0, partfree0, xbar0;
     SlotHdr* hdr;
     float2* part;
     float2* fold;
@@ -453,82 +480,91 @@ __device__ void producer(const Params& p, const Ctx& x) {
     }
 }
 
-// Exchange (cluster), fold, outputs: warp 0 of every CTA, after the row's
-// partials of this CTA are in part[buf].
+// The fold warp: for each row, once every consumer warp of this CTA has put
+// its tiles' partials in part[b], push this CTA's shard of partials into
+// each peer CTA (virtual TP > 1), wait for the peers' shards, fold all tiles
+// in index order, write the outputs, and release the buffer.
 template <int MODE>
-__device__ void fold_row(const Params& p, const Ctx& x, int64_t n) {
+__device__ void fold_warp(const Params& p, const Ctx& x) {
     const int lane = x.lane;
-    const int buf = (int)(n & 1);
-    float2* part = x.part + (size_t)buf * p.NT;
-    bool ok = !*x.wt.abort_flag;
-    if (p.C > 1) {
-        if (ok && lane < p.C && (uint32_t)lane != x.rank) {
-            // Push this CTA's shard of partials into peer `lane`, then release them.
-            for (int kk = x.k0; kk < x.k0 + x.ntl; ++kk) {
-                const float2 v = part[kk];
-                st_cluster_f32x2(mapa_shared(smem_u32(&part[kk]), (uint32_t)lane), v.x, v.y);
+    for (int64_t n = 0; n < x.nrows; ++n) {
+        const int b = (int)(n % kRowBufs);
+        const uint32_t par = (uint32_t)((n / kRowBufs) & 1);
+        float2* part = x.part + (size_t)b * p.NT;
+        bool ok = x.wt.warp_wait(x.rowdone0 + 8u * b, par);
+        if (p.C > 1) {
+            if (ok && lane < p.C && (uint32_t)lane != x.rank) {
+                for (int kk = x.k0; kk < x.k0 + x.ntl; ++kk) {
+                    const float2 v = part[kk];
+                    st_cluster_f32x2(mapa_shared(smem_u32(&part[kk]), (uint32_t)lane), v.x, v.y);
+                }
+                mbar_arrive_remote(mapa_shared(x.xbar0 + 8u * b, (uint32_t)lane));
             }
-            mbar_arrive_remote(mapa_shared(x.xbar0 + 8u * buf, (uint32_t)lane));
+            __syncwarp();
+            ok = x.wt.warp_wait(x.xbar0 + 8u * b, par, true) && ok;
+        }
+        if (!ok) continue;
+        // Left fold over k = 0..NT-1.  The running maxima M_k are an exact
+        // prefix max; the rescale factors f_k = exp(M_{k-1} - M_k) and terms
+        // b_k = s_k exp(m_k - M_k) are formed lane-parallel; the sum
+        // recurrence S_k = S_{k-1} f_k + b_k then runs in index order in one lane.
+        float carry = -INFINITY;
+        for (int c0 = 0; c0 < p.NT; c0 += 32) {
+            const int k = c0 + lane;
+            const float2 pk = k < p.NT ? part[k] : make_float2(-INFINITY, 0.f);
+            float v = pk.x;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(0xFFFFFFFFu, v, off);
+                if (lane >= off) v = fmax_nan(v, o);
+            }
+            const float Mk = fmax_nan(carry, v);
+            float Mp = __shfl_up_sync(0xFFFFFFFFu, Mk, 1);
+            if (lane == 0) Mp = carry;
+            const float f = (Mp == -INFINITY) ? 0.f : ex2_approx(__fmul_rn(__fsub_rn(Mp, Mk), kLog2e));
+            const float bk =
+                (pk.x == -INFINITY) ? 0.f : __fmul_rn(pk.y, ex2_approx(__fmul_rn(__fsub_rn(pk.x, Mk), kLog2e)));
+            if (k < p.NT) x.fold[k] = make_float2(f, bk);
+            carry = __shfl_sync(0xFFFFFFFFu, Mk, 31);
         }
         __syncwarp();
-        ok = x.wt.warp_wait(x.xbar0 + 8u * buf, (uint32_t)((n >> 1) & 1), true) && ok;
-    }
-    if (!ok) return;
-    // Left fold over k = 0..NT-1.  The running maxima M_k are an exact prefix
-    // max; the rescale factors f_k = exp(M_{k-1} - M_k) and the terms
-    // b_k = s_k exp(m_k - M_k) are formed lane-parallel; the sum recurrence
-    // S_k = S_{k-1} f_k + b_k then runs in index order in one lane.
-    float carry = -INFINITY;
-    for (int c0 = 0; c0 < p.NT; c0 += 32) {
-        const int k = c0 + lane;
-        const float2 pk = k < p.NT ? part[k] : make_float2(-INFINITY, 0.f);
-        float v = pk.x;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float o = __shfl_up_sync(0xFFFFFFFFu, v, off);
-            if (lane >= off) v = fmax_nan(v, o);
-        }
-        const float Mk = fmax_nan(carry, v);
-        float Mp = __shfl_up_sync(0xFFFFFFFFu, Mk, 1);
-        if (lane == 0) Mp = carry;
-        const float f = (Mp == -INFINITY) ? 0.f : ex2_approx(__fmul_rn(__fsub_rn(Mp, Mk), kLog2e));
-        const float b = (pk.x == -INFINITY) ? 0.f : __fmul_rn(pk.y, ex2_approx(__fmul_rn(__fsub_rn(pk.x, Mk), kLog2e)));
-        if (k < p.NT) x.fold[k] = make_float2(f, b);
-        carry = __shfl_sync(0xFFFFFFFFu, Mk, 31);
-    }
-    __syncwarp();
-    float lse_v = 0.f;
-    if (lane == 0) {
-        float S = 0.f;
-        for (int k = 0; k < p.NT; ++k) {
-            const float2 fb = x.fold[k];
-            S = __fmaf_rn(S, fb.x, fb.y);
-        }
-        lse_v = (carry == -INFINITY) ? -INFINITY : __fadd_rn(carry, logf(S));
-    }
-    lse_v = __shfl_sync(0xFFFFFFFFu, lse_v, 0);
-    const int64_t row = x.q + n * x.G;
-    if (lane == 0) {
-        RowShared& rs = x.rows[buf];
-        const bool active = rs.active != 0;
-        const int64_t t = rs.target;
-        if (x.rank == 0) {
-            p.a.lse[row] = lse_v;
-            if (!active) {
-                p.a.logp[row] = 0.f;
-            } else if (t < 0 || t >= p.Vr) {
-                p.a.logp[row] = __int_as_float(0x7FC00000);
-                atomicOr(p.a.status, kStatusTargetRange);
+        float lse_v = 0.f;
+        if (lane == 0) {
+            float S = 0.f;
+#pragma unroll 8
+            for (int k = 0; k < p.NT; ++k) {
+                const float2 fb = x.fold[k];
+                S = __fmaf_rn(S, fb.x, fb.y);
             }
-            if (active && !isfinite(lse_v)) atomicOr(p.a.status, kStatusNonFinite);
+            lse_v = (carry == -INFINITY) ? -INFINITY : __fadd_rn(carry, logf(S));
         }
-        if (active && rs.has_xt) p.a.logp[row] = __fsub_rn(rs.xt, lse_v);
-        rs.has_xt = 0;
-        rs.lse = lse_v;
-    }
-    if (p.a.partials && x.rank == 0) {
-        float2* out = reinterpret_cast<float2*>(p.a.partials) + row * p.NT;
-        for (int k = lane; k < p.NT; k += 32) out[k] = part[k];
+        lse_v = __shfl_sync(0xFFFFFFFFu, lse_v, 0);
+        const int64_t row = x.q + n * x.G;
+        if (p.a.partials && x.rank == 0) {
+            float2* out = reinterpret_cast<float2*>(p.a.partials) + row * p.NT;
+            for (int k = lane; k < p.NT; k += 32) out[k] = part[k];
+        }
+        __syncwarp();
+        if (lane == 0) {
+            RowShared& rs = x.rows[b];
+            const bool active = rs.active != 0;
+            const int64_t t = rs.target;
+            if (x.rank == 0) {
+                p.a.lse[row] = lse_v;
+                if (!active) {
+                    p.a.logp[row] = 0.f;
+                } else if (t < 0 || t >= p.Vr) {
+                    p.a.logp[row] = __int_as_float(0x7FC00000);
+                    atomicOr(p.a.status, kStatusTargetRange);
+                }
+                if (active && !isfinite(lse_v)) atomicOr(p.a.status, kStatusNonFinite);
+            }
+            if (active && rs.has_xt) p.a.logp[row] = __fsub_rn(rs.xt, lse_v);
+            rs.has_xt = 0;
+            rs.lse = lse_v;
+            if (MODE == kModeFused) mbar_arrive(x.lseready0 + 8u * b);
+            mbar_arrive(x.partfree0 + 8u * b);
+        }
     }
 }
 
@@ -544,15 +580,92 @@ __device__ __forceinline__ RingPos ring_add(RingPos r, int k, int NS) {
     return RingPos{s - q * NS, r.par ^ (uint32_t)(q & 1)};
 }
 
+// Phase A of row n for one consumer warp: the partials of its chunks, the
+// row metadata (chunk 0) and the target logit (the chunk that holds it).
+// FWD releases each slot at once; FUSED keeps them for phase B.
+template <int MODE>
+__device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, RingPos rb) {
+    constexpr int W = kConsumerWarps;
+    const int lane = x.lane;
+    const int b = (int)(n % kRowBufs);
+    bool ok = true;
+    if (n >= kRowBufs) ok = x.wt.warp_wait(x.partfree0 + 8u * b, (uint32_t)((n / kRowBufs - 1) & 1));
+    uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
+    const int slot_elems = p.slot_bytes / 2;
+    const int lfirst = (x.warp - (int)((n * x.nch) & (W - 1))) & (W - 1);
+    for (int c = lfirst; c < x.nch && ok; c += W) {
+        const RingPos ps = ring_add(rb, c, p.NS);
+        const int slot = ps.slot;
+        if (!x.wt.warp_wait(x.full0 + 8u * slot, ps.par)) {
+            ok = false;
+            break;
+        }
+        const SlotHdr h = x.hdr[slot];
+        const int kf = x.k0 + c * p.tps, kl = min(kf + p.tps, x.k0 + x.ntl);
+        const Span sp = chunk_span(kf, kl, p);
+        const uint16_t* grow = p.a.logits + h.row * p.stride;
+        if (c == 0 && lane == 0) {
+            RowShared& rs = x.rows[b];
+            rs.target = h.target;
+            rs.active = h.active;
+            rs.g = h.g;
+        }
+        for (int k = kf; k < kl; ++k) {
+            const TileGeom tg = tile_geom(k, p, sp);
+            const uint16_t* sl = slots + (size_t)slot * slot_elems + (tg.a - sp.a);
+            const float2 pr = tile_partial(sl, grow, tg, p.Vr, lane);
+            if (lane == 0) {
+                x.part[(size_t)b * p.NT + k] = pr;
+                if (h.active && h.target >= tg.ts && h.target < tg.hi) {
+                    const uint16_t bits = (h.target < tg.b) ? sl[h.target - tg.a] : ldg_bf16(grow + h.target);
+                    RowShared& rs = x.rows[b];
+                    rs.xt = __uint_as_float((uint32_t)bits << 16);
+                    rs.has_xt = 1;
+                }
+            }
+        }
+        if (MODE == kModeFwd) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(x.empty0 + 8u * slot);
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(x.rowdone0 + 8u * b);
+    return ok;
+}
+
+// Phase B of row n (FUSED) for one consumer warp: dlogits of its chunks from
+// the resident slots, then release them.
+__device__ void phase_b(const Params& p, const Ctx& x, int64_t n, RingPos rb, float lse_v) {
+    constexpr int W = kConsumerWarps;
+    const int lane = x.lane;
+    uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
+    const int slot_elems = p.slot_bytes / 2;
+    const int lfirst = (x.warp - (int)((n * x.nch) & (W - 1))) & (W - 1);
+    for (int c = lfirst; c < x.nch; c += W) {
+        const int slot = ring_add(rb, c, p.NS).slot;
+        const SlotHdr h = x.hdr[slot];
+        const int kf = x.k0 + c * p.tps, kl = min(kf + p.tps, x.k0 + x.ntl);
+        const Span sp = chunk_span(kf, kl, p);
+        for (int k = kf; k < kl; ++k) {
+            const TileGeom tg = tile_geom(k, p, sp);
+            tile_grad(slots + (size_t)slot * slot_elems + (tg.a - sp.a), p.a.logits + h.row * p.stride,
+                      p.a.dlogits + h.row * p.stride, tg, p.Vr, h.active != 0, h.target, h.g, lse_v, lane);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(x.empty0 + 8u * slot);
+    }
+}
+
 template <int MODE>
 __device__ void consumer(const Params& p, const Ctx& x) {
     constexpr int W = kConsumerWarps;
     static_assert((W & (W - 1)) == 0, "consumer warp count must be a power of two");
     const int lane = x.lane;
-    uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
-    const int slot_elems = p.slot_bytes / 2;
     if constexpr (MODE == kModeBwd) {
         // Items (row, chunk) in order; warp w takes items w, w+W, ...
+        uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
+        const int slot_elems = p.slot_bytes / 2;
         const int64_t total = x.nrows * x.nch;
         RingPos pos = ring_add(RingPos{0, 0u}, x.warp, p.NS);
         int c = x.warp % x.nch;
@@ -578,76 +691,28 @@ __device__ void consumer(const Params& p, const Ctx& x) {
             __syncwarp();
             if (lane == 0) mbar_arrive(x.empty0 + 8u * slot);
         }
-    } else {
-        // Row n's chunks are items n*nch + c; warp w takes the chunks with
-        // (n*nch + c) mod W == w.
+    } else if constexpr (MODE == kModeFwd) {
         RingPos base{0, 0u};
         for (int64_t n = 0; n < x.nrows; ++n) {
-            const RingPos rb = base;
+            phase_a<MODE>(p, x, n, base);
             base = ring_add(base, x.nch, p.NS);
-            const int buf = (int)(n & 1);
-            const int lfirst = (x.warp - (int)((n * x.nch) & (W - 1))) & (W - 1);
-            bool row_ok = true;  // every phase-A wait of this warp in this row succeeded
-            for (int c = lfirst; c < x.nch; c += W) {
-                const RingPos ps = ring_add(rb, c, p.NS);
-                const int slot = ps.slot;
-                if (!x.wt.warp_wait(x.full0 + 8u * slot, ps.par)) {
-                    row_ok = false;
-                    continue;
-                }
-                const SlotHdr h = x.hdr[slot];
-                const int kf = x.k0 + c * p.tps, kl = min(kf + p.tps, x.k0 + x.ntl);
-                const Span sp = chunk_span(kf, kl, p);
-                const uint16_t* grow = p.a.logits + h.row * p.stride;
-                if (c == 0 && lane == 0) {
-                    RowShared& rs = x.rows[buf];
-                    rs.target = h.target;
-                    rs.active = h.active;
-                    rs.g = h.g;
-                }
-                for (int k = kf; k < kl; ++k) {
-                    const TileGeom tg = tile_geom(k, p, sp);
-                    const uint16_t* sl = slots + (size_t)slot * slot_elems + (tg.a - sp.a);
-                    const float2 pr = tile_partial(sl, grow, tg, p.Vr, lane);
-                    if (lane == 0) {
-                        x.part[(size_t)buf * p.NT + k] = pr;
-                        if (h.active && h.target >= tg.ts && h.target < tg.hi) {
-                            const uint16_t bits =
-                                (h.target < tg.b) ? sl[h.target - tg.a] : ldg_bf16(grow + h.target);
-                            RowShared& rs = x.rows[buf];
-                            rs.xt = __uint_as_float((uint32_t)bits << 16);
-                            rs.has_xt = 1;
-                        }
-                    }
-                }
-                if (MODE == kModeFwd) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(x.empty0 + 8u * slot);
-                }
-            }
-            named_bar_sync(1, W * 32);
-            if (x.warp == 0) fold_row<MODE>(p, x, n);
-            if (MODE == kModeFused) {
-                named_bar_sync(2, W * 32);
-                // After an expired wait the slot headers may be stale: skip the
-                // writes (the status word already says RLK_ERR_TIMEOUT).
-                if (!row_ok || *x.wt.abort_flag) continue;
-                const float lse_v = x.rows[buf].lse;
-                for (int c = lfirst; c < x.nch; c += W) {
-                    const int slot = ring_add(rb, c, p.NS).slot;
-                    const SlotHdr h = x.hdr[slot];
-                    const int kf = x.k0 + c * p.tps, kl = min(kf + p.tps, x.k0 + x.ntl);
-                    const Span sp = chunk_span(kf, kl, p);
-                    for (int k = kf; k < kl; ++k) {
-                        const TileGeom tg = tile_geom(k, p, sp);
-                        tile_grad(slots + (size_t)slot * slot_elems + (tg.a - sp.a), p.a.logits + h.row * p.stride,
-                                  p.a.dlogits + h.row * p.stride, tg, p.Vr, h.active != 0, h.target, h.g, lse_v,
-                                  lane);
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(x.empty0 + 8u * slot);
-                }
-            }
+        }
+    } else {
+        // Skewed order A(0), A(1), B(0), A(2), B(1), ...: the fold of row n
+        // overlaps phase A of row n+1.  Two rows of slots are resident.
+        RingPos base{0, 0u};
+        bool ok_cur = x.nrows > 0 ? phase_a<MODE>(p, x, 0, base) : true;
+        for (int64_t n = 0; n < x.nrows; ++n) {
+            const RingPos next = ring_add(base, x.nch, p.NS);
+            bool ok_next = true;
+            if (n + 1 < x.nrows) ok_next = phase_a<MODE>(p, x, n + 1, next);
+            const int b = (int)(n % kRowBufs);
+            const bool ready = x.wt.warp_wait(x.lseready0 + 8u * b, (uint32_t)((n / kRowBufs) & 1));
+            // After an expired wait the slot headers may be stale: skip the
+            // writes (the status word already says RLK_ERR_TIMEOUT).
+            if (ready && ok_cur && !*x.wt.abort_flag) phase_b(p, x, n, base, x.rows[b].lse);
+            base = next;
+            ok_cur = ok_next;
         }
     }
 }
@@ -669,7 +734,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     x.sbase = smem_u32(smem);
     x.full0 = x.sbase + p.off_full;
     x.empty0 = x.sbase + p.off_empty;
-    x.xbar0 = x.sbase + p.off_xbar;
+    x.rowdone0 = x.sbase + p.off_bars;
+    x.lseready0 = x.rowdone0 + 8u * kRowBufs;
+    x.partfree0 = x.lseready0 + 8u * kRowBufs;
+    x.xbar0 = x.partfree0 + 8u * kRowBufs;
     x.hdr = reinterpret_cast<SlotHdr*>(smem + p.off_hdr);
     x.part = reinterpret_cast<float2*>(smem + p.off_part);
     x.fold = reinterpret_cast<float2*>(smem + p.off_fold);
@@ -684,19 +752,25 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
             mbar_init(x.full0 + 8u * s, 1);
             mbar_init(x.empty0 + 8u * s, 1);
         }
-        if (p.C > 1) {
-            mbar_init(x.xbar0, (uint32_t)(p.C - 1));
-            mbar_init(x.xbar0 + 8u, (uint32_t)(p.C - 1));
+        for (int b = 0; b < kRowBufs; ++b) {
+            mbar_init(x.rowdone0 + 8u * b, kConsumerWarps);
+            mbar_init(x.lseready0 + 8u * b, 1);
+            mbar_init(x.partfree0 + 8u * b, 1);
+            mbar_init(x.xbar0 + 8u * b, (uint32_t)(p.C > 1 ? p.C - 1 : 1));
+            x.rows[b].has_xt = 0;
         }
         *abort_flag = 0;
-        x.rows[0].has_xt = 0;
-        x.rows[1].has_xt = 0;
         fence_mbar_init();
     }
     if (p.C > 1) cluster_sync_all(); else __syncthreads();
 
-    if (x.warp == kConsumerWarps) producer<MODE>(p, x);
-    else consumer<MODE>(p, x);
+    if (x.warp == kProducerWarp) {
+        producer<MODE>(p, x);
+    } else if (x.warp == kFoldWarp) {
+        if (MODE != kModeBwd) fold_warp<MODE>(p, x);
+    } else {
+        consumer<MODE>(p, x);
+    }
 
     __syncthreads();
     if (p.C > 1) cluster_sync_all();  // no CTA leaves while a peer may still write into it
@@ -754,13 +828,13 @@ uint32_t layout(Params& p, int NS) {
     p.off_hdr = align_up(off, 16);
     off = p.off_hdr + (uint32_t)sizeof(SlotHdr) * NS;
     p.off_part = align_up(off, 16);
-    off = p.off_part + 2u * 8u * (uint32_t)p.NT;
+    off = p.off_part + (uint32_t)kRowBufs * 8u * (uint32_t)p.NT;
     p.off_fold = off;
     off += 8u * (uint32_t)p.NT;
     p.off_rows = align_up(off, 16);
-    off = p.off_rows + 2u * (uint32_t)sizeof(RowShared);
-    p.off_xbar = align_up(off, 8);
-    off = p.off_xbar + 16u;
+    off = p.off_rows + (uint32_t)kRowBufs * (uint32_t)sizeof(RowShared);
+    p.off_bars = align_up(off, 8);
+    off = p.off_bars + 4u * 8u * (uint32_t)kRowBufs;  // rowdone, lseready, partfree, xbar
     p.off_flag = off;
     off += 16u;
     return align_up(off, 128);
@@ -818,8 +892,9 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         for (;;) {
             p.C = C;
             NS = max_slots(p);
+            // The skewed fused order keeps two rows of this CTA's chunks resident.
             const int ntl_max = (c.num_tiles + C - 1) / C;
-            if (NS >= (ntl_max + p.tps - 1) / p.tps) break;
+            if (NS >= 2 * ((ntl_max + p.tps - 1) / p.tps)) break;
             C *= 2;
             if (C > 8 || C > c.num_tiles)
                 return fail(RLK_ERR_UNSUPPORTED,
