@@ -153,6 +153,32 @@ rlk_status rlk_logp_bwd(const rlk_logp_contract* contract, const void* logits_bf
                         float* logp_out, float* lse_out, void* workspace, rlk_stream_t stream);
 
 /*
+ * rlk_logp_fwd without a workspace argument, for callers that cannot
+ * allocate device memory while they run: an engine or server whose device
+ * memory is reserved up front, a plugin that is handed a stream but no
+ * allocator, or a step that must not call the synchronising cudaMalloc.
+ * (The pages have no counterpart; this entry point only changes where the
+ * scratch lives.)
+ *
+ * Arguments and results are those of rlk_logp_fwd.  The forward's scratch --
+ * the status word, at most 256 bytes -- lives in a static device array that
+ * every GPU which loads the library holds until the process exits; a contract
+ * that would need more returns RLK_ERR_UNSUPPORTED.  The call allocates no
+ * device memory and calls no allocating routine.  The first call on a device
+ * looks up the array's device address with that device current (one
+ * cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call on a device shares the one array and clears the status word
+ * first, so calls that overlap on the GPU race on it: serialise them (one
+ * stream, or events).  Device-side conditions (RLK_ERR_TARGET_RANGE,
+ * RLK_ERR_NONFINITE_LSE, RLK_ERR_TIMEOUT) are returned only with
+ * validate == 1; with validate == 0 the call is asynchronous and they are
+ * not reported (an out-of-range active target still yields logp = NaN).
+ */
+rlk_status rlk_logp_fwd_noalloc(const rlk_logp_contract* contract, const void* logits_bf16,
+                                const int64_t* targets, const uint8_t* active_mask, float* logp,
+                                float* lse, float* partials, rlk_stream_t stream);
+
+/*
  * Synchronises `stream` and decodes the status word a previous asynchronous
  * call left in `workspace` (RLK_OK when no device-side error was recorded).
  */

@@ -30,6 +30,7 @@ EXPORTED = (
     "rlk_logp_workspace_size",
     "rlk_logp_fwd",
     "rlk_logp_bwd",
+    "rlk_logp_fwd_noalloc",
     "rlk_logp_workspace_status",
     "rlk_selftest_bounded_wait",
     "rlk_status_string",
@@ -89,6 +90,8 @@ def library():
         lib.rlk_logp_fwd.restype = i
         lib.rlk_logp_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.rlk_logp_bwd.restype = i
+        lib.rlk_logp_fwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp]
+        lib.rlk_logp_fwd_noalloc.restype = i
         lib.rlk_logp_workspace_status.argtypes = [vp, vp]
         lib.rlk_logp_workspace_status.restype = i
         lib.rlk_selftest_bounded_wait.argtypes = [ctypes.c_int64, vp, vp]
@@ -120,6 +123,11 @@ def rlk_logp_bwd(contract, logits, targets, active_mask, lse_in, grad_logp, dlog
                  workspace, stream):
     return library().rlk_logp_bwd(ctypes.byref(contract), logits, targets, active_mask, lse_in, grad_logp,
                                   dlogits, logp_out, lse_out, workspace, stream)
+
+
+def rlk_logp_fwd_noalloc(contract, logits, targets, active_mask, logp, lse, partials, stream):
+    return library().rlk_logp_fwd_noalloc(ctypes.byref(contract), logits, targets, active_mask, logp, lse,
+                                          partials, stream)
 
 
 def rlk_logp_workspace_status(workspace, stream):

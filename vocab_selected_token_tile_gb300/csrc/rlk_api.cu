@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <string>
 
 #include "rlk_internal.h"
@@ -171,6 +172,75 @@ RLK_EXPORT rlk_status rlk_logp_bwd(const rlk_logp_contract* c, const void* logit
     a.status = static_cast<uint32_t*>(workspace);
     if ((s = launch_stream(*c, lse_in ? kModeBwd : kModeFused, a, st)) != RLK_OK) return s;
     return c->validate ? read_status(workspace, st) : RLK_OK;
+}
+
+// ---------------------------------------------------------------- allocation-free forward
+//
+// rlk_logp_fwd_noalloc serves callers that may not allocate device memory
+// while they run -- an engine whose memory is reserved up front, a plugin
+// that is handed a stream but no allocator, a step that must not call the
+// synchronising cudaMalloc.  The forward's only scratch (the 256-byte status
+// word area that rlk_logp_fwd takes as `workspace`) lives in this file-scope
+// array instead; every GPU that loads the library holds it until exit.
+
+namespace rlk {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 256;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current.  In host code the array's name is only a host-side stand-in.
+rlk_status noalloc_scratch(void** out) {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(RLK_ERR_UNSUPPORTED, "device ordinal above 63");
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(RLK_ERR_CUDA, std::string("cudaGetSymbolAddress of the static scratch: ") +
+                                          cudaGetErrorString(e));
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return RLK_OK;
+}
+
+}  // namespace
+}  // namespace rlk
+
+RLK_EXPORT rlk_status rlk_logp_fwd_noalloc(const rlk_logp_contract* c, const void* logits_bf16,
+                                           const int64_t* targets, const uint8_t* active_mask, float* logp,
+                                           float* lse, float* partials, rlk_stream_t stream) {
+    rlk_status s = check_contract(c);
+    if (s != RLK_OK) return s;
+    if (c->T == 0) return RLK_OK;
+    if (kWorkspaceBytes > kNoAllocScratchBytes)
+        return fail(RLK_ERR_UNSUPPORTED, "this contract needs more scratch than the 256-byte static array; "
+                                         "use rlk_logp_fwd with a workspace");
+    if (!logits_bf16) return fail(RLK_ERR_INVALID_ARG, "logits is NULL");
+    if ((s = select_device(logits_bf16)) != RLK_OK) return s;
+    void* scratch = nullptr;
+    if ((s = noalloc_scratch(&scratch)) != RLK_OK) return s;
+    if ((s = check_common(c, logits_bf16, targets, active_mask, scratch)) != RLK_OK) return s;
+    if (!logp || !lse) return fail(RLK_ERR_INVALID_ARG, "logp and lse outputs are required");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = begin(scratch, st)) != RLK_OK) return s;  // the status word starts at zero on every call
+    StreamArgs a{};
+    a.logits = static_cast<const uint16_t*>(logits_bf16);
+    a.targets = targets;
+    a.mask = active_mask;
+    a.logp = logp;
+    a.lse = lse;
+    a.partials = partials;
+    a.status = static_cast<uint32_t*>(scratch);
+    if ((s = launch_stream(*c, kModeFwd, a, st)) != RLK_OK) return s;
+    return c->validate ? read_status(scratch, st) : RLK_OK;
 }
 
 RLK_EXPORT rlk_status rlk_logp_workspace_status(const void* workspace, rlk_stream_t stream) {
