@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--extra", action="store_true", help="also time the forward-only and split paths")
     ap.add_argument("--rows", type=int, default=0,
                     help="profiling only: shrink the batch to this many rows (not a bench number)")
+    ap.add_argument("--path", default="fused", choices=["fused", "fwd", "split"],
+                    help="profiling only: time the forward kernel or the split path instead of the fused step")
     return ap.parse_args()
 
 
@@ -198,9 +200,17 @@ def run_ours(args, ws, rank, local):
     ws_buf = rlk.workspace_for(c, dev, stream)
 
     def step():
-        rlk.check(rlk.rlk_logp_bwd(c, logits.data_ptr(), targets.data_ptr(), dmask.data_ptr(), None,
-                                   dg.data_ptr(), dlogits.data_ptr(), logp.data_ptr(), lse.data_ptr(),
-                                   ws_buf.data_ptr(), stream.cuda_stream))
+        if args.path in ("fwd", "split"):
+            rlk.check(rlk.rlk_logp_fwd(c, logits.data_ptr(), targets.data_ptr(), dmask.data_ptr(), logp.data_ptr(),
+                                       lse.data_ptr(), None, ws_buf.data_ptr(), stream.cuda_stream))
+        if args.path == "split":
+            rlk.check(rlk.rlk_logp_bwd(c, logits.data_ptr(), targets.data_ptr(), dmask.data_ptr(), lse.data_ptr(),
+                                       dg.data_ptr(), dlogits.data_ptr(), None, None, ws_buf.data_ptr(),
+                                       stream.cuda_stream))
+        if args.path == "fused":
+            rlk.check(rlk.rlk_logp_bwd(c, logits.data_ptr(), targets.data_ptr(), dmask.data_ptr(), None,
+                                       dg.data_ptr(), dlogits.data_ptr(), logp.data_ptr(), lse.data_ptr(),
+                                       ws_buf.data_ptr(), stream.cuda_stream))
 
     for _ in range(args.warmup):
         step()
@@ -252,8 +262,8 @@ def run_ours(args, ws, rank, local):
         "dtype": "bf16",
         "data": "synthetic (seeded counter-based generator; no dataset)",
         "config": {
-            "workload": "grpo: fused fwd+bwd, T=65536 (32x2048) x V_padded=152576 (V_real=151936), 64 tiles, "
-                        f"virtual TP {args.vtp}, g = A_b*mask/active_count",
+            "workload": f"{w.name}: {args.path} fwd+bwd, T={T} ({w.batch}x{w.seq}) x V_padded={Vp} (V_real={Vr}), "
+                        f"64 tiles, virtual TP {args.vtp}, g = A_b*mask/active_count",
             "active_tokens": int(active.sum()),
             "parallelism": f"dp{ws} (independent rows, no collective)" if ws > 1 else "single GPU",
             "l2": "inputs (20.0 GB logits) larger than L2; no flush",

@@ -1,0 +1,204 @@
+"""A host-side model of the streaming kernel's slot-ring protocol.
+
+Agents per CTA: one producer (issues bulk copies into a ring of NS slots),
+one fold warp, W consumer warps; C CTAs per cluster exchange tile partials.
+mbarriers follow the PTX rules: a phase completes when its pending arrival
+count reaches zero and its expected bytes have landed; a parity wait succeeds
+when the given parity is that of the phase before the current one (so a wait
+two phases ahead succeeds wrongly).  The model drives every agent with random
+speeds and random copy latencies and asserts that each read of a slot sees
+the item it expects and that nothing deadlocks.
+
+It mirrors the kernel's waits: full/empty per slot, rowdone/lseready/
+partfree/xbar per row buffer, and the per-slot issued-item number (`seq`)
+that consumers wait for before the full-barrier parity.
+"""
+import random
+
+
+class Bar:
+    def __init__(self, count):
+        self.count = count
+        self.pending = count
+        self.phase = 0
+        self.tx = 0
+
+    def arrive(self, n=1):
+        self.pending -= n
+        assert self.pending >= 0, "more arrivals than the phase expects"
+        self.check()
+
+    def check(self):
+        if self.pending == 0 and self.tx == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def try_wait(self, par):
+        return par != (self.phase & 1)
+
+
+class ProtocolError(AssertionError):
+    pass
+
+
+def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80):
+    """mode: 'fwd' | 'bwd' | 'fused'.  Raises ProtocolError on a stale read or a deadlock."""
+    rng = random.Random(seed)
+    ntl = NT // C
+    nch = (ntl + tps - 1) // tps
+    R = 2
+
+    class CTA:
+        pass
+
+    ctas = []
+    for r in range(C):
+        c = CTA()
+        c.rank = r
+        c.full = [Bar(1) for _ in range(NS)]
+        c.empty = [Bar(tps) for _ in range(NS)]
+        c.hdr = [None] * NS
+        c.seq = [None] * NS
+        c.data = [None] * NS
+        c.inflight = []
+        c.rowdone = [Bar(W) for _ in range(R)]
+        c.lseready = [Bar(1) for _ in range(R)]
+        c.partfree = [Bar(1) for _ in range(R)]
+        c.xbar = [Bar(max(C - 1, 1)) for _ in range(R)]
+        c.part = [[None] * NT for _ in range(R)]
+        ctas.append(c)
+
+    def ring(i):
+        return i % NS, (i // NS) & 1
+
+    def chunk_of(l):
+        ch = l // tps
+        kf = ch * tps
+        kl = min(kf + tps, ntl)
+        return ch, (1 + tps - (kl - kf)) if l == kl - 1 else 1
+
+    def wait(bar, par):
+        while not bar.try_wait(par):
+            yield "wait"
+
+    def wait_item(c, s, par, i):
+        if seqcheck:
+            while c.seq[s] != i:
+                yield "wait"
+        yield from wait(c.full[s], par)
+
+    def check_slot(c, s, i, where):
+        if c.hdr[s] != i or c.data[s] != i:
+            raise ProtocolError(f"{mode} {where}: slot {s} holds item {c.hdr[s]}/{c.data[s]}, expected {i}")
+
+    def producer(c):
+        i = 0
+        for _ in range(rows):
+            for _ in range(nch):
+                s, par = ring(i)
+                yield from wait(c.empty[s], par ^ 1)
+                c.hdr[s] = i
+                c.seq[s] = i
+                c.data[s] = None
+                c.full[s].tx += 1
+                c.full[s].arrive()
+                c.inflight.append([rng.randint(1, max_delay), s, i])
+                i += 1
+                yield "issue"
+
+    def tiles_of(w, n):
+        return range((w - n * ntl) % W, ntl, W)
+
+    def phase_a(c, w, n):
+        b = n % R
+        if n >= R:
+            yield from wait(c.partfree[b], (n // R - 1) & 1)
+        for l in tiles_of(w, n):
+            ch, share = chunk_of(l)
+            i = n * nch + ch
+            s, par = ring(i)
+            yield from wait_item(c, s, par, i)
+            check_slot(c, s, i, "phase A")
+            c.part[b][c.rank * ntl + l] = n
+            yield "tile"
+            if mode == "fwd":
+                c.empty[s].arrive(share)
+        c.rowdone[b].arrive()
+
+    def phase_b(c, w, n):
+        for l in tiles_of(w, n):
+            ch, share = chunk_of(l)
+            i = n * nch + ch
+            s, par = ring(i)
+            if mode == "bwd":
+                yield from wait_item(c, s, par, i)
+            check_slot(c, s, i, "phase B")
+            yield "grad"
+            c.empty[s].arrive(share)
+
+    def consumer(c, w):
+        if mode == "bwd":
+            for n in range(rows):
+                yield from phase_b(c, w, n)
+        elif mode == "fwd":
+            for n in range(rows):
+                yield from phase_a(c, w, n)
+        else:
+            yield from phase_a(c, w, 0)
+            for n in range(rows):
+                if n + 1 < rows:
+                    yield from phase_a(c, w, n + 1)
+                yield from wait(c.lseready[n % R], (n // R) & 1)
+                yield from phase_b(c, w, n)
+
+    def fold(c):
+        for n in range(rows):
+            b, par = n % R, (n // R) & 1
+            yield from wait(c.rowdone[b], par)
+            if C > 1:
+                for peer in ctas:
+                    if peer is not c:
+                        for k in range(c.rank * ntl, (c.rank + 1) * ntl):
+                            peer.part[b][k] = c.part[b][k]
+                        peer.xbar[b].arrive()
+                yield "push"
+                yield from wait(c.xbar[b], par)
+            if any(v != n for v in c.part[b]):
+                raise ProtocolError(f"{mode} fold of row {n} saw partials of rows {sorted(set(c.part[b]))}")
+            yield "fold"
+            if mode == "fused":
+                c.lseready[b].arrive()
+            c.partfree[b].arrive()
+
+    agents = []
+    for c in ctas:
+        agents.append(producer(c))
+        if mode != "bwd":
+            agents.append(fold(c))
+        agents.extend(consumer(c, w) for w in range(W))
+    speed = {id(a): rng.choice([0.02, 0.1, 0.5, 1.0]) for a in agents}
+    live = list(agents)
+    idle = 0
+    while live:
+        progressed = False
+        for c in ctas:
+            for f in c.inflight:
+                f[0] -= 1
+            for f in [f for f in c.inflight if f[0] <= 0]:
+                c.inflight.remove(f)
+                c.data[f[1]] = f[2]
+                c.full[f[1]].tx -= 1
+                c.full[f[1]].check()
+                progressed = True
+        picked = [a for a in live if rng.random() < speed[id(a)]] or [rng.choice(live)]
+        rng.shuffle(picked)
+        for a in picked:
+            try:
+                if next(a) != "wait":
+                    progressed = True
+            except StopIteration:
+                live.remove(a)
+                progressed = True
+        idle = 0 if progressed else idle + 1
+        if idle > 5000:
+            raise ProtocolError(f"{mode}: deadlock with {len(live)} agents waiting")

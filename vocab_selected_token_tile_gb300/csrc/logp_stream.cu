@@ -85,7 +85,7 @@ struct Params {
     uint64_t wait_ns;
     int32_t NT, W, C, mask_mode, NS, slot_bytes;
     int32_t tps;  // tiles per ring slot (consecutive tiles of one row share a slot when narrow)
-    uint32_t off_full, off_empty, off_hdr, off_part, off_fold, off_rows, off_bars, off_flag;
+    uint32_t off_full, off_empty, off_hdr, off_seq, off_part, off_fold, off_rows, off_bars, off_flag;
 };
 
 struct TileGeom {
@@ -135,6 +135,21 @@ struct Waiter {
         const uint64_t t0 = globaltimer_ns();
         for (;;) {
             if (poll()) return true;
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > limit_ns) {
+                *abort_flag = 1;
+                atomicOr(status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+    // Bounded wait until a shared-memory word equals `want`.
+    __device__ bool wait_value(const volatile uint32_t* addr, uint32_t want) const {
+        if (*addr == want) return true;
+        if (*abort_flag) return false;
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+            if (*addr == want) return true;
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
@@ -386,6 +401,11 @@ struct Ctx {
     // partials arrived)
     uint32_t rowdone0, lseready0, partfree0, xbar0;
     SlotHdr* hdr;
+    // seq[s]: number of the item the producer last issued into slot s.  A
+    // consumer waits for its own item number before the slot's full-barrier
+    // parity, so it never waits more than one phase ahead (a parity wait two
+    // phases ahead would report a completion that has not happened).
+    volatile uint32_t* seq;
     float2* part;
     float2* fold;
     RowShared* rows;
@@ -444,6 +464,7 @@ __device__ void producer(const Params& p, const Ctx& x) {
                 h.pad = 0;
                 h.row = row;
                 x.hdr[slot] = h;
+                x.seq[slot] = (uint32_t)issued;
                 const int kf = x.k0 + c * p.tps;
                 const int kl = min(kf + p.tps, x.k0 + x.ntl);
                 const Span sp = chunk_span(kf, kl, p);
@@ -580,9 +601,49 @@ __device__ __forceinline__ RingPos ring_add(RingPos r, int k, int NS) {
     return RingPos{s - q * NS, r.par ^ (uint32_t)(q & 1)};
 }
 
-// Phase A of row n for one consumer warp: the partials of its chunks, the
-// row metadata (chunk 0) and the target logit (the chunk that holds it).
-// FWD releases each slot at once; FUSED keeps them for phase B.
+// Work is per tile, copies are per chunk of tps tiles: consumer warp w
+// takes the tiles l of row n with (n*ntl + l) mod W == w, waits on the full
+// barrier of the tile's chunk, and releases its share of the chunk's slot
+// when done.  A slot's empty barrier expects tps arrivals; the last tile of
+// a short (end-of-row) chunk arrives for the missing tiles too.
+struct TileItem {
+    int slot;
+    uint32_t par;
+    int kf, kl;      // tiles [kf, kl) of the chunk
+    uint32_t share;  // arrivals this tile owes the slot's empty barrier
+};
+
+__device__ __forceinline__ TileItem tile_item(const Params& p, const Ctx& x, RingPos rb, int l) {
+    const int c = l / p.tps;
+    const RingPos ps = ring_add(rb, c, p.NS);
+    TileItem it;
+    it.slot = ps.slot;
+    it.par = ps.par;
+    it.kf = x.k0 + c * p.tps;
+    it.kl = min(it.kf + p.tps, x.k0 + x.ntl);
+    const int in_chunk = it.kl - it.kf;
+    it.share = (x.k0 + l == it.kl - 1) ? (uint32_t)(1 + p.tps - in_chunk) : 1u;
+    return it;
+}
+
+// Waits (bounded, all 32 lanes) until the tile's slot holds item `item` and
+// its bulk copy has landed.
+__device__ __forceinline__ bool wait_item(const Ctx& x, const TileItem& it, uint32_t item) {
+    const bool issued = __all_sync(0xFFFFFFFFu, x.wt.wait_value(x.seq + it.slot, item));
+    const bool landed = x.wt.warp_wait(x.full0 + 8u * it.slot, it.par);
+    if (!(issued && landed)) *x.wt.abort_flag = 1;
+    return issued && landed;
+}
+
+__device__ __forceinline__ int first_tile(const Ctx& x, int64_t n) {
+    constexpr int W = kConsumerWarps;
+    return (x.warp - (int)((n * x.ntl) & (W - 1))) & (W - 1);
+}
+
+// Phase A of row n for one consumer warp: the partials of its tiles, the
+// row metadata (tile 0) and the target logit (the tile that holds it).
+// FWD releases each tile's share of its slot at once; FUSED keeps the slots
+// for phase B.
 template <int MODE>
 __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, RingPos rb) {
     constexpr int W = kConsumerWarps;
@@ -592,41 +653,36 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, RingPos rb) {
     if (n >= kRowBufs) ok = x.wt.warp_wait(x.partfree0 + 8u * b, (uint32_t)((n / kRowBufs - 1) & 1));
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
     const int slot_elems = p.slot_bytes / 2;
-    const int lfirst = (x.warp - (int)((n * x.nch) & (W - 1))) & (W - 1);
-    for (int c = lfirst; c < x.nch && ok; c += W) {
-        const RingPos ps = ring_add(rb, c, p.NS);
-        const int slot = ps.slot;
-        if (!x.wt.warp_wait(x.full0 + 8u * slot, ps.par)) {
+    for (int l = first_tile(x, n); l < x.ntl && ok; l += W) {
+        const TileItem it = tile_item(p, x, rb, l);
+        if (!wait_item(x, it, (uint32_t)(n * x.nch + l / p.tps))) {
             ok = false;
             break;
         }
-        const SlotHdr h = x.hdr[slot];
-        const int kf = x.k0 + c * p.tps, kl = min(kf + p.tps, x.k0 + x.ntl);
-        const Span sp = chunk_span(kf, kl, p);
+        const SlotHdr h = x.hdr[it.slot];
+        const Span sp = chunk_span(it.kf, it.kl, p);
         const uint16_t* grow = p.a.logits + h.row * p.stride;
-        if (c == 0 && lane == 0) {
+        const int k = x.k0 + l;
+        const TileGeom tg = tile_geom(k, p, sp);
+        const uint16_t* sl = slots + (size_t)it.slot * slot_elems + (tg.a - sp.a);
+        const float2 pr = tile_partial(sl, grow, tg, p.Vr, lane);
+        if (lane == 0) {
             RowShared& rs = x.rows[b];
-            rs.target = h.target;
-            rs.active = h.active;
-            rs.g = h.g;
-        }
-        for (int k = kf; k < kl; ++k) {
-            const TileGeom tg = tile_geom(k, p, sp);
-            const uint16_t* sl = slots + (size_t)slot * slot_elems + (tg.a - sp.a);
-            const float2 pr = tile_partial(sl, grow, tg, p.Vr, lane);
-            if (lane == 0) {
-                x.part[(size_t)b * p.NT + k] = pr;
-                if (h.active && h.target >= tg.ts && h.target < tg.hi) {
-                    const uint16_t bits = (h.target < tg.b) ? sl[h.target - tg.a] : ldg_bf16(grow + h.target);
-                    RowShared& rs = x.rows[b];
-                    rs.xt = __uint_as_float((uint32_t)bits << 16);
-                    rs.has_xt = 1;
-                }
+            if (l == 0) {
+                rs.target = h.target;
+                rs.active = h.active;
+                rs.g = h.g;
+            }
+            x.part[(size_t)b * p.NT + k] = pr;
+            if (h.active && h.target >= tg.ts && h.target < tg.hi) {
+                const uint16_t bits = (h.target < tg.b) ? sl[h.target - tg.a] : ldg_bf16(grow + h.target);
+                rs.xt = __uint_as_float((uint32_t)bits << 16);
+                rs.has_xt = 1;
             }
         }
         if (MODE == kModeFwd) {
             __syncwarp();
-            if (lane == 0) mbar_arrive(x.empty0 + 8u * slot);
+            if (lane == 0) mbar_arrive_n(x.empty0 + 8u * it.slot, it.share);
         }
     }
     __syncwarp();
@@ -634,65 +690,46 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, RingPos rb) {
     return ok;
 }
 
-// Phase B of row n (FUSED) for one consumer warp: dlogits of its chunks from
-// the resident slots, then release them.
-__device__ void phase_b(const Params& p, const Ctx& x, int64_t n, RingPos rb, float lse_v) {
+// dlogits of row n's tiles for one consumer warp; each tile then releases its
+// share of its slot.  FUSED: the slots are still resident from phase A and
+// lse_v is the fold's LSE.  BWD: the tile waits for its chunk here and reads
+// the row's LSE (lse_in) from the slot header.
+template <int MODE>
+__device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, RingPos rb, float lse_v) {
     constexpr int W = kConsumerWarps;
     const int lane = x.lane;
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
     const int slot_elems = p.slot_bytes / 2;
-    const int lfirst = (x.warp - (int)((n * x.nch) & (W - 1))) & (W - 1);
-    for (int c = lfirst; c < x.nch; c += W) {
-        const int slot = ring_add(rb, c, p.NS).slot;
-        const SlotHdr h = x.hdr[slot];
-        const int kf = x.k0 + c * p.tps, kl = min(kf + p.tps, x.k0 + x.ntl);
-        const Span sp = chunk_span(kf, kl, p);
-        for (int k = kf; k < kl; ++k) {
-            const TileGeom tg = tile_geom(k, p, sp);
-            tile_grad(slots + (size_t)slot * slot_elems + (tg.a - sp.a), p.a.logits + h.row * p.stride,
-                      p.a.dlogits + h.row * p.stride, tg, p.Vr, h.active != 0, h.target, h.g, lse_v, lane);
+    for (int l = first_tile(x, n); l < x.ntl; l += W) {
+        const TileItem it = tile_item(p, x, rb, l);
+        if (MODE == kModeBwd && !wait_item(x, it, (uint32_t)(n * x.nch + l / p.tps))) return false;
+        const SlotHdr h = x.hdr[it.slot];
+        const Span sp = chunk_span(it.kf, it.kl, p);
+        const int k = x.k0 + l;
+        const TileGeom tg = tile_geom(k, p, sp);
+        const float lse = (MODE == kModeBwd) ? h.lse_in : lse_v;
+        if (MODE == kModeBwd && l == 0 && lane == 0 && h.active) {
+            if (h.target < 0 || h.target >= p.Vr) atomicOr(p.a.status, kStatusTargetRange);
+            if (!isfinite(h.lse_in)) atomicOr(p.a.status, kStatusNonFinite);
         }
+        tile_grad(slots + (size_t)it.slot * slot_elems + (tg.a - sp.a), p.a.logits + h.row * p.stride,
+                  p.a.dlogits + h.row * p.stride, tg, p.Vr, h.active != 0, h.target, h.g, lse, lane);
         __syncwarp();
-        if (lane == 0) mbar_arrive(x.empty0 + 8u * slot);
+        if (lane == 0) mbar_arrive_n(x.empty0 + 8u * it.slot, it.share);
     }
+    return true;
 }
 
 template <int MODE>
 __device__ void consumer(const Params& p, const Ctx& x) {
-    constexpr int W = kConsumerWarps;
-    static_assert((W & (W - 1)) == 0, "consumer warp count must be a power of two");
-    const int lane = x.lane;
+    static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0, "consumer warp count must be a power of two");
+    RingPos base{0, 0u};
     if constexpr (MODE == kModeBwd) {
-        // Items (row, chunk) in order; warp w takes items w, w+W, ...
-        uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
-        const int slot_elems = p.slot_bytes / 2;
-        const int64_t total = x.nrows * x.nch;
-        RingPos pos = ring_add(RingPos{0, 0u}, x.warp, p.NS);
-        int c = x.warp % x.nch;
-        for (int64_t i = x.warp; i < total; i += W) {
-            const int slot = pos.slot;
-            const bool ok = x.wt.warp_wait(x.full0 + 8u * slot, pos.par);
-            const int cc = c;
-            pos = ring_add(pos, W, p.NS);
-            c = (c + W) % x.nch;
-            if (!ok) continue;
-            const SlotHdr h = x.hdr[slot];
-            const int kf = x.k0 + cc * p.tps, kl = min(kf + p.tps, x.k0 + x.ntl);
-            const Span sp = chunk_span(kf, kl, p);
-            if (cc == 0 && lane == 0 && h.active) {
-                if (h.target < 0 || h.target >= p.Vr) atomicOr(p.a.status, kStatusTargetRange);
-                if (!isfinite(h.lse_in)) atomicOr(p.a.status, kStatusNonFinite);
-            }
-            for (int k = kf; k < kl; ++k) {
-                const TileGeom tg = tile_geom(k, p, sp);
-                tile_grad(slots + (size_t)slot * slot_elems + (tg.a - sp.a), p.a.logits + h.row * p.stride,
-                          p.a.dlogits + h.row * p.stride, tg, p.Vr, h.active != 0, h.target, h.g, h.lse_in, lane);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(x.empty0 + 8u * slot);
+        for (int64_t n = 0; n < x.nrows; ++n) {
+            if (!phase_b<MODE>(p, x, n, base, 0.f)) break;
+            base = ring_add(base, x.nch, p.NS);
         }
     } else if constexpr (MODE == kModeFwd) {
-        RingPos base{0, 0u};
         for (int64_t n = 0; n < x.nrows; ++n) {
             phase_a<MODE>(p, x, n, base);
             base = ring_add(base, x.nch, p.NS);
@@ -700,7 +737,6 @@ __device__ void consumer(const Params& p, const Ctx& x) {
     } else {
         // Skewed order A(0), A(1), B(0), A(2), B(1), ...: the fold of row n
         // overlaps phase A of row n+1.  Two rows of slots are resident.
-        RingPos base{0, 0u};
         bool ok_cur = x.nrows > 0 ? phase_a<MODE>(p, x, 0, base) : true;
         for (int64_t n = 0; n < x.nrows; ++n) {
             const RingPos next = ring_add(base, x.nch, p.NS);
@@ -710,7 +746,7 @@ __device__ void consumer(const Params& p, const Ctx& x) {
             const bool ready = x.wt.warp_wait(x.lseready0 + 8u * b, (uint32_t)((n / kRowBufs) & 1));
             // After an expired wait the slot headers may be stale: skip the
             // writes (the status word already says RLK_ERR_TIMEOUT).
-            if (ready && ok_cur && !*x.wt.abort_flag) phase_b(p, x, n, base, x.rows[b].lse);
+            if (ready && ok_cur && !*x.wt.abort_flag) phase_b<MODE>(p, x, n, base, x.rows[b].lse);
             base = next;
             ok_cur = ok_next;
         }
@@ -739,6 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     x.partfree0 = x.lseready0 + 8u * kRowBufs;
     x.xbar0 = x.partfree0 + 8u * kRowBufs;
     x.hdr = reinterpret_cast<SlotHdr*>(smem + p.off_hdr);
+    x.seq = reinterpret_cast<volatile uint32_t*>(smem + p.off_seq);
     x.part = reinterpret_cast<float2*>(smem + p.off_part);
     x.fold = reinterpret_cast<float2*>(smem + p.off_fold);
     x.rows = reinterpret_cast<RowShared*>(smem + p.off_rows);
@@ -750,7 +787,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.NS; ++s) {
             mbar_init(x.full0 + 8u * s, 1);
-            mbar_init(x.empty0 + 8u * s, 1);
+            mbar_init(x.empty0 + 8u * s, (uint32_t)p.tps);
+            x.seq[s] = 0xFFFFFFFFu;
         }
         for (int b = 0; b < kRowBufs; ++b) {
             mbar_init(x.rowdone0 + 8u * b, kConsumerWarps);
@@ -827,6 +865,8 @@ uint32_t layout(Params& p, int NS) {
     off += 8u * NS;
     p.off_hdr = align_up(off, 16);
     off = p.off_hdr + (uint32_t)sizeof(SlotHdr) * NS;
+    p.off_seq = off;
+    off += 4u * NS;
     p.off_part = align_up(off, 16);
     off = p.off_part + (uint32_t)kRowBufs * 8u * (uint32_t)p.NT;
     p.off_fold = off;
@@ -866,13 +906,16 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     p.NT = c.num_tiles;
     p.W = (int32_t)(c.V_padded / c.num_tiles);
     p.mask_mode = c.mask_mode;
-    // Narrow tiles share a slot: about 4096 columns per slot.
-    p.tps = p.W >= 4096 ? 1 : 4096 / p.W;
-    {
-        const int64_t cols = (int64_t)p.tps * p.W;
+    // One bulk copy per chunk of tps consecutive tiles, about 8192 columns
+    // (16 KB): a copy costs about the same issue time whatever its size, so
+    // large copies are what keeps the stream near HBM bandwidth.
+    const int tps_target = p.W >= 8192 ? 1 : 8192 / p.W;
+    auto set_chunk = [&](int tps) {
+        p.tps = tps;
+        const int64_t cols = (int64_t)tps * p.W;
         p.slot_bytes = (int32_t)align_up((uint32_t)((((cols + 7) & ~(int64_t)7) + 8) * 2), 16);
-    }
-
+    };
+    set_chunk(tps_target);
     const int ctas_per_sm = env_int("RLK_CTAS_PER_SM", 1) >= 2 ? 2 : 1;
     const uint32_t budget = (uint32_t)di.smem_optin / (uint32_t)ctas_per_sm - 1024u;
     const int cap = env_int("RLK_MAX_SLOTS", kMaxSlots);
@@ -891,9 +934,13 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     if (mode == kModeFused) {
         for (;;) {
             p.C = C;
+            // Chunks that divide the CTA's tiles evenly pack two rows without waste.
+            const int ntl_max = (c.num_tiles + C - 1) / C;
+            int tps = tps_target < ntl_max ? tps_target : ntl_max;
+            while (tps > 1 && ntl_max % tps) --tps;
+            set_chunk(tps);
             NS = max_slots(p);
             // The skewed fused order keeps two rows of this CTA's chunks resident.
-            const int ntl_max = (c.num_tiles + C - 1) / C;
             if (NS >= 2 * ((ntl_max + p.tps - 1) / p.tps)) break;
             C *= 2;
             if (C > 8 || C > c.num_tiles)
