@@ -397,7 +397,7 @@ def main():
         steps = max(1, args.steps)
         budget = max(2.0, 120.0 / (steps + args.warmup))
         for i in range(args.warmup + steps):
-            tps, rows, secs = time_oracle(W.GRPO, budget_s=budget, max_rows=256)
+            tps, rows, secs = time_oracle(W.GRPO, budget_s=budget, max_rows=4096)
             if i >= args.warmup:
                 per_step.append(tps)
             sample_desc = f"{rows} seeded rows of the grpo workload (fwd LSE/logp + dlogits), {secs:.1f} s"
@@ -422,7 +422,7 @@ def main():
     result = run_ours(args, ws, rank, local)
     if rank == 0 and not args.no_cpu:
         from synth import workloads as W
-        tps, rows, secs = time_oracle(W.GRPO, budget_s=15.0, max_rows=512)
+        tps, rows, secs = time_oracle(W.GRPO, budget_s=15.0, max_rows=8192)
         result["cpu_baseline"] = {"value": tps, "unit": UNIT, "cores": 1, "kind": "oracle",
                                   "sample": f"{rows} seeded rows of the grpo workload, FP64 numpy oracle "
                                             f"(fwd LSE/logp + dlogits), {secs:.1f} s of CPU time; "
