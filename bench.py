@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--extra", action="store_true", help="also time the forward-only and split paths")
     ap.add_argument("--rows", type=int, default=0,
                     help="profiling only: shrink the batch to this many rows (not a bench number)")
-    ap.add_argument("--path", default="fused", choices=["fused", "fwd", "split"],
+    ap.add_argument("--path", default="fused", choices=["fused", "fwd", "split", "lmhead"],
                     help="profiling only: time the forward kernel or the split path instead of the fused step")
     return ap.parse_args()
 
@@ -178,6 +178,12 @@ def run_ours(args, ws, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.path == "lmhead":
+        res = lmhead_bench(rlk, args, dev, steps=args.steps, warmup=args.warmup, rows=args.rows)
+        return {"metric": "lm_head fused forward tokens/s (profiling run)", "value": res["tokens_per_s"],
+                "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
+                "higher_is_better": True, "config": {"workload": res["workload"]}, "roofline": res["roofline"],
+                "gpu_launches": 2 * args.steps}
     w = W.GRPO
     if args.rows:
         w = w.with_(batch=max(1, args.rows // w.seq), name="grpo-profile")
@@ -290,6 +296,42 @@ def run_ours(args, ws, rank, local):
     return result
 
 
+def lmhead_bench(rlk, args, dev, steps=10, warmup=3, rows=0):
+    """The fused lm_head forward: hidden [8192, 4096] x W [152576, 4096], 64 tiles."""
+    import torch
+
+    import synth
+    from synth import workloads as W
+    w = W.LMHEAD
+    T = rows or w.T
+    H, Vr, Vp = w.hidden, w.v_real, w.v_padded
+    hd = torch.empty((T, H), dtype=torch.int16, device=dev)
+    wd = torch.empty((Vp, H), dtype=torch.int16, device=dev)
+    synth.normal_bf16_device(hd, 0, T, H, w.seed, synth.STREAM_HIDDEN, w.hidden_sigma)
+    synth.normal_bf16_device(wd, 0, Vp, H, w.seed, synth.STREAM_WEIGHT, w.weight_sigma)
+    tgt = torch.from_numpy(W.targets(w)[:T]).to(dev)
+    mask = torch.from_numpy(W.active_mask(w)[:T]).to(dev)
+    c = rlk.Contract(T=T, V_real=Vr, V_padded=Vp, num_tiles=w.num_tiles, virtual_tp=args.vtp, validate=0)
+    ws = torch.empty(rlk.rlk_logp_lmhead_workspace_size(c, H), dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        rlk.logp_fused_lmhead(c, hd, wd, tgt, mask, workspace=ws)
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        rlk.logp_fused_lmhead(c, hd, wd, tgt, mask, workspace=ws)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    flop = 2.0 * T * Vp * H
+    _, bf16_peak, kind = measured_peaks()
+    tflops = flop / (ms * 1e-3) / 1e12
+    return {"workload": f"lmhead fwd: hidden [{T},{H}] x W [{Vp},{H}] BF16, 64 tiles, virtual TP {args.vtp}",
+            "ms": ms, "tokens_per_s": T / (ms * 1e-3), "tflops": tflops,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": tflops / bf16_peak, "peak_source": f"{kind} bf16_tflops (cuBLAS burst)"}}
+
+
 def extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, Vp, args):
     import torch
     out = {}
@@ -318,6 +360,7 @@ def extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, V
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / args.steps
         out[name] = {"ms": ms, "tokens_per_s": T / ms * 1e3, "alg_gbs": T * (2 * Vr + 2 * Vp + 21) / ms / 1e6}
+    out["lmhead_fwd"] = lmhead_bench(rlk, args, logits.device)
     # split path: fwd then bwd with lse_in
     cf = c.replace(virtual_tp=1)
     for _ in range(3):

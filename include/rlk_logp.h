@@ -153,6 +153,34 @@ rlk_status rlk_logp_bwd(const rlk_logp_contract* contract, const void* logits_bf
                         float* logp_out, float* lse_out, void* workspace, rlk_stream_t stream);
 
 /*
+ * Bytes of device workspace rlk_logp_fused_lmhead needs for hidden size H
+ * (the status word, FP32 partials [T, num_tiles, 2] and target logits [T]);
+ * 0 for an unsupported contract.
+ */
+size_t rlk_logp_lmhead_workspace_size(const rlk_logp_contract* contract, int64_t H);
+
+/*
+ * Fused lm_head forward: logp and LSE of logits = hidden @ weight^T without
+ * materialising the logits (the optional fused kernel of issue #323,
+ * "Validation Boundary").  A tcgen05 GEMM (FP32 accumulators in tensor
+ * memory) feeds each (128-token block, vocabulary tile) into the tile's
+ * (max, sumexp) partial in its epilogue; the partials are folded in fixed
+ * tile order.  The logits stay FP32 (never rounded to BF16).
+ *   hidden_bf16  [T, H] BF16 row-major, 16-byte aligned; H a multiple of 64.
+ *   weight_bf16  [V_padded, H] BF16 row-major; rows >= V_real are padding.
+ *   targets, active_mask, logp, lse: as for rlk_logp_fwd.
+ *   grad_logp, dhidden_bf16, dweight_bf16: must be NULL in this build
+ *                (RLK_ERR_UNSUPPORTED otherwise).
+ *   workspace    rlk_logp_lmhead_workspace_size(contract, H) bytes.
+ * The tile width V_padded / num_tiles must be a multiple of 16.  row_stride
+ * is not used.  Outputs are bitwise identical for every virtual_tp.
+ */
+rlk_status rlk_logp_fused_lmhead(const rlk_logp_contract* contract, const void* hidden_bf16, int64_t H,
+                                 const void* weight_bf16, const int64_t* targets, const uint8_t* active_mask,
+                                 const float* grad_logp, float* logp, float* lse, void* dhidden_bf16,
+                                 void* dweight_bf16, void* workspace, rlk_stream_t stream);
+
+/*
  * rlk_logp_fwd without a workspace argument, for callers that cannot
  * allocate device memory while they run: an engine or server whose device
  * memory is reserved up front, a plugin that is handed a stream but no

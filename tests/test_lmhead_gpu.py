@@ -1,0 +1,125 @@
+"""The fused lm_head forward (tcgen05 GEMM + per-tile partials) against the FP64 oracle.
+
+logits = hidden @ W^T are never materialised on the GPU; the oracle forms
+them in FP64 from the same BF16 bits.  Tolerance: LSE and logp max abs
+<= 1e-4 (FP32 accumulation over H terms stays far inside it); masking
+bit-exact; outputs bitwise identical across virtual TP 1/2/4/8.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import vocab_selected_token_tile_gb300 as rlk
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+TOL = 1e-4
+
+
+def make(T, H, v_real, v_padded, seed, w_sigma=0.2):
+    hb = synth.normal_bf16_host(0, T, H, seed, synth.STREAM_HIDDEN, 1.0)
+    wb = synth.normal_bf16_host(0, v_padded, H, seed, synth.STREAM_WEIGHT, w_sigma)
+    rng = np.random.default_rng(seed)
+    wb[v_real:] = rng.integers(0, 1 << 16, size=(v_padded - v_real, H), dtype=np.uint16)  # padding rows: any bits
+    return hb, wb
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def run(c, hb, wb, tgt, mask):
+    return rlk.logp_fused_lmhead(c, dev(hb), dev(wb), torch.from_numpy(tgt).cuda(),
+                                 None if mask is None else torch.from_numpy(mask).cuda())
+
+
+# (T, H, V_real, V_padded, num_tiles)
+CASES = [
+    (128, 64, 256, 256, 1),        # one unit, one chunk, one K block
+    (130, 128, 600, 608, 2),       # ragged token block, 48-column remainder chunk, padded rows
+    (257, 192, 1000, 1024, 4),     # chunks of exactly 256, three token blocks
+    (64, 256, 4000, 4096, 8),      # 512-column tiles: two full chunks each
+    (96, 128, 2380, 2384 * 2, 2),  # the 2384-wide tile of the Qwen3 padded vocabulary (9 x 256 + 80)
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "T%d_H%d_V%d_P%d_NT%d" % c)
+def test_lmhead_small_cases(case):
+    T, H, v_real, v_padded, nt = case
+    hb, wb = make(T, H, v_real, v_padded, seed=T + H)
+    tgt = synth.targets(T, v_real, seed=T)
+    mask = (np.arange(T) % 7 != 3).astype(np.uint8)
+    tgt = np.where(mask != 0, tgt, -12345)  # inactive targets are never used as indices
+    ref_logp, ref_lse, _ = oracle.lmhead_forward(hb, wb, np.where(mask != 0, tgt, 0), mask != 0, v_real)
+    outs = set()
+    for vtp in (v for v in (1, 2, 4, 8) if nt % v == 0):
+        c = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=nt, virtual_tp=vtp, validate=1)
+        logp, lse = run(c, hb, wb, tgt, mask)
+        torch.cuda.synchronize()
+        lp, ls = logp.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(ls - ref_lse)) <= TOL
+        assert np.max(np.abs(lp - ref_logp)) <= TOL
+        assert np.all(lp[mask == 0] == 0.0) and not np.any(np.signbit(lp[mask == 0]))
+        outs.add((lp.tobytes(), ls.tobytes()))
+    assert len(outs) == 1, "virtual TP outputs differ"
+
+
+def test_lmhead_ignore_index_and_errors():
+    T, H, v_real, v_padded, nt = 140, 128, 600, 608, 2
+    hb, wb = make(T, H, v_real, v_padded, seed=5)
+    tgt = synth.targets(T, v_real, seed=5, ignore_frac=0.3)
+    c = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=nt, virtual_tp=2,
+                     mask_mode=rlk.MASK_IGNORE_INDEX, validate=1)
+    logp, lse = run(c, hb, wb, tgt, None)
+    active = tgt != -100
+    ref_logp, ref_lse, _ = oracle.lmhead_forward(hb, wb, np.where(active, tgt, 0), active, v_real)
+    torch.cuda.synchronize()
+    assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= TOL
+    assert np.max(np.abs(logp.cpu().numpy() - ref_logp)) <= TOL
+    bad = tgt.copy()
+    bad[np.nonzero(active)[0][0]] = v_real + 3  # an active target in the padding
+    with pytest.raises(rlk.RlkError) as ei:
+        run(c, hb, wb, bad, None)
+    assert ei.value.status == rlk.RLK_ERR_TARGET_RANGE
+
+
+def test_lmhead_rejects_unsupported_shapes():
+    c = rlk.Contract(T=8, V_real=600, V_padded=600, num_tiles=2, virtual_tp=1)  # tile width 300
+    assert rlk.rlk_logp_lmhead_workspace_size(c, 128) == 0
+    c = rlk.Contract(T=8, V_real=608, V_padded=608, num_tiles=2, virtual_tp=1)
+    assert rlk.rlk_logp_lmhead_workspace_size(c, 100) == 0                    # H not a multiple of 64
+    assert rlk.rlk_logp_lmhead_workspace_size(c, 128) > 0
+
+
+def test_lmhead_full_shape_sampled_rows():
+    """hidden [8192, 4096] x W [152576, 4096], 64 tiles, in the bench's configuration."""
+    from synth import workloads as Wl
+    w = Wl.LMHEAD
+    T, H, v_real, v_padded = w.T, w.hidden, w.v_real, w.v_padded
+    hd = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    wd = torch.empty((v_padded, H), dtype=torch.int16, device="cuda")
+    synth.normal_bf16_device(hd, 0, T, H, w.seed, synth.STREAM_HIDDEN, w.hidden_sigma)
+    synth.normal_bf16_device(wd, 0, v_padded, H, w.seed, synth.STREAM_WEIGHT, w.weight_sigma)
+    tgt = Wl.targets(w)
+    mask = Wl.active_mask(w)
+    dt, dm = torch.from_numpy(tgt).cuda(), torch.from_numpy(mask).cuda()
+    res = {}
+    for vtp in (1, 8):
+        c = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=64, virtual_tp=vtp, validate=1)
+        res[vtp] = rlk.logp_fused_lmhead(c, hd, wd, dt, dm)
+        torch.cuda.synchronize()
+    assert torch.equal(res[1][0], res[8][0]) and torch.equal(res[1][1], res[8][1])
+    rows = np.unique(np.concatenate([[0, 127, 128, T - 1], np.random.default_rng(3).choice(T, 28, replace=False)]))
+    hb = np.concatenate([synth.normal_bf16_host(int(r), 1, H, w.seed, synth.STREAM_HIDDEN, w.hidden_sigma)
+                         for r in rows])
+    wb = synth.normal_bf16_host(0, v_padded, H, w.seed, synth.STREAM_WEIGHT, w.weight_sigma)
+    assert np.array_equal(hd[torch.from_numpy(rows).cuda()].cpu().numpy().view(np.uint16), hb)
+    ref_logp, ref_lse, _ = oracle.lmhead_forward(hb, wb, tgt[rows], mask[rows] != 0, v_real)
+    logp, lse = res[1]
+    assert np.max(np.abs(lse.cpu().numpy()[rows] - ref_lse)) <= TOL
+    assert np.max(np.abs(logp.cpu().numpy()[rows] - ref_logp)) <= TOL

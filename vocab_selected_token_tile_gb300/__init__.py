@@ -31,6 +31,8 @@ EXPORTED = (
     "rlk_logp_fwd",
     "rlk_logp_bwd",
     "rlk_logp_fwd_noalloc",
+    "rlk_logp_lmhead_workspace_size",
+    "rlk_logp_fused_lmhead",
     "rlk_logp_workspace_status",
     "rlk_selftest_bounded_wait",
     "rlk_status_string",
@@ -90,6 +92,10 @@ def library():
         lib.rlk_logp_fwd.restype = i
         lib.rlk_logp_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.rlk_logp_bwd.restype = i
+        lib.rlk_logp_lmhead_workspace_size.argtypes = [P, ctypes.c_int64]
+        lib.rlk_logp_lmhead_workspace_size.restype = ctypes.c_size_t
+        lib.rlk_logp_fused_lmhead.argtypes = [P, vp, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.rlk_logp_fused_lmhead.restype = i
         lib.rlk_logp_fwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp]
         lib.rlk_logp_fwd_noalloc.restype = i
         lib.rlk_logp_workspace_status.argtypes = [vp, vp]
@@ -123,6 +129,16 @@ def rlk_logp_bwd(contract, logits, targets, active_mask, lse_in, grad_logp, dlog
                  workspace, stream):
     return library().rlk_logp_bwd(ctypes.byref(contract), logits, targets, active_mask, lse_in, grad_logp,
                                   dlogits, logp_out, lse_out, workspace, stream)
+
+
+def rlk_logp_lmhead_workspace_size(contract, H):
+    return library().rlk_logp_lmhead_workspace_size(ctypes.byref(contract), H)
+
+
+def rlk_logp_fused_lmhead(contract, hidden, H, weight, targets, active_mask, grad_logp, logp, lse, dhidden,
+                          dweight, workspace, stream):
+    return library().rlk_logp_fused_lmhead(ctypes.byref(contract), hidden, H, weight, targets, active_mask,
+                                           grad_logp, logp, lse, dhidden, dweight, workspace, stream)
 
 
 def rlk_logp_fwd_noalloc(contract, logits, targets, active_mask, logp, lse, partials, stream):
@@ -216,3 +232,19 @@ def logp_fwd_bwd(contract, logits, targets, mask, grad, dlogits=None, stream=Non
     check(rlk_logp_bwd(contract, _ptr(logits), _ptr(targets), _ptr(mask), None, _ptr(grad), _ptr(dlogits),
                        _ptr(logp), _ptr(lse), _ptr(ws), _stream(stream)))
     return dlogits, logp, lse
+
+
+def logp_fused_lmhead(contract, hidden, weight, targets, mask=None, stream=None, workspace=None):
+    """(logp, lse) of logits = hidden @ weight^T (BF16 [T, H] and [V_padded, H] on the GPU)."""
+    import torch
+    dev = hidden.device
+    T, H = hidden.shape
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    n = rlk_logp_lmhead_workspace_size(contract, H)
+    if n == 0:
+        check(rlk_logp_check_contract(contract) or RLK_ERR_UNSUPPORTED)
+    ws = workspace if workspace is not None else torch.empty(n, dtype=torch.uint8, device=dev)
+    check(rlk_logp_fused_lmhead(contract, _ptr(hidden), H, _ptr(weight), _ptr(targets), _ptr(mask), None,
+                                _ptr(logp), _ptr(lse), None, None, _ptr(ws), _stream(stream)))
+    return logp, lse

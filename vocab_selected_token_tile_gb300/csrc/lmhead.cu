@@ -1,0 +1,466 @@
+// Fused lm_head variant (sm_103a): the selected-token log-probability of
+// logits = hidden @ W^T without materialising the logits.
+//
+// The optional fused kernel of issue #323 ("[WS2][Logprob] H100 validation
+// and reproduction guide", "Validation Boundary": "the optional PR6 fused
+// kernel") is the prior art; its design is not on the pages.  Here each
+// (128-token block, global vocabulary tile) unit runs a tcgen05 GEMM over the
+// tile's columns in chunks of up to 256 vocabulary rows (accumulators in
+// tensor memory, operands staged by TMA with the 128-byte swizzle), and the
+// epilogue turns each chunk into the running (max, sumexp) partial of the
+// tile -- the same per-tile partials as the streaming path, but of FP32
+// logits that are never rounded or written.  A fold kernel then merges the
+// tiles in fixed index order (rlk_fold.cuh) and forms logp.
+//
+// Roles (192 threads, one CTA per SM): warp 0 issues the TMA loads, warp 1
+// allocates tensor memory and issues the MMAs, warps 2-5 run the epilogue
+// (warp w reads TMEM lanes 32*(w%4)..+31, one token row per thread).
+// Virtual TP: the CTAs are split into virtual_tp groups; group j computes
+// only the tiles of vocabulary shard j.  A tile's partial is computed by one
+// thread in one fixed order (chunks, then 32-column blocks, then columns),
+// whatever the grouping, so outputs do not depend on virtual_tp.
+//
+// Every wait is bounded; on expiry the CTA records RLK_ERR_TIMEOUT, stops
+// issuing, waits (bounded) for its issued copies and MMAs, frees its tensor
+// memory and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <string>
+
+#include "rlk_fold.cuh"
+#include "rlk_internal.h"
+#include "rlk_ptx.cuh"
+
+namespace rlk {
+namespace {
+
+constexpr int kBM = 128;  // token rows per unit (TMEM lanes)
+constexpr int kBN = 256;  // vocabulary rows per chunk (accumulator columns)
+constexpr int kBK = 64;   // K per stage: 64 BF16 = one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kThreadsLm = 192;
+constexpr uint32_t kTmemCols = 512;  // two accumulators of kBN columns
+constexpr uint32_t kStageA = kBM * kBK * 2;
+constexpr uint32_t kStageB = kBN * kBK * 2;
+constexpr uint64_t kDrainNsLm = 1000000000ull;
+
+struct LmParams {
+    const int64_t* targets;
+    const uint8_t* mask;
+    float2* partials;  // [T, NT]
+    float* xt;         // [T] target logits
+    uint32_t* status;
+    int64_t T, Vr, Vp, ignore_index;
+    uint64_t wait_ns;
+    int32_t K, NT, W, vtp, nchunk, rem, mask_mode;
+    int32_t MB;  // token blocks
+};
+
+struct Bars {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_addr;
+    int abort_flag;
+};
+
+// Units of this CTA: the tiles of its virtual-TP shard times the token
+// blocks, tile-major, strided over the CTAs of its group.
+struct UnitSeq {
+    int64_t u, step, end;
+    int tile0, ntile_sh, MB;
+    __device__ void init(const LmParams& p) {
+        const int G = gridDim.x;
+        const int Gj = G / p.vtp;
+        const int j = blockIdx.x / Gj;
+        const int c = blockIdx.x % Gj;
+        ntile_sh = p.NT / p.vtp;
+        tile0 = j * ntile_sh;
+        MB = p.MB;
+        u = c;
+        step = Gj;
+        end = (int64_t)ntile_sh * MB;
+    }
+    __device__ bool next(int& tile, int& mb) {
+        if (u >= end) return false;
+        tile = tile0 + (int)(u / MB);
+        mb = (int)(u % MB);
+        u += step;
+        return true;
+    }
+};
+
+__device__ bool lm_wait(Bars* bars, uint32_t bar, uint32_t parity, const LmParams& p) {
+    if (mbar_try_wait(bar, parity)) return true;
+    volatile int* ab = &bars->abort_flag;
+    if (*ab) return false;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*ab) return false;
+        if (globaltimer_ns() - t0 > p.wait_ns) {
+            *ab = 1;
+            atomicOr(p.status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ void lm_drain_wait(uint32_t bar, uint32_t parity, const LmParams& p) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kDrainNsLm) {
+            atomicOr(p.status, kStatusTimeout);
+            return;
+        }
+    }
+}
+
+// One 32-column block of a row's logits into the running partial of its
+// tile: exact block max, rescale when it grows, then the block's sum of
+// exp(x - m) with four accumulators added in a fixed order.
+__device__ __forceinline__ void online_block(const float (&v)[32], int nv, int64_t col0, int64_t Vr, float& m_run,
+                                             float& s_run) {
+    float bm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (i < nv && col0 + i < Vr) bm = fmax_nan(bm, v[i]);
+    if (bm > m_run || bm != bm) {
+        s_run = __fmul_rn(s_run, ex2_approx(__fmul_rn(__fsub_rn(m_run, bm), kLog2e)));
+        m_run = bm;
+    }
+    if (m_run == -INFINITY) return;  // nothing finite yet: the identity
+    const float nmL = -__fmul_rn(m_run, kLog2e);
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const bool ok = i < nv && col0 + i < Vr;
+        const float e = ok ? ex2_approx(__fmaf_rn(v[i], kLog2e, nmL)) : 0.f;
+        a[i & 3] = __fadd_rn(a[i & 3], e);
+    }
+    s_run = __fadd_rn(s_run, __fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])));
+}
+
+__global__ void __launch_bounds__(kThreadsLm, 1)
+    lmhead_fwd_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
+                      const __grid_constant__ CUtensorMap tmWr, const __grid_constant__ LmParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    // 1024-byte alignment for the 128-byte-swizzled operand tiles.
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* sA = smem;
+    unsigned char* sB = smem + kStages * kStageA;
+    Bars* bars = reinterpret_cast<Bars*>(smem + kStages * (kStageA + kStageB));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KB = p.K / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&bars->full[s]), 1);
+            mbar_init(smem_u32(&bars->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bars->tfull[b]), 1);
+            mbar_init(smem_u32(&bars->tempty[b]), 4);
+        }
+        mbar_init(smem_u32(&bars->drain), 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&bars->tmem_addr), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_addr;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            UnitSeq us;
+            us.init(p);
+            int tile, mb, stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool aborted = false;
+            while (!aborted && us.next(tile, mb)) {
+                for (int ch = 0; ch < p.nchunk && !aborted; ++ch) {
+                    const bool last_rem = (ch == p.nchunk - 1) && p.rem;
+                    const int nrows = last_rem ? p.rem : kBN;
+                    const int n0 = tile * p.W + ch * kBN;
+                    for (int kb = 0; kb < KB; ++kb) {
+                        const uint32_t eb = smem_u32(&bars->empty[stage]);
+                        if (!lm_wait(bars, eb, phase ^ 1u, p)) {
+                            aborted = true;
+                            break;
+                        }
+                        const uint32_t fb = smem_u32(&bars->full[stage]);
+                        mbar_arrive_expect_tx(fb, kStageA + (uint32_t)nrows * kBK * 2);
+                        tma_load_2d(smem_u32(sA + stage * kStageA), &tmH, kb * kBK, mb * kBM, fb);
+                        tma_load_2d(smem_u32(sB + stage * kStageB), last_rem ? &tmWr : &tmW, kb * kBK, n0, fb);
+                        ++issued;
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            // Drain: every issued copy lands before this CTA may exit.
+            const int64_t first = issued > kStages ? issued - kStages : 0;
+            for (int64_t j = first; j < issued; ++j)
+                lm_drain_wait(smem_u32(&bars->full[j % kStages]), (uint32_t)((j / kStages) & 1), p);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            UnitSeq us;
+            us.init(p);
+            int tile, mb, stage = 0;
+            uint32_t phase = 0;
+            int64_t chunk = 0;
+            bool aborted = false;
+            while (!aborted && us.next(tile, mb)) {
+                for (int ch = 0; ch < p.nchunk && !aborted; ++ch, ++chunk) {
+                    const int acc = (int)(chunk & 1);
+                    const uint32_t accph = (uint32_t)((chunk >> 1) & 1);
+                    if (!lm_wait(bars, smem_u32(&bars->tempty[acc]), accph ^ 1u, p)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const bool last_rem = (ch == p.nchunk - 1) && p.rem;
+                    const uint32_t idesc = idesc_bf16_f32(kBM, last_rem ? (uint32_t)p.rem : (uint32_t)kBN);
+                    const uint32_t d = tmem + (uint32_t)(acc * kBN);
+                    for (int kb = 0; kb < KB; ++kb) {
+                        if (!lm_wait(bars, smem_u32(&bars->full[stage]), phase, p)) {
+                            aborted = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a0 = smem_u32(sA + stage * kStageA);
+                        const uint32_t b0 = smem_u32(sB + stage * kStageB);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            umma_bf16(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
+                                      (kb | kk) != 0);
+                        umma_commit(smem_u32(&bars->empty[stage]));  // frees the stage when these MMAs finish
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!aborted) umma_commit(smem_u32(&bars->tfull[acc]));
+                }
+            }
+            // Every issued MMA completes before tensor memory is freed.
+            umma_commit(smem_u32(&bars->drain));
+            lm_drain_wait(smem_u32(&bars->drain), 0u, p);
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int quarter = warp & 3;
+        const int r_in = quarter * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        UnitSeq us;
+        us.init(p);
+        int tile, mb;
+        int64_t chunk = 0;
+        bool aborted = false;
+        while (!aborted && us.next(tile, mb)) {
+            const int64_t row = (int64_t)mb * kBM + r_in;
+            const bool valid = row < p.T;
+            int64_t target = -1;
+            bool active = false;
+            if (valid) {
+                target = p.targets[row];
+                active = (p.mask_mode == RLK_MASK_EXPLICIT) ? (p.mask[row] != 0) : (target != p.ignore_index);
+            }
+            float m_run = -INFINITY, s_run = 0.f, xt = 0.f;
+            bool have_xt = false;
+            for (int ch = 0; ch < p.nchunk; ++ch, ++chunk) {
+                const int acc = (int)(chunk & 1);
+                const uint32_t accph = (uint32_t)((chunk >> 1) & 1);
+                const bool ok = lm_wait(bars, smem_u32(&bars->tfull[acc]), accph, p);
+                if (!__all_sync(0xFFFFFFFFu, ok)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const int ncols = ((ch == p.nchunk - 1) && p.rem) ? p.rem : kBN;
+                const int64_t cbase = (int64_t)tile * p.W + (int64_t)ch * kBN;
+                for (int sub = 0; sub * 32 < ncols; ++sub) {
+                    float v[32];
+                    tmem_ld32(tmem + lane_base + (uint32_t)(acc * kBN + sub * 32), v);
+                    const int nv = min(32, ncols - sub * 32);
+                    const int64_t col0 = cbase + sub * 32;
+                    online_block(v, nv, col0, p.Vr, m_run, s_run);
+                    if (active && target >= col0 && target < col0 + nv && target < p.Vr) {
+                        const int idx = (int)(target - col0);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i == idx) xt = v[i];
+                        have_xt = true;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars->tempty[acc]));
+            }
+            if (!aborted && valid) {
+                p.partials[row * p.NT + tile] = make_float2(m_run, s_run);
+                if (have_xt) p.xt[row] = xt;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// LSE and logp of each row from its tile partials (one warp per row).
+__global__ void lmhead_fold_kernel(const float2* partials, const float* xt, const int64_t* targets,
+                                   const uint8_t* mask, int mask_mode, int64_t ignore_index, int64_t T, int64_t Vr,
+                                   int NT, float* logp, float* lse, uint32_t* status) {
+    extern __shared__ float2 scratch[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    float2* sc = scratch + (size_t)warp * NT;
+    for (int64_t row = (int64_t)blockIdx.x * wpb + warp; row < T; row += (int64_t)gridDim.x * wpb) {
+        const float l = fold_tiles(partials + row * NT, NT, sc, lane);
+        if (lane == 0) {
+            const int64_t t = targets[row];
+            const bool active = (mask_mode == RLK_MASK_EXPLICIT) ? (mask[row] != 0) : (t != ignore_index);
+            lse[row] = l;
+            if (!active) {
+                logp[row] = 0.f;
+            } else if (t < 0 || t >= Vr) {
+                logp[row] = __int_as_float(0x7FC00000);
+                atomicOr(status, kStatusTargetRange);
+            } else {
+                logp[row] = __fsub_rn(xt[row], l);
+            }
+            if (active && !isfinite(l)) atomicOr(status, kStatusNonFinite);
+        }
+        __syncwarp();
+    }
+}
+
+// ----------------------------------------------------------------- host
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+    static std::mutex mu;
+    static EncodeTiled fn = nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(ptr);
+    }
+    return fn;
+}
+
+// K-major [rows, K] BF16 matrix, box {64, box_rows}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, uint32_t box_rows) {
+    EncodeTiled enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t lmhead_fwd_workspace(const rlk_logp_contract& c) {
+    return ((size_t)c.T * c.num_tiles * 8 + 255) / 256 * 256 + ((size_t)c.T * 4 + 255) / 256 * 256;
+}
+
+rlk_status lmhead_check(const rlk_logp_contract& c, int64_t H) {
+    if (H < kBK || H % kBK != 0) return fail(RLK_ERR_UNSUPPORTED, "hidden size H must be a positive multiple of 64");
+    if (H > (int64_t)1 << 20) return fail(RLK_ERR_UNSUPPORTED, "hidden size H above 2^20");
+    const int64_t W = c.V_padded / c.num_tiles;
+    if (W % 16 != 0) return fail(RLK_ERR_UNSUPPORTED, "the fused lm_head needs a tile width that is a multiple of 16");
+    if (c.T > ((int64_t)1 << 31) - kBM) return fail(RLK_ERR_UNSUPPORTED, "T above 2^31 rows for the fused lm_head");
+    return RLK_OK;
+}
+
+rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                             const int64_t* targets, const uint8_t* mask, float* logp, float* lse, void* workspace,
+                             uint32_t* status, cudaStream_t stream) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    LmParams p{};
+    p.targets = targets;
+    p.mask = mask;
+    p.status = status;
+    p.T = c.T;
+    p.Vr = c.V_real;
+    p.Vp = c.V_padded;
+    p.ignore_index = c.ignore_index;
+    p.wait_ns = c.wait_timeout_ns > 0 ? (uint64_t)c.wait_timeout_ns : kDefaultWaitNs;
+    p.K = (int32_t)H;
+    p.NT = c.num_tiles;
+    p.W = (int32_t)(c.V_padded / c.num_tiles);
+    p.vtp = c.virtual_tp;
+    p.nchunk = (p.W + kBN - 1) / kBN;
+    p.rem = p.W % kBN;
+    p.mask_mode = c.mask_mode;
+    p.MB = (int32_t)((c.T + kBM - 1) / kBM);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    p.partials = reinterpret_cast<float2*>(ws);
+    p.xt = reinterpret_cast<float*>(ws + ((size_t)c.T * c.num_tiles * 8 + 255) / 256 * 256);
+
+    CUtensorMap tmH, tmW, tmWr;
+    if (!make_map(&tmH, hidden, c.T, H, kBM) || !make_map(&tmW, weight, c.V_padded, H, kBN) ||
+        !make_map(&tmWr, weight, c.V_padded, H, p.rem ? (uint32_t)p.rem : (uint32_t)kBN))
+        return fail(RLK_ERR_CUDA, "cuTensorMapEncodeTiled failed for the hidden or weight tensor");
+
+    const size_t smem = 1024 + (size_t)kStages * (kStageA + kStageB) + sizeof(Bars);
+    cudaError_t e = cudaFuncSetAttribute(lmhead_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+    const int64_t units_per_shard = (int64_t)(c.num_tiles / c.virtual_tp) * p.MB;
+    int64_t per_group = sms / c.virtual_tp;
+    if (per_group > units_per_shard) per_group = units_per_shard;
+    if (per_group < 1) per_group = 1;
+    const int grid = (int)(per_group * c.virtual_tp);
+    lmhead_fwd_kernel<<<grid, kThreadsLm, smem, stream>>>(tmH, tmW, tmWr, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("lm_head GEMM launch: ") + cudaGetErrorString(e));
+
+    const int fold_threads = 256;
+    const size_t fold_smem = (size_t)(fold_threads / 32) * c.num_tiles * sizeof(float2);
+    e = cudaFuncSetAttribute(lmhead_fold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fold_smem);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+    int64_t fold_grid = (c.T + 7) / 8;
+    if (fold_grid > (int64_t)sms * 8) fold_grid = (int64_t)sms * 8;
+    lmhead_fold_kernel<<<(unsigned)fold_grid, fold_threads, fold_smem, stream>>>(
+        p.partials, p.xt, targets, mask, c.mask_mode, c.ignore_index, c.T, c.V_real, c.num_tiles, logp, lse, status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("lm_head fold launch: ") + cudaGetErrorString(e));
+    return RLK_OK;
+}
+
+}  // namespace rlk

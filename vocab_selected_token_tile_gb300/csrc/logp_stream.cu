@@ -44,6 +44,7 @@
 #include <mutex>
 #include <string>
 
+#include "rlk_fold.cuh"
 #include "rlk_internal.h"
 #include "rlk_ptx.cuh"
 
@@ -55,7 +56,6 @@ constexpr int kFoldWarp = kConsumerWarps;          // folds each row's partials
 constexpr int kProducerWarp = kConsumerWarps + 1;  // issues the bulk copies
 constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kMaxSlots = 96;
-constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^y = 2^(y log2 e)
 constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the final drain of own copies
 
 struct SlotHdr {  // row metadata the producer writes beside each slot
@@ -525,41 +525,7 @@ __device__ void fold_warp(const Params& p, const Ctx& x) {
             ok = x.wt.warp_wait(x.xbar0 + 8u * b, par, true) && ok;
         }
         if (!ok) continue;
-        // Left fold over k = 0..NT-1.  The running maxima M_k are an exact
-        // prefix max; the rescale factors f_k = exp(M_{k-1} - M_k) and terms
-        // b_k = s_k exp(m_k - M_k) are formed lane-parallel; the sum
-        // recurrence S_k = S_{k-1} f_k + b_k then runs in index order in one lane.
-        float carry = -INFINITY;
-        for (int c0 = 0; c0 < p.NT; c0 += 32) {
-            const int k = c0 + lane;
-            const float2 pk = k < p.NT ? part[k] : make_float2(-INFINITY, 0.f);
-            float v = pk.x;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float o = __shfl_up_sync(0xFFFFFFFFu, v, off);
-                if (lane >= off) v = fmax_nan(v, o);
-            }
-            const float Mk = fmax_nan(carry, v);
-            float Mp = __shfl_up_sync(0xFFFFFFFFu, Mk, 1);
-            if (lane == 0) Mp = carry;
-            const float f = (Mp == -INFINITY) ? 0.f : ex2_approx(__fmul_rn(__fsub_rn(Mp, Mk), kLog2e));
-            const float bk =
-                (pk.x == -INFINITY) ? 0.f : __fmul_rn(pk.y, ex2_approx(__fmul_rn(__fsub_rn(pk.x, Mk), kLog2e)));
-            if (k < p.NT) x.fold[k] = make_float2(f, bk);
-            carry = __shfl_sync(0xFFFFFFFFu, Mk, 31);
-        }
-        __syncwarp();
-        float lse_v = 0.f;
-        if (lane == 0) {
-            float S = 0.f;
-#pragma unroll 8
-            for (int k = 0; k < p.NT; ++k) {
-                const float2 fb = x.fold[k];
-                S = __fmaf_rn(S, fb.x, fb.y);
-            }
-            lse_v = (carry == -INFINITY) ? -INFINITY : __fadd_rn(carry, logf(S));
-        }
-        lse_v = __shfl_sync(0xFFFFFFFFu, lse_v, 0);
+        const float lse_v = fold_tiles(part, p.NT, x.fold, lane);
         const int64_t row = x.q + n * x.G;
         if (p.a.partials && x.rank == 0) {
             float2* out = reinterpret_cast<float2*>(p.a.partials) + row * p.NT;

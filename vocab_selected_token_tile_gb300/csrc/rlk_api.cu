@@ -174,6 +174,45 @@ RLK_EXPORT rlk_status rlk_logp_bwd(const rlk_logp_contract* c, const void* logit
     return c->validate ? read_status(workspace, st) : RLK_OK;
 }
 
+// ---------------------------------------------------------------- fused lm_head
+
+RLK_EXPORT size_t rlk_logp_lmhead_workspace_size(const rlk_logp_contract* c, int64_t H) {
+    if (check_contract(c) != RLK_OK || lmhead_check(*c, H) != RLK_OK) return 0;
+    return kWorkspaceBytes + lmhead_fwd_workspace(*c);
+}
+
+RLK_EXPORT rlk_status rlk_logp_fused_lmhead(const rlk_logp_contract* c, const void* hidden_bf16, int64_t H,
+                                            const void* weight_bf16, const int64_t* targets,
+                                            const uint8_t* active_mask, const float* grad_logp, float* logp,
+                                            float* lse, void* dhidden_bf16, void* dweight_bf16, void* workspace,
+                                            rlk_stream_t stream) {
+    rlk_status s = check_contract(c);
+    if (s != RLK_OK) return s;
+    if ((s = lmhead_check(*c, H)) != RLK_OK) return s;
+    if (c->T == 0) return RLK_OK;
+    if (!hidden_bf16 || !weight_bf16) return fail(RLK_ERR_INVALID_ARG, "hidden and weight are required");
+    if (!aligned16(hidden_bf16) || !aligned16(weight_bf16))
+        return fail(RLK_ERR_MISALIGNED, "hidden and weight must be 16-byte aligned");
+    if (!targets) return fail(RLK_ERR_INVALID_ARG, "targets is NULL");
+    if (c->mask_mode == RLK_MASK_EXPLICIT && !active_mask)
+        return fail(RLK_ERR_INVALID_ARG, "explicit mask mode needs active_mask");
+    if (c->mask_mode == RLK_MASK_IGNORE_INDEX && active_mask)
+        return fail(RLK_ERR_INVALID_ARG, "ignore_index mode takes no active_mask (pass NULL)");
+    if (!logp || !lse) return fail(RLK_ERR_INVALID_ARG, "logp and lse outputs are required");
+    if (!workspace || !aligned16(workspace)) return fail(RLK_ERR_INVALID_ARG, "workspace must be non-NULL and 16-byte aligned");
+    if (grad_logp || dhidden_bf16 || dweight_bf16)
+        return fail(RLK_ERR_UNSUPPORTED, "the fused lm_head backward is not available in this build");
+    if ((s = select_device(hidden_bf16)) != RLK_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = begin(workspace, st)) != RLK_OK) return s;
+    uint32_t* status = static_cast<uint32_t*>(workspace);
+    void* ws = static_cast<unsigned char*>(workspace) + kWorkspaceBytes;
+    if ((s = launch_lmhead_fwd(*c, hidden_bf16, H, weight_bf16, targets, active_mask, logp, lse, ws, status, st)) !=
+        RLK_OK)
+        return s;
+    return c->validate ? read_status(workspace, st) : RLK_OK;
+}
+
 // ---------------------------------------------------------------- allocation-free forward
 //
 // rlk_logp_fwd_noalloc serves callers that may not allocate device memory

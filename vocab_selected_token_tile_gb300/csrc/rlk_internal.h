@@ -46,6 +46,14 @@ rlk_status fail(rlk_status s, const std::string& why);
 // validated contract; returns RLK_OK or an error with the message set.
 rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs& a, cudaStream_t stream);
 
+// Fused lm_head (lmhead.cu): host checks, workspace bytes beyond the status
+// area, and the forward launch (GEMM + epilogue partials, then the fold).
+rlk_status lmhead_check(const rlk_logp_contract& c, int64_t H);
+size_t lmhead_fwd_workspace(const rlk_logp_contract& c);
+rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                             const int64_t* targets, const uint8_t* mask, float* logp, float* lse, void* workspace,
+                             uint32_t* status, cudaStream_t stream);
+
 // Launches the bounded-wait self-test kernel (one warp waiting on an mbarrier
 // that nothing arrives at).
 rlk_status launch_selftest_wait(uint64_t limit_ns, uint32_t* status, cudaStream_t stream);
