@@ -154,13 +154,14 @@ rlk_status rlk_logp_bwd(const rlk_logp_contract* contract, const void* logits_bf
 
 /*
  * Bytes of device workspace rlk_logp_fused_lmhead needs for hidden size H
- * (the status word, FP32 partials [T, num_tiles, 2] and target logits [T]);
- * 0 for an unsupported contract.
+ * (the status word, FP32 partials [T, num_tiles, 2], target logits [T], and
+ * for the backward the BF16 dlogits [T, V_padded] plus 32 MB of GEMM
+ * workspace); 0 for an unsupported contract.
  */
 size_t rlk_logp_lmhead_workspace_size(const rlk_logp_contract* contract, int64_t H);
 
 /*
- * Fused lm_head forward: logp and LSE of logits = hidden @ weight^T without
+ * Fused lm_head: logp and LSE of logits = hidden @ weight^T without
  * materialising the logits (the optional fused kernel of issue #323,
  * "Validation Boundary").  A tcgen05 GEMM (FP32 accumulators in tensor
  * memory) feeds each (128-token block, vocabulary tile) into the tile's
@@ -169,9 +170,17 @@ size_t rlk_logp_lmhead_workspace_size(const rlk_logp_contract* contract, int64_t
  *   hidden_bf16  [T, H] BF16 row-major, 16-byte aligned; H a multiple of 64.
  *   weight_bf16  [V_padded, H] BF16 row-major; rows >= V_real are padding.
  *   targets, active_mask, logp, lse: as for rlk_logp_fwd.
- *   grad_logp, dhidden_bf16, dweight_bf16: must be NULL in this build
- *                (RLK_ERR_UNSUPPORTED otherwise).
- *   workspace    rlk_logp_lmhead_workspace_size(contract, H) bytes.
+ *   grad_logp    NULL (forward only) or [T] FP32 upstream gradient of logp.
+ *                With it the backward runs too: dlogits = g (onehot - softmax)
+ *                are recomputed from a second pass of the GEMM and the LSE just
+ *                formed (BF16, in the workspace), then
+ *   dhidden_bf16 [T, H] BF16 out = dlogits[:, :V_real] @ weight[:V_real], and
+ *   dweight_bf16 [V_padded, H] BF16 out = dlogits[:, :V_real]^T @ hidden,
+ *                rows >= V_real exactly 0.  These two are plain GEMMs (cuBLASLt,
+ *                FP32 accumulation, no cross-block reductions, so each element
+ *                is summed in one fixed order).  Both NULL without grad_logp.
+ *   workspace    rlk_logp_lmhead_workspace_size(contract, H) bytes (it holds
+ *                the BF16 dlogits, T * V_padded * 2 bytes, for the backward).
  * The tile width V_padded / num_tiles must be a multiple of 16.  row_stride
  * is not used.  Outputs are bitwise identical for every virtual_tp.
  */

@@ -11,6 +11,7 @@ import torch
 
 import oracle
 import synth
+from oracle.lmhead import lmhead_dlogits
 import vocab_selected_token_tile_gb300 as rlk
 
 pytestmark = pytest.mark.gpu
@@ -123,3 +124,81 @@ def test_lmhead_full_shape_sampled_rows():
     logp, lse = res[1]
     assert np.max(np.abs(lse.cpu().numpy()[rows] - ref_lse)) <= TOL
     assert np.max(np.abs(logp.cpu().numpy()[rows] - ref_logp)) <= TOL
+
+
+def grad_bounds(hb, wb, tgt, active, g, v_real):
+    """Oracle dhidden, dweight and the scale of their terms, sum |a||b|, in FP64."""
+    _, lse, x = oracle.lmhead_forward(hb, wb, tgt, active, v_real)
+    d = lmhead_dlogits(x, lse, tgt, active, g)
+    h = oracle.bf16_bits_to_f64(hb)
+    w = oracle.bf16_bits_to_f64(wb[:v_real])
+    dh, dw = d @ w, d.T @ h
+    return dh, dw, np.abs(d) @ np.abs(w), np.abs(d).T @ np.abs(h)
+
+
+def within(got_bits, ref, scale):
+    """BF16 result vs FP64: dlogits and the output are each rounded once to BF16 (2^-9
+    relative); the GEMM accumulates in FP32.  Bound: 2^-8 (|ref| + sum |terms|)."""
+    got = oracle.bf16_bits_to_f64(got_bits)
+    return np.abs(got - ref) <= 2.0 ** -8 * (np.abs(ref) + scale) + 1e-30
+
+
+@pytest.mark.parametrize("case", CASES[1:4], ids=lambda c: "T%d_H%d_V%d_P%d_NT%d" % c)
+def test_lmhead_backward_small_cases(case):
+    T, H, v_real, v_padded, nt = case
+    hb, wb = make(T, H, v_real, v_padded, seed=3 * T + H)
+    tgt = synth.targets(T, v_real, seed=T + 1)
+    mask = (np.arange(T) % 5 != 1).astype(np.uint8)
+    g = np.where(mask != 0, np.random.default_rng(T).standard_normal(T), 0.0).astype(np.float32)
+    ref_dh, ref_dw, sc_dh, sc_dw = grad_bounds(hb, wb, tgt, mask != 0, g, v_real)
+    ref_logp, ref_lse, _ = oracle.lmhead_forward(hb, wb, tgt, mask != 0, v_real)
+    outs = set()
+    for vtp in (v for v in (1, 2, 4) if nt % v == 0):
+        c = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=nt, virtual_tp=vtp, validate=1)
+        logp, lse, dh, dw = rlk.logp_fused_lmhead(c, dev(hb), dev(wb), torch.from_numpy(tgt).cuda(),
+                                                  torch.from_numpy(mask).cuda(), grad=torch.from_numpy(g).cuda())
+        torch.cuda.synchronize()
+        assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= TOL
+        assert np.max(np.abs(logp.cpu().numpy() - ref_logp)) <= TOL
+        dhb = dh.cpu().numpy().view(np.uint16)
+        dwb = dw.cpu().numpy().view(np.uint16)
+        assert np.all(within(dhb, ref_dh, sc_dh))
+        assert np.all(within(dwb[:v_real], ref_dw, sc_dw))
+        assert np.all(dwb[v_real:] == 0)
+        outs.add((dhb.tobytes(), dwb.tobytes()))
+    assert len(outs) == 1, "virtual TP gradients differ"
+
+
+def test_lmhead_backward_full_shape():
+    """8192 x 4096 x 152576: dhidden on sampled rows against the oracle; dweight by properties."""
+    from synth import workloads as Wl
+    w = Wl.LMHEAD
+    T, H, v_real, v_padded = w.T, w.hidden, w.v_real, w.v_padded
+    hd = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    wd = torch.empty((v_padded, H), dtype=torch.int16, device="cuda")
+    synth.normal_bf16_device(hd, 0, T, H, w.seed, synth.STREAM_HIDDEN, w.hidden_sigma)
+    synth.normal_bf16_device(wd, 0, v_padded, H, w.seed, synth.STREAM_WEIGHT, w.weight_sigma)
+    tgt = Wl.targets(w)
+    mask = Wl.active_mask(w)
+    g = Wl.grad(w, mask != 0)
+    c = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=64, virtual_tp=2, validate=1)
+    logp, lse, dh, dw = rlk.logp_fused_lmhead(c, hd, wd, torch.from_numpy(tgt).cuda(), torch.from_numpy(mask).cuda(),
+                                              grad=torch.from_numpy(g).cuda())
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 4095, T - 1])
+    hb = np.concatenate([synth.normal_bf16_host(int(r), 1, H, w.seed, synth.STREAM_HIDDEN, w.hidden_sigma)
+                         for r in rows])
+    wb = synth.normal_bf16_host(0, v_padded, H, w.seed, synth.STREAM_WEIGHT, w.weight_sigma)
+    _, ref_lse, x = oracle.lmhead_forward(hb, wb, tgt[rows], mask[rows] != 0, v_real)
+    d = lmhead_dlogits(x, ref_lse, tgt[rows], mask[rows] != 0, g[rows])
+    wv = oracle.bf16_bits_to_f64(wb[:v_real])
+    ref = d @ wv
+    scale = np.abs(d) @ np.abs(wv)
+    got = dh[torch.from_numpy(rows).cuda()].cpu().numpy().view(np.uint16)
+    assert np.all(within(got, ref, scale))
+    dwb = dw.view(torch.bfloat16)
+    assert not dw[v_real:].any()
+    # sum over the vocabulary of dW = sum_t h_t * sum_v dlogits[t, v] = 0, up to BF16 rounding
+    col_sum = dwb[:v_real].float().sum(dim=0)
+    col_abs = dwb[:v_real].float().abs().sum(dim=0)
+    assert (col_sum.abs() <= 2.0 ** -6 * col_abs + 1e-6).all()

@@ -234,17 +234,23 @@ def logp_fwd_bwd(contract, logits, targets, mask, grad, dlogits=None, stream=Non
     return dlogits, logp, lse
 
 
-def logp_fused_lmhead(contract, hidden, weight, targets, mask=None, stream=None, workspace=None):
-    """(logp, lse) of logits = hidden @ weight^T (BF16 [T, H] and [V_padded, H] on the GPU)."""
+def logp_fused_lmhead(contract, hidden, weight, targets, mask=None, grad=None, stream=None, workspace=None):
+    """Fused lm_head on BF16 hidden [T, H] and weight [V_padded, H] (GPU tensors).
+
+    Forward only: returns (logp, lse).  With ``grad`` (FP32 [T]): returns
+    (logp, lse, dhidden [T, H] BF16, dweight [V_padded, H] BF16).
+    """
     import torch
     dev = hidden.device
     T, H = hidden.shape
     logp = torch.empty(T, dtype=torch.float32, device=dev)
     lse = torch.empty(T, dtype=torch.float32, device=dev)
+    dh = torch.empty_like(hidden) if grad is not None else None
+    dw = torch.empty_like(weight) if grad is not None else None
     n = rlk_logp_lmhead_workspace_size(contract, H)
     if n == 0:
         check(rlk_logp_check_contract(contract) or RLK_ERR_UNSUPPORTED)
     ws = workspace if workspace is not None else torch.empty(n, dtype=torch.uint8, device=dev)
-    check(rlk_logp_fused_lmhead(contract, _ptr(hidden), H, _ptr(weight), _ptr(targets), _ptr(mask), None,
-                                _ptr(logp), _ptr(lse), None, None, _ptr(ws), _stream(stream)))
-    return logp, lse
+    check(rlk_logp_fused_lmhead(contract, _ptr(hidden), H, _ptr(weight), _ptr(targets), _ptr(mask), _ptr(grad),
+                                _ptr(logp), _ptr(lse), _ptr(dh), _ptr(dw), _ptr(ws), _stream(stream)))
+    return (logp, lse) if grad is None else (logp, lse, dh, dw)

@@ -8,6 +8,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIB_DIR, "librlk_logp.so")
 INCLUDE = os.path.join(ROOT, "include")
+CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 
 
 def sources():
@@ -21,7 +22,8 @@ def commands(nvcc="nvcc"):
         return []
     argv = [nvcc, "-O3", "-std=c++17", "-shared", "-Xcompiler", "-fPIC,-fvisibility=hidden",
             "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
-            "-I", INCLUDE, "-I", CSRC, "--threads", "0"] + src + ["-o", LIB]
+            "-I", INCLUDE, "-I", CSRC, "--threads", "0"] + src + [
+            "-lcublasLt", "-Xlinker", "-rpath," + os.path.join(CUDA_HOME, "lib64"), "-o", LIB]
     if os.environ.get("RLK_PTXAS_VERBOSE"):
         argv.insert(1, "-Xptxas=-v")
     return [(argv, LIB)]

@@ -23,6 +23,7 @@
 // Every wait is bounded; on expiry the CTA records RLK_ERR_TIMEOUT, stops
 // issuing, waits (bounded) for its issued copies and MMAs, frees its tensor
 // memory and returns.
+#include <cublasLt.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -48,11 +49,16 @@ constexpr uint32_t kStageA = kBM * kBK * 2;
 constexpr uint32_t kStageB = kBN * kBK * 2;
 constexpr uint64_t kDrainNsLm = 1000000000ull;
 
+enum : int { kEpiPartials = 0, kEpiGrad = 1 };
+
 struct LmParams {
     const int64_t* targets;
     const uint8_t* mask;
-    float2* partials;  // [T, NT]
-    float* xt;         // [T] target logits
+    float2* partials;  // [T, NT]                     (kEpiPartials)
+    float* xt;         // [T] target logits          (kEpiPartials)
+    const float* lse_in;  // [T]                      (kEpiGrad)
+    const float* grad;    // [T] upstream g of logp   (kEpiGrad)
+    uint16_t* dlogits;    // [T, Vp] BF16 out         (kEpiGrad)
     uint32_t* status;
     int64_t T, Vr, Vp, ignore_index;
     uint64_t wait_ns;
@@ -147,8 +153,36 @@ __device__ __forceinline__ void online_block(const float (&v)[32], int nv, int64
     s_run = __fadd_rn(s_run, __fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])));
 }
 
+// dlogits of one 32-column block of a row: g * ([c == t] - exp(x - LSE)) on
+// real columns of an active row, exactly 0 elsewhere; BF16, stored as
+// nv / 8 16-byte vectors (nv is 32 or 16).
+__device__ __forceinline__ void grad_block(const float (&v)[32], int nv, int64_t col0, int64_t Vr, bool active,
+                                           int64_t target, float g, float nlL, uint16_t* drow) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        float d[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int64_t c = col0 + i + j;
+            float dj = 0.f;
+            if (active && c < Vr && i + j < nv) {
+                const float pr = ex2_approx(__fmaf_rn(v[i + j], kLog2e, nlL));
+                dj = (c == target) ? __fmul_rn(g, __fsub_rn(1.f, pr)) : __fmul_rn(-g, pr);
+            }
+            d[j] = dj;
+        }
+        w[i >> 1] = pack_bf16x2_rn(d[0], d[1]);
+    }
+    uint4* out = reinterpret_cast<uint4*>(drow + col0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        if (q * 8 < nv) out[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+}
+
+template <int EPI>
 __global__ void __launch_bounds__(kThreadsLm, 1)
-    lmhead_fwd_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
+    lmhead_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmWr, const __grid_constant__ LmParams p) {
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzled operand tiles.
@@ -285,6 +319,13 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             }
             float m_run = -INFINITY, s_run = 0.f, xt = 0.f;
             bool have_xt = false;
+            float g = 0.f, nlL = 0.f;
+            uint16_t* drow = nullptr;
+            if (EPI == kEpiGrad && valid) {
+                g = p.grad[row];
+                nlL = -__fmul_rn(p.lse_in[row], kLog2e);
+                drow = p.dlogits + row * p.Vp;
+            }
             for (int ch = 0; ch < p.nchunk; ++ch, ++chunk) {
                 const int acc = (int)(chunk & 1);
                 const uint32_t accph = (uint32_t)((chunk >> 1) & 1);
@@ -301,6 +342,10 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                     tmem_ld32(tmem + lane_base + (uint32_t)(acc * kBN + sub * 32), v);
                     const int nv = min(32, ncols - sub * 32);
                     const int64_t col0 = cbase + sub * 32;
+                    if (EPI == kEpiGrad) {
+                        if (valid) grad_block(v, nv, col0, p.Vr, active, target, g, nlL, drow);
+                        continue;
+                    }
                     online_block(v, nv, col0, p.Vr, m_run, s_run);
                     if (active && target >= col0 && target < col0 + nv && target < p.Vr) {
                         const int idx = (int)(target - col0);
@@ -314,7 +359,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars->tempty[acc]));
             }
-            if (!aborted && valid) {
+            if (EPI == kEpiPartials && !aborted && valid) {
                 p.partials[row * p.NT + tile] = make_float2(m_run, s_run);
                 if (have_xt) p.xt[row] = xt;
             }
@@ -405,14 +450,22 @@ rlk_status lmhead_check(const rlk_logp_contract& c, int64_t H) {
     return RLK_OK;
 }
 
-rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
-                             const int64_t* targets, const uint8_t* mask, float* logp, float* lse, void* workspace,
-                             uint32_t* status, cudaStream_t stream) {
+namespace {
+
+struct LmLaunch {
+    LmParams p;
+    CUtensorMap tmH, tmW, tmWr;
+    int grid, sms;
+};
+
+rlk_status prepare(LmLaunch& L, const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                   const int64_t* targets, const uint8_t* mask, uint32_t* status) {
     int dev = 0;
     cudaGetDevice(&dev);
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    LmParams p{};
+    LmParams& p = L.p;
+    p = LmParams{};
     p.targets = targets;
     p.mask = mask;
     p.status = status;
@@ -429,27 +482,47 @@ rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int
     p.rem = p.W % kBN;
     p.mask_mode = c.mask_mode;
     p.MB = (int32_t)((c.T + kBM - 1) / kBM);
-    unsigned char* ws = static_cast<unsigned char*>(workspace);
-    p.partials = reinterpret_cast<float2*>(ws);
-    p.xt = reinterpret_cast<float*>(ws + ((size_t)c.T * c.num_tiles * 8 + 255) / 256 * 256);
-
-    CUtensorMap tmH, tmW, tmWr;
-    if (!make_map(&tmH, hidden, c.T, H, kBM) || !make_map(&tmW, weight, c.V_padded, H, kBN) ||
-        !make_map(&tmWr, weight, c.V_padded, H, p.rem ? (uint32_t)p.rem : (uint32_t)kBN))
+    if (!make_map(&L.tmH, hidden, c.T, H, kBM) || !make_map(&L.tmW, weight, c.V_padded, H, kBN) ||
+        !make_map(&L.tmWr, weight, c.V_padded, H, p.rem ? (uint32_t)p.rem : (uint32_t)kBN))
         return fail(RLK_ERR_CUDA, "cuTensorMapEncodeTiled failed for the hidden or weight tensor");
-
-    const size_t smem = 1024 + (size_t)kStages * (kStageA + kStageB) + sizeof(Bars);
-    cudaError_t e = cudaFuncSetAttribute(lmhead_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
     const int64_t units_per_shard = (int64_t)(c.num_tiles / c.virtual_tp) * p.MB;
     int64_t per_group = sms / c.virtual_tp;
     if (per_group > units_per_shard) per_group = units_per_shard;
     if (per_group < 1) per_group = 1;
-    const int grid = (int)(per_group * c.virtual_tp);
-    lmhead_fwd_kernel<<<grid, kThreadsLm, smem, stream>>>(tmH, tmW, tmWr, p);
+    L.grid = (int)(per_group * c.virtual_tp);
+    L.sms = sms;
+    return RLK_OK;
+}
+
+template <int EPI>
+rlk_status run_gemm(const LmLaunch& L, cudaStream_t stream) {
+    const size_t smem = 1024 + (size_t)kStages * (kStageA + kStageB) + sizeof(Bars);
+    cudaError_t e = cudaFuncSetAttribute(lmhead_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+    lmhead_kernel<EPI><<<L.grid, kThreadsLm, smem, stream>>>(L.tmH, L.tmW, L.tmWr, L.p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("lm_head GEMM launch: ") + cudaGetErrorString(e));
+    return RLK_OK;
+}
 
+}  // namespace
+
+rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                             const int64_t* targets, const uint8_t* mask, float* logp, float* lse, void* workspace,
+                             uint32_t* status, cudaStream_t stream) {
+    LmLaunch L;
+    rlk_status st = prepare(L, c, hidden, H, weight, targets, mask, status);
+    if (st != RLK_OK) return st;
+    LmParams& p = L.p;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    p.partials = reinterpret_cast<float2*>(ws);
+    p.xt = reinterpret_cast<float*>(ws + ((size_t)c.T * c.num_tiles * 8 + 255) / 256 * 256);
+    if ((st = run_gemm<kEpiPartials>(L, stream)) != RLK_OK) return st;
+    const int sms = L.sms;
+    cudaError_t e;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    (void)dev;
     const int fold_threads = 256;
     const size_t fold_smem = (size_t)(fold_threads / 32) * c.num_tiles * sizeof(float2);
     e = cudaFuncSetAttribute(lmhead_fold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fold_smem);
@@ -460,6 +533,112 @@ rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int
         p.partials, p.xt, targets, mask, c.mask_mode, c.ignore_index, c.T, c.V_real, c.num_tiles, logp, lse, status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("lm_head fold launch: ") + cudaGetErrorString(e));
+    return RLK_OK;
+}
+
+// ----------------------------------------------------------------- backward
+
+namespace {
+
+constexpr size_t kLtWorkspace = (size_t)32 << 20;
+
+cublasLtHandle_t lt_handle(int dev) {
+    static std::mutex mu;
+    static cublasLtHandle_t handles[64] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64) return nullptr;
+    if (!handles[dev] && cublasLtCreate(&handles[dev]) != CUBLAS_STATUS_SUCCESS) handles[dev] = nullptr;
+    return handles[dev];
+}
+
+// C[m, n] = op(A) op(B) in column-major terms, BF16 in and out, FP32 accumulate;
+// reductions across K chunks are excluded, so every output element is summed in
+// one fixed order (deterministic, no atomics).
+rlk_status lt_gemm(cublasLtHandle_t h, cublasOperation_t opA, cublasOperation_t opB, uint64_t m, uint64_t n,
+                   uint64_t k, const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                   void* ws, cudaStream_t stream) {
+    cublasLtMatmulDesc_t op = nullptr;
+    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
+    cublasLtMatmulPreference_t pref = nullptr;
+    rlk_status st = RLK_OK;
+    auto ok = [&](cublasStatus_t s, const char* what) {
+        if (s != CUBLAS_STATUS_SUCCESS && st == RLK_OK) st = fail(RLK_ERR_CUDA, std::string("cuBLASLt ") + what);
+        return st == RLK_OK;
+    };
+    const uint32_t scheme = CUBLASLT_REDUCTION_SCHEME_NONE;
+    const uint64_t wsb = kLtWorkspace;
+    if (ok(cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F), "desc") &&
+        ok(cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &opA, sizeof(opA)), "transa") &&
+        ok(cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &opB, sizeof(opB)), "transb") &&
+        ok(cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, opA == CUBLAS_OP_N ? m : k, opA == CUBLAS_OP_N ? k : m, lda),
+           "layout A") &&
+        ok(cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, opB == CUBLAS_OP_N ? k : n, opB == CUBLAS_OP_N ? n : k, ldb),
+           "layout B") &&
+        ok(cublasLtMatrixLayoutCreate(&lc, CUDA_R_16BF, m, n, ldc), "layout C") &&
+        ok(cublasLtMatmulPreferenceCreate(&pref), "preference") &&
+        ok(cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &wsb, sizeof(wsb)),
+           "workspace pref") &&
+        ok(cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_REDUCTION_SCHEME_MASK, &scheme,
+                                                sizeof(scheme)),
+           "reduction pref")) {
+        cublasLtMatmulHeuristicResult_t res{};
+        int found = 0;
+        if (ok(cublasLtMatmulAlgoGetHeuristic(h, op, la, lb, lc, lc, pref, 1, &res, &found), "heuristic")) {
+            if (found < 1) {
+                st = fail(RLK_ERR_UNSUPPORTED, "cuBLASLt found no deterministic algorithm for the lm_head backward");
+            } else {
+                const float alpha = 1.f, beta = 0.f;
+                ok(cublasLtMatmul(h, op, &alpha, A, la, B, lb, &beta, C, lc, C, lc, &res.algo, ws, kLtWorkspace, stream),
+                   "matmul");
+            }
+        }
+    }
+    if (pref) cublasLtMatmulPreferenceDestroy(pref);
+    if (lc) cublasLtMatrixLayoutDestroy(lc);
+    if (lb) cublasLtMatrixLayoutDestroy(lb);
+    if (la) cublasLtMatrixLayoutDestroy(la);
+    if (op) cublasLtMatmulDescDestroy(op);
+    return st;
+}
+
+}  // namespace
+
+size_t lmhead_bwd_workspace(const rlk_logp_contract& c) {
+    return lmhead_fwd_workspace(c) + ((size_t)c.T * c.V_padded * 2 + 255) / 256 * 256 + kLtWorkspace;
+}
+
+rlk_status launch_lmhead_bwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                             const int64_t* targets, const uint8_t* mask, const float* grad, float* logp, float* lse,
+                             void* dhidden, void* dweight, void* workspace, uint32_t* status, cudaStream_t stream) {
+    rlk_status st = launch_lmhead_fwd(c, hidden, H, weight, targets, mask, logp, lse, workspace, status, stream);
+    if (st != RLK_OK) return st;
+    unsigned char* ws = static_cast<unsigned char*>(workspace) + lmhead_fwd_workspace(c);
+    uint16_t* dlogits = reinterpret_cast<uint16_t*>(ws);
+    void* lt_ws = ws + ((size_t)c.T * c.V_padded * 2 + 255) / 256 * 256;
+    // dlogits = g * (onehot - exp(x - LSE)) from the recomputed logits (BF16 [T, V_padded]).
+    LmLaunch L;
+    if ((st = prepare(L, c, hidden, H, weight, targets, mask, status)) != RLK_OK) return st;
+    L.p.lse_in = lse;
+    L.p.grad = grad;
+    L.p.dlogits = dlogits;
+    if ((st = run_gemm<kEpiGrad>(L, stream)) != RLK_OK) return st;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cublasLtHandle_t h = lt_handle(dev);
+    if (!h) return fail(RLK_ERR_CUDA, "cublasLtCreate failed");
+    // dHidden [T, H] = dlogits[:, :V_real] W[:V_real]; column-major: [H, T] = W_cm[H, Vr] x dlogits_cm[Vr, T].
+    if ((st = lt_gemm(h, CUBLAS_OP_N, CUBLAS_OP_N, (uint64_t)H, (uint64_t)c.T, (uint64_t)c.V_real, weight, H, dlogits,
+                      c.V_padded, dhidden, H, lt_ws, stream)) != RLK_OK)
+        return st;
+    // dW[:V_real] = dlogits[:, :V_real]^T hidden; column-major: [H, Vr] = hidden_cm[H, T] x (dlogits_cm[Vr, T])^T.
+    if ((st = lt_gemm(h, CUBLAS_OP_N, CUBLAS_OP_T, (uint64_t)H, (uint64_t)c.V_real, (uint64_t)c.T, hidden, H, dlogits,
+                      c.V_padded, dweight, H, lt_ws, stream)) != RLK_OK)
+        return st;
+    if (c.V_padded > c.V_real) {
+        const cudaError_t e = cudaMemsetAsync(static_cast<uint16_t*>(dweight) + (size_t)c.V_real * H, 0,
+                                              (size_t)(c.V_padded - c.V_real) * H * 2, stream);
+        if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("clearing padded dW rows: ") + cudaGetErrorString(e));
+    }
     return RLK_OK;
 }
 

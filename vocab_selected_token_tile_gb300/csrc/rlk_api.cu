@@ -178,7 +178,7 @@ RLK_EXPORT rlk_status rlk_logp_bwd(const rlk_logp_contract* c, const void* logit
 
 RLK_EXPORT size_t rlk_logp_lmhead_workspace_size(const rlk_logp_contract* c, int64_t H) {
     if (check_contract(c) != RLK_OK || lmhead_check(*c, H) != RLK_OK) return 0;
-    return kWorkspaceBytes + lmhead_fwd_workspace(*c);
+    return kWorkspaceBytes + lmhead_bwd_workspace(*c);
 }
 
 RLK_EXPORT rlk_status rlk_logp_fused_lmhead(const rlk_logp_contract* c, const void* hidden_bf16, int64_t H,
@@ -200,16 +200,24 @@ RLK_EXPORT rlk_status rlk_logp_fused_lmhead(const rlk_logp_contract* c, const vo
         return fail(RLK_ERR_INVALID_ARG, "ignore_index mode takes no active_mask (pass NULL)");
     if (!logp || !lse) return fail(RLK_ERR_INVALID_ARG, "logp and lse outputs are required");
     if (!workspace || !aligned16(workspace)) return fail(RLK_ERR_INVALID_ARG, "workspace must be non-NULL and 16-byte aligned");
-    if (grad_logp || dhidden_bf16 || dweight_bf16)
-        return fail(RLK_ERR_UNSUPPORTED, "the fused lm_head backward is not available in this build");
+    const bool bwd = grad_logp != nullptr;
+    if (bwd && (!dhidden_bf16 || !dweight_bf16))
+        return fail(RLK_ERR_INVALID_ARG, "the backward (grad_logp given) needs dhidden and dweight");
+    if (!bwd && (dhidden_bf16 || dweight_bf16))
+        return fail(RLK_ERR_INVALID_ARG, "dhidden/dweight are written only when grad_logp is given");
+    if (bwd && (!aligned16(dhidden_bf16) || !aligned16(dweight_bf16)))
+        return fail(RLK_ERR_MISALIGNED, "dhidden and dweight must be 16-byte aligned");
     if ((s = select_device(hidden_bf16)) != RLK_OK) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if ((s = begin(workspace, st)) != RLK_OK) return s;
     uint32_t* status = static_cast<uint32_t*>(workspace);
     void* ws = static_cast<unsigned char*>(workspace) + kWorkspaceBytes;
-    if ((s = launch_lmhead_fwd(*c, hidden_bf16, H, weight_bf16, targets, active_mask, logp, lse, ws, status, st)) !=
-        RLK_OK)
-        return s;
+    if (bwd)
+        s = launch_lmhead_bwd(*c, hidden_bf16, H, weight_bf16, targets, active_mask, grad_logp, logp, lse,
+                              dhidden_bf16, dweight_bf16, ws, status, st);
+    else
+        s = launch_lmhead_fwd(*c, hidden_bf16, H, weight_bf16, targets, active_mask, logp, lse, ws, status, st);
+    if (s != RLK_OK) return s;
     return c->validate ? read_status(workspace, st) : RLK_OK;
 }
 

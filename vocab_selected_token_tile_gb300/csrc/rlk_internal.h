@@ -54,6 +54,11 @@ rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int
                              const int64_t* targets, const uint8_t* mask, float* logp, float* lse, void* workspace,
                              uint32_t* status, cudaStream_t stream);
 
+size_t lmhead_bwd_workspace(const rlk_logp_contract& c);
+rlk_status launch_lmhead_bwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                             const int64_t* targets, const uint8_t* mask, const float* grad, float* logp, float* lse,
+                             void* dhidden, void* dweight, void* workspace, uint32_t* status, cudaStream_t stream);
+
 // Launches the bounded-wait self-test kernel (one warp waiting on an mbarrier
 // that nothing arrives at).
 rlk_status launch_selftest_wait(uint64_t limit_ns, uint32_t* status, cudaStream_t stream);
