@@ -297,7 +297,8 @@ def run_ours(args, ws, rank, local):
 
 
 def lmhead_bench(rlk, args, dev, steps=10, warmup=3, rows=0):
-    """The fused lm_head forward: hidden [8192, 4096] x W [152576, 4096], 64 tiles."""
+    """The fused lm_head: hidden [8192, 4096] x W [152576, 4096], 64 tiles; forward, then forward+backward."""
+    import numpy as np
     import torch
 
     import synth
@@ -312,6 +313,7 @@ def lmhead_bench(rlk, args, dev, steps=10, warmup=3, rows=0):
     tgt = torch.from_numpy(W.targets(w)[:T]).to(dev)
     mask = torch.from_numpy(W.active_mask(w)[:T]).to(dev)
     c = rlk.Contract(T=T, V_real=Vr, V_padded=Vp, num_tiles=w.num_tiles, virtual_tp=args.vtp, validate=0)
+    rlk.check(rlk.rlk_logp_check_contract(c))
     ws = torch.empty(rlk.rlk_logp_lmhead_workspace_size(c, H), dtype=torch.uint8, device=dev)
     for _ in range(warmup):
         rlk.logp_fused_lmhead(c, hd, wd, tgt, mask, workspace=ws)
@@ -326,10 +328,26 @@ def lmhead_bench(rlk, args, dev, steps=10, warmup=3, rows=0):
     flop = 2.0 * T * Vp * H
     _, bf16_peak, kind = measured_peaks()
     tflops = flop / (ms * 1e-3) / 1e12
-    return {"workload": f"lmhead fwd: hidden [{T},{H}] x W [{Vp},{H}] BF16, 64 tiles, virtual TP {args.vtp}",
-            "ms": ms, "tokens_per_s": T / (ms * 1e-3), "tflops": tflops,
-            "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s",
-                         "frac": tflops / bf16_peak, "peak_source": f"{kind} bf16_tflops (cuBLAS burst)"}}
+    out = {"workload": f"lmhead fwd: hidden [{T},{H}] x W [{Vp},{H}] BF16, 64 tiles, virtual TP {args.vtp}",
+           "ms": ms, "tokens_per_s": T / (ms * 1e-3), "tflops": tflops,
+           "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s",
+                        "frac": tflops / bf16_peak, "peak_source": f"{kind} bf16_tflops (cuBLAS burst)"}}
+    # forward + backward: GEMM, recompute GEMM with the dlogits epilogue, dHidden and dW GEMMs
+    g = torch.from_numpy(W.grad(w, W.active_rows(w))[:T].astype(np.float32)).to(dev)
+    wsb = torch.empty(rlk.rlk_logp_lmhead_workspace_size(c, H), dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        rlk.logp_fused_lmhead(c, hd, wd, tgt, mask, grad=g, workspace=wsb)
+    a.record(stream)
+    for _ in range(steps):
+        rlk.logp_fused_lmhead(c, hd, wd, tgt, mask, grad=g, workspace=wsb)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms_b = a.elapsed_time(b) / steps
+    tf_b = 4 * flop / (ms_b * 1e-3) / 1e12
+    out["fwd_bwd"] = {"ms": ms_b, "tokens_per_s": T / (ms_b * 1e-3), "tflops_executed": tf_b,
+                      "frac_executed": tf_b / bf16_peak,
+                      "note": "4 x 2*T*V_padded*H executed: forward, recompute with dlogits, dHidden, dW"}
+    return out
 
 
 def extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, Vp, args):
