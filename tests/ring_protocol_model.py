@@ -41,8 +41,24 @@ class ProtocolError(AssertionError):
     pass
 
 
+def block_schedule(mode, rows):
+    """Blocks of nch items the producer issues, in order: ('A' | 'B', row)."""
+    if mode == "fwd":
+        return [("A", n) for n in range(rows)]
+    if mode == "bwd":
+        return [("B", n) for n in range(rows)]
+    if mode == "fused":
+        return [("A", n) for n in range(rows)]  # one load per row; phase B reuses the resident slots
+    seq = [("A", 0)]  # fused_l2: A0, A1, B0, A2, B1, ..., B(R-1)
+    for n in range(rows):
+        if n + 1 < rows:
+            seq.append(("A", n + 1))
+        seq.append(("B", n))
+    return seq
+
+
 def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80):
-    """mode: 'fwd' | 'bwd' | 'fused'.  Raises ProtocolError on a stale read or a deadlock."""
+    """mode: 'fwd' | 'bwd' | 'fused' | 'fused_l2'.  Raises ProtocolError on a stale read or a deadlock."""
     rng = random.Random(seed)
     ntl = NT // C
     nch = (ntl + tps - 1) // tps
@@ -91,9 +107,17 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80)
         if c.hdr[s] != i or c.data[s] != i:
             raise ProtocolError(f"{mode} {where}: slot {s} holds item {c.hdr[s]}/{c.data[s]}, expected {i}")
 
+    sched = block_schedule(mode, rows)
+    block_index = {blk: b for b, blk in enumerate(sched)}
+
+    def item_of(phase, n, ch):
+        if mode == "fused":
+            return n * nch + ch
+        return block_index[(phase, n)] * nch + ch
+
     def producer(c):
         i = 0
-        for _ in range(rows):
+        for _ in sched:
             for _ in range(nch):
                 s, par = ring(i)
                 yield from wait(c.empty[s], par ^ 1)
@@ -115,22 +139,22 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80)
             yield from wait(c.partfree[b], (n // R - 1) & 1)
         for l in tiles_of(w, n):
             ch, share = chunk_of(l)
-            i = n * nch + ch
+            i = item_of("A", n, ch)
             s, par = ring(i)
             yield from wait_item(c, s, par, i)
             check_slot(c, s, i, "phase A")
             c.part[b][c.rank * ntl + l] = n
             yield "tile"
-            if mode == "fwd":
+            if mode in ("fwd", "fused_l2"):
                 c.empty[s].arrive(share)
         c.rowdone[b].arrive()
 
     def phase_b(c, w, n):
         for l in tiles_of(w, n):
             ch, share = chunk_of(l)
-            i = n * nch + ch
+            i = item_of("A" if mode == "fused" else "B", n, ch)
             s, par = ring(i)
-            if mode == "bwd":
+            if mode in ("bwd", "fused_l2"):
                 yield from wait_item(c, s, par, i)
             check_slot(c, s, i, "phase B")
             yield "grad"
@@ -166,7 +190,7 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80)
             if any(v != n for v in c.part[b]):
                 raise ProtocolError(f"{mode} fold of row {n} saw partials of rows {sorted(set(c.part[b]))}")
             yield "fold"
-            if mode == "fused":
+            if mode in ("fused", "fused_l2"):
                 c.lseready[b].arrive()
             c.partfree[b].arrive()
 

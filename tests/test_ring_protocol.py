@@ -59,13 +59,18 @@ def plan(mode, vtp, v_padded, nt):
     return C, tps, max_slots(slot_bytes(tps))
 
 
-CONFIGS = [(mode, vtp) for mode in ("fwd", "bwd", "fused") for vtp in (1, 2, 4, 8)
+def plan_l2(vtp, v_padded, nt):
+    """The L2-assisted fused mode is planned like the forward: C = virtual TP, no residency."""
+    return plan("fwd", vtp, v_padded, nt)
+
+
+CONFIGS = [(mode, vtp) for mode in ("fwd", "bwd", "fused", "fused_l2") for vtp in (1, 2, 4, 8)
            if not (mode == "bwd" and vtp > 1)]
 
 
 @pytest.mark.parametrize("mode,vtp", CONFIGS)
 def test_ring_protocol_reads_only_landed_slots(mode, vtp):
-    C, tps, ns = plan(mode, vtp, 152576, 64)
+    C, tps, ns = plan_l2(vtp, 152576, 64) if mode == "fused_l2" else plan(mode, vtp, 152576, 64)
     for seed in range(3):
         simulate(mode, rows=24, C=C, NT=64, tps=tps, NS=ns, W=16, seed=seed)
 
@@ -73,6 +78,15 @@ def test_ring_protocol_reads_only_landed_slots(mode, vtp):
 def test_planner_replay_matches_the_benchmark_shapes():
     assert plan("fused", 2, 152576, 64) == (4, 2, 23)
     assert plan("fwd", 1, 152576, 64) == (1, 3, 15)
+
+
+@pytest.mark.parametrize("ns", [1, 2, 3, 5])
+def test_l2_fused_schedule_progresses_with_tiny_rings(ns):
+    # The skewed producer order A(0), A(1), B(0), A(2), ... must not need more
+    # than one slot: consumers take items in the order they are issued.
+    for C in (1, 2, 4):
+        for tps in (1, 3):
+            simulate("fused_l2", rows=7, C=C, NT=64, tps=tps, NS=ns, W=16, seed=10 * ns + C)
 
 
 def test_without_the_issued_item_check_the_model_finds_stale_reads():

@@ -9,6 +9,12 @@
 //   kModeFused both, with each row's slice held in shared memory between the
 //              two phases so the logits are read from HBM once
 //                                                       (rlk_logp_bwd, no lse_in)
+//   kModeFusedL2 both, streaming like kModeFwd: phase A releases each slot at
+//              once and phase B copies the row again, which the L2 still holds
+//              (phase-A copies of rows that need a gradient carry an
+//              evict-last hint, every other copy evict-first), so HBM still
+//              sees one read of the logits; the default for rlk_logp_bwd
+//              without lse_in, since it needs no shared memory for residency
 //
 // Method (PR #289 "[WS2][PR4][Logp] feat: add distributed TP/CP logprob drift
 // report": the PR-1 contract commit, the global-tile commit and the typed
@@ -412,22 +418,72 @@ struct Ctx {
     Waiter wt;
 };
 
+// Position of an item in the slot ring: slot index and the parity of the pass.
+struct RingPos {
+    int slot;
+    uint32_t par;
+};
+
+__device__ __forceinline__ RingPos ring_add(RingPos r, int k, int NS) {
+    const int s = r.slot + k;
+    const int q = s / NS;
+    return RingPos{s - q * NS, r.par ^ (uint32_t)(q & 1)};
+}
+
+// The producer issues blocks of nch items (one row's chunks for one phase).
+// kModeFwd / kModeBwd / kModeFused: block n is row n.  kModeFusedL2 follows
+// the consumers' skewed order A(0), A(1), B(0), A(2), B(1), ..., B(R-1).
+__device__ __forceinline__ int64_t block_of(int MODE, int64_t n, bool phase_b, int64_t R) {
+    if (MODE != kModeFusedL2) return n;
+    if (!phase_b) return n == 0 ? 0 : 2 * n - 1;
+    return n == R - 1 ? 2 * R - 1 : 2 * n + 2;
+}
+
+// Inverse of block_of for kModeFusedL2: block j -> (row, is phase B).
+__device__ __forceinline__ void block_row(int64_t j, int64_t R, int64_t& n, bool& phase_b) {
+    if (j == 0) {
+        n = 0;
+        phase_b = false;
+    } else if (j == 2 * R - 1) {
+        n = R - 1;
+        phase_b = true;
+    } else if (j & 1) {
+        n = (j + 1) / 2;
+        phase_b = false;
+    } else {
+        n = (j - 2) / 2;
+        phase_b = true;
+    }
+}
+
+__device__ __forceinline__ RingPos ring_of(uint32_t item, int NS) {
+    return RingPos{(int)(item % (uint32_t)NS), (item / (uint32_t)NS) & 1u};
+}
+
+// Row metadata of 32 consecutive rows of this CTA, one row per lane.
+struct MetaWindow {
+    int64_t t = 0;
+    int32_t act = 0;
+    float g = 0.f, lin = 0.f;
+};
+
 template <int MODE>
 __device__ void producer(const Params& p, const Ctx& x) {
     const int lane = x.lane;
-    const uint64_t policy = l2_policy_evict_first();
+    const uint64_t pol_first = l2_policy_evict_first();
+    const uint64_t pol_last = l2_policy_evict_last();
+    // Windows [base, base+32) and [base-32, base): kModeFusedL2 visits row n
+    // after row n+1, which can lie in the next window.
     int64_t meta_base = 0;
-    int64_t m_t = 0;
-    int32_t m_act = 0;
-    float m_g = 0.f, m_l = 0.f;
+    MetaWindow cur, prev;
     auto load_meta = [&](int64_t base) {
         const int64_t n = base + lane;
         if (n < x.nrows) {
             const int64_t r = x.q + n * x.G;
-            m_t = p.a.targets[r];
-            m_act = (p.mask_mode == RLK_MASK_EXPLICIT) ? (p.a.mask[r] != 0) : (m_t != p.ignore_index);
-            m_g = (MODE != kModeFwd) ? p.a.grad[r] : 0.f;
-            m_l = (MODE == kModeBwd) ? p.a.lse_in[r] : 0.f;
+            cur.t = p.a.targets[r];
+            cur.act = (p.mask_mode == RLK_MASK_EXPLICIT) ? (p.a.mask[r] != 0) : (cur.t != p.ignore_index);
+            cur.g = (MODE != kModeFwd) ? p.a.grad[r] : 0.f;
+            cur.lin = (MODE == kModeBwd) ? p.a.lse_in[r] : 0.f;
         }
     };
     load_meta(0);
@@ -435,16 +491,32 @@ __device__ void producer(const Params& p, const Ctx& x) {
     int slot = 0;
     uint32_t phase = 0;
     bool aborted = false;
-    for (int64_t n = 0; n < x.nrows && !aborted; ++n) {
+    const int64_t nblocks = (MODE == kModeFusedL2) ? 2 * x.nrows : x.nrows;
+    for (int64_t j = 0; j < nblocks && !aborted; ++j) {
+        int64_t n = j;
+        bool second = false;  // kModeFusedL2: the phase-B copy of row n
+        if (MODE == kModeFusedL2) block_row(j, x.nrows, n, second);
         if (n - meta_base >= 32) {
-            meta_base = n;
-            load_meta(n);
+            prev = cur;
+            meta_base += 32;
+            load_meta(meta_base);
         }
-        const int src = (int)(n - meta_base);
-        const int64_t t = (int64_t)__shfl_sync(0xFFFFFFFFu, (unsigned long long)m_t, src);
-        const int32_t act = __shfl_sync(0xFFFFFFFFu, m_act, src);
-        const float g = __shfl_sync(0xFFFFFFFFu, m_g, src);
-        const float lin = __shfl_sync(0xFFFFFFFFu, m_l, src);
+        const bool in_cur = n >= meta_base;
+        const int src = (int)(in_cur ? n - meta_base : n - meta_base + 32);
+        const int64_t t_c = (int64_t)__shfl_sync(0xFFFFFFFFu, (unsigned long long)cur.t, src);
+        const int64_t t_p = (int64_t)__shfl_sync(0xFFFFFFFFu, (unsigned long long)prev.t, src);
+        const int32_t a_c = __shfl_sync(0xFFFFFFFFu, cur.act, src), a_p = __shfl_sync(0xFFFFFFFFu, prev.act, src);
+        const float g_c = __shfl_sync(0xFFFFFFFFu, cur.g, src), g_p = __shfl_sync(0xFFFFFFFFu, prev.g, src);
+        const float l_c = __shfl_sync(0xFFFFFFFFu, cur.lin, src), l_p = __shfl_sync(0xFFFFFFFFu, prev.lin, src);
+        const int64_t t = in_cur ? t_c : t_p;
+        const int32_t act = in_cur ? a_c : a_p;
+        const float g = in_cur ? g_c : g_p;
+        const float lin = in_cur ? l_c : l_p;
+        // Which copies move bytes, and their L2 hint: an inactive row's
+        // columns are needed by phase A only; the first copy of a row that
+        // kModeFusedL2 reads again stays in L2 (evict-last).
+        const bool needs_bytes = !((MODE == kModeBwd || second) && !act);
+        const uint64_t policy = (MODE == kModeFusedL2 && !second && act) ? pol_last : pol_first;
         const int64_t row = x.q + n * x.G;
         const uint16_t* grow = p.a.logits + row * p.stride;
         for (int c = 0; c < x.nch; ++c) {
@@ -468,8 +540,7 @@ __device__ void producer(const Params& p, const Ctx& x) {
                 const int kf = x.k0 + c * p.tps;
                 const int kl = min(kf + p.tps, x.k0 + x.ntl);
                 const Span sp = chunk_span(kf, kl, p);
-                const uint32_t bytes =
-                    (sp.b > sp.a && (MODE != kModeBwd || act)) ? (uint32_t)((sp.b - sp.a) * 2) : 0u;
+                const uint32_t bytes = (sp.b > sp.a && needs_bytes) ? (uint32_t)((sp.b - sp.a) * 2) : 0u;
                 const uint32_t fb = x.full0 + 8u * slot;
                 if (bytes) {
                     mbar_arrive_expect_tx(fb, bytes);
@@ -549,22 +620,10 @@ __device__ void fold_warp(const Params& p, const Ctx& x) {
             if (active && rs.has_xt) p.a.logp[row] = __fsub_rn(rs.xt, lse_v);
             rs.has_xt = 0;
             rs.lse = lse_v;
-            if (MODE == kModeFused) mbar_arrive(x.lseready0 + 8u * b);
+            if (MODE == kModeFused || MODE == kModeFusedL2) mbar_arrive(x.lseready0 + 8u * b);
             mbar_arrive(x.partfree0 + 8u * b);
         }
     }
-}
-
-// Position of an item in the slot ring: slot index and the parity of the pass.
-struct RingPos {
-    int slot;
-    uint32_t par;
-};
-
-__device__ __forceinline__ RingPos ring_add(RingPos r, int k, int NS) {
-    const int s = r.slot + k;
-    const int q = s / NS;
-    return RingPos{s - q * NS, r.par ^ (uint32_t)(q & 1)};
 }
 
 // Work is per tile, copies are per chunk of tps tiles: consumer warp w
@@ -611,7 +670,7 @@ __device__ __forceinline__ int first_tile(const Ctx& x, int64_t n) {
 // FWD releases each tile's share of its slot at once; FUSED keeps the slots
 // for phase B.
 template <int MODE>
-__device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, RingPos rb) {
+__device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0) {
     constexpr int W = kConsumerWarps;
     const int lane = x.lane;
     const int b = (int)(n % kRowBufs);
@@ -619,9 +678,10 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, RingPos rb) {
     if (n >= kRowBufs) ok = x.wt.warp_wait(x.partfree0 + 8u * b, (uint32_t)((n / kRowBufs - 1) & 1));
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
     const int slot_elems = p.slot_bytes / 2;
+    const RingPos rb = ring_of(item0, p.NS);
     for (int l = first_tile(x, n); l < x.ntl && ok; l += W) {
         const TileItem it = tile_item(p, x, rb, l);
-        if (!wait_item(x, it, (uint32_t)(n * x.nch + l / p.tps))) {
+        if (!wait_item(x, it, item0 + (uint32_t)(l / p.tps))) {
             ok = false;
             break;
         }
@@ -646,7 +706,7 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, RingPos rb) {
                 rs.has_xt = 1;
             }
         }
-        if (MODE == kModeFwd) {
+        if (MODE == kModeFwd || MODE == kModeFusedL2) {
             __syncwarp();
             if (lane == 0) mbar_arrive_n(x.empty0 + 8u * it.slot, it.share);
         }
@@ -658,17 +718,20 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, RingPos rb) {
 
 // dlogits of row n's tiles for one consumer warp; each tile then releases its
 // share of its slot.  FUSED: the slots are still resident from phase A and
-// lse_v is the fold's LSE.  BWD: the tile waits for its chunk here and reads
-// the row's LSE (lse_in) from the slot header.
+// lse_v is the fold's LSE.  FUSED_L2: the tile waits for the second copy of
+// its chunk; lse_v is the fold's LSE.  BWD: the tile waits for its chunk and
+// reads the row's LSE (lse_in) from the slot header.
 template <int MODE>
-__device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, RingPos rb, float lse_v) {
+__device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0, float lse_v) {
     constexpr int W = kConsumerWarps;
+    constexpr bool kWaits = MODE == kModeBwd || MODE == kModeFusedL2;
     const int lane = x.lane;
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
     const int slot_elems = p.slot_bytes / 2;
+    const RingPos rb = ring_of(item0, p.NS);
     for (int l = first_tile(x, n); l < x.ntl; l += W) {
         const TileItem it = tile_item(p, x, rb, l);
-        if (MODE == kModeBwd && !wait_item(x, it, (uint32_t)(n * x.nch + l / p.tps))) return false;
+        if (kWaits && !wait_item(x, it, item0 + (uint32_t)(l / p.tps))) return false;
         const SlotHdr h = x.hdr[it.slot];
         const Span sp = chunk_span(it.kf, it.kl, p);
         const int k = x.k0 + l;
@@ -689,31 +752,28 @@ __device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, RingPos rb, fl
 template <int MODE>
 __device__ void consumer(const Params& p, const Ctx& x) {
     static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0, "consumer warp count must be a power of two");
-    RingPos base{0, 0u};
+    const int64_t R = x.nrows;
+    const uint32_t nch = (uint32_t)x.nch;
+    auto item_a = [&](int64_t n) { return (uint32_t)block_of(MODE, n, false, R) * nch; };
+    auto item_b = [&](int64_t n) { return (uint32_t)block_of(MODE, n, MODE != kModeFused, R) * nch; };
     if constexpr (MODE == kModeBwd) {
-        for (int64_t n = 0; n < x.nrows; ++n) {
-            if (!phase_b<MODE>(p, x, n, base, 0.f)) break;
-            base = ring_add(base, x.nch, p.NS);
-        }
+        for (int64_t n = 0; n < R; ++n)
+            if (!phase_b<MODE>(p, x, n, item_b(n), 0.f)) break;
     } else if constexpr (MODE == kModeFwd) {
-        for (int64_t n = 0; n < x.nrows; ++n) {
-            phase_a<MODE>(p, x, n, base);
-            base = ring_add(base, x.nch, p.NS);
-        }
+        for (int64_t n = 0; n < R; ++n) phase_a<MODE>(p, x, n, item_a(n));
     } else {
         // Skewed order A(0), A(1), B(0), A(2), B(1), ...: the fold of row n
-        // overlaps phase A of row n+1.  Two rows of slots are resident.
-        bool ok_cur = x.nrows > 0 ? phase_a<MODE>(p, x, 0, base) : true;
-        for (int64_t n = 0; n < x.nrows; ++n) {
-            const RingPos next = ring_add(base, x.nch, p.NS);
+        // overlaps phase A of row n+1.  kModeFused keeps two rows of slots
+        // resident; kModeFusedL2 copies each row a second time for phase B.
+        bool ok_cur = R > 0 ? phase_a<MODE>(p, x, 0, item_a(0)) : true;
+        for (int64_t n = 0; n < R; ++n) {
             bool ok_next = true;
-            if (n + 1 < x.nrows) ok_next = phase_a<MODE>(p, x, n + 1, next);
+            if (n + 1 < R) ok_next = phase_a<MODE>(p, x, n + 1, item_a(n + 1));
             const int b = (int)(n % kRowBufs);
             const bool ready = x.wt.warp_wait(x.lseready0 + 8u * b, (uint32_t)((n / kRowBufs) & 1));
             // After an expired wait the slot headers may be stale: skip the
             // writes (the status word already says RLK_ERR_TIMEOUT).
-            if (ready && ok_cur && !*x.wt.abort_flag) phase_b<MODE>(p, x, n, base, x.rows[b].lse);
-            base = next;
+            if (ready && ok_cur && !*x.wt.abort_flag) phase_b<MODE>(p, x, n, item_b(n), x.rows[b].lse);
             ok_cur = ok_next;
         }
     }
@@ -894,6 +954,11 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         return lo;
     };
 
+    // The fused schedule: RLK_FUSED_SCHEDULE=l2 (second read from L2) or resident.
+    if (mode == kModeFused) {
+        const char* sch = std::getenv("RLK_FUSED_SCHEDULE");
+        if (sch && std::string(sch) == "l2") mode = kModeFusedL2;
+    }
     int C = (mode == kModeBwd) ? 1 : c.virtual_tp;
     int NS = 0;
     p.C = C;
@@ -921,9 +986,10 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     p.NS = NS;
     const uint32_t smem = layout(p, NS);
 
-    void (*kfn)(Params) = (mode == kModeFwd) ? stream_kernel<kModeFwd>
-                        : (mode == kModeBwd) ? stream_kernel<kModeBwd>
-                                             : stream_kernel<kModeFused>;
+    void (*kfn)(Params) = (mode == kModeFwd)     ? stream_kernel<kModeFwd>
+                        : (mode == kModeBwd)     ? stream_kernel<kModeBwd>
+                        : (mode == kModeFusedL2) ? stream_kernel<kModeFusedL2>
+                                                 : stream_kernel<kModeFused>;
     const void* fn = reinterpret_cast<const void*>(kfn);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));

@@ -23,7 +23,9 @@ constexpr int64_t kMaxTileCols = 16384;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 constexpr size_t kWorkspaceBytes = 256;
 
-enum StreamMode : int { kModeFwd = 0, kModeBwd = 1, kModeFused = 2 };
+// kModeFused is what callers ask for; the planner runs it as kModeFusedL2
+// (second read of each row from L2) when RLK_FUSED_SCHEDULE=l2.
+enum StreamMode : int { kModeFwd = 0, kModeBwd = 1, kModeFused = 2, kModeFusedL2 = 3 };
 
 // Arguments of one streaming launch (all device pointers).
 struct StreamArgs {
