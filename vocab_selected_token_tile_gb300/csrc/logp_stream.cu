@@ -14,7 +14,7 @@
 //              (phase-A copies of rows that need a gradient carry an
 //              evict-last hint, every other copy evict-first), so HBM still
 //              sees one read of the logits; the default for rlk_logp_bwd
-//              without lse_in, since it needs no shared memory for residency
+//              without lse_in (RLK_FUSED_SCHEDULE=resident selects kModeFused)
 //
 // Method (PR #289 "[WS2][PR4][Logp] feat: add distributed TP/CP logprob drift
 // report": the PR-1 contract commit, the global-tile commit and the typed
@@ -954,10 +954,11 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         return lo;
     };
 
-    // The fused schedule: RLK_FUSED_SCHEDULE=l2 (second read from L2) or resident.
+    // The fused schedule: second read from L2 (default) or, with
+    // RLK_FUSED_SCHEDULE=resident, the row shard held in shared memory.
     if (mode == kModeFused) {
         const char* sch = std::getenv("RLK_FUSED_SCHEDULE");
-        if (sch && std::string(sch) == "l2") mode = kModeFusedL2;
+        if (!(sch && std::string(sch) == "resident")) mode = kModeFusedL2;
     }
     int C = (mode == kModeBwd) ? 1 : c.virtual_tp;
     int NS = 0;

@@ -24,7 +24,7 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 constexpr size_t kWorkspaceBytes = 256;
 
 // kModeFused is what callers ask for; the planner runs it as kModeFusedL2
-// (second read of each row from L2) when RLK_FUSED_SCHEDULE=l2.
+// (second read of each row from L2) unless RLK_FUSED_SCHEDULE=resident.
 enum StreamMode : int { kModeFwd = 0, kModeBwd = 1, kModeFused = 2, kModeFusedL2 = 3 };
 
 // Arguments of one streaming launch (all device pointers).
