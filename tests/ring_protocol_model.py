@@ -41,7 +41,7 @@ class ProtocolError(AssertionError):
     pass
 
 
-def block_schedule(mode, rows):
+def block_schedule(mode, rows, skew=1):
     """Blocks of nch items the producer issues, in order: ('A' | 'B', row)."""
     if mode == "fwd":
         return [("A", n) for n in range(rows)]
@@ -49,20 +49,24 @@ def block_schedule(mode, rows):
         return [("B", n) for n in range(rows)]
     if mode == "fused":
         return [("A", n) for n in range(rows)]  # one load per row; phase B reuses the resident slots
-    seq = [("A", 0)]  # fused_l2: A0, A1, B0, A2, B1, ..., B(R-1)
+    # fused_l2 with skew S: A(0..S-1), then A(n+S), B(n) for each n
+    seq = [("A", n) for n in range(min(skew, rows))]
     for n in range(rows):
-        if n + 1 < rows:
-            seq.append(("A", n + 1))
+        if n + skew < rows:
+            seq.append(("A", n + skew))
         seq.append(("B", n))
     return seq
 
 
-def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80):
-    """mode: 'fwd' | 'bwd' | 'fused' | 'fused_l2'.  Raises ProtocolError on a stale read or a deadlock."""
+def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80, rbufs=2, skew=1):
+    """mode: 'fwd' | 'bwd' | 'fused' | 'fused_l2'; rbufs row buffers, fused_l2 row skew.
+
+    Raises ProtocolError on a stale read or a deadlock."""
     rng = random.Random(seed)
     ntl = NT // C
     nch = (ntl + tps - 1) // tps
-    R = 2
+    R = rbufs
+    S = skew if mode == "fused_l2" else 1
 
     class CTA:
         pass
@@ -82,6 +86,7 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80)
         c.partfree = [Bar(1) for _ in range(R)]
         c.xbar = [Bar(max(C - 1, 1)) for _ in range(R)]
         c.part = [[None] * NT for _ in range(R)]
+        c.lse = [None] * R
         ctas.append(c)
 
     def ring(i):
@@ -107,7 +112,7 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80)
         if c.hdr[s] != i or c.data[s] != i:
             raise ProtocolError(f"{mode} {where}: slot {s} holds item {c.hdr[s]}/{c.data[s]}, expected {i}")
 
-    sched = block_schedule(mode, rows)
+    sched = block_schedule(mode, rows, S)
     block_index = {blk: b for b, blk in enumerate(sched)}
 
     def item_of(phase, n, ch):
@@ -148,8 +153,11 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80)
             if mode in ("fwd", "fused_l2"):
                 c.empty[s].arrive(share)
         c.rowdone[b].arrive()
+        yield "arrived"
 
     def phase_b(c, w, n):
+        if mode in ("fused", "fused_l2") and c.lse[n % R] != n:
+            raise ProtocolError(f"{mode} phase B of row {n} read the LSE of row {c.lse[n % R]}")
         for l in tiles_of(w, n):
             ch, share = chunk_of(l)
             i = item_of("A" if mode == "fused" else "B", n, ch)
@@ -168,10 +176,11 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80)
             for n in range(rows):
                 yield from phase_a(c, w, n)
         else:
-            yield from phase_a(c, w, 0)
+            for n in range(min(S, rows)):
+                yield from phase_a(c, w, n)
             for n in range(rows):
-                if n + 1 < rows:
-                    yield from phase_a(c, w, n + 1)
+                if n + S < rows:
+                    yield from phase_a(c, w, n + S)
                 yield from wait(c.lseready[n % R], (n // R) & 1)
                 yield from phase_b(c, w, n)
 
@@ -190,6 +199,7 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80)
             if any(v != n for v in c.part[b]):
                 raise ProtocolError(f"{mode} fold of row {n} saw partials of rows {sorted(set(c.part[b]))}")
             yield "fold"
+            c.lse[b] = n
             if mode in ("fused", "fused_l2"):
                 c.lseready[b].arrive()
             c.partfree[b].arrive()

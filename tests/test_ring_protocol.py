@@ -10,7 +10,7 @@ finds it); with the check, no configuration reads a stale slot or deadlocks.
 """
 import pytest
 
-from ring_protocol_model import ProtocolError, simulate
+from ring_protocol_model import ProtocolError, block_schedule, simulate
 
 SMEM_OPTIN = 232448
 
@@ -28,9 +28,14 @@ def layout(ns, slot_bytes, nt, rbufs=2):
     return align(off, 128)
 
 
+def row_bufs(mode, nt):
+    return 2 if mode in ("bwd", "fused") else (4 if nt <= 256 else 2)
+
+
 def plan(mode, vtp, v_padded, nt):
     """(C, tps, NS) as the host planner picks them."""
     w = v_padded // nt
+    rb = row_bufs(mode, nt)
     budget = SMEM_OPTIN - 1024
     tps_target = 1 if w >= 8192 else 8192 // w
 
@@ -40,7 +45,7 @@ def plan(mode, vtp, v_padded, nt):
     def max_slots(sb):
         best = 0
         for ns in range(1, 97):
-            if layout(ns, sb, nt) <= budget:
+            if layout(ns, sb, nt, rb) <= budget:
                 best = ns
         return best
 
@@ -64,6 +69,48 @@ def plan_l2(vtp, v_padded, nt):
     return plan("fwd", vtp, v_padded, nt)
 
 
+def l2_skew(vtp, v_padded, nt, sm_count=152, reuse_bytes=64 << 20):
+    """Rows of skew of the L2-assisted fused mode, as the host planner picks them."""
+    w = v_padded // nt
+    fit = reuse_bytes // (-(-nt // vtp) * w * 2 * sm_count)
+    return max(1, min(fit - 1, row_bufs("fused_l2", nt) - 1))
+
+
+def kernel_block_of(n, phase_b, R, S):
+    """The kernel's closed form of a block's position (block_of in logp_stream.cu)."""
+    S0, P = min(S, R), max(R - S, 0)
+    if not phase_b:
+        return n if n < S0 else S0 + 2 * (n - S)
+    return S0 + 2 * n + 1 if n < P else S0 + 2 * P + (n - P)
+
+
+def kernel_block_row(j, R, S):
+    """The kernel's inverse (block_row in logp_stream.cu): block j -> (row, phase B)."""
+    S0, P = min(S, R), max(R - S, 0)
+    if j < S0:
+        return j, False
+    jj = j - S0
+    if jj < 2 * P:
+        return (jj // 2, True) if jj & 1 else (jj // 2 + S, False)
+    return P + (jj - 2 * P), True
+
+
+def test_kernel_block_numbering_matches_the_schedule():
+    for R in range(0, 12):
+        for S in range(1, 8):
+            sched = block_schedule("fused_l2", R, S)
+            assert len(sched) == 2 * R
+            for j, (ph, n) in enumerate(sched):
+                assert kernel_block_of(n, ph == "B", R, S) == j
+                assert kernel_block_row(j, R, S) == (n, ph == "B")
+
+
+def test_l2_skew_at_the_benchmark_shapes():
+    # 152 SMs, 152576 x 64 tiles: virtual TP 1 and 2 keep one row of skew;
+    # 4 and 8 take three (bounded by four row buffers)
+    assert [l2_skew(v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 3, 3]
+
+
 CONFIGS = [(mode, vtp) for mode in ("fwd", "bwd", "fused", "fused_l2") for vtp in (1, 2, 4, 8)
            if not (mode == "bwd" and vtp > 1)]
 
@@ -71,8 +118,9 @@ CONFIGS = [(mode, vtp) for mode in ("fwd", "bwd", "fused", "fused_l2") for vtp i
 @pytest.mark.parametrize("mode,vtp", CONFIGS)
 def test_ring_protocol_reads_only_landed_slots(mode, vtp):
     C, tps, ns = plan_l2(vtp, 152576, 64) if mode == "fused_l2" else plan(mode, vtp, 152576, 64)
+    skew = l2_skew(vtp, 152576, 64) if mode == "fused_l2" else 1
     for seed in range(3):
-        simulate(mode, rows=24, C=C, NT=64, tps=tps, NS=ns, W=16, seed=seed)
+        simulate(mode, rows=24, C=C, NT=64, tps=tps, NS=ns, W=16, seed=seed, rbufs=row_bufs(mode, 64), skew=skew)
 
 
 def test_planner_replay_matches_the_benchmark_shapes():
@@ -87,6 +135,26 @@ def test_l2_fused_schedule_progresses_with_tiny_rings(ns):
     for C in (1, 2, 4):
         for tps in (1, 3):
             simulate("fused_l2", rows=7, C=C, NT=64, tps=tps, NS=ns, W=16, seed=10 * ns + C)
+
+
+@pytest.mark.parametrize("rbufs,skew", [(2, 1), (4, 1), (4, 3), (8, 3), (8, 7)])
+def test_deeper_row_pipelines(rbufs, skew):
+    for mode in ("fwd", "fused_l2"):
+        for C, tps in ((1, 3), (8, 3)):
+            simulate(mode, rows=20, C=C, NT=64, tps=tps, NS=15, W=16, seed=rbufs * 10 + skew,
+                     rbufs=rbufs, skew=skew)
+
+
+def test_skew_needs_more_row_buffers_than_rows_in_flight():
+    # With as many row buffers as the skew, the fold of row n+S can
+    # overwrite row n's LSE before a slow warp reads it in phase B.
+    found = 0
+    for seed in range(12):
+        try:
+            simulate("fused_l2", rows=16, C=2, NT=64, tps=1, NS=40, W=16, seed=seed, rbufs=2, skew=2)
+        except ProtocolError:
+            found += 1
+    assert found > 0
 
 
 def test_without_the_issued_item_check_the_model_finds_stale_reads():

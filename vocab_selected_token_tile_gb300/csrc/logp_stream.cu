@@ -63,6 +63,7 @@ constexpr int kProducerWarp = kConsumerWarps + 1;  // issues the bulk copies
 constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kMaxSlots = 96;
 constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the final drain of own copies
+constexpr int64_t kL2ReuseBytes = 64ll << 20;  // logits held in L2 between the two reads of kModeFusedL2
 
 struct SlotHdr {  // row metadata the producer writes beside each slot
     int64_t target;
@@ -91,6 +92,8 @@ struct Params {
     uint64_t wait_ns;
     int32_t NT, W, C, mask_mode, NS, slot_bytes;
     int32_t tps;  // tiles per ring slot (consecutive tiles of one row share a slot when narrow)
+    int32_t rbufs, rb_shift;  // row buffers of the fold (a power of two) and its log2
+    int32_t skew;             // kModeFusedL2: phase A runs `skew` rows ahead of phase B (< rbufs)
     uint32_t off_full, off_empty, off_hdr, off_seq, off_part, off_fold, off_rows, off_bars, off_flag;
 };
 
@@ -391,8 +394,13 @@ __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* 
 
 // ----------------------------------------------------------------- kernel roles
 
-// Per-row buffers of the fold: row n uses buffer n % kRowBufs.
-constexpr int kRowBufs = 2;
+// Per-row buffers of the fold: row n uses buffer n % rbufs, and its
+// mbarriers complete once per use, so a wait for row n takes parity
+// (n / rbufs) & 1.
+constexpr int kMaxRowBufs = 8;
+
+__device__ __forceinline__ int row_buf(const Params& p, int64_t n) { return (int)(n & (p.rbufs - 1)); }
+__device__ __forceinline__ uint32_t row_par(const Params& p, int64_t n) { return (uint32_t)((n >> p.rb_shift) & 1); }
 
 struct Ctx {
     int warp, lane;
@@ -431,28 +439,35 @@ __device__ __forceinline__ RingPos ring_add(RingPos r, int k, int NS) {
 }
 
 // The producer issues blocks of nch items (one row's chunks for one phase).
-// kModeFwd / kModeBwd / kModeFused: block n is row n.  kModeFusedL2 follows
-// the consumers' skewed order A(0), A(1), B(0), A(2), B(1), ..., B(R-1).
-__device__ __forceinline__ int64_t block_of(int MODE, int64_t n, bool phase_b, int64_t R) {
+// kModeFwd / kModeBwd / kModeFused: block n is row n.  kModeFusedL2 with
+// skew S follows the consumers' order: A(0), ..., A(S-1), then A(n+S), B(n)
+// for n = 0, 1, ... (A(n+S) only while n+S < R).  With S0 = min(S, R) and
+// P = max(R - S, 0) full pairs: A(n) is block n for n < S0 and S0 + 2(n-S)
+// after; B(n) is block S0 + 2n + 1 for n < P and S0 + 2P + (n - P) after.
+__device__ __forceinline__ int64_t block_of(int MODE, int64_t n, bool phase_b, int64_t R, int64_t S) {
     if (MODE != kModeFusedL2) return n;
-    if (!phase_b) return n == 0 ? 0 : 2 * n - 1;
-    return n == R - 1 ? 2 * R - 1 : 2 * n + 2;
+    const int64_t S0 = S < R ? S : R;
+    const int64_t P = R > S ? R - S : 0;
+    if (!phase_b) return n < S0 ? n : S0 + 2 * (n - S);
+    return n < P ? S0 + 2 * n + 1 : S0 + 2 * P + (n - P);
 }
 
 // Inverse of block_of for kModeFusedL2: block j -> (row, is phase B).
-__device__ __forceinline__ void block_row(int64_t j, int64_t R, int64_t& n, bool& phase_b) {
-    if (j == 0) {
-        n = 0;
+__device__ __forceinline__ void block_row(int64_t j, int64_t R, int64_t S, int64_t& n, bool& phase_b) {
+    const int64_t S0 = S < R ? S : R;
+    const int64_t P = R > S ? R - S : 0;
+    if (j < S0) {
+        n = j;
         phase_b = false;
-    } else if (j == 2 * R - 1) {
-        n = R - 1;
-        phase_b = true;
-    } else if (j & 1) {
-        n = (j + 1) / 2;
-        phase_b = false;
+        return;
+    }
+    const int64_t jj = j - S0;
+    if (jj < 2 * P) {
+        phase_b = (jj & 1) != 0;
+        n = phase_b ? jj / 2 : jj / 2 + S;
     } else {
-        n = (j - 2) / 2;
         phase_b = true;
+        n = P + (jj - 2 * P);
     }
 }
 
@@ -495,7 +510,7 @@ __device__ void producer(const Params& p, const Ctx& x) {
     for (int64_t j = 0; j < nblocks && !aborted; ++j) {
         int64_t n = j;
         bool second = false;  // kModeFusedL2: the phase-B copy of row n
-        if (MODE == kModeFusedL2) block_row(j, x.nrows, n, second);
+        if (MODE == kModeFusedL2) block_row(j, x.nrows, p.skew, n, second);
         if (n - meta_base >= 32) {
             prev = cur;
             meta_base += 32;
@@ -580,8 +595,8 @@ template <int MODE>
 __device__ void fold_warp(const Params& p, const Ctx& x) {
     const int lane = x.lane;
     for (int64_t n = 0; n < x.nrows; ++n) {
-        const int b = (int)(n % kRowBufs);
-        const uint32_t par = (uint32_t)((n / kRowBufs) & 1);
+        const int b = row_buf(p, n);
+        const uint32_t par = row_par(p, n);
         float2* part = x.part + (size_t)b * p.NT;
         bool ok = x.wt.warp_wait(x.rowdone0 + 8u * b, par);
         if (p.C > 1) {
@@ -673,9 +688,9 @@ template <int MODE>
 __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0) {
     constexpr int W = kConsumerWarps;
     const int lane = x.lane;
-    const int b = (int)(n % kRowBufs);
+    const int b = row_buf(p, n);
     bool ok = true;
-    if (n >= kRowBufs) ok = x.wt.warp_wait(x.partfree0 + 8u * b, (uint32_t)((n / kRowBufs - 1) & 1));
+    if (n >= p.rbufs) ok = x.wt.warp_wait(x.partfree0 + 8u * b, row_par(p, n - p.rbufs));
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
     const int slot_elems = p.slot_bytes / 2;
     const RingPos rb = ring_of(item0, p.NS);
@@ -754,27 +769,29 @@ __device__ void consumer(const Params& p, const Ctx& x) {
     static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0, "consumer warp count must be a power of two");
     const int64_t R = x.nrows;
     const uint32_t nch = (uint32_t)x.nch;
-    auto item_a = [&](int64_t n) { return (uint32_t)block_of(MODE, n, false, R) * nch; };
-    auto item_b = [&](int64_t n) { return (uint32_t)block_of(MODE, n, MODE != kModeFused, R) * nch; };
+    const int64_t S = (MODE == kModeFusedL2) ? p.skew : 1;
+    auto item_a = [&](int64_t n) { return (uint32_t)block_of(MODE, n, false, R, S) * nch; };
+    auto item_b = [&](int64_t n) { return (uint32_t)block_of(MODE, n, MODE != kModeFused, R, S) * nch; };
     if constexpr (MODE == kModeBwd) {
         for (int64_t n = 0; n < R; ++n)
             if (!phase_b<MODE>(p, x, n, item_b(n), 0.f)) break;
     } else if constexpr (MODE == kModeFwd) {
         for (int64_t n = 0; n < R; ++n) phase_a<MODE>(p, x, n, item_a(n));
     } else {
-        // Skewed order A(0), A(1), B(0), A(2), B(1), ...: the fold of row n
-        // overlaps phase A of row n+1.  kModeFused keeps two rows of slots
-        // resident; kModeFusedL2 copies each row a second time for phase B.
-        bool ok_cur = R > 0 ? phase_a<MODE>(p, x, 0, item_a(0)) : true;
+        // Skewed order A(0), ..., A(S-1), then A(n+S), B(n): the fold of row
+        // n overlaps phase A of rows n+1..n+S.  kModeFused (S = 1) keeps two
+        // rows of slots resident; kModeFusedL2 copies each row a second time
+        // for phase B.  rbufs > S keeps rows[b].lse of row n until every warp
+        // has read it: row n + rbufs comes after B(n) in every warp's order.
+        for (int64_t n = 0; n < S && n < R; ++n) phase_a<MODE>(p, x, n, item_a(n));
         for (int64_t n = 0; n < R; ++n) {
-            bool ok_next = true;
-            if (n + 1 < R) ok_next = phase_a<MODE>(p, x, n + 1, item_a(n + 1));
-            const int b = (int)(n % kRowBufs);
-            const bool ready = x.wt.warp_wait(x.lseready0 + 8u * b, (uint32_t)((n / kRowBufs) & 1));
-            // After an expired wait the slot headers may be stale: skip the
-            // writes (the status word already says RLK_ERR_TIMEOUT).
-            if (ready && ok_cur && !*x.wt.abort_flag) phase_b<MODE>(p, x, n, item_b(n), x.rows[b].lse);
-            ok_cur = ok_next;
+            if (n + S < R) phase_a<MODE>(p, x, n + S, item_a(n + S));
+            const int b = row_buf(p, n);
+            const bool ready = x.wt.warp_wait(x.lseready0 + 8u * b, row_par(p, n));
+            // A failed wait anywhere sets the abort flag; the slot headers may
+            // then be stale, so skip the writes (the status word already says
+            // RLK_ERR_TIMEOUT).
+            if (ready && !*x.wt.abort_flag) phase_b<MODE>(p, x, n, item_b(n), x.rows[b].lse);
         }
     }
 }
@@ -797,9 +814,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     x.full0 = x.sbase + p.off_full;
     x.empty0 = x.sbase + p.off_empty;
     x.rowdone0 = x.sbase + p.off_bars;
-    x.lseready0 = x.rowdone0 + 8u * kRowBufs;
-    x.partfree0 = x.lseready0 + 8u * kRowBufs;
-    x.xbar0 = x.partfree0 + 8u * kRowBufs;
+    x.lseready0 = x.rowdone0 + 8u * p.rbufs;
+    x.partfree0 = x.lseready0 + 8u * p.rbufs;
+    x.xbar0 = x.partfree0 + 8u * p.rbufs;
     x.hdr = reinterpret_cast<SlotHdr*>(smem + p.off_hdr);
     x.seq = reinterpret_cast<volatile uint32_t*>(smem + p.off_seq);
     x.part = reinterpret_cast<float2*>(smem + p.off_part);
@@ -816,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
             mbar_init(x.empty0 + 8u * s, (uint32_t)p.tps);
             x.seq[s] = 0xFFFFFFFFu;
         }
-        for (int b = 0; b < kRowBufs; ++b) {
+        for (int b = 0; b < p.rbufs; ++b) {
             mbar_init(x.rowdone0 + 8u * b, kConsumerWarps);
             mbar_init(x.lseready0 + 8u * b, 1);
             mbar_init(x.partfree0 + 8u * b, 1);
@@ -894,13 +911,13 @@ uint32_t layout(Params& p, int NS) {
     p.off_seq = off;
     off += 4u * NS;
     p.off_part = align_up(off, 16);
-    off = p.off_part + (uint32_t)kRowBufs * 8u * (uint32_t)p.NT;
+    off = p.off_part + (uint32_t)p.rbufs * 8u * (uint32_t)p.NT;
     p.off_fold = off;
     off += 8u * (uint32_t)p.NT;
     p.off_rows = align_up(off, 16);
-    off = p.off_rows + (uint32_t)kRowBufs * (uint32_t)sizeof(RowShared);
+    off = p.off_rows + (uint32_t)p.rbufs * (uint32_t)sizeof(RowShared);
     p.off_bars = align_up(off, 8);
-    off = p.off_bars + 4u * 8u * (uint32_t)kRowBufs;  // rowdone, lseready, partfree, xbar
+    off = p.off_bars + 4u * 8u * (uint32_t)p.rbufs;  // rowdone, lseready, partfree, xbar
     p.off_flag = off;
     off += 16u;
     return align_up(off, 128);
@@ -961,6 +978,29 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         if (!(sch && std::string(sch) == "resident")) mode = kModeFusedL2;
     }
     int C = (mode == kModeBwd) ? 1 : c.virtual_tp;
+    // Row buffers of the fold: more buffers let the fold of a row lag further
+    // behind phase A (short shards give short rows per CTA); they cost
+    // rbufs * 8 * num_tiles bytes of shared memory.
+    {
+        int rb = env_int("RLK_ROW_BUFS", c.num_tiles <= 256 ? 4 : 2);
+        rb = rb >= 8 ? 8 : rb >= 4 ? 4 : 2;
+        if (mode == kModeBwd || mode == kModeFused) rb = 2;
+        p.rbufs = rb;
+        p.rb_shift = rb == 8 ? 3 : rb == 4 ? 2 : 1;
+        // kModeFusedL2 skew: the rows of phase A between a row's two copies
+        // must stay in L2.  Keep (skew + 1) rows of every SM's shard within
+        // kL2ReuseBytes, at least one row of skew, and skew < rbufs.
+        int skew = 1;
+        if (mode == kModeFusedL2) {
+            const int64_t shard_bytes = (int64_t)((c.num_tiles + C - 1) / C) * p.W * 2;
+            const int64_t gpu_row = shard_bytes * di.sm_count;
+            int fit = (int)(kL2ReuseBytes / (gpu_row > 0 ? gpu_row : 1));
+            skew = env_int("RLK_FUSED_SKEW", fit - 1);
+            if (skew > rb - 1) skew = rb - 1;
+            if (skew < 1) skew = 1;
+        }
+        p.skew = skew;
+    }
     int NS = 0;
     p.C = C;
     if (mode == kModeFused) {
