@@ -252,7 +252,14 @@ def run_ours(args, ws, rank, local):
     ms_per_step = total_ms / args.steps
 
     hbm_peak, bf16_peak, peak_kind = measured_peaks()
-    alg_bytes = T * (2 * Vr + 2 * Vp) + T * (8 + 1 + 4 + 4 + 4)
+    n_active = int(active.sum())
+    fwd_bytes = T * 2 * Vr + T * (8 + 1 + 4 + 4)              # logits, targets, mask, logp, LSE
+    bwd_bytes = n_active * 2 * Vr + T * 2 * Vp + T * (8 + 1 + 4 + 4)  # logits of active rows, dlogits, g, LSE
+    alg_bytes = {"fused": T * (2 * Vr + 2 * Vp) + T * (8 + 1 + 4 + 4 + 4),
+                 "fwd": fwd_bytes, "split": fwd_bytes + bwd_bytes}[args.path]
+    kernel = {"fused": "stream_kernel<kModeFusedL2>", "fwd": "stream_kernel<kModeFwd>",
+              "split": "stream_kernel<kModeFwd> + stream_kernel<kModeBwd>"}[args.path]
+    launches_per_step = 2 if args.path == "split" else 1
     achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
     result = {
         "metric": METRIC,
@@ -270,7 +277,7 @@ def run_ours(args, ws, rank, local):
         "config": {
             "workload": f"{w.name}: {args.path} fwd+bwd, T={T} ({w.batch}x{w.seq}) x V_padded={Vp} (V_real={Vr}), "
                         f"64 tiles, virtual TP {args.vtp}, g = A_b*mask/active_count",
-            "active_tokens": int(active.sum()),
+            "active_tokens": n_active,
             "parallelism": f"dp{ws} (independent rows, no collective)" if ws > 1 else "single GPU",
             "l2": "inputs (20.0 GB logits) larger than L2; no flush",
             "alg_bytes_per_step": alg_bytes,
@@ -282,12 +289,12 @@ def run_ours(args, ws, rank, local):
             "peak": hbm_peak,
             "unit": "GB/s",
             "frac": achieved / hbm_peak,
-            "traffic": recorded_traffic("stream_kernel<fused>", "grpo"),
+            "traffic": recorded_traffic(kernel, w.name) if args.path != "split" else None,
             "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)",
-            "kernel": "stream_kernel<kModeFused>",
+            "kernel": kernel,
         },
         "clocks": clk,
-        "gpu_launches": args.steps,
+        "gpu_launches": launches_per_step * args.steps,
     }
     if args.extra and rank == 0:
         result["extra"] = extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, Vp, args)

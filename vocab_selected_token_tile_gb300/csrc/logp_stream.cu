@@ -46,6 +46,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <cstdio>
 #include <cstdlib>
 #include <mutex>
 #include <string>
@@ -1065,6 +1066,11 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     }
     if (clusters > p.T) clusters = p.T;
     cfg.gridDim = dim3((unsigned)(clusters * p.C), 1, 1);
+    if (env_int("RLK_VERBOSE", 0))
+        std::fprintf(stderr,
+                     "rlk stream plan: mode %d, %lld clusters x %d CTAs, %d tiles/copy, %d slots of %d B, "
+                     "%d row buffers, skew %d, %u B shared memory\n",
+                     mode, (long long)clusters, p.C, p.tps, p.NS, p.slot_bytes, p.rbufs, p.skew, smem);
     e = cudaLaunchKernelEx(&cfg, kfn, p);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(e));
     return RLK_OK;
