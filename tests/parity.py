@@ -5,6 +5,8 @@ GPU side gets the same bits copied to the device, or generated there by the
 synth device build (checked bit-identical in test_parity_gpu).
 """
 import hashlib
+import json
+import os
 
 import numpy as np
 import torch
@@ -14,6 +16,15 @@ import vocab_selected_token_tile_gb300 as rlk
 
 LSE_TOL = 1e-4     # LSE and logp max abs error against the FP64 oracle
 DL_TOL = 1e-2      # dlogits max abs error (BF16 output)
+
+
+def report(kind, value):
+    """Appends a measured error to the JSON-lines file named by RLK_PARITY_REPORT, if set."""
+    path = os.environ.get("RLK_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0],
+                                "kind": kind, "max_abs": float(value)}) + "\n")
 
 
 def to_dev(bits):
@@ -48,6 +59,8 @@ def check_fwd(bits, tgt, active, v_real, logp, lse, tol=LSE_TOL):
     assert np.array_equal(np.isfinite(lse), fin)
     err_lse = np.max(np.abs(lse[fin] - ref_lse[fin])) if fin.any() else 0.0
     err_logp = np.max(np.abs(logp[active & fin] - ref_logp[active & fin])) if (active & fin).any() else 0.0
+    report("lse", err_lse)
+    report("logp", err_logp)
     assert err_lse <= tol, f"LSE max abs {err_lse}"
     assert err_logp <= tol, f"logp max abs {err_logp}"
     # inactive rows: exactly +0.0
@@ -71,6 +84,7 @@ def check_dlogits(bits, tgt, active, g, v_real, v_padded, dl_bits, rows=None):
         assert np.all(err <= bound), f"dlogits outside the BF16 rounding bound at rows {rr[np.any(err > bound, 1)]}"
         assert np.all(dl_bits[rr][:, v_real:v_padded] == 0), "padded columns must be exactly 0"
         assert np.all(dl_bits[rr][~active[rr]][:, :v_padded] == 0), "inactive rows must be exactly 0"
+    report("dlogits", worst)
     assert worst <= DL_TOL
     return worst
 

@@ -13,6 +13,7 @@ import oracle
 import synth
 from oracle.lmhead import lmhead_dlogits
 import vocab_selected_token_tile_gb300 as rlk
+from parity import report
 
 pytestmark = pytest.mark.gpu
 
@@ -20,6 +21,13 @@ if not torch.cuda.is_available():  # pragma: no cover
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 TOL = 1e-4
+
+
+def close(kind, got, ref):
+    """Max abs error of an FP32 output against the FP64 oracle, within TOL."""
+    err = float(np.max(np.abs(np.asarray(got, dtype=np.float64) - ref)))
+    report("lmhead_" + kind, err)
+    assert err <= TOL, f"{kind} max abs {err}"
 
 
 def make(T, H, v_real, v_padded, seed, w_sigma=0.2):
@@ -63,8 +71,8 @@ def test_lmhead_small_cases(case):
         logp, lse = run(c, hb, wb, tgt, mask)
         torch.cuda.synchronize()
         lp, ls = logp.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
-        assert np.max(np.abs(ls - ref_lse)) <= TOL
-        assert np.max(np.abs(lp - ref_logp)) <= TOL
+        close("lse", ls, ref_lse)
+        close("logp", lp, ref_logp)
         assert np.all(lp[mask == 0] == 0.0) and not np.any(np.signbit(lp[mask == 0]))
         outs.add((lp.tobytes(), ls.tobytes()))
     assert len(outs) == 1, "virtual TP outputs differ"
@@ -80,8 +88,8 @@ def test_lmhead_ignore_index_and_errors():
     active = tgt != -100
     ref_logp, ref_lse, _ = oracle.lmhead_forward(hb, wb, np.where(active, tgt, 0), active, v_real)
     torch.cuda.synchronize()
-    assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= TOL
-    assert np.max(np.abs(logp.cpu().numpy() - ref_logp)) <= TOL
+    close("lse", lse.cpu().numpy(), ref_lse)
+    close("logp", logp.cpu().numpy(), ref_logp)
     bad = tgt.copy()
     bad[np.nonzero(active)[0][0]] = v_real + 3  # an active target in the padding
     with pytest.raises(rlk.RlkError) as ei:
@@ -122,8 +130,8 @@ def test_lmhead_full_shape_sampled_rows():
     assert np.array_equal(hd[torch.from_numpy(rows).cuda()].cpu().numpy().view(np.uint16), hb)
     ref_logp, ref_lse, _ = oracle.lmhead_forward(hb, wb, tgt[rows], mask[rows] != 0, v_real)
     logp, lse = res[1]
-    assert np.max(np.abs(lse.cpu().numpy()[rows] - ref_lse)) <= TOL
-    assert np.max(np.abs(logp.cpu().numpy()[rows] - ref_logp)) <= TOL
+    close("lse", lse.cpu().numpy()[rows], ref_lse)
+    close("logp", logp.cpu().numpy()[rows], ref_logp)
 
 
 def grad_bounds(hb, wb, tgt, active, g, v_real):
@@ -158,8 +166,8 @@ def test_lmhead_backward_small_cases(case):
         logp, lse, dh, dw = rlk.logp_fused_lmhead(c, dev(hb), dev(wb), torch.from_numpy(tgt).cuda(),
                                                   torch.from_numpy(mask).cuda(), grad=torch.from_numpy(g).cuda())
         torch.cuda.synchronize()
-        assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= TOL
-        assert np.max(np.abs(logp.cpu().numpy() - ref_logp)) <= TOL
+        close("lse", lse.cpu().numpy(), ref_lse)
+        close("logp", logp.cpu().numpy(), ref_logp)
         dhb = dh.cpu().numpy().view(np.uint16)
         dwb = dw.cpu().numpy().view(np.uint16)
         assert np.all(within(dhb, ref_dh, sc_dh))
