@@ -12,6 +12,14 @@ the item it expects and that nothing deadlocks.
 It mirrors the kernel's waits: full/empty per slot, rowdone/lseready/
 partfree/xbar per row buffer, and the per-slot issued-item number (`seq`)
 that consumers wait for before the full-barrier parity.
+
+The exchange of partials between the C CTAs of a cluster is asynchronous:
+each CTA arms its own xbar barrier with the bytes it expects (one local
+arrival plus expect-tx) and sends its shard to every peer with remote stores
+that complete on the peer's xbar barrier after a random delay.  With
+fold_depth D = 1 the fold warp sends row m before it folds row m - 1.  The
+fold reads the partials over several steps and checks at the end that no
+push of a later row overwrote them.
 """
 import random
 
@@ -58,8 +66,10 @@ def block_schedule(mode, rows, skew=1):
     return seq
 
 
-def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80, rbufs=2, skew=1):
-    """mode: 'fwd' | 'bwd' | 'fused' | 'fused_l2'; rbufs row buffers, fused_l2 row skew.
+def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80, rbufs=2, skew=1,
+             fold_depth=None):
+    """mode: 'fwd' | 'bwd' | 'fused' | 'fused_l2'; rbufs row buffers, fused_l2 row skew;
+    fold_depth (default: the kernel's choice, 1 when C > 1 and rbufs >= 4, else 0).
 
     Raises ProtocolError on a stale read or a deadlock."""
     rng = random.Random(seed)
@@ -67,6 +77,8 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
     nch = (ntl + tps - 1) // tps
     R = rbufs
     S = skew if mode == "fused_l2" else 1
+    D = fold_depth if fold_depth is not None else (1 if C > 1 and rbufs >= 4 else 0)
+    pushes = []  # in flight: [delay, receiver CTA, buffer, tile, row]
 
     class CTA:
         pass
@@ -84,7 +96,7 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
         c.rowdone = [Bar(W) for _ in range(R)]
         c.lseready = [Bar(1) for _ in range(R)]
         c.partfree = [Bar(1) for _ in range(R)]
-        c.xbar = [Bar(max(C - 1, 1)) for _ in range(R)]
+        c.xbar = [Bar(1) for _ in range(R)]
         c.part = [[None] * NT for _ in range(R)]
         c.lse = [None] * R
         ctas.append(c)
@@ -184,25 +196,39 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
                 yield from wait(c.lseready[n % R], (n // R) & 1)
                 yield from phase_b(c, w, n)
 
+    def push(c, m):
+        b, par = m % R, (m // R) & 1
+        yield from wait(c.rowdone[b], par)
+        if C > 1:
+            c.xbar[b].tx += (C - 1) * ntl  # expect-tx, then the local arrival
+            c.xbar[b].arrive()
+            for peer in ctas:
+                if peer is not c:
+                    for k in range(c.rank * ntl, (c.rank + 1) * ntl):
+                        pushes.append([rng.randint(1, max_delay), peer, b, k, c.part[b][k]])
+            yield "push"
+
+    def finish(c, n):
+        b, par = n % R, (n // R) & 1
+        if C > 1:
+            yield from wait(c.xbar[b], par)
+        if any(v != n for v in c.part[b]):
+            raise ProtocolError(f"{mode} fold of row {n} saw partials of rows {sorted(set(c.part[b]))}")
+        yield "fold"
+        yield "fold"
+        if any(v != n for v in c.part[b]):
+            raise ProtocolError(f"{mode} partials of row {n} were overwritten during its fold")
+        c.lse[b] = n
+        if mode in ("fused", "fused_l2"):
+            c.lseready[b].arrive()
+        c.partfree[b].arrive()
+
     def fold(c):
-        for n in range(rows):
-            b, par = n % R, (n // R) & 1
-            yield from wait(c.rowdone[b], par)
-            if C > 1:
-                for peer in ctas:
-                    if peer is not c:
-                        for k in range(c.rank * ntl, (c.rank + 1) * ntl):
-                            peer.part[b][k] = c.part[b][k]
-                        peer.xbar[b].arrive()
-                yield "push"
-                yield from wait(c.xbar[b], par)
-            if any(v != n for v in c.part[b]):
-                raise ProtocolError(f"{mode} fold of row {n} saw partials of rows {sorted(set(c.part[b]))}")
-            yield "fold"
-            c.lse[b] = n
-            if mode in ("fused", "fused_l2"):
-                c.lseready[b].arrive()
-            c.partfree[b].arrive()
+        for m in range(rows + D):
+            if m < rows:
+                yield from push(c, m)
+            if m - D >= 0:
+                yield from finish(c, m - D)
 
     agents = []
     for c in ctas:
@@ -215,6 +241,15 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
     idle = 0
     while live:
         progressed = False
+        for f in pushes:
+            f[0] -= 1
+        for f in [f for f in pushes if f[0] <= 0]:
+            pushes.remove(f)
+            _, peer, b, k, v = f
+            peer.part[b][k] = v
+            peer.xbar[b].tx -= 1
+            peer.xbar[b].check()
+            progressed = True
         for c in ctas:
             for f in c.inflight:
                 f[0] -= 1

@@ -157,6 +157,24 @@ def test_skew_needs_more_row_buffers_than_rows_in_flight():
     assert found > 0
 
 
+def test_pipelined_fold_needs_four_row_buffers():
+    # With the fold one row behind its pushes (D = 1), two row buffers let a
+    # peer's push of row n+2 land in the buffer of row n before row n's
+    # exchange or fold is done; the kernel pipelines only with rbufs >= 4.
+    found = 0
+    for seed in range(12):
+        try:
+            simulate("fwd", rows=24, C=4, NT=64, tps=1, NS=40, W=16, seed=seed, rbufs=2, fold_depth=1,
+                     max_delay=200)
+        except ProtocolError:
+            found += 1
+    assert found > 0
+    for seed in range(4):
+        for mode in ("fwd", "fused_l2"):
+            simulate(mode, rows=24, C=4, NT=64, tps=1, NS=40, W=16, seed=seed, rbufs=4, fold_depth=1,
+                     max_delay=200, skew=3 if mode == "fused_l2" else 1)
+
+
 def test_without_the_issued_item_check_the_model_finds_stale_reads():
     C, tps, ns = plan("bwd", 1, 152576, 64)
     found = 0

@@ -588,56 +588,94 @@ __device__ void producer(const Params& p, const Ctx& x) {
     }
 }
 
-// The fold warp: for each row, once every consumer warp of this CTA has put
-// its tiles' partials in part[b], push this CTA's shard of partials into
-// each peer CTA (virtual TP > 1), wait for the peers' shards, fold all tiles
-// in index order, write the outputs, and release the buffer.
+// The fold warp, for each row n of this CTA:
+//  * push: once every consumer warp has put its tiles' partials in part[b],
+//    arm this CTA's xbar[b] with the bytes the peers will send (one local
+//    arrival + expect-tx) and send this CTA's shard of partials to every peer
+//    CTA with asynchronous remote stores that complete on the peer's xbar[b]
+//    (virtual TP > 1);
+//  * finish: wait for xbar[b] (every peer's shard has landed), fold all tiles
+//    in index order, write the outputs and release the buffer.
+// With four or more row buffers the warp pushes row m before it finishes row
+// m - 1 (depth 1), so the exchange latency of one row overlaps the fold of
+// the previous one.  Ordering: a peer sends row n + rbufs into buffer b only
+// after it has finished row n + rbufs - 2, which needs this CTA's push of
+// that row, which this warp issues only after finishing row n + rbufs - 3
+// >= n when rbufs >= 4; so xbar[b] has completed row n's phase and its fold
+// has read part[b] before any byte of row n + rbufs arrives.  With fewer
+// buffers the warp finishes each row before pushing the next (depth 0).
+template <int MODE>
+__device__ bool push_row(const Params& p, const Ctx& x, int64_t n) {
+    const int lane = x.lane;
+    const int b = row_buf(p, n);
+    const bool ok = x.wt.warp_wait(x.rowdone0 + 8u * b, row_par(p, n));
+    if (p.C > 1 && ok) {
+        float2* part = x.part + (size_t)b * p.NT;
+        const int peers = p.C - 1;
+        // the peers' shards: every tile but this CTA's own
+        if (lane == 0) mbar_arrive_expect_tx(x.xbar0 + 8u * b, (uint32_t)((p.NT - x.ntl) * 8));
+        for (int i = lane; i < peers * x.ntl; i += 32) {
+            const int pi = i / x.ntl;
+            const int kk = x.k0 + (i - pi * x.ntl);
+            const uint32_t peer = (uint32_t)pi < x.rank ? (uint32_t)pi : (uint32_t)pi + 1u;
+            const float2 v = part[kk];
+            st_async_f32x2(mapa_shared(smem_u32(&part[kk]), peer), v.x, v.y,
+                           mapa_shared(x.xbar0 + 8u * b, peer));
+        }
+    }
+    return ok;
+}
+
+template <int MODE>
+__device__ void finish_row(const Params& p, const Ctx& x, int64_t n, bool ok) {
+    const int lane = x.lane;
+    const int b = row_buf(p, n);
+    float2* part = x.part + (size_t)b * p.NT;
+    if (p.C > 1) ok = x.wt.warp_wait(x.xbar0 + 8u * b, row_par(p, n), true) && ok;
+    if (!ok) return;
+    const float lse_v = fold_tiles(part, p.NT, x.fold, lane);
+    const int64_t row = x.q + n * x.G;
+    if (p.a.partials && x.rank == 0) {
+        float2* out = reinterpret_cast<float2*>(p.a.partials) + row * p.NT;
+        for (int k = lane; k < p.NT; k += 32) out[k] = part[k];
+    }
+    __syncwarp();
+    if (lane == 0) {
+        RowShared& rs = x.rows[b];
+        const bool active = rs.active != 0;
+        const int64_t t = rs.target;
+        if (x.rank == 0) {
+            p.a.lse[row] = lse_v;
+            if (!active) {
+                p.a.logp[row] = 0.f;
+            } else if (t < 0 || t >= p.Vr) {
+                p.a.logp[row] = __int_as_float(0x7FC00000);
+                atomicOr(p.a.status, kStatusTargetRange);
+            }
+            if (active && !isfinite(lse_v)) atomicOr(p.a.status, kStatusNonFinite);
+        }
+        if (active && rs.has_xt) p.a.logp[row] = __fsub_rn(rs.xt, lse_v);
+        rs.has_xt = 0;
+        rs.lse = lse_v;
+        if (MODE == kModeFused || MODE == kModeFusedL2) mbar_arrive(x.lseready0 + 8u * b);
+        mbar_arrive(x.partfree0 + 8u * b);
+    }
+}
+
 template <int MODE>
 __device__ void fold_warp(const Params& p, const Ctx& x) {
-    const int lane = x.lane;
-    for (int64_t n = 0; n < x.nrows; ++n) {
-        const int b = row_buf(p, n);
-        const uint32_t par = row_par(p, n);
-        float2* part = x.part + (size_t)b * p.NT;
-        bool ok = x.wt.warp_wait(x.rowdone0 + 8u * b, par);
-        if (p.C > 1) {
-            if (ok && lane < p.C && (uint32_t)lane != x.rank) {
-                for (int kk = x.k0; kk < x.k0 + x.ntl; ++kk) {
-                    const float2 v = part[kk];
-                    st_cluster_f32x2(mapa_shared(smem_u32(&part[kk]), (uint32_t)lane), v.x, v.y);
-                }
-                mbar_arrive_remote(mapa_shared(x.xbar0 + 8u * b, (uint32_t)lane));
-            }
-            __syncwarp();
-            ok = x.wt.warp_wait(x.xbar0 + 8u * b, par, true) && ok;
-        }
-        if (!ok) continue;
-        const float lse_v = fold_tiles(part, p.NT, x.fold, lane);
-        const int64_t row = x.q + n * x.G;
-        if (p.a.partials && x.rank == 0) {
-            float2* out = reinterpret_cast<float2*>(p.a.partials) + row * p.NT;
-            for (int k = lane; k < p.NT; k += 32) out[k] = part[k];
-        }
-        __syncwarp();
-        if (lane == 0) {
-            RowShared& rs = x.rows[b];
-            const bool active = rs.active != 0;
-            const int64_t t = rs.target;
-            if (x.rank == 0) {
-                p.a.lse[row] = lse_v;
-                if (!active) {
-                    p.a.logp[row] = 0.f;
-                } else if (t < 0 || t >= p.Vr) {
-                    p.a.logp[row] = __int_as_float(0x7FC00000);
-                    atomicOr(p.a.status, kStatusTargetRange);
-                }
-                if (active && !isfinite(lse_v)) atomicOr(p.a.status, kStatusNonFinite);
-            }
-            if (active && rs.has_xt) p.a.logp[row] = __fsub_rn(rs.xt, lse_v);
-            rs.has_xt = 0;
-            rs.lse = lse_v;
-            if (MODE == kModeFused || MODE == kModeFusedL2) mbar_arrive(x.lseready0 + 8u * b);
-            mbar_arrive(x.partfree0 + 8u * b);
+    const int D = (p.C > 1 && p.rbufs >= 4) ? 1 : 0;
+    bool ok_prev = true, ok_cur = true;
+    for (int64_t m = 0; m < x.nrows + D; ++m) {
+        if (m < x.nrows) ok_cur = push_row<MODE>(p, x, m);
+        if (m - D >= 0) finish_row<MODE>(p, x, m - D, D ? ok_prev : ok_cur);
+        ok_prev = ok_cur;
+    }
+    // After an expired wait some peer stores may still be on their way into
+    // this CTA's shared memory: give them time to land before the kernel ends.
+    if (p.C > 1 && *x.wt.abort_flag) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) {
         }
     }
 }
@@ -838,7 +876,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
             mbar_init(x.rowdone0 + 8u * b, kConsumerWarps);
             mbar_init(x.lseready0 + 8u * b, 1);
             mbar_init(x.partfree0 + 8u * b, 1);
-            mbar_init(x.xbar0 + 8u * b, (uint32_t)(p.C > 1 ? p.C - 1 : 1));
+            mbar_init(x.xbar0 + 8u * b, 1);  // the local arrival (with expect-tx)
             x.rows[b].has_xt = 0;
         }
         *abort_flag = 0;
@@ -953,7 +991,8 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     // One bulk copy per chunk of tps consecutive tiles, about 8192 columns
     // (16 KB): a copy costs about the same issue time whatever its size, so
     // large copies are what keeps the stream near HBM bandwidth.
-    const int tps_target = p.W >= 8192 ? 1 : 8192 / p.W;
+    int tps_target = env_int("RLK_TPS", p.W >= 8192 ? 1 : 8192 / p.W);
+    if (tps_target < 1) tps_target = 1;
     auto set_chunk = [&](int tps) {
         p.tps = tps;
         const int64_t cols = (int64_t)tps * p.W;
@@ -984,7 +1023,7 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     // rbufs * 8 * num_tiles bytes of shared memory.
     {
         int rb = env_int("RLK_ROW_BUFS", c.num_tiles <= 256 ? 4 : 2);
-        rb = rb >= 8 ? 8 : rb >= 4 ? 4 : 2;
+        rb = rb >= kMaxRowBufs ? kMaxRowBufs : rb >= 4 ? 4 : 2;
         if (mode == kModeBwd || mode == kModeFused) rb = 2;
         p.rbufs = rb;
         p.rb_shift = rb == 8 ? 3 : rb == 4 ? 2 : 1;

@@ -190,6 +190,16 @@ __device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
 
+// Asynchronous 8-byte store into another CTA's shared memory (address from
+// mapa); its completion is counted in bytes on that CTA's mbarrier
+// `remote_bar` (also from mapa), with release semantics at cluster scope.
+// The value comes from registers, so the sender's memory may be reused at once.
+__device__ __forceinline__ void st_async_f32x2(uint32_t addr, float a, float b, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+                 "f"(a), "f"(b), "r"(remote_bar)
+                 : "memory");
+}
+
 // All threads of all CTAs of the cluster; release/acquire at cluster scope.
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
