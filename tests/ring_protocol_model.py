@@ -69,7 +69,8 @@ def block_schedule(mode, rows, skew=1):
 def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80, rbufs=2, skew=1,
              fold_depth=None):
     """mode: 'fwd' | 'bwd' | 'fused' | 'fused_l2'; rbufs row buffers, fused_l2 row skew;
-    fold_depth (default: the kernel's choice, 1 when C > 1 and rbufs >= 4, else 0).
+    fold_depth (default: the kernel's choice, 1 when C > 1, rbufs >= 4 and, in the fused
+    modes, skew >= 2; else 0).
 
     Raises ProtocolError on a stale read or a deadlock."""
     rng = random.Random(seed)
@@ -77,7 +78,8 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
     nch = (ntl + tps - 1) // tps
     R = rbufs
     S = skew if mode == "fused_l2" else 1
-    D = fold_depth if fold_depth is not None else (1 if C > 1 and rbufs >= 4 else 0)
+    D = fold_depth if fold_depth is not None else (
+        1 if C > 1 and rbufs >= 4 and (mode == "fwd" or (mode == "fused_l2" and S >= 2)) else 0)
     pushes = []  # in flight: [delay, receiver CTA, buffer, tile, row]
 
     class CTA:

@@ -598,7 +598,9 @@ __device__ void producer(const Params& p, const Ctx& x) {
 //    in index order, write the outputs and release the buffer.
 // With four or more row buffers the warp pushes row m before it finishes row
 // m - 1 (depth 1), so the exchange latency of one row overlaps the fold of
-// the previous one.  Ordering: a peer sends row n + rbufs into buffer b only
+// the previous one.  Pushing row m waits until every consumer warp has done
+// phase A of row m, so in the fused modes the depth stays below the skew:
+// consumers wait for row n's LSE right after phase A of row n + skew.  Ordering: a peer sends row n + rbufs into buffer b only
 // after it has finished row n + rbufs - 2, which needs this CTA's push of
 // that row, which this warp issues only after finishing row n + rbufs - 3
 // >= n when rbufs >= 4; so xbar[b] has completed row n's phase and its fold
@@ -664,7 +666,7 @@ __device__ void finish_row(const Params& p, const Ctx& x, int64_t n, bool ok) {
 
 template <int MODE>
 __device__ void fold_warp(const Params& p, const Ctx& x) {
-    const int D = (p.C > 1 && p.rbufs >= 4) ? 1 : 0;
+    const int D = (p.C > 1 && p.rbufs >= 4 && (MODE == kModeFwd || p.skew >= 2)) ? 1 : 0;
     bool ok_prev = true, ok_cur = true;
     for (int64_t m = 0; m < x.nrows + D; ++m) {
         if (m < x.nrows) ok_cur = push_row<MODE>(p, x, m);
