@@ -13,13 +13,16 @@ It mirrors the kernel's waits: full/empty per slot, rowdone/lseready/
 partfree/xbar per row buffer, and the per-slot issued-item number (`seq`)
 that consumers wait for before the full-barrier parity.
 
-The exchange of partials between the C CTAs of a cluster is asynchronous:
-each CTA arms its own xbar barrier with the bytes it expects (one local
-arrival plus expect-tx) and sends its shard to every peer with remote stores
-that complete on the peer's xbar barrier after a random delay.  With
-fold_depth D = 1 the fold warp sends row m before it folds row m - 1.  The
-fold reads the partials over several steps and checks at the end that no
-push of a later row overwrote them.
+The exchange between the C CTAs of a cluster is asynchronous.  Row n is
+folded by one CTA, the folder F(n) = n mod C: every other CTA sends it its
+shard of partials and its target-logit record with remote stores that
+complete on the folder's xbar barrier after a random delay; the folder folds
+and sends the LSE back to every peer, completing on their lsebar barriers.
+Every CTA arrives once per row on xbar and lsebar (with expect-tx where it
+receives), so both barriers have one phase per row.  A CTA releases a row's
+buffers (partfree) only once it holds the row's LSE.  With fold_depth D = 1
+the fold warp sends row m before it finishes row m - 1.  The folder reads the
+partials over several steps and checks that nothing overwrote them.
 """
 import random
 
@@ -66,11 +69,24 @@ def block_schedule(mode, rows, skew=1):
     return seq
 
 
+def kernel_fold_depth(mode, C, rbufs, skew):
+    """Rows the fold warp sends ahead of the row it finishes (the host planner's rule):
+    none without peers; below the row buffers (the push of row n + D waits for
+    phase A of that row, which waits for the release of row n + D - rbufs);
+    in the fused modes below the skew (consumers wait for row n's LSE right
+    after phase A of row n + skew); at most 3."""
+    if C == 1:
+        return 0
+    d = min(rbufs - 1, 3)
+    if mode in ("fused", "fused_l2"):
+        d = min(d, (skew if mode == "fused_l2" else 1) - 1)
+    return max(d, 0)
+
+
 def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80, rbufs=2, skew=1,
              fold_depth=None):
     """mode: 'fwd' | 'bwd' | 'fused' | 'fused_l2'; rbufs row buffers, fused_l2 row skew;
-    fold_depth (default: the kernel's choice, 1 when C > 1, rbufs >= 4 and, in the fused
-    modes, skew >= 2; else 0).
+    fold_depth (default: the kernel's choice, kernel_fold_depth).
 
     Raises ProtocolError on a stale read or a deadlock."""
     rng = random.Random(seed)
@@ -78,9 +94,11 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
     nch = (ntl + tps - 1) // tps
     R = rbufs
     S = skew if mode == "fused_l2" else 1
-    D = fold_depth if fold_depth is not None else (
-        1 if C > 1 and rbufs >= 4 and (mode == "fwd" or (mode == "fused_l2" and S >= 2)) else 0)
-    pushes = []  # in flight: [delay, receiver CTA, buffer, tile, row]
+    D = fold_depth if fold_depth is not None else kernel_fold_depth(mode, C, rbufs, S)
+    pushes = []  # in flight: [delay, receiver CTA, kind, buffer, index, value]
+
+    def folder(n):
+        return n % C
 
     class CTA:
         pass
@@ -99,8 +117,11 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
         c.lseready = [Bar(1) for _ in range(R)]
         c.partfree = [Bar(1) for _ in range(R)]
         c.xbar = [Bar(1) for _ in range(R)]
+        c.lsebar = [Bar(1) for _ in range(R)]
+        c.xt = [[None] * C for _ in range(R)]
         c.part = [[None] * NT for _ in range(R)]
         c.lse = [None] * R
+        c.xtrow = [None] * R
         ctas.append(c)
 
     def ring(i):
@@ -163,6 +184,7 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
             yield from wait_item(c, s, par, i)
             check_slot(c, s, i, "phase A")
             c.part[b][c.rank * ntl + l] = n
+            c.xtrow[b] = n
             yield "tile"
             if mode in ("fwd", "fused_l2"):
                 c.empty[s].arrive(share)
@@ -202,25 +224,39 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
         b, par = m % R, (m // R) & 1
         yield from wait(c.rowdone[b], par)
         if C > 1:
-            c.xbar[b].tx += (C - 1) * ntl  # expect-tx, then the local arrival
-            c.xbar[b].arrive()
-            for peer in ctas:
-                if peer is not c:
-                    for k in range(c.rank * ntl, (c.rank + 1) * ntl):
-                        pushes.append([rng.randint(1, max_delay), peer, b, k, c.part[b][k]])
+            f = ctas[folder(m)]
+            if f is c:
+                c.xbar[b].tx += (C - 1) * (ntl + 1)  # expect the peers' shards and records
+                c.xbar[b].arrive()
+                c.lsebar[b].arrive()
+            else:
+                c.xbar[b].arrive()
+                c.lsebar[b].tx += 1  # expect the LSE
+                c.lsebar[b].arrive()
+                for k in range(c.rank * ntl, (c.rank + 1) * ntl):
+                    pushes.append([rng.randint(1, max_delay), f, "part", b, k, c.part[b][k]])
+                pushes.append([rng.randint(1, max_delay), f, "xt", b, c.rank, c.xtrow[b]])
             yield "push"
 
     def finish(c, n):
         b, par = n % R, (n // R) & 1
         if C > 1:
             yield from wait(c.xbar[b], par)
-        if any(v != n for v in c.part[b]):
-            raise ProtocolError(f"{mode} fold of row {n} saw partials of rows {sorted(set(c.part[b]))}")
-        yield "fold"
-        yield "fold"
-        if any(v != n for v in c.part[b]):
-            raise ProtocolError(f"{mode} partials of row {n} were overwritten during its fold")
-        c.lse[b] = n
+        if C == 1 or folder(n) == c.rank:
+            if any(v != n for v in c.part[b]) or any(c.xt[b][j] != n for j in range(C) if C > 1 and j != c.rank):
+                raise ProtocolError(f"{mode} fold of row {n} saw partials of rows {sorted(set(map(str, c.part[b])))}")
+            yield "fold"
+            yield "fold"
+            if any(v != n for v in c.part[b]):
+                raise ProtocolError(f"{mode} partials of row {n} were overwritten during its fold")
+            c.lse[b] = n
+            for peer in ctas:
+                if peer is not c:
+                    pushes.append([rng.randint(1, max_delay), peer, "lse", b, 0, n])
+        if C > 1:
+            yield from wait(c.lsebar[b], par)
+        if c.lse[b] != n:
+            raise ProtocolError(f"{mode} CTA {c.rank} released row {n} holding the LSE of row {c.lse[b]}")
         if mode in ("fused", "fused_l2"):
             c.lseready[b].arrive()
         c.partfree[b].arrive()
@@ -247,10 +283,16 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
             f[0] -= 1
         for f in [f for f in pushes if f[0] <= 0]:
             pushes.remove(f)
-            _, peer, b, k, v = f
-            peer.part[b][k] = v
-            peer.xbar[b].tx -= 1
-            peer.xbar[b].check()
+            _, peer, kind, b, k, v = f
+            if kind == "part":
+                peer.part[b][k] = v
+            elif kind == "xt":
+                peer.xt[b][k] = v
+            else:
+                peer.lse[b] = v
+            bar = peer.lsebar[b] if kind == "lse" else peer.xbar[b]
+            bar.tx -= 1
+            bar.check()
             progressed = True
         for c in ctas:
             for f in c.inflight:

@@ -24,12 +24,13 @@ def layout(ns, slot_bytes, nt, rbufs=2):
     off = align(off, 16) + 36 * ns
     off = align(off, 16) + rbufs * 8 * nt + 8 * nt
     off = align(off, 16) + rbufs * 32
-    off = align(off, 8) + 32 * rbufs + 16
+    off = align(off, 16) + rbufs * 8 * 8
+    off = align(off, 8) + 40 * rbufs + 16
     return align(off, 128)
 
 
 def row_bufs(mode, nt):
-    return 2 if mode in ("bwd", "fused") else (4 if nt <= 256 else 2)
+    return 2 if mode in ("bwd", "fused") else (8 if nt <= 128 else 4 if nt <= 256 else 2)
 
 
 def plan(mode, vtp, v_padded, nt):
@@ -73,7 +74,7 @@ def l2_skew(vtp, v_padded, nt, sm_count=152, reuse_bytes=64 << 20):
     """Rows of skew of the L2-assisted fused mode, as the host planner picks them."""
     w = v_padded // nt
     fit = reuse_bytes // (-(-nt // vtp) * w * 2 * sm_count)
-    return max(1, min(fit - 1, row_bufs("fused_l2", nt) - 1))
+    return max(1, min(fit - 1, row_bufs("fused_l2", nt) - 1, 4))
 
 
 def kernel_block_of(n, phase_b, R, S):
@@ -107,8 +108,8 @@ def test_kernel_block_numbering_matches_the_schedule():
 
 def test_l2_skew_at_the_benchmark_shapes():
     # 152 SMs, 152576 x 64 tiles: virtual TP 1 and 2 keep one row of skew;
-    # 4 and 8 take three (bounded by four row buffers)
-    assert [l2_skew(v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 3, 3]
+    # 4 and 8 take four (the cap)
+    assert [l2_skew(v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 4, 4]
 
 
 CONFIGS = [(mode, vtp) for mode in ("fwd", "bwd", "fused", "fused_l2") for vtp in (1, 2, 4, 8)
@@ -157,22 +158,34 @@ def test_skew_needs_more_row_buffers_than_rows_in_flight():
     assert found > 0
 
 
-def test_pipelined_fold_needs_four_row_buffers():
-    # With the fold one row behind its pushes (D = 1), two row buffers let a
-    # peer's push of row n+2 land in the buffer of row n before row n's
-    # exchange or fold is done; the kernel pipelines only with rbufs >= 4.
-    found = 0
-    for seed in range(12):
-        try:
-            simulate("fwd", rows=24, C=4, NT=64, tps=1, NS=40, W=16, seed=seed, rbufs=2, fold_depth=1,
-                     max_delay=200)
-        except ProtocolError:
-            found += 1
-    assert found > 0
-    for seed in range(4):
-        for mode in ("fwd", "fused_l2"):
-            simulate(mode, rows=24, C=4, NT=64, tps=1, NS=40, W=16, seed=seed, rbufs=4, fold_depth=1,
-                     max_delay=200, skew=3 if mode == "fused_l2" else 1)
+@pytest.mark.parametrize("rbufs,skew", [(2, 1), (4, 1), (4, 3), (8, 3), (8, 7)])
+def test_single_folder_exchange_at_every_pipeline_depth(rbufs, skew):
+    # One CTA folds each row and returns the LSE; buffers are reused only once
+    # the LSE of the row they held is back, so every depth the planner allows
+    # (below the row buffers, and below the skew in the fused modes) is safe.
+    for mode in ("fwd", "fused_l2"):
+        top = rbufs - 1 if mode == "fwd" else min(rbufs - 1, skew - 1)
+        for depth in range(0, top + 1):
+            for C in (2, 8):
+                simulate(mode, rows=20, C=C, NT=64, tps=1, NS=24, W=16, seed=rbufs + 7 * depth + C,
+                         rbufs=rbufs, skew=skew, fold_depth=depth, max_delay=150)
+
+
+def test_fold_depth_at_the_row_buffer_count_deadlocks():
+    # The push of row n + D waits for phase A of that row, which needs the
+    # release of row n + D - rbufs: with D = rbufs that release comes after it.
+    with pytest.raises(ProtocolError, match="deadlock"):
+        simulate("fwd", rows=12, C=2, NT=64, tps=1, NS=24, W=16, seed=1, rbufs=2, fold_depth=2)
+
+
+def test_planner_fold_depths():
+    from ring_protocol_model import kernel_fold_depth
+    assert kernel_fold_depth("fwd", 1, 8, 1) == 0
+    assert kernel_fold_depth("fwd", 8, 8, 1) == 3
+    assert kernel_fold_depth("fwd", 2, 4, 1) == 3
+    assert kernel_fold_depth("fused_l2", 2, 8, 1) == 0
+    assert kernel_fold_depth("fused_l2", 8, 8, 3) == 2
+    assert kernel_fold_depth("fused", 4, 2, 1) == 0
 
 
 def test_without_the_issued_item_check_the_model_finds_stale_reads():

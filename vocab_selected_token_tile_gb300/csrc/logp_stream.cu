@@ -65,6 +65,7 @@ constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kMaxSlots = 96;
 constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the final drain of own copies
 constexpr int64_t kL2ReuseBytes = 64ll << 20;  // logits held in L2 between the two reads of kModeFusedL2
+constexpr int kMaxSkew = 4;
 
 struct SlotHdr {  // row metadata the producer writes beside each slot
     int64_t target;
@@ -95,7 +96,8 @@ struct Params {
     int32_t tps;  // tiles per ring slot (consecutive tiles of one row share a slot when narrow)
     int32_t rbufs, rb_shift;  // row buffers of the fold (a power of two) and its log2
     int32_t skew;             // kModeFusedL2: phase A runs `skew` rows ahead of phase B (< rbufs)
-    uint32_t off_full, off_empty, off_hdr, off_seq, off_part, off_fold, off_rows, off_bars, off_flag;
+    int32_t fold_depth;       // rows the fold warp sends ahead of the row it finishes (< rbufs, < skew)
+    uint32_t off_full, off_empty, off_hdr, off_seq, off_part, off_fold, off_rows, off_xtin, off_bars, off_flag;
 };
 
 struct TileGeom {
@@ -399,6 +401,8 @@ __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* 
 // mbarriers complete once per use, so a wait for row n takes parity
 // (n / rbufs) & 1.
 constexpr int kMaxRowBufs = 8;
+constexpr int kMaxCluster = 8;
+constexpr int kMaxFoldDepth = 3;
 
 __device__ __forceinline__ int row_buf(const Params& p, int64_t n) { return (int)(n & (p.rbufs - 1)); }
 __device__ __forceinline__ uint32_t row_par(const Params& p, int64_t n) { return (uint32_t)((n >> p.rb_shift) & 1); }
@@ -411,10 +415,11 @@ struct Ctx {
     unsigned char* smem;
     uint32_t sbase, full0, empty0;
     // per row buffer b: rowdone[b] (every consumer warp arrived: partials of the
-    // row are in part[b]), lseready[b] (fold done, rows[b].lse valid),
-    // partfree[b] (part[b] and rows[b] may be reused), xbar[b] (peer CTAs'
-    // partials arrived)
-    uint32_t rowdone0, lseready0, partfree0, xbar0;
+    // row are in part[b]), lseready[b] (rows[b].lse valid), partfree[b]
+    // (part[b] and rows[b] may be reused), xbar[b] (the folder: every peer's
+    // partials and target record arrived), lsebar[b] (the others: the
+    // folder's LSE arrived)
+    uint32_t rowdone0, lseready0, partfree0, xbar0, lsebar0;
     SlotHdr* hdr;
     // seq[s]: number of the item the producer last issued into slot s.  A
     // consumer waits for its own item number before the slot's full-barrier
@@ -424,6 +429,7 @@ struct Ctx {
     float2* part;
     float2* fold;
     RowShared* rows;
+    float2* xtin;  // [rbufs][kMaxCluster]: each peer's (x_t, has_xt) of the row this CTA folds
     Waiter wt;
 };
 
@@ -588,41 +594,62 @@ __device__ void producer(const Params& p, const Ctx& x) {
     }
 }
 
-// The fold warp, for each row n of this CTA:
+// The fold warp.  Row n of a cluster is folded by one CTA, its folder
+// F(n) = n mod C (every CTA folds every row when C = 1).  For each row:
 //  * push: once every consumer warp has put its tiles' partials in part[b],
-//    arm this CTA's xbar[b] with the bytes the peers will send (one local
-//    arrival + expect-tx) and send this CTA's shard of partials to every peer
-//    CTA with asynchronous remote stores that complete on the peer's xbar[b]
-//    (virtual TP > 1);
-//  * finish: wait for xbar[b] (every peer's shard has landed), fold all tiles
-//    in index order, write the outputs and release the buffer.
-// With four or more row buffers the warp pushes row m before it finishes row
-// m - 1 (depth 1), so the exchange latency of one row overlaps the fold of
-// the previous one.  Pushing row m waits until every consumer warp has done
-// phase A of row m, so in the fused modes the depth stays below the skew:
-// consumers wait for row n's LSE right after phase A of row n + skew.  Ordering: a peer sends row n + rbufs into buffer b only
-// after it has finished row n + rbufs - 2, which needs this CTA's push of
-// that row, which this warp issues only after finishing row n + rbufs - 3
-// >= n when rbufs >= 4; so xbar[b] has completed row n's phase and its fold
-// has read part[b] before any byte of row n + rbufs arrives.  With fewer
-// buffers the warp finishes each row before pushing the next (depth 0).
+//    a CTA that does not fold the row sends its shard of partials and its
+//    target record (x_t, has_xt) to the folder with asynchronous remote
+//    stores, which complete on the folder's xbar[b]; the folder arms xbar[b]
+//    with the bytes it expects (one local arrival with expect-tx).  Every CTA
+//    arrives once per row on xbar[b] and lsebar[b] (with expect-tx where it
+//    receives), so both have one phase per row.
+//  * finish: the folder waits for xbar[b], folds all tiles in index order
+//    (fold_tiles), writes LSE and logp and sends the LSE to every other CTA
+//    (remote stores completing on their lsebar[b]); the others wait for
+//    lsebar[b].  Then rows[b].lse is valid (lseready) and the buffers of the
+//    row may be reused (partfree).
+// A buffer is reused only after its row's LSE is back, so no push of a later
+// row can land in a buffer whose row is still being exchanged or folded: the
+// push of row n + rbufs needs phase A of that row, which needs the release of
+// row n, which needs row n's LSE, which the folder sends after its fold.
+// The warp sends `fold_depth` rows ahead of the row it finishes, so one row's
+// round trip overlaps the next rows' pushes.  The depth stays below rbufs (the
+// push of row n + D waits for phase A of that row, which needs the release of
+// row n + D - rbufs) and, in the fused modes, below the skew (consumers wait
+// for row n's LSE right after phase A of row n + skew).
+__device__ __forceinline__ bool folds_row(const Params& p, const Ctx& x, int64_t n) {
+    return p.C == 1 || (uint32_t)(n % p.C) == x.rank;
+}
+
 template <int MODE>
 __device__ bool push_row(const Params& p, const Ctx& x, int64_t n) {
     const int lane = x.lane;
     const int b = row_buf(p, n);
     const bool ok = x.wt.warp_wait(x.rowdone0 + 8u * b, row_par(p, n));
     if (p.C > 1 && ok) {
-        float2* part = x.part + (size_t)b * p.NT;
-        const int peers = p.C - 1;
-        // the peers' shards: every tile but this CTA's own
-        if (lane == 0) mbar_arrive_expect_tx(x.xbar0 + 8u * b, (uint32_t)((p.NT - x.ntl) * 8));
-        for (int i = lane; i < peers * x.ntl; i += 32) {
-            const int pi = i / x.ntl;
-            const int kk = x.k0 + (i - pi * x.ntl);
-            const uint32_t peer = (uint32_t)pi < x.rank ? (uint32_t)pi : (uint32_t)pi + 1u;
-            const float2 v = part[kk];
-            st_async_f32x2(mapa_shared(smem_u32(&part[kk]), peer), v.x, v.y,
-                           mapa_shared(x.xbar0 + 8u * b, peer));
+        const uint32_t xb = x.xbar0 + 8u * b, lb = x.lsebar0 + 8u * b;
+        if (folds_row(p, x, n)) {
+            // every peer's shard (all tiles but this CTA's own) and target record
+            if (lane == 0) {
+                mbar_arrive_expect_tx(xb, (uint32_t)((p.NT - x.ntl) * 8 + (p.C - 1) * 8));
+                mbar_arrive(lb);
+            }
+        } else {
+            const uint32_t f = (uint32_t)(n % p.C);
+            const float2* part = x.part + (size_t)b * p.NT;
+            const uint32_t fxb = mapa_shared(xb, f);
+            for (int i = lane; i < x.ntl; i += 32) {
+                const float2 v = part[x.k0 + i];
+                st_async_f32x2(mapa_shared(smem_u32(&part[x.k0 + i]), f), v.x, v.y, fxb);
+            }
+            if (lane == 0) {
+                RowShared& rs = x.rows[b];
+                st_async_f32x2(mapa_shared(smem_u32(&x.xtin[b * kMaxCluster + x.rank]), f), rs.xt,
+                               __int_as_float(rs.has_xt), fxb);
+                rs.has_xt = 0;
+                mbar_arrive(xb);
+                mbar_arrive_expect_tx(lb, 4u);  // the folder's LSE
+            }
         }
     }
     return ok;
@@ -632,33 +659,56 @@ template <int MODE>
 __device__ void finish_row(const Params& p, const Ctx& x, int64_t n, bool ok) {
     const int lane = x.lane;
     const int b = row_buf(p, n);
+    const uint32_t par = row_par(p, n);
     float2* part = x.part + (size_t)b * p.NT;
-    if (p.C > 1) ok = x.wt.warp_wait(x.xbar0 + 8u * b, row_par(p, n), true) && ok;
+    RowShared& rs = x.rows[b];
     if (!ok) return;
-    const float lse_v = fold_tiles(part, p.NT, x.fold, lane);
-    const int64_t row = x.q + n * x.G;
-    if (p.a.partials && x.rank == 0) {
-        float2* out = reinterpret_cast<float2*>(p.a.partials) + row * p.NT;
-        for (int k = lane; k < p.NT; k += 32) out[k] = part[k];
-    }
-    __syncwarp();
-    if (lane == 0) {
-        RowShared& rs = x.rows[b];
-        const bool active = rs.active != 0;
-        const int64_t t = rs.target;
-        if (x.rank == 0) {
+    if (folds_row(p, x, n)) {
+        if (p.C > 1 && !x.wt.warp_wait(x.xbar0 + 8u * b, par, true)) return;
+        const float lse_v = fold_tiles(part, p.NT, x.fold, lane);
+        const int64_t row = x.q + n * x.G;
+        if (p.a.partials) {
+            float2* out = reinterpret_cast<float2*>(p.a.partials) + row * p.NT;
+            for (int k = lane; k < p.NT; k += 32) out[k] = part[k];
+        }
+        // the target logit: captured here or sent by the CTA that owns its tile
+        bool has = rs.has_xt != 0;
+        float xt = rs.xt;
+        if (p.C > 1) {
+            const float2 r = lane < p.C && (uint32_t)lane != x.rank ? x.xtin[b * kMaxCluster + lane]
+                                                                   : make_float2(0.f, 0.f);
+            const unsigned from = __ballot_sync(0xFFFFFFFFu, __float_as_int(r.y) != 0);
+            if (!has && from) {
+                has = true;
+                xt = __shfl_sync(0xFFFFFFFFu, r.x, __ffs(from) - 1);
+            }
+        }
+        // the LSE to every other CTA of the cluster
+        if (lane < p.C && (uint32_t)lane != x.rank)
+            st_async_f32(mapa_shared(smem_u32(&rs.lse), (uint32_t)lane), lse_v,
+                         mapa_shared(x.lsebar0 + 8u * b, (uint32_t)lane));
+        __syncwarp();
+        if (lane == 0) {
+            const bool active = rs.active != 0;
+            const int64_t t = rs.target;
             p.a.lse[row] = lse_v;
             if (!active) {
                 p.a.logp[row] = 0.f;
             } else if (t < 0 || t >= p.Vr) {
                 p.a.logp[row] = __int_as_float(0x7FC00000);
                 atomicOr(p.a.status, kStatusTargetRange);
+            } else if (has) {
+                p.a.logp[row] = __fsub_rn(xt, lse_v);
             }
             if (active && !isfinite(lse_v)) atomicOr(p.a.status, kStatusNonFinite);
+            rs.has_xt = 0;
+            rs.lse = lse_v;
         }
-        if (active && rs.has_xt) p.a.logp[row] = __fsub_rn(rs.xt, lse_v);
-        rs.has_xt = 0;
-        rs.lse = lse_v;
+    } else if (!x.wt.warp_wait(x.lsebar0 + 8u * b, par, true)) {
+        return;
+    }
+    __syncwarp();
+    if (lane == 0) {
         if (MODE == kModeFused || MODE == kModeFusedL2) mbar_arrive(x.lseready0 + 8u * b);
         mbar_arrive(x.partfree0 + 8u * b);
     }
@@ -666,12 +716,14 @@ __device__ void finish_row(const Params& p, const Ctx& x, int64_t n, bool ok) {
 
 template <int MODE>
 __device__ void fold_warp(const Params& p, const Ctx& x) {
-    const int D = (p.C > 1 && p.rbufs >= 4 && (MODE == kModeFwd || p.skew >= 2)) ? 1 : 0;
-    bool ok_prev = true, ok_cur = true;
+    const int D = p.fold_depth;
+    uint32_t okbits = 0;  // bit (m & kMaxFoldDepth): the push of row m succeeded
     for (int64_t m = 0; m < x.nrows + D; ++m) {
-        if (m < x.nrows) ok_cur = push_row<MODE>(p, x, m);
-        if (m - D >= 0) finish_row<MODE>(p, x, m - D, D ? ok_prev : ok_cur);
-        ok_prev = ok_cur;
+        if (m < x.nrows) {
+            const uint32_t bit = 1u << (m & kMaxFoldDepth);
+            okbits = push_row<MODE>(p, x, m) ? (okbits | bit) : (okbits & ~bit);
+        }
+        if (m - D >= 0) finish_row<MODE>(p, x, m - D, (okbits >> ((m - D) & kMaxFoldDepth)) & 1u);
     }
     // After an expired wait some peer stores may still be on their way into
     // this CTA's shared memory: give them time to land before the kernel ends.
@@ -858,11 +910,13 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     x.lseready0 = x.rowdone0 + 8u * p.rbufs;
     x.partfree0 = x.lseready0 + 8u * p.rbufs;
     x.xbar0 = x.partfree0 + 8u * p.rbufs;
+    x.lsebar0 = x.xbar0 + 8u * p.rbufs;
     x.hdr = reinterpret_cast<SlotHdr*>(smem + p.off_hdr);
     x.seq = reinterpret_cast<volatile uint32_t*>(smem + p.off_seq);
     x.part = reinterpret_cast<float2*>(smem + p.off_part);
     x.fold = reinterpret_cast<float2*>(smem + p.off_fold);
     x.rows = reinterpret_cast<RowShared*>(smem + p.off_rows);
+    x.xtin = reinterpret_cast<float2*>(smem + p.off_xtin);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.off_flag);
     x.wt.abort_flag = abort_flag;
     x.wt.status = p.a.status;
@@ -878,7 +932,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
             mbar_init(x.rowdone0 + 8u * b, kConsumerWarps);
             mbar_init(x.lseready0 + 8u * b, 1);
             mbar_init(x.partfree0 + 8u * b, 1);
-            mbar_init(x.xbar0 + 8u * b, 1);  // the local arrival (with expect-tx)
+            mbar_init(x.xbar0 + 8u * b, 1);    // the local arrival (with expect-tx on the folder)
+            mbar_init(x.lsebar0 + 8u * b, 1);  // the local arrival (with expect-tx off the folder)
             x.rows[b].has_xt = 0;
         }
         *abort_flag = 0;
@@ -957,8 +1012,10 @@ uint32_t layout(Params& p, int NS) {
     off += 8u * (uint32_t)p.NT;
     p.off_rows = align_up(off, 16);
     off = p.off_rows + (uint32_t)p.rbufs * (uint32_t)sizeof(RowShared);
+    p.off_xtin = align_up(off, 16);
+    off = p.off_xtin + (uint32_t)p.rbufs * (uint32_t)kMaxCluster * 8u;
     p.off_bars = align_up(off, 8);
-    off = p.off_bars + 4u * 8u * (uint32_t)p.rbufs;  // rowdone, lseready, partfree, xbar
+    off = p.off_bars + 5u * 8u * (uint32_t)p.rbufs;  // rowdone, lseready, partfree, xbar, lsebar
     p.off_flag = off;
     off += 16u;
     return align_up(off, 128);
@@ -1020,28 +1077,41 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         if (!(sch && std::string(sch) == "resident")) mode = kModeFusedL2;
     }
     int C = (mode == kModeBwd) ? 1 : c.virtual_tp;
-    // Row buffers of the fold: more buffers let the fold of a row lag further
-    // behind phase A (short shards give short rows per CTA); they cost
-    // rbufs * 8 * num_tiles bytes of shared memory.
+    // Row buffers of the fold: more buffers let a row's exchange and fold lag
+    // further behind phase A (short shards give short rows per CTA); they
+    // cost rbufs * (8 * num_tiles + 128) bytes of shared memory.
     {
-        int rb = env_int("RLK_ROW_BUFS", c.num_tiles <= 256 ? 4 : 2);
+        int rb = env_int("RLK_ROW_BUFS", c.num_tiles <= 128 ? 8 : c.num_tiles <= 256 ? 4 : 2);
         rb = rb >= kMaxRowBufs ? kMaxRowBufs : rb >= 4 ? 4 : 2;
         if (mode == kModeBwd || mode == kModeFused) rb = 2;
         p.rbufs = rb;
         p.rb_shift = rb == 8 ? 3 : rb == 4 ? 2 : 1;
         // kModeFusedL2 skew: the rows of phase A between a row's two copies
         // must stay in L2.  Keep (skew + 1) rows of every SM's shard within
-        // kL2ReuseBytes, at least one row of skew, and skew < rbufs.
+        // kL2ReuseBytes, at least one row of skew, skew < rbufs, at most kMaxSkew.
         int skew = 1;
         if (mode == kModeFusedL2) {
             const int64_t shard_bytes = (int64_t)((c.num_tiles + C - 1) / C) * p.W * 2;
             const int64_t gpu_row = shard_bytes * di.sm_count;
             int fit = (int)(kL2ReuseBytes / (gpu_row > 0 ? gpu_row : 1));
             skew = env_int("RLK_FUSED_SKEW", fit - 1);
+            if (skew > kMaxSkew) skew = kMaxSkew;
             if (skew > rb - 1) skew = rb - 1;
             if (skew < 1) skew = 1;
         }
         p.skew = skew;
+        // Fold depth: none without peers; below rbufs; below the skew in the
+        // fused modes (kModeFused runs with skew 1).
+        int depth = 0;
+        if (C > 1 || mode == kModeFused) {
+            depth = env_int("RLK_FOLD_DEPTH", kMaxFoldDepth);
+            if (depth > kMaxFoldDepth) depth = kMaxFoldDepth;
+            if (depth > rb - 1) depth = rb - 1;
+            if (mode == kModeFusedL2 && depth > skew - 1) depth = skew - 1;
+            if (mode == kModeFused) depth = 0;
+            if (depth < 0) depth = 0;
+        }
+        p.fold_depth = depth;
     }
     int NS = 0;
     p.C = C;
@@ -1110,8 +1180,8 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     if (env_int("RLK_VERBOSE", 0))
         std::fprintf(stderr,
                      "rlk stream plan: mode %d, %lld clusters x %d CTAs, %d tiles/copy, %d slots of %d B, "
-                     "%d row buffers, skew %d, %u B shared memory\n",
-                     mode, (long long)clusters, p.C, p.tps, p.NS, p.slot_bytes, p.rbufs, p.skew, smem);
+                     "%d row buffers, skew %d, fold depth %d, %u B shared memory\n",
+                     mode, (long long)clusters, p.C, p.tps, p.NS, p.slot_bytes, p.rbufs, p.skew, p.fold_depth, smem);
     e = cudaLaunchKernelEx(&cfg, kfn, p);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(e));
     return RLK_OK;

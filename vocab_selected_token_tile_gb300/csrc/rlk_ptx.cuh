@@ -200,6 +200,13 @@ __device__ __forceinline__ void st_async_f32x2(uint32_t addr, float a, float b, 
                  : "memory");
 }
 
+// The 4-byte form of st_async_f32x2.
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float a, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr), "f"(a),
+                 "r"(remote_bar)
+                 : "memory");
+}
+
 // All threads of all CTAs of the cluster; release/acquire at cluster scope.
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
