@@ -20,9 +20,10 @@ complete on the folder's xbar barrier after a random delay; the folder folds
 and sends the LSE back to every peer, completing on their lsebar barriers.
 Every CTA arrives once per row on xbar and lsebar (with expect-tx where it
 receives), so both barriers have one phase per row.  A CTA releases a row's
-buffers (partfree) only once it holds the row's LSE.  With fold_depth D = 1
-the fold warp sends row m before it finishes row m - 1.  The folder reads the
-partials over several steps and checks that nothing overwrote them.
+buffers (partfree) only once it holds the row's LSE.  The fold warp is an
+event loop that pushes, folds and releases rows as each becomes possible.
+The folder reads the partials over several steps and checks that nothing
+overwrote them.
 """
 import random
 
@@ -69,24 +70,8 @@ def block_schedule(mode, rows, skew=1):
     return seq
 
 
-def kernel_fold_depth(mode, C, rbufs, skew):
-    """Rows the fold warp sends ahead of the row it finishes (the host planner's rule):
-    none without peers; below the row buffers (the push of row n + D waits for
-    phase A of that row, which waits for the release of row n + D - rbufs);
-    in the fused modes below the skew (consumers wait for row n's LSE right
-    after phase A of row n + skew); at most 3."""
-    if C == 1:
-        return 0
-    d = min(rbufs - 1, 3)
-    if mode in ("fused", "fused_l2"):
-        d = min(d, (skew if mode == "fused_l2" else 1) - 1)
-    return max(d, 0)
-
-
-def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80, rbufs=2, skew=1,
-             fold_depth=None):
-    """mode: 'fwd' | 'bwd' | 'fused' | 'fused_l2'; rbufs row buffers, fused_l2 row skew;
-    fold_depth (default: the kernel's choice, kernel_fold_depth).
+def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80, rbufs=2, skew=1):
+    """mode: 'fwd' | 'bwd' | 'fused' | 'fused_l2'; rbufs row buffers, fused_l2 row skew.
 
     Raises ProtocolError on a stale read or a deadlock."""
     rng = random.Random(seed)
@@ -94,7 +79,6 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
     nch = (ntl + tps - 1) // tps
     R = rbufs
     S = skew if mode == "fused_l2" else 1
-    D = fold_depth if fold_depth is not None else kernel_fold_depth(mode, C, rbufs, S)
     pushes = []  # in flight: [delay, receiver CTA, kind, buffer, index, value]
 
     def folder(n):
@@ -220,9 +204,8 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
                 yield from wait(c.lseready[n % R], (n // R) & 1)
                 yield from phase_b(c, w, n)
 
-    def push(c, m):
-        b, par = m % R, (m // R) & 1
-        yield from wait(c.rowdone[b], par)
+    def do_push(c, m):
+        b = m % R
         if C > 1:
             f = ctas[folder(m)]
             if f is c:
@@ -236,37 +219,48 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
                 for k in range(c.rank * ntl, (c.rank + 1) * ntl):
                     pushes.append([rng.randint(1, max_delay), f, "part", b, k, c.part[b][k]])
                 pushes.append([rng.randint(1, max_delay), f, "xt", b, c.rank, c.xtrow[b]])
-            yield "push"
-
-    def finish(c, n):
-        b, par = n % R, (n // R) & 1
-        if C > 1:
-            yield from wait(c.xbar[b], par)
-        if C == 1 or folder(n) == c.rank:
-            if any(v != n for v in c.part[b]) or any(c.xt[b][j] != n for j in range(C) if C > 1 and j != c.rank):
-                raise ProtocolError(f"{mode} fold of row {n} saw partials of rows {sorted(set(map(str, c.part[b])))}")
-            yield "fold"
-            yield "fold"
-            if any(v != n for v in c.part[b]):
-                raise ProtocolError(f"{mode} partials of row {n} were overwritten during its fold")
-            c.lse[b] = n
-            for peer in ctas:
-                if peer is not c:
-                    pushes.append([rng.randint(1, max_delay), peer, "lse", b, 0, n])
-        if C > 1:
-            yield from wait(c.lsebar[b], par)
-        if c.lse[b] != n:
-            raise ProtocolError(f"{mode} CTA {c.rank} released row {n} holding the LSE of row {c.lse[b]}")
-        if mode in ("fused", "fused_l2"):
-            c.lseready[b].arrive()
-        c.partfree[b].arrive()
 
     def fold(c):
-        for m in range(rows + D):
-            if m < rows:
-                yield from push(c, m)
-            if m - D >= 0:
-                yield from finish(c, m - D)
+        # The fold warp as an event loop: push rows in order as their phase A
+        # completes, fold this CTA's rows as soon as their shards are in, and
+        # release rows in order as their LSE is known.  No step waits for
+        # another: a row's fold never waits for an earlier row's LSE.
+        np_, nr = 0, 0
+        nf = c.rank if C > 1 else 0
+        step = C if C > 1 else 1
+        while nr < rows:
+            progressed = False
+            if np_ < rows and c.rowdone[np_ % R].try_wait((np_ // R) & 1):
+                do_push(c, np_)
+                np_ += 1
+                progressed = True
+            if nf < rows and nf < np_ and (C == 1 or c.xbar[nf % R].try_wait((nf // R) & 1)):
+                n, b = nf, nf % R
+                if any(v != n for v in c.part[b]) or any(c.xt[b][j] != n for j in range(C) if C > 1 and j != c.rank):
+                    raise ProtocolError(f"{mode} fold of row {n} saw partials of rows "
+                                        f"{sorted(set(map(str, c.part[b])))}")
+                yield "fold"
+                yield "fold"
+                if any(v != n for v in c.part[b]):
+                    raise ProtocolError(f"{mode} partials of row {n} were overwritten during its fold")
+                c.lse[b] = n
+                for peer in ctas:
+                    if peer is not c:
+                        pushes.append([rng.randint(1, max_delay), peer, "lse", b, 0, n])
+                nf += step
+                progressed = True
+            if nr < np_:
+                b = nr % R
+                ready = nr < nf if (C == 1 or folder(nr) == c.rank) else c.lsebar[b].try_wait((nr // R) & 1)
+                if ready:
+                    if c.lse[b] != nr:
+                        raise ProtocolError(f"{mode} CTA {c.rank} released row {nr} holding the LSE of row {c.lse[b]}")
+                    if mode in ("fused", "fused_l2"):
+                        c.lseready[b].arrive()
+                    c.partfree[b].arrive()
+                    nr += 1
+                    progressed = True
+            yield "step" if progressed else "wait"
 
     agents = []
     for c in ctas:

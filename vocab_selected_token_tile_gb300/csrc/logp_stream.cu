@@ -96,7 +96,6 @@ struct Params {
     int32_t tps;  // tiles per ring slot (consecutive tiles of one row share a slot when narrow)
     int32_t rbufs, rb_shift;  // row buffers of the fold (a power of two) and its log2
     int32_t skew;             // kModeFusedL2: phase A runs `skew` rows ahead of phase B (< rbufs)
-    int32_t fold_depth;       // rows the fold warp sends ahead of the row it finishes (< rbufs, < skew)
     uint32_t off_full, off_empty, off_hdr, off_seq, off_part, off_fold, off_rows, off_xtin, off_bars, off_flag;
 };
 
@@ -402,7 +401,6 @@ __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* 
 // (n / rbufs) & 1.
 constexpr int kMaxRowBufs = 8;
 constexpr int kMaxCluster = 8;
-constexpr int kMaxFoldDepth = 3;
 
 __device__ __forceinline__ int row_buf(const Params& p, int64_t n) { return (int)(n & (p.rbufs - 1)); }
 __device__ __forceinline__ uint32_t row_par(const Params& p, int64_t n) { return (uint32_t)((n >> p.rb_shift) & 1); }
@@ -595,141 +593,172 @@ __device__ void producer(const Params& p, const Ctx& x) {
 }
 
 // The fold warp.  Row n of a cluster is folded by one CTA, its folder
-// F(n) = n mod C (every CTA folds every row when C = 1).  For each row:
-//  * push: once every consumer warp has put its tiles' partials in part[b],
-//    a CTA that does not fold the row sends its shard of partials and its
-//    target record (x_t, has_xt) to the folder with asynchronous remote
-//    stores, which complete on the folder's xbar[b]; the folder arms xbar[b]
-//    with the bytes it expects (one local arrival with expect-tx).  Every CTA
-//    arrives once per row on xbar[b] and lsebar[b] (with expect-tx where it
-//    receives), so both have one phase per row.
-//  * finish: the folder waits for xbar[b], folds all tiles in index order
-//    (fold_tiles), writes LSE and logp and sends the LSE to every other CTA
-//    (remote stores completing on their lsebar[b]); the others wait for
-//    lsebar[b].  Then rows[b].lse is valid (lseready) and the buffers of the
-//    row may be reused (partfree).
-// A buffer is reused only after its row's LSE is back, so no push of a later
-// row can land in a buffer whose row is still being exchanged or folded: the
-// push of row n + rbufs needs phase A of that row, which needs the release of
-// row n, which needs row n's LSE, which the folder sends after its fold.
-// The warp sends `fold_depth` rows ahead of the row it finishes, so one row's
-// round trip overlaps the next rows' pushes.  The depth stays below rbufs (the
-// push of row n + D waits for phase A of that row, which needs the release of
-// row n + D - rbufs) and, in the fused modes, below the skew (consumers wait
-// for row n's LSE right after phase A of row n + skew).
+// F(n) = n mod C (every row by the CTA itself when C = 1).
+//  * push (row order, once every consumer warp has put its tiles' partials in
+//    part[b]): a CTA that does not fold the row sends its shard of partials
+//    and its target record (x_t, has_xt) to the folder with asynchronous
+//    remote stores, which complete on the folder's xbar[b]; the folder arms
+//    xbar[b] with the bytes it expects (one local arrival with expect-tx).
+//    Every CTA arrives once per row on xbar[b] and lsebar[b] (with expect-tx
+//    where it receives), so both have one phase per row.
+//  * fold (this CTA's rows, in order, as soon as xbar[b] completes): fold all
+//    tiles in index order (fold_tiles), write LSE and logp, and send the LSE
+//    to every other CTA (remote stores completing on their lsebar[b]).
+//  * release (row order, once the row's LSE is here): rows[b].lse is valid
+//    (lseready) and the row's buffers may be reused (partfree).
+// The warp runs the three as an event loop with non-blocking tests, so a
+// row's fold never waits for the LSE of an earlier row folded elsewhere; the
+// only chain between rows is the reuse of a buffer: the push of row
+// n + rbufs needs phase A of that row, which needs the release of row n,
+// which needs row n's LSE, which its folder sends after its fold.  So no
+// push of a later row can land in a buffer whose row is still being
+// exchanged or folded.  Each test of a phase expects the barrier to have
+// completed the phase of the previous use of its buffer, which the loop's
+// order guarantees: rows are pushed, folded and released in increasing order.
 __device__ __forceinline__ bool folds_row(const Params& p, const Ctx& x, int64_t n) {
     return p.C == 1 || (uint32_t)(n % p.C) == x.rank;
 }
 
-template <int MODE>
-__device__ bool push_row(const Params& p, const Ctx& x, int64_t n) {
-    const int lane = x.lane;
-    const int b = row_buf(p, n);
-    const bool ok = x.wt.warp_wait(x.rowdone0 + 8u * b, row_par(p, n));
-    if (p.C > 1 && ok) {
-        const uint32_t xb = x.xbar0 + 8u * b, lb = x.lsebar0 + 8u * b;
-        if (folds_row(p, x, n)) {
-            // every peer's shard (all tiles but this CTA's own) and target record
-            if (lane == 0) {
-                mbar_arrive_expect_tx(xb, (uint32_t)((p.NT - x.ntl) * 8 + (p.C - 1) * 8));
-                mbar_arrive(lb);
-            }
-        } else {
-            const uint32_t f = (uint32_t)(n % p.C);
-            const float2* part = x.part + (size_t)b * p.NT;
-            const uint32_t fxb = mapa_shared(xb, f);
-            for (int i = lane; i < x.ntl; i += 32) {
-                const float2 v = part[x.k0 + i];
-                st_async_f32x2(mapa_shared(smem_u32(&part[x.k0 + i]), f), v.x, v.y, fxb);
-            }
-            if (lane == 0) {
-                RowShared& rs = x.rows[b];
-                st_async_f32x2(mapa_shared(smem_u32(&x.xtin[b * kMaxCluster + x.rank]), f), rs.xt,
-                               __int_as_float(rs.has_xt), fxb);
-                rs.has_xt = 0;
-                mbar_arrive(xb);
-                mbar_arrive_expect_tx(lb, 4u);  // the folder's LSE
-            }
-        }
-    }
-    return ok;
+__device__ __forceinline__ bool warp_test(uint32_t bar, uint32_t parity, bool cluster_scope) {
+    const bool ok = cluster_scope ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity);
+    return __all_sync(0xFFFFFFFFu, ok);
 }
 
-template <int MODE>
-__device__ void finish_row(const Params& p, const Ctx& x, int64_t n, bool ok) {
+__device__ void push_row(const Params& p, const Ctx& x, int64_t n) {
+    if (p.C == 1) return;
     const int lane = x.lane;
     const int b = row_buf(p, n);
-    const uint32_t par = row_par(p, n);
+    const uint32_t xb = x.xbar0 + 8u * b, lb = x.lsebar0 + 8u * b;
+    if (folds_row(p, x, n)) {
+        // every peer's shard (all tiles but this CTA's own) and target record
+        if (lane == 0) {
+            mbar_arrive_expect_tx(xb, (uint32_t)((p.NT - x.ntl) * 8 + (p.C - 1) * 8));
+            mbar_arrive(lb);
+        }
+        return;
+    }
+    const uint32_t f = (uint32_t)(n % p.C);
+    const float2* part = x.part + (size_t)b * p.NT;
+    const uint32_t fxb = mapa_shared(xb, f);
+    for (int i = lane; i < x.ntl; i += 32) {
+        const float2 v = part[x.k0 + i];
+        st_async_f32x2(mapa_shared(smem_u32(&part[x.k0 + i]), f), v.x, v.y, fxb);
+    }
+    if (lane == 0) {
+        RowShared& rs = x.rows[b];
+        st_async_f32x2(mapa_shared(smem_u32(&x.xtin[b * kMaxCluster + x.rank]), f), rs.xt,
+                       __int_as_float(rs.has_xt), fxb);
+        rs.has_xt = 0;
+        mbar_arrive(xb);
+        mbar_arrive_expect_tx(lb, 4u);  // the folder's LSE
+    }
+}
+
+__device__ void fold_row(const Params& p, const Ctx& x, int64_t n) {
+    const int lane = x.lane;
+    const int b = row_buf(p, n);
     float2* part = x.part + (size_t)b * p.NT;
     RowShared& rs = x.rows[b];
-    if (!ok) return;
-    if (folds_row(p, x, n)) {
-        if (p.C > 1 && !x.wt.warp_wait(x.xbar0 + 8u * b, par, true)) return;
-        const float lse_v = fold_tiles(part, p.NT, x.fold, lane);
-        const int64_t row = x.q + n * x.G;
-        if (p.a.partials) {
-            float2* out = reinterpret_cast<float2*>(p.a.partials) + row * p.NT;
-            for (int k = lane; k < p.NT; k += 32) out[k] = part[k];
-        }
-        // the target logit: captured here or sent by the CTA that owns its tile
-        bool has = rs.has_xt != 0;
-        float xt = rs.xt;
-        if (p.C > 1) {
-            const float2 r = lane < p.C && (uint32_t)lane != x.rank ? x.xtin[b * kMaxCluster + lane]
-                                                                   : make_float2(0.f, 0.f);
-            const unsigned from = __ballot_sync(0xFFFFFFFFu, __float_as_int(r.y) != 0);
-            if (!has && from) {
-                has = true;
-                xt = __shfl_sync(0xFFFFFFFFu, r.x, __ffs(from) - 1);
-            }
+    const float lse_v = fold_tiles(part, p.NT, x.fold, lane);
+    const int64_t row = x.q + n * x.G;
+    if (p.a.partials) {
+        float2* out = reinterpret_cast<float2*>(p.a.partials) + row * p.NT;
+        for (int k = lane; k < p.NT; k += 32) out[k] = part[k];
+    }
+    // the target logit: captured here or sent by the CTA that owns its tile
+    bool has = rs.has_xt != 0;
+    float xt = rs.xt;
+    if (p.C > 1) {
+        const float2 r =
+            lane < p.C && (uint32_t)lane != x.rank ? x.xtin[b * kMaxCluster + lane] : make_float2(0.f, 0.f);
+        const unsigned from = __ballot_sync(0xFFFFFFFFu, __float_as_int(r.y) != 0);
+        if (!has && from) {
+            has = true;
+            xt = __shfl_sync(0xFFFFFFFFu, r.x, __ffs(from) - 1);
         }
         // the LSE to every other CTA of the cluster
         if (lane < p.C && (uint32_t)lane != x.rank)
             st_async_f32(mapa_shared(smem_u32(&rs.lse), (uint32_t)lane), lse_v,
                          mapa_shared(x.lsebar0 + 8u * b, (uint32_t)lane));
-        __syncwarp();
-        if (lane == 0) {
-            const bool active = rs.active != 0;
-            const int64_t t = rs.target;
-            p.a.lse[row] = lse_v;
-            if (!active) {
-                p.a.logp[row] = 0.f;
-            } else if (t < 0 || t >= p.Vr) {
-                p.a.logp[row] = __int_as_float(0x7FC00000);
-                atomicOr(p.a.status, kStatusTargetRange);
-            } else if (has) {
-                p.a.logp[row] = __fsub_rn(xt, lse_v);
-            }
-            if (active && !isfinite(lse_v)) atomicOr(p.a.status, kStatusNonFinite);
-            rs.has_xt = 0;
-            rs.lse = lse_v;
-        }
-    } else if (!x.wt.warp_wait(x.lsebar0 + 8u * b, par, true)) {
-        return;
     }
     __syncwarp();
     if (lane == 0) {
-        if (MODE == kModeFused || MODE == kModeFusedL2) mbar_arrive(x.lseready0 + 8u * b);
-        mbar_arrive(x.partfree0 + 8u * b);
+        const bool active = rs.active != 0;
+        const int64_t t = rs.target;
+        p.a.lse[row] = lse_v;
+        if (!active) {
+            p.a.logp[row] = 0.f;
+        } else if (t < 0 || t >= p.Vr) {
+            p.a.logp[row] = __int_as_float(0x7FC00000);
+            atomicOr(p.a.status, kStatusTargetRange);
+        } else if (has) {
+            p.a.logp[row] = __fsub_rn(xt, lse_v);
+        }
+        if (active && !isfinite(lse_v)) atomicOr(p.a.status, kStatusNonFinite);
+        rs.has_xt = 0;
+        rs.lse = lse_v;
     }
+    __syncwarp();
 }
 
 template <int MODE>
 __device__ void fold_warp(const Params& p, const Ctx& x) {
-    const int D = p.fold_depth;
-    uint32_t okbits = 0;  // bit (m & kMaxFoldDepth): the push of row m succeeded
-    for (int64_t m = 0; m < x.nrows + D; ++m) {
-        if (m < x.nrows) {
-            const uint32_t bit = 1u << (m & kMaxFoldDepth);
-            okbits = push_row<MODE>(p, x, m) ? (okbits | bit) : (okbits & ~bit);
+    const int64_t R = x.nrows;
+    int64_t np = 0, nr = 0;                         // next row to push, to release
+    int64_t nf = p.C > 1 ? (int64_t)x.rank : 0;     // next row this CTA folds
+    const int64_t fstep = p.C > 1 ? p.C : 1;
+    bool idle = false;
+    uint64_t t0 = 0;
+    while (nr < R) {
+        bool progressed = false;
+        if (np < R && warp_test(x.rowdone0 + 8u * row_buf(p, np), row_par(p, np), false)) {
+            push_row(p, x, np);
+            ++np;
+            progressed = true;
         }
-        if (m - D >= 0) finish_row<MODE>(p, x, m - D, (okbits >> ((m - D) & kMaxFoldDepth)) & 1u);
+        if (nf < R && nf < np &&
+            (p.C == 1 || warp_test(x.xbar0 + 8u * row_buf(p, nf), row_par(p, nf), true))) {
+            fold_row(p, x, nf);
+            nf += fstep;
+            progressed = true;
+        }
+        if (nr < np) {
+            const int b = row_buf(p, nr);
+            const bool ready =
+                folds_row(p, x, nr) ? nr < nf : warp_test(x.lsebar0 + 8u * b, row_par(p, nr), true);
+            if (ready) {
+                if (x.lane == 0) {
+                    if (MODE == kModeFused || MODE == kModeFusedL2) mbar_arrive(x.lseready0 + 8u * b);
+                    mbar_arrive(x.partfree0 + 8u * b);
+                }
+                ++nr;
+                progressed = true;
+            }
+        }
+        if (progressed) {
+            idle = false;
+            continue;
+        }
+        // Every decision below is the same in all lanes: the clock is lane 0's.
+        if (__any_sync(0xFFFFFFFFu, *x.wt.abort_flag != 0)) break;
+        const uint64_t now = __shfl_sync(0xFFFFFFFFu, (unsigned long long)globaltimer_ns(), 0);
+        if (!idle) {
+            idle = true;
+            t0 = now;
+        } else if (now - t0 > x.wt.limit_ns) {
+            if (x.lane == 0) {
+                *x.wt.abort_flag = 1;
+                atomicOr(x.wt.status, kStatusTimeout);
+            }
+            break;
+        }
     }
+    __syncwarp();
     // After an expired wait some peer stores may still be on their way into
     // this CTA's shared memory: give them time to land before the kernel ends.
     if (p.C > 1 && *x.wt.abort_flag) {
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 1000000ull) {
+        const uint64_t t1 = globaltimer_ns();
+        while (globaltimer_ns() - t1 < 1000000ull) {
         }
     }
 }
@@ -1100,18 +1129,6 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
             if (skew < 1) skew = 1;
         }
         p.skew = skew;
-        // Fold depth: none without peers; below rbufs; below the skew in the
-        // fused modes (kModeFused runs with skew 1).
-        int depth = 0;
-        if (C > 1 || mode == kModeFused) {
-            depth = env_int("RLK_FOLD_DEPTH", kMaxFoldDepth);
-            if (depth > kMaxFoldDepth) depth = kMaxFoldDepth;
-            if (depth > rb - 1) depth = rb - 1;
-            if (mode == kModeFusedL2 && depth > skew - 1) depth = skew - 1;
-            if (mode == kModeFused) depth = 0;
-            if (depth < 0) depth = 0;
-        }
-        p.fold_depth = depth;
     }
     int NS = 0;
     p.C = C;
@@ -1180,8 +1197,8 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     if (env_int("RLK_VERBOSE", 0))
         std::fprintf(stderr,
                      "rlk stream plan: mode %d, %lld clusters x %d CTAs, %d tiles/copy, %d slots of %d B, "
-                     "%d row buffers, skew %d, fold depth %d, %u B shared memory\n",
-                     mode, (long long)clusters, p.C, p.tps, p.NS, p.slot_bytes, p.rbufs, p.skew, p.fold_depth, smem);
+                     "%d row buffers, skew %d, %u B shared memory\n",
+                     mode, (long long)clusters, p.C, p.tps, p.NS, p.slot_bytes, p.rbufs, p.skew, smem);
     e = cudaLaunchKernelEx(&cfg, kfn, p);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(e));
     return RLK_OK;
