@@ -183,3 +183,20 @@ def test_without_the_issued_item_check_the_model_finds_stale_reads():
         except ProtocolError:
             found += 1
     assert found > 0
+
+
+def test_division_by_invariant_divisors():
+    # The kernel divides ring positions by NS and tile numbers by tps with
+    # m = floor(2^32 (2^s - d) / d) + 1, s = ceil(log2 d), q = (umulhi(n, m) + n) >> s.
+    import random
+    rng = random.Random(7)
+    for d in range(1, 1025):
+        s = 0
+        while (1 << s) < d:
+            s += 1
+        m = ((1 << 32) * ((1 << s) - d)) // d + 1
+        assert m < (1 << 32)
+        ns = list(range(0, 3 * d + 3)) + [(1 << 32) - 1, (1 << 32) - d, (1 << 31)] + \
+            [rng.randrange(1 << 32) for _ in range(200)]
+        for n in ns:
+            assert (((n * m) >> 32) + n) >> s == n // d, (d, n)

@@ -88,12 +88,25 @@ struct RowShared {  // per-row state of the fold, double-buffered by row parity
 };
 static_assert(sizeof(RowShared) == 32, "RowShared layout");
 
+// Division by a divisor fixed for the launch (Granlund and Montgomery,
+// "Division by invariant integers using multiplication", 1994): with
+// s = ceil(log2 d) and m = floor(2^32 (2^s - d) / d) + 1, n / d equals
+// (umulhi(n, m) + n) >> s for every 32-bit n (the sum taken in 33 bits).
+struct FastDiv {
+    uint32_t d, m, s;
+};
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+    return (uint32_t)(((uint64_t)__umulhi(n, f.m) + n) >> f.s);
+}
+
 struct Params {
     StreamArgs a;
     int64_t T, Vr, Vp, stride, ignore_index;
     uint64_t wait_ns;
     int32_t NT, W, C, mask_mode, NS, slot_bytes;
     int32_t tps;  // tiles per ring slot (consecutive tiles of one row share a slot when narrow)
+    FastDiv ns_div, tps_div;  // division by NS and by tps
     int32_t rbufs, rb_shift;  // row buffers of the fold (a power of two) and its log2
     int32_t skew;             // kModeFusedL2: phase A runs `skew` rows ahead of phase B (< rbufs)
     uint32_t off_full, off_empty, off_hdr, off_seq, off_part, off_fold, off_rows, off_xtin, off_bars, off_flag;
@@ -437,11 +450,6 @@ struct RingPos {
     uint32_t par;
 };
 
-__device__ __forceinline__ RingPos ring_add(RingPos r, int k, int NS) {
-    const int s = r.slot + k;
-    const int q = s / NS;
-    return RingPos{s - q * NS, r.par ^ (uint32_t)(q & 1)};
-}
 
 // The producer issues blocks of nch items (one row's chunks for one phase).
 // kModeFwd / kModeBwd / kModeFused: block n is row n.  kModeFusedL2 with
@@ -476,8 +484,9 @@ __device__ __forceinline__ void block_row(int64_t j, int64_t R, int64_t S, int64
     }
 }
 
-__device__ __forceinline__ RingPos ring_of(uint32_t item, int NS) {
-    return RingPos{(int)(item % (uint32_t)NS), (item / (uint32_t)NS) & 1u};
+__device__ __forceinline__ RingPos ring_of(uint32_t item, const FastDiv& ns) {
+    const uint32_t q = fdiv(item, ns);
+    return RingPos{(int)(item - q * ns.d), q & 1u};
 }
 
 // Row metadata of 32 consecutive rows of this CTA, one row per lane.
@@ -616,7 +625,7 @@ __device__ void producer(const Params& p, const Ctx& x) {
 // completed the phase of the previous use of its buffer, which the loop's
 // order guarantees: rows are pushed, folded and released in increasing order.
 __device__ __forceinline__ bool folds_row(const Params& p, const Ctx& x, int64_t n) {
-    return p.C == 1 || (uint32_t)(n % p.C) == x.rank;
+    return p.C == 1 || (uint32_t)(n & (p.C - 1)) == x.rank;  // C is a power of two
 }
 
 __device__ __forceinline__ bool warp_test(uint32_t bar, uint32_t parity, bool cluster_scope) {
@@ -637,7 +646,7 @@ __device__ void push_row(const Params& p, const Ctx& x, int64_t n) {
         }
         return;
     }
-    const uint32_t f = (uint32_t)(n % p.C);
+    const uint32_t f = (uint32_t)(n & (p.C - 1));
     const float2* part = x.part + (size_t)b * p.NT;
     const uint32_t fxb = mapa_shared(xb, f);
     for (int i = lane; i < x.ntl; i += 32) {
@@ -769,16 +778,19 @@ __device__ void fold_warp(const Params& p, const Ctx& x) {
 // when done.  A slot's empty barrier expects tps arrivals; the last tile of
 // a short (end-of-row) chunk arrives for the missing tiles too.
 struct TileItem {
+    uint32_t item;   // number of the chunk's item in the producer's order
     int slot;
     uint32_t par;
     int kf, kl;      // tiles [kf, kl) of the chunk
     uint32_t share;  // arrivals this tile owes the slot's empty barrier
 };
 
-__device__ __forceinline__ TileItem tile_item(const Params& p, const Ctx& x, RingPos rb, int l) {
-    const int c = l / p.tps;
-    const RingPos ps = ring_add(rb, c, p.NS);
+// Tile l of a block whose first item is item0.
+__device__ __forceinline__ TileItem tile_item(const Params& p, const Ctx& x, uint32_t item0, int l) {
+    const int c = (int)fdiv((uint32_t)l, p.tps_div);
     TileItem it;
+    it.item = item0 + (uint32_t)c;
+    const RingPos ps = ring_of(it.item, p.ns_div);
     it.slot = ps.slot;
     it.par = ps.par;
     it.kf = x.k0 + c * p.tps;
@@ -815,10 +827,9 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
     if (n >= p.rbufs) ok = x.wt.warp_wait(x.partfree0 + 8u * b, row_par(p, n - p.rbufs));
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
     const int slot_elems = p.slot_bytes / 2;
-    const RingPos rb = ring_of(item0, p.NS);
     for (int l = first_tile(x, n); l < x.ntl && ok; l += W) {
-        const TileItem it = tile_item(p, x, rb, l);
-        if (!wait_item(x, it, item0 + (uint32_t)(l / p.tps))) {
+        const TileItem it = tile_item(p, x, item0, l);
+        if (!wait_item(x, it, it.item)) {
             ok = false;
             break;
         }
@@ -865,10 +876,9 @@ __device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0
     const int lane = x.lane;
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
     const int slot_elems = p.slot_bytes / 2;
-    const RingPos rb = ring_of(item0, p.NS);
     for (int l = first_tile(x, n); l < x.ntl; l += W) {
-        const TileItem it = tile_item(p, x, rb, l);
-        if (kWaits && !wait_item(x, it, item0 + (uint32_t)(l / p.tps))) return false;
+        const TileItem it = tile_item(p, x, item0, l);
+        if (kWaits && !wait_item(x, it, it.item)) return false;
         const SlotHdr h = x.hdr[it.slot];
         const Span sp = chunk_span(it.kf, it.kl, p);
         const int k = x.k0 + l;
@@ -1024,6 +1034,15 @@ int env_int(const char* name, int dflt) {
 
 uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
+FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    f.d = d;
+    f.s = 0;
+    while ((1ull << f.s) < d) ++f.s;
+    f.m = (uint32_t)((((uint64_t)1 << 32) * (((uint64_t)1 << f.s) - d)) / d + 1);
+    return f;
+}
+
 // Shared-memory layout for NS slots; returns the total bytes.
 uint32_t layout(Params& p, int NS) {
     uint32_t off = (uint32_t)NS * (uint32_t)p.slot_bytes;
@@ -1154,6 +1173,8 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     }
     if (NS < 1) return fail(RLK_ERR_UNSUPPORTED, "tile too wide for one shared-memory slot");
     p.NS = NS;
+    p.ns_div = make_fastdiv((uint32_t)NS);
+    p.tps_div = make_fastdiv((uint32_t)p.tps);
     const uint32_t smem = layout(p, NS);
 
     void (*kfn)(Params) = (mode == kModeFwd)     ? stream_kernel<kModeFwd>
