@@ -33,11 +33,23 @@ def row_bufs(mode, nt):
     return 2 if mode in ("bwd", "fused") else (8 if nt <= 128 else 4 if nt <= 256 else 2)
 
 
+def ctas_per_sm(mode, vtp, v_padded, nt, sm_count=152, reuse_bytes=64 << 20):
+    """CTAs per SM as the host planner picks them: two for the streaming modes,
+    one for the resident fused mode, and two for the L2 fused mode only while
+    the rows between a row's two copies still fit in L2 with twice the CTAs."""
+    if mode == "fused":
+        return 1
+    if mode == "fused_l2":
+        shard = -(-nt // vtp) * (v_padded // nt) * 2
+        return 2 if reuse_bytes // (shard * 2 * sm_count) >= 2 else 1
+    return 2
+
+
 def plan(mode, vtp, v_padded, nt):
     """(C, tps, NS) as the host planner picks them."""
     w = v_padded // nt
     rb = row_bufs(mode, nt)
-    budget = SMEM_OPTIN - 1024
+    budget = SMEM_OPTIN // ctas_per_sm(mode, vtp, v_padded, nt) - 1024
     tps_target = 1 if w >= 8192 else 8192 // w
 
     def slot_bytes(tps):
@@ -67,13 +79,14 @@ def plan(mode, vtp, v_padded, nt):
 
 def plan_l2(vtp, v_padded, nt):
     """The L2-assisted fused mode is planned like the forward: C = virtual TP, no residency."""
-    return plan("fwd", vtp, v_padded, nt)
+    return plan("fused_l2", vtp, v_padded, nt)
 
 
 def l2_skew(vtp, v_padded, nt, sm_count=152, reuse_bytes=64 << 20):
     """Rows of skew of the L2-assisted fused mode, as the host planner picks them."""
     w = v_padded // nt
-    fit = reuse_bytes // (-(-nt // vtp) * w * 2 * sm_count)
+    ctas = sm_count * ctas_per_sm("fused_l2", vtp, v_padded, nt)
+    fit = reuse_bytes // (-(-nt // vtp) * w * 2 * ctas)
     return max(1, min(fit - 1, row_bufs("fused_l2", nt) - 1, 4))
 
 
@@ -107,9 +120,9 @@ def test_kernel_block_numbering_matches_the_schedule():
 
 
 def test_l2_skew_at_the_benchmark_shapes():
-    # 152 SMs, 152576 x 64 tiles: virtual TP 1 and 2 keep one row of skew;
-    # 4 and 8 take four (the cap)
-    assert [l2_skew(v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 4, 4]
+    # 152 SMs, 152576 x 64 tiles: virtual TP 1 and 2 (one CTA per SM) keep one
+    # row of skew; 4 (two per SM) one; 8 (two per SM) four, the cap
+    assert [l2_skew(v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 1, 4]
 
 
 CONFIGS = [(mode, vtp) for mode in ("fwd", "bwd", "fused", "fused_l2") for vtp in (1, 2, 4, 8)
@@ -126,7 +139,8 @@ def test_ring_protocol_reads_only_landed_slots(mode, vtp):
 
 def test_planner_replay_matches_the_benchmark_shapes():
     assert plan("fused", 2, 152576, 64) == (4, 2, 23)
-    assert plan("fwd", 1, 152576, 64) == (1, 3, 15)
+    assert plan("fwd", 1, 152576, 64) == (1, 3, 7)
+    assert [ctas_per_sm("fused_l2", v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 2, 2]
 
 
 @pytest.mark.parametrize("ns", [1, 2, 3, 5])
