@@ -33,16 +33,10 @@ def row_bufs(mode, nt):
     return 2 if mode in ("bwd", "fused") else (8 if nt <= 128 else 4 if nt <= 256 else 2)
 
 
-def ctas_per_sm(mode, vtp, v_padded, nt, sm_count=152, reuse_bytes=64 << 20):
+def ctas_per_sm(mode, vtp, v_padded, nt):
     """CTAs per SM as the host planner picks them: two for the streaming modes,
-    one for the resident fused mode, and two for the L2 fused mode only while
-    the rows between a row's two copies still fit in L2 with twice the CTAs."""
-    if mode == "fused":
-        return 1
-    if mode == "fused_l2":
-        shard = -(-nt // vtp) * (v_padded // nt) * 2
-        return 2 if reuse_bytes // (shard * 2 * sm_count) >= 2 else 1
-    return 2
+    one for both fused schedules."""
+    return 2 if mode in ("fwd", "bwd") else 1
 
 
 def plan(mode, vtp, v_padded, nt):
@@ -120,9 +114,9 @@ def test_kernel_block_numbering_matches_the_schedule():
 
 
 def test_l2_skew_at_the_benchmark_shapes():
-    # 152 SMs, 152576 x 64 tiles: virtual TP 1 and 2 (one CTA per SM) keep one
-    # row of skew; 4 (two per SM) one; 8 (two per SM) four, the cap
-    assert [l2_skew(v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 1, 4]
+    # 152 SMs, 152576 x 64 tiles: virtual TP 1 and 2 keep one row of skew;
+    # 4 and 8 take four (the cap)
+    assert [l2_skew(v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 4, 4]
 
 
 CONFIGS = [(mode, vtp) for mode in ("fwd", "bwd", "fused", "fused_l2") for vtp in (1, 2, 4, 8)
@@ -140,7 +134,6 @@ def test_ring_protocol_reads_only_landed_slots(mode, vtp):
 def test_planner_replay_matches_the_benchmark_shapes():
     assert plan("fused", 2, 152576, 64) == (4, 2, 23)
     assert plan("fwd", 1, 152576, 64) == (1, 3, 7)
-    assert [ctas_per_sm("fused_l2", v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 2, 2]
 
 
 @pytest.mark.parametrize("ns", [1, 2, 3, 5])

@@ -1116,15 +1116,14 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     }
     int C = (mode == kModeBwd) ? 1 : c.virtual_tp;
     // CTAs per SM.  Two streaming CTAs per SM double the bulk-copy issue rate
-    // (two producer warps) and let clusters of 8 cover every SM; measured on
-    // GB300 the forward runs at 99% of copy bandwidth with two against 88%
-    // with one.  kModeFusedL2 takes two only while the rows between a row's
-    // two copies still fit in L2 with twice the CTAs; the resident schedule
-    // needs the whole shared memory.
+    // (two producer warps) and let clusters of 8 cover every SM: measured on
+    // GB300 the forward streams at the copy bandwidth with two against 88% of
+    // it with one.  The fused modes keep one: the resident schedule needs the
+    // whole shared memory, and the L2 schedule measured slower with two (its
+    // rows between a row's two copies outgrow L2 at virtual TP 1-2, and at 4-8
+    // the smaller register budget spills).
     const int64_t shard_bytes = (int64_t)((c.num_tiles + C - 1) / C) * p.W * 2;
-    int ctas_per_sm = 2;
-    if (mode == kModeFused) ctas_per_sm = 1;
-    if (mode == kModeFusedL2 && kL2ReuseBytes / (shard_bytes * 2 * di.sm_count) < 2) ctas_per_sm = 1;
+    int ctas_per_sm = (mode == kModeFwd || mode == kModeBwd) ? 2 : 1;
     const int forced = env_int("RLK_CTAS_PER_SM", 0);
     if (forced == 1 || forced == 2) ctas_per_sm = forced;
     uint32_t budget = (uint32_t)di.smem_optin / (uint32_t)ctas_per_sm - 1024u;
