@@ -1152,10 +1152,13 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         if (mode == kModeFusedL2) {
             const int64_t gpu_row = shard_bytes * di.sm_count * ctas_per_sm;
             int fit = (int)(kL2ReuseBytes / (gpu_row > 0 ? gpu_row : 1));
-            skew = env_int("RLK_FUSED_SKEW", fit - 1);
+            skew = fit - 1;
             if (skew > kMaxSkew) skew = kMaxSkew;
             if (skew > rb - 1) skew = rb - 1;
             if (skew < 1) skew = 1;
+            // skew 0: phase B of a row right after its phase A and LSE
+            const int forced_skew = env_int("RLK_FUSED_SKEW", -1);
+            if (forced_skew >= 0) skew = forced_skew < rb - 1 ? forced_skew : rb - 1;
         }
         p.skew = skew;
     }
@@ -1188,34 +1191,23 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         }
     }
     if (NS < 1) return fail(RLK_ERR_UNSUPPORTED, "tile too wide for one shared-memory slot");
-    p.NS = NS;
-    p.ns_div = make_fastdiv((uint32_t)NS);
-    p.tps_div = make_fastdiv((uint32_t)p.tps);
-    const uint32_t smem = layout(p, NS);
 
-    void (*kfn)(Params) = nullptr;
-    if (ctas_per_sm == 2) {
-        kfn = (mode == kModeFwd)     ? stream_kernel<kModeFwd, 2>
-            : (mode == kModeBwd)     ? stream_kernel<kModeBwd, 2>
-            : (mode == kModeFusedL2) ? stream_kernel<kModeFusedL2, 2>
-                                     : stream_kernel<kModeFused, 2>;
-    } else {
-        kfn = (mode == kModeFwd)     ? stream_kernel<kModeFwd, 1>
-            : (mode == kModeBwd)     ? stream_kernel<kModeBwd, 1>
-            : (mode == kModeFusedL2) ? stream_kernel<kModeFusedL2, 1>
-                                     : stream_kernel<kModeFused, 1>;
-    }
-    const void* fn = reinterpret_cast<const void*>(kfn);
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-
+    auto pick = [&](int per_sm) -> void (*)(Params) {
+        if (per_sm == 2)
+            return (mode == kModeFwd)     ? stream_kernel<kModeFwd, 2>
+                 : (mode == kModeBwd)     ? stream_kernel<kModeBwd, 2>
+                 : (mode == kModeFusedL2) ? stream_kernel<kModeFusedL2, 2>
+                                          : stream_kernel<kModeFused, 2>;
+        return (mode == kModeFwd)     ? stream_kernel<kModeFwd, 1>
+             : (mode == kModeBwd)     ? stream_kernel<kModeBwd, 1>
+             : (mode == kModeFusedL2) ? stream_kernel<kModeFusedL2, 1>
+                                      : stream_kernel<kModeFused, 1>;
+    };
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.numAttrs = 0;
-    int64_t clusters = 0;
     if (p.C > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = (unsigned)p.C;
@@ -1223,20 +1215,68 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cfg.gridDim = dim3((unsigned)(p.C * (di.sm_count / p.C)), 1, 1);
-        int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, kfn, &cfg);
-        if (e != cudaSuccess || n <= 0)
-            return fail(RLK_ERR_CUDA, std::string("no cluster of ") + std::to_string(p.C) +
-                                          " CTAs fits: " + cudaGetErrorString(e));
-        clusters = n;
-    } else {
-        int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
-        if (e != cudaSuccess || per_sm <= 0)
-            return fail(RLK_ERR_CUDA, std::string("kernel does not fit on an SM: ") + cudaGetErrorString(e));
-        clusters = (int64_t)per_sm * di.sm_count;
     }
+    // Clusters (or CTAs when C = 1) resident at once for the kernel and
+    // shared-memory size; 0 with the message set when none fits.
+    auto resident = [&](void (*k)(Params), uint32_t bytes) -> int64_t {
+        const void* f = reinterpret_cast<const void*>(k);
+        cudaError_t err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (err != cudaSuccess) {
+            fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(err));
+            return 0;
+        }
+        cfg.dynamicSmemBytes = bytes;
+        if (p.C > 1) {
+            cfg.gridDim = dim3((unsigned)(p.C * (di.sm_count / p.C)), 1, 1);
+            int n = 0;
+            err = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
+            if (err != cudaSuccess || n <= 0) {
+                fail(RLK_ERR_CUDA, std::string("no cluster of ") + std::to_string(p.C) +
+                                       " CTAs fits: " + cudaGetErrorString(err));
+                return 0;
+            }
+            return n;
+        }
+        int per_sm = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f, kThreads, bytes);
+        if (err != cudaSuccess || per_sm <= 0) {
+            fail(RLK_ERR_CUDA, std::string("kernel does not fit on an SM: ") + cudaGetErrorString(err));
+            return 0;
+        }
+        return (int64_t)per_sm * di.sm_count;
+    };
+
+    uint32_t smem = layout(p, NS);
+    int64_t clusters = resident(pick(ctas_per_sm), smem);
+    if (clusters <= 0) return RLK_ERR_CUDA;
+    // kModeFusedL2 with clusters that leave SMs idle at one CTA per SM (8 CTAs
+    // per cluster on GB300's GPCs: 15 clusters, 120 of 152 SMs): two CTAs per
+    // SM cover them all; the skew drops to one row to keep the L2 reuse set.
+    if (mode == kModeFusedL2 && forced == 0 && ctas_per_sm == 1 &&
+        clusters * p.C * 10 < (int64_t)di.sm_count * 9) {
+        Params q = p;
+        q.skew = 1;
+        budget = (uint32_t)di.smem_optin / 2u - 1024u;
+        const int ns2 = max_slots(q);
+        if (ns2 >= kMinSlotsShared) {
+            const uint32_t smem2 = layout(q, ns2);
+            const int64_t clusters2 = resident(pick(2), smem2);
+            if (clusters2 > clusters) {
+                p = q;
+                NS = ns2;
+                smem = smem2;
+                clusters = clusters2;
+                ctas_per_sm = 2;
+            }
+        }
+    }
+    void (*kfn)(Params) = pick(ctas_per_sm);
+    p.NS = NS;
+    p.ns_div = make_fastdiv((uint32_t)NS);
+    p.tps_div = make_fastdiv((uint32_t)p.tps);
+    smem = layout(p, NS);
+    cfg.dynamicSmemBytes = smem;
+    cudaError_t e = cudaSuccess;
     if (clusters > p.T) clusters = p.T;
     cfg.gridDim = dim3((unsigned)(clusters * p.C), 1, 1);
     if (env_int("RLK_VERBOSE", 0))
