@@ -70,8 +70,12 @@ def block_schedule(mode, rows, skew=1):
     return seq
 
 
-def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80, rbufs=2, skew=1):
-    """mode: 'fwd' | 'bwd' | 'fused' | 'fused_l2'; rbufs row buffers, fused_l2 row skew.
+def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80, rbufs=2, skew=1,
+             producers=1, producer_seqcheck=True):
+    """mode: 'fwd' | 'bwd' | 'fused' | 'fused_l2'; rbufs row buffers, fused_l2 row skew;
+    producers: producer warps per CTA, producer p issuing the items i with i mod producers == p
+    (each waits until the slot's previous item is issued before its empty-barrier parity,
+    unless producer_seqcheck is off).
 
     Raises ProtocolError on a stale read or a deadlock."""
     rng = random.Random(seed)
@@ -139,12 +143,21 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
             return n * nch + ch
         return block_index[(phase, n)] * nch + ch
 
-    def producer(c):
+    def producer(c, pid):
         i = 0
         for _ in sched:
             for _ in range(nch):
+                if i % producers != pid:
+                    i += 1
+                    continue
                 s, par = ring(i)
+                if producer_seqcheck and i >= NS:
+                    while c.seq[s] != i - NS:
+                        yield "wait"
                 yield from wait(c.empty[s], par ^ 1)
+                if c.hdr[s] is not None and c.hdr[s] != i - NS:
+                    raise ProtocolError(f"{mode} producer {pid} reused slot {s} for item {i} "
+                                        f"while it held item {c.hdr[s]}")
                 c.hdr[s] = i
                 c.seq[s] = i
                 c.data[s] = None
@@ -264,7 +277,7 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
 
     agents = []
     for c in ctas:
-        agents.append(producer(c))
+        agents.extend(producer(c, pid) for pid in range(producers))
         if mode != "bwd":
             agents.append(fold(c))
         agents.extend(consumer(c, w) for w in range(W))

@@ -207,3 +207,28 @@ def test_division_by_invariant_divisors():
             [rng.randrange(1 << 32) for _ in range(200)]
         for n in ns:
             assert (((n * m) >> 32) + n) >> s == n // d, (d, n)
+
+
+@pytest.mark.parametrize("mode", ["fwd", "bwd", "fused_l2", "fused"])
+def test_two_producers_wait_for_the_slots_previous_item(mode):
+    # With two producer warps taking alternate items and an odd ring, the
+    # previous item of a slot belongs to the other producer; a producer that
+    # only waits on the empty barrier's parity can then run two phases ahead
+    # and overwrite a slot that is still in use.  Waiting first until the
+    # slot holds item i - NS closes it.
+    found = 0
+    resident = mode == "fused"
+    C, tps, rb = (4, 2, 2) if resident else (1, 3, 4)
+    odd_ns = 23 if resident else 7
+    if not resident:  # (the resident schedule holds its slots for two rows; the model finds no race there)
+        for seed in range(8):
+            try:
+                simulate(mode, rows=16, C=C, NT=64, tps=tps, NS=odd_ns, W=16, seed=seed, rbufs=rb,
+                         producers=2, producer_seqcheck=False, max_delay=150)
+            except ProtocolError:
+                found += 1
+        assert found > 0
+    for seed in range(4):
+        for ns in (odd_ns - 1, odd_ns):
+            simulate(mode, rows=16, C=C if mode != "bwd" else 1, NT=64, tps=tps, NS=ns, W=16, seed=seed,
+                     rbufs=rb, producers=2, max_delay=150)

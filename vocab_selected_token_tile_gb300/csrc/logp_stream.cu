@@ -60,8 +60,13 @@ namespace {
 
 constexpr int kConsumerWarps = 16;
 constexpr int kFoldWarp = kConsumerWarps;          // folds each row's partials
-constexpr int kProducerWarp = kConsumerWarps + 1;  // issues the bulk copies
-constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kProducerWarp = kConsumerWarps + 1;  // first of the warps that issue the bulk copies
+
+// Producer warps of a CTA: two when the CTA has the SM to itself (one
+// thread's bulk-copy issue rate does not keep up with HBM), one when two
+// CTAs share an SM (two producers per SM already, and no registers to spare).
+__host__ __device__ constexpr int producers_for(int per_sm) { return per_sm == 1 ? 2 : 1; }
+__host__ __device__ constexpr int threads_for(int per_sm) { return (kConsumerWarps + 1 + producers_for(per_sm)) * 32; }
 constexpr int kMaxSlots = 96;
 constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the final drain of own copies
 constexpr int64_t kL2ReuseBytes = 64ll << 20;  // logits held in L2 between the two reads of kModeFusedL2
@@ -497,8 +502,13 @@ struct MetaWindow {
     float g = 0.f, lin = 0.f;
 };
 
-template <int MODE>
-__device__ void producer(const Params& p, const Ctx& x) {
+// Producer warp pid of NP issues the items i with i mod NP == pid, in order.
+// Before the parity wait on a slot's empty barrier it waits until the slot
+// holds item i - NS: with several producers the slot's previous item may
+// belong to another one, and a parity wait while that item is not yet
+// issued could pass two phases ahead and overwrite a slot still in use.
+template <int MODE, int NP>
+__device__ void producer(const Params& p, const Ctx& x, int pid) {
     const int lane = x.lane;
     const uint64_t pol_first = l2_policy_evict_first();
     const uint64_t pol_last = l2_policy_evict_last();
@@ -550,14 +560,18 @@ __device__ void producer(const Params& p, const Ctx& x) {
         const int64_t row = x.q + n * x.G;
         const uint16_t* grow = p.a.logits + row * p.stride;
         for (int c = 0; c < x.nch; ++c) {
+            const bool mine = NP == 1 || (int)(issued % NP) == pid;
             bool ok = true;
-            if (lane == 0) ok = x.wt.wait(x.empty0 + 8u * slot, phase ^ 1u, false);
+            if (lane == 0 && mine) {
+                if (NP > 1 && issued >= p.NS) ok = x.wt.wait_value(x.seq + slot, (uint32_t)(issued - p.NS));
+                if (ok) ok = x.wt.wait(x.empty0 + 8u * slot, phase ^ 1u, false);
+            }
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) {
                 aborted = true;
                 break;
             }
-            if (lane == 0) {
+            if (lane == 0 && mine) {
                 SlotHdr h;
                 h.target = t;
                 h.g = g;
@@ -586,10 +600,11 @@ __device__ void producer(const Params& p, const Ctx& x) {
             }
         }
     }
-    // Drain: wait (bounded) until every copy this CTA issued has landed.
+    // Drain: wait (bounded) until every copy this warp issued has landed.
     if (lane == 0) {
         const int64_t first = issued > p.NS ? issued - p.NS : 0;
         for (int64_t j = first; j < issued; ++j) {
+            if (NP > 1 && (int)(j % NP) != pid) continue;
             const uint32_t s = (uint32_t)(j % p.NS), par = (uint32_t)((j / p.NS) & 1);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(x.full0 + 8u * s, par)) {
@@ -810,6 +825,18 @@ __device__ __forceinline__ bool wait_item(const Ctx& x, const TileItem& it, uint
     return issued && landed;
 }
 
+// Guard of every tile: the slot's header must name the row this CTA expects.
+// A slip of the ring protocol then stops the kernel with a status bit instead
+// of addressing another row's memory.
+__device__ __forceinline__ bool header_ok(const Params& p, const Ctx& x, const SlotHdr& h, int64_t n) {
+    if (h.row == x.q + n * x.G) return true;
+    if (x.lane == 0) {
+        atomicOr(p.a.status, kStatusInternal);
+        *x.wt.abort_flag = 1;
+    }
+    return false;
+}
+
 __device__ __forceinline__ int first_tile(const Ctx& x, int64_t n) {
     constexpr int W = kConsumerWarps;
     return (x.warp - (int)((n * x.ntl) & (W - 1))) & (W - 1);
@@ -835,6 +862,10 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
             break;
         }
         const SlotHdr h = x.hdr[it.slot];
+        if (!header_ok(p, x, h, n)) {
+            ok = false;
+            break;
+        }
         const Span sp = chunk_span(it.kf, it.kl, p);
         const uint16_t* grow = p.a.logits + h.row * p.stride;
         const int k = x.k0 + l;
@@ -881,6 +912,7 @@ __device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0
         const TileItem it = tile_item(p, x, item0, l);
         if (kWaits && !wait_item(x, it, it.item)) return false;
         const SlotHdr h = x.hdr[it.slot];
+        if (!header_ok(p, x, h, n)) return false;
         const Span sp = chunk_span(it.kf, it.kl, p);
         const int k = x.k0 + l;
         const TileGeom tg = tile_geom(k, p, sp);
@@ -931,7 +963,7 @@ __device__ void consumer(const Params& p, const Ctx& x) {
 
 // PER_SM: CTAs resident per SM (1 or 2); the register budget follows from it.
 template <int MODE, int PER_SM>
-__global__ void __launch_bounds__(kThreads, PER_SM) stream_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(threads_for(PER_SM), PER_SM) stream_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) unsigned char smem[];
     Ctx x;
     x.warp = threadIdx.x >> 5;
@@ -982,8 +1014,8 @@ __global__ void __launch_bounds__(kThreads, PER_SM) stream_kernel(const __grid_c
     }
     if (p.C > 1) cluster_sync_all(); else __syncthreads();
 
-    if (x.warp == kProducerWarp) {
-        producer<MODE>(p, x);
+    if (x.warp >= kProducerWarp) {
+        producer<MODE, producers_for(PER_SM)>(p, x, x.warp - kProducerWarp);
     } else if (x.warp == kFoldWarp) {
         if (MODE != kModeBwd) fold_warp<MODE>(p, x);
     } else {
@@ -1205,7 +1237,7 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     };
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads_for(ctas_per_sm), 1, 1);
     cfg.stream = stream;
     cfg.numAttrs = 0;
     if (p.C > 1) {
@@ -1218,8 +1250,10 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     }
     // Clusters (or CTAs when C = 1) resident at once for the kernel and
     // shared-memory size; 0 with the message set when none fits.
-    auto resident = [&](void (*k)(Params), uint32_t bytes) -> int64_t {
+    auto resident = [&](int per_sm, uint32_t bytes) -> int64_t {
+        void (*k)(Params) = pick(per_sm);
         const void* f = reinterpret_cast<const void*>(k);
+        cfg.blockDim = dim3(threads_for(per_sm), 1, 1);
         cudaError_t err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
         if (err != cudaSuccess) {
             fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(err));
@@ -1237,17 +1271,17 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
             }
             return n;
         }
-        int per_sm = 0;
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f, kThreads, bytes);
-        if (err != cudaSuccess || per_sm <= 0) {
+        int blocks = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, f, (int)cfg.blockDim.x, bytes);
+        if (err != cudaSuccess || blocks <= 0) {
             fail(RLK_ERR_CUDA, std::string("kernel does not fit on an SM: ") + cudaGetErrorString(err));
             return 0;
         }
-        return (int64_t)per_sm * di.sm_count;
+        return (int64_t)blocks * di.sm_count;
     };
 
     uint32_t smem = layout(p, NS);
-    int64_t clusters = resident(pick(ctas_per_sm), smem);
+    int64_t clusters = resident(ctas_per_sm, smem);
     if (clusters <= 0) return RLK_ERR_CUDA;
     // kModeFusedL2 with clusters that leave SMs idle at one CTA per SM (8 CTAs
     // per cluster on GB300's GPCs: 15 clusters, 120 of 152 SMs): two CTAs per
@@ -1260,7 +1294,7 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         const int ns2 = max_slots(q);
         if (ns2 >= kMinSlotsShared) {
             const uint32_t smem2 = layout(q, ns2);
-            const int64_t clusters2 = resident(pick(2), smem2);
+            const int64_t clusters2 = resident(2, smem2);
             if (clusters2 > clusters) {
                 p = q;
                 NS = ns2;
@@ -1271,6 +1305,7 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         }
     }
     void (*kfn)(Params) = pick(ctas_per_sm);
+    cfg.blockDim = dim3(threads_for(ctas_per_sm), 1, 1);
     p.NS = NS;
     p.ns_div = make_fastdiv((uint32_t)NS);
     p.tps_div = make_fastdiv((uint32_t)p.tps);

@@ -84,6 +84,8 @@ rlk_status select_device(const void* ptr) {
 }
 
 rlk_status decode_status(uint32_t bits) {
+    if (bits & kStatusInternal)
+        return fail(RLK_ERR_CUDA, "a streaming kernel found a ring slot holding an unexpected row and stopped");
     if (bits & kStatusTimeout) return fail(RLK_ERR_TIMEOUT, "a bounded device-side wait expired");
     if (bits & kStatusTargetRange) return fail(RLK_ERR_TARGET_RANGE, "an active target lies outside [0, V_real)");
     if (bits & kStatusNonFinite)

@@ -16,6 +16,7 @@ enum : uint32_t {
     kStatusTargetRange = 1u << 0,
     kStatusNonFinite = 1u << 1,
     kStatusTimeout = 1u << 2,
+    kStatusInternal = 1u << 3,  // a kernel found its own bookkeeping inconsistent and stopped
 };
 
 constexpr int kMaxTiles = 1024;
