@@ -828,12 +828,14 @@ __device__ __forceinline__ bool wait_item(const Ctx& x, const TileItem& it, uint
 // Guard of every tile: the slot's header must name the row this CTA expects.
 // A slip of the ring protocol then stops the kernel with a status bit instead
 // of addressing another row's memory.
-__device__ __forceinline__ bool header_ok(const Params& p, const Ctx& x, const SlotHdr& h, int64_t n) {
-    if (h.row == x.q + n * x.G) return true;
-    if (x.lane == 0) {
-        atomicOr(p.a.status, kStatusInternal);
-        *x.wt.abort_flag = 1;
-    }
+__device__ __noinline__ void header_fail(uint32_t* status, volatile int* abort_flag) {
+    atomicOr(status, kStatusInternal);
+    *abort_flag = 1;
+}
+
+__device__ __forceinline__ bool header_ok(const Params& p, const Ctx& x, const SlotHdr& h, uint32_t want) {
+    if (__builtin_expect((uint32_t)h.row == want, 1)) return true;  // rows of one launch differ in their low 32 bits
+    if (x.lane == 0) header_fail(p.a.status, x.wt.abort_flag);
     return false;
 }
 
@@ -855,6 +857,7 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
     if (n >= p.rbufs) ok = x.wt.warp_wait(x.partfree0 + 8u * b, row_par(p, n - p.rbufs));
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
     const int slot_elems = p.slot_bytes / 2;
+    const uint32_t want = (uint32_t)(x.q + n * x.G);
     for (int l = first_tile(x, n); l < x.ntl && ok; l += W) {
         const TileItem it = tile_item(p, x, item0, l);
         if (!wait_item(x, it, it.item)) {
@@ -862,7 +865,7 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
             break;
         }
         const SlotHdr h = x.hdr[it.slot];
-        if (!header_ok(p, x, h, n)) {
+        if (!header_ok(p, x, h, want)) {
             ok = false;
             break;
         }
@@ -908,11 +911,12 @@ __device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0
     const int lane = x.lane;
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
     const int slot_elems = p.slot_bytes / 2;
+    const uint32_t want = (uint32_t)(x.q + n * x.G);
     for (int l = first_tile(x, n); l < x.ntl; l += W) {
         const TileItem it = tile_item(p, x, item0, l);
         if (kWaits && !wait_item(x, it, it.item)) return false;
         const SlotHdr h = x.hdr[it.slot];
-        if (!header_ok(p, x, h, n)) return false;
+        if (!header_ok(p, x, h, want)) return false;
         const Span sp = chunk_span(it.kf, it.kl, p);
         const int k = x.k0 + l;
         const TileGeom tg = tile_geom(k, p, sp);
