@@ -29,6 +29,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <cstdlib>
 #include <mutex>
 #include <string>
 
@@ -38,6 +39,11 @@
 
 namespace rlk {
 namespace {
+
+int env_int_lm(const char* name, int dflt) {
+    const char* v = std::getenv(name);
+    return (v && *v) ? std::atoi(v) : dflt;
+}
 
 constexpr int kBM = 128;  // token rows per unit (TMEM lanes)
 constexpr int kBN = 256;  // vocabulary rows per chunk (accumulator columns)
@@ -63,7 +69,8 @@ struct LmParams {
     int64_t T, Vr, Vp, ignore_index;
     uint64_t wait_ns;
     int32_t K, NT, W, vtp, nchunk, rem, mask_mode;
-    int32_t MB;  // token blocks
+    int32_t MB;    // token blocks
+    int32_t pair;  // CTAs per cluster: 2 = two token blocks share each weight chunk (multicast), else 1
 };
 
 struct Bars {
@@ -77,26 +84,33 @@ struct Bars {
 };
 
 // Units of this CTA: the tiles of its virtual-TP shard times the token
-// blocks, tile-major, strided over the CTAs of its group.
+// blocks, tile-major, strided over the clusters of its group.  With pairs
+// (p.pair = 2) a unit is a tile times a pair of token blocks: rank r of the
+// cluster takes block 2i + r (which may lie past the last block; its rows
+// are then out of range and masked).  The group of a cluster is a
+// contiguous run of clusters, so both ranks see the same units.
 struct UnitSeq {
     int64_t u, step, end;
-    int tile0, ntile_sh, MB;
+    int tile0, ntile_sh, MBU, rank, pair;
     __device__ void init(const LmParams& p) {
-        const int G = gridDim.x;
+        pair = p.pair;
+        const int cl = blockIdx.x / pair;
+        rank = blockIdx.x % pair;
+        const int G = gridDim.x / pair;
         const int Gj = G / p.vtp;
-        const int j = blockIdx.x / Gj;
-        const int c = blockIdx.x % Gj;
+        const int j = cl / Gj;
+        const int c = cl % Gj;
         ntile_sh = p.NT / p.vtp;
         tile0 = j * ntile_sh;
-        MB = p.MB;
+        MBU = (p.MB + pair - 1) / pair;
         u = c;
         step = Gj;
-        end = (int64_t)ntile_sh * MB;
+        end = (int64_t)ntile_sh * MBU;
     }
     __device__ bool next(int& tile, int& mb) {
         if (u >= end) return false;
-        tile = tile0 + (int)(u / MB);
-        mb = (int)(u % MB);
+        tile = tile0 + (int)(u / MBU);
+        mb = (int)(u % MBU) * pair + rank;
         u += step;
         return true;
     }
@@ -184,6 +198,8 @@ template <int EPI>
 __global__ void __launch_bounds__(kThreadsLm, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmWr, const __grid_constant__ LmParams p) {
+    // With pairs, tmW and tmWr describe half a chunk (128 rows, rem/2 rows):
+    // each rank loads its half and multicasts it to both CTAs.
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzled operand tiles.
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -196,7 +212,8 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&bars->full[s]), 1);
-            mbar_init(smem_u32(&bars->empty[s]), 1);
+            // with pairs a stage is free once both CTAs' MMAs have read it
+            mbar_init(smem_u32(&bars->empty[s]), (uint32_t)p.pair);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bars->tfull[b]), 1);
@@ -212,6 +229,8 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
     }
     tc_fence_before();
     __syncthreads();
+    // the peer's barriers must be initialised before any multicast or commit reaches them
+    if (p.pair > 1) cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_addr;
 
@@ -238,7 +257,14 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                         const uint32_t fb = smem_u32(&bars->full[stage]);
                         mbar_arrive_expect_tx(fb, kStageA + (uint32_t)nrows * kBK * 2);
                         tma_load_2d(smem_u32(sA + stage * kStageA), &tmH, kb * kBK, mb * kBM, fb);
-                        tma_load_2d(smem_u32(sB + stage * kStageB), last_rem ? &tmWr : &tmW, kb * kBK, n0, fb);
+                        if (p.pair == 1) {
+                            tma_load_2d(smem_u32(sB + stage * kStageB), last_rem ? &tmWr : &tmW, kb * kBK, n0, fb);
+                        } else {
+                            // rows [rank*half, (rank+1)*half) of the chunk, to both CTAs
+                            const int half = nrows / 2;
+                            tma_load_2d_mc(smem_u32(sB + stage * kStageB + us.rank * half * (kBK * 2)),
+                                           last_rem ? &tmWr : &tmW, kb * kBK, n0 + us.rank * half, fb, 0x3);
+                        }
                         ++issued;
                         if (++stage == kStages) {
                             stage = 0;
@@ -285,7 +311,11 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                         for (int kk = 0; kk < kBK / 16; ++kk)
                             umma_bf16(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
                                       (kb | kk) != 0);
-                        umma_commit(smem_u32(&bars->empty[stage]));  // frees the stage when these MMAs finish
+                        // frees the stage (in both CTAs of a pair) when these MMAs finish
+                        if (p.pair == 1)
+                            umma_commit(smem_u32(&bars->empty[stage]));
+                        else
+                            umma_commit_mc(smem_u32(&bars->empty[stage]), 0x3);
                         if (++stage == kStages) {
                             stage = 0;
                             phase ^= 1u;
@@ -371,6 +401,8 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    // no CTA of a pair leaves while the other may still multicast or commit into it
+    if (p.pair > 1) cluster_sync_all();
 }
 
 // LSE and logp of each row from its tile partials (one warp per row).
@@ -458,6 +490,10 @@ struct LmLaunch {
     int grid, sms;
 };
 
+// Pairs of CTAs share each weight chunk when every virtual-TP group gets a
+// whole number of pairs on the SMs (all but virtual TP 8 on 152 SMs); the
+// number of pairs per group stays within the group's units.
+
 rlk_status prepare(LmLaunch& L, const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
                    const int64_t* targets, const uint8_t* mask, uint32_t* status) {
     int dev = 0;
@@ -482,14 +518,19 @@ rlk_status prepare(LmLaunch& L, const rlk_logp_contract& c, const void* hidden, 
     p.rem = p.W % kBN;
     p.mask_mode = c.mask_mode;
     p.MB = (int32_t)((c.T + kBM - 1) / kBM);
-    if (!make_map(&L.tmH, hidden, c.T, H, kBM) || !make_map(&L.tmW, weight, c.V_padded, H, kBN) ||
-        !make_map(&L.tmWr, weight, c.V_padded, H, p.rem ? (uint32_t)p.rem : (uint32_t)kBN))
+    const int forced = env_int_lm("RLK_LMHEAD_PAIR", 0);
+    p.pair = ((sms / 2) % c.virtual_tp == 0 && p.MB >= 2) ? 2 : 1;
+    if (forced == 1 || forced == 2) p.pair = forced;
+    const uint32_t brows = p.pair == 2 ? kBN / 2 : kBN;
+    const uint32_t rrows = p.rem ? (uint32_t)p.rem / (uint32_t)p.pair : brows;
+    if (!make_map(&L.tmH, hidden, c.T, H, kBM) || !make_map(&L.tmW, weight, c.V_padded, H, brows) ||
+        !make_map(&L.tmWr, weight, c.V_padded, H, rrows))
         return fail(RLK_ERR_CUDA, "cuTensorMapEncodeTiled failed for the hidden or weight tensor");
-    const int64_t units_per_shard = (int64_t)(c.num_tiles / c.virtual_tp) * p.MB;
-    int64_t per_group = sms / c.virtual_tp;
+    const int64_t units_per_shard = (int64_t)(c.num_tiles / c.virtual_tp) * ((p.MB + p.pair - 1) / p.pair);
+    int64_t per_group = sms / p.pair / c.virtual_tp;  // clusters per virtual-TP group
     if (per_group > units_per_shard) per_group = units_per_shard;
     if (per_group < 1) per_group = 1;
-    L.grid = (int)(per_group * c.virtual_tp);
+    L.grid = (int)(per_group * c.virtual_tp * p.pair);
     L.sms = sms;
     return RLK_OK;
 }
@@ -499,8 +540,24 @@ rlk_status run_gemm(const LmLaunch& L, cudaStream_t stream) {
     const size_t smem = 1024 + (size_t)kStages * (kStageA + kStageB) + sizeof(Bars);
     cudaError_t e = cudaFuncSetAttribute(lmhead_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-    lmhead_kernel<EPI><<<L.grid, kThreadsLm, smem, stream>>>(L.tmH, L.tmW, L.tmWr, L.p);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)L.grid, 1, 1);
+    cfg.blockDim = dim3(kThreadsLm, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.numAttrs = 0;
+    if (L.p.pair > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)L.p.pair;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // The two CTAs of a pair wait on each other; the hardware schedules a
+        // cluster's CTAs together, and pairs never wait on other pairs.
+    }
+    e = cudaLaunchKernelEx(&cfg, lmhead_kernel<EPI>, L.tmH, L.tmW, L.tmWr, L.p);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("lm_head GEMM launch: ") + cudaGetErrorString(e));
     return RLK_OK;
 }
