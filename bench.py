@@ -49,6 +49,8 @@ def parse():
                     help="profiling only: shrink the batch to this many rows (not a bench number)")
     ap.add_argument("--path", default="fused", choices=["fused", "fwd", "split", "lmhead"],
                     help="profiling only: time the forward kernel or the split path instead of the fused step")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="--impl reference: CPU seconds spread over the warm-up and timed steps")
     return ap.parse_args()
 
 
@@ -57,6 +59,16 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def max_over_ranks(x, device):
+    """The largest value of x over the ranks of the default process group (x itself with one rank)."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
 
 
 def kernel_hash():
@@ -246,9 +258,7 @@ def run_ours(args, ws, rank, local):
     total_ms = t_begin.elapsed_time(t_end)
     per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
 
     hbm_peak, bf16_peak, peak_kind = measured_peaks()
@@ -463,7 +473,7 @@ def main():
         per_step = []
         sample_desc = None
         steps = max(1, args.steps)
-        budget = max(2.0, 120.0 / (steps + args.warmup))
+        budget = max(0.5, args.ref_seconds / (steps + args.warmup))
         for i in range(args.warmup + steps):
             tps, rows, secs = time_oracle(W.GRPO, budget_s=budget, max_rows=4096)
             if i >= args.warmup:
