@@ -69,7 +69,8 @@ typedef enum {
     RLK_ERR_TARGET_RANGE = 5,  /* an active target outside [0, V_real) (device status) */
     RLK_ERR_NONFINITE_LSE = 6, /* an active row's LSE is not finite (device status) */
     RLK_ERR_TIMEOUT = 7,       /* a bounded device-side wait expired (device status) */
-    RLK_ERR_CUDA = 8           /* a CUDA runtime call failed */
+    RLK_ERR_CUDA = 8           /* a CUDA runtime call failed, or (device status) a streaming kernel found a ring
+                                  slot holding an unexpected row and stopped before touching memory */
 } rlk_status;
 
 typedef enum {

@@ -23,16 +23,18 @@
 // identity (-inf, 0) when it has no finite column; partials are merged in
 // fixed global tile order.  Virtual TP (the H100 matrix document, "Fixes
 // exercised": fixed virtual TP8) is a cluster of virtual_tp CTAs: CTA j owns
-// the tile-aligned shard j, computes its tiles' partials and pushes them into
-// every peer's shared memory (the on-chip analogue of the pages' all-gather);
-// every CTA then folds all num_tiles partials in index order, so the result
-// does not depend on virtual_tp.
+// the tile-aligned shard j and computes its tiles' partials; each row's
+// shards meet in the shared memory of one CTA, the row's folder, which folds
+// all num_tiles partials in index order and returns the LSE to the others
+// (the on-chip analogue of the pages' gather), so the result does not depend
+// on virtual_tp.
 //
 // Layout of work.  Cluster q handles rows q, q + G, q + 2G, ... (G clusters).
-// Within a CTA, warp kConsumerWarps is the producer: lane 0 streams each
-// (row, tile) item's 16-byte-aligned column span into a ring slot with a 1-D
-// bulk copy (cp.async.bulk, completion on the slot's "full" mbarrier).  The
-// other warps consume items round-robin; one warp reduces one tile.  Within a
+// Within a CTA, 16 consumer warps reduce tiles (one warp per tile), one warp
+// runs the exchange and fold, and one or two producer warps stream each item
+// (one row's chunk of consecutive tiles, its 16-byte-aligned column span)
+// into a ring slot with a 1-D bulk copy (cp.async.bulk, completion on the
+// slot's "full" mbarrier).  Within a
 // tile the order of arithmetic depends only on the tile's columns: lane l
 // takes 8-column groups l, l+32, ... from the aligned start; the exact tile
 // maximum is formed first (packed BF16 max), then sum exp(x - m) in FP32, and
