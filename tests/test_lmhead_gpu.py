@@ -210,3 +210,27 @@ def test_lmhead_backward_full_shape():
     col_sum = dwb[:v_real].float().sum(dim=0)
     col_abs = dwb[:v_real].float().abs().sum(dim=0)
     assert (col_sum.abs() <= 2.0 ** -6 * col_abs + 1e-6).all()
+
+
+def test_lmhead_cta_pairs_change_no_bit(monkeypatch):
+    """CTA pairs (token blocks 2i and 2i+1 sharing each weight chunk by
+    multicast) run the same per-tile arithmetic as single CTAs: logp, LSE and
+    both gradients are bitwise equal.  Three token blocks: the last pair's
+    second CTA reads out-of-range rows only."""
+    T, H, v_real, v_padded, nt = 300, 128, 2380, 2384 * 2, 2
+    hb, wb = make(T, H, v_real, v_padded, seed=11)
+    tgt = synth.targets(T, v_real, seed=12)
+    mask = (np.arange(T) % 3 != 0).astype(np.uint8)
+    g = np.where(mask != 0, np.random.default_rng(13).standard_normal(T), 0.0).astype(np.float32)
+    outs = {}
+    for pair in ("1", "2"):
+        monkeypatch.setenv("RLK_LMHEAD_PAIR", pair)
+        c = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=nt, virtual_tp=2, validate=1)
+        logp, lse, dh, dw = rlk.logp_fused_lmhead(c, dev(hb), dev(wb), torch.from_numpy(tgt).cuda(),
+                                                  torch.from_numpy(mask).cuda(), grad=torch.from_numpy(g).cuda())
+        torch.cuda.synchronize()
+        outs[pair] = [t.cpu().numpy().tobytes() for t in (logp, lse, dh, dw)]
+    assert outs["1"] == outs["2"]
+    ref_logp, ref_lse, _ = oracle.lmhead_forward(hb, wb, tgt, mask != 0, v_real)
+    logp = np.frombuffer(outs["2"][0], dtype=np.float32)
+    close("logp", logp, ref_logp)
