@@ -196,6 +196,27 @@ def test_fused_schedules_agree_bitwise(monkeypatch):
             assert (sha(logp), sha(lse)) == ref[:2], (per_sm, vtp)
 
 
+def test_host_pipelined_call_equals_one_device_call():
+    """logp_fwd_bwd_host copies ragged row chunks on a second stream while the
+    previous chunk computes; rows are independent, so every output is
+    bitwise that of one call on the whole batch."""
+    from synth import workloads as W
+    w = W.QWEN3
+    bits = W.logits_host(w)
+    tgt = W.targets(w)
+    active = tgt != w.ignore_index
+    g = W.grad(w, active)
+    c = contract(w.T, w.v_real, w.v_padded, w.num_tiles, 2, rlk.MASK_IGNORE_INDEX)
+    dl_ref, logp_ref, lse_ref = rlk.logp_fwd_bwd(c, to_dev(bits), torch.from_numpy(tgt).cuda(), None,
+                                                 torch.from_numpy(g).cuda())
+    h_logits = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).pin_memory()
+    dl, logp, lse = rlk.logp_fwd_bwd_host(c, h_logits, torch.from_numpy(tgt).pin_memory(), None,
+                                          torch.from_numpy(g).pin_memory(), torch.device("cuda"), chunk_rows=1000)
+    torch.cuda.synchronize()
+    assert torch.equal(dl, dl_ref)
+    assert torch.equal(logp, logp_ref.cpu()) and torch.equal(lse, lse_ref.cpu())
+
+
 def test_device_generator_matches_host():
     from synth import workloads as W
     w = W.QWEN3

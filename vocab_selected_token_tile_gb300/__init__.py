@@ -234,6 +234,63 @@ def logp_fwd_bwd(contract, logits, targets, mask, grad, dlogits=None, stream=Non
     return dlogits, logp, lse
 
 
+def logp_fwd_bwd_host(contract, logits, targets, mask, grad, device, chunk_rows=8192, dlogits=None,
+                      staging=None):
+    """Fused forward+backward of inputs in (pinned) host memory.
+
+    Row chunks of ``logits`` (host, [T, row_stride] bf16/int16) are copied to
+    the device on a copy stream while the previous chunk computes on the
+    current stream; rows are independent, so the results are bitwise those of
+    one call on the whole batch.  ``targets`` int64 [T], ``mask`` uint8 [T]
+    (None in ignore_index mode) and ``grad`` float32 [T] are host tensors too.
+    ``staging`` (device, like ``logits``) and ``dlogits`` (device) may be
+    passed to reuse allocations.  Returns (dlogits on the device, logp and LSE
+    in pinned host memory); the copies back are enqueued on the current
+    stream, so synchronise it before reading them.  With contract.validate the
+    call synchronises and checks every chunk's status.
+    """
+    import torch
+    T = contract.T
+    comp = torch.cuda.current_stream(device)
+    copy = torch.cuda.Stream(device)
+    d_logits = staging if staging is not None else torch.empty(logits.shape, dtype=logits.dtype, device=device)
+    d_dl = dlogits if dlogits is not None else torch.empty(logits.shape, dtype=logits.dtype, device=device)
+    d_tgt = torch.empty(T, dtype=torch.int64, device=device)
+    d_mask = torch.empty(T, dtype=torch.uint8, device=device) if mask is not None else None
+    d_g = torch.empty(T, dtype=torch.float32, device=device)
+    d_logp = torch.empty(T, dtype=torch.float32, device=device)
+    d_lse = torch.empty(T, dtype=torch.float32, device=device)
+    h_logp = torch.empty(T, dtype=torch.float32, pin_memory=True)
+    h_lse = torch.empty(T, dtype=torch.float32, pin_memory=True)
+    starts = list(range(0, T, chunk_rows))
+    ws = torch.zeros(max(len(starts), 1) * 256, dtype=torch.uint8, device=device)  # a status word per chunk
+    copy.wait_stream(comp)  # the buffers above exist before the copy stream writes them
+    with torch.cuda.stream(copy):
+        d_tgt.copy_(targets, non_blocking=True)
+        if mask is not None:
+            d_mask.copy_(mask, non_blocking=True)
+        d_g.copy_(grad, non_blocking=True)
+    for i, r0 in enumerate(starts):
+        r1 = min(T, r0 + chunk_rows)
+        with torch.cuda.stream(copy):
+            d_logits[r0:r1].copy_(logits[r0:r1], non_blocking=True)
+            landed = torch.cuda.Event()
+            landed.record(copy)
+        comp.wait_event(landed)
+        c = contract.replace(T=r1 - r0, validate=0)
+        check(rlk_logp_bwd(c, d_logits[r0].data_ptr(), d_tgt[r0:].data_ptr(),
+                           None if d_mask is None else d_mask[r0:].data_ptr(), None, d_g[r0:].data_ptr(),
+                           d_dl[r0].data_ptr(), d_logp[r0:].data_ptr(), d_lse[r0:].data_ptr(),
+                           ws[i * 256:].data_ptr(), comp.cuda_stream))
+    comp.wait_stream(copy)
+    h_logp.copy_(d_logp, non_blocking=True)
+    h_lse.copy_(d_lse, non_blocking=True)
+    if contract.validate:
+        for i in range(len(starts)):
+            check(rlk_logp_workspace_status(ws[i * 256:].data_ptr(), comp.cuda_stream))
+    return d_dl, h_logp, h_lse
+
+
 def logp_fused_lmhead(contract, hidden, weight, targets, mask=None, grad=None, stream=None, workspace=None):
     """Fused lm_head on BF16 hidden [T, H] and weight [V_padded, H] (GPU tensors).
 
