@@ -30,7 +30,9 @@ def layout(ns, slot_bytes, nt, rbufs=2):
 
 
 def row_bufs(mode, nt):
-    return 2 if mode in ("bwd", "fused") else (8 if nt <= 128 else 4 if nt <= 256 else 2)
+    if mode in ("bwd", "fused") or nt > 256:
+        return 2
+    return 8 if (mode == "fused_l2" and nt <= 128) else 4
 
 
 def ctas_per_sm(mode, vtp, v_padded, nt):
@@ -58,6 +60,9 @@ def plan(mode, vtp, v_padded, nt):
 
     C = 1 if mode == "bwd" else vtp
     tps = tps_target
+    if mode == "fused_l2":  # the largest divisor of the shard's tiles within 16384 columns
+        ntl = nt // C
+        tps = max(d for d in range(1, ntl + 1) if ntl % d == 0 and d * w <= 16384)
     if mode == "fused":
         while True:
             ntl = -(-nt // C)
@@ -134,6 +139,7 @@ def test_ring_protocol_reads_only_landed_slots(mode, vtp):
 def test_planner_replay_matches_the_benchmark_shapes():
     assert plan("fused", 2, 152576, 64) == (4, 2, 23)
     assert plan("fwd", 1, 152576, 64) == (1, 3, 7)
+    assert [plan("fused_l2", v, 152576, 64)[1:] for v in (1, 2, 4, 8)] == [(4, 11)] * 4
 
 
 @pytest.mark.parametrize("ns", [1, 2, 3, 5])

@@ -74,6 +74,7 @@ constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the final drain of ow
 constexpr int64_t kL2ReuseBytes = 64ll << 20;  // logits held in L2 between the two reads of kModeFusedL2
 constexpr int kMaxSkew = 4;
 constexpr int kMinSlotsShared = 4;  // fewest ring slots worth running two CTAs per SM
+constexpr int64_t kFusedChunkCols = 16384;
 
 struct SlotHdr {  // row metadata the producer writes beside each slot
     int64_t target;
@@ -1153,6 +1154,17 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         if (!(sch && std::string(sch) == "resident")) mode = kModeFusedL2;
     }
     int C = (mode == kModeBwd) ? 1 : c.virtual_tp;
+    // kModeFusedL2 issues twice the copies of the forward (both phases): it
+    // takes larger chunks, the largest number of tiles that divides the CTA's
+    // shard and stays within kFusedChunkCols columns (measured: 4 tiles of
+    // 2384 columns run 2-7% faster than 3 at every virtual TP).
+    if (mode == kModeFusedL2 && env_int("RLK_TPS", 0) == 0) {
+        const int ntl = c.num_tiles / C;
+        int best = 1;
+        for (int d = 1; d <= ntl; ++d)
+            if (ntl % d == 0 && (int64_t)d * p.W <= kFusedChunkCols) best = d;
+        set_chunk(best);
+    }
     // CTAs per SM.  Two streaming CTAs per SM double the bulk-copy issue rate
     // (two producer warps) and let clusters of 8 cover every SM: measured on
     // GB300 the forward streams at the copy bandwidth with two against 88% of
@@ -1178,7 +1190,10 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     // further behind phase A (short shards give short rows per CTA); they
     // cost rbufs * (8 * num_tiles + 128) bytes of shared memory.
     {
-        int rb = env_int("RLK_ROW_BUFS", c.num_tiles <= 128 ? 8 : c.num_tiles <= 256 ? 4 : 2);
+        // (measured at virtual TP 8: the forward runs 5% faster with 4 than with
+        // 8; the fused L2 schedule needs skew + 1 of them)
+        const int rb_default = c.num_tiles > 256 ? 2 : (mode == kModeFusedL2 && c.num_tiles <= 128) ? 8 : 4;
+        int rb = env_int("RLK_ROW_BUFS", rb_default);
         rb = rb >= kMaxRowBufs ? kMaxRowBufs : rb >= 4 ? 4 : 2;
         if (mode == kModeBwd || mode == kModeFused) rb = 2;
         p.rbufs = rb;
@@ -1289,27 +1304,6 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     uint32_t smem = layout(p, NS);
     int64_t clusters = resident(ctas_per_sm, smem);
     if (clusters <= 0) return RLK_ERR_CUDA;
-    // kModeFusedL2 with clusters that leave SMs idle at one CTA per SM (8 CTAs
-    // per cluster on GB300's GPCs: 15 clusters, 120 of 152 SMs): two CTAs per
-    // SM cover them all; the skew drops to one row to keep the L2 reuse set.
-    if (mode == kModeFusedL2 && forced == 0 && ctas_per_sm == 1 &&
-        clusters * p.C * 10 < (int64_t)di.sm_count * 9) {
-        Params q = p;
-        q.skew = 1;
-        budget = (uint32_t)di.smem_optin / 2u - 1024u;
-        const int ns2 = max_slots(q);
-        if (ns2 >= kMinSlotsShared) {
-            const uint32_t smem2 = layout(q, ns2);
-            const int64_t clusters2 = resident(2, smem2);
-            if (clusters2 > clusters) {
-                p = q;
-                NS = ns2;
-                smem = smem2;
-                clusters = clusters2;
-                ctas_per_sm = 2;
-            }
-        }
-    }
     void (*kfn)(Params) = pick(ctas_per_sm);
     cfg.blockDim = dim3(threads_for(ctas_per_sm), 1, 1);
     p.NS = NS;
