@@ -35,10 +35,22 @@ def row_bufs(mode, nt):
     return 8 if (mode == "fused_l2" and nt <= 128) else 4
 
 
-def ctas_per_sm(mode, vtp, v_padded, nt):
-    """CTAs per SM as the host planner picks them: two for the streaming modes,
-    one for both fused schedules."""
-    return 2 if mode in ("fwd", "bwd") else 1
+def ctas_per_sm(mode, vtp, v_padded, nt, sm_count=152, reuse_bytes=64 << 20):
+    """CTAs per SM as the host planner picks them: two for the streaming modes, one for the
+    resident fused schedule, two for the L2 fused schedule while one row of skew fits L2."""
+    if mode in ("fwd", "bwd"):
+        return 2
+    if mode == "fused_l2":
+        shard = -(-nt // vtp) * (v_padded // nt) * 2
+        return 2 if reuse_bytes // (shard * 2 * sm_count) >= 2 else 1
+    return 1
+
+
+def consumers_for(mode, per_sm):
+    """Consumer warps of a CTA, as the kernel instantiates them."""
+    if per_sm == 1:
+        return 16
+    return 8 if mode in ("fused", "fused_l2") else 12
 
 
 def plan(mode, vtp, v_padded, nt):
@@ -119,9 +131,10 @@ def test_kernel_block_numbering_matches_the_schedule():
 
 
 def test_l2_skew_at_the_benchmark_shapes():
-    # 152 SMs, 152576 x 64 tiles: virtual TP 1 and 2 keep one row of skew;
-    # 4 and 8 take four (the cap)
-    assert [l2_skew(v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 4, 4]
+    # 152 SMs, 152576 x 64 tiles: virtual TP 1, 2 (one CTA per SM) and 4 (two)
+    # keep one row of skew; 8 (two per SM) takes four, the cap
+    assert [l2_skew(v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 1, 4]
+    assert [ctas_per_sm("fused_l2", v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 2, 2]
 
 
 CONFIGS = [(mode, vtp) for mode in ("fwd", "bwd", "fused", "fused_l2") for vtp in (1, 2, 4, 8)
@@ -132,14 +145,16 @@ CONFIGS = [(mode, vtp) for mode in ("fwd", "bwd", "fused", "fused_l2") for vtp i
 def test_ring_protocol_reads_only_landed_slots(mode, vtp):
     C, tps, ns = plan_l2(vtp, 152576, 64) if mode == "fused_l2" else plan(mode, vtp, 152576, 64)
     skew = l2_skew(vtp, 152576, 64) if mode == "fused_l2" else 1
+    nw = consumers_for(mode, ctas_per_sm(mode, vtp, 152576, 64))
     for seed in range(3):
-        simulate(mode, rows=24, C=C, NT=64, tps=tps, NS=ns, W=16, seed=seed, rbufs=row_bufs(mode, 64), skew=skew)
+        simulate(mode, rows=24, C=C, NT=64, tps=tps, NS=ns, W=nw, seed=seed, rbufs=row_bufs(mode, 64), skew=skew,
+                 producers=2 if ctas_per_sm(mode, vtp, 152576, 64) == 1 else 1)
 
 
 def test_planner_replay_matches_the_benchmark_shapes():
     assert plan("fused", 2, 152576, 64) == (4, 2, 23)
     assert plan("fwd", 1, 152576, 64) == (1, 3, 7)
-    assert [plan("fused_l2", v, 152576, 64)[1:] for v in (1, 2, 4, 8)] == [(4, 11)] * 4
+    assert [plan("fused_l2", v, 152576, 64)[1:] for v in (1, 2, 4, 8)] == [(4, 11), (4, 11), (4, 5), (4, 5)]
 
 
 @pytest.mark.parametrize("ns", [1, 2, 3, 5])

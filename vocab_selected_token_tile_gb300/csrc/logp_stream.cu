@@ -30,7 +30,7 @@
 // on virtual_tp.
 //
 // Layout of work.  Cluster q handles rows q, q + G, q + 2G, ... (G clusters).
-// Within a CTA, 16 consumer warps reduce tiles (one warp per tile), one warp
+// Within a CTA, 8-16 consumer warps reduce tiles (one warp per tile), one warp
 // runs the exchange and fold, and one or two producer warps stream each item
 // (one row's chunk of consecutive tiles, its 16-byte-aligned column span)
 // into a ring slot with a 1-D bulk copy (cp.async.bulk, completion on the
@@ -60,15 +60,20 @@
 namespace rlk {
 namespace {
 
-constexpr int kConsumerWarps = 16;
-constexpr int kFoldWarp = kConsumerWarps;          // folds each row's partials
-constexpr int kProducerWarp = kConsumerWarps + 1;  // first of the warps that issue the bulk copies
-
-// Producer warps of a CTA: two when the CTA has the SM to itself (one
-// thread's bulk-copy issue rate does not keep up with HBM), one when two
-// CTAs share an SM (two producers per SM already, and no registers to spare).
+// Warps of a CTA: NW consumer warps (0 .. NW-1), the fold warp (NW), then the
+// producer warps.  Measured on GB300 (same-box sweeps of 8-30 consumer warps):
+//  * one CTA per SM: 16 consumer warps, two producers (one thread's bulk-copy
+//    issue rate does not keep up with HBM);
+//  * two CTAs per SM, one producer each: 12 consumer warps for the streaming
+//    modes and 8 for the fused ones -- fewer, fatter warps fit the halved
+//    register budget without spilling (16 spilled and ran up to 40% slower).
+__host__ __device__ constexpr int consumers_for(int mode, int per_sm) {
+    return per_sm == 1 ? 16 : (mode == kModeFused || mode == kModeFusedL2) ? 8 : 12;
+}
 __host__ __device__ constexpr int producers_for(int per_sm) { return per_sm == 1 ? 2 : 1; }
-__host__ __device__ constexpr int threads_for(int per_sm) { return (kConsumerWarps + 1 + producers_for(per_sm)) * 32; }
+__host__ __device__ constexpr int threads_for(int mode, int per_sm) {
+    return (consumers_for(mode, per_sm) + 1 + producers_for(per_sm)) * 32;
+}
 constexpr int kMaxSlots = 96;
 constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the final drain of own copies
 constexpr int64_t kL2ReuseBytes = 64ll << 20;  // logits held in L2 between the two reads of kModeFusedL2
@@ -842,18 +847,20 @@ __device__ __forceinline__ bool header_ok(const Params& p, const Ctx& x, const S
     return false;
 }
 
+// Consumer warp w of NW takes the tiles l of row n with (n*ntl + l) mod NW == w.
+template <int NW>
 __device__ __forceinline__ int first_tile(const Ctx& x, int64_t n) {
-    constexpr int W = kConsumerWarps;
-    return (x.warp - (int)((n * x.ntl) & (W - 1))) & (W - 1);
+    const int r = (int)((n * x.ntl) % NW);
+    const int f = x.warp - r;
+    return f < 0 ? f + NW : f;
 }
 
 // Phase A of row n for one consumer warp: the partials of its tiles, the
 // row metadata (tile 0) and the target logit (the tile that holds it).
 // FWD releases each tile's share of its slot at once; FUSED keeps the slots
 // for phase B.
-template <int MODE>
+template <int MODE, int W>
 __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0) {
-    constexpr int W = kConsumerWarps;
     const int lane = x.lane;
     const int b = row_buf(p, n);
     bool ok = true;
@@ -861,7 +868,7 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
     const int slot_elems = p.slot_bytes / 2;
     const uint32_t want = (uint32_t)(x.q + n * x.G);
-    for (int l = first_tile(x, n); l < x.ntl && ok; l += W) {
+    for (int l = first_tile<W>(x, n); l < x.ntl && ok; l += W) {
         const TileItem it = tile_item(p, x, item0, l);
         if (!wait_item(x, it, it.item)) {
             ok = false;
@@ -907,15 +914,14 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
 // lse_v is the fold's LSE.  FUSED_L2: the tile waits for the second copy of
 // its chunk; lse_v is the fold's LSE.  BWD: the tile waits for its chunk and
 // reads the row's LSE (lse_in) from the slot header.
-template <int MODE>
+template <int MODE, int W>
 __device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0, float lse_v) {
-    constexpr int W = kConsumerWarps;
     constexpr bool kWaits = MODE == kModeBwd || MODE == kModeFusedL2;
     const int lane = x.lane;
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
     const int slot_elems = p.slot_bytes / 2;
     const uint32_t want = (uint32_t)(x.q + n * x.G);
-    for (int l = first_tile(x, n); l < x.ntl; l += W) {
+    for (int l = first_tile<W>(x, n); l < x.ntl; l += W) {
         const TileItem it = tile_item(p, x, item0, l);
         if (kWaits && !wait_item(x, it, it.item)) return false;
         const SlotHdr h = x.hdr[it.slot];
@@ -936,9 +942,8 @@ __device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0
     return true;
 }
 
-template <int MODE>
+template <int MODE, int NW>
 __device__ void consumer(const Params& p, const Ctx& x) {
-    static_assert((kConsumerWarps & (kConsumerWarps - 1)) == 0, "consumer warp count must be a power of two");
     const int64_t R = x.nrows;
     const uint32_t nch = (uint32_t)x.nch;
     const int64_t S = (MODE == kModeFusedL2) ? p.skew : 1;
@@ -946,31 +951,33 @@ __device__ void consumer(const Params& p, const Ctx& x) {
     auto item_b = [&](int64_t n) { return (uint32_t)block_of(MODE, n, MODE != kModeFused, R, S) * nch; };
     if constexpr (MODE == kModeBwd) {
         for (int64_t n = 0; n < R; ++n)
-            if (!phase_b<MODE>(p, x, n, item_b(n), 0.f)) break;
+            if (!phase_b<MODE, NW>(p, x, n, item_b(n), 0.f)) break;
     } else if constexpr (MODE == kModeFwd) {
-        for (int64_t n = 0; n < R; ++n) phase_a<MODE>(p, x, n, item_a(n));
+        for (int64_t n = 0; n < R; ++n) phase_a<MODE, NW>(p, x, n, item_a(n));
     } else {
         // Skewed order A(0), ..., A(S-1), then A(n+S), B(n): the fold of row
         // n overlaps phase A of rows n+1..n+S.  kModeFused (S = 1) keeps two
         // rows of slots resident; kModeFusedL2 copies each row a second time
         // for phase B.  rbufs > S keeps rows[b].lse of row n until every warp
         // has read it: row n + rbufs comes after B(n) in every warp's order.
-        for (int64_t n = 0; n < S && n < R; ++n) phase_a<MODE>(p, x, n, item_a(n));
+        for (int64_t n = 0; n < S && n < R; ++n) phase_a<MODE, NW>(p, x, n, item_a(n));
         for (int64_t n = 0; n < R; ++n) {
-            if (n + S < R) phase_a<MODE>(p, x, n + S, item_a(n + S));
+            if (n + S < R) phase_a<MODE, NW>(p, x, n + S, item_a(n + S));
             const int b = row_buf(p, n);
             const bool ready = x.wt.warp_wait(x.lseready0 + 8u * b, row_par(p, n));
             // A failed wait anywhere sets the abort flag; the slot headers may
             // then be stale, so skip the writes (the status word already says
             // RLK_ERR_TIMEOUT).
-            if (ready && !*x.wt.abort_flag) phase_b<MODE>(p, x, n, item_b(n), x.rows[b].lse);
+            if (ready && !*x.wt.abort_flag) phase_b<MODE, NW>(p, x, n, item_b(n), x.rows[b].lse);
         }
     }
 }
 
 // PER_SM: CTAs resident per SM (1 or 2); the register budget follows from it.
 template <int MODE, int PER_SM>
-__global__ void __launch_bounds__(threads_for(PER_SM), PER_SM) stream_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(threads_for(MODE, PER_SM), PER_SM)
+    stream_kernel(const __grid_constant__ Params p) {
+    constexpr int NW = consumers_for(MODE, PER_SM);
     extern __shared__ __align__(1024) unsigned char smem[];
     Ctx x;
     x.warp = threadIdx.x >> 5;
@@ -1009,7 +1016,7 @@ __global__ void __launch_bounds__(threads_for(PER_SM), PER_SM) stream_kernel(con
             x.seq[s] = 0xFFFFFFFFu;
         }
         for (int b = 0; b < p.rbufs; ++b) {
-            mbar_init(x.rowdone0 + 8u * b, kConsumerWarps);
+            mbar_init(x.rowdone0 + 8u * b, NW);
             mbar_init(x.lseready0 + 8u * b, 1);
             mbar_init(x.partfree0 + 8u * b, 1);
             mbar_init(x.xbar0 + 8u * b, 1);    // the local arrival (with expect-tx on the folder)
@@ -1021,12 +1028,12 @@ __global__ void __launch_bounds__(threads_for(PER_SM), PER_SM) stream_kernel(con
     }
     if (p.C > 1) cluster_sync_all(); else __syncthreads();
 
-    if (x.warp >= kProducerWarp) {
-        producer<MODE, producers_for(PER_SM)>(p, x, x.warp - kProducerWarp);
-    } else if (x.warp == kFoldWarp) {
+    if (x.warp > NW) {
+        producer<MODE, producers_for(PER_SM)>(p, x, x.warp - NW - 1);
+    } else if (x.warp == NW) {
         if (MODE != kModeBwd) fold_warp<MODE>(p, x);
     } else {
-        consumer<MODE>(p, x);
+        consumer<MODE, NW>(p, x);
     }
 
     __syncthreads();
@@ -1168,12 +1175,13 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     // CTAs per SM.  Two streaming CTAs per SM double the bulk-copy issue rate
     // (two producer warps) and let clusters of 8 cover every SM: measured on
     // GB300 the forward streams at the copy bandwidth with two against 88% of
-    // it with one.  The fused modes keep one: the resident schedule needs the
-    // whole shared memory, and the L2 schedule measured slower with two (its
-    // rows between a row's two copies outgrow L2 at virtual TP 1-2, and at 4-8
-    // the smaller register budget spills).
+    // it with one.  The resident fused schedule needs the whole shared
+    // memory.  The L2 fused schedule takes two while the rows between a row's
+    // two copies, with one row of skew, still fit kL2ReuseBytes at twice the
+    // CTAs (virtual TP 4 and 8 at 152576 x 64 tiles; at TP 1-2 they outgrow L2).
     const int64_t shard_bytes = (int64_t)((c.num_tiles + C - 1) / C) * p.W * 2;
     int ctas_per_sm = (mode == kModeFwd || mode == kModeBwd) ? 2 : 1;
+    if (mode == kModeFusedL2 && kL2ReuseBytes / (shard_bytes * 2 * di.sm_count) >= 2) ctas_per_sm = 2;
     const int forced = env_int("RLK_CTAS_PER_SM", 0);
     if (forced == 1 || forced == 2) ctas_per_sm = forced;
     uint32_t budget = (uint32_t)di.smem_optin / (uint32_t)ctas_per_sm - 1024u;
@@ -1258,7 +1266,7 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     };
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(threads_for(ctas_per_sm), 1, 1);
+    cfg.blockDim = dim3(threads_for(mode, ctas_per_sm), 1, 1);
     cfg.stream = stream;
     cfg.numAttrs = 0;
     if (p.C > 1) {
@@ -1274,7 +1282,7 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     auto resident = [&](int per_sm, uint32_t bytes) -> int64_t {
         void (*k)(Params) = pick(per_sm);
         const void* f = reinterpret_cast<const void*>(k);
-        cfg.blockDim = dim3(threads_for(per_sm), 1, 1);
+        cfg.blockDim = dim3(threads_for(mode, per_sm), 1, 1);
         cudaError_t err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
         if (err != cudaSuccess) {
             fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(err));
@@ -1305,7 +1313,7 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     int64_t clusters = resident(ctas_per_sm, smem);
     if (clusters <= 0) return RLK_ERR_CUDA;
     void (*kfn)(Params) = pick(ctas_per_sm);
-    cfg.blockDim = dim3(threads_for(ctas_per_sm), 1, 1);
+    cfg.blockDim = dim3(threads_for(mode, ctas_per_sm), 1, 1);
     p.NS = NS;
     p.ns_div = make_fastdiv((uint32_t)NS);
     p.tps_div = make_fastdiv((uint32_t)p.tps);
