@@ -36,12 +36,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa),
-// releasing this thread's prior writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -50,7 +44,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Acquire at cluster scope: pairs with mbar_arrive_remote of a peer CTA.
+// Acquire at cluster scope: pairs with a peer CTA's release (st.async
+// complete-tx, or a cluster-scope arrive).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -224,10 +219,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
-}
-
 // Asynchronous 8-byte store into another CTA's shared memory (address from
 // mapa); its completion is counted in bytes on that CTA's mbarrier
 // `remote_bar` (also from mapa), with release semantics at cluster scope.
@@ -248,10 +239,6 @@ __device__ __forceinline__ void st_async_f32(uint32_t addr, float a, uint32_t re
 // All threads of all CTAs of the cluster; release/acquire at cluster scope.
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ----------------------------------------------------------------- arithmetic
