@@ -11,7 +11,8 @@ What it computes, and where the pages define it:
 
 * ``logprob`` -- the plain full-vocabulary definition (no tiles): LSE over the
   real vocabulary, the selected log-probability, and its gradient
-  ``g * (onehot(target) - softmax)``; plus the tiled method's own steps
+  ``g * (onehot(target) - softmax)``, and the softmax's entropy; plus the
+  tiled method's own steps
   (per-tile (max, sumexp) partials with the (-inf, 0) identity, merged in
   fixed tile-index order), so that the method's algebra can be pinned
   against the plain definition.
@@ -25,6 +26,7 @@ from .logprob import (  # noqa: F401
     active_rows,
     bf16_bits_to_f64,
     dlogits,
+    entropy,
     fold_partials,
     merge_partials,
     lse_full,

@@ -131,6 +131,27 @@ def dlogits(logits_bits, targets, active, grad, v_real, v_padded):
     return out
 
 
+def entropy(logits_bits, v_real):
+    """Entropy of each row's softmax over the real vocabulary, FP64, no tiles.
+
+    H_r = -sum_{c < v_real} p_rc log p_rc with p_r = softmax(x_r[:v_real]); a
+    column with p = 0 adds 0.  The pages log a mean policy entropy beside the
+    loss in their RL runs (the H100 matrix document, "Completed full-model
+    matrix"); the formula is Shannon's definition.  A row whose LSE is not
+    finite (all -inf, +inf or NaN in its real columns) has no distribution:
+    NaN.
+    """
+    x = bf16_bits_to_f64(np.asarray(logits_bits)[:, :v_real])
+    lse = lse_of_values(x)
+    with np.errstate(invalid="ignore", over="ignore", divide="ignore"):
+        logp = x - lse[:, None]
+        p = np.exp(logp)
+        terms = np.where(p > 0, -p * logp, 0.0)
+    h = terms.sum(axis=1)
+    h[~np.isfinite(lse)] = np.nan
+    return h
+
+
 def tile_bounds(v_padded, num_tiles):
     """Column ranges [k*W, (k+1)*W) of the num_tiles global tiles, W = v_padded / num_tiles."""
     if num_tiles <= 0 or v_padded % num_tiles:

@@ -368,3 +368,80 @@ def test_pins_catch_planted_mistakes():
     assert not _pins_pass(oracle.lse_full, dlogits_sign_flipped, oracle.fold_partials)
     assert not _pins_pass(oracle.lse_full, dlogits_onehot_shifted, oracle.fold_partials)
     assert not _pins_pass(oracle.lse_full, oracle.dlogits, fold_without_rescale)
+
+
+# ------------------------------------------------------------------ entropy
+
+def _row(vals):
+    """One row of BF16 bits from values that BF16 holds exactly."""
+    v = np.asarray(vals, dtype=np.float32)
+    return (v.view(np.uint32) >> 16).astype(np.uint16)[None, :]
+
+
+def _entropy_pins_pass(fn):
+    """Every entropy pin, for an entropy implementation fn(bits, v_real)."""
+    import math
+    try:
+        for v_real, c in ((1, 0.0), (7, 3.0), (151936, -2.5)):  # uniform: log V (five padded columns)
+            if abs(fn(_row([c] * (v_real + 5)), v_real)[0] - np.log(v_real)) > 1e-9 * max(1.0, np.log(v_real)):
+                return False
+        V = 1000
+        for a in (1.0, 4.0, 16.0):  # one column at a, V-1 at 0: H = log Z - a e^a / Z
+            vals = np.zeros(V, dtype=np.float32)
+            vals[17] = a
+            Z = np.exp(a) + (V - 1)
+            if abs(fn(_row(vals), V)[0] - (np.log(Z) - a * np.exp(a) / Z)) > 1e-9:
+                return False
+        rng = np.random.default_rng(5)
+        for V in (1, 2, 3, 9):  # direct summation
+            vals = rng.integers(-12, 12, size=V).astype(np.float32) / 4.0
+            ex = [math.exp(float(v)) for v in vals]
+            Z = sum(ex)
+            if abs(fn(_row(vals), V)[0] + sum((e / Z) * math.log(e / Z) for e in ex)) > 1e-12:
+                return False
+        # shift and permutation invariance, 0 <= H <= log V; values k/4 with |k| <= 64 need at
+        # most 7 significant bits, also after +8: exact in BF16
+        rng = np.random.default_rng(6)
+        x = (rng.integers(-64, 65, size=(4, 333)) / 4.0).astype(np.float32)
+        bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+        h = fn(bits, 333)
+        shifted = ((x + np.float32(8.0)).view(np.uint32) >> 16).astype(np.uint16)
+        if not np.allclose(fn(shifted, 333), h, atol=1e-9, rtol=0):
+            return False
+        if not np.allclose(fn(bits[:, rng.permutation(333)], 333), h, atol=1e-12, rtol=0):
+            return False
+        return bool(np.all(h >= 0) and np.all(h <= np.log(333) + 1e-12))
+    except (ValueError, FloatingPointError):
+        return False
+
+
+def test_entropy_pins():
+    assert _entropy_pins_pass(oracle.entropy)
+
+
+def test_entropy_pins_catch_planted_mistakes():
+    def with_padding(bits, v_real):
+        return oracle.entropy(bits, np.asarray(bits).shape[1])
+
+    def sign_flipped(bits, v_real):
+        return -oracle.entropy(bits, v_real)
+
+    def log2_based(bits, v_real):
+        return oracle.entropy(bits, v_real) / np.log(2.0)
+
+    def unnormalised(bits, v_real):         # p = exp(x - max) instead of exp(x - LSE)
+        x = oracle.bf16_bits_to_f64(np.asarray(bits)[:, :v_real])
+        q = np.exp(x - x.max(axis=1, keepdims=True))
+        with np.errstate(divide="ignore", invalid="ignore"):
+            return np.where(q > 0, -q * np.log(q), 0.0).sum(axis=1)
+
+    for mistake in (with_padding, sign_flipped, log2_based, unnormalised):
+        assert not _entropy_pins_pass(mistake), mistake.__name__
+
+
+def test_entropy_special_rows():
+    ninf = np.float32(-np.inf)
+    bits = np.concatenate([_row([ninf, ninf, 0.0, ninf]), _row([ninf] * 4), _row([np.nan, 0, 0, 0])])
+    h = oracle.entropy(bits, 4)
+    assert h[0] == 0.0  # a single finite column: a point mass
+    assert np.isnan(h[1]) and np.isnan(h[2])
