@@ -395,6 +395,24 @@ def extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, V
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / args.steps
         out[name] = {"ms": ms, "tokens_per_s": T / ms * 1e3, "alg_gbs": T * (2 * Vr + 2 * Vp + 21) / ms / 1e6}
+    # the forward with the entropy of each row (one pass; one more FMA per pair of logits)
+    cf = c.replace(virtual_tp=1)
+    ent = torch.empty(T, dtype=torch.float32, device=logits.device)
+    ws_e = rlk.workspace_for(cf, logits.device, stream)
+    for _ in range(3):
+        rlk.check(rlk.rlk_logp_fwd_entropy(cf, logits.data_ptr(), targets.data_ptr(), dmask.data_ptr(),
+                                           logp.data_ptr(), lse.data_ptr(), ent.data_ptr(), ws_e.data_ptr(),
+                                           stream.cuda_stream))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        rlk.check(rlk.rlk_logp_fwd_entropy(cf, logits.data_ptr(), targets.data_ptr(), dmask.data_ptr(),
+                                           logp.data_ptr(), lse.data_ptr(), ent.data_ptr(), ws_e.data_ptr(),
+                                           stream.cuda_stream))
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    out["fwd_entropy_vtp1"] = {"ms": ms, "tokens_per_s": T / ms * 1e3, "alg_gbs": T * (2 * Vr + 21) / ms / 1e6}
     out["lmhead_fwd"] = lmhead_bench(rlk, args, logits.device)
     # split path: fwd then bwd with lse_in
     cf = c.replace(virtual_tp=1)

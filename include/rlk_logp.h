@@ -132,6 +132,24 @@ rlk_status rlk_logp_fwd(const rlk_logp_contract* contract, const void* logits_bf
                         float* lse, float* partials, void* workspace, rlk_stream_t stream);
 
 /*
+ * Forward plus the entropy of each row's softmax over the real vocabulary,
+ * in the same single pass over the logits: every tile also sums
+ * t_k = sum_c e^(x_c - m_k) x_c beside s_k, the fold runs the same
+ * fixed-order recurrence on it, and entropy = LSE - (sum_c p_c x_c), which
+ * equals -sum_c p_c log p_c.  The pages log a mean policy entropy beside the
+ * loss in their RL runs (the H100 matrix document, "Completed full-model
+ * matrix"); the formula is Shannon's.
+ *   entropy      [T] FP32 out, every row (active or not); NaN where the LSE
+ *                is not finite.
+ * Every other argument, output and status is that of rlk_logp_fwd; logp and
+ * LSE are bitwise those of rlk_logp_fwd.  Outputs are bitwise identical for
+ * every virtual_tp.
+ */
+rlk_status rlk_logp_fwd_entropy(const rlk_logp_contract* contract, const void* logits_bf16,
+                                const int64_t* targets, const uint8_t* active_mask, float* logp, float* lse,
+                                float* entropy, void* workspace, rlk_stream_t stream);
+
+/*
  * Backward (and, with lse_in == NULL, the fused single-pass forward+backward).
  *   grad_logp    [T] FP32: upstream gradient g_r of logp_r (used on active rows).
  *   dlogits_bf16 [T, row_stride] BF16 out, 16-byte aligned: columns

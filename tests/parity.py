@@ -15,6 +15,7 @@ import oracle
 import vocab_selected_token_tile_gb300 as rlk
 
 LSE_TOL = 1e-4     # LSE and logp max abs error against the FP64 oracle
+ENT_TOL = 1e-4     # entropy max abs error: H = LSE - T/S; FP32 rounding of T/S at |E[x]| <= 20 is ~1e-5
 DL_TOL = 1e-2      # dlogits max abs error (BF16 output)
 
 
@@ -92,3 +93,16 @@ def check_dlogits(bits, tgt, active, g, v_real, v_padded, dl_bits, rows=None):
 def contract(T, v_real, v_padded, nt, vtp=1, mode=rlk.MASK_EXPLICIT, stride=0, validate=1, **kw):
     return rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=nt, virtual_tp=vtp, mask_mode=mode,
                         ignore_index=-100, validate=validate, row_stride=stride, **kw)
+
+
+def check_entropy(bits, v_real, ent, rows=None, tol=ENT_TOL):
+    """Entropy parity with the oracle: NaN exactly where the oracle's is NaN, max abs <= tol elsewhere."""
+    rows = np.arange(bits.shape[0]) if rows is None else rows
+    ref = oracle.entropy(bits[rows], v_real)
+    got = np.asarray(ent, dtype=np.float64)[rows]
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(got), fin)
+    err = float(np.max(np.abs(got[fin] - ref[fin]))) if fin.any() else 0.0
+    report("entropy", err)
+    assert err <= tol, f"entropy max abs {err}"
+    return err

@@ -14,7 +14,7 @@ import torch
 import oracle
 import synth
 import vocab_selected_token_tile_gb300 as rlk
-from parity import (check_dlogits, check_fwd, contract, f32_bits, sha, to_dev)
+from parity import (check_dlogits, check_entropy, check_fwd, contract, f32_bits, sha, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -215,6 +215,60 @@ def test_host_pipelined_call_equals_one_device_call():
     torch.cuda.synchronize()
     assert torch.equal(dl, dl_ref)
     assert torch.equal(logp, logp_ref.cpu()) and torch.equal(lse, lse_ref.cpu())
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "T%d_V%d_P%d_NT%d" % c[:4])
+def test_entropy_small_cases(case):
+    """The forward's entropy against the FP64 oracle; logp and LSE stay bitwise
+    those of rlk_logp_fwd; the entropy is bitwise identical across virtual TP."""
+    T, v_real, v_padded, nt, extra = case
+    stride, bits, tgt, mask, active, g = make_inputs(T, v_real, v_padded, nt, extra, seed=T * 7 + nt)
+    dlog = to_dev(bits)
+    dt, dm = torch.from_numpy(tgt).cuda(), torch.from_numpy(mask).cuda()
+    shas = set()
+    for vtp in vtps(nt):
+        c = contract(T, v_real, v_padded, nt, vtp, rlk.MASK_EXPLICIT, stride)
+        logp_e, lse_e, ent = rlk.logp_fwd_entropy(c, dlog, dt, dm)
+        logp, lse = rlk.logp_fwd(c, dlog, dt, dm)
+        torch.cuda.synchronize()
+        assert torch.equal(logp_e, logp) and torch.equal(lse_e, lse)
+        check_entropy(bits, v_real, ent.cpu().numpy())
+        shas.add(sha(ent))
+    assert len(shas) == 1, "virtual TP entropies differ"
+
+
+def test_entropy_special_rows_and_qwen3_shape(monkeypatch):
+    """Rows with one finite column (entropy 0) and no finite column (NaN);
+    then the Qwen3-shaped batch, every 13th row against the oracle, at one
+    and two CTAs per SM and every virtual TP, bitwise equal."""
+    v_real, v_padded, nt = 1000, 1024, 64
+    bits = synth.logits_host(0, 4, v_padded, v_padded, v_real, seed=9, sigma=2.0)
+    bits[1, :v_real] = 0xFF80          # all -inf
+    bits[2, :v_real] = 0xFF80
+    bits[2, 500] = 0x3F80              # one finite column (1.0)
+    c = contract(4, v_real, v_padded, nt, 2, rlk.MASK_IGNORE_INDEX, validate=0)
+    _, lse, ent = rlk.logp_fwd_entropy(c, to_dev(bits), torch.full((4,), -100, dtype=torch.int64).cuda())
+    torch.cuda.synchronize()
+    e = ent.cpu().numpy()
+    assert np.isnan(e[1]) and e[2] == 0.0
+    check_entropy(bits, v_real, e)
+
+    from synth import workloads as W
+    w = W.QWEN3
+    qbits = W.logits_host(w)
+    dq = to_dev(qbits)
+    dt = torch.from_numpy(W.targets(w)).cuda()
+    ref = None
+    for per_sm in ("1", "2"):
+        monkeypatch.setenv("RLK_CTAS_PER_SM", per_sm)
+        for vtp in (1, 2, 4, 8):
+            cq = contract(w.T, w.v_real, w.v_padded, w.num_tiles, vtp, rlk.MASK_IGNORE_INDEX)
+            _, _, eq = rlk.logp_fwd_entropy(cq, dq, dt)
+            torch.cuda.synchronize()
+            if ref is None:
+                ref = sha(eq)
+                check_entropy(qbits, w.v_real, eq.cpu().numpy(), rows=np.arange(0, w.T, 13))
+            assert sha(eq) == ref, (per_sm, vtp)
 
 
 def test_device_generator_matches_host():

@@ -31,6 +31,7 @@ EXPORTED = (
     "rlk_logp_fwd",
     "rlk_logp_bwd",
     "rlk_logp_fwd_noalloc",
+    "rlk_logp_fwd_entropy",
     "rlk_logp_lmhead_workspace_size",
     "rlk_logp_fused_lmhead",
     "rlk_logp_workspace_status",
@@ -98,6 +99,8 @@ def library():
         lib.rlk_logp_fused_lmhead.restype = i
         lib.rlk_logp_fwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp]
         lib.rlk_logp_fwd_noalloc.restype = i
+        lib.rlk_logp_fwd_entropy.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.rlk_logp_fwd_entropy.restype = i
         lib.rlk_logp_workspace_status.argtypes = [vp, vp]
         lib.rlk_logp_workspace_status.restype = i
         lib.rlk_selftest_bounded_wait.argtypes = [ctypes.c_int64, vp, vp]
@@ -139,6 +142,11 @@ def rlk_logp_fused_lmhead(contract, hidden, H, weight, targets, active_mask, gra
                           dweight, workspace, stream):
     return library().rlk_logp_fused_lmhead(ctypes.byref(contract), hidden, H, weight, targets, active_mask,
                                            grad_logp, logp, lse, dhidden, dweight, workspace, stream)
+
+
+def rlk_logp_fwd_entropy(contract, logits, targets, active_mask, logp, lse, entropy, workspace, stream):
+    return library().rlk_logp_fwd_entropy(ctypes.byref(contract), logits, targets, active_mask, logp, lse, entropy,
+                                          workspace, stream)
 
 
 def rlk_logp_fwd_noalloc(contract, logits, targets, active_mask, logp, lse, partials, stream):
@@ -217,6 +225,18 @@ def logp_bwd(contract, logits, targets, mask, lse, grad, dlogits=None, stream=No
     check(rlk_logp_bwd(contract, _ptr(logits), _ptr(targets), _ptr(mask), _ptr(lse), _ptr(grad),
                        _ptr(dlogits), None, None, _ptr(ws), _stream(stream)))
     return dlogits
+
+
+def logp_fwd_entropy(contract, logits, targets, mask=None, stream=None):
+    """(logp, lse, entropy) for BF16 ``logits`` on the GPU, in one pass; entropy of each row's softmax."""
+    import torch
+    dev = logits.device
+    T = contract.T
+    logp, lse, ent = (torch.empty(T, dtype=torch.float32, device=dev) for _ in range(3))
+    ws = workspace_for(contract, dev, stream)
+    check(rlk_logp_fwd_entropy(contract, _ptr(logits), _ptr(targets), _ptr(mask), _ptr(logp), _ptr(lse), _ptr(ent),
+                               _ptr(ws), _stream(stream)))
+    return logp, lse, ent
 
 
 def logp_fwd_bwd(contract, logits, targets, mask, grad, dlogits=None, stream=None, out=None):

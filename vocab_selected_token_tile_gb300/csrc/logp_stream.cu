@@ -123,7 +123,9 @@ struct Params {
     FastDiv ns_div, tps_div;  // division by NS and by tps
     int32_t rbufs, rb_shift;  // row buffers of the fold (a power of two) and its log2
     int32_t skew;             // kModeFusedL2: phase A runs `skew` rows ahead of phase B (< rbufs)
+    int32_t ent;  // the launch computes the entropy (stream_kernel's ENT)
     uint32_t off_full, off_empty, off_hdr, off_seq, off_part, off_fold, off_rows, off_xtin, off_bars, off_flag;
+    uint32_t off_tpart, off_foldt;  // ENT: t_k per row buffer, and the fold's scratch for them
 };
 
 struct TileGeom {
@@ -311,12 +313,33 @@ __device__ __forceinline__ void sum8(float2 (&s)[4], const uint4& v, float nmL) 
     s[3] = __fadd2_rn(s[3], exp_terms2(bf16x2_to_f32x2(v.w), c));
 }
 
+// sum8 plus t[j] += e x for the same terms (the tile's sum_c e^(x_c - m) x_c).
+__device__ __forceinline__ void sum8_ent(float2 (&s)[4], float2 (&t)[4], const uint4& v, float nmL) {
+    const float2 c = make_float2(nmL, nmL);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 x = bf16x2_to_f32x2(w[j]);
+        const float2 e = exp_terms2(x, c);
+        s[j] = __fadd2_rn(s[j], e);
+        t[j] = __ffma2_rn(e, x, t[j]);
+    }
+}
+
+__device__ __forceinline__ float combine8(const float2 (&a)[4]) {
+    return __fadd_rn(__fadd_rn(__fadd_rn(a[0].x, a[0].y), __fadd_rn(a[1].x, a[1].y)),
+                     __fadd_rn(__fadd_rn(a[2].x, a[2].y), __fadd_rn(a[3].x, a[3].y)));
+}
+
 // (m_k, s_k) of one tile, computed by one warp; every lane returns the same value.
 // Lane l visits interior groups lo+l, lo+l+32, ... then its edge groups; the
 // tile maximum is exact, the sum uses 8 accumulators combined pairwise, then
-// a fixed xor butterfly across lanes.
+// a fixed xor butterfly across lanes.  ENT: also t_k = sum_c e^(x_c - m_k) x_c
+// into *t_out, accumulated beside s in the same order (s is unchanged).
+template <bool ENT>
 __device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const TileGeom& t, int64_t Vr,
-                               int lane) {
+                               int lane, float* t_out) {
+    if (ENT) *t_out = 0.f;
     if (t.hi <= t.ts) return make_float2(-INFINITY, 0.f);  // padding-only tile: identity
     const GroupRange gr = group_range(t, t.hi, Vr);
     const int ne = gr.lo + (gr.n - gr.hi);
@@ -330,12 +353,21 @@ __device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const
     if (m == -INFINITY) return make_float2(-INFINITY, 0.f);  // all -inf: identity
     const float nmL = -__fmul_rn(m, kLog2e);
     float2 sm[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    if constexpr (!ENT) {
 #pragma unroll 4
-    for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) sum8(sm, s4[gi], nmL);
-    for (int e = lane; e < ne; e += 32) sum8(sm, load_group(slot, grow, t.a + 8 * (int64_t)edge_group(gr, e), t), nmL);
-    const float s = warp_sum(__fadd_rn(__fadd_rn(__fadd_rn(sm[0].x, sm[0].y), __fadd_rn(sm[1].x, sm[1].y)),
-                                       __fadd_rn(__fadd_rn(sm[2].x, sm[2].y), __fadd_rn(sm[3].x, sm[3].y))));
-    return make_float2(m, s);
+        for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) sum8(sm, s4[gi], nmL);
+        for (int e = lane; e < ne; e += 32)
+            sum8(sm, load_group(slot, grow, t.a + 8 * (int64_t)edge_group(gr, e), t), nmL);
+        return make_float2(m, warp_sum(combine8(sm)));
+    } else {
+        float2 tm[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll 4
+        for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) sum8_ent(sm, tm, s4[gi], nmL);
+        for (int e = lane; e < ne; e += 32)
+            sum8_ent(sm, tm, load_group(slot, grow, t.a + 8 * (int64_t)edge_group(gr, e), t), nmL);
+        *t_out = warp_sum(combine8(tm));
+        return make_float2(m, warp_sum(combine8(sm)));
+    }
 }
 
 // dlogits of 8 columns from their exp terms: -g * p, and g * (1 - p) at the target.
@@ -455,6 +487,8 @@ struct Ctx {
     float2* fold;
     RowShared* rows;
     float2* xtin;  // [rbufs][kMaxCluster]: each peer's (x_t, has_xt) of the row this CTA folds
+    float* tpart;  // ENT: [rbufs][NT] t_k = sum_c e^(x_c - m_k) x_c beside part
+    float* foldt;  // ENT: [NT] fold scratch
     Waiter wt;
 };
 
@@ -657,6 +691,7 @@ __device__ __forceinline__ bool warp_test(uint32_t bar, uint32_t parity, bool cl
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
+template <bool ENT>
 __device__ void push_row(const Params& p, const Ctx& x, int64_t n) {
     if (p.C == 1) return;
     const int lane = x.lane;
@@ -665,7 +700,7 @@ __device__ void push_row(const Params& p, const Ctx& x, int64_t n) {
     if (folds_row(p, x, n)) {
         // every peer's shard (all tiles but this CTA's own) and target record
         if (lane == 0) {
-            mbar_arrive_expect_tx(xb, (uint32_t)((p.NT - x.ntl) * 8 + (p.C - 1) * 8));
+            mbar_arrive_expect_tx(xb, (uint32_t)((p.NT - x.ntl) * (ENT ? 12 : 8) + (p.C - 1) * 8));
             mbar_arrive(lb);
         }
         return;
@@ -676,6 +711,10 @@ __device__ void push_row(const Params& p, const Ctx& x, int64_t n) {
     for (int i = lane; i < x.ntl; i += 32) {
         const float2 v = part[x.k0 + i];
         st_async_f32x2(mapa_shared(smem_u32(&part[x.k0 + i]), f), v.x, v.y, fxb);
+        if (ENT) {
+            float* tp = x.tpart + (size_t)b * p.NT + x.k0 + i;
+            st_async_f32(mapa_shared(smem_u32(tp), f), *tp, fxb);
+        }
     }
     if (lane == 0) {
         RowShared& rs = x.rows[b];
@@ -687,12 +726,20 @@ __device__ void push_row(const Params& p, const Ctx& x, int64_t n) {
     }
 }
 
+template <bool ENT>
 __device__ void fold_row(const Params& p, const Ctx& x, int64_t n) {
     const int lane = x.lane;
     const int b = row_buf(p, n);
     float2* part = x.part + (size_t)b * p.NT;
     RowShared& rs = x.rows[b];
-    const float lse_v = fold_tiles(part, p.NT, x.fold, lane);
+    float lse_v, ent_v = 0.f;
+    if constexpr (ENT) {
+        const float2 r = fold_tiles_ent(part, x.tpart + (size_t)b * p.NT, p.NT, x.fold, x.foldt, lane);
+        lse_v = r.x;
+        ent_v = r.y;
+    } else {
+        lse_v = fold_tiles(part, p.NT, x.fold, lane);
+    }
     const int64_t row = x.q + n * x.G;
     if (p.a.partials) {
         float2* out = reinterpret_cast<float2*>(p.a.partials) + row * p.NT;
@@ -719,6 +766,7 @@ __device__ void fold_row(const Params& p, const Ctx& x, int64_t n) {
         const bool active = rs.active != 0;
         const int64_t t = rs.target;
         p.a.lse[row] = lse_v;
+        if (ENT) p.a.entropy[row] = ent_v;
         if (!active) {
             p.a.logp[row] = 0.f;
         } else if (t < 0 || t >= p.Vr) {
@@ -734,7 +782,7 @@ __device__ void fold_row(const Params& p, const Ctx& x, int64_t n) {
     __syncwarp();
 }
 
-template <int MODE>
+template <int MODE, bool ENT>
 __device__ void fold_warp(const Params& p, const Ctx& x) {
     const int64_t R = x.nrows;
     int64_t np = 0, nr = 0;                         // next row to push, to release
@@ -745,13 +793,13 @@ __device__ void fold_warp(const Params& p, const Ctx& x) {
     while (nr < R) {
         bool progressed = false;
         if (np < R && warp_test(x.rowdone0 + 8u * row_buf(p, np), row_par(p, np), false)) {
-            push_row(p, x, np);
+            push_row<ENT>(p, x, np);
             ++np;
             progressed = true;
         }
         if (nf < R && nf < np &&
             (p.C == 1 || warp_test(x.xbar0 + 8u * row_buf(p, nf), row_par(p, nf), true))) {
-            fold_row(p, x, nf);
+            fold_row<ENT>(p, x, nf);
             nf += fstep;
             progressed = true;
         }
@@ -859,7 +907,7 @@ __device__ __forceinline__ int first_tile(const Ctx& x, int64_t n) {
 // row metadata (tile 0) and the target logit (the tile that holds it).
 // FWD releases each tile's share of its slot at once; FUSED keeps the slots
 // for phase B.
-template <int MODE, int W>
+template <int MODE, int W, bool ENT>
 __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0) {
     const int lane = x.lane;
     const int b = row_buf(p, n);
@@ -884,7 +932,8 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
         const int k = x.k0 + l;
         const TileGeom tg = tile_geom(k, p, sp);
         const uint16_t* sl = slots + (size_t)it.slot * slot_elems + (tg.a - sp.a);
-        const float2 pr = tile_partial(sl, grow, tg, p.Vr, lane);
+        float tk = 0.f;
+        const float2 pr = tile_partial<ENT>(sl, grow, tg, p.Vr, lane, &tk);
         if (lane == 0) {
             RowShared& rs = x.rows[b];
             if (l == 0) {
@@ -893,6 +942,7 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
                 rs.g = h.g;
             }
             x.part[(size_t)b * p.NT + k] = pr;
+            if (ENT) x.tpart[(size_t)b * p.NT + k] = tk;
             if (h.active && h.target >= tg.ts && h.target < tg.hi) {
                 const uint16_t bits = (h.target < tg.b) ? sl[h.target - tg.a] : ldg_bf16(grow + h.target);
                 rs.xt = __uint_as_float((uint32_t)bits << 16);
@@ -942,7 +992,7 @@ __device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0
     return true;
 }
 
-template <int MODE, int NW>
+template <int MODE, int NW, bool ENT>
 __device__ void consumer(const Params& p, const Ctx& x) {
     const int64_t R = x.nrows;
     const uint32_t nch = (uint32_t)x.nch;
@@ -953,16 +1003,16 @@ __device__ void consumer(const Params& p, const Ctx& x) {
         for (int64_t n = 0; n < R; ++n)
             if (!phase_b<MODE, NW>(p, x, n, item_b(n), 0.f)) break;
     } else if constexpr (MODE == kModeFwd) {
-        for (int64_t n = 0; n < R; ++n) phase_a<MODE, NW>(p, x, n, item_a(n));
+        for (int64_t n = 0; n < R; ++n) phase_a<MODE, NW, ENT>(p, x, n, item_a(n));
     } else {
         // Skewed order A(0), ..., A(S-1), then A(n+S), B(n): the fold of row
         // n overlaps phase A of rows n+1..n+S.  kModeFused (S = 1) keeps two
         // rows of slots resident; kModeFusedL2 copies each row a second time
         // for phase B.  rbufs > S keeps rows[b].lse of row n until every warp
         // has read it: row n + rbufs comes after B(n) in every warp's order.
-        for (int64_t n = 0; n < S && n < R; ++n) phase_a<MODE, NW>(p, x, n, item_a(n));
+        for (int64_t n = 0; n < S && n < R; ++n) phase_a<MODE, NW, ENT>(p, x, n, item_a(n));
         for (int64_t n = 0; n < R; ++n) {
-            if (n + S < R) phase_a<MODE, NW>(p, x, n + S, item_a(n + S));
+            if (n + S < R) phase_a<MODE, NW, ENT>(p, x, n + S, item_a(n + S));
             const int b = row_buf(p, n);
             const bool ready = x.wt.warp_wait(x.lseready0 + 8u * b, row_par(p, n));
             // A failed wait anywhere sets the abort flag; the slot headers may
@@ -974,7 +1024,8 @@ __device__ void consumer(const Params& p, const Ctx& x) {
 }
 
 // PER_SM: CTAs resident per SM (1 or 2); the register budget follows from it.
-template <int MODE, int PER_SM>
+// ENT (forward only): also the entropy of each row's softmax.
+template <int MODE, int PER_SM, bool ENT>
 __global__ void __launch_bounds__(threads_for(MODE, PER_SM), PER_SM)
     stream_kernel(const __grid_constant__ Params p) {
     constexpr int NW = consumers_for(MODE, PER_SM);
@@ -1004,6 +1055,8 @@ __global__ void __launch_bounds__(threads_for(MODE, PER_SM), PER_SM)
     x.fold = reinterpret_cast<float2*>(smem + p.off_fold);
     x.rows = reinterpret_cast<RowShared*>(smem + p.off_rows);
     x.xtin = reinterpret_cast<float2*>(smem + p.off_xtin);
+    x.tpart = reinterpret_cast<float*>(smem + p.off_tpart);
+    x.foldt = reinterpret_cast<float*>(smem + p.off_foldt);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.off_flag);
     x.wt.abort_flag = abort_flag;
     x.wt.status = p.a.status;
@@ -1031,9 +1084,9 @@ __global__ void __launch_bounds__(threads_for(MODE, PER_SM), PER_SM)
     if (x.warp > NW) {
         producer<MODE, producers_for(PER_SM)>(p, x, x.warp - NW - 1);
     } else if (x.warp == NW) {
-        if (MODE != kModeBwd) fold_warp<MODE>(p, x);
+        if (MODE != kModeBwd) fold_warp<MODE, ENT>(p, x);
     } else {
-        consumer<MODE, NW>(p, x);
+        consumer<MODE, NW, ENT>(p, x);
     }
 
     __syncthreads();
@@ -1110,6 +1163,10 @@ uint32_t layout(Params& p, int NS) {
     off = p.off_rows + (uint32_t)p.rbufs * (uint32_t)sizeof(RowShared);
     p.off_xtin = align_up(off, 16);
     off = p.off_xtin + (uint32_t)p.rbufs * (uint32_t)kMaxCluster * 8u;
+    p.off_tpart = align_up(off, 16);
+    if (p.ent) off = p.off_tpart + (uint32_t)p.rbufs * 4u * (uint32_t)p.NT;
+    p.off_foldt = align_up(off, 16);
+    if (p.ent) off = p.off_foldt + 4u * (uint32_t)p.NT;
     p.off_bars = align_up(off, 8);
     off = p.off_bars + 5u * 8u * (uint32_t)p.rbufs;  // rowdone, lseready, partfree, xbar, lsebar
     p.off_flag = off;
@@ -1143,6 +1200,8 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     p.NT = c.num_tiles;
     p.W = (int32_t)(c.V_padded / c.num_tiles);
     p.mask_mode = c.mask_mode;
+    p.ent = (a.entropy != nullptr) ? 1 : 0;
+    if (p.ent && mode != kModeFwd) return fail(RLK_ERR_UNSUPPORTED, "the entropy is computed by the forward only");
     // One bulk copy per chunk of tps consecutive tiles, about 8192 columns
     // (16 KB): a copy costs about the same issue time whatever its size, so
     // large copies are what keeps the stream near HBM bandwidth.
@@ -1254,15 +1313,16 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     if (NS < 1) return fail(RLK_ERR_UNSUPPORTED, "tile too wide for one shared-memory slot");
 
     auto pick = [&](int per_sm) -> void (*)(Params) {
+        if (p.ent) return per_sm == 2 ? stream_kernel<kModeFwd, 2, true> : stream_kernel<kModeFwd, 1, true>;
         if (per_sm == 2)
-            return (mode == kModeFwd)     ? stream_kernel<kModeFwd, 2>
-                 : (mode == kModeBwd)     ? stream_kernel<kModeBwd, 2>
-                 : (mode == kModeFusedL2) ? stream_kernel<kModeFusedL2, 2>
-                                          : stream_kernel<kModeFused, 2>;
-        return (mode == kModeFwd)     ? stream_kernel<kModeFwd, 1>
-             : (mode == kModeBwd)     ? stream_kernel<kModeBwd, 1>
-             : (mode == kModeFusedL2) ? stream_kernel<kModeFusedL2, 1>
-                                      : stream_kernel<kModeFused, 1>;
+            return (mode == kModeFwd)     ? stream_kernel<kModeFwd, 2, false>
+                 : (mode == kModeBwd)     ? stream_kernel<kModeBwd, 2, false>
+                 : (mode == kModeFusedL2) ? stream_kernel<kModeFusedL2, 2, false>
+                                          : stream_kernel<kModeFused, 2, false>;
+        return (mode == kModeFwd)     ? stream_kernel<kModeFwd, 1, false>
+             : (mode == kModeBwd)     ? stream_kernel<kModeBwd, 1, false>
+             : (mode == kModeFusedL2) ? stream_kernel<kModeFusedL2, 1, false>
+                                      : stream_kernel<kModeFused, 1, false>;
     };
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];

@@ -144,6 +144,29 @@ RLK_EXPORT rlk_status rlk_logp_fwd(const rlk_logp_contract* c, const void* logit
     return c->validate ? read_status(workspace, st) : RLK_OK;
 }
 
+RLK_EXPORT rlk_status rlk_logp_fwd_entropy(const rlk_logp_contract* c, const void* logits_bf16,
+                                           const int64_t* targets, const uint8_t* active_mask, float* logp,
+                                           float* lse, float* entropy, void* workspace, rlk_stream_t stream) {
+    rlk_status s = check_contract(c);
+    if (s != RLK_OK) return s;
+    if (c->T == 0) return RLK_OK;
+    if ((s = check_common(c, logits_bf16, targets, active_mask, workspace)) != RLK_OK) return s;
+    if (!logp || !lse || !entropy) return fail(RLK_ERR_INVALID_ARG, "logp, lse and entropy outputs are required");
+    if ((s = select_device(logits_bf16)) != RLK_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = begin(workspace, st)) != RLK_OK) return s;
+    StreamArgs a{};
+    a.logits = static_cast<const uint16_t*>(logits_bf16);
+    a.targets = targets;
+    a.mask = active_mask;
+    a.logp = logp;
+    a.lse = lse;
+    a.entropy = entropy;
+    a.status = static_cast<uint32_t*>(workspace);
+    if ((s = launch_stream(*c, kModeFwd, a, st)) != RLK_OK) return s;
+    return c->validate ? read_status(workspace, st) : RLK_OK;
+}
+
 RLK_EXPORT rlk_status rlk_logp_bwd(const rlk_logp_contract* c, const void* logits_bf16, const int64_t* targets,
                                    const uint8_t* active_mask, const float* lse_in, const float* grad_logp,
                                    void* dlogits_bf16, float* logp_out, float* lse_out, void* workspace,

@@ -39,6 +39,7 @@ struct StreamArgs {
     float* logp;
     float* lse;
     float* partials;
+    float* entropy;  // optional (forward): entropy of each row's softmax
     uint32_t* status;
 };
 
