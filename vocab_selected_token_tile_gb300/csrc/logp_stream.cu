@@ -314,12 +314,16 @@ __device__ __forceinline__ void sum8(float2 (&s)[4], const uint4& v, float nmL) 
 }
 
 // sum8 plus t[j] += e x for the same terms (the tile's sum_c e^(x_c - m) x_c).
+// A -inf column (padding, masked edges, or a -inf logit) must add 0 to t, not
+// 0 * -inf: the pair is first clamped to the largest finite negative BF16
+// (max.NaN keeps a NaN).  Its term e stays exactly 0 (x log2e overflows to
+// -inf), so s is bitwise that of sum8.
 __device__ __forceinline__ void sum8_ent(float2 (&s)[4], float2 (&t)[4], const uint4& v, float nmL) {
     const float2 c = make_float2(nmL, nmL);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float2 x = bf16x2_to_f32x2(w[j]);
+        const float2 x = bf16x2_to_f32x2(bf16x2_max_nan(w[j], 0xFF7FFF7Fu));
         const float2 e = exp_terms2(x, c);
         s[j] = __fadd2_rn(s[j], e);
         t[j] = __ffma2_rn(e, x, t[j]);
