@@ -18,6 +18,8 @@ What it computes, and where the pages define it:
   against the plain definition.
 * ``lmhead`` -- the same quantities when the logits are ``hidden @ W^T``
   (the fused lm_head variant), plus the gradients of hidden and W.
+* ``grpo`` -- the token-mean GRPO loss of per-token log-probabilities, with
+  an optional KL term, and its gradient with respect to each logp.
 
 Every function is FP64 and loops only where the definition does.
 """
@@ -36,3 +38,4 @@ from .logprob import (  # noqa: F401
     tile_partials,
 )
 from .lmhead import lmhead_logits, lmhead_forward, lmhead_grads  # noqa: F401
+from .grpo import grpo_loss  # noqa: F401

@@ -445,3 +445,60 @@ def test_entropy_special_rows():
     h = oracle.entropy(bits, 4)
     assert h[0] == 0.0  # a single finite column: a point mass
     assert np.isnan(h[1]) and np.isnan(h[2])
+
+
+# ------------------------------------------------------------------ GRPO loss
+
+def _grpo_pins_pass(fn):
+    """Every GRPO-loss pin, for an implementation fn(logp, adv, active, ref, beta) -> (loss, g, n)."""
+    rng = np.random.default_rng(31)
+    T = 50
+    logp = -rng.random(T) * 5
+    adv = rng.standard_normal(T)
+    act = rng.random(T) < 0.6
+    # closed form without KL: minus the mean of A * logp over active tokens
+    loss, g, n = fn(logp, adv, act, None, 0.0)
+    if n != act.sum() or abs(loss + (adv * logp)[act].mean()) > 1e-12:
+        return False
+    if not np.allclose(g, np.where(act, -adv / act.sum(), 0.0), rtol=0, atol=1e-15):
+        return False
+    # KL term: zero where ref == logp, non-negative, and the gradient is the derivative
+    if abs(fn(logp, adv, act, logp, 0.3)[0] - loss) > 1e-12:
+        return False
+    ref = logp + rng.standard_normal(T) * 0.5
+    l0 = fn(logp, np.zeros(T), act, ref, 0.3)[0]
+    if l0 < 0:
+        return False
+    loss_k, g_k, _ = fn(logp, adv, act, ref, 0.3)
+    h = 1e-6
+    for r in np.nonzero(act)[0][:5]:
+        e = np.zeros(T)
+        e[r] = h
+        fd = (fn(logp + e, adv, act, ref, 0.3)[0] - fn(logp - e, adv, act, ref, 0.3)[0]) / (2 * h)
+        if abs(fd - g_k[r]) > 1e-7:
+            return False
+    if np.any(g_k[~act] != 0):
+        return False
+    # no active token: loss and gradients 0
+    l_empty, g_empty, n_empty = fn(logp, adv, np.zeros(T, dtype=bool), ref, 0.3)
+    return l_empty == 0.0 and n_empty == 0 and not g_empty.any()
+
+
+def test_grpo_loss_pins():
+    assert _grpo_pins_pass(oracle.grpo_loss)
+
+
+def test_grpo_pins_catch_planted_mistakes():
+    def sequence_mean(logp, adv, act, ref=None, beta=0.0):  # divides by T, not the active count
+        loss, g, n = oracle.grpo_loss(logp, adv, act, ref, beta)
+        return loss * n / len(logp), g * n / len(logp), n
+
+    def kl_sign(logp, adv, act, ref=None, beta=0.0):
+        return oracle.grpo_loss(logp, adv, act, ref, -beta)
+
+    def grad_sign(logp, adv, act, ref=None, beta=0.0):
+        loss, g, n = oracle.grpo_loss(logp, adv, act, ref, beta)
+        return loss, -g, n
+
+    for mistake in (sequence_mean, kl_sign, grad_sign):
+        assert not _grpo_pins_pass(mistake), mistake.__name__
