@@ -413,6 +413,25 @@ def extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, V
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / args.steps
     out["fwd_entropy_vtp1"] = {"ms": ms, "tokens_per_s": T / ms * 1e3, "alg_gbs": T * (2 * Vr + 21) / ms / 1e6}
+    # the GRPO loss and g from this batch's logp (reads logp, A, mask, ref; writes g: 17 B per row)
+    ref = logp + 0.01
+    loss, gl, cnt = (torch.empty(1, dtype=torch.float32, device=logits.device),
+                     torch.empty(T, dtype=torch.float32, device=logits.device),
+                     torch.empty(1, dtype=torch.float32, device=logits.device))
+
+    def grpo():
+        rlk.check(rlk.rlk_grpo_loss(T, logp.data_ptr(), dg.data_ptr(), dmask.data_ptr(), ref.data_ptr(), 0.01,
+                                    loss.data_ptr(), gl.data_ptr(), cnt.data_ptr(), stream.cuda_stream))
+    for _ in range(3):
+        grpo()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        grpo()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    out["grpo_loss"] = {"ms": ms, "tokens_per_s": T / ms * 1e3, "alg_gbs": T * 17 / ms / 1e6}
     out["lmhead_fwd"] = lmhead_bench(rlk, args, logits.device)
     # split path: fwd then bwd with lse_in
     cf = c.replace(virtual_tp=1)

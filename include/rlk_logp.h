@@ -150,6 +150,31 @@ rlk_status rlk_logp_fwd_entropy(const rlk_logp_contract* contract, const void* l
                                 float* entropy, void* workspace, rlk_stream_t stream);
 
 /*
+ * Token-mean GRPO loss of per-token log-probabilities and its gradient with
+ * respect to each logp: the step after the forward, whose g feeds
+ * rlk_logp_bwd.  The pages name a GRPO loss contract (issue #323 "[WS2]
+ * [Logprob] H100 validation and reproduction guide", "Validation Boundary":
+ * the PR5 GRPO contract tests) and a KL coefficient of 0.01 (the H100 matrix
+ * document, "Completed full-model matrix") but print no formula; this is the
+ * convention:
+ *   N     = number of active rows (token mean); with N = 0 the loss and every
+ *           gradient are 0;
+ *   loss  = (1/N) sum over active r of (-A_r logp_r + beta k3_r), where
+ *           k3_r = exp(ref_r - logp_r) - (ref_r - logp_r) - 1 if ref_logp is
+ *           given (the k3 estimator of KL(pi || pi_ref)), else no KL term;
+ *   g_r   = (mask_r / N) (-A_r + beta (1 - exp(ref_r - logp_r))).
+ * Arguments (device pointers, FP32 unless said): logp, advantage (per row;
+ * a caller broadcasts per-sequence advantages), active_mask (uint8), ref_logp
+ * (NULL: no KL term), beta (>= 0), loss (one float out), grad_logp ([T] out),
+ * active_count (NULL, or one float out: N).  One CTA sums in a fixed order
+ * with FP64 accumulation, so the loss is bitwise reproducible.  Asynchronous
+ * on `stream`; returns RLK_ERR_INVALID_ARG for missing pointers or a bad beta.
+ */
+rlk_status rlk_grpo_loss(int64_t T, const float* logp, const float* advantage, const uint8_t* active_mask,
+                         const float* ref_logp, float beta, float* loss, float* grad_logp, float* active_count,
+                         rlk_stream_t stream);
+
+/*
  * Backward (and, with lse_in == NULL, the fused single-pass forward+backward).
  *   grad_logp    [T] FP32: upstream gradient g_r of logp_r (used on active rows).
  *   dlogits_bf16 [T, row_stride] BF16 out, 16-byte aligned: columns

@@ -32,6 +32,7 @@ EXPORTED = (
     "rlk_logp_bwd",
     "rlk_logp_fwd_noalloc",
     "rlk_logp_fwd_entropy",
+    "rlk_grpo_loss",
     "rlk_logp_lmhead_workspace_size",
     "rlk_logp_fused_lmhead",
     "rlk_logp_workspace_status",
@@ -101,6 +102,8 @@ def library():
         lib.rlk_logp_fwd_noalloc.restype = i
         lib.rlk_logp_fwd_entropy.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.rlk_logp_fwd_entropy.restype = i
+        lib.rlk_grpo_loss.argtypes = [ctypes.c_int64, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
+        lib.rlk_grpo_loss.restype = i
         lib.rlk_logp_workspace_status.argtypes = [vp, vp]
         lib.rlk_logp_workspace_status.restype = i
         lib.rlk_selftest_bounded_wait.argtypes = [ctypes.c_int64, vp, vp]
@@ -147,6 +150,11 @@ def rlk_logp_fused_lmhead(contract, hidden, H, weight, targets, active_mask, gra
 def rlk_logp_fwd_entropy(contract, logits, targets, active_mask, logp, lse, entropy, workspace, stream):
     return library().rlk_logp_fwd_entropy(ctypes.byref(contract), logits, targets, active_mask, logp, lse, entropy,
                                           workspace, stream)
+
+
+def rlk_grpo_loss(T, logp, advantage, active_mask, ref_logp, beta, loss, grad_logp, active_count, stream):
+    return library().rlk_grpo_loss(T, logp, advantage, active_mask, ref_logp, beta, loss, grad_logp, active_count,
+                                   stream)
 
 
 def rlk_logp_fwd_noalloc(contract, logits, targets, active_mask, logp, lse, partials, stream):
@@ -237,6 +245,19 @@ def logp_fwd_entropy(contract, logits, targets, mask=None, stream=None):
     check(rlk_logp_fwd_entropy(contract, _ptr(logits), _ptr(targets), _ptr(mask), _ptr(logp), _ptr(lse), _ptr(ent),
                                _ptr(ws), _stream(stream)))
     return logp, lse, ent
+
+
+def grpo_loss(logp, advantage, mask, ref_logp=None, beta=0.0, stream=None):
+    """(loss, grad_logp, active_count) of the token-mean GRPO loss (GPU tensors; loss and count are 1-element)."""
+    import torch
+    dev = logp.device
+    T = logp.numel()
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    count = torch.empty(1, dtype=torch.float32, device=dev)
+    g = torch.empty(T, dtype=torch.float32, device=dev)
+    check(rlk_grpo_loss(T, _ptr(logp), _ptr(advantage), _ptr(mask), _ptr(ref_logp), float(beta), _ptr(loss),
+                        _ptr(g), _ptr(count), _stream(stream)))
+    return loss, g, count
 
 
 def logp_fwd_bwd(contract, logits, targets, mask, grad, dlogits=None, stream=None, out=None):

@@ -167,6 +167,20 @@ RLK_EXPORT rlk_status rlk_logp_fwd_entropy(const rlk_logp_contract* c, const voi
     return c->validate ? read_status(workspace, st) : RLK_OK;
 }
 
+RLK_EXPORT rlk_status rlk_grpo_loss(int64_t T, const float* logp, const float* advantage, const uint8_t* active_mask,
+                                    const float* ref_logp, float beta, float* loss, float* grad_logp,
+                                    float* active_count, rlk_stream_t stream) {
+    if (T < 0) return fail(RLK_ERR_INVALID_ARG, "T must be >= 0");
+    if (!loss) return fail(RLK_ERR_INVALID_ARG, "loss output is required");
+    if (T > 0 && (!logp || !advantage || !active_mask || !grad_logp))
+        return fail(RLK_ERR_INVALID_ARG, "logp, advantage, active_mask and grad_logp are required");
+    if (!(beta >= 0.f) || !isfinite(beta)) return fail(RLK_ERR_INVALID_ARG, "beta must be finite and >= 0");
+    rlk_status s = select_device(loss);
+    if (s != RLK_OK) return s;
+    return launch_grpo_loss(T, logp, advantage, active_mask, ref_logp, beta, loss, grad_logp, active_count,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
 RLK_EXPORT rlk_status rlk_logp_bwd(const rlk_logp_contract* c, const void* logits_bf16, const int64_t* targets,
                                    const uint8_t* active_mask, const float* lse_in, const float* grad_logp,
                                    void* dlogits_bf16, float* logp_out, float* lse_out, void* workspace,

@@ -63,6 +63,10 @@ rlk_status launch_lmhead_bwd(const rlk_logp_contract& c, const void* hidden, int
                              const int64_t* targets, const uint8_t* mask, const float* grad, float* logp, float* lse,
                              void* dhidden, void* dweight, void* workspace, uint32_t* status, cudaStream_t stream);
 
+// Token-mean GRPO loss and its gradient (grpo_loss.cu); one CTA, fixed order.
+rlk_status launch_grpo_loss(int64_t T, const float* logp, const float* adv, const uint8_t* mask, const float* ref,
+                            float beta, float* loss, float* grad, float* count, cudaStream_t stream);
+
 // Launches the bounded-wait self-test kernel (one warp waiting on an mbarrier
 // that nothing arrives at).
 rlk_status launch_selftest_wait(uint64_t limit_ns, uint32_t* status, cudaStream_t stream);
