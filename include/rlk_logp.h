@@ -166,9 +166,11 @@ rlk_status rlk_logp_fwd_entropy(const rlk_logp_contract* contract, const void* l
  * Arguments (device pointers, FP32 unless said): logp, advantage (per row;
  * a caller broadcasts per-sequence advantages), active_mask (uint8), ref_logp
  * (NULL: no KL term), beta (>= 0), loss (one float out), grad_logp ([T] out),
- * active_count (NULL, or one float out: N).  One CTA sums in a fixed order
- * with FP64 accumulation, so the loss is bitwise reproducible.  Asynchronous
- * on `stream`; returns RLK_ERR_INVALID_ARG for missing pointers or a bad beta.
+ * active_count (NULL, or one float out: N, exact up to 2^24).  Per-row terms
+ * are FP32; one cluster of 8 CTAs sums them in FP64 in a fixed order that
+ * depends on T only, so the loss is bitwise reproducible.  grad_logp must not
+ * overlap the inputs.  Asynchronous on `stream`; returns RLK_ERR_INVALID_ARG
+ * for missing pointers or a bad beta.
  */
 rlk_status rlk_grpo_loss(int64_t T, const float* logp, const float* advantage, const uint8_t* active_mask,
                          const float* ref_logp, float beta, float* loss, float* grad_logp, float* active_count,

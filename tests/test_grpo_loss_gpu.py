@@ -80,8 +80,9 @@ def test_grpo_loss_edge_cases_and_repeatability():
     one[1234] = 1
     check(logp, adv, one, ref, 0.01)                           # N = 1
     check(logp, adv, np.ones_like(mask), ref, 0.01)            # every row active
-    for T in (1, 1023, 1024, 1025):                            # around the CTA's stride
+    for T in (1, 1023, 1024, 1025, 8191, 8193):                # around a CTA's and the cluster's stride
         check(logp[:T], adv[:T], np.ones(T, np.uint8), ref[:T], 0.01)
+    check(*grpo_batch(3, 33337, 100, 1, 33000, seed=5), 0.01)  # several unrolled passes, ragged end
     loss, g, n = run(logp[:0], adv[:0], mask[:0], ref[:0], 0.01)  # T = 0
     assert loss == 0.0 and n == 0.0 and g.size == 0
     a = run(logp, adv, mask, ref, 0.01)

@@ -14,12 +14,17 @@
 //   g_r    = (mask_r / N) (-A_r + beta (1 - exp(ref_r - logp_r))), the
 //            upstream gradient of the backward.
 //
-// Determinism: one CTA of 1024 threads sums in a fixed order -- thread i
-// adds rows i, i + 1024, ... in FP64 (the per-token terms are FP32, the
-// inputs' precision), then a fixed shuffle and shared-memory tree -- so the
-// loss is bitwise reproducible for a given input whatever the GPU; the count
-// N is an exact sum.  The gradient needs N first, so
-// the kernel computes both in one CTA: count, then losses, then gradients.
+// Layout: one cluster of 8 CTAs of 1024 threads.  Thread t of CTA k takes
+// rows k*1024 + t + j*8192 (j = 0, 1, ...), so every pass is coalesced and
+// each thread keeps four rows' loads in flight.  Pass 1 forms each row's FP32
+// term and unnormalised gradient, writes the latter to grad, and sums the
+// terms in FP64 and the active rows as an integer.  The CTAs then exchange
+// their (sum, count) through distributed shared memory; every CTA folds the
+// eight partials in rank order, so all agree on N, and pass 2 scales its own
+// rows of grad by 1/N.  Each step runs in a fixed order -- a thread's rows in
+// index order, a fixed xor butterfly in the warp, warps 0..31 by the same
+// butterfly, CTAs 0..7 in rank order -- that does not depend on the GPU or on
+// timing, so the loss is bitwise reproducible; N is an exact integer sum.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -27,60 +32,136 @@
 #include <string>
 
 #include "rlk_internal.h"
+#include "rlk_ptx.cuh"
 
 namespace rlk {
 namespace {
 
 constexpr int kLossThreads = 1024;
+constexpr int kLossCtas = 8;  // one portable cluster
+constexpr int64_t kLossStride = (int64_t)kLossThreads * kLossCtas;
+constexpr int kLossUnroll = 4;
 
-__device__ __forceinline__ double block_sum(double v, double* sh) {
+struct LossPart {
+    double sum;
+    unsigned long long count;
+};
+
+__device__ __forceinline__ double warp_sum(double v) {
 #pragma unroll
     for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) sh[warp] = v;
-    __syncthreads();
-    double r = 0.0;
-    if (warp == 0) {
-        r = lane < (kLossThreads / 32) ? sh[lane] : 0.0;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, off);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) sh[0] = r;
-    __syncthreads();
-    r = sh[0];
-    __syncthreads();
-    return r;
+    return v;
 }
 
-__global__ void __launch_bounds__(kLossThreads, 1)
-    grpo_loss_kernel(int64_t T, const float* logp, const float* adv, const uint8_t* mask, const float* ref,
-                     float beta, float* loss, float* grad, float* count) {
-    __shared__ double sh[kLossThreads / 32];
-    double n_local = 0.0;
-    for (int64_t r = threadIdx.x; r < T; r += kLossThreads) n_local += (mask[r] != 0) ? 1.0 : 0.0;
-    const double n = block_sum(n_local, sh);
-    const double inv_n = n > 0.0 ? 1.0 / n : 0.0;
-    const float inv_nf = (float)inv_n;
+__device__ __forceinline__ unsigned long long warp_sum(unsigned long long v) {
+#pragma unroll
+    for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+    return v;
+}
+
+__device__ __forceinline__ double ld_cluster_f64(uint32_t addr) {
+    double v;
+    asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_cluster_u64(uint32_t addr) {
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__global__ void __cluster_dims__(kLossCtas, 1, 1) __launch_bounds__(kLossThreads, 1)
+    grpo_loss_kernel(int64_t T, const float* __restrict__ logp, const float* __restrict__ adv,
+                     const uint8_t* __restrict__ mask, const float* __restrict__ ref, float beta,
+                     float* __restrict__ loss, float* __restrict__ grad, float* __restrict__ count) {
+    __shared__ double warp_s[kLossThreads / 32];
+    __shared__ unsigned long long warp_n[kLossThreads / 32];
+    __shared__ LossPart part;    // this CTA's partial, read by every CTA of the cluster
+    __shared__ LossPart folded;  // the cluster's total, for this CTA's threads
+    const uint32_t rank = cluster_ctarank();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t0 = (int64_t)rank * kLossThreads + threadIdx.x;
+
+    // pass 1: per-row terms in FP32 (the inputs' precision), sums in FP64
     double acc = 0.0;
-    for (int64_t r = threadIdx.x; r < T; r += kLossThreads) {
-        // per-token terms in FP32 (the inputs' precision), the sum in FP64
-        const bool act = mask[r] != 0;
-        const float lp = logp[r], a = adv[r];
-        float term = -a * lp, dterm = -a;
-        if (ref) {
-            const float d = ref[r] - lp;
-            const float e = expf(d);
-            term = fmaf(beta, (e - d) - 1.f, term);
-            dterm = fmaf(beta, 1.f - e, dterm);
+    unsigned long long n_act = 0;
+    for (int64_t base = t0; base < T; base += kLossUnroll * kLossStride) {
+        float lp[kLossUnroll], a[kLossUnroll], rf[kLossUnroll];
+        bool act[kLossUnroll];
+#pragma unroll
+        for (int u = 0; u < kLossUnroll; ++u) {
+            const int64_t r = base + u * kLossStride;
+            const bool in = r < T;
+            act[u] = in && mask[r] != 0;
+            lp[u] = in ? logp[r] : 0.f;
+            a[u] = in ? adv[r] : 0.f;
+            rf[u] = (in && ref) ? ref[r] : 0.f;
         }
-        if (act) acc += (double)term;
-        grad[r] = act ? dterm * inv_nf : 0.f;
+#pragma unroll
+        for (int u = 0; u < kLossUnroll; ++u) {
+            const int64_t r = base + u * kLossStride;
+            float term = -a[u] * lp[u], dterm = -a[u];
+            if (ref) {
+                const float d = rf[u] - lp[u];
+                const float e = expf(d);
+                term = fmaf(beta, (e - d) - 1.f, term);
+                dterm = fmaf(beta, 1.f - e, dterm);
+            }
+            if (act[u]) {
+                acc += (double)term;
+                ++n_act;
+            }
+            if (r < T) grad[r] = act[u] ? dterm : 0.f;
+        }
     }
-    const double total = block_sum(acc, sh);
+
+    // the CTA's partial, then the cluster's fold in rank order
+    acc = warp_sum(acc);
+    n_act = warp_sum(n_act);
+    if (lane == 0) {
+        warp_s[warp] = acc;
+        warp_n[warp] = n_act;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const double s = warp_sum(warp_s[lane]);
+        const unsigned long long c = warp_sum(warp_n[lane]);
+        if (lane == 0) part = LossPart{s, c};
+    }
+    cluster_sync_all();
     if (threadIdx.x == 0) {
-        *loss = (float)(total * inv_n);
+        double total = 0.0;
+        unsigned long long n = 0;
+        for (int k = 0; k < kLossCtas; ++k) {
+            const uint32_t remote = mapa_shared(smem_u32(&part), (uint32_t)k);
+            total += ld_cluster_f64(remote);
+            n += ld_cluster_u64(remote + 8);
+        }
+        folded = LossPart{total, n};
+    }
+    cluster_sync_all();  // no CTA leaves while a peer may still read its partial
+    const unsigned long long n = folded.count;
+    const double inv_n = n > 0 ? 1.0 / (double)n : 0.0;
+    if (rank == 0 && threadIdx.x == 0) {
+        *loss = (float)(folded.sum * inv_n);
         if (count) *count = (float)n;
+    }
+
+    // pass 2: g_r = (unnormalised gradient) / N on this thread's own rows
+    const float inv_nf = (float)inv_n;
+    for (int64_t base = t0; base < T; base += kLossUnroll * kLossStride) {
+        float v[kLossUnroll];
+#pragma unroll
+        for (int u = 0; u < kLossUnroll; ++u) {
+            const int64_t r = base + u * kLossStride;
+            v[u] = r < T ? grad[r] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kLossUnroll; ++u) {
+            const int64_t r = base + u * kLossStride;
+            if (r < T) grad[r] = v[u] * inv_nf;
+        }
     }
 }
 
@@ -88,7 +169,7 @@ __global__ void __launch_bounds__(kLossThreads, 1)
 
 rlk_status launch_grpo_loss(int64_t T, const float* logp, const float* adv, const uint8_t* mask, const float* ref,
                             float beta, float* loss, float* grad, float* count, cudaStream_t stream) {
-    grpo_loss_kernel<<<1, kLossThreads, 0, stream>>>(T, logp, adv, mask, ref, beta, loss, grad, count);
+    grpo_loss_kernel<<<kLossCtas, kLossThreads, 0, stream>>>(T, logp, adv, mask, ref, beta, loss, grad, count);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("GRPO loss launch: ") + cudaGetErrorString(e));
     return RLK_OK;
