@@ -74,7 +74,7 @@ def test_grpo_loss_matches_oracle(shape, beta):
 
 
 def test_grpo_loss_edge_cases_and_repeatability():
-    logp, adv, mask, ref = grpo_batch(3, 700, 10, 1, 690, seed=3)
+    logp, adv, mask, ref = grpo_batch(3, 3000, 10, 1, 2990, seed=3)
     check(logp, adv, np.zeros_like(mask), ref, 0.01)           # N = 0
     one = np.zeros_like(mask)
     one[1234] = 1
