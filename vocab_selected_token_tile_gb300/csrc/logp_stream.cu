@@ -128,24 +128,25 @@ struct Params {
     uint32_t off_tpart, off_foldt;  // ENT: t_k per row buffer, and the fold's scratch for them
 };
 
+// Columns fit in 32 bits: V_padded = num_tiles * W <= 1024 * 16384.
 struct TileGeom {
-    int64_t ts, te;  // tile columns [ts, te)
-    int64_t hi;      // min(te, V_real): end of the tile's real columns
-    int64_t a;       // floor8(ts): column of the tile's first 8-column group
-    int64_t b;       // end of the data held in shared memory (multiple of 8)
+    int ts, te;  // tile columns [ts, te)
+    int hi;      // min(te, V_real): end of the tile's real columns
+    int a;       // floor8(ts): column of the tile's first 8-column group
+    int b;       // end of the data held in shared memory (multiple of 8)
 };
 
 // Columns [a, b) of tiles [kf, kl) that one ring slot holds:
 // a = floor8(kf*W), b = min(ceil8(kl*W), floor8(V_real)); b <= a means nothing to copy.
 struct Span {
-    int64_t a, b;
+    int a, b;
 };
 
 __device__ __forceinline__ Span chunk_span(int kf, int kl, const Params& p) {
     Span s;
-    s.a = ((int64_t)kf * p.W) & ~(int64_t)7;
-    const int64_t ce = ((int64_t)kl * p.W + 7) & ~(int64_t)7;
-    const int64_t fv = p.Vr & ~(int64_t)7;
+    s.a = (kf * p.W) & ~7;
+    const int ce = (kl * p.W + 7) & ~7;
+    const int fv = (int)p.Vr & ~7;
     s.b = ce < fv ? ce : fv;
     return s;
 }
@@ -153,10 +154,10 @@ __device__ __forceinline__ Span chunk_span(int kf, int kl, const Params& p) {
 // Geometry of tile k inside a slot that holds columns [sp.a, sp.b).
 __device__ __forceinline__ TileGeom tile_geom(int k, const Params& p, const Span& sp) {
     TileGeom t;
-    t.ts = (int64_t)k * p.W;
+    t.ts = k * p.W;
     t.te = t.ts + p.W;
-    t.hi = t.te < p.Vr ? t.te : p.Vr;
-    t.a = t.ts & ~(int64_t)7;
+    t.hi = t.te < (int)p.Vr ? t.te : (int)p.Vr;
+    t.a = t.ts & ~7;
     t.b = sp.b;
     return t;
 }
@@ -220,7 +221,7 @@ __device__ __forceinline__ uint16_t ldg_bf16(const uint16_t* p) {
 // tile's real range [ts, hi) read as -inf.  Groups inside the slot span come
 // from shared memory; the ragged real tail [floor8(V_real), V_real) is read
 // from global memory one element at a time.
-__device__ __forceinline__ uint4 load_group(const uint16_t* slot, const uint16_t* grow, int64_t c0,
+__device__ __forceinline__ uint4 load_group(const uint16_t* slot, const uint16_t* grow, int c0,
                                             const TileGeom& t) {
     uint4 v;
     if (c0 + 8 <= t.b) {
@@ -229,7 +230,7 @@ __device__ __forceinline__ uint4 load_group(const uint16_t* slot, const uint16_t
         uint32_t w[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int64_t c = c0 + 2 * j;
+            const int c = c0 + 2 * j;
             const uint32_t lo = (c < t.hi && c >= t.ts) ? ldg_bf16(grow + c) : 0xFF80u;
             const uint32_t hi = (c + 1 < t.hi && c + 1 >= t.ts) ? ldg_bf16(grow + c + 1) : 0xFF80u;
             w[j] = lo | (hi << 16);
@@ -240,7 +241,7 @@ __device__ __forceinline__ uint4 load_group(const uint16_t* slot, const uint16_t
         uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int64_t c = c0 + 2 * j;
+            const int c = c0 + 2 * j;
             if (c < t.ts || c >= t.hi) w[j] = neg_inf_lo(w[j]);
             if (c + 1 < t.ts || c + 1 >= t.hi) w[j] = neg_inf_hi(w[j]);
         }
@@ -270,14 +271,14 @@ struct GroupRange {
     int lo, hi, n;  // interior [lo, hi), all groups [0, n)
 };
 
-__device__ __forceinline__ GroupRange group_range(const TileGeom& t, int64_t end, int64_t Vr) {
+__device__ __forceinline__ GroupRange group_range(const TileGeom& t, int end, int Vr) {
     GroupRange g;
     g.lo = (t.ts > t.a) ? 1 : 0;
-    const int64_t fv = Vr & ~(int64_t)7;
-    const int64_t lim = end < fv ? end : fv;
-    const int64_t hi = (lim - t.a) >> 3;
-    g.n = (int)((((end + 7) & ~(int64_t)7) - t.a) >> 3);
-    g.hi = hi < g.lo ? g.lo : (int)hi;
+    const int fv = Vr & ~7;
+    const int lim = end < fv ? end : fv;
+    const int hi = (lim - t.a) >> 3;
+    g.n = (((end + 7) & ~7) - t.a) >> 3;
+    g.hi = hi < g.lo ? g.lo : hi;
     if (g.hi > g.n) g.hi = g.n;
     return g;
 }
@@ -299,7 +300,7 @@ __device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w) {
 // 2^(x*log2e + c) of an FP32 pair: one packed FMA (each lane rounded as a
 // scalar FMA would be) and two SFU exponentials.
 __device__ __forceinline__ float2 exp_terms2(float2 x, float2 c) {
-    const float2 t = __ffma2_rn(x, make_float2(kLog2e, kLog2e), c);
+    const float2 t = ffma2(x, make_float2(kLog2e, kLog2e), c);
     return make_float2(ex2_approx(t.x), ex2_approx(t.y));
 }
 
@@ -307,10 +308,10 @@ __device__ __forceinline__ float2 exp_terms2(float2 x, float2 c) {
 // s[j] holds the running sums of elements 2j and 2j+1 of every group.
 __device__ __forceinline__ void sum8(float2 (&s)[4], const uint4& v, float nmL) {
     const float2 c = make_float2(nmL, nmL);
-    s[0] = __fadd2_rn(s[0], exp_terms2(bf16x2_to_f32x2(v.x), c));
-    s[1] = __fadd2_rn(s[1], exp_terms2(bf16x2_to_f32x2(v.y), c));
-    s[2] = __fadd2_rn(s[2], exp_terms2(bf16x2_to_f32x2(v.z), c));
-    s[3] = __fadd2_rn(s[3], exp_terms2(bf16x2_to_f32x2(v.w), c));
+    s[0] = fadd2(s[0], exp_terms2(bf16x2_to_f32x2(v.x), c));
+    s[1] = fadd2(s[1], exp_terms2(bf16x2_to_f32x2(v.y), c));
+    s[2] = fadd2(s[2], exp_terms2(bf16x2_to_f32x2(v.z), c));
+    s[3] = fadd2(s[3], exp_terms2(bf16x2_to_f32x2(v.w), c));
 }
 
 // sum8 plus t[j] += e x for the same terms (the tile's sum_c e^(x_c - m) x_c).
@@ -325,8 +326,8 @@ __device__ __forceinline__ void sum8_ent(float2 (&s)[4], float2 (&t)[4], const u
     for (int j = 0; j < 4; ++j) {
         const float2 x = bf16x2_to_f32x2(bf16x2_max_nan(w[j], 0xFF7FFF7Fu));
         const float2 e = exp_terms2(x, c);
-        s[j] = __fadd2_rn(s[j], e);
-        t[j] = __ffma2_rn(e, x, t[j]);
+        s[j] = fadd2(s[j], e);
+        t[j] = ffma2(e, x, t[j]);
     }
 }
 
@@ -341,7 +342,7 @@ __device__ __forceinline__ float combine8(const float2 (&a)[4]) {
 // a fixed xor butterfly across lanes.  ENT: also t_k = sum_c e^(x_c - m_k) x_c
 // into *t_out, accumulated beside s in the same order (s is unchanged).
 template <bool ENT>
-__device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const TileGeom& t, int64_t Vr,
+__device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const TileGeom& t, int Vr,
                                int lane, float* t_out) {
     if (ENT) *t_out = 0.f;
     if (t.hi <= t.ts) return make_float2(-INFINITY, 0.f);  // padding-only tile: identity
@@ -351,7 +352,7 @@ __device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const
     uint32_t acc[4] = {0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u};
 #pragma unroll 4
     for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) max4(acc, s4[gi]);
-    for (int e = lane; e < ne; e += 32) max4(acc, load_group(slot, grow, t.a + 8 * (int64_t)edge_group(gr, e), t));
+    for (int e = lane; e < ne; e += 32) max4(acc, load_group(slot, grow, t.a + 8 * edge_group(gr, e), t));
     acc[0] = bf16x2_max_nan(bf16x2_max_nan(acc[0], acc[1]), bf16x2_max_nan(acc[2], acc[3]));
     const float m = warp_max_nan(fmax_nan(bf16lo_to_f32(acc[0]), bf16hi_to_f32(acc[0])));
     if (m == -INFINITY) return make_float2(-INFINITY, 0.f);  // all -inf: identity
@@ -361,31 +362,31 @@ __device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const
 #pragma unroll 4
         for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) sum8(sm, s4[gi], nmL);
         for (int e = lane; e < ne; e += 32)
-            sum8(sm, load_group(slot, grow, t.a + 8 * (int64_t)edge_group(gr, e), t), nmL);
+            sum8(sm, load_group(slot, grow, t.a + 8 * edge_group(gr, e), t), nmL);
         return make_float2(m, warp_sum(combine8(sm)));
     } else {
         float2 tm[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll 4
         for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) sum8_ent(sm, tm, s4[gi], nmL);
         for (int e = lane; e < ne; e += 32)
-            sum8_ent(sm, tm, load_group(slot, grow, t.a + 8 * (int64_t)edge_group(gr, e), t), nmL);
+            sum8_ent(sm, tm, load_group(slot, grow, t.a + 8 * edge_group(gr, e), t), nmL);
         *t_out = warp_sum(combine8(tm));
         return make_float2(m, warp_sum(combine8(sm)));
     }
 }
 
 // dlogits of 8 columns from their exp terms: -g * p, and g * (1 - p) at the target.
-__device__ __forceinline__ uint4 grad8(const float (&pr)[8], int64_t c0, bool tgt_ok, int64_t target, float g) {
+__device__ __forceinline__ uint4 grad8(const float (&pr)[8], int c0, bool tgt_ok, int64_t target, float g) {
     float d[8];
     const float2 ng2 = make_float2(-g, -g);
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
-        const float2 q = __fmul2_rn(make_float2(pr[e], pr[e + 1]), ng2);
+        const float2 q = fmul2(make_float2(pr[e], pr[e + 1]), ng2);
         d[e] = q.x;
         d[e + 1] = q.y;
     }
-    if (tgt_ok && (uint64_t)(target - c0) < 8u) {
-        const int e = (int)(target - c0);
+    if (tgt_ok && (uint64_t)(target - (int64_t)c0) < 8u) {
+        const int e = (int)(target - (int64_t)c0);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             if (j == e) d[j] = __fmul_rn(g, __fsub_rn(1.f, pr[j]));
@@ -396,16 +397,16 @@ __device__ __forceinline__ uint4 grad8(const float (&pr)[8], int64_t c0, bool tg
 
 // dlogits of one tile's columns [ts, te) of one row, by one warp.
 __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* drow, const TileGeom& t,
-                          int64_t Vr, bool active, int64_t target, float g, float lse, int lane) {
+                          int Vr, bool active, int64_t target, float g, float lse, int lane) {
     const GroupRange gr = group_range(t, t.te, Vr);
     const int ne = gr.lo + (gr.n - gr.hi);
     uint4* d4 = reinterpret_cast<uint4*>(drow + t.a);
     if (!active) {
         for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) __stcs(d4 + gi, make_uint4(0u, 0u, 0u, 0u));
         for (int e = lane; e < ne; e += 32) {
-            const int64_t c0 = t.a + 8 * (int64_t)edge_group(gr, e);
+            const int c0 = t.a + 8 * edge_group(gr, e);
             for (int j = 0; j < 8; ++j) {
-                const int64_t c = c0 + j;
+                const int c = c0 + j;
                 if (c >= t.ts && c < t.te) drow[c] = 0;
             }
         }
@@ -421,10 +422,10 @@ __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* 
         const float2 p0 = exp_terms2(bf16x2_to_f32x2(v.x), c), p1 = exp_terms2(bf16x2_to_f32x2(v.y), c);
         const float2 p2 = exp_terms2(bf16x2_to_f32x2(v.z), c), p3 = exp_terms2(bf16x2_to_f32x2(v.w), c);
         const float pr[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
-        __stcs(d4 + gi, grad8(pr, t.a + 8 * (int64_t)gi, tgt_ok, target, g));
+        __stcs(d4 + gi, grad8(pr, t.a + 8 * gi, tgt_ok, target, g));
     }
     for (int e = lane; e < ne; e += 32) {
-        const int64_t c0 = t.a + 8 * (int64_t)edge_group(gr, e);
+        const int c0 = t.a + 8 * edge_group(gr, e);
         float pr[8];
         if (c0 + 8 <= t.b) {
             const uint4 v = *reinterpret_cast<const uint4*>(slot + (c0 - t.a));
@@ -438,7 +439,7 @@ __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* 
         } else {
 #pragma unroll
             for (int j = 0; j < 8; j += 2) {
-                const int64_t c = c0 + j;
+                const int c = c0 + j;
                 const uint32_t lo = (c < Vr) ? ldg_bf16(grow + c) : 0xFF80u;
                 const uint32_t hi = (c + 1 < Vr) ? ldg_bf16(grow + c + 1) : 0xFF80u;
                 const float2 q = exp_terms2(bf16x2_to_f32x2(lo | (hi << 16)), make_float2(nlL, nlL));
@@ -450,7 +451,7 @@ __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* 
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int64_t c = c0 + j;
+            const int c = c0 + j;
             if (c >= t.ts && c < t.te)
                 drow[c] = (c >= Vr) ? (uint16_t)0 : (uint16_t)((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
         }
@@ -937,7 +938,7 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
         const TileGeom tg = tile_geom(k, p, sp);
         const uint16_t* sl = slots + (size_t)it.slot * slot_elems + (tg.a - sp.a);
         float tk = 0.f;
-        const float2 pr = tile_partial<ENT>(sl, grow, tg, p.Vr, lane, &tk);
+        const float2 pr = tile_partial<ENT>(sl, grow, tg, (int)p.Vr, lane, &tk);
         if (lane == 0) {
             RowShared& rs = x.rows[b];
             if (l == 0) {
@@ -989,7 +990,7 @@ __device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0
             if (!isfinite(h.lse_in)) atomicOr(p.a.status, kStatusNonFinite);
         }
         tile_grad(slots + (size_t)it.slot * slot_elems + (tg.a - sp.a), p.a.logits + h.row * p.stride,
-                  p.a.dlogits + h.row * p.stride, tg, p.Vr, h.active != 0, h.target, h.g, lse, lane);
+                  p.a.dlogits + h.row * p.stride, tg, (int)p.Vr, h.active != 0, h.target, h.g, lse, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive_n(x.empty0 + 8u * it.slot, it.share);
     }

@@ -251,6 +251,35 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Packed FP32 pair arithmetic (PTX fma/add/mul .rn.f32x2, sm_100+): one
+// instruction for both lanes of the pair, each rounded exactly as the scalar
+// operation would be.  The pair travels as one 64-bit register pair.
+__device__ __forceinline__ uint64_t pack_f32x2(float2 v) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+    return r;
+}
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pack_f32x2(a)), "l"(pack_f32x2(b)), "l"(pack_f32x2(c)));
+    return unpack_f32x2(d);
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack_f32x2(a)), "l"(pack_f32x2(b)));
+    return unpack_f32x2(d);
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack_f32x2(a)), "l"(pack_f32x2(b)));
+    return unpack_f32x2(d);
+}
+
 // max that returns NaN if either operand is NaN (fmaxf would drop it).
 __device__ __forceinline__ float fmax_nan(float a, float b) {
     float r;
