@@ -375,8 +375,9 @@ __device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const
     }
 }
 
-// dlogits of 8 columns from their exp terms: -g * p, and g * (1 - p) at the target.
-__device__ __forceinline__ uint4 grad8(const float (&pr)[8], int c0, bool tgt_ok, int64_t target, float g) {
+// dlogits of 8 columns from their exp terms: -g * p, and g * (1 - p) at
+// column e of the group (the target), if 0 <= e < 8.
+__device__ __forceinline__ uint4 grad8(const float (&pr)[8], int e, float g) {
     float d[8];
     const float2 ng2 = make_float2(-g, -g);
 #pragma unroll
@@ -385,8 +386,7 @@ __device__ __forceinline__ uint4 grad8(const float (&pr)[8], int c0, bool tgt_ok
         d[e] = q.x;
         d[e + 1] = q.y;
     }
-    if (tgt_ok && (uint64_t)(target - (int64_t)c0) < 8u) {
-        const int e = (int)(target - (int64_t)c0);
+    if ((unsigned)e < 8u) {
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             if (j == e) d[j] = __fmul_rn(g, __fsub_rn(1.f, pr[j]));
@@ -413,7 +413,9 @@ __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* 
         return;
     }
     const float nlL = -__fmul_rn(lse, kLog2e);
-    const bool tgt_ok = target >= 0 && target < Vr;
+    // the target's column relative to the tile's first group (-1: not in this tile)
+    const int trel = (target >= t.ts && target < t.hi) ? (int)(target - t.a) : -1;
+    const int tg_gi = trel >> 3, tg_e = trel & 7;
     const uint4* s4 = reinterpret_cast<const uint4*>(slot);
 #pragma unroll 2
     for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) {
@@ -422,7 +424,7 @@ __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* 
         const float2 p0 = exp_terms2(bf16x2_to_f32x2(v.x), c), p1 = exp_terms2(bf16x2_to_f32x2(v.y), c);
         const float2 p2 = exp_terms2(bf16x2_to_f32x2(v.z), c), p3 = exp_terms2(bf16x2_to_f32x2(v.w), c);
         const float pr[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
-        __stcs(d4 + gi, grad8(pr, t.a + 8 * gi, tgt_ok, target, g));
+        __stcs(d4 + gi, grad8(pr, gi == tg_gi ? tg_e : -1, g));
     }
     for (int e = lane; e < ne; e += 32) {
         const int c0 = t.a + 8 * edge_group(gr, e);
@@ -447,7 +449,7 @@ __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* 
                 pr[j + 1] = q.y;
             }
         }
-        uint4 q = grad8(pr, c0, tgt_ok, target, g);
+        uint4 q = grad8(pr, trel - (c0 - t.a), g);
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
