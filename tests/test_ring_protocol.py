@@ -19,12 +19,13 @@ def align(v, a):
     return (v + a - 1) // a * a
 
 
-def layout(ns, slot_bytes, nt, rbufs=2):
+def layout(ns, slot_bytes, nt, rbufs=2, C=1):
     off = ns * slot_bytes + 16 * ns
     off = align(off, 16) + 36 * ns
     off = align(off, 16) + rbufs * 8 * nt + 8 * nt
     off = align(off, 16) + rbufs * 32
     off = align(off, 16) + rbufs * 8 * 8
+    off = align(off, 16) + 48 * -(-nt // C)  # per-tile constants of the CTA's shard
     off = align(off, 8) + 40 * rbufs + 16
     return align(off, 128)
 
@@ -66,7 +67,7 @@ def plan(mode, vtp, v_padded, nt):
     def max_slots(sb):
         best = 0
         for ns in range(1, 97):
-            if layout(ns, sb, nt, rb) <= budget:
+            if layout(ns, sb, nt, rb, C) <= budget:
                 best = ns
         return best
 

@@ -120,11 +120,12 @@ struct Params {
     uint64_t wait_ns;
     int32_t NT, W, C, mask_mode, NS, slot_bytes;
     int32_t tps;  // tiles per ring slot (consecutive tiles of one row share a slot when narrow)
-    FastDiv ns_div, tps_div;  // division by NS and by tps
+    FastDiv ns_div;  // division by NS
     int32_t rbufs, rb_shift;  // row buffers of the fold (a power of two) and its log2
     int32_t skew;             // kModeFusedL2: phase A runs `skew` rows ahead of phase B (< rbufs)
     int32_t ent;  // the launch computes the entropy (stream_kernel's ENT)
     uint32_t off_full, off_empty, off_hdr, off_seq, off_part, off_fold, off_rows, off_xtin, off_bars, off_flag;
+    uint32_t off_meta;  // TileMeta of each of the CTA's tiles
     uint32_t off_tpart, off_foldt;  // ENT: t_k per row buffer, and the fold's scratch for them
 };
 
@@ -285,6 +286,37 @@ __device__ __forceinline__ GroupRange group_range(const TileGeom& t, int end, in
 
 __device__ __forceinline__ int edge_group(const GroupRange& g, int e) { return e < g.lo ? 0 : g.hi + (e - g.lo); }
 
+// Constants of tile l of a CTA's shard (global tile k0 + l), the same for
+// every row: computed once per launch into shared memory.
+struct __align__(16) TileMeta {
+    TileGeom g;      // columns, in the slot that holds the tile's chunk
+    int c;           // chunk of the tile: l / tps
+    int share;       // arrivals the tile owes its slot's empty barrier
+    int soff;        // elements from the slot's start to the tile's first group
+    GroupRange ga;   // groups of the partial (real columns)
+    int nb;          // groups of the gradient (all the tile's columns)
+};
+static_assert(sizeof(TileMeta) == 48, "TileMeta layout");
+
+// A slot's empty barrier expects tps arrivals: the last tile of a short
+// (end-of-row) chunk arrives for the missing tiles too.
+__device__ void fill_meta(const Params& p, int k0, int ntl, TileMeta* meta) {
+    for (int l = threadIdx.x; l < ntl; l += blockDim.x) {
+        const int c = l / p.tps;
+        const int kf = k0 + c * p.tps;
+        const int kl = min(kf + p.tps, k0 + ntl);
+        const Span sp = chunk_span(kf, kl, p);
+        TileMeta m;
+        m.g = tile_geom(k0 + l, p, sp);
+        m.c = c;
+        m.share = (k0 + l == kl - 1) ? 1 + p.tps - (kl - kf) : 1;
+        m.soff = m.g.a - sp.a;
+        m.ga = group_range(m.g, m.g.hi, (int)p.Vr);
+        m.nb = group_range(m.g, m.g.te, (int)p.Vr).n;
+        meta[l] = m;
+    }
+}
+
 __device__ __forceinline__ void max4(uint32_t (&acc)[4], const uint4& v) {
     acc[0] = bf16x2_max_nan(acc[0], v.x);
     acc[1] = bf16x2_max_nan(acc[1], v.y);
@@ -342,11 +374,10 @@ __device__ __forceinline__ float combine8(const float2 (&a)[4]) {
 // a fixed xor butterfly across lanes.  ENT: also t_k = sum_c e^(x_c - m_k) x_c
 // into *t_out, accumulated beside s in the same order (s is unchanged).
 template <bool ENT>
-__device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const TileGeom& t, int Vr,
+__device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const TileGeom& t, const GroupRange& gr,
                                int lane, float* t_out) {
     if (ENT) *t_out = 0.f;
     if (t.hi <= t.ts) return make_float2(-INFINITY, 0.f);  // padding-only tile: identity
-    const GroupRange gr = group_range(t, t.hi, Vr);
     const int ne = gr.lo + (gr.n - gr.hi);
     const uint4* s4 = reinterpret_cast<const uint4*>(slot);
     uint32_t acc[4] = {0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u};
@@ -397,8 +428,7 @@ __device__ __forceinline__ uint4 grad8(const float (&pr)[8], int e, float g) {
 
 // dlogits of one tile's columns [ts, te) of one row, by one warp.
 __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* drow, const TileGeom& t,
-                          int Vr, bool active, int64_t target, float g, float lse, int lane) {
-    const GroupRange gr = group_range(t, t.te, Vr);
+                          const GroupRange& gr, int Vr, bool active, int64_t target, float g, float lse, int lane) {
     const int ne = gr.lo + (gr.n - gr.hi);
     uint4* d4 = reinterpret_cast<uint4*>(drow + t.a);
     if (!active) {
@@ -496,6 +526,7 @@ struct Ctx {
     float2* xtin;  // [rbufs][kMaxCluster]: each peer's (x_t, has_xt) of the row this CTA folds
     float* tpart;  // ENT: [rbufs][NT] t_k = sum_c e^(x_c - m_k) x_c beside part
     float* foldt;  // ENT: [NT] fold scratch
+    const TileMeta* meta;  // [ntl] per-tile constants
     Waiter wt;
 };
 
@@ -860,22 +891,15 @@ struct TileItem {
     uint32_t item;   // number of the chunk's item in the producer's order
     int slot;
     uint32_t par;
-    int kf, kl;      // tiles [kf, kl) of the chunk
-    uint32_t share;  // arrivals this tile owes the slot's empty barrier
 };
 
-// Tile l of a block whose first item is item0.
-__device__ __forceinline__ TileItem tile_item(const Params& p, const Ctx& x, uint32_t item0, int l) {
-    const int c = (int)fdiv((uint32_t)l, p.tps_div);
+// The item of a tile whose chunk is number c of a block whose first item is item0.
+__device__ __forceinline__ TileItem tile_item(const Params& p, uint32_t item0, int c) {
     TileItem it;
     it.item = item0 + (uint32_t)c;
     const RingPos ps = ring_of(it.item, p.ns_div);
     it.slot = ps.slot;
     it.par = ps.par;
-    it.kf = x.k0 + c * p.tps;
-    it.kl = min(it.kf + p.tps, x.k0 + x.ntl);
-    const int in_chunk = it.kl - it.kf;
-    it.share = (x.k0 + l == it.kl - 1) ? (uint32_t)(1 + p.tps - in_chunk) : 1u;
     return it;
 }
 
@@ -924,7 +948,8 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
     const int slot_elems = p.slot_bytes / 2;
     const uint32_t want = (uint32_t)(x.q + n * x.G);
     for (int l = first_tile<W>(x, n); l < x.ntl && ok; l += W) {
-        const TileItem it = tile_item(p, x, item0, l);
+        const TileMeta m = x.meta[l];
+        const TileItem it = tile_item(p, item0, m.c);
         if (!wait_item(x, it, it.item)) {
             ok = false;
             break;
@@ -934,13 +959,12 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
             ok = false;
             break;
         }
-        const Span sp = chunk_span(it.kf, it.kl, p);
         const uint16_t* grow = p.a.logits + h.row * p.stride;
         const int k = x.k0 + l;
-        const TileGeom tg = tile_geom(k, p, sp);
-        const uint16_t* sl = slots + (size_t)it.slot * slot_elems + (tg.a - sp.a);
+        const TileGeom& tg = m.g;
+        const uint16_t* sl = slots + (size_t)it.slot * slot_elems + m.soff;
         float tk = 0.f;
-        const float2 pr = tile_partial<ENT>(sl, grow, tg, (int)p.Vr, lane, &tk);
+        const float2 pr = tile_partial<ENT>(sl, grow, tg, m.ga, lane, &tk);
         if (lane == 0) {
             RowShared& rs = x.rows[b];
             if (l == 0) {
@@ -958,7 +982,7 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
         }
         if (MODE == kModeFwd || MODE == kModeFusedL2) {
             __syncwarp();
-            if (lane == 0) mbar_arrive_n(x.empty0 + 8u * it.slot, it.share);
+            if (lane == 0) mbar_arrive_n(x.empty0 + 8u * it.slot, (uint32_t)m.share);
         }
     }
     __syncwarp();
@@ -979,22 +1003,22 @@ __device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0
     const int slot_elems = p.slot_bytes / 2;
     const uint32_t want = (uint32_t)(x.q + n * x.G);
     for (int l = first_tile<W>(x, n); l < x.ntl; l += W) {
-        const TileItem it = tile_item(p, x, item0, l);
+        const TileMeta m = x.meta[l];
+        const TileItem it = tile_item(p, item0, m.c);
         if (kWaits && !wait_item(x, it, it.item)) return false;
         const SlotHdr h = x.hdr[it.slot];
         if (!header_ok(p, x, h, want)) return false;
-        const Span sp = chunk_span(it.kf, it.kl, p);
-        const int k = x.k0 + l;
-        const TileGeom tg = tile_geom(k, p, sp);
+        const TileGeom& tg = m.g;
         const float lse = (MODE == kModeBwd) ? h.lse_in : lse_v;
         if (MODE == kModeBwd && l == 0 && lane == 0 && h.active) {
             if (h.target < 0 || h.target >= p.Vr) atomicOr(p.a.status, kStatusTargetRange);
             if (!isfinite(h.lse_in)) atomicOr(p.a.status, kStatusNonFinite);
         }
-        tile_grad(slots + (size_t)it.slot * slot_elems + (tg.a - sp.a), p.a.logits + h.row * p.stride,
-                  p.a.dlogits + h.row * p.stride, tg, (int)p.Vr, h.active != 0, h.target, h.g, lse, lane);
+        tile_grad(slots + (size_t)it.slot * slot_elems + m.soff, p.a.logits + h.row * p.stride,
+                  p.a.dlogits + h.row * p.stride, tg, GroupRange{m.ga.lo, m.ga.hi, m.nb}, (int)p.Vr,
+                  h.active != 0, h.target, h.g, lse, lane);
         __syncwarp();
-        if (lane == 0) mbar_arrive_n(x.empty0 + 8u * it.slot, it.share);
+        if (lane == 0) mbar_arrive_n(x.empty0 + 8u * it.slot, (uint32_t)m.share);
     }
     return true;
 }
@@ -1064,6 +1088,7 @@ __global__ void __launch_bounds__(threads_for(MODE, PER_SM), PER_SM)
     x.xtin = reinterpret_cast<float2*>(smem + p.off_xtin);
     x.tpart = reinterpret_cast<float*>(smem + p.off_tpart);
     x.foldt = reinterpret_cast<float*>(smem + p.off_foldt);
+    x.meta = reinterpret_cast<const TileMeta*>(smem + p.off_meta);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.off_flag);
     x.wt.abort_flag = abort_flag;
     x.wt.status = p.a.status;
@@ -1086,6 +1111,7 @@ __global__ void __launch_bounds__(threads_for(MODE, PER_SM), PER_SM)
         *abort_flag = 0;
         fence_mbar_init();
     }
+    fill_meta(p, x.k0, x.ntl, reinterpret_cast<TileMeta*>(smem + p.off_meta));
     if (p.C > 1) cluster_sync_all(); else __syncthreads();
 
     if (x.warp > NW) {
@@ -1170,6 +1196,8 @@ uint32_t layout(Params& p, int NS) {
     off = p.off_rows + (uint32_t)p.rbufs * (uint32_t)sizeof(RowShared);
     p.off_xtin = align_up(off, 16);
     off = p.off_xtin + (uint32_t)p.rbufs * (uint32_t)kMaxCluster * 8u;
+    p.off_meta = align_up(off, 16);
+    off = p.off_meta + (uint32_t)sizeof(TileMeta) * (uint32_t)((p.NT + p.C - 1) / p.C);
     p.off_tpart = align_up(off, 16);
     if (p.ent) off = p.off_tpart + (uint32_t)p.rbufs * 4u * (uint32_t)p.NT;
     p.off_foldt = align_up(off, 16);
@@ -1383,7 +1411,6 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     cfg.blockDim = dim3(threads_for(mode, ctas_per_sm), 1, 1);
     p.NS = NS;
     p.ns_div = make_fastdiv((uint32_t)NS);
-    p.tps_div = make_fastdiv((uint32_t)p.tps);
     smem = layout(p, NS);
     cfg.dynamicSmemBytes = smem;
     cudaError_t e = cudaSuccess;
