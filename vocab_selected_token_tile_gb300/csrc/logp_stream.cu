@@ -926,20 +926,28 @@ __device__ __forceinline__ bool header_ok(const Params& p, const Ctx& x, const S
     return false;
 }
 
-// Consumer warp w of NW takes the tiles l of row n with (n*ntl + l) mod NW == w.
+// Consumer warp w of NW takes the tiles l of row n with (n*ntl + l) mod NW
+// == w.  Rows come in order, so the rotation r = (n*ntl) mod NW advances by
+// ntl mod NW per row.
 template <int NW>
-__device__ __forceinline__ int first_tile(const Ctx& x, int64_t n) {
-    const int r = (int)((n * x.ntl) % NW);
-    const int f = x.warp - r;
-    return f < 0 ? f + NW : f;
-}
+struct TileRotation {
+    int r = 0, step = 0;
+    __device__ explicit TileRotation(int ntl) : step(ntl % NW) {}
+    // The first tile of this warp in the current row; moves to the next row.
+    __device__ int next(int warp) {
+        const int f = warp - r;
+        r += step;
+        if (r >= NW) r -= NW;
+        return f < 0 ? f + NW : f;
+    }
+};
 
 // Phase A of row n for one consumer warp: the partials of its tiles, the
 // row metadata (tile 0) and the target logit (the tile that holds it).
 // FWD releases each tile's share of its slot at once; FUSED keeps the slots
 // for phase B.
 template <int MODE, int W, bool ENT>
-__device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0) {
+__device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0, int first) {
     const int lane = x.lane;
     const int b = row_buf(p, n);
     bool ok = true;
@@ -947,7 +955,7 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
     const int slot_elems = p.slot_bytes / 2;
     const uint32_t want = (uint32_t)(x.q + n * x.G);
-    for (int l = first_tile<W>(x, n); l < x.ntl && ok; l += W) {
+    for (int l = first; l < x.ntl && ok; l += W) {
         const TileMeta m = x.meta[l];
         const TileItem it = tile_item(p, item0, m.c);
         if (!wait_item(x, it, it.item)) {
@@ -996,13 +1004,13 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
 // its chunk; lse_v is the fold's LSE.  BWD: the tile waits for its chunk and
 // reads the row's LSE (lse_in) from the slot header.
 template <int MODE, int W>
-__device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0, float lse_v) {
+__device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0, float lse_v, int first) {
     constexpr bool kWaits = MODE == kModeBwd || MODE == kModeFusedL2;
     const int lane = x.lane;
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
     const int slot_elems = p.slot_bytes / 2;
     const uint32_t want = (uint32_t)(x.q + n * x.G);
-    for (int l = first_tile<W>(x, n); l < x.ntl; l += W) {
+    for (int l = first; l < x.ntl; l += W) {
         const TileMeta m = x.meta[l];
         const TileItem it = tile_item(p, item0, m.c);
         if (kWaits && !wait_item(x, it, it.item)) return false;
@@ -1030,26 +1038,28 @@ __device__ void consumer(const Params& p, const Ctx& x) {
     const int64_t S = (MODE == kModeFusedL2) ? p.skew : 1;
     auto item_a = [&](int64_t n) { return (uint32_t)block_of(MODE, n, false, R, S) * nch; };
     auto item_b = [&](int64_t n) { return (uint32_t)block_of(MODE, n, MODE != kModeFused, R, S) * nch; };
+    TileRotation<NW> rot_a(x.ntl), rot_b(x.ntl);  // phase A and phase B each visit rows in order
     if constexpr (MODE == kModeBwd) {
         for (int64_t n = 0; n < R; ++n)
-            if (!phase_b<MODE, NW>(p, x, n, item_b(n), 0.f)) break;
+            if (!phase_b<MODE, NW>(p, x, n, item_b(n), 0.f, rot_b.next(x.warp))) break;
     } else if constexpr (MODE == kModeFwd) {
-        for (int64_t n = 0; n < R; ++n) phase_a<MODE, NW, ENT>(p, x, n, item_a(n));
+        for (int64_t n = 0; n < R; ++n) phase_a<MODE, NW, ENT>(p, x, n, item_a(n), rot_a.next(x.warp));
     } else {
         // Skewed order A(0), ..., A(S-1), then A(n+S), B(n): the fold of row
         // n overlaps phase A of rows n+1..n+S.  kModeFused (S = 1) keeps two
         // rows of slots resident; kModeFusedL2 copies each row a second time
         // for phase B.  rbufs > S keeps rows[b].lse of row n until every warp
         // has read it: row n + rbufs comes after B(n) in every warp's order.
-        for (int64_t n = 0; n < S && n < R; ++n) phase_a<MODE, NW, ENT>(p, x, n, item_a(n));
+        for (int64_t n = 0; n < S && n < R; ++n) phase_a<MODE, NW, ENT>(p, x, n, item_a(n), rot_a.next(x.warp));
         for (int64_t n = 0; n < R; ++n) {
-            if (n + S < R) phase_a<MODE, NW, ENT>(p, x, n + S, item_a(n + S));
+            if (n + S < R) phase_a<MODE, NW, ENT>(p, x, n + S, item_a(n + S), rot_a.next(x.warp));
             const int b = row_buf(p, n);
             const bool ready = x.wt.warp_wait(x.lseready0 + 8u * b, row_par(p, n));
             // A failed wait anywhere sets the abort flag; the slot headers may
             // then be stale, so skip the writes (the status word already says
             // RLK_ERR_TIMEOUT).
-            if (ready && !*x.wt.abort_flag) phase_b<MODE, NW>(p, x, n, item_b(n), x.rows[b].lse);
+            const int first_b = rot_b.next(x.warp);
+            if (ready && !*x.wt.abort_flag) phase_b<MODE, NW>(p, x, n, item_b(n), x.rows[b].lse, first_b);
         }
     }
 }
