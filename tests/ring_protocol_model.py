@@ -101,7 +101,7 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
         c.seq = [None] * NS
         c.data = [None] * NS
         c.inflight = []
-        c.rowdone = [Bar(W) for _ in range(R)]
+        c.rowdone = [Bar(min(W, ntl) if mode == "fwd" else W) for _ in range(R)]
         c.lseready = [Bar(1) for _ in range(R)]
         c.partfree = [Bar(1) for _ in range(R)]
         c.xbar = [Bar(1) for _ in range(R)]
@@ -172,6 +172,8 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
 
     def phase_a(c, w, n):
         b = n % R
+        if mode == "fwd" and not tiles_of(w, n):  # forward: a warp without tiles skips the row
+            return
         if n >= R:
             yield from wait(c.partfree[b], (n // R - 1) & 1)
         for l in tiles_of(w, n):

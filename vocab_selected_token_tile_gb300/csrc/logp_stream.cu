@@ -948,6 +948,13 @@ struct TileRotation {
 // for phase B.
 template <int MODE, int W, bool ENT>
 __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0, int first) {
+    // Forward: a warp with no tile in the row (ntl < NW) skips it: it writes
+    // nothing, and rowdone counts only the min(NW, ntl) warps that have
+    // tiles.  Each of those waits for partfree of row n - rbufs first, so
+    // rowdone and partfree cannot run a phase ahead of any warp that still
+    // uses them.  (The fused modes keep every warp in every row: the LSE of
+    // row n must outlive phase B of row n in every warp.)
+    if (MODE == kModeFwd && first >= x.ntl) return true;
     const int lane = x.lane;
     const int b = row_buf(p, n);
     bool ok = true;
@@ -1111,7 +1118,7 @@ __global__ void __launch_bounds__(threads_for(MODE, PER_SM), PER_SM)
             x.seq[s] = 0xFFFFFFFFu;
         }
         for (int b = 0; b < p.rbufs; ++b) {
-            mbar_init(x.rowdone0 + 8u * b, NW);
+            mbar_init(x.rowdone0 + 8u * b, (uint32_t)(MODE == kModeFwd ? min(NW, x.ntl) : NW));
             mbar_init(x.lseready0 + 8u * b, 1);
             mbar_init(x.partfree0 + 8u * b, 1);
             mbar_init(x.xbar0 + 8u * b, 1);    // the local arrival (with expect-tx on the folder)
