@@ -157,7 +157,8 @@ def test_workload_qwen3_all_rows_and_vtp_sha():
 
 def test_fused_schedules_agree_bitwise(monkeypatch):
     """The L2 schedule (default) and the resident schedule of the fused
-    forward+backward, and the forward, at one or two CTAs per SM, run the
+    forward+backward, and the forward, at one or two CTAs per SM and row
+    skews 0-2, run the
     same per-tile arithmetic on the same bytes, so their outputs are bitwise
     equal, at every virtual TP, on the Qwen3-shaped batch (13-27 rows per
     CTA: the skewed row order wraps the ring many times)."""
@@ -170,9 +171,11 @@ def test_fused_schedules_agree_bitwise(monkeypatch):
     dlog = to_dev(bits)
     dt, dg = torch.from_numpy(tgt).cuda(), torch.from_numpy(g).cuda()
     ref = None
-    for schedule, per_sm in (("l2", "0"), ("l2", "1"), ("l2", "2"), ("resident", "0")):
+    for schedule, per_sm, skew in (("l2", "0", "-1"), ("l2", "1", "-1"), ("l2", "2", "-1"), ("l2", "2", "0"),
+                                   ("l2", "1", "0"), ("l2", "2", "2"), ("resident", "0", "-1")):
         monkeypatch.setenv("RLK_FUSED_SCHEDULE", schedule)
         monkeypatch.setenv("RLK_CTAS_PER_SM", per_sm)  # 0: the planner's choice
+        monkeypatch.setenv("RLK_FUSED_SKEW", skew)  # -1: the planner's choice
         for vtp in (1, 2, 4, 8):
             c = contract(w.T, w.v_real, w.v_padded, w.num_tiles, vtp, rlk.MASK_IGNORE_INDEX)
             dl, logp, lse = rlk.logp_fwd_bwd(c, dlog, dt, None, dg)
@@ -184,9 +187,10 @@ def test_fused_schedules_agree_bitwise(monkeypatch):
                 rows = np.unique(np.concatenate([np.arange(0, w.T, 29), [w.T - 1]]))
                 check_dlogits(bits, tgt, active, g, w.v_real, w.v_padded, dl.cpu().numpy().view(np.uint16),
                               rows=rows)
-            assert got == ref, (schedule, per_sm, vtp)
+            assert got == ref, (schedule, per_sm, skew, vtp)
     # the forward at one and two CTAs per SM gives the same LSE and logp
     monkeypatch.delenv("RLK_FUSED_SCHEDULE")
+    monkeypatch.delenv("RLK_FUSED_SKEW")
     for per_sm in ("1", "2"):
         monkeypatch.setenv("RLK_CTAS_PER_SM", per_sm)
         for vtp in (1, 8):

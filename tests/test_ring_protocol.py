@@ -42,8 +42,8 @@ def ctas_per_sm(mode, vtp, v_padded, nt, sm_count=152, reuse_bytes=64 << 20):
     if mode in ("fwd", "bwd"):
         return 2
     if mode == "fused_l2":
-        shard = -(-nt // vtp) * (v_padded // nt) * 2
-        return 2 if reuse_bytes // (shard * 2 * sm_count) >= 2 else 1
+        row1 = -(-nt // vtp) * (v_padded // nt) * 2 * sm_count
+        return 2 if (reuse_bytes // (2 * row1) >= 2 or reuse_bytes // row1 < 2) else 1
     return 1
 
 
@@ -97,9 +97,9 @@ def plan_l2(vtp, v_padded, nt):
 def l2_skew(vtp, v_padded, nt, sm_count=152, reuse_bytes=64 << 20):
     """Rows of skew of the L2-assisted fused mode, as the host planner picks them."""
     w = v_padded // nt
-    ctas = sm_count * ctas_per_sm("fused_l2", vtp, v_padded, nt)
-    fit = reuse_bytes // (-(-nt // vtp) * w * 2 * ctas)
-    return max(1, min(fit - 1, row_bufs("fused_l2", nt) - 1, 4))
+    per_sm = ctas_per_sm("fused_l2", vtp, v_padded, nt)
+    fit = reuse_bytes // (-(-nt // vtp) * w * 2 * sm_count * per_sm)
+    return max(0 if per_sm == 2 else 1, min(fit - 1, row_bufs("fused_l2", nt) - 1, 2))
 
 
 def kernel_block_of(n, phase_b, R, S):
@@ -132,10 +132,10 @@ def test_kernel_block_numbering_matches_the_schedule():
 
 
 def test_l2_skew_at_the_benchmark_shapes():
-    # 152 SMs, 152576 x 64 tiles: virtual TP 1, 2 (one CTA per SM) and 4 (two)
-    # keep one row of skew; 8 (two per SM) takes four, the cap
-    assert [l2_skew(v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 1, 4]
-    assert [ctas_per_sm("fused_l2", v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 2, 2]
+    # 152 SMs, 152576 x 64 tiles: virtual TP 1 fits no row of skew (two CTAs
+    # per SM, none), 2 one at one CTA per SM, 4 one at two, 8 two (the cap)
+    assert [l2_skew(v, 152576, 64) for v in (1, 2, 4, 8)] == [0, 1, 1, 2]
+    assert [ctas_per_sm("fused_l2", v, 152576, 64) for v in (1, 2, 4, 8)] == [2, 1, 2, 2]
 
 
 CONFIGS = [(mode, vtp) for mode in ("fwd", "bwd", "fused", "fused_l2") for vtp in (1, 2, 4, 8)
@@ -155,7 +155,7 @@ def test_ring_protocol_reads_only_landed_slots(mode, vtp):
 def test_planner_replay_matches_the_benchmark_shapes():
     assert plan("fused", 2, 152576, 64) == (4, 2, 23)
     assert plan("fwd", 1, 152576, 64) == (1, 3, 7)
-    assert [plan("fused_l2", v, 152576, 64)[1:] for v in (1, 2, 4, 8)] == [(4, 11), (4, 11), (4, 5), (4, 5)]
+    assert [plan("fused_l2", v, 152576, 64)[1:] for v in (1, 2, 4, 8)] == [(4, 5), (4, 11), (4, 5), (4, 5)]
 
 
 @pytest.mark.parametrize("ns", [1, 2, 3, 5])
@@ -167,7 +167,7 @@ def test_l2_fused_schedule_progresses_with_tiny_rings(ns):
             simulate("fused_l2", rows=7, C=C, NT=64, tps=tps, NS=ns, W=16, seed=10 * ns + C)
 
 
-@pytest.mark.parametrize("rbufs,skew", [(2, 1), (4, 1), (4, 3), (8, 3), (8, 7)])
+@pytest.mark.parametrize("rbufs,skew", [(2, 0), (2, 1), (4, 1), (4, 3), (8, 0), (8, 3), (8, 7)])
 def test_deeper_row_pipelines(rbufs, skew):
     for mode in ("fwd", "fused_l2"):
         for C, tps in ((1, 3), (8, 3)):
@@ -187,7 +187,7 @@ def test_skew_needs_more_row_buffers_than_rows_in_flight():
     assert found > 0
 
 
-@pytest.mark.parametrize("rbufs,skew", [(2, 1), (4, 1), (4, 3), (8, 1), (8, 4), (8, 7)])
+@pytest.mark.parametrize("rbufs,skew", [(2, 1), (4, 0), (4, 1), (4, 3), (8, 0), (8, 1), (8, 4), (8, 7)])
 def test_single_folder_exchange(rbufs, skew):
     # One CTA folds each row and returns the LSE; buffers are reused only once
     # the LSE of the row they held is back.

@@ -77,7 +77,7 @@ __host__ __device__ constexpr int threads_for(int mode, int per_sm) {
 constexpr int kMaxSlots = 96;
 constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the final drain of own copies
 constexpr int64_t kL2ReuseBytes = 64ll << 20;  // logits held in L2 between the two reads of kModeFusedL2
-constexpr int kMaxSkew = 4;
+constexpr int kMaxSkew = 2;  // measured at virtual TP 8: skew 1-2 beat 3-4
 constexpr int kMinSlotsShared = 4;  // fewest ring slots worth running two CTAs per SM
 constexpr int64_t kFusedChunkCols = 16384;
 
@@ -1289,10 +1289,16 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     // it with one.  The resident fused schedule needs the whole shared
     // memory.  The L2 fused schedule takes two while the rows between a row's
     // two copies, with one row of skew, still fit kL2ReuseBytes at twice the
-    // CTAs (virtual TP 4 and 8 at 152576 x 64 tiles; at TP 1-2 they outgrow L2).
+    // CTAs (virtual TP 4 and 8 at 152576 x 64 tiles); else one while they fit
+    // at one CTA per SM (TP 2); else (TP 1, nothing fits) two with no skew,
+    // each CTA covering the other's wait for its row's LSE (measured on GB300:
+    // 6.3 ms against 6.6 for one CTA per SM with a row of skew).
     const int64_t shard_bytes = (int64_t)((c.num_tiles + C - 1) / C) * p.W * 2;
     int ctas_per_sm = (mode == kModeFwd || mode == kModeBwd) ? 2 : 1;
-    if (mode == kModeFusedL2 && kL2ReuseBytes / (shard_bytes * 2 * di.sm_count) >= 2) ctas_per_sm = 2;
+    if (mode == kModeFusedL2) {
+        const int64_t row1 = shard_bytes * di.sm_count;  // one row shard per SM
+        if (kL2ReuseBytes / (2 * row1) >= 2 || kL2ReuseBytes / row1 < 2) ctas_per_sm = 2;
+    }
     const int forced = env_int("RLK_CTAS_PER_SM", 0);
     if (forced == 1 || forced == 2) ctas_per_sm = forced;
     uint32_t budget = (uint32_t)di.smem_optin / (uint32_t)ctas_per_sm - 1024u;
@@ -1319,7 +1325,9 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         p.rb_shift = rb == 8 ? 3 : rb == 4 ? 2 : 1;
         // kModeFusedL2 skew: the rows of phase A between a row's two copies
         // must stay in L2.  Keep (skew + 1) rows of every SM's shard within
-        // kL2ReuseBytes, at least one row of skew, skew < rbufs, at most kMaxSkew.
+        // kL2ReuseBytes, skew < rbufs, at most kMaxSkew; at least one row of
+        // skew with one CTA per SM (nothing else runs while a CTA waits for its
+        // LSE), none needed with two.
         int skew = 1;
         if (mode == kModeFusedL2) {
             const int64_t gpu_row = shard_bytes * di.sm_count * ctas_per_sm;
@@ -1327,7 +1335,7 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
             skew = fit - 1;
             if (skew > kMaxSkew) skew = kMaxSkew;
             if (skew > rb - 1) skew = rb - 1;
-            if (skew < 1) skew = 1;
+            if (skew < (ctas_per_sm == 2 ? 0 : 1)) skew = ctas_per_sm == 2 ? 0 : 1;
             // skew 0: phase B of a row right after its phase A and LSE
             const int forced_skew = env_int("RLK_FUSED_SKEW", -1);
             if (forced_skew >= 0) skew = forced_skew < rb - 1 ? forced_skew : rb - 1;
