@@ -1,0 +1,57 @@
+"""torch.autograd entry point of the selected-token log-probability.
+
+Argument marshalling only: the forward calls ``rlk_logp_fwd`` and the
+backward ``rlk_logp_bwd`` with the saved LSE, so every step of the arithmetic
+runs in the CUDA library.  The outputs follow the typed contract of PR #289
+("[WS2][PR4][Logp] feat: add distributed TP/CP logprob drift report",
+"typed contract" commit: FP32 logprob and FP32 LSE outputs); the LSE is not
+differentiable.
+"""
+import torch
+
+from . import MASK_EXPLICIT, MASK_IGNORE_INDEX, Contract, logp_bwd, logp_fwd
+
+_LOGIT_DTYPES = (torch.bfloat16, torch.int16)  # int16: BF16 bits viewed as integers
+
+
+class SelectedTokenLogprob(torch.autograd.Function):
+    """(logp, lse) of BF16 logits [T, row_stride]; d logits = g (onehot - softmax) in BF16."""
+
+    @staticmethod
+    def forward(ctx, logits, targets, mask, contract):
+        if logits.dtype not in _LOGIT_DTYPES or not logits.is_cuda:
+            raise TypeError("logits must be a CUDA tensor of BF16 (or its int16 bits)")
+        logp, lse = logp_fwd(contract, logits, targets, mask)
+        ctx.save_for_backward(logits, targets, mask, lse)
+        ctx.contract = contract
+        ctx.mark_non_differentiable(lse)
+        return logp, lse
+
+    @staticmethod
+    def backward(ctx, grad_logp, grad_lse):
+        logits, targets, mask, lse = ctx.saved_tensors
+        if grad_logp is None:
+            return None, None, None, None
+        g = grad_logp if (grad_logp.dtype == torch.float32 and grad_logp.is_contiguous()) else \
+            grad_logp.to(torch.float32).contiguous()
+        c = ctx.contract
+        # columns [V_padded, row_stride) are not the kernel's: their gradient is zero
+        out = torch.zeros_like(logits) if c.row_stride > c.V_padded else None
+        dlogits = logp_bwd(c, logits, targets, mask, lse, g, dlogits=out)
+        return dlogits, None, None, None
+
+
+def selected_logprob(logits, targets, mask=None, v_real=None, v_padded=None, num_tiles=64, virtual_tp=1,
+                     ignore_index=-100):
+    """(logp, lse) with autograd; ``mask`` None selects ignore_index mode.
+
+    ``logits`` is [T, row_stride] BF16 on the GPU; columns [v_real, v_padded)
+    are padding (v_padded defaults to row_stride, v_real to v_padded).
+    """
+    T, stride = logits.shape
+    vp = stride if v_padded is None else v_padded
+    vr = vp if v_real is None else v_real
+    c = Contract(T=T, V_real=vr, V_padded=vp, num_tiles=num_tiles, virtual_tp=virtual_tp,
+                 mask_mode=MASK_EXPLICIT if mask is not None else MASK_IGNORE_INDEX, ignore_index=ignore_index,
+                 row_stride=stride)
+    return SelectedTokenLogprob.apply(logits, targets, mask, c)
