@@ -32,6 +32,7 @@ UNIT = "tokens/s"
 KERNEL_SOURCES = [
     "vocab_selected_token_tile_gb300/csrc/logp_stream.cu",
     "vocab_selected_token_tile_gb300/csrc/rlk_ptx.cuh",
+    "vocab_selected_token_tile_gb300/csrc/rlk_fold.cuh",
 ]
 
 

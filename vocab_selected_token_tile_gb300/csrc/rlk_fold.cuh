@@ -18,13 +18,75 @@ namespace rlk {
 
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^y = 2^(y log2 e)
 
+// Up to 64 tiles the fold keeps everything in registers: lane l holds tiles
+// l and l + 32, the two prefix-max scans run interleaved, and the recurrence
+// runs warp-uniformly on values broadcast by shuffles, which do not depend on
+// S and so issue ahead of the FMA chain.  Every value is formed by exactly
+// the operations of the general path below, in the same order, so both give
+// the same bits.
+struct FoldTerms {
+    float f[2];  // rescale factors f_k = exp(M_{k-1} - M_k) of tiles lane, lane + 32
+    float e[2];  // exp(m_k - M_k), 0 for an identity tile
+    float b[2];  // terms b_k = s_k exp(m_k - M_k)
+    float M;     // the prefix max over all tiles (the row's max)
+};
+
+__device__ __forceinline__ FoldTerms fold_terms64(const float2 (&p)[2], int lane) {
+    float v0 = p[0].x, v1 = p[1].x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float o0 = __shfl_up_sync(0xFFFFFFFFu, v0, off);
+        const float o1 = __shfl_up_sync(0xFFFFFFFFu, v1, off);
+        if (lane >= off) {
+            v0 = fmax_nan(v0, o0);
+            v1 = fmax_nan(v1, o1);
+        }
+    }
+    float M[2];
+    M[0] = fmax_nan(-INFINITY, v0);
+    const float carry = __shfl_sync(0xFFFFFFFFu, M[0], 31);
+    M[1] = fmax_nan(carry, v1);
+    float Mp[2] = {__shfl_up_sync(0xFFFFFFFFu, M[0], 1), __shfl_up_sync(0xFFFFFFFFu, M[1], 1)};
+    if (lane == 0) {
+        Mp[0] = -INFINITY;
+        Mp[1] = carry;
+    }
+    FoldTerms t;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        t.f[h] = (Mp[h] == -INFINITY) ? 0.f : ex2_approx(__fmul_rn(__fsub_rn(Mp[h], M[h]), kLog2e));
+        t.e[h] = (p[h].x == -INFINITY) ? 0.f : ex2_approx(__fmul_rn(__fsub_rn(p[h].x, M[h]), kLog2e));
+        t.b[h] = (p[h].x == -INFINITY) ? 0.f : __fmul_rn(p[h].y, t.e[h]);
+    }
+    t.M = __shfl_sync(0xFFFFFFFFu, M[1], 31);
+    return t;
+}
+
+__device__ __forceinline__ void load_parts64(const float2* part, int NT, int lane, float2 (&p)[2]) {
+    p[0] = lane < NT ? part[lane] : make_float2(-INFINITY, 0.f);
+    p[1] = lane + 32 < NT ? part[lane + 32] : make_float2(-INFINITY, 0.f);
+}
+
 // Left fold of part[0..NT) by one warp; returns LSE = m + log s in every lane
 // (-inf when every tile is the identity; NaN propagates).  The running maxima
 // M_k are an exact prefix max; the rescale factors f_k = exp(M_{k-1} - M_k)
-// and the terms b_k = s_k exp(m_k - M_k) are formed lane-parallel into
-// scratch[0..NT); the sum recurrence S_k = S_{k-1} f_k + b_k then runs in
-// index order in lane 0.
+// and the terms b_k = s_k exp(m_k - M_k) are formed lane-parallel (beyond 64
+// tiles into scratch[0..NT)); the sum recurrence S_k = S_{k-1} f_k + b_k then
+// runs in index order.
 __device__ __forceinline__ float fold_tiles(const float2* part, int NT, float2* scratch, int lane) {
+    if (NT <= 64) {
+        float2 p[2];
+        load_parts64(part, NT, lane, p);
+        const FoldTerms t = fold_terms64(p, lane);
+        float S = 0.f;
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+            const float f = __shfl_sync(0xFFFFFFFFu, t.f[k >> 5], k & 31);
+            const float b = __shfl_sync(0xFFFFFFFFu, t.b[k >> 5], k & 31);
+            if (k < NT) S = __fmaf_rn(S, f, b);
+        }
+        return (t.M == -INFINITY) ? -INFINITY : __fadd_rn(t.M, logf(S));
+    }
     float carry = -INFINITY;
     for (int c0 = 0; c0 < NT; c0 += 32) {
         const int k = c0 + lane;
@@ -66,6 +128,31 @@ __device__ __forceinline__ float fold_tiles(const float2* part, int NT, float2* 
 // lane; the entropy is NaN when the LSE is not finite.
 __device__ __forceinline__ float2 fold_tiles_ent(const float2* part, const float* tpart, int NT, float2* scratch,
                                                  float* scratch_t, int lane) {
+    if (NT <= 64) {
+        float2 p[2];
+        load_parts64(part, NT, lane, p);
+        const FoldTerms t = fold_terms64(p, lane);
+        float te[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int k = lane + 32 * h;
+            te[h] = (k >= NT || p[h].x == -INFINITY) ? 0.f : __fmul_rn(tpart[k], t.e[h]);
+        }
+        float S = 0.f, Tt = 0.f;
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+            const float f = __shfl_sync(0xFFFFFFFFu, t.f[k >> 5], k & 31);
+            const float b = __shfl_sync(0xFFFFFFFFu, t.b[k >> 5], k & 31);
+            const float tk = __shfl_sync(0xFFFFFFFFu, te[k >> 5], k & 31);
+            if (k < NT) {
+                S = __fmaf_rn(S, f, b);
+                Tt = __fmaf_rn(Tt, f, tk);
+            }
+        }
+        const float lse = (t.M == -INFINITY) ? -INFINITY : __fadd_rn(t.M, logf(S));
+        const float ent = isfinite(lse) ? __fsub_rn(lse, __fdiv_rn(Tt, S)) : __int_as_float(0x7FC00000);
+        return make_float2(lse, ent);
+    }
     float carry = -INFINITY;
     for (int c0 = 0; c0 < NT; c0 += 32) {
         const int k = c0 + lane;
