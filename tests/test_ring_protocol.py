@@ -73,9 +73,11 @@ def plan(mode, vtp, v_padded, nt):
 
     C = 1 if mode == "bwd" else vtp
     tps = tps_target
-    if mode == "fused_l2":  # the largest divisor of the shard's tiles within 16384 columns
+    if mode in ("fused_l2", "fwd", "bwd"):  # the largest divisor of the shard's tiles within 16384 columns
         ntl = nt // C
-        tps = max(d for d in range(1, ntl + 1) if ntl % d == 0 and d * w <= 16384)
+        best = max(d for d in range(1, ntl + 1) if ntl % d == 0 and d * w <= 16384)
+        if mode == "fused_l2" or 2 * best >= tps_target:
+            tps = best
     if mode == "fused":
         while True:
             ntl = -(-nt // C)
@@ -154,7 +156,7 @@ def test_ring_protocol_reads_only_landed_slots(mode, vtp):
 
 def test_planner_replay_matches_the_benchmark_shapes():
     assert plan("fused", 2, 152576, 64) == (4, 2, 23)
-    assert plan("fwd", 1, 152576, 64) == (1, 3, 7)
+    assert plan("fwd", 1, 152576, 64) == (1, 4, 5)
     assert [plan("fused_l2", v, 152576, 64)[1:] for v in (1, 2, 4, 8)] == [(4, 5), (4, 11), (4, 5), (4, 5)]
 
 

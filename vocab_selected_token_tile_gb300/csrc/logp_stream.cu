@@ -1272,16 +1272,19 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         if (!(sch && std::string(sch) == "resident")) mode = kModeFusedL2;
     }
     int C = (mode == kModeBwd) ? 1 : c.virtual_tp;
-    // kModeFusedL2 issues twice the copies of the forward (both phases): it
-    // takes larger chunks, the largest number of tiles that divides the CTA's
-    // shard and stays within kFusedChunkCols columns (measured: 4 tiles of
-    // 2384 columns run 2-7% faster than 3 at every virtual TP).
-    if (mode == kModeFusedL2 && env_int("RLK_TPS", 0) == 0) {
+    // The streaming modes take larger chunks where the CTA's shard allows:
+    // the largest number of tiles that divides it and stays within
+    // kFusedChunkCols columns (measured: 4 tiles of 2384 columns run 2-7%
+    // faster than 3 for kModeFusedL2, which issues twice the copies, and
+    // 0.3-1.5% faster for the forward and the backward).  The forward and the
+    // backward keep the ~8192-column target where no such divisor reaches
+    // half of it (a shard of a prime number of tiles, say).
+    if ((mode == kModeFusedL2 || mode == kModeFwd || mode == kModeBwd) && env_int("RLK_TPS", 0) == 0) {
         const int ntl = c.num_tiles / C;
         int best = 1;
         for (int d = 1; d <= ntl; ++d)
             if (ntl % d == 0 && (int64_t)d * p.W <= kFusedChunkCols) best = d;
-        set_chunk(best);
+        if (mode == kModeFusedL2 || 2 * best >= tps_target) set_chunk(best);
     }
     // CTAs per SM.  Two streaming CTAs per SM double the bulk-copy issue rate
     // (two producer warps) and let clusters of 8 cover every SM: measured on
