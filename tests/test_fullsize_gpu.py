@@ -93,6 +93,13 @@ def test_grpo_fused_full_size_in_bench_configuration(batch):
     dl1 = rlk.logp_bwd(c1, batch["logits"], batch["dt"], batch["dm"], lse1, batch["dg"])
     torch.cuda.synchronize()
     assert torch.equal(dl1, dl)
+    # the fused step at virtual TP 1 and 8 (their own planner choices: two CTAs per SM with
+    # no row skew, and two rows of skew) gives the same bits as the bench configuration
+    for vtp in (1, 8):
+        dlv, lpv, lsv = rlk.logp_fwd_bwd(c.replace(virtual_tp=vtp), batch["logits"], batch["dt"], batch["dm"],
+                                         batch["dg"], dlogits=dl1)
+        torch.cuda.synchronize()
+        assert torch.equal(lpv, logp) and torch.equal(lsv, lse) and torch.equal(dlv, dl), vtp
     # oracle-side sanity of the sampled rows' gradient sums (pins the device property above)
     ref = oracle.dlogits(batch["bits"][:8], batch["tgt"][rows[:8]], batch["active"][rows[:8]],
                          batch["g"][rows[:8]], w.v_real, w.v_padded)
