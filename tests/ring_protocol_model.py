@@ -37,7 +37,8 @@ class Bar:
 
     def arrive(self, n=1):
         self.pending -= n
-        assert self.pending >= 0, "more arrivals than the phase expects"
+        if self.pending < 0:
+            raise ProtocolError("more arrivals than the phase expects")
         self.check()
 
     def check(self):
@@ -70,16 +71,39 @@ def block_schedule(mode, rows, skew=1):
     return seq
 
 
+def row_skip_safe(W, ntl, rbufs):
+    """The planner's condition for the forward's row skip (row_skip_safe in logp_stream.cu): every
+    warp's first row below 2*rbufs and its consecutive rows at most rbufs apart."""
+    if ntl >= W:
+        return False
+    step = ntl % W
+    for w in range(W):
+        last, r = -1, 0
+        for n in range(2 * W + 2 * rbufs):
+            if (w - r) % W < ntl:
+                if (n >= 2 * rbufs) if last < 0 else (n - last > rbufs):
+                    return False
+                last = n
+            r = (r + step) % W
+        if last < 0:
+            return False
+    return True
+
+
 def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80, rbufs=2, skew=1,
-             producers=1, producer_seqcheck=True):
+             producers=1, producer_seqcheck=True, row_skip=None):
     """mode: 'fwd' | 'bwd' | 'fused' | 'fused_l2'; rbufs row buffers, fused_l2 row skew;
     producers: producer warps per CTA, producer p issuing the items i with i mod producers == p
     (each waits until the slot's previous item is issued before its empty-barrier parity,
     unless producer_seqcheck is off).
 
+    row_skip: the forward's skip of rows without a tile (None: the planner's condition).
+
     Raises ProtocolError on a stale read or a deadlock."""
     rng = random.Random(seed)
     ntl = NT // C
+    if row_skip is None:
+        row_skip = mode == "fwd" and row_skip_safe(W, ntl, rbufs)
     nch = (ntl + tps - 1) // tps
     R = rbufs
     S = skew if mode == "fused_l2" else 1
@@ -101,7 +125,7 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
         c.seq = [None] * NS
         c.data = [None] * NS
         c.inflight = []
-        c.rowdone = [Bar(min(W, ntl) if mode == "fwd" else W) for _ in range(R)]
+        c.rowdone = [Bar(min(W, ntl) if row_skip else W) for _ in range(R)]
         c.lseready = [Bar(1) for _ in range(R)]
         c.partfree = [Bar(1) for _ in range(R)]
         c.xbar = [Bar(1) for _ in range(R)]
@@ -172,7 +196,7 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
 
     def phase_a(c, w, n):
         b = n % R
-        if mode == "fwd" and not tiles_of(w, n):  # forward: a warp without tiles skips the row
+        if row_skip and not tiles_of(w, n):  # forward: a warp without tiles skips the row
             return
         if n >= R:
             yield from wait(c.partfree[b], (n // R - 1) & 1)

@@ -13,7 +13,8 @@ import sys
 import pytest
 import torch
 
-from test_ring_protocol import SMEM_OPTIN, ctas_per_sm, l2_skew, plan, row_bufs
+from ring_protocol_model import row_skip_safe
+from test_ring_protocol import SMEM_OPTIN, consumers_for, ctas_per_sm, l2_skew, plan, row_bufs
 
 pytestmark = pytest.mark.gpu
 
@@ -21,7 +22,7 @@ if not torch.cuda.is_available():  # pragma: no cover - the CPU suite deselects 
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 PLAN = re.compile(r"rlk stream plan: mode (\d+), (\d+) CTA\(s\)/SM, (\d+) clusters x (\d+) CTAs, (\d+) tiles/copy, "
-                  r"(\d+) slots of (\d+) B, (\d+) row buffers, skew (\d+)")
+                  r"(\d+) slots of (\d+) B, (\d+) row buffers, skew (\d+), row skip (\d+)")
 MODES = {0: "fwd", 1: "bwd", 3: "fused_l2"}
 
 SCRIPT = r"""
@@ -57,10 +58,12 @@ def test_compiled_planner_matches_the_replay():
     assert len(plans) == 12, out.stderr[-2000:]
     for i, vtp in enumerate((1, 2, 4, 8)):
         for j, want_mode in enumerate(("fwd", "bwd", "fused_l2")):
-            mode, per_sm, clusters, C, tps, ns, _, rb, skew = plans[3 * i + j]
+            mode, per_sm, clusters, C, tps, ns, _, rb, skew, skip = plans[3 * i + j]
             assert MODES[mode] == want_mode
             assert (C, tps, ns) == plan(want_mode, vtp, 152576, 64), (want_mode, vtp)
             assert per_sm == ctas_per_sm(want_mode, vtp, 152576, 64), (want_mode, vtp)
             assert rb == row_bufs(want_mode, 64), (want_mode, vtp)
             if want_mode == "fused_l2":
                 assert skew == l2_skew(vtp, 152576, 64), vtp
+            want_skip = want_mode == "fwd" and row_skip_safe(consumers_for("fwd", per_sm), 64 // C, rb)
+            assert skip == int(want_skip), (want_mode, vtp)

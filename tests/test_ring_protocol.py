@@ -10,7 +10,7 @@ finds it); with the check, no configuration reads a stale slot or deadlocks.
 """
 import pytest
 
-from ring_protocol_model import ProtocolError, block_schedule, simulate
+from ring_protocol_model import ProtocolError, block_schedule, row_skip_safe, simulate
 
 SMEM_OPTIN = 232448
 
@@ -256,3 +256,35 @@ def test_two_producers_wait_for_the_slots_previous_item(mode):
         for ns in (odd_ns - 1, odd_ns):
             simulate(mode, rows=16, C=C if mode != "bwd" else 1, NT=64, tps=tps, NS=ns, W=16, seed=seed,
                      rbufs=rb, producers=2, max_delay=150)
+
+
+def test_forward_row_skip_condition():
+    # virtual TP 8 at 64 tiles (8 tiles per CTA and row, 12 consumer warps): each warp works two
+    # rows of every three, so its partfree parity wait stays within one phase; at 1-2 tiles per
+    # row a warp works one row in 6 or 12 and the skip is off
+    assert row_skip_safe(12, 8, 4) and row_skip_safe(12, 4, 4)
+    assert not row_skip_safe(12, 2, 4) and not row_skip_safe(12, 1, 4)
+    assert not row_skip_safe(12, 12, 4) and not row_skip_safe(12, 64, 4)
+
+
+def test_forward_row_skip_without_the_condition_is_caught():
+    # 8 tiles over 8 CTAs: one tile per CTA and row.  Forcing the skip lets a warp that works
+    # one row in 12 wait on a partfree parity two phases stale; the model finds it.  With the
+    # planner's condition (the skip off here) every seed passes.
+    found = 0
+    for seed in range(6):
+        try:
+            simulate("fwd", rows=96, C=8, NT=8, tps=1024, NS=6, W=12, seed=seed, rbufs=4, max_delay=200,
+                     row_skip=True)
+        except ProtocolError:
+            found += 1
+        simulate("fwd", rows=96, C=8, NT=8, tps=1024, NS=6, W=12, seed=seed, rbufs=4, max_delay=200)
+    assert found > 0
+
+
+@pytest.mark.parametrize("C", [1, 2, 4, 8])
+def test_forward_row_skip_many_short_rows(C):
+    # the shape of the many-short-rows GPU test (8 tiles of 8 columns), where the skip is on
+    # at C = 1, 2 and off at 4, 8
+    for seed in range(4):
+        simulate("fwd", rows=150, C=C, NT=8, tps=1024, NS=6, W=12, seed=seed, rbufs=4, max_delay=200)

@@ -1,0 +1,60 @@
+"""Many short rows: every CTA runs hundreds of rows, so the slot ring, the row
+buffers, the tile rotation and (at virtual TP 8, one tile per CTA and row)
+the row skip of the forward wrap around many times.  All rows of every output
+are compared with the FP64 oracle; outputs are bitwise equal across virtual
+TP and between the fused, split and entropy paths."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import vocab_selected_token_tile_gb300 as rlk
+from parity import ENT_TOL, LSE_TOL, contract, f32_bits, to_dev
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - the CPU suite deselects this module
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+
+def test_many_short_rows_all_paths_all_virtual_tp():
+    T, v_real, v_padded, nt = 131072 + 37, 61, 64, 8
+    bits = synth.logits_host(0, T, v_padded, v_padded, v_real, seed=29, sigma=3.0, nspikes=1, garbage=True)
+    tgt = synth.targets(T, v_real, 29)
+    rng = np.random.default_rng(29)
+    mask = (rng.random(T) < 0.6).astype(np.uint8)
+    active = mask != 0
+    g = np.where(active, rng.standard_normal(T), 0.0).astype(np.float32)
+
+    ref_logp, ref_lse = oracle.selected_logp(bits, tgt, active, v_real)
+    ref_ent = oracle.entropy(bits, v_real)
+    ref_dl = oracle.dlogits(bits, tgt, active, g, v_real, v_padded)
+
+    d = to_dev(bits)
+    dt, dm, dg = (torch.from_numpy(a).cuda() for a in (tgt, mask, g))
+    first = None
+    for vtp in (1, 2, 4, 8):
+        c = contract(T, v_real, v_padded, nt, vtp)
+        logp, lse = rlk.logp_fwd(c, d, dt, dm)
+        lp_e, ls_e, ent = rlk.logp_fwd_entropy(c, d, dt, dm)
+        dl, lp_f, ls_f = rlk.logp_fwd_bwd(c, d, dt, dm, dg)
+        dl_s = rlk.logp_bwd(c, d, dt, dm, lse, dg)
+        torch.cuda.synchronize()
+        outs = [t.cpu().numpy() for t in (logp, lse, ent, dl)]
+        for a, b in ((logp, lp_e), (lse, ls_e), (logp, lp_f), (lse, ls_f), (dl, dl_s)):
+            assert torch.equal(a, b), vtp
+        if first is None:
+            first = outs
+            lp, ls, en, dlb = outs
+            assert np.max(np.abs(ls - ref_lse)) <= LSE_TOL
+            assert np.max(np.abs(lp[active] - ref_logp[active])) <= LSE_TOL
+            assert np.all(f32_bits(lp[~active]) == 0)
+            assert np.max(np.abs(en - ref_ent)) <= ENT_TOL
+            got = oracle.bf16_bits_to_f64(dlb.view(np.uint16)[:, :v_padded])
+            err = np.abs(got - ref_dl)
+            assert np.all(err <= np.ldexp(np.abs(ref_dl), -8) + 4e-6 * np.abs(g)[:, None] + 1e-30)
+            assert not dlb.view(np.uint16)[:, v_real:].any() and not dlb.view(np.uint16)[~active].any()
+        else:
+            for a, b in zip(first, outs):
+                assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), vtp

@@ -124,6 +124,7 @@ struct Params {
     int32_t rbufs, rb_shift;  // row buffers of the fold (a power of two) and its log2
     int32_t skew;             // kModeFusedL2: phase A runs `skew` rows ahead of phase B (< rbufs)
     int32_t ent;  // the launch computes the entropy (stream_kernel's ENT)
+    int32_t row_skip;  // kModeFwd: consumer warps skip the rows in which they have no tile (row_skip_safe)
     uint32_t off_full, off_empty, off_hdr, off_seq, off_part, off_fold, off_rows, off_xtin, off_bars, off_flag;
     uint32_t off_meta;  // TileMeta of each of the CTA's tiles
     uint32_t off_tpart, off_foldt;  // ENT: t_k per row buffer, and the fold's scratch for them
@@ -948,13 +949,14 @@ struct TileRotation {
 // for phase B.
 template <int MODE, int W, bool ENT>
 __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0, int first) {
-    // Forward: a warp with no tile in the row (ntl < NW) skips it: it writes
-    // nothing, and rowdone counts only the min(NW, ntl) warps that have
-    // tiles.  Each of those waits for partfree of row n - rbufs first, so
-    // rowdone and partfree cannot run a phase ahead of any warp that still
-    // uses them.  (The fused modes keep every warp in every row: the LSE of
-    // row n must outlive phase B of row n in every warp.)
-    if (MODE == kModeFwd && first >= x.ntl) return true;
+    // Forward with row_skip: a warp with no tile in the row (ntl < NW) skips
+    // it: it writes nothing, and rowdone counts only the min(NW, ntl) warps
+    // that have tiles.  Each of those waits for partfree of row n - rbufs
+    // first, and the planner allows the skip only where that parity wait
+    // stays within one phase (row_skip_safe).  The fused modes keep every
+    // warp in every row: the LSE of row n must outlive phase B of row n in
+    // every warp.
+    if (MODE == kModeFwd && p.row_skip && first >= x.ntl) return true;
     const int lane = x.lane;
     const int b = row_buf(p, n);
     bool ok = true;
@@ -1118,7 +1120,7 @@ __global__ void __launch_bounds__(threads_for(MODE, PER_SM), PER_SM)
             x.seq[s] = 0xFFFFFFFFu;
         }
         for (int b = 0; b < p.rbufs; ++b) {
-            mbar_init(x.rowdone0 + 8u * b, (uint32_t)(MODE == kModeFwd ? min(NW, x.ntl) : NW));
+            mbar_init(x.rowdone0 + 8u * b, (uint32_t)(MODE == kModeFwd && p.row_skip ? min(NW, x.ntl) : NW));
             mbar_init(x.lseready0 + 8u * b, 1);
             mbar_init(x.partfree0 + 8u * b, 1);
             mbar_init(x.xbar0 + 8u * b, 1);    // the local arrival (with expect-tx on the folder)
@@ -1192,6 +1194,31 @@ FastDiv make_fastdiv(uint32_t d) {
     while ((1ull << f.s) < d) ++f.s;
     f.m = (uint32_t)((((uint64_t)1 << 32) * (((uint64_t)1 << f.s) - d)) / d + 1);
     return f;
+}
+
+// Whether forward consumer warps may skip the rows in which they have no
+// tile.  A warp still waits for the release of row n - rbufs (a parity wait
+// on partfree) before each row it works on, and a parity wait is right only
+// while the barrier is within one phase of it: row n - 2*rbufs must already
+// be released.  That holds when every warp's first row is below 2*rbufs and
+// its consecutive rows are at most rbufs apart (its previous wait then
+// covered row n - 2*rbufs); the tile rotation repeats within NW rows.
+bool row_skip_safe(int NW, int ntl, int rbufs) {
+    if (ntl >= NW) return false;  // every warp has a tile in every row
+    const int step = ntl % NW;
+    for (int w = 0; w < NW; ++w) {
+        int last = -1, r = 0;
+        for (int n = 0; n < 2 * NW + 2 * rbufs; ++n) {
+            const int f = ((w - r) % NW + NW) % NW;
+            if (f < ntl) {
+                if (last < 0 ? n >= 2 * rbufs : n - last > rbufs) return false;
+                last = n;
+            }
+            r = (r + step) % NW;
+        }
+        if (last < 0) return false;
+    }
+    return true;
 }
 
 // Shared-memory layout for NS slots; returns the total bytes.
@@ -1437,6 +1464,10 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     if (clusters <= 0) return RLK_ERR_CUDA;
     void (*kfn)(Params) = pick(ctas_per_sm);
     cfg.blockDim = dim3(threads_for(mode, ctas_per_sm), 1, 1);
+    p.row_skip = (mode == kModeFwd &&
+                  row_skip_safe(consumers_for(mode, ctas_per_sm), (c.num_tiles + p.C - 1) / p.C, p.rbufs))
+                     ? 1
+                     : 0;
     p.NS = NS;
     p.ns_div = make_fastdiv((uint32_t)NS);
     smem = layout(p, NS);
@@ -1447,8 +1478,9 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     if (env_int("RLK_VERBOSE", 0))
         std::fprintf(stderr,
                      "rlk stream plan: mode %d, %d CTA(s)/SM, %lld clusters x %d CTAs, %d tiles/copy, %d slots of %d B, "
-                     "%d row buffers, skew %d, %u B shared memory\n",
-                     mode, ctas_per_sm, (long long)clusters, p.C, p.tps, p.NS, p.slot_bytes, p.rbufs, p.skew, smem);
+                     "%d row buffers, skew %d, row skip %d, %u B shared memory\n",
+                     mode, ctas_per_sm, (long long)clusters, p.C, p.tps, p.NS, p.slot_bytes, p.rbufs, p.skew,
+                     p.row_skip, smem);
     e = cudaLaunchKernelEx(&cfg, kfn, p);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(e));
     return RLK_OK;
