@@ -58,3 +58,39 @@ def test_many_short_rows_all_paths_all_virtual_tp():
         else:
             for a, b in zip(first, outs):
                 assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), vtp
+
+
+def test_many_short_rows_every_planner_choice_gives_the_same_bits(monkeypatch):
+    """The same many-row batch under every planner override (one or two CTAs per SM,
+    2/4/8 row buffers, row skew 0-2, the resident fused schedule): bitwise the
+    default outputs at every virtual TP."""
+    T, v_real, v_padded, nt = 65536 + 11, 61, 64, 8
+    bits = synth.logits_host(0, T, v_padded, v_padded, v_real, seed=31, sigma=3.0, nspikes=1, garbage=True)
+    tgt = synth.targets(T, v_real, 31)
+    rng = np.random.default_rng(31)
+    mask = (rng.random(T) < 0.6).astype(np.uint8)
+    g = np.where(mask != 0, rng.standard_normal(T), 0.0).astype(np.float32)
+    d = to_dev(bits)
+    dt, dm, dg = (torch.from_numpy(a).cuda() for a in (tgt, mask, g))
+
+    def run(vtp):
+        c = contract(T, v_real, v_padded, nt, vtp)
+        logp, lse = rlk.logp_fwd(c, d, dt, dm)
+        _, _, ent = rlk.logp_fwd_entropy(c, d, dt, dm)
+        dl, lp_f, ls_f = rlk.logp_fwd_bwd(c, d, dt, dm, dg)
+        dl_s = rlk.logp_bwd(c, d, dt, dm, lse, dg)
+        torch.cuda.synchronize()
+        return [t.cpu().numpy().view(np.uint8) for t in (logp, lse, ent, dl, lp_f, ls_f, dl_s)]
+
+    ref = run(1)
+    variants = [{"RLK_CTAS_PER_SM": "1"}, {"RLK_CTAS_PER_SM": "2"}, {"RLK_ROW_BUFS": "2"}, {"RLK_ROW_BUFS": "8"},
+                {"RLK_FUSED_SKEW": "0"}, {"RLK_FUSED_SKEW": "2"}, {"RLK_FUSED_SCHEDULE": "resident"}]
+    for env in [{}] + variants:
+        for k, v in env.items():
+            monkeypatch.setenv(k, v)
+        for vtp in (1, 2, 4, 8):
+            got = run(vtp)
+            for i, (a, b) in enumerate(zip(ref, got)):
+                assert np.array_equal(a, b), (env, vtp, i)
+        for k in env:
+            monkeypatch.delenv(k)
