@@ -94,3 +94,46 @@ def test_many_short_rows_every_planner_choice_gives_the_same_bits(monkeypatch):
                 assert np.array_equal(a, b), (env, vtp, i)
         for k in env:
             monkeypatch.delenv(k)
+
+
+# (T, V_real, V_padded, num_tiles): the widest tiles (16384 columns, one per copy), the most
+# tiles (1024 of 8 columns, a 48 KB per-tile table), and an odd tile count
+SHAPES = [(3001, 32765, 32768, 2), (16384 + 5, 8190, 8192, 1024), (20000 + 3, 6997, 7007, 7)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "T%d_V%d_P%d_NT%d" % s)
+def test_many_rows_at_extreme_tile_shapes(shape):
+    T, v_real, v_padded, nt = shape
+    stride = (v_padded + 7) // 8 * 8
+    bits = synth.logits_host(0, T, stride, v_padded, v_real, seed=37, sigma=3.0, nspikes=2, garbage=True)
+    tgt = synth.targets(T, v_real, 37, ignore_frac=0.2)
+    active = tgt != -100
+    g = np.where(active, np.random.default_rng(37).standard_normal(T), 0.0).astype(np.float32)
+    d = to_dev(bits)
+    dt, dg = torch.from_numpy(tgt).cuda(), torch.from_numpy(g).cuda()
+    rows = np.unique(np.concatenate([np.arange(0, T, max(1, T // 600)), [T - 1]]))
+    ref_logp, ref_lse = oracle.selected_logp(bits[rows], tgt[rows], active[rows], v_real)
+    first = None
+    for vtp in [v for v in (1, 2, 4, 8) if nt % v == 0]:
+        c = contract(T, v_real, v_padded, nt, vtp, rlk.MASK_IGNORE_INDEX, stride=stride)
+        logp, lse = rlk.logp_fwd(c, d, dt)
+        dl, lp_f, ls_f = rlk.logp_fwd_bwd(c, d, dt, None, dg)
+        dl_s = rlk.logp_bwd(c, d, dt, None, lse, dg)
+        torch.cuda.synchronize()
+        assert torch.equal(logp, lp_f) and torch.equal(lse, ls_f) and torch.equal(dl, dl_s), vtp
+        out = [t.cpu().numpy() for t in (logp, lse, dl)]
+        if first is None:
+            first = out
+            lp, ls, dlb = out
+            assert np.max(np.abs(ls[rows] - ref_lse)) <= LSE_TOL
+            a = active[rows]
+            assert np.max(np.abs(lp[rows][a] - ref_logp[a])) <= LSE_TOL
+            assert np.all(f32_bits(lp[~active]) == 0)
+            sub = rows[:64]
+            ref_dl = oracle.dlogits(bits[sub], tgt[sub], active[sub], g[sub], v_real, v_padded)
+            got = oracle.bf16_bits_to_f64(dlb.view(np.uint16)[sub][:, :v_padded])
+            assert np.all(np.abs(got - ref_dl) <= np.ldexp(np.abs(ref_dl), -8) + 4e-6 * np.abs(g[sub])[:, None] + 1e-30)
+            assert not dlb.view(np.uint16)[:, v_real:v_padded].any() and not dlb.view(np.uint16)[~active].any()
+        else:
+            for x, y in zip(first, out):
+                assert np.array_equal(x.view(np.uint8), y.view(np.uint8)), vtp
