@@ -120,6 +120,8 @@ def test_many_rows_at_extreme_tile_shapes(shape):
         dl, lp_f, ls_f = rlk.logp_fwd_bwd(c, d, dt, None, dg)
         dl_s = rlk.logp_bwd(c, d, dt, None, lse, dg)
         torch.cuda.synchronize()
+        # columns [V_padded, row_stride) of dlogits are not written (the caller's memory)
+        dl, dl_s = dl[:, :v_padded], dl_s[:, :v_padded]
         assert torch.equal(logp, lp_f) and torch.equal(lse, ls_f) and torch.equal(dl, dl_s), vtp
         out = [t.cpu().numpy() for t in (logp, lse, dl)]
         if first is None:
@@ -131,7 +133,7 @@ def test_many_rows_at_extreme_tile_shapes(shape):
             assert np.all(f32_bits(lp[~active]) == 0)
             sub = rows[:64]
             ref_dl = oracle.dlogits(bits[sub], tgt[sub], active[sub], g[sub], v_real, v_padded)
-            got = oracle.bf16_bits_to_f64(dlb.view(np.uint16)[sub][:, :v_padded])
+            got = oracle.bf16_bits_to_f64(dlb.view(np.uint16)[sub])
             assert np.all(np.abs(got - ref_dl) <= np.ldexp(np.abs(ref_dl), -8) + 4e-6 * np.abs(g[sub])[:, None] + 1e-30)
             assert not dlb.view(np.uint16)[:, v_real:v_padded].any() and not dlb.view(np.uint16)[~active].any()
         else:
