@@ -36,6 +36,9 @@
  * Conventions for every entry point:
  *   - Device pointers are CUDA global-memory pointers owned by the caller;
  *     the library allocates nothing and keeps no pointer after returning.
+ *     Every pointer must be device (or managed) memory of the device that
+ *     holds the call's first operand; host memory, pinned or not, and
+ *     another GPU's memory return RLK_ERR_INVALID_ARG before any launch.
  *   - Work is enqueued on `stream` (NULL = the legacy default stream) and
  *     is asynchronous, unless contract->validate == 1: then the call
  *     synchronises the stream and turns the device status word into the
@@ -200,9 +203,9 @@ rlk_status rlk_logp_bwd(const rlk_logp_contract* contract, const void* logits_bf
 
 /*
  * Bytes of device workspace rlk_logp_fused_lmhead needs for hidden size H
- * (the status word, FP32 partials [T, num_tiles, 2], target logits [T], and
- * for the backward the BF16 dlogits [T, V_padded] plus 32 MB of GEMM
- * workspace); 0 for an unsupported contract.
+ * (the status word, 256 bytes of work tickets, FP32 partials
+ * [T, num_tiles, 2], target logits [T], and for the backward the BF16 dlogits
+ * [T, V_padded]); 0 for an unsupported contract.
  */
 size_t rlk_logp_lmhead_workspace_size(const rlk_logp_contract* contract, int64_t H);
 
@@ -214,17 +217,21 @@ size_t rlk_logp_lmhead_workspace_size(const rlk_logp_contract* contract, int64_t
  * (max, sumexp) partial in its epilogue; the partials are folded in fixed
  * tile order.  The logits stay FP32 (never rounded to BF16).
  *   hidden_bf16  [T, H] BF16 row-major, 16-byte aligned; H a multiple of 64.
- *   weight_bf16  [V_padded, H] BF16 row-major; rows >= V_real are padding.
+ *   weight_bf16  [V_padded, H] BF16 row-major; rows >= V_real are padding
+ *                and are never read.
  *   targets, active_mask, logp, lse: as for rlk_logp_fwd.
  *   grad_logp    NULL (forward only) or [T] FP32 upstream gradient of logp.
  *                With it the backward runs too: dlogits = g (onehot - softmax)
  *                are recomputed from a second pass of the GEMM and the LSE just
- *                formed (BF16, in the workspace), then
+ *                formed (BF16, in the workspace), then two more tcgen05 GEMMs
+ *                with FP32 accumulation give
  *   dhidden_bf16 [T, H] BF16 out = dlogits[:, :V_real] @ weight[:V_real], and
- *   dweight_bf16 [V_padded, H] BF16 out = dlogits[:, :V_real]^T @ hidden,
- *                rows >= V_real exactly 0.  These two are plain GEMMs (cuBLASLt,
- *                FP32 accumulation, no cross-block reductions, so each element
- *                is summed in one fixed order).  Both NULL without grad_logp.
+ *   dweight_f32  [V_padded, H] FP32 out, or NULL, and
+ *   dweight_bf16 [V_padded, H] BF16 out, or NULL (at least one of the two):
+ *                dlogits[:, :V_real]^T @ hidden, rows >= V_real exactly 0.
+ *                Each output element is accumulated over its whole K range in
+ *                one fixed order by one CTA (no split-K, no atomics), so the
+ *                gradients are deterministic.  All three NULL without grad_logp.
  *   workspace    rlk_logp_lmhead_workspace_size(contract, H) bytes (it holds
  *                the BF16 dlogits, T * V_padded * 2 bytes, for the backward).
  * The tile width V_padded / num_tiles must be a multiple of 16.  row_stride
@@ -233,7 +240,71 @@ size_t rlk_logp_lmhead_workspace_size(const rlk_logp_contract* contract, int64_t
 rlk_status rlk_logp_fused_lmhead(const rlk_logp_contract* contract, const void* hidden_bf16, int64_t H,
                                  const void* weight_bf16, const int64_t* targets, const uint8_t* active_mask,
                                  const float* grad_logp, float* logp, float* lse, void* dhidden_bf16,
-                                 void* dweight_bf16, void* workspace, rlk_stream_t stream);
+                                 float* dweight_f32, void* dweight_bf16, void* workspace, rlk_stream_t stream);
+
+/*
+ * Vocabulary-parallel tensor parallelism across GPUs (PR #289 "[WS2][PR4]
+ * [Logp] feat: add distributed TP/CP logprob drift report", PR-1 contract
+ * commit: tile-aligned vocabulary shards, FP32 (max, sumexp) partials moved by
+ * all-gather and merged by every rank in fixed global tile order, the target
+ * logit taken from the owner rank; issue #323, "Six-Case TP/CP Matrix").
+ * The three calls below are what one rank runs; the exchange between them is
+ * the caller's all-gather (NCCL, say) of plain device buffers.
+ *
+ * A shard call's contract is the whole problem's: T, V_real, V_padded,
+ * num_tiles, mask mode, ignore_index as for rlk_logp_fwd, and virtual_tp =
+ * tp, the number of shards (1, 2, 4 or 8, dividing num_tiles).  Shard j
+ * holds columns [j*Vs, (j+1)*Vs) of the padded vocabulary, Vs = V_padded/tp,
+ * which must be a multiple of 8 (16-byte shard starts), in a buffer of its
+ * own: logits_shard [T, row_stride] BF16 with row_stride >= Vs (0 -> Vs), a
+ * multiple of 8.  Targets are global column indices.  The results are
+ * bitwise those of rlk_logp_fwd / rlk_logp_bwd on the whole vocabulary, for
+ * every tp.
+ */
+
+/* Host-only check of a shard call's contract and shard index (touches no device). */
+rlk_status rlk_logp_check_shard_contract(const rlk_logp_contract* contract, int32_t shard);
+
+/* Bytes of device workspace each shard call needs; 0 for an invalid contract. */
+size_t rlk_logp_shard_workspace_size(const rlk_logp_contract* contract);
+
+/*
+ * Rank side of the forward, on shard `shard`:
+ *   partials_shard [T, num_tiles/tp, 2] FP32 out: the (m_k, s_k) partials of
+ *                  global tiles shard*num_tiles/tp .. (shard+1)*num_tiles/tp - 1;
+ *   target_logit   [T] FP32 out: float(logit[r, t_r]) on active rows whose
+ *                  target column this shard holds, 0 on every other row.
+ * No target is checked here (the fold does).
+ */
+rlk_status rlk_logp_shard_fwd(const rlk_logp_contract* contract, int32_t shard, const void* logits_shard,
+                              const int64_t* targets, const uint8_t* active_mask, float* partials_shard,
+                              float* target_logit, void* workspace, rlk_stream_t stream);
+
+/*
+ * The merge after the exchange, run by every rank on the same gathered data:
+ *   gathered_partials     [tp, T, num_tiles/tp, 2] FP32: every shard's
+ *                         partials_shard, shard-major (what an all-gather of
+ *                         them along a new leading dimension leaves);
+ *   gathered_target_logit [tp, T] FP32: every shard's target_logit.
+ *   logp, lse             [T] FP32 out, as rlk_logp_fwd's (the target logit
+ *                         is taken from shard t_r / Vs).
+ * Device status as for rlk_logp_fwd (target range, non-finite LSE).
+ */
+rlk_status rlk_logp_fold(const rlk_logp_contract* contract, const float* gathered_partials,
+                         const float* gathered_target_logit, const int64_t* targets, const uint8_t* active_mask,
+                         float* logp, float* lse, void* workspace, rlk_stream_t stream);
+
+/*
+ * Rank side of the backward, given the (replicated) LSE from rlk_logp_fold:
+ *   dlogits_shard [T, row_stride] BF16 out: columns [0, Vs) of every row,
+ *                 g (onehot - exp(x - LSE)) with the one-hot term only in the
+ *                 shard that holds the target; padding and inactive rows 0.
+ * No collective is needed.  Device status: an active target outside
+ * [0, V_real), a non-finite lse_in on an active row.
+ */
+rlk_status rlk_logp_shard_bwd(const rlk_logp_contract* contract, int32_t shard, const void* logits_shard,
+                              const int64_t* targets, const uint8_t* active_mask, const float* lse_in,
+                              const float* grad_logp, void* dlogits_shard, void* workspace, rlk_stream_t stream);
 
 /*
  * rlk_logp_fwd without a workspace argument, for callers that cannot
@@ -250,6 +321,10 @@ rlk_status rlk_logp_fused_lmhead(const rlk_logp_contract* contract, const void* 
  * device memory and calls no allocating routine.  The first call on a device
  * looks up the array's device address with that device current (one
  * cudaGetSymbolAddress); make that first call before any stream capture.
+ * The address is kept per device together with the id of the CUDA context
+ * it was looked up in; if that context is gone (cudaDeviceReset, say), the
+ * next call looks the address up again in the new context, so make the
+ * first call after a reset before any stream capture too.
  * Every call on a device shares the one array and clears the status word
  * first, so calls that overlap on the GPU race on it: serialise them (one
  * stream, or events).  Device-side conditions (RLK_ERR_TARGET_RANGE,

@@ -120,3 +120,27 @@ def test_product_path_has_no_fallback():
     for f in os.listdir(csrc):
         if f.endswith((".cu", ".cuh", ".h", ".cpp")):
             assert "oracle" not in open(os.path.join(csrc, f)).read().lower()
+
+
+@pytest.mark.parametrize("name,value", [("RLK_ROW_BUFS", "3"), ("RLK_ROW_BUFS", "16"), ("RLK_CTAS_PER_SM", "3"),
+                                        ("RLK_FUSED_SKEW", "9"), ("RLK_FUSED_SKEW", "x"),
+                                        ("RLK_FUSED_SCHEDULE", "fast"), ("RLK_TPS", "2"), ("RLK_MAX_SLOTS", "7"),
+                                        ("RLK_LMHEAD_PAIR", "2")])
+def test_off_model_planner_overrides_fail_closed(built, monkeypatch, name, value):
+    """Planner overrides outside the ring shapes the protocol model replays are
+    rejected on the host, before any device is touched."""
+    c = rlk.Contract(T=16, V_real=1000, V_padded=1024, num_tiles=4)
+    assert rlk.rlk_logp_check_contract(c) == rlk.RLK_OK
+    monkeypatch.setenv(name, value)
+    assert rlk.rlk_logp_check_contract(c) == rlk.RLK_ERR_UNSUPPORTED
+    assert name in rlk.rlk_last_error_message()
+    assert rlk.rlk_logp_workspace_size(c) == 0
+
+
+@pytest.mark.parametrize("name,value", [("RLK_ROW_BUFS", "2"), ("RLK_ROW_BUFS", "8"), ("RLK_CTAS_PER_SM", "1"),
+                                        ("RLK_FUSED_SKEW", "0"), ("RLK_FUSED_SKEW", "-1"),
+                                        ("RLK_FUSED_SCHEDULE", "resident"), ("RLK_FUSED_SCHEDULE", "l2")])
+def test_modelled_planner_overrides_are_accepted(built, monkeypatch, name, value):
+    c = rlk.Contract(T=16, V_real=1000, V_padded=1024, num_tiles=4)
+    monkeypatch.setenv(name, value)
+    assert rlk.rlk_logp_check_contract(c) == rlk.RLK_OK

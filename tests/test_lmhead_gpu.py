@@ -151,7 +151,7 @@ def within(got_bits, ref, scale):
     return np.abs(got - ref) <= 2.0 ** -8 * (np.abs(ref) + scale) + 1e-30
 
 
-@pytest.mark.parametrize("case", CASES[1:4], ids=lambda c: "T%d_H%d_V%d_P%d_NT%d" % c)
+@pytest.mark.parametrize("case", CASES[1:5] + [(129, 64, 300, 320, 5)], ids=lambda c: "T%d_H%d_V%d_P%d_NT%d" % c)
 def test_lmhead_backward_small_cases(case):
     T, H, v_real, v_padded, nt = case
     hb, wb = make(T, H, v_real, v_padded, seed=3 * T + H)
@@ -212,25 +212,57 @@ def test_lmhead_backward_full_shape():
     assert (col_sum.abs() <= 2.0 ** -6 * col_abs + 1e-6).all()
 
 
-def test_lmhead_cta_pairs_change_no_bit(monkeypatch):
-    """CTA pairs (token blocks 2i and 2i+1 sharing each weight chunk by
-    multicast) run the same per-tile arithmetic as single CTAs: logp, LSE and
-    both gradients are bitwise equal.  Three token blocks: the last pair's
-    second CTA reads out-of-range rows only."""
+def test_lmhead_repeat_runs_are_bitwise_equal():
+    """Units are handed out by an atomic ticket, so which CTA runs which
+    (token block, tile) unit changes from run to run; every unit's arithmetic
+    is fixed, so logp, LSE and both gradients are bitwise the same on every
+    run.  Three token blocks and a 2384-wide tile (9 x 256 + 80 columns)."""
     T, H, v_real, v_padded, nt = 300, 128, 2380, 2384 * 2, 2
     hb, wb = make(T, H, v_real, v_padded, seed=11)
     tgt = synth.targets(T, v_real, seed=12)
     mask = (np.arange(T) % 3 != 0).astype(np.uint8)
     g = np.where(mask != 0, np.random.default_rng(13).standard_normal(T), 0.0).astype(np.float32)
-    outs = {}
-    for pair in ("1", "2"):
-        monkeypatch.setenv("RLK_LMHEAD_PAIR", pair)
+    outs = set()
+    for _ in range(3):
         c = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=nt, virtual_tp=2, validate=1)
         logp, lse, dh, dw = rlk.logp_fused_lmhead(c, dev(hb), dev(wb), torch.from_numpy(tgt).cuda(),
                                                   torch.from_numpy(mask).cuda(), grad=torch.from_numpy(g).cuda())
         torch.cuda.synchronize()
-        outs[pair] = [t.cpu().numpy().tobytes() for t in (logp, lse, dh, dw)]
-    assert outs["1"] == outs["2"]
+        outs.add(tuple(t.cpu().numpy().tobytes() for t in (logp, lse, dh, dw)))
+    assert len(outs) == 1
     ref_logp, ref_lse, _ = oracle.lmhead_forward(hb, wb, tgt, mask != 0, v_real)
-    logp = np.frombuffer(outs["2"][0], dtype=np.float32)
+    logp = np.frombuffer(next(iter(outs))[0], dtype=np.float32)
     close("logp", logp, ref_logp)
+
+
+def bf16_rn_bits(x):
+    """FP32 values rounded to BF16 (round to nearest even), as uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+@pytest.mark.parametrize("case", [CASES[1], CASES[4], (200, 320, 1000, 1024, 4)],
+                         ids=lambda c: "T%d_H%d_V%d_P%d_NT%d" % c)
+def test_lmhead_fp32_dweight(case):
+    """The FP32 dweight output is the GEMM's FP32 accumulator: within the FP32
+    accumulation bound of the FP64 oracle, and its BF16 rounding is bitwise
+    the BF16 dweight output of the same call.  H = 320 leaves a 64-wide last
+    block of the hidden dimension."""
+    T, H, v_real, v_padded, nt = case
+    hb, wb = make(T, H, v_real, v_padded, seed=7 * T + H)
+    tgt = synth.targets(T, v_real, seed=T + 5)
+    mask = (np.arange(T) % 4 != 2).astype(np.uint8)
+    g = np.where(mask != 0, np.random.default_rng(T + 1).standard_normal(T), 0.0).astype(np.float32)
+    ref_dh, ref_dw, sc_dh, sc_dw = grad_bounds(hb, wb, tgt, mask != 0, g, v_real)
+    c = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=nt, virtual_tp=1, validate=1)
+    _, _, dh, (dwf, dwb) = rlk.logp_fused_lmhead(c, dev(hb), dev(wb), torch.from_numpy(tgt).cuda(),
+                                                 torch.from_numpy(mask).cuda(), grad=torch.from_numpy(g).cuda(),
+                                                 dweight_dtype="both")
+    torch.cuda.synchronize()
+    f = dwf.cpu().numpy().astype(np.float64)
+    # dlogits are BF16 (one rounding, 2^-9 relative) and the sum is FP32
+    assert np.all(np.abs(f[:v_real] - ref_dw) <= 2.0 ** -8 * (np.abs(ref_dw) + sc_dw) + 1e-30)
+    assert np.all(f[v_real:] == 0.0) and not np.any(np.signbit(f[v_real:]))
+    assert np.array_equal(bf16_rn_bits(dwf.cpu().numpy()), dwb.cpu().numpy().view(np.uint16))
+    assert np.all(within(dh.cpu().numpy().view(np.uint16), ref_dh, sc_dh))

@@ -317,6 +317,102 @@ def test_lmhead_grads_match_finite_differences():
     assert np.all(dh[2] == 0.0)
 
 
+def _lmhead_fwd_pins_pass(fwd):
+    """Pins of the lm_head forward's logp and LSE (fwd has the signature of
+    oracle.lmhead_forward); True when every pin holds.
+
+    * Uniform logits: hidden row r = a_r e_0 and every real W row = 1.5 e_0
+      give x_rc = 1.5 a_r for all real c, so LSE_r = 1.5 a_r + ln V_real and
+      logp_r = -ln V_real whatever the target.
+    * One-hot spike: hidden row r = s_r e_1 and W = e_1 on row t* only give
+      x_{r,t*} = s_r and 0 elsewhere, so logp = -log1p((V_real - 1) e^-s_r)
+      for target t*, and -log(V_real - 1 + e^s_r) for any other target.
+    * Padded W rows hold NaN, +inf and random bits and take no part.
+    * Inactive rows give logp = +0.0 exactly; an active target in the padding
+      raises ValueError.
+    """
+    ok = True
+    H, v_real, v_padded = 8, 37, 40
+    rng = np.random.default_rng(43)
+    W = np.zeros((v_padded, H), dtype=np.uint16)
+    W[:v_real, 0] = bf16_bits([1.5])[0]
+    W[v_real:] = garbage_bits(rng, (v_padded - v_real, H))
+    W[v_real, :] = 0x7FC0   # NaN
+    W[v_real + 1, :] = 0x7F80  # +inf
+    a = np.array([0.5, 1.0, 2.0, 3.0])
+    h = np.zeros((4, H), dtype=np.uint16)
+    h[:, 0] = bf16_bits(a)
+    targets = np.array([0, 36, 5, 17])
+    with np.errstate(all="ignore"):
+        logp, lse, _ = fwd(h, W, targets, np.ones(4, dtype=bool), v_real)
+        ok &= bool(np.all(np.abs(logp + LN(v_real)) < 1e-12))
+        ok &= bool(np.all(np.abs(lse - (1.5 * a + LN(v_real))) < 1e-12))
+        # one-hot spike
+        t_star = 11
+        W2 = W.copy()
+        W2[:v_real] = 0
+        W2[t_star, 1] = bf16_bits([1.0])[0]
+        sv = np.array([4.0, 8.0, 15.0, 30.0])
+        h2 = np.zeros((4, H), dtype=np.uint16)
+        h2[:, 1] = bf16_bits(sv)
+        t2 = np.array([t_star, t_star, 3, t_star])
+        logp2, lse2, _ = fwd(h2, W2, t2, np.ones(4, dtype=bool), v_real)
+        want = np.where(t2 == t_star, -np.log1p((v_real - 1) * np.exp(-sv)), -np.log(v_real - 1 + np.exp(sv)))
+        ok &= bool(np.all(np.abs(logp2 - want) < 1e-12 * np.maximum(1.0, np.abs(want))))
+        ok &= bool(np.all(np.abs(lse2 - np.log(v_real - 1 + np.exp(sv))) < 1e-12 * np.maximum(1.0, sv)))
+        # inactive rows: exactly +0.0, their targets never used
+        act = np.array([True, False, True, False])
+        logp3, _, _ = fwd(h, W, np.array([0, -7, 5, 10 ** 6]), act, v_real)
+        ok &= bool(np.all(logp3[~act] == 0.0) and not np.any(np.signbit(logp3[~act])))
+        ok &= bool(np.all(np.abs(logp3[act] + LN(v_real)) < 1e-12))
+        # an active target in the padding is an error
+        try:
+            fwd(h, W, np.array([0, v_real + 1, 5, 17]), np.ones(4, dtype=bool), v_real)
+            ok = False
+        except ValueError:
+            pass
+        except Exception:
+            ok = False
+    return ok
+
+
+def test_lmhead_forward_pins():
+    assert _lmhead_fwd_pins_pass(oracle.lmhead_forward)
+
+
+def test_lmhead_forward_pins_catch_planted_mistakes():
+    from oracle.lmhead import lmhead_logits
+
+    def sign_flipped(hb, wb, targets, active, v_real):
+        logp, lse, x = oracle.lmhead_forward(hb, wb, targets, active, v_real)
+        return -logp, lse, x
+
+    def wrong_row(hb, wb, targets, active, v_real):
+        x = lmhead_logits(hb, wb, v_cols=v_real)
+        lse = oracle.lse_of_values(x)
+        logp = np.zeros(len(lse))
+        rows = np.nonzero(np.asarray(active))[0]
+        t = np.asarray(targets)[rows]
+        if np.any((t < 0) | (t >= v_real)):
+            raise ValueError("active target outside [0, V_real)")
+        logp[rows] = x[np.roll(rows, 1), t] - lse[rows]
+        return logp, lse, x
+
+    def padding_included(hb, wb, targets, active, v_real):
+        return oracle.lmhead_forward(hb, wb, targets, active, np.asarray(wb).shape[0])
+
+    def no_range_check(hb, wb, targets, active, v_real):
+        x = lmhead_logits(hb, wb)
+        lse = oracle.lse_of_values(x[:, :v_real])
+        logp = np.zeros(len(lse))
+        rows = np.nonzero(np.asarray(active))[0]
+        logp[rows] = x[rows, np.asarray(targets)[rows]] - lse[rows]
+        return logp, lse, x
+
+    for bad in (sign_flipped, wrong_row, padding_included, no_range_check):
+        assert not _lmhead_fwd_pins_pass(bad), bad.__name__
+
+
 # ----------------------------------------------------------------------------- pin sensitivity
 
 def _pins_pass(lse_fn, dlogits_fn, fold_fn):

@@ -35,6 +35,11 @@ EXPORTED = (
     "rlk_grpo_loss",
     "rlk_logp_lmhead_workspace_size",
     "rlk_logp_fused_lmhead",
+    "rlk_logp_check_shard_contract",
+    "rlk_logp_shard_workspace_size",
+    "rlk_logp_shard_fwd",
+    "rlk_logp_fold",
+    "rlk_logp_shard_bwd",
     "rlk_logp_workspace_status",
     "rlk_selftest_bounded_wait",
     "rlk_status_string",
@@ -96,7 +101,7 @@ def library():
         lib.rlk_logp_bwd.restype = i
         lib.rlk_logp_lmhead_workspace_size.argtypes = [P, ctypes.c_int64]
         lib.rlk_logp_lmhead_workspace_size.restype = ctypes.c_size_t
-        lib.rlk_logp_fused_lmhead.argtypes = [P, vp, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.rlk_logp_fused_lmhead.argtypes = [P, vp, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.rlk_logp_fused_lmhead.restype = i
         lib.rlk_logp_fwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp]
         lib.rlk_logp_fwd_noalloc.restype = i
@@ -104,6 +109,16 @@ def library():
         lib.rlk_logp_fwd_entropy.restype = i
         lib.rlk_grpo_loss.argtypes = [ctypes.c_int64, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
         lib.rlk_grpo_loss.restype = i
+        lib.rlk_logp_check_shard_contract.argtypes = [P, ctypes.c_int32]
+        lib.rlk_logp_check_shard_contract.restype = i
+        lib.rlk_logp_shard_workspace_size.argtypes = [P]
+        lib.rlk_logp_shard_workspace_size.restype = ctypes.c_size_t
+        lib.rlk_logp_shard_fwd.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp]
+        lib.rlk_logp_shard_fwd.restype = i
+        lib.rlk_logp_fold.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.rlk_logp_fold.restype = i
+        lib.rlk_logp_shard_bwd.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.rlk_logp_shard_bwd.restype = i
         lib.rlk_logp_workspace_status.argtypes = [vp, vp]
         lib.rlk_logp_workspace_status.restype = i
         lib.rlk_selftest_bounded_wait.argtypes = [ctypes.c_int64, vp, vp]
@@ -142,9 +157,10 @@ def rlk_logp_lmhead_workspace_size(contract, H):
 
 
 def rlk_logp_fused_lmhead(contract, hidden, H, weight, targets, active_mask, grad_logp, logp, lse, dhidden,
-                          dweight, workspace, stream):
+                          dweight_f32, dweight_bf16, workspace, stream):
     return library().rlk_logp_fused_lmhead(ctypes.byref(contract), hidden, H, weight, targets, active_mask,
-                                           grad_logp, logp, lse, dhidden, dweight, workspace, stream)
+                                           grad_logp, logp, lse, dhidden, dweight_f32, dweight_bf16, workspace,
+                                           stream)
 
 
 def rlk_logp_fwd_entropy(contract, logits, targets, active_mask, logp, lse, entropy, workspace, stream):
@@ -160,6 +176,32 @@ def rlk_grpo_loss(T, logp, advantage, active_mask, ref_logp, beta, loss, grad_lo
 def rlk_logp_fwd_noalloc(contract, logits, targets, active_mask, logp, lse, partials, stream):
     return library().rlk_logp_fwd_noalloc(ctypes.byref(contract), logits, targets, active_mask, logp, lse,
                                           partials, stream)
+
+
+def rlk_logp_check_shard_contract(contract, shard):
+    return library().rlk_logp_check_shard_contract(ctypes.byref(contract), shard)
+
+
+def rlk_logp_shard_workspace_size(contract):
+    return library().rlk_logp_shard_workspace_size(ctypes.byref(contract))
+
+
+def rlk_logp_shard_fwd(contract, shard, logits_shard, targets, active_mask, partials_shard, target_logit, workspace,
+                       stream):
+    return library().rlk_logp_shard_fwd(ctypes.byref(contract), shard, logits_shard, targets, active_mask,
+                                        partials_shard, target_logit, workspace, stream)
+
+
+def rlk_logp_fold(contract, gathered_partials, gathered_target_logit, targets, active_mask, logp, lse, workspace,
+                  stream):
+    return library().rlk_logp_fold(ctypes.byref(contract), gathered_partials, gathered_target_logit, targets,
+                                   active_mask, logp, lse, workspace, stream)
+
+
+def rlk_logp_shard_bwd(contract, shard, logits_shard, targets, active_mask, lse_in, grad_logp, dlogits_shard,
+                       workspace, stream):
+    return library().rlk_logp_shard_bwd(ctypes.byref(contract), shard, logits_shard, targets, active_mask, lse_in,
+                                        grad_logp, dlogits_shard, workspace, stream)
 
 
 def rlk_logp_workspace_status(workspace, stream):
@@ -332,23 +374,35 @@ def logp_fwd_bwd_host(contract, logits, targets, mask, grad, device, chunk_rows=
     return d_dl, h_logp, h_lse
 
 
-def logp_fused_lmhead(contract, hidden, weight, targets, mask=None, grad=None, stream=None, workspace=None):
+def logp_fused_lmhead(contract, hidden, weight, targets, mask=None, grad=None, stream=None, workspace=None,
+                      dweight_dtype="bf16"):
     """Fused lm_head on BF16 hidden [T, H] and weight [V_padded, H] (GPU tensors).
 
     Forward only: returns (logp, lse).  With ``grad`` (FP32 [T]): returns
-    (logp, lse, dhidden [T, H] BF16, dweight [V_padded, H] BF16).
+    (logp, lse, dhidden [T, H] BF16, dweight [V_padded, H]); ``dweight_dtype``
+    "bf16" (default), "f32", or "both" (then dweight is a (f32, bf16) pair).
     """
     import torch
     dev = hidden.device
     T, H = hidden.shape
     logp = torch.empty(T, dtype=torch.float32, device=dev)
     lse = torch.empty(T, dtype=torch.float32, device=dev)
-    dh = torch.empty_like(hidden) if grad is not None else None
-    dw = torch.empty_like(weight) if grad is not None else None
+    dh = dwf = dwb = None
+    if grad is not None:
+        if dweight_dtype not in ("bf16", "f32", "both"):
+            raise ValueError("dweight_dtype must be bf16, f32 or both")
+        dh = torch.empty_like(hidden)
+        if dweight_dtype in ("f32", "both"):
+            dwf = torch.empty(weight.shape, dtype=torch.float32, device=dev)
+        if dweight_dtype in ("bf16", "both"):
+            dwb = torch.empty_like(weight)
     n = rlk_logp_lmhead_workspace_size(contract, H)
     if n == 0:
         check(rlk_logp_check_contract(contract) or RLK_ERR_UNSUPPORTED)
     ws = workspace if workspace is not None else torch.empty(n, dtype=torch.uint8, device=dev)
     check(rlk_logp_fused_lmhead(contract, _ptr(hidden), H, _ptr(weight), _ptr(targets), _ptr(mask), _ptr(grad),
-                                _ptr(logp), _ptr(lse), _ptr(dh), _ptr(dw), _ptr(ws), _stream(stream)))
-    return (logp, lse) if grad is None else (logp, lse, dh, dw)
+                                _ptr(logp), _ptr(lse), _ptr(dh), _ptr(dwf), _ptr(dwb), _ptr(ws), _stream(stream)))
+    if grad is None:
+        return logp, lse
+    dw = {"bf16": dwb, "f32": dwf, "both": (dwf, dwb)}[dweight_dtype]
+    return logp, lse, dh, dw

@@ -23,7 +23,7 @@ def commands(nvcc="nvcc"):
     argv = [nvcc, "-O3", "-std=c++17", "-shared", "-Xcompiler", "-fPIC,-fvisibility=hidden",
             "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
             "-I", INCLUDE, "-I", CSRC, "--threads", "0"] + src + [
-            "-lcublasLt", "-Xlinker", "-rpath," + os.path.join(CUDA_HOME, "lib64"), "-o", LIB]
+            "-Xlinker", "-rpath," + os.path.join(CUDA_HOME, "lib64"), "-o", LIB]
     if os.environ.get("RLK_PTXAS_VERBOSE"):
         argv.insert(1, "-Xptxas=-v")
     return [(argv, LIB)]

@@ -1,5 +1,6 @@
 // Fused lm_head variant (sm_103a): the selected-token log-probability of
-// logits = hidden @ W^T without materialising the logits.
+// logits = hidden @ W^T without materialising the logits, and its gradients
+// with respect to hidden and W.
 //
 // The optional fused kernel of issue #323 ("[WS2][Logprob] H100 validation
 // and reproduction guide", "Validation Boundary": "the optional PR6 fused
@@ -15,21 +16,33 @@
 // Roles (192 threads, one CTA per SM): warp 0 issues the TMA loads, warp 1
 // allocates tensor memory and issues the MMAs, warps 2-5 run the epilogue
 // (warp w reads TMEM lanes 32*(w%4)..+31, one token row per thread).
-// Virtual TP: the CTAs are split into virtual_tp groups; group j computes
-// only the tiles of vocabulary shard j.  A tile's partial is computed by one
+// Units are handed out by an atomic ticket in tile-major order: the units in
+// flight at any moment are a window of consecutive units, so the token blocks
+// that share a weight tile run together and the tile is read from HBM about
+// once.  The producer's lane takes the ticket and passes the unit to the
+// other roles through a small queue in shared memory.
+// Virtual TP: the CTAs are split into virtual_tp groups; group j takes
+// tickets only for the tiles of shard j.  A tile's partial is computed by one
 // thread in one fixed order (chunks, then 32-column blocks, then columns),
-// whatever the grouping, so outputs do not depend on virtual_tp.
+// whatever the grouping or the CTA that runs it, so outputs do not depend on
+// virtual_tp.
+//
+// Backward: the same GEMM re-runs with an epilogue that writes
+// dlogits = g (onehot - exp(x - LSE)) in BF16, then one persistent launch
+// runs the two gradient contractions as tcgen05 GEMMs with FP32 accumulators:
+//   dHidden[T, H]  = dlogits[:, :V_real] W[:V_real]      (A K-major, B MN-major)
+//   dW[V_padded, H] = dlogits[:, :V_real]^T hidden       (A and B MN-major)
+// Each output tile accumulates its whole K range in one fixed order on one
+// CTA: no split-K, no atomics on data.
 //
 // Every wait is bounded; on expiry the CTA records RLK_ERR_TIMEOUT, stops
 // issuing, waits (bounded) for its issued copies and MMAs, frees its tensor
 // memory and returns.
-#include <cublasLt.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 
-#include <cstdlib>
 #include <mutex>
 #include <string>
 
@@ -40,22 +53,112 @@
 namespace rlk {
 namespace {
 
-int env_int_lm(const char* name, int dflt) {
-    const char* v = std::getenv(name);
-    return (v && *v) ? std::atoi(v) : dflt;
-}
-
 constexpr int kBM = 128;  // token rows per unit (TMEM lanes)
 constexpr int kBN = 256;  // vocabulary rows per chunk (accumulator columns)
 constexpr int kBK = 64;   // K per stage: 64 BF16 = one 128-byte swizzle row
 constexpr int kStages = 4;
+constexpr int kUq = 4;  // depth of the unit queue from the producer to the other roles
 constexpr int kThreadsLm = 192;
 constexpr uint32_t kTmemCols = 512;  // two accumulators of kBN columns
 constexpr uint32_t kStageA = kBM * kBK * 2;
 constexpr uint32_t kStageB = kBN * kBK * 2;
+constexpr uint32_t kMnBlock = 64 * kBK * 2;  // one 64-wide block of an MN-major stage: 64 K rows x 128 B
 constexpr uint64_t kDrainNsLm = 1000000000ull;
+constexpr int kMaxGroups = 8;
+// Workspace: 256 bytes of tickets (three launches x kMaxGroups 64-bit counters).
+constexpr size_t kTicketBytes = 256;
 
 enum : int { kEpiPartials = 0, kEpiGrad = 1 };
+
+struct Bars {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t ufull[kUq];   // unit queue entry written (the producer's arrival)
+    uint64_t uempty[kUq];  // entry read by the MMA thread and the four epilogue warps
+    uint64_t drain;
+    int64_t unit[kUq];
+    uint32_t tmem_addr;
+    int abort_flag;
+};
+
+struct WaitCtl {
+    uint32_t* status;
+    uint64_t wait_ns;
+};
+
+__device__ bool lm_wait(Bars* bars, uint32_t bar, uint32_t parity, const WaitCtl& w) {
+    if (mbar_try_wait(bar, parity)) return true;
+    volatile int* ab = &bars->abort_flag;
+    if (*ab) return false;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*ab) return false;
+        if (globaltimer_ns() - t0 > w.wait_ns) {
+            *ab = 1;
+            atomicOr(w.status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ void lm_drain_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kDrainNsLm) {
+            atomicOr(w.status, kStatusTimeout);
+            return;
+        }
+    }
+}
+
+// The producer publishes the CTA's n-th unit (-1: no more units).
+__device__ bool unit_put(Bars* bars, int64_t n, int64_t u, const WaitCtl& w) {
+    const int s = (int)(n % kUq);
+    const uint32_t par = (uint32_t)((n / kUq) & 1);
+    if (!lm_wait(bars, smem_u32(&bars->uempty[s]), par ^ 1u, w)) return false;
+    *reinterpret_cast<volatile int64_t*>(&bars->unit[s]) = u;
+    mbar_arrive(smem_u32(&bars->ufull[s]));  // release: the entry is visible to whoever acquires the phase
+    return true;
+}
+
+__device__ bool unit_get(Bars* bars, int64_t n, int64_t& u, const WaitCtl& w) {
+    const int s = (int)(n % kUq);
+    if (!lm_wait(bars, smem_u32(&bars->ufull[s]), (uint32_t)((n / kUq) & 1), w)) return false;
+    u = *reinterpret_cast<volatile int64_t*>(&bars->unit[s]);
+    return true;
+}
+
+__device__ __forceinline__ void unit_done(Bars* bars, int64_t n) { mbar_arrive(smem_u32(&bars->uempty[n % kUq])); }
+
+__device__ void init_bars(Bars* bars) {
+    for (int s = 0; s < kStages; ++s) {
+        mbar_init(smem_u32(&bars->full[s]), 1);
+        mbar_init(smem_u32(&bars->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+        mbar_init(smem_u32(&bars->tfull[b]), 1);
+        mbar_init(smem_u32(&bars->tempty[b]), 4);
+    }
+    for (int s = 0; s < kUq; ++s) {
+        mbar_init(smem_u32(&bars->ufull[s]), 1);
+        mbar_init(smem_u32(&bars->uempty[s]), 5);
+    }
+    mbar_init(smem_u32(&bars->drain), 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+}
+
+// The producer's final step: every copy it issued lands before the CTA may exit.
+__device__ void drain_copies(Bars* bars, int64_t issued, const WaitCtl& w) {
+    const int64_t first = issued > kStages ? issued - kStages : 0;
+    for (int64_t j = first; j < issued; ++j)
+        lm_drain_wait(smem_u32(&bars->full[j % kStages]), (uint32_t)((j / kStages) & 1), w);
+}
+
+// ----------------------------------------------------------------- logits GEMM (forward partials / dlogits)
 
 struct LmParams {
     const int64_t* targets;
@@ -65,81 +168,29 @@ struct LmParams {
     const float* lse_in;  // [T]                      (kEpiGrad)
     const float* grad;    // [T] upstream g of logp   (kEpiGrad)
     uint16_t* dlogits;    // [T, Vp] BF16 out         (kEpiGrad)
-    uint32_t* status;
+    unsigned long long* tickets;  // one per virtual-TP group, 0 at launch
+    WaitCtl w;
     int64_t T, Vr, Vp, ignore_index;
-    uint64_t wait_ns;
     int32_t K, NT, W, vtp, nchunk, rem, mask_mode;
-    int32_t MB;    // token blocks
-    int32_t pair;  // CTAs per cluster: 2 = two token blocks share each weight chunk (multicast), else 1
+    int32_t MB;  // token blocks
 };
 
-struct Bars {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
-    uint64_t drain;
-    uint32_t tmem_addr;
-    int abort_flag;
+// Virtual-TP group of this CTA: group j takes tickets for units
+// [0, NT/vtp * MB) of shard j, tile-major (unit u = tile j*NT/vtp + u / MB,
+// token block u % MB).
+struct Group {
+    int j, tile0;
+    int64_t end;
 };
 
-// Units of this CTA: the tiles of its virtual-TP shard times the token
-// blocks, tile-major, strided over the clusters of its group.  With pairs
-// (p.pair = 2) a unit is a tile times a pair of token blocks: rank r of the
-// cluster takes block 2i + r (which may lie past the last block; its rows
-// are then out of range and masked).  The group of a cluster is a
-// contiguous run of clusters, so both ranks see the same units.
-struct UnitSeq {
-    int64_t u, step, end;
-    int tile0, ntile_sh, MBU, rank, pair;
-    __device__ void init(const LmParams& p) {
-        pair = p.pair;
-        const int cl = blockIdx.x / pair;
-        rank = blockIdx.x % pair;
-        const int G = gridDim.x / pair;
-        const int Gj = G / p.vtp;
-        const int j = cl / Gj;
-        const int c = cl % Gj;
-        ntile_sh = p.NT / p.vtp;
-        tile0 = j * ntile_sh;
-        MBU = (p.MB + pair - 1) / pair;
-        u = c;
-        step = Gj;
-        end = (int64_t)ntile_sh * MBU;
-    }
-    __device__ bool next(int& tile, int& mb) {
-        if (u >= end) return false;
-        tile = tile0 + (int)(u / MBU);
-        mb = (int)(u % MBU) * pair + rank;
-        u += step;
-        return true;
-    }
-};
-
-__device__ bool lm_wait(Bars* bars, uint32_t bar, uint32_t parity, const LmParams& p) {
-    if (mbar_try_wait(bar, parity)) return true;
-    volatile int* ab = &bars->abort_flag;
-    if (*ab) return false;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*ab) return false;
-        if (globaltimer_ns() - t0 > p.wait_ns) {
-            *ab = 1;
-            atomicOr(p.status, kStatusTimeout);
-            return false;
-        }
-    }
-}
-
-__device__ void lm_drain_wait(uint32_t bar, uint32_t parity, const LmParams& p) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kDrainNsLm) {
-            atomicOr(p.status, kStatusTimeout);
-            return;
-        }
-    }
+__device__ Group group_of(const LmParams& p) {
+    const int Gj = (int)gridDim.x / p.vtp;
+    Group g;
+    g.j = (int)blockIdx.x / Gj;
+    const int ntl = p.NT / p.vtp;
+    g.tile0 = g.j * ntl;
+    g.end = (int64_t)ntl * p.MB;
+    return g;
 }
 
 // One 32-column block of a row's logits into the running partial of its
@@ -197,74 +248,54 @@ __device__ __forceinline__ void grad_block(const float (&v)[32], int nv, int64_t
 template <int EPI>
 __global__ void __launch_bounds__(kThreadsLm, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
-                      const __grid_constant__ CUtensorMap tmWr, const __grid_constant__ LmParams p) {
-    // With pairs, tmW and tmWr describe half a chunk (128 rows, rem/2 rows):
-    // each rank loads its half and multicasts it to both CTAs.
+                  const __grid_constant__ CUtensorMap tmWr, const __grid_constant__ LmParams p) {
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzled operand tiles.
-    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* smem =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* sA = smem;
     unsigned char* sB = smem + kStages * kStageA;
     Bars* bars = reinterpret_cast<Bars*>(smem + kStages * (kStageA + kStageB));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = p.K / kBK;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&bars->full[s]), 1);
-            // with pairs a stage is free once both CTAs' MMAs have read it
-            mbar_init(smem_u32(&bars->empty[s]), (uint32_t)p.pair);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&bars->tfull[b]), 1);
-            mbar_init(smem_u32(&bars->tempty[b]), 4);
-        }
-        mbar_init(smem_u32(&bars->drain), 1);
-        bars->abort_flag = 0;
-        fence_mbar_init();
-    }
+    if (threadIdx.x == 0) init_bars(bars);
     if (warp == 1) {
         tmem_alloc(smem_u32(&bars->tmem_addr), kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
-    // the peer's barriers must be initialised before any multicast or commit reaches them
-    if (p.pair > 1) cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_addr;
+    const Group grp = group_of(p);
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            UnitSeq us;
-            us.init(p);
-            int tile, mb, stage = 0;
+            int stage = 0;
             uint32_t phase = 0;
-            int64_t issued = 0;
+            int64_t issued = 0, n = 0;
             bool aborted = false;
-            while (!aborted && us.next(tile, mb)) {
+            while (!aborted) {
+                int64_t u = (int64_t)atomicAdd(&p.tickets[grp.j], 1ull);
+                if (u >= grp.end) u = -1;
+                if (!unit_put(bars, n++, u, p.w) || u < 0) break;
+                const int tile = grp.tile0 + (int)(u / p.MB);
+                const int mb = (int)(u % p.MB);
                 for (int ch = 0; ch < p.nchunk && !aborted; ++ch) {
                     const bool last_rem = (ch == p.nchunk - 1) && p.rem;
                     const int nrows = last_rem ? p.rem : kBN;
                     const int n0 = tile * p.W + ch * kBN;
                     for (int kb = 0; kb < KB; ++kb) {
-                        const uint32_t eb = smem_u32(&bars->empty[stage]);
-                        if (!lm_wait(bars, eb, phase ^ 1u, p)) {
+                        if (!lm_wait(bars, smem_u32(&bars->empty[stage]), phase ^ 1u, p.w)) {
                             aborted = true;
                             break;
                         }
                         const uint32_t fb = smem_u32(&bars->full[stage]);
                         mbar_arrive_expect_tx(fb, kStageA + (uint32_t)nrows * kBK * 2);
                         tma_load_2d(smem_u32(sA + stage * kStageA), &tmH, kb * kBK, mb * kBM, fb);
-                        if (p.pair == 1) {
-                            tma_load_2d(smem_u32(sB + stage * kStageB), last_rem ? &tmWr : &tmW, kb * kBK, n0, fb);
-                        } else {
-                            // rows [rank*half, (rank+1)*half) of the chunk, to both CTAs
-                            const int half = nrows / 2;
-                            tma_load_2d_mc(smem_u32(sB + stage * kStageB + us.rank * half * (kBK * 2)),
-                                           last_rem ? &tmWr : &tmW, kb * kBK, n0 + us.rank * half, fb, 0x3);
-                        }
+                        tma_load_2d(smem_u32(sB + stage * kStageB), last_rem ? &tmWr : &tmW, kb * kBK, n0, fb);
                         ++issued;
                         if (++stage == kStages) {
                             stage = 0;
@@ -273,25 +304,24 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                     }
                 }
             }
-            // Drain: every issued copy lands before this CTA may exit.
-            const int64_t first = issued > kStages ? issued - kStages : 0;
-            for (int64_t j = first; j < issued; ++j)
-                lm_drain_wait(smem_u32(&bars->full[j % kStages]), (uint32_t)((j / kStages) & 1), p);
+            drain_copies(bars, issued, p.w);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            UnitSeq us;
-            us.init(p);
-            int tile, mb, stage = 0;
+            int stage = 0;
             uint32_t phase = 0;
-            int64_t chunk = 0;
+            int64_t chunk = 0, n = 0;
             bool aborted = false;
-            while (!aborted && us.next(tile, mb)) {
+            while (!aborted) {
+                int64_t u;
+                if (!unit_get(bars, n, u, p.w)) break;
+                unit_done(bars, n++);
+                if (u < 0) break;
                 for (int ch = 0; ch < p.nchunk && !aborted; ++ch, ++chunk) {
                     const int acc = (int)(chunk & 1);
                     const uint32_t accph = (uint32_t)((chunk >> 1) & 1);
-                    if (!lm_wait(bars, smem_u32(&bars->tempty[acc]), accph ^ 1u, p)) {
+                    if (!lm_wait(bars, smem_u32(&bars->tempty[acc]), accph ^ 1u, p.w)) {
                         aborted = true;
                         break;
                     }
@@ -300,7 +330,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                     const uint32_t idesc = idesc_bf16_f32(kBM, last_rem ? (uint32_t)p.rem : (uint32_t)kBN);
                     const uint32_t d = tmem + (uint32_t)(acc * kBN);
                     for (int kb = 0; kb < KB; ++kb) {
-                        if (!lm_wait(bars, smem_u32(&bars->full[stage]), phase, p)) {
+                        if (!lm_wait(bars, smem_u32(&bars->full[stage]), phase, p.w)) {
                             aborted = true;
                             break;
                         }
@@ -311,11 +341,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                         for (int kk = 0; kk < kBK / 16; ++kk)
                             umma_bf16(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
                                       (kb | kk) != 0);
-                        // frees the stage (in both CTAs of a pair) when these MMAs finish
-                        if (p.pair == 1)
-                            umma_commit(smem_u32(&bars->empty[stage]));
-                        else
-                            umma_commit_mc(smem_u32(&bars->empty[stage]), 0x3);
+                        umma_commit(smem_u32(&bars->empty[stage]));  // frees the stage when these MMAs finish
                         if (++stage == kStages) {
                             stage = 0;
                             phase ^= 1u;
@@ -326,19 +352,25 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             }
             // Every issued MMA completes before tensor memory is freed.
             umma_commit(smem_u32(&bars->drain));
-            lm_drain_wait(smem_u32(&bars->drain), 0u, p);
+            lm_drain_wait(smem_u32(&bars->drain), 0u, p.w);
         }
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
         const int quarter = warp & 3;
         const int r_in = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        UnitSeq us;
-        us.init(p);
-        int tile, mb;
-        int64_t chunk = 0;
+        int64_t chunk = 0, n = 0;
         bool aborted = false;
-        while (!aborted && us.next(tile, mb)) {
+        while (!aborted) {
+            int64_t u = -1;
+            const bool got = unit_get(bars, n, u, p.w);
+            if (!__all_sync(0xFFFFFFFFu, got)) break;
+            __syncwarp();
+            if (lane == 0) unit_done(bars, n);
+            ++n;
+            if (u < 0) break;
+            const int tile = grp.tile0 + (int)(u / p.MB);
+            const int mb = (int)(u % p.MB);
             const int64_t row = (int64_t)mb * kBM + r_in;
             const bool valid = row < p.T;
             int64_t target = -1;
@@ -359,7 +391,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             for (int ch = 0; ch < p.nchunk; ++ch, ++chunk) {
                 const int acc = (int)(chunk & 1);
                 const uint32_t accph = (uint32_t)((chunk >> 1) & 1);
-                const bool ok = lm_wait(bars, smem_u32(&bars->tfull[acc]), accph, p);
+                const bool ok = lm_wait(bars, smem_u32(&bars->tfull[acc]), accph, p.w);
                 if (!__all_sync(0xFFFFFFFFu, ok)) {
                     aborted = true;
                     break;
@@ -401,8 +433,6 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    // no CTA of a pair leaves while the other may still multicast or commit into it
-    if (p.pair > 1) cluster_sync_all();
 }
 
 // LSE and logp of each row from its tile partials (one warp per row).
@@ -433,6 +463,215 @@ __global__ void lmhead_fold_kernel(const float2* partials, const float* xt, cons
     }
 }
 
+// ----------------------------------------------------------------- gradient GEMMs (dHidden and dW)
+
+// Two problems share one persistent launch and one ticket: tiles [0, n0) of
+// problem 0 (dHidden, M = T, K = V_real) come first, then tiles [n0, n0 + n1)
+// of problem 1 (dW, M = V_padded, K = T); both have N = H in blocks of 256
+// (the last one possibly narrower, in 64-wide steps) and a 128-row M block.
+// The long dHidden tiles go first so that the short dW tiles fill the tail.
+struct GradParams {
+    uint16_t* dhidden;  // [T, H] BF16
+    uint16_t* dw_bf16;  // [V_padded, H] BF16, or NULL
+    float* dw_f32;      // [V_padded, H] FP32, or NULL
+    unsigned long long* ticket;
+    WaitCtl w;
+    int64_t T, Vr, Vp, n0, n1;
+    int32_t H, NB, KB0, KB1;  // n-blocks of H; K blocks of problem 0 (V_real) and problem 1 (T)
+};
+
+struct GradTile {
+    int prob;  // 0: dHidden, 1: dW
+    int64_t mb;
+    int nb, nbox, KB;
+};
+
+__device__ __forceinline__ GradTile grad_tile(const GradParams& p, int64_t u) {
+    GradTile t;
+    t.prob = u < p.n0 ? 0 : 1;
+    const int64_t v = t.prob ? u - p.n0 : u;
+    t.mb = v / p.NB;
+    t.nb = (int)(v % p.NB);
+    const int left = p.H - t.nb * kBN;
+    t.nbox = left >= kBN ? 4 : left / 64;
+    t.KB = t.prob ? p.KB1 : p.KB0;
+    return t;
+}
+
+__global__ void __launch_bounds__(kThreadsLm, 1)
+    lmhead_grad_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+                       const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                       const __grid_constant__ GradParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* sA = smem;
+    unsigned char* sB = smem + kStages * kStageA;
+    Bars* bars = reinterpret_cast<Bars*>(smem + kStages * (kStageA + kStageB));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t total = p.n0 + p.n1;
+
+    if (threadIdx.x == 0) init_bars(bars);
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&bars->tmem_addr), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_addr;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0, n = 0;
+            bool aborted = false;
+            while (!aborted) {
+                int64_t u = (int64_t)atomicAdd(p.ticket, 1ull);
+                if (u >= total) u = -1;
+                if (!unit_put(bars, n++, u, p.w) || u < 0) break;
+                const GradTile t = grad_tile(p, u);
+                const int m0 = (int)(t.mb * kBM);
+                const int h0 = t.nb * kBN;
+                for (int kb = 0; kb < t.KB; ++kb) {
+                    if (!lm_wait(bars, smem_u32(&bars->empty[stage]), phase ^ 1u, p.w)) {
+                        aborted = true;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&bars->full[stage]);
+                    const uint32_t a = smem_u32(sA + stage * kStageA);
+                    const uint32_t b = smem_u32(sB + stage * kStageB);
+                    mbar_arrive_expect_tx(fb, kStageA + (uint32_t)t.nbox * kMnBlock);
+                    if (t.prob == 0) {
+                        // dlogits rows m0.., columns (K) kb*64..; W rows (K) kb*64.., columns h
+                        tma_load_2d(a, &tmA0, kb * kBK, m0, fb);
+                        for (int j = 0; j < t.nbox; ++j) tma_load_2d(b + j * kMnBlock, &tmB0, h0 + 64 * j, kb * kBK, fb);
+                    } else {
+                        // dlogits columns (M) m0.., rows (K) kb*64..; hidden rows (K) kb*64.., columns h
+                        tma_load_2d(a, &tmA1, m0, kb * kBK, fb);
+                        tma_load_2d(a + kMnBlock, &tmA1, m0 + 64, kb * kBK, fb);
+                        for (int j = 0; j < t.nbox; ++j) tma_load_2d(b + j * kMnBlock, &tmB1, h0 + 64 * j, kb * kBK, fb);
+                    }
+                    ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            drain_copies(bars, issued, p.w);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t tiles = 0, n = 0;
+            bool aborted = false;
+            while (!aborted) {
+                int64_t u;
+                if (!unit_get(bars, n, u, p.w)) break;
+                unit_done(bars, n++);
+                if (u < 0) break;
+                const GradTile t = grad_tile(p, u);
+                const int acc = (int)(tiles & 1);
+                const uint32_t accph = (uint32_t)((tiles >> 1) & 1);
+                ++tiles;
+                if (!lm_wait(bars, smem_u32(&bars->tempty[acc]), accph ^ 1u, p.w)) break;
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16_f32_major(kBM, (uint32_t)(64 * t.nbox), t.prob == 1, true);
+                const uint32_t d = tmem + (uint32_t)(acc * kBN);
+                for (int kb = 0; kb < t.KB; ++kb) {
+                    if (!lm_wait(bars, smem_u32(&bars->full[stage]), phase, p.w)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + stage * kStageA);
+                    const uint32_t b0 = smem_u32(sB + stage * kStageB);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        // K-major A advances 16 elements (32 B) within its swizzle rows; an
+                        // MN-major operand advances two 8-row K groups (2 x 1024 B).
+                        const uint64_t ad = t.prob == 0 ? smem_desc_sw128(a0 + kk * 32)
+                                                        : smem_desc_sw128_mn(a0 + kk * 2048, kMnBlock, 1024);
+                        const uint64_t bd = smem_desc_sw128_mn(b0 + kk * 2048, kMnBlock, 1024);
+                        umma_bf16(d, ad, bd, idesc, (kb | kk) != 0);
+                    }
+                    umma_commit(smem_u32(&bars->empty[stage]));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!aborted) umma_commit(smem_u32(&bars->tfull[acc]));
+            }
+            umma_commit(smem_u32(&bars->drain));
+            lm_drain_wait(smem_u32(&bars->drain), 0u, p.w);
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5): TMEM -> BF16 / FP32 rows
+        const int quarter = warp & 3;
+        const int r_in = quarter * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        int64_t tiles = 0, n = 0;
+        for (;;) {
+            int64_t u = -1;
+            const bool got = unit_get(bars, n, u, p.w);
+            if (!__all_sync(0xFFFFFFFFu, got)) break;
+            __syncwarp();
+            if (lane == 0) unit_done(bars, n);
+            ++n;
+            if (u < 0) break;
+            const GradTile t = grad_tile(p, u);
+            const int acc = (int)(tiles & 1);
+            const uint32_t accph = (uint32_t)((tiles >> 1) & 1);
+            ++tiles;
+            const bool ok = lm_wait(bars, smem_u32(&bars->tfull[acc]), accph, p.w);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after();
+            const int64_t row = t.mb * kBM + r_in;
+            const bool valid = row < (t.prob == 0 ? p.T : p.Vp);
+            const bool pad_row = t.prob == 1 && row >= p.Vr;  // dW rows of padding: exactly 0
+            for (int sub = 0; sub < 2 * t.nbox; ++sub) {
+                float v[32];
+                tmem_ld32(tmem + lane_base + (uint32_t)(acc * kBN + sub * 32), v);
+                if (!valid) continue;
+                if (pad_row) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                }
+                const int64_t col0 = (int64_t)t.nb * kBN + sub * 32;
+                uint16_t* ob = t.prob == 0 ? p.dhidden : p.dw_bf16;
+                if (ob) {
+                    uint4* o = reinterpret_cast<uint4*>(ob + row * p.H + col0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        o[q] = make_uint4(pack_bf16x2_rn(v[8 * q], v[8 * q + 1]), pack_bf16x2_rn(v[8 * q + 2], v[8 * q + 3]),
+                                          pack_bf16x2_rn(v[8 * q + 4], v[8 * q + 5]),
+                                          pack_bf16x2_rn(v[8 * q + 6], v[8 * q + 7]));
+                }
+                if (t.prob == 1 && p.dw_f32) {
+                    float4* o = reinterpret_cast<float4*>(p.dw_f32 + row * p.H + col0);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->tempty[acc]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
 // ----------------------------------------------------------------- host
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -454,23 +693,36 @@ EncodeTiled encode_fn() {
     return fn;
 }
 
-// K-major [rows, K] BF16 matrix, box {64, box_rows}, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, uint32_t box_rows) {
+// A BF16 matrix of `rows` rows of `inner` contiguous elements, `stride`
+// elements apart, read in boxes of {box_inner, box_rows} with the 128-byte
+// swizzle; elements outside [0, inner) x [0, rows) read as zero.
+bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows, int64_t stride, uint32_t box_inner,
+              uint32_t box_rows) {
     EncodeTiled enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
+    const cuuint32_t box[2] = {box_inner, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+constexpr size_t kGemmSmem = 1024 + (size_t)kStages * (kStageA + kStageB) + sizeof(Bars);
+
 }  // namespace
 
+// Workspace beyond the status word: tickets, FP32 partials [T, NT, 2], target
+// logits [T]; the backward adds BF16 dlogits [T, V_padded].
 size_t lmhead_fwd_workspace(const rlk_logp_contract& c) {
-    return ((size_t)c.T * c.num_tiles * 8 + 255) / 256 * 256 + ((size_t)c.T * 4 + 255) / 256 * 256;
+    return kTicketBytes + round256((size_t)c.T * c.num_tiles * 8) + round256((size_t)c.T * 4);
+}
+
+size_t lmhead_bwd_workspace(const rlk_logp_contract& c) {
+    return lmhead_fwd_workspace(c) + round256((size_t)c.T * c.V_padded * 2);
 }
 
 rlk_status lmhead_check(const rlk_logp_contract& c, int64_t H) {
@@ -490,26 +742,30 @@ struct LmLaunch {
     int grid, sms;
 };
 
-// Pairs of CTAs share each weight chunk when every virtual-TP group gets a
-// whole number of pairs on the SMs (all but virtual TP 8 on 152 SMs); the
-// number of pairs per group stays within the group's units.
+rlk_status sm_count(int* sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || *sms <= 0)
+        return fail(RLK_ERR_CUDA, "cannot query the device's SM count");
+    return RLK_OK;
+}
 
 rlk_status prepare(LmLaunch& L, const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
-                   const int64_t* targets, const uint8_t* mask, uint32_t* status) {
-    int dev = 0;
-    cudaGetDevice(&dev);
+                   const int64_t* targets, const uint8_t* mask, uint32_t* status, unsigned long long* tickets) {
     int sms = 0;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    rlk_status st = sm_count(&sms);
+    if (st != RLK_OK) return st;
     LmParams& p = L.p;
     p = LmParams{};
     p.targets = targets;
     p.mask = mask;
-    p.status = status;
+    p.tickets = tickets;
+    p.w.status = status;
+    p.w.wait_ns = c.wait_timeout_ns > 0 ? (uint64_t)c.wait_timeout_ns : kDefaultWaitNs;
     p.T = c.T;
     p.Vr = c.V_real;
     p.Vp = c.V_padded;
     p.ignore_index = c.ignore_index;
-    p.wait_ns = c.wait_timeout_ns > 0 ? (uint64_t)c.wait_timeout_ns : kDefaultWaitNs;
     p.K = (int32_t)H;
     p.NT = c.num_tiles;
     p.W = (int32_t)(c.V_padded / c.num_tiles);
@@ -518,47 +774,32 @@ rlk_status prepare(LmLaunch& L, const rlk_logp_contract& c, const void* hidden, 
     p.rem = p.W % kBN;
     p.mask_mode = c.mask_mode;
     p.MB = (int32_t)((c.T + kBM - 1) / kBM);
-    const int forced = env_int_lm("RLK_LMHEAD_PAIR", 0);
-    p.pair = ((sms / 2) % c.virtual_tp == 0 && p.MB >= 2) ? 2 : 1;
-    if (forced == 1 || forced == 2) p.pair = forced;
-    const uint32_t brows = p.pair == 2 ? kBN / 2 : kBN;
-    const uint32_t rrows = p.rem ? (uint32_t)p.rem / (uint32_t)p.pair : brows;
-    if (!make_map(&L.tmH, hidden, c.T, H, kBM) || !make_map(&L.tmW, weight, c.V_padded, H, brows) ||
-        !make_map(&L.tmWr, weight, c.V_padded, H, rrows))
+    const uint32_t rrows = p.rem ? (uint32_t)p.rem : (uint32_t)kBN;
+    if (!make_map(&L.tmH, hidden, H, c.T, H, kBK, kBM) || !make_map(&L.tmW, weight, H, c.V_padded, H, kBK, kBN) ||
+        !make_map(&L.tmWr, weight, H, c.V_padded, H, kBK, rrows))
         return fail(RLK_ERR_CUDA, "cuTensorMapEncodeTiled failed for the hidden or weight tensor");
-    const int64_t units_per_shard = (int64_t)(c.num_tiles / c.virtual_tp) * ((p.MB + p.pair - 1) / p.pair);
-    int64_t per_group = sms / p.pair / c.virtual_tp;  // clusters per virtual-TP group
+    const int64_t units_per_shard = (int64_t)(c.num_tiles / c.virtual_tp) * p.MB;
+    int64_t per_group = sms / c.virtual_tp;  // CTAs per virtual-TP group
     if (per_group > units_per_shard) per_group = units_per_shard;
     if (per_group < 1) per_group = 1;
-    L.grid = (int)(per_group * c.virtual_tp * p.pair);
+    L.grid = (int)(per_group * c.virtual_tp);
     L.sms = sms;
     return RLK_OK;
 }
 
-template <int EPI>
-rlk_status run_gemm(const LmLaunch& L, cudaStream_t stream) {
-    const size_t smem = 1024 + (size_t)kStages * (kStageA + kStageB) + sizeof(Bars);
-    cudaError_t e = cudaFuncSetAttribute(lmhead_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+template <class K, class... Args>
+rlk_status launch_gemm(K kernel, int grid, cudaStream_t stream, const char* what, Args... args) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-    cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3((unsigned)L.grid, 1, 1);
-    cfg.blockDim = dim3(kThreadsLm, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cfg.numAttrs = 0;
-    if (L.p.pair > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)L.p.pair;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        // The two CTAs of a pair wait on each other; the hardware schedules a
-        // cluster's CTAs together, and pairs never wait on other pairs.
-    }
-    e = cudaLaunchKernelEx(&cfg, lmhead_kernel<EPI>, L.tmH, L.tmW, L.tmWr, L.p);
-    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("lm_head GEMM launch: ") + cudaGetErrorString(e));
+    kernel<<<(unsigned)grid, kThreadsLm, kGemmSmem, stream>>>(args...);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string(what) + " launch: " + cudaGetErrorString(e));
+    return RLK_OK;
+}
+
+rlk_status clear_tickets(void* tickets, cudaStream_t stream) {
+    const cudaError_t e = cudaMemsetAsync(tickets, 0, kTicketBytes, stream);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("clearing the tickets: ") + cudaGetErrorString(e));
     return RLK_OK;
 }
 
@@ -567,25 +808,25 @@ rlk_status run_gemm(const LmLaunch& L, cudaStream_t stream) {
 rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
                              const int64_t* targets, const uint8_t* mask, float* logp, float* lse, void* workspace,
                              uint32_t* status, cudaStream_t stream) {
-    LmLaunch L;
-    rlk_status st = prepare(L, c, hidden, H, weight, targets, mask, status);
-    if (st != RLK_OK) return st;
-    LmParams& p = L.p;
     unsigned char* ws = static_cast<unsigned char*>(workspace);
-    p.partials = reinterpret_cast<float2*>(ws);
-    p.xt = reinterpret_cast<float*>(ws + ((size_t)c.T * c.num_tiles * 8 + 255) / 256 * 256);
-    if ((st = run_gemm<kEpiPartials>(L, stream)) != RLK_OK) return st;
-    const int sms = L.sms;
-    cudaError_t e;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    (void)dev;
+    unsigned long long* tickets = reinterpret_cast<unsigned long long*>(ws);
+    rlk_status st = clear_tickets(tickets, stream);
+    if (st != RLK_OK) return st;
+    LmLaunch L;
+    if ((st = prepare(L, c, hidden, H, weight, targets, mask, status, tickets)) != RLK_OK) return st;
+    LmParams& p = L.p;
+    p.partials = reinterpret_cast<float2*>(ws + kTicketBytes);
+    p.xt = reinterpret_cast<float*>(ws + kTicketBytes + round256((size_t)c.T * c.num_tiles * 8));
+    if ((st = launch_gemm(lmhead_kernel<kEpiPartials>, L.grid, stream, "lm_head GEMM", L.tmH, L.tmW, L.tmWr, p)) !=
+        RLK_OK)
+        return st;
     const int fold_threads = 256;
     const size_t fold_smem = (size_t)(fold_threads / 32) * c.num_tiles * sizeof(float2);
-    e = cudaFuncSetAttribute(lmhead_fold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fold_smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(lmhead_fold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fold_smem);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
     int64_t fold_grid = (c.T + 7) / 8;
-    if (fold_grid > (int64_t)sms * 8) fold_grid = (int64_t)sms * 8;
+    if (fold_grid > (int64_t)L.sms * 8) fold_grid = (int64_t)L.sms * 8;
     lmhead_fold_kernel<<<(unsigned)fold_grid, fold_threads, fold_smem, stream>>>(
         p.partials, p.xt, targets, mask, c.mask_mode, c.ignore_index, c.T, c.V_real, c.num_tiles, logp, lse, status);
     e = cudaGetLastError();
@@ -593,110 +834,53 @@ rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int
     return RLK_OK;
 }
 
-// ----------------------------------------------------------------- backward
-
-namespace {
-
-constexpr size_t kLtWorkspace = (size_t)32 << 20;
-
-cublasLtHandle_t lt_handle(int dev) {
-    static std::mutex mu;
-    static cublasLtHandle_t handles[64] = {};
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev < 0 || dev >= 64) return nullptr;
-    if (!handles[dev] && cublasLtCreate(&handles[dev]) != CUBLAS_STATUS_SUCCESS) handles[dev] = nullptr;
-    return handles[dev];
-}
-
-// C[m, n] = op(A) op(B) in column-major terms, BF16 in and out, FP32 accumulate;
-// reductions across K chunks are excluded, so every output element is summed in
-// one fixed order (deterministic, no atomics).
-rlk_status lt_gemm(cublasLtHandle_t h, cublasOperation_t opA, cublasOperation_t opB, uint64_t m, uint64_t n,
-                   uint64_t k, const void* A, int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
-                   void* ws, cudaStream_t stream) {
-    cublasLtMatmulDesc_t op = nullptr;
-    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
-    cublasLtMatmulPreference_t pref = nullptr;
-    rlk_status st = RLK_OK;
-    auto ok = [&](cublasStatus_t s, const char* what) {
-        if (s != CUBLAS_STATUS_SUCCESS && st == RLK_OK) st = fail(RLK_ERR_CUDA, std::string("cuBLASLt ") + what);
-        return st == RLK_OK;
-    };
-    const uint32_t scheme = CUBLASLT_REDUCTION_SCHEME_NONE;
-    const uint64_t wsb = kLtWorkspace;
-    if (ok(cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F), "desc") &&
-        ok(cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &opA, sizeof(opA)), "transa") &&
-        ok(cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &opB, sizeof(opB)), "transb") &&
-        ok(cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, opA == CUBLAS_OP_N ? m : k, opA == CUBLAS_OP_N ? k : m, lda),
-           "layout A") &&
-        ok(cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, opB == CUBLAS_OP_N ? k : n, opB == CUBLAS_OP_N ? n : k, ldb),
-           "layout B") &&
-        ok(cublasLtMatrixLayoutCreate(&lc, CUDA_R_16BF, m, n, ldc), "layout C") &&
-        ok(cublasLtMatmulPreferenceCreate(&pref), "preference") &&
-        ok(cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &wsb, sizeof(wsb)),
-           "workspace pref") &&
-        ok(cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_REDUCTION_SCHEME_MASK, &scheme,
-                                                sizeof(scheme)),
-           "reduction pref")) {
-        cublasLtMatmulHeuristicResult_t res{};
-        int found = 0;
-        if (ok(cublasLtMatmulAlgoGetHeuristic(h, op, la, lb, lc, lc, pref, 1, &res, &found), "heuristic")) {
-            if (found < 1) {
-                st = fail(RLK_ERR_UNSUPPORTED, "cuBLASLt found no deterministic algorithm for the lm_head backward");
-            } else {
-                const float alpha = 1.f, beta = 0.f;
-                ok(cublasLtMatmul(h, op, &alpha, A, la, B, lb, &beta, C, lc, C, lc, &res.algo, ws, kLtWorkspace, stream),
-                   "matmul");
-            }
-        }
-    }
-    if (pref) cublasLtMatmulPreferenceDestroy(pref);
-    if (lc) cublasLtMatrixLayoutDestroy(lc);
-    if (lb) cublasLtMatrixLayoutDestroy(lb);
-    if (la) cublasLtMatrixLayoutDestroy(la);
-    if (op) cublasLtMatmulDescDestroy(op);
-    return st;
-}
-
-}  // namespace
-
-size_t lmhead_bwd_workspace(const rlk_logp_contract& c) {
-    return lmhead_fwd_workspace(c) + ((size_t)c.T * c.V_padded * 2 + 255) / 256 * 256 + kLtWorkspace;
-}
-
 rlk_status launch_lmhead_bwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
                              const int64_t* targets, const uint8_t* mask, const float* grad, float* logp, float* lse,
-                             void* dhidden, void* dweight, void* workspace, uint32_t* status, cudaStream_t stream) {
+                             void* dhidden, float* dweight_f32, void* dweight_bf16, void* workspace, uint32_t* status,
+                             cudaStream_t stream) {
+    // 1. forward: LSE and logp (clears all three launches' tickets first)
     rlk_status st = launch_lmhead_fwd(c, hidden, H, weight, targets, mask, logp, lse, workspace, status, stream);
     if (st != RLK_OK) return st;
-    unsigned char* ws = static_cast<unsigned char*>(workspace) + lmhead_fwd_workspace(c);
-    uint16_t* dlogits = reinterpret_cast<uint16_t*>(ws);
-    void* lt_ws = ws + ((size_t)c.T * c.V_padded * 2 + 255) / 256 * 256;
-    // dlogits = g * (onehot - exp(x - LSE)) from the recomputed logits (BF16 [T, V_padded]).
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    unsigned long long* tickets = reinterpret_cast<unsigned long long*>(ws);
+    uint16_t* dlogits = reinterpret_cast<uint16_t*>(ws + lmhead_fwd_workspace(c));
+    // 2. dlogits = g * (onehot - exp(x - LSE)) from the recomputed logits (BF16 [T, V_padded])
     LmLaunch L;
-    if ((st = prepare(L, c, hidden, H, weight, targets, mask, status)) != RLK_OK) return st;
+    if ((st = prepare(L, c, hidden, H, weight, targets, mask, status, tickets + kMaxGroups)) != RLK_OK) return st;
     L.p.lse_in = lse;
     L.p.grad = grad;
     L.p.dlogits = dlogits;
-    if ((st = run_gemm<kEpiGrad>(L, stream)) != RLK_OK) return st;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cublasLtHandle_t h = lt_handle(dev);
-    if (!h) return fail(RLK_ERR_CUDA, "cublasLtCreate failed");
-    // dHidden [T, H] = dlogits[:, :V_real] W[:V_real]; column-major: [H, T] = W_cm[H, Vr] x dlogits_cm[Vr, T].
-    if ((st = lt_gemm(h, CUBLAS_OP_N, CUBLAS_OP_N, (uint64_t)H, (uint64_t)c.T, (uint64_t)c.V_real, weight, H, dlogits,
-                      c.V_padded, dhidden, H, lt_ws, stream)) != RLK_OK)
+    if ((st = launch_gemm(lmhead_kernel<kEpiGrad>, L.grid, stream, "lm_head recompute GEMM", L.tmH, L.tmW, L.tmWr,
+                          L.p)) != RLK_OK)
         return st;
-    // dW[:V_real] = dlogits[:, :V_real]^T hidden; column-major: [H, Vr] = hidden_cm[H, T] x (dlogits_cm[Vr, T])^T.
-    if ((st = lt_gemm(h, CUBLAS_OP_N, CUBLAS_OP_T, (uint64_t)H, (uint64_t)c.V_real, (uint64_t)c.T, hidden, H, dlogits,
-                      c.V_padded, dweight, H, lt_ws, stream)) != RLK_OK)
-        return st;
-    if (c.V_padded > c.V_real) {
-        const cudaError_t e = cudaMemsetAsync(static_cast<uint16_t*>(dweight) + (size_t)c.V_real * H, 0,
-                                              (size_t)(c.V_padded - c.V_real) * H * 2, stream);
-        if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("clearing padded dW rows: ") + cudaGetErrorString(e));
-    }
-    return RLK_OK;
+    // 3. dHidden = dlogits[:, :V_real] W[:V_real] and dW = dlogits[:, :V_real]^T hidden in one launch.
+    // The maps stop at V_real (and at T), so padded columns of dlogits, padded
+    // rows of W and rows past T read as zero; rows [V_real, V_padded) of dW
+    // come out exactly 0.
+    CUtensorMap tmA0, tmB0, tmA1, tmB1;
+    if (!make_map(&tmA0, dlogits, c.V_real, c.T, c.V_padded, kBK, kBM) ||
+        !make_map(&tmB0, weight, H, c.V_real, H, 64, kBK) ||
+        !make_map(&tmA1, dlogits, c.V_real, c.T, c.V_padded, 64, kBK) ||
+        !make_map(&tmB1, hidden, H, c.T, H, 64, kBK))
+        return fail(RLK_ERR_CUDA, "cuTensorMapEncodeTiled failed for a gradient operand");
+    GradParams g{};
+    g.dhidden = static_cast<uint16_t*>(dhidden);
+    g.dw_bf16 = static_cast<uint16_t*>(dweight_bf16);
+    g.dw_f32 = dweight_f32;
+    g.ticket = tickets + 2 * kMaxGroups;
+    g.w = L.p.w;
+    g.T = c.T;
+    g.Vr = c.V_real;
+    g.Vp = c.V_padded;
+    g.H = (int32_t)H;
+    g.NB = (int32_t)((H + kBN - 1) / kBN);
+    g.KB0 = (int32_t)((c.V_real + kBK - 1) / kBK);
+    g.KB1 = (int32_t)((c.T + kBK - 1) / kBK);
+    g.n0 = ((c.T + kBM - 1) / kBM) * g.NB;
+    g.n1 = ((c.V_padded + kBM - 1) / kBM) * g.NB;
+    const int64_t total = g.n0 + g.n1;
+    const int grid = (int)(total < L.sms ? total : L.sms);
+    return launch_gemm(lmhead_grad_kernel, grid, stream, "lm_head gradient GEMM", tmA0, tmB0, tmA1, tmB1, g);
 }
 
 }  // namespace rlk

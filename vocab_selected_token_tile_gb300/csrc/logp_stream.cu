@@ -50,6 +50,7 @@
 
 #include <cstdio>
 #include <cstdlib>
+#include <initializer_list>
 #include <mutex>
 #include <string>
 
@@ -1028,7 +1029,7 @@ __device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0
         const TileGeom& tg = m.g;
         const float lse = (MODE == kModeBwd) ? h.lse_in : lse_v;
         if (MODE == kModeBwd && l == 0 && lane == 0 && h.active) {
-            if (h.target < 0 || h.target >= p.Vr) atomicOr(p.a.status, kStatusTargetRange);
+            if (!p.a.foreign_targets && (h.target < 0 || h.target >= p.Vr)) atomicOr(p.a.status, kStatusTargetRange);
             if (!isfinite(h.lse_in)) atomicOr(p.a.status, kStatusNonFinite);
         }
         tile_grad(slots + (size_t)it.slot * slot_elems + m.soff, p.a.logits + h.row * p.stride,
@@ -1185,6 +1186,27 @@ int env_int(const char* name, int dflt) {
     return (v && *v) ? std::atoi(v) : dflt;
 }
 
+// Planner overrides, for measurement: RLK_CTAS_PER_SM (1 or 2), RLK_ROW_BUFS
+// (2, 4 or 8), RLK_FUSED_SKEW (0 .. row buffers - 1) and RLK_FUSED_SCHEDULE
+// (l2 or resident).  These are the ring shapes the host protocol model
+// replays; any other value fails closed with RLK_ERR_UNSUPPORTED instead of
+// being clamped, so no process can run a ring shape the model has not run.
+rlk_status knob(const char* name, int dflt, std::initializer_list<int> allowed, int* out) {
+    const char* v = std::getenv(name);
+    *out = dflt;
+    if (!v || !*v) return RLK_OK;
+    char* end = nullptr;
+    const long x = std::strtol(v, &end, 10);
+    if (end && *end == '\0')
+        for (int a : allowed)
+            if (x == a) {
+                *out = a;
+                return RLK_OK;
+            }
+    return fail(RLK_ERR_UNSUPPORTED, std::string(name) + "=" + v +
+                                         " is not a planner value the ring protocol model replays");
+}
+
 uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
 FastDiv make_fastdiv(uint32_t d) {
@@ -1255,6 +1277,22 @@ uint32_t layout(Params& p, int NS) {
 
 }  // namespace
 
+rlk_status check_planner_env() {
+    int v = 0;
+    rlk_status s;
+    if ((s = knob("RLK_CTAS_PER_SM", 0, {0, 1, 2}, &v)) != RLK_OK) return s;
+    if ((s = knob("RLK_ROW_BUFS", 0, {2, 4, kMaxRowBufs}, &v)) != RLK_OK) return s;
+    if ((s = knob("RLK_FUSED_SKEW", -1, {-1, 0, 1, 2, 3, 4, 5, 6, 7}, &v)) != RLK_OK) return s;
+    const char* sch = std::getenv("RLK_FUSED_SCHEDULE");
+    if (sch && *sch && std::string(sch) != "l2" && std::string(sch) != "resident")
+        return fail(RLK_ERR_UNSUPPORTED, "RLK_FUSED_SCHEDULE must be l2 or resident");
+    for (const char* gone : {"RLK_TPS", "RLK_MAX_SLOTS", "RLK_LMHEAD_PAIR"}) {
+        const char* g = std::getenv(gone);
+        if (g && *g) return fail(RLK_ERR_UNSUPPORTED, std::string(gone) + " is not a planner override (unset it)");
+    }
+    return RLK_OK;
+}
+
 rlk_status launch_selftest_wait(uint64_t limit_ns, uint32_t* status, cudaStream_t stream) {
     selftest_wait_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
     const cudaError_t e = cudaGetLastError();
@@ -1284,8 +1322,7 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     // One bulk copy per chunk of tps consecutive tiles, about 8192 columns
     // (16 KB): a copy costs about the same issue time whatever its size, so
     // large copies are what keeps the stream near HBM bandwidth.
-    int tps_target = env_int("RLK_TPS", p.W >= 8192 ? 1 : 8192 / p.W);
-    if (tps_target < 1) tps_target = 1;
+    const int tps_target = p.W >= 8192 ? 1 : 8192 / p.W;
     auto set_chunk = [&](int tps) {
         p.tps = tps;
         const int64_t cols = (int64_t)tps * p.W;
@@ -1296,7 +1333,10 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     // RLK_FUSED_SCHEDULE=resident, the row shard held in shared memory.
     if (mode == kModeFused) {
         const char* sch = std::getenv("RLK_FUSED_SCHEDULE");
-        if (!(sch && std::string(sch) == "resident")) mode = kModeFusedL2;
+        const std::string s = sch ? sch : "";
+        if (!s.empty() && s != "l2" && s != "resident")
+            return fail(RLK_ERR_UNSUPPORTED, "RLK_FUSED_SCHEDULE must be l2 or resident");
+        if (s != "resident") mode = kModeFusedL2;
     }
     int C = (mode == kModeBwd) ? 1 : c.virtual_tp;
     // The streaming modes take larger chunks where the CTA's shard allows:
@@ -1306,7 +1346,7 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     // 0.3-1.5% faster for the forward and the backward).  The forward and the
     // backward keep the ~8192-column target where no such divisor reaches
     // half of it (a shard of a prime number of tiles, say).
-    if ((mode == kModeFusedL2 || mode == kModeFwd || mode == kModeBwd) && env_int("RLK_TPS", 0) == 0) {
+    if (mode == kModeFusedL2 || mode == kModeFwd || mode == kModeBwd) {
         const int ntl = c.num_tiles / C;
         int best = 1;
         for (int d = 1; d <= ntl; ++d)
@@ -1329,10 +1369,12 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         const int64_t row1 = shard_bytes * di.sm_count;  // one row shard per SM
         if (kL2ReuseBytes / (2 * row1) >= 2 || kL2ReuseBytes / row1 < 2) ctas_per_sm = 2;
     }
-    const int forced = env_int("RLK_CTAS_PER_SM", 0);
+    int forced = 0;
+    rlk_status kst = knob("RLK_CTAS_PER_SM", 0, {0, 1, 2}, &forced);
+    if (kst != RLK_OK) return kst;
     if (forced == 1 || forced == 2) ctas_per_sm = forced;
     uint32_t budget = (uint32_t)di.smem_optin / (uint32_t)ctas_per_sm - 1024u;
-    const int cap = env_int("RLK_MAX_SLOTS", kMaxSlots);
+    const int cap = kMaxSlots;
     auto max_slots = [&](Params& q) {
         int lo = 0;
         for (int ns = 1; ns <= cap; ++ns) {
@@ -1348,8 +1390,8 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         // (measured at virtual TP 8: the forward runs 5% faster with 4 than with
         // 8; the fused L2 schedule needs skew + 1 of them)
         const int rb_default = c.num_tiles > 256 ? 2 : (mode == kModeFusedL2 && c.num_tiles <= 128) ? 8 : 4;
-        int rb = env_int("RLK_ROW_BUFS", rb_default);
-        rb = rb >= kMaxRowBufs ? kMaxRowBufs : rb >= 4 ? 4 : 2;
+        int rb = rb_default;
+        if ((kst = knob("RLK_ROW_BUFS", rb_default, {2, 4, kMaxRowBufs}, &rb)) != RLK_OK) return kst;
         if (mode == kModeBwd || mode == kModeFused) rb = 2;
         p.rbufs = rb;
         p.rb_shift = rb == 8 ? 3 : rb == 4 ? 2 : 1;
@@ -1367,8 +1409,11 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
             if (skew > rb - 1) skew = rb - 1;
             if (skew < (ctas_per_sm == 2 ? 0 : 1)) skew = ctas_per_sm == 2 ? 0 : 1;
             // skew 0: phase B of a row right after its phase A and LSE
-            const int forced_skew = env_int("RLK_FUSED_SKEW", -1);
-            if (forced_skew >= 0) skew = forced_skew < rb - 1 ? forced_skew : rb - 1;
+            int forced_skew = -1;
+            if ((kst = knob("RLK_FUSED_SKEW", -1, {-1, 0, 1, 2, 3, 4, 5, 6, 7}, &forced_skew)) != RLK_OK) return kst;
+            if (forced_skew >= rb)
+                return fail(RLK_ERR_UNSUPPORTED, "RLK_FUSED_SKEW must be below the row buffers of the fold");
+            if (forced_skew >= 0) skew = forced_skew;
         }
         p.skew = skew;
     }

@@ -4,9 +4,11 @@
 // _tile_size and _validate_invocation precede any work; "typed contract"
 // commit: incompatible requests are rejected with explicit reasons and never
 // served by a silent fallback).
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <initializer_list>
 #include <mutex>
 #include <string>
 
@@ -54,7 +56,7 @@ rlk_status check_contract(const rlk_logp_contract* c) {
         return fail(RLK_ERR_INVALID_ARG, "mask_mode must be RLK_MASK_EXPLICIT or RLK_MASK_IGNORE_INDEX");
     if (c->validate != 0 && c->validate != 1) return fail(RLK_ERR_INVALID_ARG, "validate must be 0 or 1");
     if (c->wait_timeout_ns < 0) return fail(RLK_ERR_INVALID_ARG, "wait_timeout_ns must be >= 0");
-    return RLK_OK;
+    return check_planner_env();
 }
 
 rlk_status check_common(const rlk_logp_contract* c, const void* logits, const int64_t* targets,
@@ -75,11 +77,48 @@ rlk_status check_common(const rlk_logp_contract* c, const void* logits, const in
 rlk_status select_device(const void* ptr) {
     cudaPointerAttributes attr{};
     cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
-    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaPointerGetAttributes: ") + cudaGetErrorString(e));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(RLK_ERR_INVALID_ARG, std::string("the first device operand is not a CUDA pointer: ") +
+                                             cudaGetErrorString(e));
+    }
     if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
         return fail(RLK_ERR_INVALID_ARG, "device buffers must be device memory");
     e = cudaSetDevice(attr.device);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaSetDevice: ") + cudaGetErrorString(e));
+    return RLK_OK;
+}
+
+struct DevPtr {
+    const void* ptr;
+    const char* name;
+};
+
+// Every other pointer a call receives must be device memory of the device
+// select_device made current (or managed memory, which that device can
+// reach).  Host memory -- pinned or not -- and another GPU's memory fail
+// closed here, before any launch, instead of reaching a kernel.  NULL
+// entries are optional arguments the caller left out.
+rlk_status check_device_ptrs(std::initializer_list<DevPtr> ptrs) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    for (const DevPtr& d : ptrs) {
+        if (!d.ptr) continue;
+        cudaPointerAttributes attr{};
+        e = cudaPointerGetAttributes(&attr, d.ptr);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(RLK_ERR_INVALID_ARG, std::string(d.name) + " is not a CUDA pointer");
+        }
+        if (attr.type == cudaMemoryTypeManaged) continue;
+        if (attr.type != cudaMemoryTypeDevice)
+            return fail(RLK_ERR_INVALID_ARG, std::string(d.name) + " must be device memory (it is host memory)");
+        if (attr.device != dev)
+            return fail(RLK_ERR_INVALID_ARG, std::string(d.name) + " lives on device " + std::to_string(attr.device) +
+                                                 ", not on device " + std::to_string(dev) +
+                                                 " that holds the first operand");
+    }
     return RLK_OK;
 }
 
@@ -130,6 +169,9 @@ RLK_EXPORT rlk_status rlk_logp_fwd(const rlk_logp_contract* c, const void* logit
     if ((s = check_common(c, logits_bf16, targets, active_mask, workspace)) != RLK_OK) return s;
     if (!logp || !lse) return fail(RLK_ERR_INVALID_ARG, "logp and lse outputs are required");
     if ((s = select_device(logits_bf16)) != RLK_OK) return s;
+    if ((s = check_device_ptrs({{targets, "targets"}, {active_mask, "active_mask"}, {logp, "logp"}, {lse, "lse"},
+                                {partials, "partials"}, {workspace, "workspace"}})) != RLK_OK)
+        return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if ((s = begin(workspace, st)) != RLK_OK) return s;
     StreamArgs a{};
@@ -153,6 +195,9 @@ RLK_EXPORT rlk_status rlk_logp_fwd_entropy(const rlk_logp_contract* c, const voi
     if ((s = check_common(c, logits_bf16, targets, active_mask, workspace)) != RLK_OK) return s;
     if (!logp || !lse || !entropy) return fail(RLK_ERR_INVALID_ARG, "logp, lse and entropy outputs are required");
     if ((s = select_device(logits_bf16)) != RLK_OK) return s;
+    if ((s = check_device_ptrs({{targets, "targets"}, {active_mask, "active_mask"}, {logp, "logp"}, {lse, "lse"},
+                                {entropy, "entropy"}, {workspace, "workspace"}})) != RLK_OK)
+        return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if ((s = begin(workspace, st)) != RLK_OK) return s;
     StreamArgs a{};
@@ -177,6 +222,10 @@ RLK_EXPORT rlk_status rlk_grpo_loss(int64_t T, const float* logp, const float* a
     if (!(beta >= 0.f) || !isfinite(beta)) return fail(RLK_ERR_INVALID_ARG, "beta must be finite and >= 0");
     rlk_status s = select_device(loss);
     if (s != RLK_OK) return s;
+    if ((s = check_device_ptrs({{logp, "logp"}, {advantage, "advantage"}, {active_mask, "active_mask"},
+                                {ref_logp, "ref_logp"}, {grad_logp, "grad_logp"}, {active_count, "active_count"}})) !=
+        RLK_OK)
+        return s;
     return launch_grpo_loss(T, logp, advantage, active_mask, ref_logp, beta, loss, grad_logp, active_count,
                             reinterpret_cast<cudaStream_t>(stream));
 }
@@ -197,6 +246,10 @@ RLK_EXPORT rlk_status rlk_logp_bwd(const rlk_logp_contract* c, const void* logit
     if (!lse_in && (!logp_out || !lse_out))
         return fail(RLK_ERR_INVALID_ARG, "the fused form (lse_in NULL) needs logp_out and lse_out");
     if ((s = select_device(logits_bf16)) != RLK_OK) return s;
+    if ((s = check_device_ptrs({{targets, "targets"}, {active_mask, "active_mask"}, {lse_in, "lse_in"},
+                                {grad_logp, "grad_logp"}, {dlogits_bf16, "dlogits"}, {logp_out, "logp_out"},
+                                {lse_out, "lse_out"}, {workspace, "workspace"}})) != RLK_OK)
+        return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if ((s = begin(workspace, st)) != RLK_OK) return s;
     StreamArgs a{};
@@ -223,8 +276,8 @@ RLK_EXPORT size_t rlk_logp_lmhead_workspace_size(const rlk_logp_contract* c, int
 RLK_EXPORT rlk_status rlk_logp_fused_lmhead(const rlk_logp_contract* c, const void* hidden_bf16, int64_t H,
                                             const void* weight_bf16, const int64_t* targets,
                                             const uint8_t* active_mask, const float* grad_logp, float* logp,
-                                            float* lse, void* dhidden_bf16, void* dweight_bf16, void* workspace,
-                                            rlk_stream_t stream) {
+                                            float* lse, void* dhidden_bf16, float* dweight_f32, void* dweight_bf16,
+                                            void* workspace, rlk_stream_t stream) {
     rlk_status s = check_contract(c);
     if (s != RLK_OK) return s;
     if ((s = lmhead_check(*c, H)) != RLK_OK) return s;
@@ -240,23 +293,143 @@ RLK_EXPORT rlk_status rlk_logp_fused_lmhead(const rlk_logp_contract* c, const vo
     if (!logp || !lse) return fail(RLK_ERR_INVALID_ARG, "logp and lse outputs are required");
     if (!workspace || !aligned16(workspace)) return fail(RLK_ERR_INVALID_ARG, "workspace must be non-NULL and 16-byte aligned");
     const bool bwd = grad_logp != nullptr;
-    if (bwd && (!dhidden_bf16 || !dweight_bf16))
-        return fail(RLK_ERR_INVALID_ARG, "the backward (grad_logp given) needs dhidden and dweight");
-    if (!bwd && (dhidden_bf16 || dweight_bf16))
+    if (bwd && (!dhidden_bf16 || (!dweight_f32 && !dweight_bf16)))
+        return fail(RLK_ERR_INVALID_ARG, "the backward (grad_logp given) needs dhidden and at least one dweight output");
+    if (!bwd && (dhidden_bf16 || dweight_f32 || dweight_bf16))
         return fail(RLK_ERR_INVALID_ARG, "dhidden/dweight are written only when grad_logp is given");
-    if (bwd && (!aligned16(dhidden_bf16) || !aligned16(dweight_bf16)))
+    if (bwd && (!aligned16(dhidden_bf16) || !aligned16(dweight_f32) || !aligned16(dweight_bf16)))
         return fail(RLK_ERR_MISALIGNED, "dhidden and dweight must be 16-byte aligned");
     if ((s = select_device(hidden_bf16)) != RLK_OK) return s;
+    if ((s = check_device_ptrs({{weight_bf16, "weight"}, {targets, "targets"}, {active_mask, "active_mask"},
+                                {grad_logp, "grad_logp"}, {logp, "logp"}, {lse, "lse"}, {dhidden_bf16, "dhidden"},
+                                {dweight_f32, "dweight_f32"}, {dweight_bf16, "dweight_bf16"},
+                                {workspace, "workspace"}})) != RLK_OK)
+        return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if ((s = begin(workspace, st)) != RLK_OK) return s;
     uint32_t* status = static_cast<uint32_t*>(workspace);
     void* ws = static_cast<unsigned char*>(workspace) + kWorkspaceBytes;
     if (bwd)
         s = launch_lmhead_bwd(*c, hidden_bf16, H, weight_bf16, targets, active_mask, grad_logp, logp, lse,
-                              dhidden_bf16, dweight_bf16, ws, status, st);
+                              dhidden_bf16, dweight_f32, dweight_bf16, ws, status, st);
     else
         s = launch_lmhead_fwd(*c, hidden_bf16, H, weight_bf16, targets, active_mask, logp, lse, ws, status, st);
     if (s != RLK_OK) return s;
+    return c->validate ? read_status(workspace, st) : RLK_OK;
+}
+
+// ---------------------------------------------------------------- vocabulary-parallel shards
+
+namespace rlk {
+namespace {
+
+// A shard call's contract is the whole problem's, with virtual_tp = the
+// number of shards and row_stride that of the shard's buffer (0 -> Vs).
+rlk_status check_shard(const rlk_logp_contract* c, int32_t shard) {
+    if (!c) return fail(RLK_ERR_INVALID_ARG, "contract is NULL");
+    rlk_logp_contract whole = *c;
+    whole.row_stride = 0;
+    rlk_status s = check_contract(&whole);
+    if (s != RLK_OK) return s;
+    if (shard < 0 || shard >= c->virtual_tp) return fail(RLK_ERR_INVALID_ARG, "shard must lie in [0, virtual_tp)");
+    const int64_t Vs = c->V_padded / c->virtual_tp;
+    if (Vs % 8 != 0)
+        return fail(RLK_ERR_MISALIGNED, "every shard must start on a 16-byte boundary: V_padded/virtual_tp must be a "
+                                        "multiple of 8");
+    const int64_t stride = c->row_stride ? c->row_stride : Vs;
+    if (stride < Vs) return fail(RLK_ERR_INVALID_ARG, "row_stride of a shard must be >= V_padded/virtual_tp");
+    if (stride % 8 != 0) return fail(RLK_ERR_MISALIGNED, "row_stride must be a multiple of 8 elements (16-byte rows)");
+    return RLK_OK;
+}
+
+}  // namespace
+
+rlk_status check_shard_contract(const rlk_logp_contract& c, int32_t shard) { return check_shard(&c, shard); }
+
+}  // namespace rlk
+
+RLK_EXPORT rlk_status rlk_logp_check_shard_contract(const rlk_logp_contract* c, int32_t shard) {
+    return check_shard(c, shard);
+}
+
+RLK_EXPORT size_t rlk_logp_shard_workspace_size(const rlk_logp_contract* c) {
+    return check_shard(c, 0) == RLK_OK ? kWorkspaceBytes + shard_workspace(*c) : 0;
+}
+
+RLK_EXPORT rlk_status rlk_logp_shard_fwd(const rlk_logp_contract* c, int32_t shard, const void* logits_shard,
+                                         const int64_t* targets, const uint8_t* active_mask, float* partials_shard,
+                                         float* target_logit, void* workspace, rlk_stream_t stream) {
+    rlk_status s = check_shard(c, shard);
+    if (s != RLK_OK) return s;
+    if (c->T == 0) return RLK_OK;
+    if ((s = check_common(c, logits_shard, targets, active_mask, workspace)) != RLK_OK) return s;
+    if (!partials_shard || !target_logit)
+        return fail(RLK_ERR_INVALID_ARG, "partials_shard and target_logit outputs are required");
+    if ((s = select_device(logits_shard)) != RLK_OK) return s;
+    if ((s = check_device_ptrs({{targets, "targets"}, {active_mask, "active_mask"}, {partials_shard, "partials_shard"},
+                                {target_logit, "target_logit"}, {workspace, "workspace"}})) != RLK_OK)
+        return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = begin(workspace, st)) != RLK_OK) return s;
+    if ((s = launch_shard_fwd(*c, shard, static_cast<const uint16_t*>(logits_shard), targets, active_mask,
+                              partials_shard, target_logit, static_cast<unsigned char*>(workspace) + kWorkspaceBytes,
+                              static_cast<uint32_t*>(workspace), st)) != RLK_OK)
+        return s;
+    return c->validate ? read_status(workspace, st) : RLK_OK;
+}
+
+RLK_EXPORT rlk_status rlk_logp_fold(const rlk_logp_contract* c, const float* gathered_partials,
+                                    const float* gathered_target_logit, const int64_t* targets,
+                                    const uint8_t* active_mask, float* logp, float* lse, void* workspace,
+                                    rlk_stream_t stream) {
+    rlk_status s = check_shard(c, 0);
+    if (s != RLK_OK) return s;
+    if (c->T == 0) return RLK_OK;
+    if (!gathered_partials || !gathered_target_logit)
+        return fail(RLK_ERR_INVALID_ARG, "gathered_partials and gathered_target_logit are required");
+    if (!targets) return fail(RLK_ERR_INVALID_ARG, "targets is NULL");
+    if (c->mask_mode == RLK_MASK_EXPLICIT && !active_mask)
+        return fail(RLK_ERR_INVALID_ARG, "explicit mask mode needs active_mask");
+    if (c->mask_mode == RLK_MASK_IGNORE_INDEX && active_mask)
+        return fail(RLK_ERR_INVALID_ARG, "ignore_index mode takes no active_mask (pass NULL)");
+    if (!logp || !lse) return fail(RLK_ERR_INVALID_ARG, "logp and lse outputs are required");
+    if (!workspace || !aligned16(workspace)) return fail(RLK_ERR_INVALID_ARG, "workspace must be non-NULL and 16-byte aligned");
+    if ((s = select_device(gathered_partials)) != RLK_OK) return s;
+    if ((s = check_device_ptrs({{gathered_target_logit, "gathered_target_logit"}, {targets, "targets"},
+                                {active_mask, "active_mask"}, {logp, "logp"}, {lse, "lse"},
+                                {workspace, "workspace"}})) != RLK_OK)
+        return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = begin(workspace, st)) != RLK_OK) return s;
+    if ((s = launch_gathered_fold(*c, gathered_partials, gathered_target_logit, targets, active_mask, logp, lse,
+                                  static_cast<uint32_t*>(workspace), st)) != RLK_OK)
+        return s;
+    return c->validate ? read_status(workspace, st) : RLK_OK;
+}
+
+RLK_EXPORT rlk_status rlk_logp_shard_bwd(const rlk_logp_contract* c, int32_t shard, const void* logits_shard,
+                                         const int64_t* targets, const uint8_t* active_mask, const float* lse_in,
+                                         const float* grad_logp, void* dlogits_shard, void* workspace,
+                                         rlk_stream_t stream) {
+    rlk_status s = check_shard(c, shard);
+    if (s != RLK_OK) return s;
+    if (c->T == 0) return RLK_OK;
+    if ((s = check_common(c, logits_shard, targets, active_mask, workspace)) != RLK_OK) return s;
+    if (!lse_in || !grad_logp) return fail(RLK_ERR_INVALID_ARG, "lse_in and grad_logp are required");
+    if (!dlogits_shard) return fail(RLK_ERR_INVALID_ARG, "dlogits_shard is NULL");
+    if (!aligned16(dlogits_shard)) return fail(RLK_ERR_MISALIGNED, "dlogits_shard must be 16-byte aligned");
+    if ((s = select_device(logits_shard)) != RLK_OK) return s;
+    if ((s = check_device_ptrs({{targets, "targets"}, {active_mask, "active_mask"}, {lse_in, "lse_in"},
+                                {grad_logp, "grad_logp"}, {dlogits_shard, "dlogits_shard"},
+                                {workspace, "workspace"}})) != RLK_OK)
+        return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = begin(workspace, st)) != RLK_OK) return s;
+    if ((s = launch_shard_bwd(*c, shard, static_cast<const uint16_t*>(logits_shard), targets, active_mask, lse_in,
+                              grad_logp, static_cast<uint16_t*>(dlogits_shard),
+                              static_cast<unsigned char*>(workspace) + kWorkspaceBytes, static_cast<uint32_t*>(workspace),
+                              st)) != RLK_OK)
+        return s;
     return c->validate ? read_status(workspace, st) : RLK_OK;
 }
 
@@ -275,23 +448,60 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = 256;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch, looked up once per device with that
-// device current.  In host code the array's name is only a host-side stand-in.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Process-unique id of the calling thread's current CUDA context (the
+// driver never reuses one), so that an address looked up in a context that
+// has since been destroyed -- by cudaDeviceReset, say -- is never used again.
+rlk_status current_context_id(unsigned long long* id) {
+    static std::mutex mu;
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!get_current || !get_id) {
+            void* f1 = nullptr;
+            void* f2 = nullptr;
+            cudaDriverEntryPointQueryResult q1, q2;
+            if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+                q1 != cudaDriverEntryPointSuccess ||
+                cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+                q2 != cudaDriverEntryPointSuccess)
+                return fail(RLK_ERR_CUDA, "cannot resolve cuCtxGetCurrent / cuCtxGetId");
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+            get_id = reinterpret_cast<CtxGetIdFn>(f2);
+        }
+    }
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, id) != CUDA_SUCCESS)
+        return fail(RLK_ERR_CUDA, "no current CUDA context");
+    return RLK_OK;
+}
+
+// Device address of g_noalloc_scratch, looked up (cudaGetSymbolAddress, with
+// the device current) once per device and context; in host code the array's
+// name is only a host-side stand-in, never a device address.
 rlk_status noalloc_scratch(void** out) {
     static std::mutex mu;
     static void* addr[64] = {};
+    static unsigned long long ctx_of[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
     if (dev < 0 || dev >= 64) return fail(RLK_ERR_UNSUPPORTED, "device ordinal above 63");
+    unsigned long long ctx = 0;
+    rlk_status s = current_context_id(&ctx);
+    if (s != RLK_OK) return s;
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (!addr[dev] || ctx_of[dev] != ctx) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p)
             return fail(RLK_ERR_CUDA, std::string("cudaGetSymbolAddress of the static scratch: ") +
                                           cudaGetErrorString(e));
         addr[dev] = p;
+        ctx_of[dev] = ctx;
     }
     *out = addr[dev];
     return RLK_OK;
@@ -315,6 +525,9 @@ RLK_EXPORT rlk_status rlk_logp_fwd_noalloc(const rlk_logp_contract* c, const voi
     if ((s = noalloc_scratch(&scratch)) != RLK_OK) return s;
     if ((s = check_common(c, logits_bf16, targets, active_mask, scratch)) != RLK_OK) return s;
     if (!logp || !lse) return fail(RLK_ERR_INVALID_ARG, "logp and lse outputs are required");
+    if ((s = check_device_ptrs({{targets, "targets"}, {active_mask, "active_mask"}, {logp, "logp"}, {lse, "lse"},
+                                {partials, "partials"}})) != RLK_OK)
+        return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if ((s = begin(scratch, st)) != RLK_OK) return s;  // the status word starts at zero on every call
     StreamArgs a{};
@@ -331,6 +544,8 @@ RLK_EXPORT rlk_status rlk_logp_fwd_noalloc(const rlk_logp_contract* c, const voi
 
 RLK_EXPORT rlk_status rlk_logp_workspace_status(const void* workspace, rlk_stream_t stream) {
     if (!workspace) return fail(RLK_ERR_INVALID_ARG, "workspace is NULL");
+    rlk_status s = select_device(workspace);
+    if (s != RLK_OK) return s;
     return read_status(workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 

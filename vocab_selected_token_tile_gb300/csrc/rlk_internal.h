@@ -41,10 +41,19 @@ struct StreamArgs {
     float* partials;
     float* entropy;  // optional (forward): entropy of each row's softmax
     uint32_t* status;
+    // kModeBwd on one vocabulary shard: an active row's target may lie in
+    // another shard (any value outside [0, V_real) of this launch); it then
+    // takes no one-hot term here and is not an error.
+    int32_t foreign_targets;
 };
 
 // Records a failure reason for rlk_last_error_message() and returns `s`.
 rlk_status fail(rlk_status s, const std::string& why);
+
+// Host check of the planner overrides in the environment (RLK_CTAS_PER_SM,
+// RLK_ROW_BUFS, RLK_FUSED_SKEW, RLK_FUSED_SCHEDULE): RLK_ERR_UNSUPPORTED for
+// any value outside the ring shapes the protocol model replays.
+rlk_status check_planner_env();
 
 // Launches one streaming kernel (mode kModeFwd / kModeBwd / kModeFused) for a
 // validated contract; returns RLK_OK or an error with the message set.
@@ -61,7 +70,26 @@ rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int
 size_t lmhead_bwd_workspace(const rlk_logp_contract& c);
 rlk_status launch_lmhead_bwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
                              const int64_t* targets, const uint8_t* mask, const float* grad, float* logp, float* lse,
-                             void* dhidden, void* dweight, void* workspace, uint32_t* status, cudaStream_t stream);
+                             void* dhidden, float* dweight_f32, void* dweight_bf16, void* workspace, uint32_t* status,
+                             cudaStream_t stream);
+
+// Vocabulary-parallel pieces (shard.cu).  A shard call's contract describes
+// the whole problem with virtual_tp = the number of shards; shard j holds
+// columns [j*Vs, (j+1)*Vs) of the padded vocabulary, Vs = V_padded/virtual_tp.
+rlk_status check_shard_contract(const rlk_logp_contract& c, int32_t shard);
+// The contract of shard j's columns as a vocabulary of its own (V_real of it
+// may be 0: a shard of padding only).
+rlk_logp_contract shard_local_contract(const rlk_logp_contract& c, int32_t shard);
+size_t shard_workspace(const rlk_logp_contract& c);
+rlk_status launch_shard_fwd(const rlk_logp_contract& c, int32_t shard, const uint16_t* logits, const int64_t* targets,
+                            const uint8_t* mask, float* partials, float* target_logit, void* workspace,
+                            uint32_t* status, cudaStream_t stream);
+rlk_status launch_gathered_fold(const rlk_logp_contract& c, const float* gathered_partials,
+                                const float* gathered_xt, const int64_t* targets, const uint8_t* mask, float* logp,
+                                float* lse, uint32_t* status, cudaStream_t stream);
+rlk_status launch_shard_bwd(const rlk_logp_contract& c, int32_t shard, const uint16_t* logits, const int64_t* targets,
+                            const uint8_t* mask, const float* lse_in, const float* grad, uint16_t* dlogits,
+                            void* workspace, uint32_t* status, cudaStream_t stream);
 
 // Token-mean GRPO loss and its gradient (grpo_loss.cu); one CTA, fixed order.
 rlk_status launch_grpo_loss(int64_t T, const float* logp, const float* adv, const uint8_t* mask, const float* ref,

@@ -115,17 +115,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
-// The same load delivered to every CTA of the cluster named in `cta_mask`, at
-// the same shared-memory offset, completing on each one's mbarrier at `bar`.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, int32_t c0, int32_t c1, uint32_t bar,
-                                               uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
-
 // ----------------------------------------------------------------- tcgen05 (5th-gen tensor cores, TMEM)
 
 // Allocate / free `ncols` columns of tensor memory (a power of two >= 32);
@@ -154,15 +143,6 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// Arrive on the mbarrier at offset `bar` of every CTA in `cta_mask` once the
-// previously issued MMAs of this thread have completed.
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                     bar),
-                 "h"(cta_mask)
                  : "memory");
 }
 
@@ -198,11 +178,29 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// Shared-memory matrix descriptor of an MN-major BF16 tile stored with the
+// 128-byte swizzle: the operand's M (or N) index is the contiguous one, 64
+// elements (128 B) per swizzle row, and each 1024-byte swizzle atom holds 8
+// consecutive K indices of one 64-wide MN block.  `lbo` is the byte distance
+// between consecutive 64-wide MN blocks (leading-dimension offset, bits
+// [16,30)), `sbo` the distance between consecutive groups of 8 K indices
+// (stride-dimension offset, bits [32,46)); both in 16-byte units.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
 // Instruction descriptor of kind::f16: FP32 accumulator (bits [4,6) = 1),
 // BF16 A and B (bits [7,10) and [10,13) = 1), both K-major, N >> 3 in
 // bits [17,23), M >> 4 in bits [24,29).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// The same with the major-ness of each operand: bit 15 set = A is MN-major
+// (transposed), bit 16 set = B is MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_major(uint32_t M, uint32_t N, bool a_mn, bool b_mn) {
+    return idesc_bf16_f32(M, N) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
 }
 
 // ----------------------------------------------------------------- clusters
