@@ -7,12 +7,23 @@ active_count; it writes BF16 dlogits [65536, 152576] plus FP32 logp and LSE.
 Every row is read once and written once.  Inputs (20 GB) are larger than L2,
 so no flush is needed between steps.
 
-Prints ONE JSON line on rank 0.  ``--impl reference`` times the FP64 CPU
-oracle instead, on a bounded sample of the same workload.
+Prints ONE JSON line on rank 0.  Beside the headline it carries, under
+``extra``, the other paths timed the same way, each with its own clock
+record: the forward at virtual TP 1 and 8 (rollout), the fused step at
+virtual TP 1 and 8, and the fused lm_head (hidden [8192, 4096] x W
+[152576, 4096]) forward and forward+backward (``--no-extra`` skips them).
+``--impl reference`` times the FP64 CPU oracle instead, on a bounded sample
+of the same workload, across the host's cores.
 
-Multi-GPU (torchrun): token rows are independent, so each rank runs its own
-full batch with no collective on the data path (weak scaling); the time is the
-max over ranks.
+Multi-GPU (torchrun), ``--split``:
+* ``none`` (default): each rank runs its own full batch with no collective on
+  the data path (weak scaling);
+* ``rows``: the batch's token rows are split over the ranks, T/n each, no
+  collective (strong scaling);
+* ``vocab``: vocabulary-parallel TP -- every rank holds V_padded/n columns of
+  all T rows; a step is the shard forward, one all-gather of the partials and
+  target logits (NCCL), the fold, and the shard backward (strong scaling).
+The time is the max over ranks.
 """
 import argparse
 import hashlib
@@ -43,15 +54,18 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--vtp", type=int, default=2)
+    ap.add_argument("--split", default="none", choices=["none", "rows", "vocab"],
+                    help="multi-GPU: full batch per rank (weak), rows or vocabulary columns split (strong)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--extra", action="store_true", help="also time the forward-only and split paths")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other paths' timings")
     ap.add_argument("--rows", type=int, default=0,
                     help="profiling only: shrink the batch to this many rows (not a bench number)")
-    ap.add_argument("--path", default="fused", choices=["fused", "fwd", "split", "lmhead"],
-                    help="profiling only: time the forward kernel or the split path instead of the fused step")
-    ap.add_argument("--ref-seconds", type=float, default=120.0,
-                    help="--impl reference: CPU seconds spread over the warm-up and timed steps")
+    ap.add_argument("--path", default="fused", choices=["fused", "fwd", "split", "lmhead", "lmhead_bwd"],
+                    help="profiling only: time another kernel instead of the fused step")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="--impl reference: oracle seconds per core spread over the warm-up and timed steps")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle seconds per core for cpu_baseline")
     return ap.parse_args()
 
 
@@ -83,7 +97,7 @@ def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1885.4)), "measured"
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1900.0)), "measured"
     return 6800.0, 1900.0, "fallback"
 
 
@@ -121,6 +135,7 @@ class ClockSampler:
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        time.sleep(0.15)  # the first sample lands before the timed region
 
     def _read(self):
         for line in self.proc.stdout:
@@ -155,29 +170,73 @@ def cpu_threads():
 
 # --------------------------------------------------------------------------- CPU oracle leg
 
-def time_oracle(w, budget_s=15.0, max_rows=512):
-    """The FP64 oracle, as it stands, on a seeded row sample of the workload; tokens/s."""
+def _oracle_worker(task):
+    """One pool worker: the FP64 oracle on seeded rows of the grpo workload until `budget` seconds of oracle
+    time are spent; returns (rows, oracle seconds).  Row generation is outside the timed part."""
+    os.environ["OMP_NUM_THREADS"] = "1"
     import numpy as np
 
     import oracle
     from synth import workloads as W
+    worker, nworkers, budget, max_rows = task
+    w = W.GRPO
     tgt = W.targets(w)
     active = W.active_rows(w, tgt=tgt)
     g = W.grad(w, active)
-    rng = np.random.default_rng(0)
-    order = rng.permutation(w.T)
-    done = 0
-    t_total = 0.0
-    chunk = 16
-    while done < max_rows and t_total < budget_s:
+    order = np.random.default_rng(0).permutation(w.T)[worker::nworkers]
+    done, secs, chunk = 0, 0.0, 8
+    while done < min(max_rows, len(order)) and secs < budget:
         rows = np.sort(order[done:done + chunk])
         bits = np.concatenate([W.logits_host(w, row0=int(r), nrows=1) for r in rows])
         t0 = time.perf_counter()
         oracle.selected_logp(bits, tgt[rows], active[rows], w.v_real)
         oracle.dlogits(bits, tgt[rows], active[rows], g[rows], w.v_real, w.v_padded)
-        t_total += time.perf_counter() - t0
+        secs += time.perf_counter() - t0
         done += len(rows)
-    return done / t_total, done, t_total
+    return done, secs
+
+
+def oracle_pool(cores):
+    """One worker process per core, spawned (so no CUDA state is inherited)."""
+    import multiprocessing as mpr
+    return mpr.get_context("spawn").Pool(cores)
+
+
+def time_oracle(pool, budget_s, cores, max_rows_per_core=4096):
+    """The FP64 oracle, as it stands, on seeded row samples of the grpo workload, every core busy at
+    once; tokens/s summed over the cores."""
+    res = pool.map(_oracle_worker, [(i, cores, budget_s, max_rows_per_core) for i in range(cores)])
+    rows = sum(r for r, _ in res)
+    rate = sum(r / s for r, s in res if s > 0)
+    return rate, rows, max(s for _, s in res)
+
+
+# --------------------------------------------------------------------------- timing helpers
+
+def timed(fn, steps, warmup, stream, clock_index, per_launch=True):
+    """Runs fn() warmup times, then steps times between CUDA events on `stream` with a clock record;
+    returns (total ms, mean per-call ms, clocks)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(clock_index)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        if per_launch:
+            ev[i][0].record(stream)
+        fn()
+        if per_launch:
+            ev[i][1].record(stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total = a.elapsed_time(b)
+    per = statistics.mean(x.elapsed_time(y) for x, y in ev) if per_launch else total / steps
+    return total, per, clk
 
 
 # --------------------------------------------------------------------------- GPU leg
@@ -191,12 +250,15 @@ def run_ours(args, ws, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if args.path == "lmhead":
-        res = lmhead_bench(rlk, args, dev, steps=args.steps, warmup=args.warmup, rows=args.rows)
-        return {"metric": "lm_head fused forward tokens/s (profiling run)", "value": res["tokens_per_s"],
-                "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
+    if args.path in ("lmhead", "lmhead_bwd"):
+        res = lmhead_bench(rlk, args, dev, local, steps=args.steps, warmup=args.warmup, rows=args.rows,
+                           bwd=args.path == "lmhead_bwd")
+        return {"metric": "lm_head fused tokens/s (profiling run)", "value": res["tokens_per_s"], "unit": UNIT,
+                "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
                 "higher_is_better": True, "config": {"workload": res["workload"]}, "roofline": res["roofline"],
-                "gpu_launches": 2 * args.steps}
+                "clocks": res["clocks"], "gpu_launches": res["launches_per_step"] * args.steps}
+    if args.split == "vocab":
+        return vocab_split_bench(rlk, args, ws, rank, local, dev)
     w = W.GRPO
     if args.rows:
         w = w.with_(batch=max(1, args.rows // w.seq), name="grpo-profile")
@@ -205,15 +267,20 @@ def run_ours(args, ws, rank, local):
     mask = W.active_mask(w)
     active = mask != 0
     g = W.grad(w, active)
-    logits = torch.empty((T, Vp), dtype=torch.int16, device=dev)
-    W.logits_device(w, logits)
-    targets = torch.from_numpy(tgt).to(dev)
-    dmask = torch.from_numpy(mask).to(dev)
-    dg = torch.from_numpy(g).to(dev)
+    r0, r1 = 0, T
+    if args.split == "rows" and ws > 1:
+        from vocab_selected_token_tile_gb300.vocab_parallel import split_rows
+        r0, r1 = split_rows(T, ws, rank)
+    Tl = r1 - r0
+    logits = torch.empty((Tl, Vp), dtype=torch.int16, device=dev)
+    W.logits_device(w, logits, row0=r0, nrows=Tl)
+    targets = torch.from_numpy(tgt[r0:r1]).to(dev)
+    dmask = torch.from_numpy(mask[r0:r1]).to(dev)
+    dg = torch.from_numpy(g[r0:r1]).to(dev)
     dlogits = torch.empty_like(logits)
-    logp = torch.empty(T, dtype=torch.float32, device=dev)
-    lse = torch.empty(T, dtype=torch.float32, device=dev)
-    c = rlk.Contract(T=T, V_real=Vr, V_padded=Vp, num_tiles=w.num_tiles, virtual_tp=args.vtp,
+    logp = torch.empty(Tl, dtype=torch.float32, device=dev)
+    lse = torch.empty(Tl, dtype=torch.float32, device=dev)
+    c = rlk.Contract(T=Tl, V_real=Vr, V_padded=Vp, num_tiles=w.num_tiles, virtual_tp=args.vtp,
                      mask_mode=rlk.MASK_EXPLICIT, validate=0)
     stream = torch.cuda.current_stream()
     ws_buf = rlk.workspace_for(c, dev, stream)
@@ -241,55 +308,42 @@ def run_ours(args, ws, rank, local):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
-    clocks.start()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    t_begin = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_begin.record(stream)
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
+    total_ms, per_launch_ms, clk = timed(step, args.steps, 0, stream, local)
     if ws > 1:
         torch.distributed.barrier()
-    total_ms = t_begin.elapsed_time(t_end)
-    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    if ws > 1:
         total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
 
     hbm_peak, bf16_peak, peak_kind = measured_peaks()
-    n_active = int(active.sum())
-    fwd_bytes = T * 2 * Vr + T * (8 + 1 + 4 + 4)              # logits, targets, mask, logp, LSE
-    bwd_bytes = n_active * 2 * Vr + T * 2 * Vp + T * (8 + 1 + 4 + 4)  # logits of active rows, dlogits, g, LSE
-    alg_bytes = {"fused": T * (2 * Vr + 2 * Vp) + T * (8 + 1 + 4 + 4 + 4),
+    n_active = int(active[r0:r1].sum())
+    fwd_bytes = Tl * 2 * Vr + Tl * (8 + 1 + 4 + 4)              # logits, targets, mask, logp, LSE
+    bwd_bytes = n_active * 2 * Vr + Tl * 2 * Vp + Tl * (8 + 1 + 4 + 4)  # logits of active rows, dlogits, g, LSE
+    alg_bytes = {"fused": Tl * (2 * Vr + 2 * Vp) + Tl * (8 + 1 + 4 + 4 + 4),
                  "fwd": fwd_bytes, "split": fwd_bytes + bwd_bytes}[args.path]
     kernel = {"fused": "stream_kernel<kModeFusedL2>", "fwd": "stream_kernel<kModeFwd>",
               "split": "stream_kernel<kModeFwd> + stream_kernel<kModeBwd>"}[args.path]
     launches_per_step = 2 if args.path == "split" else 1
     achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
+    rows_split = args.split == "rows" and ws > 1
     result = {
         "metric": METRIC,
-        "value": ws * T / (ms_per_step * 1e-3),
+        "value": (T if rows_split else ws * T) / (ms_per_step * 1e-3),
         "unit": UNIT,
         "n_gpus": ws,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": ms_per_step,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong" if rows_split else "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded counter-based generator; no dataset)",
         "config": {
             "workload": f"{w.name}: {args.path} fwd+bwd, T={T} ({w.batch}x{w.seq}) x V_padded={Vp} (V_real={Vr}), "
                         f"64 tiles, virtual TP {args.vtp}, g = A_b*mask/active_count",
-            "active_tokens": n_active,
-            "parallelism": f"dp{ws} (independent rows, no collective)" if ws > 1 else "single GPU",
+            "active_tokens": int(active.sum()),
+            "parallelism": (f"rows split over {ws} GPUs ({Tl} rows on rank 0), no collective" if rows_split else
+                            f"dp{ws} (independent rows, no collective)" if ws > 1 else "single GPU"),
             "l2": "inputs (20.0 GB logits) larger than L2; no flush",
             "alg_bytes_per_step": alg_bytes,
         },
@@ -300,21 +354,82 @@ def run_ours(args, ws, rank, local):
             "peak": hbm_peak,
             "unit": "GB/s",
             "frac": achieved / hbm_peak,
-            "traffic": recorded_traffic(kernel, w.name) if args.path != "split" else None,
+            "traffic": recorded_traffic(kernel, w.name) if (args.path == "fused" and Tl == 65536) else None,
             "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)",
             "kernel": kernel,
         },
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
     }
-    if args.extra and rank == 0:
-        result["extra"] = extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, Vp, args)
+    if not args.no_extra and rank == 0 and not args.rows:
+        result["extra"] = extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, Tl, Vr, Vp, args,
+                                      local)
     if not args.no_e2e:
-        result["e2e"] = e2e(rlk, c, w, logits, tgt, mask, g, dev, args)
+        result["e2e"] = e2e(rlk, c, w, logits, tgt[r0:r1], mask[r0:r1], g[r0:r1], dev, args)
     return result
 
 
-def lmhead_bench(rlk, args, dev, steps=10, warmup=3, rows=0):
+def vocab_split_bench(rlk, args, ws, rank, local, dev):
+    """Vocabulary-parallel TP over the ranks: each holds V_padded/ws columns of all T rows of the grpo batch."""
+    import torch
+
+    from synth import workloads as W
+    from vocab_selected_token_tile_gb300.vocab_parallel import VocabParallelLogp
+    w = W.GRPO
+    T, Vr, Vp = w.T, w.v_real, w.v_padded
+    vs = Vp // ws
+    tgt = W.targets(w)
+    mask = W.active_mask(w)
+    g = W.grad(w, mask != 0)
+    shard = torch.empty((T, vs), dtype=torch.int16, device=dev)
+    chunk = 4096
+    tmp = torch.empty((chunk, Vp), dtype=torch.int16, device=dev)
+    for r0 in range(0, T, chunk):
+        n = min(chunk, T - r0)
+        W.logits_device(w, tmp, row0=r0, nrows=n)
+        shard[r0:r0 + n] = tmp[:n, rank * vs:(rank + 1) * vs]
+    del tmp
+    targets = torch.from_numpy(tgt).to(dev)
+    dmask = torch.from_numpy(mask).to(dev)
+    dg = torch.from_numpy(g).to(dev)
+    dl = torch.empty_like(shard)
+    c = rlk.Contract(T=T, V_real=Vr, V_padded=Vp, num_tiles=w.num_tiles, virtual_tp=ws,
+                     mask_mode=rlk.MASK_EXPLICIT, validate=0)
+    layer = VocabParallelLogp(c)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        logp, lse = layer.forward(shard, targets, dmask)
+        rlk.shard_bwd(c, rank, shard, targets, dmask, lse, dg, dlogits=dl)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    torch.distributed.barrier()
+    total_ms, per_ms, clk = timed(step, args.steps, 0, stream, local, per_launch=False)
+    torch.distributed.barrier()
+    total_ms = max_over_ranks(total_ms, dev)
+    ms = total_ms / args.steps
+    hbm_peak, _, kind = measured_peaks()
+    n_active = int((mask != 0).sum())
+    vr_l = min(max(Vr - rank * vs, 0), vs)
+    alg = T * 2 * vr_l + n_active * 2 * vr_l + T * 2 * vs  # shard read by the forward, active rows again, dlogits
+    return {
+        "metric": METRIC, "value": T / (ms * 1e-3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "strong",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded counter-based generator; no dataset)",
+        "config": {"workload": f"grpo: vocabulary-parallel fwd+bwd, T={T} x V_padded={Vp} over {ws} GPUs "
+                               f"({vs} columns each), 64 tiles",
+                   "parallelism": f"tp{ws} (all-gather of [T, {64 // ws}, 2] partials + [T] target logits)",
+                   "l2": "inputs larger than L2; no flush"},
+        "roofline": {"bound": "hbm", "achieved": alg / (ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": alg / (ms * 1e-3) / 1e9 / hbm_peak, "traffic": None,
+                     "peak_source": f"{kind} hbm_gbs", "kernel": "rank 0: shard fwd + fold + shard bwd (whole step)"},
+        "clocks": clk, "gpu_launches": 5 * args.steps,
+    }
+
+
+def lmhead_bench(rlk, args, dev, clock_index, steps=10, warmup=3, rows=0, bwd=True):
     """The fused lm_head: hidden [8192, 4096] x W [152576, 4096], 64 tiles; forward, then forward+backward."""
     import numpy as np
     import torch
@@ -332,88 +447,84 @@ def lmhead_bench(rlk, args, dev, steps=10, warmup=3, rows=0):
     mask = torch.from_numpy(W.active_mask(w)[:T]).to(dev)
     c = rlk.Contract(T=T, V_real=Vr, V_padded=Vp, num_tiles=w.num_tiles, virtual_tp=args.vtp, validate=0)
     rlk.check(rlk.rlk_logp_check_contract(c))
-    ws = torch.empty(rlk.rlk_logp_lmhead_workspace_size(c, H), dtype=torch.uint8, device=dev)
-    for _ in range(warmup):
-        rlk.logp_fused_lmhead(c, hd, wd, tgt, mask, workspace=ws)
+    wsb = torch.empty(rlk.rlk_logp_lmhead_workspace_size(c, H), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        rlk.logp_fused_lmhead(c, hd, wd, tgt, mask, workspace=ws)
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
     flop = 2.0 * T * Vp * H
     _, bf16_peak, kind = measured_peaks()
+    peak_src = f"{kind} bf16_tflops (MEASURED_PEAKS.json cuBLAS burst)"
+    _, ms, clk = timed(lambda: rlk.logp_fused_lmhead(c, hd, wd, tgt, mask, workspace=wsb), steps, warmup, stream,
+                       clock_index)
     tflops = flop / (ms * 1e-3) / 1e12
     out = {"workload": f"lmhead fwd: hidden [{T},{H}] x W [{Vp},{H}] BF16, 64 tiles, virtual TP {args.vtp}",
-           "ms": ms, "tokens_per_s": T / (ms * 1e-3), "tflops": tflops,
+           "ms": ms, "tokens_per_s": T / (ms * 1e-3), "tflops": tflops, "clocks": clk, "launches_per_step": 2,
            "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s",
-                        "frac": tflops / bf16_peak, "peak_source": f"{kind} bf16_tflops (cuBLAS burst)"}}
+                        "frac": tflops / bf16_peak, "peak_source": peak_src,
+                        "kernel": "lmhead_kernel<kEpiPartials> + lmhead_fold_kernel"}}
+    if not bwd:
+        return out
     # forward + backward: GEMM, recompute GEMM with the dlogits epilogue, dHidden and dW GEMMs
     g = torch.from_numpy(W.grad(w, W.active_rows(w))[:T].astype(np.float32)).to(dev)
-    wsb = torch.empty(rlk.rlk_logp_lmhead_workspace_size(c, H), dtype=torch.uint8, device=dev)
-    for _ in range(warmup):
-        rlk.logp_fused_lmhead(c, hd, wd, tgt, mask, grad=g, workspace=wsb)
-    a.record(stream)
-    for _ in range(steps):
-        rlk.logp_fused_lmhead(c, hd, wd, tgt, mask, grad=g, workspace=wsb)
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms_b = a.elapsed_time(b) / steps
-    tf_b = 4 * flop / (ms_b * 1e-3) / 1e12
-    out["fwd_bwd"] = {"ms": ms_b, "tokens_per_s": T / (ms_b * 1e-3), "tflops_executed": tf_b,
-                      "frac_executed": tf_b / bf16_peak,
-                      "note": "4 x 2*T*V_padded*H executed: forward, recompute with dlogits, dHidden, dW"}
-    return out
+    dh = torch.empty_like(hd)
+    dw = torch.empty_like(wd)
+
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+
+    def fb():
+        rlk.check(rlk.rlk_logp_fused_lmhead(c, hd.data_ptr(), H, wd.data_ptr(), tgt.data_ptr(), mask.data_ptr(),
+                                            g.data_ptr(), logp.data_ptr(), lse.data_ptr(), dh.data_ptr(), None,
+                                            dw.data_ptr(), wsb.data_ptr(), stream.cuda_stream))
+    _, ms_b, clk_b = timed(fb, steps, warmup, stream, clock_index)
+    tf_exec = 4 * flop / (ms_b * 1e-3) / 1e12
+    tf_alg = 3 * flop / (ms_b * 1e-3) / 1e12
+    bwd_res = {"ms": ms_b, "tokens_per_s": T / (ms_b * 1e-3), "tflops_executed": tf_exec,
+               "tflops_algorithmic": tf_alg, "clocks": clk_b, "launches_per_step": 4,
+               "roofline": {"bound": "tensor", "achieved": tf_exec, "peak": bf16_peak, "unit": "TFLOP/s",
+                            "frac": tf_exec / bf16_peak, "peak_source": peak_src,
+                            "kernel": "lmhead_kernel x2 + lmhead_fold_kernel + lmhead_grad_kernel"},
+               "note": "executed = 4 x 2*T*V_padded*H (forward, recompute with the dlogits epilogue, dHidden, dW); "
+                       "algorithmic = 3 x (the recompute is overhead)"}
+    if rows == 0 and args.path == "fused":
+        out["fwd_bwd"] = bwd_res
+        return out
+    return {**bwd_res, "workload": out["workload"].replace("lmhead fwd", "lmhead fwd+bwd"),
+            "tflops": tf_exec, "fwd": {k: out[k] for k in ("ms", "tflops", "roofline", "clocks")}}
 
 
-def extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, Vp, args):
+def extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, Vp, args, clock_index):
+    """The other paths on the same batch, each timed like the headline (events on the launching stream,
+    warm-up first, a clock record of its own)."""
     import torch
     out = {}
     stream = torch.cuda.current_stream()
+    hbm_peak, _, kind = measured_peaks()
+
+    def entry(ms, alg_bytes, clk, kernel):
+        gbs = alg_bytes / (ms * 1e-3) / 1e9
+        return {"ms": ms, "tokens_per_s": T / (ms * 1e-3), "alg_gbs": gbs, "frac": gbs / hbm_peak,
+                "peak_source": f"{kind} hbm_gbs", "kernel": kernel, "clocks": clk}
+
     for name, vtp in (("fwd_vtp1", 1), ("fwd_vtp8", 8)):
         cf = c.replace(virtual_tp=vtp)
-        for _ in range(3):
-            rlk.logp_fwd(cf, logits, targets, dmask, out=(logp, lse))
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.steps):
-            rlk.logp_fwd(cf, logits, targets, dmask, out=(logp, lse))
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / args.steps
-        out[name] = {"ms": ms, "tokens_per_s": T / ms * 1e3, "alg_gbs": T * (2 * Vr + 17) / ms / 1e6}
+        _, ms, clk = timed(lambda: rlk.logp_fwd(cf, logits, targets, dmask, out=(logp, lse)), args.steps, 3, stream,
+                           clock_index)
+        out[name] = entry(ms, T * (2 * Vr + 17), clk, "stream_kernel<kModeFwd>")
     for name, vtp in (("fused_vtp1", 1), ("fused_vtp4", 4), ("fused_vtp8", 8)):
         cf = c.replace(virtual_tp=vtp)
-        for _ in range(3):
-            rlk.logp_fwd_bwd(cf, logits, targets, dmask, dg, dlogits=dlogits, out=(logp, lse))
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.steps):
-            rlk.logp_fwd_bwd(cf, logits, targets, dmask, dg, dlogits=dlogits, out=(logp, lse))
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / args.steps
-        out[name] = {"ms": ms, "tokens_per_s": T / ms * 1e3, "alg_gbs": T * (2 * Vr + 2 * Vp + 21) / ms / 1e6}
+        _, ms, clk = timed(lambda: rlk.logp_fwd_bwd(cf, logits, targets, dmask, dg, dlogits=dlogits, out=(logp, lse)),
+                           args.steps, 3, stream, clock_index)
+        out[name] = entry(ms, T * (2 * Vr + 2 * Vp + 21), clk, "stream_kernel<kModeFusedL2>")
     # the forward with the entropy of each row (one pass; one more FMA per pair of logits)
     cf = c.replace(virtual_tp=1)
     ent = torch.empty(T, dtype=torch.float32, device=logits.device)
     ws_e = rlk.workspace_for(cf, logits.device, stream)
-    for _ in range(3):
+
+    def fwd_ent():
         rlk.check(rlk.rlk_logp_fwd_entropy(cf, logits.data_ptr(), targets.data_ptr(), dmask.data_ptr(),
                                            logp.data_ptr(), lse.data_ptr(), ent.data_ptr(), ws_e.data_ptr(),
                                            stream.cuda_stream))
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(args.steps):
-        rlk.check(rlk.rlk_logp_fwd_entropy(cf, logits.data_ptr(), targets.data_ptr(), dmask.data_ptr(),
-                                           logp.data_ptr(), lse.data_ptr(), ent.data_ptr(), ws_e.data_ptr(),
-                                           stream.cuda_stream))
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / args.steps
-    out["fwd_entropy_vtp1"] = {"ms": ms, "tokens_per_s": T / ms * 1e3, "alg_gbs": T * (2 * Vr + 21) / ms / 1e6}
+    _, ms, clk = timed(fwd_ent, args.steps, 3, stream, clock_index)
+    out["fwd_entropy_vtp1"] = entry(ms, T * (2 * Vr + 21), clk, "stream_kernel<kModeFwd, ENT>")
     # the GRPO loss and g from this batch's logp (reads logp, A, mask, ref; writes g: 17 B per row)
     ref = logp + 0.01
     loss, gl, cnt = (torch.empty(1, dtype=torch.float32, device=logits.device),
@@ -423,31 +534,12 @@ def extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, V
     def grpo():
         rlk.check(rlk.rlk_grpo_loss(T, logp.data_ptr(), dg.data_ptr(), dmask.data_ptr(), ref.data_ptr(), 0.01,
                                     loss.data_ptr(), gl.data_ptr(), cnt.data_ptr(), stream.cuda_stream))
-    for _ in range(3):
-        grpo()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(args.steps):
-        grpo()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / args.steps
-    out["grpo_loss"] = {"ms": ms, "tokens_per_s": T / ms * 1e3, "alg_gbs": T * 17 / ms / 1e6}
-    out["lmhead_fwd"] = lmhead_bench(rlk, args, logits.device)
-    # split path: fwd then bwd with lse_in
-    cf = c.replace(virtual_tp=1)
-    for _ in range(3):
-        rlk.logp_fwd(cf, logits, targets, dmask, out=(logp, lse))
-        rlk.logp_bwd(cf, logits, targets, dmask, lse, dg, dlogits=dlogits)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(args.steps):
-        rlk.logp_fwd(cf, logits, targets, dmask, out=(logp, lse))
-        rlk.logp_bwd(cf, logits, targets, dmask, lse, dg, dlogits=dlogits)
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / args.steps
-    out["split_fwd_then_bwd"] = {"ms": ms, "tokens_per_s": T / ms * 1e3}
+    _, ms, clk = timed(grpo, args.steps, 3, stream, clock_index)
+    out["grpo_loss"] = {"ms": ms, "tokens_per_s": T / ms * 1e3, "alg_gbs": T * 17 / ms / 1e6, "clocks": clk,
+                        "note": "latency- and launch-bound (1.1 MB)"}
+    lm = lmhead_bench(rlk, args, logits.device, clock_index, steps=max(5, min(args.steps, 10)), warmup=3)
+    out["lmhead_fwd_bwd"] = lm.pop("fwd_bwd")
+    out["lmhead_fwd"] = lm
     return out
 
 
@@ -456,7 +548,7 @@ def e2e(rlk, c, w, logits_dev, tgt, mask, g, dev, args):
     device (row chunks on a copy stream, overlapped with the previous chunk's fused call) and the
     logp / LSE back."""
     import torch
-    T = w.T
+    T = c.T
     h_logits = torch.empty(tuple(logits_dev.shape), dtype=torch.int16, pin_memory=True)
     h_logits.copy_(logits_dev, non_blocking=False)
     h_tgt = torch.from_numpy(tgt).pin_memory()
@@ -492,20 +584,22 @@ def e2e(rlk, c, w, logits_dev, tgt, mask, g, dev, args):
 def main():
     args = parse()
     ws, rank, local = dist_env()
+    cores = cpu_threads()
     if args.impl == "reference":
         if rank != 0:
             return
-        from synth import workloads as W
         t0 = time.perf_counter()
         per_step = []
         sample_desc = None
         steps = max(1, args.steps)
         budget = max(0.5, args.ref_seconds / (steps + args.warmup))
-        for i in range(args.warmup + steps):
-            tps, rows, secs = time_oracle(W.GRPO, budget_s=budget, max_rows=4096)
-            if i >= args.warmup:
-                per_step.append(tps)
-            sample_desc = f"{rows} seeded rows of the grpo workload (fwd LSE/logp + dlogits), {secs:.1f} s"
+        with oracle_pool(cores) as pool:
+            for i in range(args.warmup + steps):
+                tps, rows, secs = time_oracle(pool, budget, cores, max_rows_per_core=4096)
+                if i >= args.warmup:
+                    per_step.append(tps)
+                sample_desc = (f"{rows} seeded rows of the grpo workload (fwd LSE/logp + dlogits) over {cores} "
+                               f"processes, {secs:.1f} s of oracle time each")
         value = statistics.mean(per_step)
         line = {
             "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
@@ -513,25 +607,28 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded counter-based generator)",
             "config": {"workload": "grpo: fused fwd+bwd, T=65536 x V_padded=152576 (V_real=151936), 64 tiles"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample_desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample_desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": time.perf_counter() - t0,
         }
         print(json.dumps(line))
         return
 
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        # the oracle's pool is spawned before the first CUDA call of this process
+        with oracle_pool(cores) as pool:
+            tps, rows, secs = time_oracle(pool, args.cpu_seconds, cores)
+        cpu = {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{rows} seeded rows of the grpo workload, FP64 numpy oracle (fwd LSE/logp + dlogits), "
+                         f"one spawned process per core, {secs:.1f} s of oracle time each"}
     import torch
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     result = run_ours(args, ws, rank, local)
-    if rank == 0 and not args.no_cpu:
-        from synth import workloads as W
-        tps, rows, secs = time_oracle(W.GRPO, budget_s=15.0, max_rows=8192)
-        result["cpu_baseline"] = {"value": tps, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                  "sample": f"{rows} seeded rows of the grpo workload, FP64 numpy oracle "
-                                            f"(fwd LSE/logp + dlogits), {secs:.1f} s of CPU time; "
-                                            f"host has {cpu_threads()} cores"}
+    if cpu is not None:
+        result["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(result))
     if ws > 1:

@@ -406,3 +406,52 @@ def logp_fused_lmhead(contract, hidden, weight, targets, mask=None, grad=None, s
         return logp, lse
     dw = {"bf16": dwb, "f32": dwf, "both": (dwf, dwb)}[dweight_dtype]
     return logp, lse, dh, dw
+
+
+# ------------------------------------------------------------------ vocabulary shards (one rank's calls)
+
+def shard_workspace(contract, device):
+    import torch
+    n = rlk_logp_shard_workspace_size(contract)
+    if n == 0:
+        check(rlk_logp_check_shard_contract(contract, 0) or RLK_ERR_INVALID_ARG)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def shard_fwd(contract, shard, logits_shard, targets, mask=None, stream=None, workspace=None):
+    """(partials [T, num_tiles/tp, 2], target_logit [T]) of one vocabulary shard (GPU tensors)."""
+    import torch
+    dev = logits_shard.device
+    T = contract.T
+    part = torch.empty((T, contract.num_tiles // contract.virtual_tp, 2), dtype=torch.float32, device=dev)
+    xt = torch.empty(T, dtype=torch.float32, device=dev)
+    ws = workspace if workspace is not None else shard_workspace(contract, dev)
+    check(rlk_logp_shard_fwd(contract, shard, _ptr(logits_shard), _ptr(targets), _ptr(mask), _ptr(part), _ptr(xt),
+                             _ptr(ws), _stream(stream)))
+    return part, xt
+
+
+def fold_gathered(contract, gathered_partials, gathered_target_logit, targets, mask=None, stream=None,
+                  workspace=None):
+    """(logp, lse) from every shard's partials [tp, T, num_tiles/tp, 2] and target logits [tp, T]."""
+    import torch
+    dev = gathered_partials.device
+    T = contract.T
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    ws = workspace if workspace is not None else shard_workspace(contract, dev)
+    check(rlk_logp_fold(contract, _ptr(gathered_partials), _ptr(gathered_target_logit), _ptr(targets), _ptr(mask),
+                        _ptr(logp), _ptr(lse), _ptr(ws), _stream(stream)))
+    return logp, lse
+
+
+def shard_bwd(contract, shard, logits_shard, targets, mask, lse, grad, dlogits=None, stream=None, workspace=None):
+    """BF16 dlogits of one vocabulary shard [T, row_stride] (columns [0, V_padded/tp) written)."""
+    import torch
+    dev = logits_shard.device
+    if dlogits is None:
+        dlogits = torch.empty_like(logits_shard)
+    ws = workspace if workspace is not None else shard_workspace(contract, dev)
+    check(rlk_logp_shard_bwd(contract, shard, _ptr(logits_shard), _ptr(targets), _ptr(mask), _ptr(lse), _ptr(grad),
+                             _ptr(dlogits), _ptr(ws), _stream(stream)))
+    return dlogits
