@@ -623,15 +623,20 @@ def main():
                "sample": f"{rows} seeded rows of the grpo workload, FP64 numpy oracle (fwd LSE/logp + dlogits), "
                          f"one spawned process per core, {secs:.1f} s of oracle time each"}
     import torch
-    if ws > 1:
+    if ws > 1 or args.split == "vocab":
         import torch.distributed as dist
+        if ws == 1:  # a one-rank group: the vocabulary-parallel path with tp = 1
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            os.environ.setdefault("MASTER_PORT", "29517")
+            os.environ.setdefault("RANK", "0")
+            os.environ.setdefault("WORLD_SIZE", "1")
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     result = run_ours(args, ws, rank, local)
     if cpu is not None:
         result["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(result))
-    if ws > 1:
+    if torch.distributed.is_initialized():
         torch.distributed.destroy_process_group()
 
 

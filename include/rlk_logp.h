@@ -243,6 +243,23 @@ rlk_status rlk_logp_fused_lmhead(const rlk_logp_contract* contract, const void* 
                                  float* dweight_f32, void* dweight_bf16, void* workspace, rlk_stream_t stream);
 
 /*
+ * The fused lm_head backward alone, from the LSE an earlier forward returned
+ * (rlk_logp_fused_lmhead without grad_logp): the recompute GEMM writes
+ * dlogits = g (onehot - exp(x - lse_in)) in BF16, then the dHidden and dW
+ * GEMMs run, exactly as in rlk_logp_fused_lmhead with grad_logp (so the
+ * outputs are bitwise those of that call when lse_in is its LSE).  It skips
+ * the forward GEMM: an autograd backward costs three GEMM passes, not four.
+ *   lse_in      [T] FP32; grad_logp [T] FP32; the other arguments and
+ *               outputs as for rlk_logp_fused_lmhead.
+ * Device status (validate == 1): an active target outside [0, V_real), a
+ * non-finite lse_in on an active row.
+ */
+rlk_status rlk_logp_fused_lmhead_bwd(const rlk_logp_contract* contract, const void* hidden_bf16, int64_t H,
+                                     const void* weight_bf16, const int64_t* targets, const uint8_t* active_mask,
+                                     const float* lse_in, const float* grad_logp, void* dhidden_bf16,
+                                     float* dweight_f32, void* dweight_bf16, void* workspace, rlk_stream_t stream);
+
+/*
  * Vocabulary-parallel tensor parallelism across GPUs (PR #289 "[WS2][PR4]
  * [Logp] feat: add distributed TP/CP logprob drift report", PR-1 contract
  * commit: tile-aligned vocabulary shards, FP32 (max, sumexp) partials moved by

@@ -49,3 +49,45 @@ def test_autograd_matches_the_c_entry_points(explicit, vtp):
     check_fwd(bits, tgt, active, v_real, logp.detach().cpu().numpy(), lse.cpu().numpy())
     check_dlogits(bits, tgt, active, np.where(active, w, 0).astype(np.float32), v_real, v_padded,
                   grad_bits.cpu().numpy().view(np.uint16))
+
+
+def test_lmhead_autograd_matches_the_c_entry_points_and_the_oracle():
+    """FusedLmHeadLogprob: forward = rlk_logp_fused_lmhead, backward = rlk_logp_fused_lmhead_bwd from
+    the saved LSE; the gradients of sum(w * logp) are bitwise those of the fused call with
+    grad_logp = w, and within the BF16 bound of the FP64 oracle's."""
+    import oracle
+    from vocab_selected_token_tile_gb300.autograd import lmhead_logprob
+    T, H, v_real, v_padded, nt = 130, 128, 600, 608, 2
+    hb = synth.normal_bf16_host(0, T, H, 41, synth.STREAM_HIDDEN, 1.0)
+    wb = synth.normal_bf16_host(0, v_padded, H, 41, synth.STREAM_WEIGHT, 0.2)
+    tgt = synth.targets(T, v_real, seed=41)
+    mask = (np.arange(T) % 5 != 0).astype(np.uint8)
+    w = np.random.default_rng(41).standard_normal(T).astype(np.float32)
+    h = torch.from_numpy(hb.view(np.int16)).cuda().view(torch.bfloat16).requires_grad_(True)
+    W = torch.from_numpy(wb.view(np.int16)).cuda().view(torch.bfloat16).requires_grad_(True)
+    dt, dm = torch.from_numpy(tgt).cuda(), torch.from_numpy(mask).cuda()
+    logp, lse = lmhead_logprob(h, W, dt, dm, v_real=v_real, num_tiles=nt)
+    (logp * torch.from_numpy(w).cuda()).sum().backward()
+    torch.cuda.synchronize()
+    c = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=nt, virtual_tp=1)
+    ref = rlk.logp_fused_lmhead(c, h.detach(), W.detach(), dt, dm,
+                                grad=torch.from_numpy(np.where(mask != 0, w, 0).astype(np.float32)).cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(logp.detach(), ref[0]) and torch.equal(lse, ref[1])
+    assert torch.equal(h.grad, ref[2]) and torch.equal(W.grad, ref[3])
+    from oracle.lmhead import lmhead_dlogits
+    act = mask != 0
+    gw = np.where(act, w, 0.0)
+    ref_logp, ref_lse, x = oracle.lmhead_forward(hb, wb, tgt, act, v_real)
+    assert np.max(np.abs(logp.detach().cpu().numpy() - ref_logp)) <= 1e-4
+    dh_ref, dw_ref = oracle.lmhead_grads(hb, wb, tgt, act, gw, v_real)
+    # BF16 dlogits (one rounding) summed in FP32, then one BF16 rounding of the result:
+    # |err| <= 2^-8 (|ref| + sum |dlogits| |operand|)
+    d = np.abs(lmhead_dlogits(x, ref_lse, tgt, act, gw))
+    sc_dh = d @ np.abs(oracle.bf16_bits_to_f64(wb[:v_real]))
+    sc_dw = d.T @ np.abs(oracle.bf16_bits_to_f64(hb))
+    got_dh = h.grad.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got_dh - dh_ref) <= 2.0 ** -8 * (np.abs(dh_ref) + sc_dh) + 1e-30)
+    got_dw = W.grad.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got_dw[:v_real] - dw_ref[:v_real]) <= 2.0 ** -8 * (np.abs(dw_ref[:v_real]) + sc_dw) + 1e-30)
+    assert np.all(got_dw[v_real:] == 0.0)

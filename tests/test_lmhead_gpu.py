@@ -266,3 +266,32 @@ def test_lmhead_fp32_dweight(case):
     assert np.all(f[v_real:] == 0.0) and not np.any(np.signbit(f[v_real:]))
     assert np.array_equal(bf16_rn_bits(dwf.cpu().numpy()), dwb.cpu().numpy().view(np.uint16))
     assert np.all(within(dh.cpu().numpy().view(np.uint16), ref_dh, sc_dh))
+
+
+@pytest.mark.parametrize("case", [CASES[1], CASES[4]], ids=lambda c: "T%d_H%d_V%d_P%d_NT%d" % c)
+def test_lmhead_backward_from_a_given_lse_is_bitwise_the_fused_call(case):
+    """rlk_logp_fused_lmhead_bwd (recompute + gradient GEMMs from the forward's LSE) gives bitwise
+    the gradients of rlk_logp_fused_lmhead with grad_logp; an out-of-range active target and a
+    non-finite LSE on an active row are reported."""
+    T, H, v_real, v_padded, nt = case
+    hb, wb = make(T, H, v_real, v_padded, seed=5 * T + H)
+    tgt = synth.targets(T, v_real, seed=T + 9)
+    mask = (np.arange(T) % 6 != 4).astype(np.uint8)
+    g = np.where(mask != 0, np.random.default_rng(T + 2).standard_normal(T), 0.0).astype(np.float32)
+    c = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=nt, virtual_tp=1, validate=1)
+    dh_, dw_ = dev(hb), dev(wb)
+    dt, dm, dg = torch.from_numpy(tgt).cuda(), torch.from_numpy(mask).cuda(), torch.from_numpy(g).cuda()
+    logp, lse, dh, dw = rlk.logp_fused_lmhead(c, dh_, dw_, dt, dm, grad=dg, dweight_dtype="both")
+    dh2, dw2 = rlk.logp_fused_lmhead_bwd(c, dh_, dw_, dt, dm, lse, dg, dweight_dtype="both")
+    torch.cuda.synchronize()
+    assert torch.equal(dh, dh2) and torch.equal(dw[0], dw2[0]) and torch.equal(dw[1], dw2[1])
+    bad = dt.clone()
+    bad[int(np.nonzero(mask)[0][0])] = v_real + 1
+    with pytest.raises(rlk.RlkError) as ei:
+        rlk.logp_fused_lmhead_bwd(c, dh_, dw_, bad, dm, lse, dg)
+    assert ei.value.status == rlk.RLK_ERR_TARGET_RANGE
+    l2 = lse.clone()
+    l2[int(np.nonzero(mask)[0][1])] = float("inf")
+    with pytest.raises(rlk.RlkError) as ei:
+        rlk.logp_fused_lmhead_bwd(c, dh_, dw_, dt, dm, l2, dg)
+    assert ei.value.status == rlk.RLK_ERR_NONFINITE_LSE

@@ -35,6 +35,7 @@ EXPORTED = (
     "rlk_grpo_loss",
     "rlk_logp_lmhead_workspace_size",
     "rlk_logp_fused_lmhead",
+    "rlk_logp_fused_lmhead_bwd",
     "rlk_logp_check_shard_contract",
     "rlk_logp_shard_workspace_size",
     "rlk_logp_shard_fwd",
@@ -103,6 +104,8 @@ def library():
         lib.rlk_logp_lmhead_workspace_size.restype = ctypes.c_size_t
         lib.rlk_logp_fused_lmhead.argtypes = [P, vp, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.rlk_logp_fused_lmhead.restype = i
+        lib.rlk_logp_fused_lmhead_bwd.argtypes = [P, vp, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.rlk_logp_fused_lmhead_bwd.restype = i
         lib.rlk_logp_fwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp]
         lib.rlk_logp_fwd_noalloc.restype = i
         lib.rlk_logp_fwd_entropy.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -161,6 +164,13 @@ def rlk_logp_fused_lmhead(contract, hidden, H, weight, targets, active_mask, gra
     return library().rlk_logp_fused_lmhead(ctypes.byref(contract), hidden, H, weight, targets, active_mask,
                                            grad_logp, logp, lse, dhidden, dweight_f32, dweight_bf16, workspace,
                                            stream)
+
+
+def rlk_logp_fused_lmhead_bwd(contract, hidden, H, weight, targets, active_mask, lse_in, grad_logp, dhidden,
+                              dweight_f32, dweight_bf16, workspace, stream):
+    return library().rlk_logp_fused_lmhead_bwd(ctypes.byref(contract), hidden, H, weight, targets, active_mask,
+                                               lse_in, grad_logp, dhidden, dweight_f32, dweight_bf16, workspace,
+                                               stream)
 
 
 def rlk_logp_fwd_entropy(contract, logits, targets, active_mask, logp, lse, entropy, workspace, stream):
@@ -406,6 +416,27 @@ def logp_fused_lmhead(contract, hidden, weight, targets, mask=None, grad=None, s
         return logp, lse
     dw = {"bf16": dwb, "f32": dwf, "both": (dwf, dwb)}[dweight_dtype]
     return logp, lse, dh, dw
+
+
+def logp_fused_lmhead_bwd(contract, hidden, weight, targets, mask, lse, grad, stream=None, workspace=None,
+                          dweight_dtype="bf16"):
+    """(dhidden [T, H] BF16, dweight [V_padded, H]) from the forward's LSE; ``dweight_dtype`` as for
+    logp_fused_lmhead."""
+    import torch
+    dev = hidden.device
+    T, H = hidden.shape
+    if dweight_dtype not in ("bf16", "f32", "both"):
+        raise ValueError("dweight_dtype must be bf16, f32 or both")
+    dh = torch.empty_like(hidden)
+    dwf = torch.empty(weight.shape, dtype=torch.float32, device=dev) if dweight_dtype in ("f32", "both") else None
+    dwb = torch.empty_like(weight) if dweight_dtype in ("bf16", "both") else None
+    n = rlk_logp_lmhead_workspace_size(contract, H)
+    if n == 0:
+        check(rlk_logp_check_contract(contract) or RLK_ERR_UNSUPPORTED)
+    ws = workspace if workspace is not None else torch.empty(n, dtype=torch.uint8, device=dev)
+    check(rlk_logp_fused_lmhead_bwd(contract, _ptr(hidden), H, _ptr(weight), _ptr(targets), _ptr(mask), _ptr(lse),
+                                    _ptr(grad), _ptr(dh), _ptr(dwf), _ptr(dwb), _ptr(ws), _stream(stream)))
+    return dh, {"bf16": dwb, "f32": dwf, "both": (dwf, dwb)}[dweight_dtype]
 
 
 # ------------------------------------------------------------------ vocabulary shards (one rank's calls)

@@ -65,6 +65,16 @@ constexpr uint32_t kStageB = kBN * kBK * 2;
 constexpr uint32_t kMnBlock = 64 * kBK * 2;  // one 64-wide block of an MN-major stage: 64 K rows x 128 B
 constexpr uint64_t kDrainNsLm = 1000000000ull;
 constexpr int kMaxGroups = 8;
+// Unit order of the logits GEMMs: bands of 32 token blocks (32 MB of hidden at H = 4096), tile-major
+// within a band, hidden loaded with an L2 evict-last policy.  Measured at 8192 x 4096 x 152576
+// (DRAM reads of the forward GEMM, its time): one band of 64 blocks 8.9 GB, 6.03 ms; bands of 32
+// 3.9 GB, 5.88 ms; of 16 6.0 GB, 6.00 ms; of 8 10.6 GB, 6.19 ms; 32 with the hint 3.75 GB,
+// 5.88 ms and the recompute GEMM 6.19 ms against 6.60.
+constexpr int kBandBlocks = 32;  // token blocks per band of the logits GEMMs' unit order
+constexpr int kKeepHidden = 1;   // 1: the logits GEMMs load hidden with an L2 evict-last policy
+// Tile order of the gradient GEMMs: bands of kBandN 256-wide H blocks, M-major within a band.
+constexpr int kBandN = 16;
+constexpr int kKeepB1 = 0;  // 1: dW's B operand (hidden) loaded with an L2 evict-last policy
 // Workspace: 256 bytes of tickets (three launches x kMaxGroups 64-bit counters).
 constexpr size_t kTicketBytes = 256;
 
@@ -172,14 +182,16 @@ struct LmParams {
     WaitCtl w;
     int64_t T, Vr, Vp, ignore_index;
     int32_t K, NT, W, vtp, nchunk, rem, mask_mode;
-    int32_t MB;  // token blocks
+    int32_t MB;   // token blocks
+    int32_t MBg;  // token blocks per band of the unit order (unit_coords)
+    int32_t keep_hidden;  // hidden tiles loaded with an L2 evict-last policy
 };
 
 // Virtual-TP group of this CTA: group j takes tickets for units
 // [0, NT/vtp * MB) of shard j, tile-major (unit u = tile j*NT/vtp + u / MB,
 // token block u % MB).
 struct Group {
-    int j, tile0;
+    int j, tile0, ntl;
     int64_t end;
 };
 
@@ -187,10 +199,29 @@ __device__ Group group_of(const LmParams& p) {
     const int Gj = (int)gridDim.x / p.vtp;
     Group g;
     g.j = (int)blockIdx.x / Gj;
-    const int ntl = p.NT / p.vtp;
-    g.tile0 = g.j * ntl;
-    g.end = (int64_t)ntl * p.MB;
+    g.ntl = p.NT / p.vtp;
+    g.tile0 = g.j * g.ntl;
+    g.end = (int64_t)g.ntl * p.MB;
     return g;
+}
+
+// Unit u of a group: token blocks are taken in bands of p.MBg blocks; within
+// a band the order is tile-major, so the units in flight share few weight
+// tiles (the band's blocks of one tile run together) and few hidden blocks
+// (one band).  The last band may be narrower.
+__device__ __forceinline__ void unit_coords(const LmParams& p, const Group& g, int64_t u, int& tile, int& mb) {
+    const int64_t band_units = (int64_t)g.ntl * p.MBg;
+    const int64_t full = p.MB / p.MBg;
+    if (u < full * band_units) {
+        const int64_t b = u / band_units, r = u % band_units;
+        tile = g.tile0 + (int)(r / p.MBg);
+        mb = (int)(b * p.MBg + r % p.MBg);
+    } else {
+        const int64_t r = u - full * band_units;
+        const int w = p.MB - (int)full * p.MBg;
+        tile = g.tile0 + (int)(r / w);
+        mb = (int)(full * p.MBg + r % w);
+    }
 }
 
 // One 32-column block of a row's logits into the running partial of its
@@ -277,12 +308,13 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             uint32_t phase = 0;
             int64_t issued = 0, n = 0;
             bool aborted = false;
+            const uint64_t keep = l2_policy_evict_last();
             while (!aborted) {
                 int64_t u = (int64_t)atomicAdd(&p.tickets[grp.j], 1ull);
                 if (u >= grp.end) u = -1;
                 if (!unit_put(bars, n++, u, p.w) || u < 0) break;
-                const int tile = grp.tile0 + (int)(u / p.MB);
-                const int mb = (int)(u % p.MB);
+                int tile, mb;
+                unit_coords(p, grp, u, tile, mb);
                 for (int ch = 0; ch < p.nchunk && !aborted; ++ch) {
                     const bool last_rem = (ch == p.nchunk - 1) && p.rem;
                     const int nrows = last_rem ? p.rem : kBN;
@@ -294,7 +326,10 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                         }
                         const uint32_t fb = smem_u32(&bars->full[stage]);
                         mbar_arrive_expect_tx(fb, kStageA + (uint32_t)nrows * kBK * 2);
-                        tma_load_2d(smem_u32(sA + stage * kStageA), &tmH, kb * kBK, mb * kBM, fb);
+                        if (p.keep_hidden)
+                            tma_load_2d_hint(smem_u32(sA + stage * kStageA), &tmH, kb * kBK, mb * kBM, fb, keep);
+                        else
+                            tma_load_2d(smem_u32(sA + stage * kStageA), &tmH, kb * kBK, mb * kBM, fb);
                         tma_load_2d(smem_u32(sB + stage * kStageB), last_rem ? &tmWr : &tmW, kb * kBK, n0, fb);
                         ++issued;
                         if (++stage == kStages) {
@@ -369,8 +404,8 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             if (lane == 0) unit_done(bars, n);
             ++n;
             if (u < 0) break;
-            const int tile = grp.tile0 + (int)(u / p.MB);
-            const int mb = (int)(u % p.MB);
+            int tile, mb;
+            unit_coords(p, grp, u, tile, mb);
             const int64_t row = (int64_t)mb * kBM + r_in;
             const bool valid = row < p.T;
             int64_t target = -1;
@@ -385,8 +420,14 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             uint16_t* drow = nullptr;
             if (EPI == kEpiGrad && valid) {
                 g = p.grad[row];
-                nlL = -__fmul_rn(p.lse_in[row], kLog2e);
+                const float l = p.lse_in[row];
+                nlL = -__fmul_rn(l, kLog2e);
                 drow = p.dlogits + row * p.Vp;
+                // the device conditions of a backward given the LSE, reported once per row
+                if (active && tile == grp.tile0 && grp.j == 0) {
+                    if (target < 0 || target >= p.Vr) atomicOr(p.w.status, kStatusTargetRange);
+                    if (!isfinite(l)) atomicOr(p.w.status, kStatusNonFinite);
+                }
             }
             for (int ch = 0; ch < p.nchunk; ++ch, ++chunk) {
                 const int acc = (int)(chunk & 1);
@@ -478,6 +519,8 @@ struct GradParams {
     WaitCtl w;
     int64_t T, Vr, Vp, n0, n1;
     int32_t H, NB, KB0, KB1;  // n-blocks of H; K blocks of problem 0 (V_real) and problem 1 (T)
+    int32_t NBg;              // H blocks per band of the tile order (grad_tile)
+    int32_t keep_b1;          // dW's hidden tiles loaded with an L2 evict-last policy
 };
 
 struct GradTile {
@@ -490,8 +533,20 @@ __device__ __forceinline__ GradTile grad_tile(const GradParams& p, int64_t u) {
     GradTile t;
     t.prob = u < p.n0 ? 0 : 1;
     const int64_t v = t.prob ? u - p.n0 : u;
-    t.mb = v / p.NB;
-    t.nb = (int)(v % p.NB);
+    // bands of p.NBg H blocks: M-major within a band (the band's H blocks of one M block run together)
+    const int64_t MBp = (t.prob ? p.n1 : p.n0) / p.NB;
+    const int64_t band_tiles = MBp * p.NBg;
+    const int64_t full = p.NB / p.NBg;
+    if (v < full * band_tiles) {
+        const int64_t b = v / band_tiles, r = v % band_tiles;
+        t.mb = r / p.NBg;
+        t.nb = (int)(b * p.NBg + r % p.NBg);
+    } else {
+        const int64_t r = v - full * band_tiles;
+        const int w = p.NB - (int)full * p.NBg;
+        t.mb = r / w;
+        t.nb = (int)(full * p.NBg + r % w);
+    }
     const int left = p.H - t.nb * kBN;
     t.nbox = left >= kBN ? 4 : left / 64;
     t.KB = t.prob ? p.KB1 : p.KB0;
@@ -528,6 +583,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             uint32_t phase = 0;
             int64_t issued = 0, n = 0;
             bool aborted = false;
+            const uint64_t keep = l2_policy_evict_last();
             while (!aborted) {
                 int64_t u = (int64_t)atomicAdd(p.ticket, 1ull);
                 if (u >= total) u = -1;
@@ -552,7 +608,12 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                         // dlogits columns (M) m0.., rows (K) kb*64..; hidden rows (K) kb*64.., columns h
                         tma_load_2d(a, &tmA1, m0, kb * kBK, fb);
                         tma_load_2d(a + kMnBlock, &tmA1, m0 + 64, kb * kBK, fb);
-                        for (int j = 0; j < t.nbox; ++j) tma_load_2d(b + j * kMnBlock, &tmB1, h0 + 64 * j, kb * kBK, fb);
+                        for (int j = 0; j < t.nbox; ++j) {
+                            if (p.keep_b1)
+                                tma_load_2d_hint(b + j * kMnBlock, &tmB1, h0 + 64 * j, kb * kBK, fb, keep);
+                            else
+                                tma_load_2d(b + j * kMnBlock, &tmB1, h0 + 64 * j, kb * kBK, fb);
+                        }
                     }
                     ++issued;
                     if (++stage == kStages) {
@@ -774,6 +835,8 @@ rlk_status prepare(LmLaunch& L, const rlk_logp_contract& c, const void* hidden, 
     p.rem = p.W % kBN;
     p.mask_mode = c.mask_mode;
     p.MB = (int32_t)((c.T + kBM - 1) / kBM);
+    p.MBg = p.MB < kBandBlocks ? p.MB : kBandBlocks;
+    p.keep_hidden = kKeepHidden;
     const uint32_t rrows = p.rem ? (uint32_t)p.rem : (uint32_t)kBN;
     if (!make_map(&L.tmH, hidden, H, c.T, H, kBK, kBM) || !make_map(&L.tmW, weight, H, c.V_padded, H, kBK, kBN) ||
         !make_map(&L.tmWr, weight, H, c.V_padded, H, kBK, rrows))
@@ -838,11 +901,22 @@ rlk_status launch_lmhead_bwd(const rlk_logp_contract& c, const void* hidden, int
                              const int64_t* targets, const uint8_t* mask, const float* grad, float* logp, float* lse,
                              void* dhidden, float* dweight_f32, void* dweight_bf16, void* workspace, uint32_t* status,
                              cudaStream_t stream) {
-    // 1. forward: LSE and logp (clears all three launches' tickets first)
+    // 1. forward: LSE and logp
     rlk_status st = launch_lmhead_fwd(c, hidden, H, weight, targets, mask, logp, lse, workspace, status, stream);
     if (st != RLK_OK) return st;
+    // 2.-3. the backward from that LSE
+    return launch_lmhead_bwd_given_lse(c, hidden, H, weight, targets, mask, grad, lse, dhidden, dweight_f32,
+                                       dweight_bf16, workspace, status, stream);
+}
+
+rlk_status launch_lmhead_bwd_given_lse(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                                       const int64_t* targets, const uint8_t* mask, const float* grad,
+                                       const float* lse, void* dhidden, float* dweight_f32, void* dweight_bf16,
+                                       void* workspace, uint32_t* status, cudaStream_t stream) {
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     unsigned long long* tickets = reinterpret_cast<unsigned long long*>(ws);
+    rlk_status st = clear_tickets(tickets, stream);
+    if (st != RLK_OK) return st;
     uint16_t* dlogits = reinterpret_cast<uint16_t*>(ws + lmhead_fwd_workspace(c));
     // 2. dlogits = g * (onehot - exp(x - LSE)) from the recomputed logits (BF16 [T, V_padded])
     LmLaunch L;
@@ -876,6 +950,8 @@ rlk_status launch_lmhead_bwd(const rlk_logp_contract& c, const void* hidden, int
     g.NB = (int32_t)((H + kBN - 1) / kBN);
     g.KB0 = (int32_t)((c.V_real + kBK - 1) / kBK);
     g.KB1 = (int32_t)((c.T + kBK - 1) / kBK);
+    g.NBg = g.NB < kBandN ? g.NB : kBandN;
+    g.keep_b1 = kKeepB1;
     g.n0 = ((c.T + kBM - 1) / kBM) * g.NB;
     g.n1 = ((c.V_padded + kBM - 1) / kBM) * g.NB;
     const int64_t total = g.n0 + g.n1;

@@ -72,6 +72,11 @@ rlk_status launch_lmhead_bwd(const rlk_logp_contract& c, const void* hidden, int
                              const int64_t* targets, const uint8_t* mask, const float* grad, float* logp, float* lse,
                              void* dhidden, float* dweight_f32, void* dweight_bf16, void* workspace, uint32_t* status,
                              cudaStream_t stream);
+// The backward alone, from a given LSE: recompute GEMM (dlogits), then dHidden and dW.
+rlk_status launch_lmhead_bwd_given_lse(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                                       const int64_t* targets, const uint8_t* mask, const float* grad,
+                                       const float* lse, void* dhidden, float* dweight_f32, void* dweight_bf16,
+                                       void* workspace, uint32_t* status, cudaStream_t stream);
 
 // Vocabulary-parallel pieces (shard.cu).  A shard call's contract describes
 // the whole problem with virtual_tp = the number of shards; shard j holds
