@@ -133,3 +133,36 @@ def test_shard_calls_fail_closed():
     with pytest.raises(rlk.RlkError) as ei:
         rlk.shard_bwd(c, 0, sh, tgt, m, torch.zeros(T, device="cuda"), torch.ones(T, device="cuda"))
     assert ei.value.status == rlk.RLK_ERR_TARGET_RANGE
+
+
+def test_layer_over_a_one_rank_nccl_group():
+    """VocabParallelLogp with a real NCCL group of one rank (tp = 1): the agreement all-reduce and the
+    all-gather run on the GPU, and logp, LSE and dlogits are bitwise those of rlk_logp_fwd / rlk_logp_bwd."""
+    import os
+    import socket
+
+    import torch.distributed as dist
+    from vocab_selected_token_tile_gb300.vocab_parallel import VocabParallelLogp
+    T, vr, vp, nt = 96, 3001, 3072, 64
+    bits = synth.logits_host(0, T, vp, vp, vr, seed=77, sigma=3.0, garbage=True)
+    tgt = synth.targets(T, vr, seed=77)
+    mask = (np.arange(T) % 3 != 0).astype(np.uint8)
+    g = np.where(mask != 0, 0.5, 0.0).astype(np.float32)
+    logits = torch.from_numpy(bits.view(np.int16)).cuda()
+    dt, dm, dg = (torch.from_numpy(a).cuda() for a in (tgt, mask, g))
+    c = rlk.Contract(T=T, V_real=vr, V_padded=vp, num_tiles=nt, virtual_tp=1, validate=1)
+    want_logp, want_lse = rlk.logp_fwd(c, logits, dt, dm)
+    want_dl = rlk.logp_bwd(c, logits, dt, dm, want_lse, dg)
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                            device_id=torch.device("cuda", torch.cuda.current_device()))
+    try:
+        layer = VocabParallelLogp(c)
+        logp, lse = layer.forward(logits, dt, dm)
+        dl = layer.backward(logits, dt, dm, lse, dg)
+        torch.cuda.synchronize()
+    finally:
+        dist.destroy_process_group()
+    assert torch.equal(logp, want_logp) and torch.equal(lse, want_lse) and torch.equal(dl, want_dl)

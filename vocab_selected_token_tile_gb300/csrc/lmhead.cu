@@ -73,8 +73,10 @@ constexpr int kMaxGroups = 8;
 constexpr int kBandBlocks = 32;  // token blocks per band of the logits GEMMs' unit order
 constexpr int kKeepHidden = 1;   // 1: the logits GEMMs load hidden with an L2 evict-last policy
 // Tile order of the gradient GEMMs: bands of kBandN 256-wide H blocks, M-major within a band.
-constexpr int kBandN = 16;
-constexpr int kKeepB1 = 0;  // 1: dW's B operand (hidden) loaded with an L2 evict-last policy
+// Measured at 8192 x 4096 x 152576 (DRAM reads, time of the gradient launch): bands of 16 (no
+// banding at H = 4096) 26.1 GB, 14.12 ms; of 8 16.6 GB, 13.89 ms; of 4 23.5 GB, 13.92 ms.  An L2
+// evict-last hint on dW's hidden loads did not help (16.8 GB at bands of 8).
+constexpr int kBandN = 8;
 // Workspace: 256 bytes of tickets (three launches x kMaxGroups 64-bit counters).
 constexpr size_t kTicketBytes = 256;
 
@@ -520,7 +522,6 @@ struct GradParams {
     int64_t T, Vr, Vp, n0, n1;
     int32_t H, NB, KB0, KB1;  // n-blocks of H; K blocks of problem 0 (V_real) and problem 1 (T)
     int32_t NBg;              // H blocks per band of the tile order (grad_tile)
-    int32_t keep_b1;          // dW's hidden tiles loaded with an L2 evict-last policy
 };
 
 struct GradTile {
@@ -583,7 +584,6 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             uint32_t phase = 0;
             int64_t issued = 0, n = 0;
             bool aborted = false;
-            const uint64_t keep = l2_policy_evict_last();
             while (!aborted) {
                 int64_t u = (int64_t)atomicAdd(p.ticket, 1ull);
                 if (u >= total) u = -1;
@@ -608,12 +608,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                         // dlogits columns (M) m0.., rows (K) kb*64..; hidden rows (K) kb*64.., columns h
                         tma_load_2d(a, &tmA1, m0, kb * kBK, fb);
                         tma_load_2d(a + kMnBlock, &tmA1, m0 + 64, kb * kBK, fb);
-                        for (int j = 0; j < t.nbox; ++j) {
-                            if (p.keep_b1)
-                                tma_load_2d_hint(b + j * kMnBlock, &tmB1, h0 + 64 * j, kb * kBK, fb, keep);
-                            else
-                                tma_load_2d(b + j * kMnBlock, &tmB1, h0 + 64 * j, kb * kBK, fb);
-                        }
+                        for (int j = 0; j < t.nbox; ++j) tma_load_2d(b + j * kMnBlock, &tmB1, h0 + 64 * j, kb * kBK, fb);
                     }
                     ++issued;
                     if (++stage == kStages) {
@@ -951,7 +946,6 @@ rlk_status launch_lmhead_bwd_given_lse(const rlk_logp_contract& c, const void* h
     g.KB0 = (int32_t)((c.V_real + kBK - 1) / kBK);
     g.KB1 = (int32_t)((c.T + kBK - 1) / kBK);
     g.NBg = g.NB < kBandN ? g.NB : kBandN;
-    g.keep_b1 = kKeepB1;
     g.n0 = ((c.T + kBM - 1) / kBM) * g.NB;
     g.n1 = ((c.V_padded + kBM - 1) / kBM) * g.NB;
     const int64_t total = g.n0 + g.n1;
