@@ -372,10 +372,16 @@ def run_ours(args, ws, rank, local):
         "gpu_launches": launches_per_step * args.steps,
     }
     if not args.no_extra and rank == 0 and not args.rows:
-        result["extra"] = extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, Tl, Vr, Vp, args,
-                                      local)
+        try:
+            result["extra"] = extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, Tl, Vr, Vp, args,
+                                          local)
+        except Exception as e:  # the headline stands on its own; say what failed
+            result["extra"] = {"error": f"{type(e).__name__}: {e}"}
     if not args.no_e2e:
-        result["e2e"] = e2e(rlk, c, w, logits, tgt[r0:r1], mask[r0:r1], g[r0:r1], dev, args)
+        try:
+            result["e2e"] = e2e(rlk, c, w, logits, tgt[r0:r1], mask[r0:r1], g[r0:r1], dev, args)
+        except Exception as e:  # reported, not hidden: the line then has no end-to-end number
+            result["e2e"] = {"error": f"{type(e).__name__}: {e}"}
     return result
 
 
