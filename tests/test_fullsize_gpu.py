@@ -104,3 +104,33 @@ def test_grpo_fused_full_size_in_bench_configuration(batch):
     ref = oracle.dlogits(batch["bits"][:8], batch["tgt"][rows[:8]], batch["active"][rows[:8]],
                          batch["g"][rows[:8]], w.v_real, w.v_padded)
     assert np.all(np.abs(ref.sum(axis=1)) <= 1e-9 * (np.abs(batch["g"][rows[:8]]) + 1e-30) * w.v_real)
+
+
+def test_vocabulary_shards_full_size(batch):
+    """The bench's --split vocab configuration emulated on one GPU: 8 column shards of the 65536 x
+    152576 batch (19072 columns each), each through rlk_logp_shard_fwd, the partials stacked as an
+    all-gather leaves them, rlk_logp_fold, then rlk_logp_shard_bwd per shard.  logp, LSE and the
+    shards' dlogits side by side are bitwise the fused step's."""
+    w = batch["w"]
+    tp = 8
+    vs = w.v_padded // tp
+    c = contract(w.T, w.v_real, w.v_padded, w.num_tiles, tp, validate=1)
+    dl, logp, lse = rlk.logp_fwd_bwd(c.replace(virtual_tp=BENCH_VTP), batch["logits"], batch["dt"], batch["dm"],
+                                     batch["dg"])
+    parts, xts = [], []
+    for j in range(tp):
+        sh = batch["logits"][:, j * vs:(j + 1) * vs].contiguous()
+        p, x = rlk.shard_fwd(c, j, sh, batch["dt"], batch["dm"])
+        parts.append(p)
+        xts.append(x)
+        del sh
+    logp_s, lse_s = rlk.fold_gathered(c, torch.stack(parts), torch.stack(xts), batch["dt"], batch["dm"])
+    torch.cuda.synchronize()
+    assert torch.equal(logp_s, logp) and torch.equal(lse_s, lse)
+    del parts, xts
+    for j in range(tp):
+        sh = batch["logits"][:, j * vs:(j + 1) * vs].contiguous()
+        d = rlk.shard_bwd(c, j, sh, batch["dt"], batch["dm"], lse_s, batch["dg"])
+        torch.cuda.synchronize()
+        assert torch.equal(d, dl[:, j * vs:(j + 1) * vs]), j
+        del sh, d
