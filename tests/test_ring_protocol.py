@@ -49,9 +49,7 @@ def ctas_per_sm(mode, vtp, v_padded, nt, sm_count=152, reuse_bytes=64 << 20):
 
 def consumers_for(mode, per_sm):
     """Consumer warps of a CTA, as the kernel instantiates them."""
-    if per_sm == 1:
-        return 16
-    return 8 if mode in ("fused", "fused_l2") else 12
+    return 16 if per_sm == 1 else 12
 
 
 def plan(mode, vtp, v_padded, nt):

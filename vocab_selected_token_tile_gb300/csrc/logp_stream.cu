@@ -62,26 +62,21 @@ namespace rlk {
 namespace {
 
 // Warps of a CTA: NW consumer warps (0 .. NW-1), the fold warp (NW), then the
-// producer warps.  Measured on GB300 (same-box sweeps of 8-30 consumer warps):
+// producer warps.  Measured on GB300 (same-box sweeps of 4-30 consumer warps):
 //  * one CTA per SM: 16 consumer warps, two producers (one thread's bulk-copy
 //    issue rate does not keep up with HBM);
-//  * two CTAs per SM, one producer each: 12 consumer warps for the streaming
-//    modes and 8 for the fused ones -- fewer, fatter warps fit the halved
-//    register budget without spilling (16 spilled and ran up to 40% slower).
+//  * two CTAs per SM, one producer each: 12 consumer warps -- they fit the
+//    halved register budget (72 registers) without spilling; 16 spilled and
+//    ran up to 40% slower, and for the fused L2 schedule 8 warps ran 1.5%
+//    slower at virtual TP 8 and 4 warps 32% slower.
 __host__ __device__ constexpr int consumers_for(int mode, int per_sm) {
-    return per_sm == 1 ? 16 : (mode == kModeFused || mode == kModeFusedL2) ? 8 : 12;
+    return per_sm == 1 ? 16 : 12;
 }
 __host__ __device__ constexpr int producers_for(int per_sm) { return per_sm == 1 ? 2 : 1; }
 __host__ __device__ constexpr int threads_for(int mode, int per_sm) {
     return (consumers_for(mode, per_sm) + 1 + producers_for(per_sm)) * 32;
 }
-// The fused L2 schedule at two CTAs per SM runs kNarrowWarps consumer warps
-// instead of consumers_for() when a CTA holds at most kFusedNarrowTiles tiles
-// of a row (each warp then takes several tiles per row, so the per-row waits
-// weigh less per tile); 0 never.
-constexpr int kNarrowWarps = 4;
-constexpr int kFusedNarrowTiles = 0;
-__host__ __device__ constexpr int threads_nw(int nw, int per_sm) { return (nw + 1 + producers_for(per_sm)) * 32; }
+
 constexpr int kMaxSlots = 96;
 constexpr uint64_t kDrainNs = 1000000000ull;   // bound of the final drain of own copies
 constexpr int64_t kL2ReuseBytes = 64ll << 20;  // logits held in L2 between the two reads of kModeFusedL2
@@ -1083,9 +1078,10 @@ __device__ void consumer(const Params& p, const Ctx& x) {
 
 // PER_SM: CTAs resident per SM (1 or 2); the register budget follows from it.
 // ENT (forward only): also the entropy of each row's softmax.
-template <int MODE, int PER_SM, bool ENT, int NW = consumers_for(MODE, PER_SM)>
-__global__ void __launch_bounds__(threads_nw(NW, PER_SM), PER_SM)
+template <int MODE, int PER_SM, bool ENT>
+__global__ void __launch_bounds__(threads_for(MODE, PER_SM), PER_SM)
     stream_kernel(const __grid_constant__ Params p) {
+    constexpr int NW = consumers_for(MODE, PER_SM);
     extern __shared__ __align__(1024) unsigned char smem[];
     Ctx x;
     x.warp = threadIdx.x >> 5;
@@ -1454,14 +1450,8 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     if (NS < 1) return fail(RLK_ERR_UNSUPPORTED, "tile too wide for one shared-memory slot");
 
     const int ntl_cta = (c.num_tiles + p.C - 1) / p.C;
-    auto nw_for = [&](int per_sm) {
-        return (mode == kModeFusedL2 && per_sm == 2 && ntl_cta <= kFusedNarrowTiles) ? kNarrowWarps
-                                                                                     : consumers_for(mode, per_sm);
-    };
     auto pick = [&](int per_sm) -> void (*)(Params) {
         if (p.ent) return per_sm == 2 ? stream_kernel<kModeFwd, 2, true> : stream_kernel<kModeFwd, 1, true>;
-        if (nw_for(per_sm) == kNarrowWarps && mode == kModeFusedL2 && per_sm == 2)
-            return stream_kernel<kModeFusedL2, 2, false, kNarrowWarps>;
         if (per_sm == 2)
             return (mode == kModeFwd)     ? stream_kernel<kModeFwd, 2, false>
                  : (mode == kModeBwd)     ? stream_kernel<kModeBwd, 2, false>
@@ -1474,7 +1464,7 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     };
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(threads_nw(nw_for(ctas_per_sm), ctas_per_sm), 1, 1);
+    cfg.blockDim = dim3(threads_for(mode, ctas_per_sm), 1, 1);
     cfg.stream = stream;
     cfg.numAttrs = 0;
     if (p.C > 1) {
@@ -1490,7 +1480,7 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     auto resident = [&](int per_sm, uint32_t bytes) -> int64_t {
         void (*k)(Params) = pick(per_sm);
         const void* f = reinterpret_cast<const void*>(k);
-        cfg.blockDim = dim3(threads_nw(nw_for(per_sm), per_sm), 1, 1);
+        cfg.blockDim = dim3(threads_for(mode, per_sm), 1, 1);
         cudaError_t err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
         if (err != cudaSuccess) {
             fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(err));
@@ -1521,8 +1511,8 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     int64_t clusters = resident(ctas_per_sm, smem);
     if (clusters <= 0) return RLK_ERR_CUDA;
     void (*kfn)(Params) = pick(ctas_per_sm);
-    cfg.blockDim = dim3(threads_nw(nw_for(ctas_per_sm), ctas_per_sm), 1, 1);
-    p.row_skip = (mode == kModeFwd && row_skip_safe(nw_for(ctas_per_sm), ntl_cta, p.rbufs)) ? 1 : 0;
+    cfg.blockDim = dim3(threads_for(mode, ctas_per_sm), 1, 1);
+    p.row_skip = (mode == kModeFwd && row_skip_safe(consumers_for(mode, ctas_per_sm), ntl_cta, p.rbufs)) ? 1 : 0;
     p.NS = NS;
     p.ns_div = make_fastdiv((uint32_t)NS);
     smem = layout(p, NS);
@@ -1535,7 +1525,7 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
                      "rlk stream plan: mode %d, %d CTA(s)/SM, %lld clusters x %d CTAs, %d tiles/copy, %d slots of %d B, "
                      "%d row buffers, skew %d, row skip %d, %u B shared memory, %d consumer warps\n",
                      mode, ctas_per_sm, (long long)clusters, p.C, p.tps, p.NS, p.slot_bytes, p.rbufs, p.skew,
-                     p.row_skip, smem, nw_for(ctas_per_sm));
+                     p.row_skip, smem, consumers_for(mode, ctas_per_sm));
     e = cudaLaunchKernelEx(&cfg, kfn, p);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("kernel launch: ") + cudaGetErrorString(e));
     return RLK_OK;
