@@ -557,10 +557,54 @@ def extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, V
     _, ms, clk = timed(grpo, args.steps, 3, stream, clock_index)
     out["grpo_loss"] = {"ms": ms, "tokens_per_s": T / ms * 1e3, "alg_gbs": T * 17 / ms / 1e6, "clocks": clk,
                         "note": "latency- and launch-bound (1.1 MB)"}
+    out["vocab_rank_tp8"] = vocab_rank_bench(rlk, c, logits, targets, dmask, dg, T, Vr, Vp, args, clock_index)
     lm = lmhead_bench(rlk, args, logits.device, clock_index, steps=max(5, min(args.steps, 10)), warmup=3)
     out["lmhead_fwd_bwd"] = lm.pop("fwd_bwd")
     out["lmhead_fwd"] = lm
     return out
+
+
+def vocab_rank_bench(rlk, c, logits, targets, dmask, dg, T, Vr, Vp, args, clock_index, tp=8, shard=0):
+    """One rank's compute in the vocabulary-parallel step at tp = 8 on this batch: the shard forward on
+    its V_padded/8 columns, the fold of the gathered [8, T, 8, 2] partials, the shard backward.  The
+    all-gather between them is NCCL's and not timed here (4 MB of partials per rank)."""
+    import torch
+    vs = Vp // tp
+    cs = c.replace(virtual_tp=tp)
+    shard_buf = logits[:, shard * vs:(shard + 1) * vs].contiguous()
+    dl = torch.empty_like(shard_buf)
+    gathered = torch.empty((tp, T, c.num_tiles // tp, 2), dtype=torch.float32, device=logits.device)
+    gathered_xt = torch.zeros((tp, T), dtype=torch.float32, device=logits.device)
+    ws = rlk.shard_workspace(cs, logits.device)
+    stream = torch.cuda.current_stream()
+    logp = torch.empty(T, dtype=torch.float32, device=logits.device)
+    lse = torch.empty(T, dtype=torch.float32, device=logits.device)
+    # the other ranks' partials: this shard's, repeated (valid input; the values do not change the cost)
+    part, xt = rlk.shard_fwd(cs, shard, shard_buf, targets, dmask, workspace=ws)
+    gathered.copy_(part.unsqueeze(0).expand_as(gathered))
+
+    def step():
+        rlk.check(rlk.rlk_logp_shard_fwd(cs, shard, shard_buf.data_ptr(), targets.data_ptr(), dmask.data_ptr(),
+                                         gathered[shard].data_ptr(), gathered_xt[shard].data_ptr(), ws.data_ptr(),
+                                         stream.cuda_stream))
+        rlk.check(rlk.rlk_logp_fold(cs, gathered.data_ptr(), gathered_xt.data_ptr(), targets.data_ptr(),
+                                    dmask.data_ptr(), logp.data_ptr(), lse.data_ptr(), ws.data_ptr(),
+                                    stream.cuda_stream))
+        rlk.check(rlk.rlk_logp_shard_bwd(cs, shard, shard_buf.data_ptr(), targets.data_ptr(), dmask.data_ptr(),
+                                         lse.data_ptr(), dg.data_ptr(), dl.data_ptr(), ws.data_ptr(),
+                                         stream.cuda_stream))
+    _, ms, clk = timed(step, args.steps, 3, stream, clock_index, per_launch=False)
+    hbm_peak, _, kind = measured_peaks()
+    n_active = int(dmask.sum().item())
+    vr_l = min(max(Vr - shard * vs, 0), vs)
+    alg = T * 2 * vr_l + n_active * 2 * vr_l + T * 2 * vs + T * (c.num_tiles * 8 + 8)
+    gbs = alg / (ms * 1e-3) / 1e9
+    del shard_buf, dl, gathered
+    return {"ms": ms, "alg_gbs": gbs, "frac": gbs / hbm_peak, "peak_source": f"{kind} hbm_gbs", "clocks": clk,
+            "launches_per_step": 5,
+            "note": f"rank {shard} of tp {tp}: shard forward ({vs} columns of all {T} rows), fold of the gathered "
+                    "partials, shard backward from the LSE; the all-gather is not timed. Bytes: the shard read by "
+                    "the forward, active rows read again by the backward, dlogits written, the gathered partials"}
 
 
 def e2e(rlk, c, w, logits_dev, tgt, mask, g, dev, args):
