@@ -61,7 +61,7 @@ def parse():
     ap.add_argument("--no-extra", action="store_true", help="skip the other paths' timings")
     ap.add_argument("--rows", type=int, default=0,
                     help="profiling only: shrink the batch to this many rows (not a bench number)")
-    ap.add_argument("--path", default="fused", choices=["fused", "fwd", "split", "lmhead", "lmhead_bwd"],
+    ap.add_argument("--path", default="fused", choices=["fused", "fwd", "split", "lmhead", "lmhead_bwd", "vocab_rank"],
                     help="profiling only: time another kernel instead of the fused step")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="--impl reference: oracle seconds per core spread over the warm-up and timed steps")
@@ -269,6 +269,22 @@ def run_ours(args, ws, rank, local):
                 "clocks": res["clocks"], "gpu_launches": res["launches_per_step"] * args.steps}
     if args.split == "vocab":
         return vocab_split_bench(rlk, args, ws, rank, local, dev)
+    if args.path == "vocab_rank":
+        w = W.GRPO
+        logits = torch.empty((w.T, w.v_padded), dtype=torch.int16, device=dev)
+        W.logits_device(w, logits)
+        mask = W.active_mask(w)
+        targets = torch.from_numpy(W.targets(w)).to(dev)
+        dmask = torch.from_numpy(mask).to(dev)
+        dg = torch.from_numpy(W.grad(w, mask != 0)).to(dev)
+        c = rlk.Contract(T=w.T, V_real=w.v_real, V_padded=w.v_padded, num_tiles=w.num_tiles, virtual_tp=1,
+                         mask_mode=rlk.MASK_EXPLICIT, validate=0)
+        res = vocab_rank_bench(rlk, c, logits, targets, dmask, dg, w.T, w.v_real, w.v_padded, args, local)
+        return {"metric": "one rank of the tp 8 vocabulary-parallel step, tokens/s (profiling run)",
+                "value": w.T / (res["ms"] * 1e-3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": res["ms"], "higher_is_better": True,
+                "config": {"workload": "grpo rank 0 of tp 8"}, "clocks": res["clocks"],
+                "gpu_launches": res["launches_per_step"] * args.steps}
     w = W.GRPO
     if args.rows:
         w = w.with_(batch=max(1, args.rows // w.seq), name="grpo-profile")

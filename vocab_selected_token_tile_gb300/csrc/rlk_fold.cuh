@@ -120,6 +120,27 @@ __device__ __forceinline__ float fold_tiles(const float2* part, int NT, float2* 
     return __shfl_sync(0xFFFFFFFFu, lse, 0);
 }
 
+// The same fold by one thread, one tile at a time, for kernels that fold
+// many rows at once (one row per thread): fold_step takes tile k's partial
+// in index order, fold_finish gives the LSE.  Every value is formed by the
+// operations fold_tiles uses, in the same order -- the running maximum M_k
+// is the exact prefix max (max is exact, so the order of a scan does not
+// change it), f_k = exp(M_{k-1} - M_k) (0 while M_{k-1} = -inf), the term
+// b_k = s_k exp(m_k - M_k) (0 for an identity tile), S = S f_k + b_k -- so
+// the bits are those of fold_tiles.
+__device__ __forceinline__ void fold_step(float& M, float& S, float2 pk) {
+    const float Mk = fmax_nan(M, pk.x);
+    const float f = (M == -INFINITY) ? 0.f : ex2_approx(__fmul_rn(__fsub_rn(M, Mk), kLog2e));
+    const float b =
+        (pk.x == -INFINITY) ? 0.f : __fmul_rn(pk.y, ex2_approx(__fmul_rn(__fsub_rn(pk.x, Mk), kLog2e)));
+    S = __fmaf_rn(S, f, b);
+    M = Mk;
+}
+
+__device__ __forceinline__ float fold_finish(float M, float S) {
+    return (M == -INFINITY) ? -INFINITY : __fadd_rn(M, logf(S));
+}
+
 // fold_tiles plus the entropy of the row's softmax.  tpart[k] holds the
 // tile's t_k = sum_c e^(x_c - m_k) x_c.  The LSE comes from exactly the same
 // operations as fold_tiles; beside S the same recurrence runs T_k =

@@ -77,37 +77,41 @@ __global__ void shard_zero_kernel(uint16_t* d, int64_t stride, int64_t T, int64_
         d[(i / cols) * stride + i % cols] = 0;
 }
 
-// LSE and logp of each row from the gathered partials (one warp per row).
-// gathered [tp, T, NT/tp] float2 (rank-major, as an all-gather of every
-// rank's [T, NT/tp] partials leaves them), gathered_xt [tp, T]; the target
-// logit is taken from the shard that holds the target's column.
+// Row `row`'s outcome from its LSE: lane 0 writes LSE and logp and reports
+// the device conditions; xt is the target logit (read by lane 0 when needed).
+__device__ __forceinline__ void finish_row(int64_t row, float l, int64_t t, bool active, float xt, int64_t Vr,
+                                           float* logp, float* lse, uint32_t* status) {
+    lse[row] = l;
+    if (!active) {
+        logp[row] = 0.f;
+    } else if (t < 0 || t >= Vr) {
+        logp[row] = __int_as_float(0x7FC00000);
+        atomicOr(status, kStatusTargetRange);
+    } else {
+        logp[row] = __fsub_rn(xt, l);
+    }
+    if (active && !isfinite(l)) atomicOr(status, kStatusNonFinite);
+}
+
+// LSE and logp of each row from the gathered partials, one row per thread
+// (fold_step / fold_finish: the bits of fold_tiles, without the warp's
+// shuffles, which bound a warp-per-row fold of many rows).  gathered
+// [tp, T, NT/tp] float2 (shard-major, as an all-gather of every rank's
+// [T, NT/tp] partials leaves them), gathered_xt [tp, T]; the target logit is
+// taken from the shard that holds the target's column.
 __global__ void gathered_fold_kernel(const float2* gathered, const float* gathered_xt, const int64_t* targets,
                                      const uint8_t* mask, int mask_mode, int64_t ignore_index, int64_t T, int64_t Vr,
-                                     int64_t Vs, int NT, int ntl, float* logp, float* lse, uint32_t* status) {
-    extern __shared__ float2 sm[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int wpb = blockDim.x >> 5;
-    float2* parts = sm + (size_t)warp * 2 * NT;
-    float2* scratch = parts + NT;
-    for (int64_t row = (int64_t)blockIdx.x * wpb + warp; row < T; row += (int64_t)gridDim.x * wpb) {
-        for (int k = lane; k < NT; k += 32) parts[k] = gathered[((int64_t)(k / ntl) * T + row) * ntl + (k % ntl)];
-        __syncwarp();
-        const float l = fold_tiles(parts, NT, scratch, lane);
-        if (lane == 0) {
-            const int64_t t = targets[row];
-            const bool active = (mask_mode == RLK_MASK_EXPLICIT) ? (mask[row] != 0) : (t != ignore_index);
-            lse[row] = l;
-            if (!active) {
-                logp[row] = 0.f;
-            } else if (t < 0 || t >= Vr) {
-                logp[row] = __int_as_float(0x7FC00000);
-                atomicOr(status, kStatusTargetRange);
-            } else {
-                logp[row] = __fsub_rn(gathered_xt[(t / Vs) * T + row], l);
-            }
-            if (active && !isfinite(l)) atomicOr(status, kStatusNonFinite);
+                                     int64_t Vs, int tp, int ntl, float* logp, float* lse, uint32_t* status) {
+    for (int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; row < T; row += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = targets[row];
+        const bool active = (mask_mode == RLK_MASK_EXPLICIT) ? (mask[row] != 0) : (t != ignore_index);
+        const float xt = (active && t >= 0 && t < Vr) ? gathered_xt[(t / Vs) * T + row] : 0.f;
+        float M = -INFINITY, S = 0.f;
+        for (int sh = 0; sh < tp; ++sh) {
+            const float2* part = gathered + ((int64_t)sh * T + row) * ntl;
+            for (int l = 0; l < ntl; ++l) fold_step(M, S, part[l]);
         }
-        __syncwarp();
+        finish_row(row, fold_finish(M, S), t, active, xt, Vr, logp, lse, status);
     }
 }
 
@@ -184,15 +188,9 @@ rlk_status launch_shard_fwd(const rlk_logp_contract& c, int32_t shard, const uin
 rlk_status launch_gathered_fold(const rlk_logp_contract& c, const float* gathered_partials, const float* gathered_xt,
                                 const int64_t* targets, const uint8_t* mask, float* logp, float* lse,
                                 uint32_t* status, cudaStream_t stream) {
-    const int threads = 256;
-    const size_t smem = (size_t)(threads / 32) * 2 * c.num_tiles * sizeof(float2);
-    cudaError_t e = cudaFuncSetAttribute(gathered_fold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-    int64_t grid = (c.T + 7) / 8;
-    if (grid > 2048) grid = 2048;
-    gathered_fold_kernel<<<(unsigned)grid, threads, smem, stream>>>(
+    gathered_fold_kernel<<<grid_for(c.T, 128), 128, 0, stream>>>(
         reinterpret_cast<const float2*>(gathered_partials), gathered_xt, targets, mask, c.mask_mode, c.ignore_index,
-        c.T, c.V_real, c.V_padded / c.virtual_tp, c.num_tiles, c.num_tiles / c.virtual_tp, logp, lse, status);
+        c.T, c.V_real, c.V_padded / c.virtual_tp, c.virtual_tp, c.num_tiles / c.virtual_tp, logp, lse, status);
     return launched("gathered fold");
 }
 
