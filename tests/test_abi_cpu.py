@@ -144,3 +144,38 @@ def test_modelled_planner_overrides_are_accepted(built, monkeypatch, name, value
     c = rlk.Contract(T=16, V_real=1000, V_padded=1024, num_tiles=4)
     monkeypatch.setenv(name, value)
     assert rlk.rlk_logp_check_contract(c) == rlk.RLK_OK
+
+
+def test_new_entry_points_fail_closed_on_the_host(built):
+    """The shard calls, the gathered fold and the lm_head backward check their arguments before any
+    CUDA call: an empty batch is a no-op, missing or misaligned pointers and bad shard indices fail."""
+    c = ok_contract(virtual_tp=8)
+    z = ok_contract(T=0, virtual_tp=8)
+    assert rlk.rlk_logp_shard_fwd(z, 0, None, None, None, None, None, None, None) == rlk.RLK_OK
+    assert rlk.rlk_logp_fold(z, None, None, None, None, None, None, None, None) == rlk.RLK_OK
+    assert rlk.rlk_logp_shard_bwd(z, 0, None, None, None, None, None, None, None, None) == rlk.RLK_OK
+    assert rlk.rlk_logp_check_shard_contract(c, 7) == rlk.RLK_OK
+    assert rlk.rlk_logp_check_shard_contract(c, 8) == rlk.RLK_ERR_INVALID_ARG
+    assert rlk.rlk_logp_shard_workspace_size(c) >= 256
+    assert rlk.rlk_logp_shard_fwd(c, 8, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, None) == rlk.RLK_ERR_INVALID_ARG
+    assert rlk.rlk_logp_shard_fwd(c, 0, None, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, None) == rlk.RLK_ERR_INVALID_ARG
+    assert rlk.rlk_logp_shard_fwd(c, 0, 0x1008, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, None) == rlk.RLK_ERR_MISALIGNED
+    assert rlk.rlk_logp_shard_fwd(c, 0, 0x1000, 0x2000, 0x3000, None, 0x5000, 0x6000, None) == rlk.RLK_ERR_INVALID_ARG
+    assert rlk.rlk_logp_fold(c, None, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, None) == rlk.RLK_ERR_INVALID_ARG
+    assert rlk.rlk_logp_fold(c, 0x1000, 0x2000, 0x3000, 0x4000, None, 0x6000, 0x7000, None) == rlk.RLK_ERR_INVALID_ARG
+    assert rlk.rlk_logp_shard_bwd(c, 0, 0x1000, 0x2000, 0x3000, None, 0x5000, 0x6000, 0x7000,
+                                  None) == rlk.RLK_ERR_INVALID_ARG
+    assert rlk.rlk_logp_shard_bwd(c, 0, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6008, 0x7000,
+                                  None) == rlk.RLK_ERR_MISALIGNED
+    # the lm_head backward from a given LSE
+    cl = ok_contract(virtual_tp=2)
+    assert rlk.rlk_logp_fused_lmhead_bwd(ok_contract(T=0), None, 128, None, None, None, None, None, None, None,
+                                         None, None, None) == rlk.RLK_OK
+    assert rlk.rlk_logp_fused_lmhead_bwd(cl, 0x1000, 100, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, None,
+                                         0x8000, 0x9000, None) == rlk.RLK_ERR_UNSUPPORTED  # H not a multiple of 64
+    assert rlk.rlk_logp_fused_lmhead_bwd(cl, 0x1000, 128, 0x2000, 0x3000, 0x4000, None, 0x6000, 0x7000, None,
+                                         0x8000, 0x9000, None) == rlk.RLK_ERR_INVALID_ARG  # no lse_in
+    assert rlk.rlk_logp_fused_lmhead_bwd(cl, 0x1000, 128, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, None,
+                                         None, 0x9000, None) == rlk.RLK_ERR_INVALID_ARG  # no dweight output
+    assert rlk.rlk_logp_fused_lmhead(cl, 0x1000, 128, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000,
+                                     0x9008, None, 0xA000, None) == rlk.RLK_ERR_MISALIGNED  # FP32 dweight
