@@ -295,3 +295,32 @@ def test_lmhead_backward_from_a_given_lse_is_bitwise_the_fused_call(case):
     with pytest.raises(rlk.RlkError) as ei:
         rlk.logp_fused_lmhead_bwd(c, dh_, dw_, dt, dm, l2, dg)
     assert ei.value.status == rlk.RLK_ERR_NONFINITE_LSE
+
+
+@pytest.mark.parametrize("case", [(1, 64, 200, 256, 2), (127, 64, 1000, 1024, 8), (3, 128, 2380, 2384 * 8, 8)],
+                         ids=lambda c: "T%d_H%d_V%d_P%d_NT%d" % c)
+def test_lmhead_degenerate_sizes(case):
+    """A single token, one partial token block, one tile per shard at virtual TP 8, padded tiles:
+    forward and backward against the oracle, bitwise across virtual TP."""
+    T, H, v_real, v_padded, nt = case
+    hb, wb = make(T, H, v_real, v_padded, seed=T + 17)
+    tgt = synth.targets(T, v_real, seed=T + 18)
+    mask = np.ones(T, dtype=np.uint8)
+    if T > 2:
+        mask[1] = 0
+    g = np.where(mask != 0, np.random.default_rng(T).standard_normal(T), 0.0).astype(np.float32)
+    ref_logp, ref_lse, _ = oracle.lmhead_forward(hb, wb, tgt, mask != 0, v_real)
+    ref_dh, ref_dw, sc_dh, sc_dw = grad_bounds(hb, wb, tgt, mask != 0, g, v_real)
+    outs = set()
+    for vtp in (v for v in (1, 2, 4, 8) if nt % v == 0):
+        c = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=nt, virtual_tp=vtp, validate=1)
+        logp, lse, dh, dw = rlk.logp_fused_lmhead(c, dev(hb), dev(wb), torch.from_numpy(tgt).cuda(),
+                                                  torch.from_numpy(mask).cuda(), grad=torch.from_numpy(g).cuda())
+        torch.cuda.synchronize()
+        close("lse", lse.cpu().numpy(), ref_lse)
+        close("logp", logp.cpu().numpy(), ref_logp)
+        dhb, dwb = dh.cpu().numpy().view(np.uint16), dw.cpu().numpy().view(np.uint16)
+        assert np.all(within(dhb, ref_dh, sc_dh))
+        assert np.all(within(dwb[:v_real], ref_dw, sc_dw)) and np.all(dwb[v_real:] == 0)
+        outs.add((logp.cpu().numpy().tobytes(), lse.cpu().numpy().tobytes(), dhb.tobytes(), dwb.tobytes()))
+    assert len(outs) == 1
