@@ -573,6 +573,16 @@ def extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, V
     _, ms, clk = timed(grpo, args.steps, 3, stream, clock_index)
     out["grpo_loss"] = {"ms": ms, "tokens_per_s": T / ms * 1e3, "alg_gbs": T * 17 / ms / 1e6, "clocks": clk,
                         "note": "latency- and launch-bound (1.1 MB)"}
+    # the split path: the forward, then the backward from its LSE (the logits are read twice)
+    cs = c.replace(virtual_tp=1)
+
+    def split():
+        rlk.logp_fwd(cs, logits, targets, dmask, out=(logp, lse))
+        rlk.logp_bwd(cs, logits, targets, dmask, lse, dg, dlogits=dlogits)
+    _, ms, clk = timed(split, args.steps, 3, stream, clock_index, per_launch=False)
+    n_active = int(dmask.sum().item())
+    out["split_fwd_then_bwd_vtp1"] = entry(ms, T * (2 * Vr + 17) + n_active * 2 * Vr + T * (2 * Vp + 17), clk,
+                                           "stream_kernel<kModeFwd> + stream_kernel<kModeBwd>")
     out["vocab_rank_tp8"] = vocab_rank_bench(rlk, c, logits, targets, dmask, dg, T, Vr, Vp, args, clock_index)
     lm = lmhead_bench(rlk, args, logits.device, clock_index, steps=max(5, min(args.steps, 10)), warmup=3)
     out["lmhead_fwd_bwd"] = lm.pop("fwd_bwd")
