@@ -153,6 +153,21 @@ rlk_status rlk_logp_fwd_entropy(const rlk_logp_contract* contract, const void* l
                                 float* entropy, void* workspace, rlk_stream_t stream);
 
 /*
+ * The fused single-pass forward+backward (rlk_logp_bwd with lse_in == NULL)
+ * plus the entropy of each row's softmax, as rlk_logp_fwd_entropy computes
+ * it, in the same pass over the logits: the step of RL training that also
+ * logs the policy's entropy.  dlogits, logp_out and lse_out are bitwise
+ * those of rlk_logp_bwd; entropy_out ([T] FP32, every row, NaN where the LSE
+ * is not finite) is bitwise that of rlk_logp_fwd_entropy.  Every argument is
+ * required; row_stride, masks, status as for rlk_logp_bwd.  Runs the L2 fused
+ * schedule (RLK_FUSED_SCHEDULE=resident returns RLK_ERR_UNSUPPORTED).
+ */
+rlk_status rlk_logp_fwd_bwd_entropy(const rlk_logp_contract* contract, const void* logits_bf16,
+                                    const int64_t* targets, const uint8_t* active_mask, const float* grad_logp,
+                                    void* dlogits_bf16, float* logp_out, float* lse_out, float* entropy_out,
+                                    void* workspace, rlk_stream_t stream);
+
+/*
  * Token-mean GRPO loss of per-token log-probabilities and its gradient with
  * respect to each logp: the step after the forward, whose g feeds
  * rlk_logp_bwd.  The pages name a GRPO loss contract (issue #323 "[WS2]

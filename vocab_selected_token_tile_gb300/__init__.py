@@ -32,6 +32,7 @@ EXPORTED = (
     "rlk_logp_bwd",
     "rlk_logp_fwd_noalloc",
     "rlk_logp_fwd_entropy",
+    "rlk_logp_fwd_bwd_entropy",
     "rlk_grpo_loss",
     "rlk_logp_lmhead_workspace_size",
     "rlk_logp_fused_lmhead",
@@ -110,6 +111,8 @@ def library():
         lib.rlk_logp_fwd_noalloc.restype = i
         lib.rlk_logp_fwd_entropy.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.rlk_logp_fwd_entropy.restype = i
+        lib.rlk_logp_fwd_bwd_entropy.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.rlk_logp_fwd_bwd_entropy.restype = i
         lib.rlk_grpo_loss.argtypes = [ctypes.c_int64, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
         lib.rlk_grpo_loss.restype = i
         lib.rlk_logp_check_shard_contract.argtypes = [P, ctypes.c_int32]
@@ -176,6 +179,12 @@ def rlk_logp_fused_lmhead_bwd(contract, hidden, H, weight, targets, active_mask,
 def rlk_logp_fwd_entropy(contract, logits, targets, active_mask, logp, lse, entropy, workspace, stream):
     return library().rlk_logp_fwd_entropy(ctypes.byref(contract), logits, targets, active_mask, logp, lse, entropy,
                                           workspace, stream)
+
+
+def rlk_logp_fwd_bwd_entropy(contract, logits, targets, active_mask, grad_logp, dlogits, logp_out, lse_out,
+                             entropy_out, workspace, stream):
+    return library().rlk_logp_fwd_bwd_entropy(ctypes.byref(contract), logits, targets, active_mask, grad_logp,
+                                              dlogits, logp_out, lse_out, entropy_out, workspace, stream)
 
 
 def rlk_grpo_loss(T, logp, advantage, active_mask, ref_logp, beta, loss, grad_logp, active_count, stream):
@@ -325,6 +334,20 @@ def logp_fwd_bwd(contract, logits, targets, mask, grad, dlogits=None, stream=Non
     check(rlk_logp_bwd(contract, _ptr(logits), _ptr(targets), _ptr(mask), None, _ptr(grad), _ptr(dlogits),
                        _ptr(logp), _ptr(lse), _ptr(ws), _stream(stream)))
     return dlogits, logp, lse
+
+
+def logp_fwd_bwd_entropy(contract, logits, targets, mask, grad, dlogits=None, stream=None):
+    """Fused single pass plus each row's entropy: (dlogits, logp, lse, entropy)."""
+    import torch
+    dev = logits.device
+    T = contract.T
+    if dlogits is None:
+        dlogits = torch.empty_like(logits)
+    logp, lse, ent = (torch.empty(T, dtype=torch.float32, device=dev) for _ in range(3))
+    ws = workspace_for(contract, dev, stream)
+    check(rlk_logp_fwd_bwd_entropy(contract, _ptr(logits), _ptr(targets), _ptr(mask), _ptr(grad), _ptr(dlogits),
+                                   _ptr(logp), _ptr(lse), _ptr(ent), _ptr(ws), _stream(stream)))
+    return dlogits, logp, lse, ent
 
 
 def logp_fwd_bwd_host(contract, logits, targets, mask, grad, device, chunk_rows=8192, dlogits=None,

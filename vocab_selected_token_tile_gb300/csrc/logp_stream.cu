@@ -1077,7 +1077,7 @@ __device__ void consumer(const Params& p, const Ctx& x) {
 }
 
 // PER_SM: CTAs resident per SM (1 or 2); the register budget follows from it.
-// ENT (forward only): also the entropy of each row's softmax.
+// ENT (the forward and the fused L2 schedule): also the entropy of each row's softmax.
 template <int MODE, int PER_SM, bool ENT>
 __global__ void __launch_bounds__(threads_for(MODE, PER_SM), PER_SM)
     stream_kernel(const __grid_constant__ Params p) {
@@ -1320,7 +1320,8 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     p.W = (int32_t)(c.V_padded / c.num_tiles);
     p.mask_mode = c.mask_mode;
     p.ent = (a.entropy != nullptr) ? 1 : 0;
-    if (p.ent && mode != kModeFwd) return fail(RLK_ERR_UNSUPPORTED, "the entropy is computed by the forward only");
+    if (p.ent && mode != kModeFwd && mode != kModeFused)
+        return fail(RLK_ERR_UNSUPPORTED, "the entropy is computed by the forward and the fused forward+backward");
     // One bulk copy per chunk of tps consecutive tiles, about 8192 columns
     // (16 KB): a copy costs about the same issue time whatever its size, so
     // large copies are what keeps the stream near HBM bandwidth.
@@ -1339,6 +1340,8 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         if (!s.empty() && s != "l2" && s != "resident")
             return fail(RLK_ERR_UNSUPPORTED, "RLK_FUSED_SCHEDULE must be l2 or resident");
         if (s != "resident") mode = kModeFusedL2;
+        if (p.ent && mode != kModeFusedL2)
+            return fail(RLK_ERR_UNSUPPORTED, "the entropy is computed by the L2 fused schedule, not the resident one");
     }
     int C = (mode == kModeBwd) ? 1 : c.virtual_tp;
     // The streaming modes take larger chunks where the CTA's shard allows:
@@ -1451,6 +1454,8 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
 
     const int ntl_cta = (c.num_tiles + p.C - 1) / p.C;
     auto pick = [&](int per_sm) -> void (*)(Params) {
+        if (p.ent && mode == kModeFusedL2)
+            return per_sm == 2 ? stream_kernel<kModeFusedL2, 2, true> : stream_kernel<kModeFusedL2, 1, true>;
         if (p.ent) return per_sm == 2 ? stream_kernel<kModeFwd, 2, true> : stream_kernel<kModeFwd, 1, true>;
         if (per_sm == 2)
             return (mode == kModeFwd)     ? stream_kernel<kModeFwd, 2, false>

@@ -212,6 +212,41 @@ RLK_EXPORT rlk_status rlk_logp_fwd_entropy(const rlk_logp_contract* c, const voi
     return c->validate ? read_status(workspace, st) : RLK_OK;
 }
 
+RLK_EXPORT rlk_status rlk_logp_fwd_bwd_entropy(const rlk_logp_contract* c, const void* logits_bf16,
+                                               const int64_t* targets, const uint8_t* active_mask,
+                                               const float* grad_logp, void* dlogits_bf16, float* logp_out,
+                                               float* lse_out, float* entropy_out, void* workspace,
+                                               rlk_stream_t stream) {
+    rlk_status s = check_contract(c);
+    if (s != RLK_OK) return s;
+    if (c->T == 0) return RLK_OK;
+    if ((s = check_common(c, logits_bf16, targets, active_mask, workspace)) != RLK_OK) return s;
+    if (!grad_logp) return fail(RLK_ERR_INVALID_ARG, "grad_logp is NULL");
+    if (!dlogits_bf16) return fail(RLK_ERR_INVALID_ARG, "dlogits is NULL");
+    if (!aligned16(dlogits_bf16)) return fail(RLK_ERR_MISALIGNED, "dlogits must be 16-byte aligned");
+    if (!logp_out || !lse_out || !entropy_out)
+        return fail(RLK_ERR_INVALID_ARG, "logp_out, lse_out and entropy_out are required");
+    if ((s = select_device(logits_bf16)) != RLK_OK) return s;
+    if ((s = check_device_ptrs({{targets, "targets"}, {active_mask, "active_mask"}, {grad_logp, "grad_logp"},
+                                {dlogits_bf16, "dlogits"}, {logp_out, "logp_out"}, {lse_out, "lse_out"},
+                                {entropy_out, "entropy_out"}, {workspace, "workspace"}})) != RLK_OK)
+        return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = begin(workspace, st)) != RLK_OK) return s;
+    StreamArgs a{};
+    a.logits = static_cast<const uint16_t*>(logits_bf16);
+    a.dlogits = static_cast<uint16_t*>(dlogits_bf16);
+    a.targets = targets;
+    a.mask = active_mask;
+    a.grad = grad_logp;
+    a.logp = logp_out;
+    a.lse = lse_out;
+    a.entropy = entropy_out;
+    a.status = static_cast<uint32_t*>(workspace);
+    if ((s = launch_stream(*c, kModeFused, a, st)) != RLK_OK) return s;
+    return c->validate ? read_status(workspace, st) : RLK_OK;
+}
+
 RLK_EXPORT rlk_status rlk_grpo_loss(int64_t T, const float* logp, const float* advantage, const uint8_t* active_mask,
                                     const float* ref_logp, float beta, float* loss, float* grad_logp,
                                     float* active_count, rlk_stream_t stream) {
