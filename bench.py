@@ -561,6 +561,16 @@ def extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, V
                                            stream.cuda_stream))
     _, ms, clk = timed(fwd_ent, args.steps, 3, stream, clock_index)
     out["fwd_entropy_vtp1"] = entry(ms, T * (2 * Vr + 21), clk, "stream_kernel<kModeFwd, ENT>")
+    # the fused forward+backward with each row's entropy (the same single pass; 4 more bytes per row)
+    c2 = c.replace(virtual_tp=2)
+    ws_f = rlk.workspace_for(c2, logits.device, stream)
+
+    def fused_ent():
+        rlk.check(rlk.rlk_logp_fwd_bwd_entropy(c2, logits.data_ptr(), targets.data_ptr(), dmask.data_ptr(),
+                                               dg.data_ptr(), dlogits.data_ptr(), logp.data_ptr(), lse.data_ptr(),
+                                               ent.data_ptr(), ws_f.data_ptr(), stream.cuda_stream))
+    _, ms, clk = timed(fused_ent, args.steps, 3, stream, clock_index)
+    out["fused_entropy_vtp2"] = entry(ms, T * (2 * Vr + 2 * Vp + 25), clk, "stream_kernel<kModeFusedL2, ENT>")
     # the GRPO loss and g from this batch's logp (reads logp, A, mask, ref; writes g: 17 B per row)
     ref = logp + 0.01
     loss, gl, cnt = (torch.empty(1, dtype=torch.float32, device=logits.device),
