@@ -159,8 +159,9 @@ rlk_status rlk_logp_fwd_entropy(const rlk_logp_contract* contract, const void* l
  * logs the policy's entropy.  dlogits, logp_out and lse_out are bitwise
  * those of rlk_logp_bwd; entropy_out ([T] FP32, every row, NaN where the LSE
  * is not finite) is bitwise that of rlk_logp_fwd_entropy.  Every argument is
- * required; row_stride, masks, status as for rlk_logp_bwd.  Runs the L2 fused
- * schedule (RLK_FUSED_SCHEDULE=resident returns RLK_ERR_UNSUPPORTED).
+ * required; row_stride, masks, status and in-place dlogits as for
+ * rlk_logp_bwd.  Runs the L2 fused schedule (RLK_FUSED_SCHEDULE=resident
+ * returns RLK_ERR_UNSUPPORTED).
  */
 rlk_status rlk_logp_fwd_bwd_entropy(const rlk_logp_contract* contract, const void* logits_bf16,
                                     const int64_t* targets, const uint8_t* active_mask, const float* grad_logp,
@@ -206,10 +207,15 @@ rlk_status rlk_grpo_loss(int64_t T, const float* logp, const float* advantage, c
  *                once: LSE is formed on chip, dlogits written, and
  *                logp_out/lse_out (both required) receive the forward
  *                outputs, bitwise equal to rlk_logp_fwd's.
- * dlogits are bitwise identical between the two forms.  The fused form keeps
- * a row's slice resident in shared memory across a cluster of CTAs; a
- * vocabulary too large for that returns RLK_ERR_UNSUPPORTED (call
- * rlk_logp_fwd, then rlk_logp_bwd with lse_in).
+ * dlogits are bitwise identical between the two forms.  The fused form
+ * reads each row's bytes from HBM once and its second copy from L2 (any
+ * vocabulary); RLK_FUSED_SCHEDULE=resident instead keeps a row's slice in
+ * shared memory across a cluster of CTAs and returns RLK_ERR_UNSUPPORTED for
+ * a vocabulary too large for that.
+ * In place: dlogits_bf16 may be logits_bf16 itself (the same pointer and
+ * row_stride), in both forms -- every logit is read before its gradient
+ * overwrites it, and the outputs are bitwise those of a separate buffer.
+ * Any other overlap of an output with an input is not allowed.
  */
 rlk_status rlk_logp_bwd(const rlk_logp_contract* contract, const void* logits_bf16,
                         const int64_t* targets, const uint8_t* active_mask,
@@ -331,7 +337,8 @@ rlk_status rlk_logp_fold(const rlk_logp_contract* contract, const float* gathere
  *   dlogits_shard [T, row_stride] BF16 out: columns [0, Vs) of every row,
  *                 g (onehot - exp(x - LSE)) with the one-hot term only in the
  *                 shard that holds the target; padding and inactive rows 0.
- * No collective is needed.  Device status: an active target outside
+ * No collective is needed.  dlogits_shard may be logits_shard itself (in
+ * place, as for rlk_logp_bwd).  Device status: an active target outside
  * [0, V_real), a non-finite lse_in on an active row.
  */
 rlk_status rlk_logp_shard_bwd(const rlk_logp_contract* contract, int32_t shard, const void* logits_shard,

@@ -179,3 +179,32 @@ def test_new_entry_points_fail_closed_on_the_host(built):
                                          None, 0x9000, None) == rlk.RLK_ERR_INVALID_ARG  # no dweight output
     assert rlk.rlk_logp_fused_lmhead(cl, 0x1000, 128, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000,
                                      0x9008, None, 0xA000, None) == rlk.RLK_ERR_MISALIGNED  # FP32 dweight
+
+
+def test_dlogits_may_alias_logits_only_exactly(built):
+    """dlogits == logits (in place) passes the host checks; a dlogits buffer that overlaps the logits at
+    another address is rejected before any CUDA call; a disjoint one passes.  (Calls that pass the host
+    checks stop at the device check here: there is no GPU.)"""
+    c = ok_contract(T=8)  # 8 rows x 152576 BF16 = 2,441,216 bytes
+    base, span = 0x10000000, 8 * 152576 * 2
+
+    def bwd(dl):
+        return rlk.rlk_logp_bwd(c, base, 0x2000, 0x3000, 0x4000, 0x5000, dl, None, None, 0x6000, None)
+
+    def fused_ent(dl):
+        return rlk.rlk_logp_fwd_bwd_entropy(c, base, 0x2000, 0x3000, 0x5000, dl, 0x7000, 0x8000, 0x9000, 0x6000,
+                                            None)
+    for call in (bwd, fused_ent):
+        for dl in (base + 16, base + span - 16, base - span + 16):
+            assert call(dl) == rlk.RLK_ERR_INVALID_ARG
+            assert "overlaps logits" in rlk.rlk_last_error_message()
+        for dl in (base, base + span, base - span):
+            call(dl)
+            assert "overlaps" not in rlk.rlk_last_error_message()
+    cs = ok_contract(T=8, virtual_tp=8)  # shard buffers of 152576/8 columns
+    sspan = 8 * (152576 // 8) * 2
+    assert rlk.rlk_logp_shard_bwd(cs, 0, base, 0x2000, 0x3000, 0x4000, 0x5000, base + sspan - 16, 0x6000,
+                                  None) == rlk.RLK_ERR_INVALID_ARG
+    assert "overlaps logits" in rlk.rlk_last_error_message()
+    rlk.rlk_logp_shard_bwd(cs, 0, base, 0x2000, 0x3000, 0x4000, 0x5000, base + sspan, 0x6000, None)
+    assert "overlaps" not in rlk.rlk_last_error_message()

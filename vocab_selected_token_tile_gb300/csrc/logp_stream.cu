@@ -218,9 +218,10 @@ struct Waiter {
 __device__ __forceinline__ uint32_t neg_inf_lo(uint32_t w) { return (w & 0xFFFF0000u) | 0xFF80u; }
 __device__ __forceinline__ uint32_t neg_inf_hi(uint32_t w) { return (w & 0x0000FFFFu) | 0xFF800000u; }
 
-__device__ __forceinline__ uint16_t ldg_bf16(const uint16_t* p) {
-    return __ldg(reinterpret_cast<const unsigned short*>(p));
-}
+// A plain, coherent global load.  The backward may write dlogits over the
+// logits it reads (in place), so no read of the logits goes through the
+// read-only data path, whose contents must not change during a kernel.
+__device__ __forceinline__ uint16_t ld_bf16(const uint16_t* p) { return *p; }
 
 // The 8 BF16 values of columns [c0, c0+8) as a uint4; columns outside the
 // tile's real range [ts, hi) read as -inf.  Groups inside the slot span come
@@ -236,8 +237,8 @@ __device__ __forceinline__ uint4 load_group(const uint16_t* slot, const uint16_t
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int c = c0 + 2 * j;
-            const uint32_t lo = (c < t.hi && c >= t.ts) ? ldg_bf16(grow + c) : 0xFF80u;
-            const uint32_t hi = (c + 1 < t.hi && c + 1 >= t.ts) ? ldg_bf16(grow + c + 1) : 0xFF80u;
+            const uint32_t lo = (c < t.hi && c >= t.ts) ? ld_bf16(grow + c) : 0xFF80u;
+            const uint32_t hi = (c + 1 < t.hi && c + 1 >= t.ts) ? ld_bf16(grow + c + 1) : 0xFF80u;
             w[j] = lo | (hi << 16);
         }
         return make_uint4(w[0], w[1], w[2], w[3]);
@@ -476,8 +477,8 @@ __device__ void tile_grad(const uint16_t* slot, const uint16_t* grow, uint16_t* 
 #pragma unroll
             for (int j = 0; j < 8; j += 2) {
                 const int c = c0 + j;
-                const uint32_t lo = (c < Vr) ? ldg_bf16(grow + c) : 0xFF80u;
-                const uint32_t hi = (c + 1 < Vr) ? ldg_bf16(grow + c + 1) : 0xFF80u;
+                const uint32_t lo = (c < Vr) ? ld_bf16(grow + c) : 0xFF80u;
+                const uint32_t hi = (c + 1 < Vr) ? ld_bf16(grow + c + 1) : 0xFF80u;
                 const float2 q = exp_terms2(bf16x2_to_f32x2(lo | (hi << 16)), make_float2(nlL, nlL));
                 pr[j] = q.x;
                 pr[j + 1] = q.y;
@@ -995,7 +996,7 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
             x.part[(size_t)b * p.NT + k] = pr;
             if (ENT) x.tpart[(size_t)b * p.NT + k] = tk;
             if (h.active && h.target >= tg.ts && h.target < tg.hi) {
-                const uint16_t bits = (h.target < tg.b) ? sl[h.target - tg.a] : ldg_bf16(grow + h.target);
+                const uint16_t bits = (h.target < tg.b) ? sl[h.target - tg.a] : ld_bf16(grow + h.target);
                 rs.xt = __uint_as_float((uint32_t)bits << 16);
                 rs.has_xt = 1;
             }

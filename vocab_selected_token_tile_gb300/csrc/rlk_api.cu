@@ -73,6 +73,20 @@ rlk_status check_common(const rlk_logp_contract* c, const void* logits, const in
     return RLK_OK;
 }
 
+// dlogits may be the logits buffer itself (in place: the kernels read every
+// logit before its gradient overwrites it) or a buffer of its own; any other
+// overlap would let one row's gradient land on logits not yet read.
+rlk_status check_dlogits_overlap(const void* logits, const void* dlogits, int64_t T, int64_t stride) {
+    if (logits == dlogits) return RLK_OK;
+    const uint64_t a = reinterpret_cast<uintptr_t>(logits), b = reinterpret_cast<uintptr_t>(dlogits);
+    const uint64_t rows = (uint64_t)T, st = (uint64_t)stride;
+    const uint64_t span = (st != 0 && rows > (UINT64_MAX / 2) / st) ? UINT64_MAX : rows * st * 2u;
+    if ((a < b ? b - a : a - b) < span)
+        return fail(RLK_ERR_INVALID_ARG, "dlogits overlaps logits without being the same buffer (only an exact "
+                                         "in-place call, dlogits == logits, may share memory)");
+    return RLK_OK;
+}
+
 // Makes the device that owns `ptr` current for this library's runtime.
 rlk_status select_device(const void* ptr) {
     cudaPointerAttributes attr{};
@@ -224,6 +238,9 @@ RLK_EXPORT rlk_status rlk_logp_fwd_bwd_entropy(const rlk_logp_contract* c, const
     if (!grad_logp) return fail(RLK_ERR_INVALID_ARG, "grad_logp is NULL");
     if (!dlogits_bf16) return fail(RLK_ERR_INVALID_ARG, "dlogits is NULL");
     if (!aligned16(dlogits_bf16)) return fail(RLK_ERR_MISALIGNED, "dlogits must be 16-byte aligned");
+    if ((s = check_dlogits_overlap(logits_bf16, dlogits_bf16, c->T, c->row_stride ? c->row_stride : c->V_padded)) !=
+        RLK_OK)
+        return s;
     if (!logp_out || !lse_out || !entropy_out)
         return fail(RLK_ERR_INVALID_ARG, "logp_out, lse_out and entropy_out are required");
     if ((s = select_device(logits_bf16)) != RLK_OK) return s;
@@ -276,6 +293,9 @@ RLK_EXPORT rlk_status rlk_logp_bwd(const rlk_logp_contract* c, const void* logit
     if (!grad_logp) return fail(RLK_ERR_INVALID_ARG, "grad_logp is NULL");
     if (!dlogits_bf16) return fail(RLK_ERR_INVALID_ARG, "dlogits is NULL");
     if (!aligned16(dlogits_bf16)) return fail(RLK_ERR_MISALIGNED, "dlogits must be 16-byte aligned");
+    if ((s = check_dlogits_overlap(logits_bf16, dlogits_bf16, c->T, c->row_stride ? c->row_stride : c->V_padded)) !=
+        RLK_OK)
+        return s;
     if (lse_in && (logp_out || lse_out))
         return fail(RLK_ERR_INVALID_ARG, "with lse_in the forward outputs logp_out/lse_out must be NULL");
     if (!lse_in && (!logp_out || !lse_out))
@@ -492,6 +512,9 @@ RLK_EXPORT rlk_status rlk_logp_shard_bwd(const rlk_logp_contract* c, int32_t sha
     if (!lse_in || !grad_logp) return fail(RLK_ERR_INVALID_ARG, "lse_in and grad_logp are required");
     if (!dlogits_shard) return fail(RLK_ERR_INVALID_ARG, "dlogits_shard is NULL");
     if (!aligned16(dlogits_shard)) return fail(RLK_ERR_MISALIGNED, "dlogits_shard must be 16-byte aligned");
+    if ((s = check_dlogits_overlap(logits_shard, dlogits_shard, c->T,
+                                   c->row_stride ? c->row_stride : c->V_padded / c->virtual_tp)) != RLK_OK)
+        return s;
     if ((s = select_device(logits_shard)) != RLK_OK) return s;
     if ((s = check_device_ptrs({{targets, "targets"}, {active_mask, "active_mask"}, {lse_in, "lse_in"},
                                 {grad_logp, "grad_logp"}, {dlogits_shard, "dlogits_shard"},
