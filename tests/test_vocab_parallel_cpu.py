@@ -12,7 +12,10 @@ host check.  What is tested is the layer's logic:
   order and owner-rank resolution of the target logit);
 * a rank whose call is invalid makes every rank raise, with no rank left
   waiting in a collective (the pages' review: rank-local validation failures
-  can strand the other TP ranks);
+  can strand the other TP ranks) -- whether the layer's own check, the C
+  library's contract check or the shard call's host checks reject it, in
+  the forward or in the backward;
+* the backward returns each rank's own shard;
 * token rows split over ranks cover every row once.
 """
 import json
@@ -89,7 +92,30 @@ class OracleOps:
         return torch.from_numpy(logp), torch.from_numpy(lse), full
 
     def shard_bwd(self, contract, shard, logits_shard, targets, mask, lse, grad):
-        raise AssertionError("not reached in these tests")
+        # a marker of the rank that computed it (the CUDA backward is checked on the GPU)
+        return torch.full(tuple(logits_shard.shape), shard, dtype=torch.int16)
+
+
+class FailingOps(OracleOps):
+    """The shard calls of one rank fail on the host, as the C library's pointer or device checks would."""
+
+    def __init__(self, lib_ops, failing_rank, failing_call):
+        super().__init__(lib_ops)
+        self.failing_rank = failing_rank
+        self.failing_call = failing_call
+
+    def _fail(self, shard, call):
+        import vocab_selected_token_tile_gb300 as rlk
+        if shard == self.failing_rank and call == self.failing_call:
+            raise rlk.RlkError(rlk.RLK_ERR_INVALID_ARG, "targets must be device memory (it is host memory)")
+
+    def shard_fwd(self, contract, shard, *args):
+        self._fail(shard, "fwd")
+        return super().shard_fwd(contract, shard, *args)
+
+    def shard_bwd(self, contract, shard, *args):
+        self._fail(shard, "bwd")
+        return super().shard_bwd(contract, shard, *args)
 
 
 def _rank_main(rank, world, port, case, out_dir):
@@ -108,7 +134,12 @@ def _rank_main(rank, world, port, case, out_dir):
             c = c.replace(num_tiles=6)  # 6 does not divide 1024: this rank's host check fails
         if case == "bad_shape" and rank == 0:
             shard = shard[:, :-8].contiguous()
-        layer = vp.VocabParallelLogp(c, ops=OracleOps(vp.KernelOps()))
+        ops = OracleOps(vp.KernelOps())
+        if case == "fwd_call_fails":
+            ops = FailingOps(vp.KernelOps(), failing_rank=1, failing_call="fwd")
+        if case in ("bwd_call_fails", "bwd_ok"):
+            ops = FailingOps(vp.KernelOps(), failing_rank=0 if case == "bwd_call_fails" else -1, failing_call="bwd")
+        layer = vp.VocabParallelLogp(c, ops=ops)
         try:
             logp, lse, full = layer.forward(shard, targets, m)
             res["ok"] = True
@@ -119,13 +150,19 @@ def _rank_main(rank, world, port, case, out_dir):
             res["ok"] = False
             res["status"] = e.status
             res["message"] = str(e)
-        if case == "bad_bwd":
+        if case in ("bad_bwd", "bad_bwd_dtype", "bwd_call_fails", "bwd_ok"):
+            lse = torch.zeros(T if rank == 0 or case != "bad_bwd" else T - 1)
+            if case == "bad_bwd_dtype" and rank == 1:
+                lse = lse.double()
             try:
-                layer.backward(shard, targets, m, torch.zeros(T if rank == 0 else T - 1), torch.zeros(T))
+                d = layer.backward(shard, targets, m, lse, torch.zeros(T))
                 res["bwd_ok"] = True
+                res["bwd_marker"] = sorted(set(d.flatten().tolist()))
+                res["bwd_shape"] = list(d.shape)
             except rlk.RlkError as e:
                 res["bwd_ok"] = False
                 res["bwd_status"] = e.status
+                res["bwd_message"] = str(e)
         dist.barrier()
     finally:
         dist.destroy_process_group()
@@ -158,20 +195,36 @@ def test_gather_order_and_fold_give_the_whole_row(built, tmp_path, world):
     assert res[0]["logp"] == res[1]["logp"]
 
 
-@pytest.mark.parametrize("case", ["bad_contract", "bad_shape", "bad_bwd"])
+@pytest.mark.parametrize("case", ["bad_contract", "bad_shape", "fwd_call_fails", "bad_bwd", "bad_bwd_dtype",
+                                  "bwd_call_fails"])
 def test_an_invalid_call_on_one_rank_fails_closed_on_every_rank(built, tmp_path, case):
+    """A host check that fails on one rank -- the layer's own, the contract check, or the shard call's
+    pointer checks -- makes every rank raise the same status, and no rank is left inside a collective
+    (the all-gather of the forward is never entered)."""
     import vocab_selected_token_tile_gb300 as rlk
     res = run(2, case, tmp_path)
-    if case == "bad_bwd":
+    if case.startswith("bad_bwd") or case == "bwd_call_fails":
         assert all(r["ok"] for r in res)  # the forward was valid on both ranks
         assert all(not r["bwd_ok"] for r in res)
         assert all(r["bwd_status"] == rlk.RLK_ERR_INVALID_ARG for r in res)
+        bad = 0 if case == "bwd_call_fails" else 1
+        assert "another rank" in res[1 - bad]["bwd_message"]
+        assert "another rank" not in res[bad]["bwd_message"]
         return
     assert all(not r["ok"] for r in res)
-    bad = 1 if case == "bad_contract" else 0
+    bad = 0 if case == "bad_shape" else 1
     want = rlk.RLK_ERR_NON_TILEABLE if case == "bad_contract" else rlk.RLK_ERR_INVALID_ARG
     assert res[bad]["status"] == want
     assert res[1 - bad]["status"] == want and "another rank" in res[1 - bad]["message"]
+    if case == "fwd_call_fails":
+        assert "device memory" in res[bad]["message"]
+
+
+def test_backward_returns_each_ranks_own_shard(built, tmp_path):
+    res = run(2, "bwd_ok", tmp_path)
+    for rank, r in enumerate(res):
+        assert r["ok"] and r["bwd_ok"]
+        assert r["bwd_marker"] == [rank] and r["bwd_shape"] == [T, V_PADDED // 2]
 
 
 def test_split_rows_covers_every_row_once():

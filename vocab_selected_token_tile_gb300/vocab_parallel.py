@@ -18,7 +18,9 @@ Forward, on every rank:
    collective (the pages' review of the vocab-parallel entry point raises
    exactly this);
 3. ``rlk_logp_shard_fwd`` on the rank's columns: partials [T, NT/tp, 2] and
-   the target logits it owns [T];
+   the target logits it owns [T].  The call's own host-side status (its
+   pointer and device checks) is agreed on the same way before the
+   exchange, so a call that fails on one rank fails on every rank;
 4. one all-gather of each (plain device buffers);
 5. ``rlk_logp_fold`` on the gathered partials, in global tile order: logp and
    LSE, replicated on every rank and bitwise those of ``rlk_logp_fwd`` on one
@@ -97,7 +99,16 @@ class VocabParallelLogp:
             return RLK_ERR_INVALID_ARG, "active_mask must be given in explicit mode and None in ignore_index mode"
         if mask is not None and (mask.dtype not in (torch.uint8, torch.bool) or mask.numel() != c.T):
             return RLK_ERR_INVALID_ARG, "active_mask must be uint8 [T]"
+        if targets.device != logits_shard.device or (mask is not None and mask.device != logits_shard.device):
+            return RLK_ERR_INVALID_ARG, "logits_shard, targets and active_mask must be on one device"
         return RLK_OK, ""
+
+    def _call(self, fn, *args):
+        """(status, message, result) of one per-rank computation; an RlkError becomes its status."""
+        try:
+            return RLK_OK, "", fn(*args)
+        except RlkError as e:
+            return e.status, str(e), None
 
     def _agree(self, status, message, device):
         """All-reduce (MAX) of the ranks' status codes; every rank raises if any rank's call is invalid."""
@@ -122,7 +133,9 @@ class VocabParallelLogp:
         """(logp, lse) of every row, replicated on every rank."""
         st, msg = self._local_check(logits_shard, targets, mask)
         self._agree(st, msg, targets.device)
-        part, xt = self.ops.shard_fwd(self.contract, self.rank, logits_shard, targets, mask)
+        st, msg, out = self._call(self.ops.shard_fwd, self.contract, self.rank, logits_shard, targets, mask)
+        self._agree(st, msg, targets.device)
+        part, xt = out
         gathered = torch.empty((self.tp,) + tuple(part.shape), dtype=part.dtype, device=part.device)
         gathered_xt = torch.empty((self.tp,) + tuple(xt.shape), dtype=xt.dtype, device=xt.device)
         self._all_gather(gathered, part)
@@ -132,7 +145,11 @@ class VocabParallelLogp:
     def backward(self, logits_shard, targets, mask, lse, grad):
         """BF16 dlogits of this rank's columns, from the replicated LSE; no exchange."""
         st, msg = self._local_check(logits_shard, targets, mask)
-        if st == RLK_OK and (lse.numel() != self.contract.T or grad.numel() != self.contract.T):
-            st, msg = RLK_ERR_INVALID_ARG, "lse and grad must be FP32 [T]"
+        if st == RLK_OK and any(t.dtype != torch.float32 or t.numel() != self.contract.T or
+                                t.device != logits_shard.device for t in (lse, grad)):
+            st, msg = RLK_ERR_INVALID_ARG, "lse and grad must be FP32 [T] on the logits' device"
         self._agree(st, msg, targets.device)
-        return self.ops.shard_bwd(self.contract, self.rank, logits_shard, targets, mask, lse, grad)
+        # no collective follows, but every rank still returns or raises together
+        st, msg, out = self._call(self.ops.shard_bwd, self.contract, self.rank, logits_shard, targets, mask, lse, grad)
+        self._agree(st, msg, targets.device)
+        return out
