@@ -36,13 +36,18 @@ def row_bufs(mode, nt):
     return 8 if (mode == "fused_l2" and nt <= 128) else 4
 
 
+def l2_cluster(vtp, nt):
+    """CTAs per cluster of the L2 fused schedule: virtual TP, but two at virtual TP 1 (even tile count)."""
+    return 2 if vtp == 1 and nt % 2 == 0 else vtp
+
+
 def ctas_per_sm(mode, vtp, v_padded, nt, sm_count=152, reuse_bytes=64 << 20):
     """CTAs per SM as the host planner picks them: two for the streaming modes, one for the
     resident fused schedule, two for the L2 fused schedule while one row of skew fits L2."""
     if mode in ("fwd", "bwd"):
         return 2
     if mode == "fused_l2":
-        row1 = -(-nt // vtp) * (v_padded // nt) * 2 * sm_count
+        row1 = -(-nt // l2_cluster(vtp, nt)) * (v_padded // nt) * 2 * sm_count
         return 2 if (reuse_bytes // (2 * row1) >= 2 or reuse_bytes // row1 < 2) else 1
     return 1
 
@@ -69,7 +74,7 @@ def plan(mode, vtp, v_padded, nt):
                 best = ns
         return best
 
-    C = 1 if mode == "bwd" else vtp
+    C = 1 if mode == "bwd" else l2_cluster(vtp, nt) if mode == "fused_l2" else vtp
     tps = tps_target
     if mode in ("fused_l2", "fwd", "bwd"):  # the largest divisor of the shard's tiles within 16384 columns
         ntl = nt // C
@@ -90,7 +95,7 @@ def plan(mode, vtp, v_padded, nt):
 
 
 def plan_l2(vtp, v_padded, nt):
-    """The L2-assisted fused mode is planned like the forward: C = virtual TP, no residency."""
+    """The L2-assisted fused mode is planned like the forward (C = virtual TP, two at TP 1), no residency."""
     return plan("fused_l2", vtp, v_padded, nt)
 
 
@@ -98,7 +103,7 @@ def l2_skew(vtp, v_padded, nt, sm_count=152, reuse_bytes=64 << 20):
     """Rows of skew of the L2-assisted fused mode, as the host planner picks them."""
     w = v_padded // nt
     per_sm = ctas_per_sm("fused_l2", vtp, v_padded, nt)
-    fit = reuse_bytes // (-(-nt // vtp) * w * 2 * sm_count * per_sm)
+    fit = reuse_bytes // (-(-nt // l2_cluster(vtp, nt)) * w * 2 * sm_count * per_sm)
     return max(0 if per_sm == 2 else 1, min(fit - 1, row_bufs("fused_l2", nt) - 1, 2))
 
 
@@ -132,10 +137,14 @@ def test_kernel_block_numbering_matches_the_schedule():
 
 
 def test_l2_skew_at_the_benchmark_shapes():
-    # 152 SMs, 152576 x 64 tiles: virtual TP 1 fits no row of skew (two CTAs
-    # per SM, none), 2 one at one CTA per SM, 4 one at two, 8 two (the cap)
-    assert [l2_skew(v, 152576, 64) for v in (1, 2, 4, 8)] == [0, 1, 1, 2]
-    assert [ctas_per_sm("fused_l2", v, 152576, 64) for v in (1, 2, 4, 8)] == [2, 1, 2, 2]
+    # 152 SMs, 152576 x 64 tiles: virtual TP 1 runs on clusters of two like
+    # TP 2 (one row of skew at one CTA per SM), 4 one at two, 8 two (the cap);
+    # 63 tiles at TP 1 (a whole row per CTA) fit no row of skew: two CTAs per
+    # SM, none
+    assert [l2_skew(v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 1, 2]
+    assert [ctas_per_sm("fused_l2", v, 152576, 64) for v in (1, 2, 4, 8)] == [1, 1, 2, 2]
+    assert plan_l2(1, 152576, 64)[0] == 2
+    assert (l2_cluster(1, 63), ctas_per_sm("fused_l2", 1, 63 * 2400, 63), l2_skew(1, 63 * 2400, 63)) == (1, 2, 0)
 
 
 CONFIGS = [(mode, vtp) for mode in ("fwd", "bwd", "fused", "fused_l2") for vtp in (1, 2, 4, 8)
@@ -155,7 +164,7 @@ def test_ring_protocol_reads_only_landed_slots(mode, vtp):
 def test_planner_replay_matches_the_benchmark_shapes():
     assert plan("fused", 2, 152576, 64) == (4, 2, 23)
     assert plan("fwd", 1, 152576, 64) == (1, 4, 5)
-    assert [plan("fused_l2", v, 152576, 64)[1:] for v in (1, 2, 4, 8)] == [(4, 5), (4, 11), (4, 5), (4, 5)]
+    assert [plan("fused_l2", v, 152576, 64)[1:] for v in (1, 2, 4, 8)] == [(4, 11), (4, 11), (4, 5), (4, 5)]
 
 
 @pytest.mark.parametrize("ns", [1, 2, 3, 5])

@@ -1345,6 +1345,14 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
             return fail(RLK_ERR_UNSUPPORTED, "the entropy is computed by the L2 fused schedule, not the resident one");
     }
     int C = (mode == kModeBwd) ? 1 : c.virtual_tp;
+    // The L2 fused schedule at virtual TP 1 splits each row over a cluster of
+    // two CTAs, as the resident schedule does when a row does not fit: every
+    // virtual shard is still computed by distinct CTAs and the fold runs in
+    // global tile order, so the bits are those of one CTA per row.  With a
+    // whole row per CTA the first copies of a row, across the GPU, put about
+    // 90 MB between its two reads (some second copies miss L2) and each CTA
+    // waits for its own row's fold.
+    if (mode == kModeFusedL2 && C == 1 && c.num_tiles % 2 == 0) C = 2;
     // The streaming modes take larger chunks where the CTA's shard allows:
     // the largest number of tiles that divides it and stays within
     // kFusedChunkCols columns (measured: 4 tiles of 2384 columns run 2-7%
@@ -1366,9 +1374,11 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     // memory.  The L2 fused schedule takes two while the rows between a row's
     // two copies, with one row of skew, still fit kL2ReuseBytes at twice the
     // CTAs (virtual TP 4 and 8 at 152576 x 64 tiles); else one while they fit
-    // at one CTA per SM (TP 2); else (TP 1, nothing fits) two with no skew,
-    // each CTA covering the other's wait for its row's LSE (measured on GB300:
-    // 6.3 ms against 6.6 for one CTA per SM with a row of skew).
+    // at one CTA per SM (TP 1 and 2); else (nothing fits: a row of an odd
+    // number of tiles per CTA, or a very wide one) two with no skew, each CTA
+    // covering the other's wait for its row's LSE (measured on GB300 with a
+    // whole 152576-column row per CTA: 6.3 ms against 6.6 for one CTA per SM
+    // with a row of skew).
     const int64_t shard_bytes = (int64_t)((c.num_tiles + C - 1) / C) * p.W * 2;
     int ctas_per_sm = (mode == kModeFwd || mode == kModeBwd) ? 2 : 1;
     if (mode == kModeFusedL2) {
