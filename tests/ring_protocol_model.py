@@ -71,17 +71,19 @@ def block_schedule(mode, rows, skew=1):
     return seq
 
 
-def row_skip_safe(W, ntl, rbufs):
-    """The planner's condition for the forward's row skip (row_skip_safe in logp_stream.cu): every
-    warp's first row below 2*rbufs and its consecutive rows at most rbufs apart."""
+def row_skip_safe(W, ntl, span, first_lim):
+    """The planner's condition for skipping rows without a tile (row_skip_safe in logp_stream.cu):
+    every warp's first row below first_lim and its consecutive rows at most span apart.  The
+    forward takes span = rbufs, first_lim = 2*rbufs; the L2 fused schedule span = rbufs - skew,
+    first_lim = rbufs."""
     if ntl >= W:
         return False
     step = ntl % W
     for w in range(W):
         last, r = -1, 0
-        for n in range(2 * W + 2 * rbufs):
+        for n in range(2 * W + 2 * first_lim):
             if (w - r) % W < ntl:
-                if (n >= 2 * rbufs) if last < 0 else (n - last > rbufs):
+                if (n >= first_lim) if last < 0 else (n - last > span):
                     return False
                 last = n
             r = (r + step) % W
@@ -90,23 +92,36 @@ def row_skip_safe(W, ntl, rbufs):
     return True
 
 
+def skip_condition(mode, W, ntl, rbufs, skew):
+    """row_skip_safe with the mode's span and first-row limit (False for modes that never skip)."""
+    if mode == "fwd":
+        return row_skip_safe(W, ntl, rbufs, 2 * rbufs)
+    if mode == "fused_l2":
+        return rbufs > skew and row_skip_safe(W, ntl, rbufs - skew, rbufs)
+    return False
+
+
 def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80, rbufs=2, skew=1,
-             producers=1, producer_seqcheck=True, row_skip=None):
+             producers=1, producer_seqcheck=True, row_skip=None, speeds=(0.02, 0.1, 0.5, 1.0)):
     """mode: 'fwd' | 'bwd' | 'fused' | 'fused_l2'; rbufs row buffers, fused_l2 row skew;
     producers: producer warps per CTA, producer p issuing the items i with i mod producers == p
     (each waits until the slot's previous item is issued before its empty-barrier parity,
     unless producer_seqcheck is off).
 
-    row_skip: the forward's skip of rows without a tile (None: the planner's condition).
+    row_skip: warps skip the rows in which they have no tile (the forward and the L2 fused
+    schedule; None: the planner's condition).
+
+    speeds: the chances per step that an agent moves, one drawn per agent (a very slow agent
+    stands for a warp held up for a long time).
 
     Raises ProtocolError on a stale read or a deadlock."""
     rng = random.Random(seed)
     ntl = NT // C
+    S = skew if mode == "fused_l2" else 1
     if row_skip is None:
-        row_skip = mode == "fwd" and row_skip_safe(W, ntl, rbufs)
+        row_skip = skip_condition(mode, W, ntl, rbufs, S)
     nch = (ntl + tps - 1) // tps
     R = rbufs
-    S = skew if mode == "fused_l2" else 1
     pushes = []  # in flight: [delay, receiver CTA, kind, buffer, index, value]
 
     def folder(n):
@@ -196,7 +211,7 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
 
     def phase_a(c, w, n):
         b = n % R
-        if row_skip and not tiles_of(w, n):  # forward: a warp without tiles skips the row
+        if row_skip and not tiles_of(w, n):  # a warp without tiles skips the row
             return
         if n >= R:
             yield from wait(c.partfree[b], (n // R - 1) & 1)
@@ -240,6 +255,8 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
             for n in range(rows):
                 if n + S < rows:
                     yield from phase_a(c, w, n + S)
+                if row_skip and not tiles_of(w, n):  # no tile: neither the LSE nor phase B
+                    continue
                 yield from wait(c.lseready[n % R], (n // R) & 1)
                 yield from phase_b(c, w, n)
 
@@ -307,7 +324,7 @@ def simulate(mode, rows, C, NT, tps, NS, W, seed=0, seqcheck=True, max_delay=80,
         if mode != "bwd":
             agents.append(fold(c))
         agents.extend(consumer(c, w) for w in range(W))
-    speed = {id(a): rng.choice([0.02, 0.1, 0.5, 1.0]) for a in agents}
+    speed = {id(a): rng.choice(list(speeds)) for a in agents}
     live = list(agents)
     idle = 0
     while live:

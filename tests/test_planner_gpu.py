@@ -13,7 +13,7 @@ import sys
 import pytest
 import torch
 
-from ring_protocol_model import row_skip_safe
+from ring_protocol_model import skip_condition
 from test_ring_protocol import SMEM_OPTIN, consumers_for, ctas_per_sm, l2_skew, plan, row_bufs
 
 pytestmark = pytest.mark.gpu
@@ -65,5 +65,5 @@ def test_compiled_planner_matches_the_replay():
             assert rb == row_bufs(want_mode, 64), (want_mode, vtp)
             if want_mode == "fused_l2":
                 assert skew == l2_skew(vtp, 152576, 64), vtp
-            want_skip = want_mode == "fwd" and row_skip_safe(consumers_for("fwd", per_sm), 64 // C, rb)
+            want_skip = skip_condition(want_mode, consumers_for(want_mode, per_sm), 64 // C, rb, skew)
             assert skip == int(want_skip), (want_mode, vtp)

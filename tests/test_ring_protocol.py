@@ -10,7 +10,7 @@ finds it); with the check, no configuration reads a stale slot or deadlocks.
 """
 import pytest
 
-from ring_protocol_model import ProtocolError, block_schedule, row_skip_safe, simulate
+from ring_protocol_model import ProtocolError, block_schedule, row_skip_safe, simulate, skip_condition
 
 SMEM_OPTIN = 232448
 
@@ -269,9 +269,60 @@ def test_forward_row_skip_condition():
     # virtual TP 8 at 64 tiles (8 tiles per CTA and row, 12 consumer warps): each warp works two
     # rows of every three, so its partfree parity wait stays within one phase; at 1-2 tiles per
     # row a warp works one row in 6 or 12 and the skip is off
-    assert row_skip_safe(12, 8, 4) and row_skip_safe(12, 4, 4)
-    assert not row_skip_safe(12, 2, 4) and not row_skip_safe(12, 1, 4)
-    assert not row_skip_safe(12, 12, 4) and not row_skip_safe(12, 64, 4)
+    assert skip_condition("fwd", 12, 8, 4, 1) and skip_condition("fwd", 12, 4, 4, 1)
+    assert not skip_condition("fwd", 12, 2, 4, 1) and not skip_condition("fwd", 12, 1, 4, 1)
+    assert not skip_condition("fwd", 12, 12, 4, 1) and not skip_condition("fwd", 12, 64, 4, 1)
+    assert row_skip_safe(12, 8, 4, 8) == skip_condition("fwd", 12, 8, 4, 1)
+
+
+def test_fused_row_skip_condition():
+    # The L2 fused schedule: a warp's consecutive rows at most rbufs - skew apart (a warp still in
+    # phase B of row n then has a tile in a row of (n + skew, n + rbufs], whose phase A holds back
+    # the fold that reuses row n's buffer) and its first row below rbufs (its first LSE wait).
+    # Virtual TP 8 at 64 tiles (12 warps, 8 tiles, 8 row buffers, skew 2): rows 2 apart -> on.
+    assert skip_condition("fused_l2", 12, 8, 8, 2)
+    assert skip_condition("fused_l2", 12, 8, 4, 2)          # span 2 = rbufs - skew
+    assert not skip_condition("fused_l2", 12, 8, 3, 2)      # span 1 < 2
+    assert skip_condition("fused_l2", 12, 4, 8, 2)          # rows 3 apart (virtual TP 8 at 32 tiles)
+    assert not skip_condition("fused_l2", 12, 4, 4, 2)      # rows 3 apart > span 2
+    assert not skip_condition("fused_l2", 16, 2, 8, 2)      # rows 8 apart > 6
+    assert not skip_condition("fused_l2", 12, 12, 8, 2)     # every warp has a tile in every row
+    assert not skip_condition("fused", 12, 8, 8, 1) and not skip_condition("bwd", 12, 8, 8, 1)
+
+
+SLOW = (0.002, 0.5, 1.0)  # some agents move once in ~500 steps: a warp held up for a long time
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_fused_row_skip_at_virtual_tp8(seed):
+    # the bench's TP 8 shape: 8 CTAs x 8 tiles, 2 copies of 4 tiles per row, 12 warps, 8 row
+    # buffers, skew 2, the skip on by the planner's condition; the same with very slow agents and
+    # a deep ring (other warps may run far ahead), and with 4 row buffers (span 2, the limit)
+    simulate("fused_l2", rows=60, C=8, NT=64, tps=4, NS=5, W=12, seed=seed, rbufs=8, skew=2, max_delay=150)
+    simulate("fused_l2", rows=60, C=8, NT=64, tps=4, NS=24, W=12, seed=seed, rbufs=8, skew=2, max_delay=50,
+             speeds=SLOW)
+    simulate("fused_l2", rows=60, C=8, NT=64, tps=4, NS=24, W=12, seed=seed, rbufs=4, skew=2, max_delay=50,
+             row_skip=True, speeds=SLOW)
+    simulate("fused_l2", rows=60, C=4, NT=32, tps=4, NS=5, W=12, seed=seed, rbufs=8, skew=1, max_delay=150,
+             row_skip=True, producers=2)
+
+
+def test_fused_row_skip_without_the_condition_is_caught():
+    # 2 tiles per CTA and row over 16 warps: a warp works one row in 8.  With 4 row buffers and
+    # skew 1, while a slow warp waits for row n's LSE, the others run ahead and the fold of row
+    # n + 4 overwrites it (or its parity passes two phases on); the model finds it.  Without the
+    # skip (the planner's condition keeps it off here) every seed passes.
+    assert not skip_condition("fused_l2", 16, 2, 4, 1)
+    found = 0
+    for seed in range(8):
+        try:
+            simulate("fused_l2", rows=80, C=2, NT=4, tps=1, NS=40, W=16, seed=seed, rbufs=4, skew=1, max_delay=50,
+                     row_skip=True, speeds=SLOW)
+        except ProtocolError:
+            found += 1
+        simulate("fused_l2", rows=80, C=2, NT=4, tps=1, NS=40, W=16, seed=seed, rbufs=4, skew=1, max_delay=50,
+                 speeds=SLOW)
+    assert found > 0
 
 
 def test_forward_row_skip_without_the_condition_is_caught():

@@ -127,7 +127,7 @@ struct Params {
     int32_t rbufs, rb_shift;  // row buffers of the fold (a power of two) and its log2
     int32_t skew;             // kModeFusedL2: phase A runs `skew` rows ahead of phase B (< rbufs)
     int32_t ent;  // the launch computes the entropy (stream_kernel's ENT)
-    int32_t row_skip;  // kModeFwd: consumer warps skip the rows in which they have no tile (row_skip_safe)
+    int32_t row_skip;  // kModeFwd, kModeFusedL2: consumer warps skip the rows in which they have no tile (row_skip_safe)
     uint32_t off_full, off_empty, off_hdr, off_seq, off_part, off_fold, off_rows, off_xtin, off_bars, off_flag;
     uint32_t off_meta;  // TileMeta of each of the CTA's tiles
     uint32_t off_tpart, off_foldt;  // ENT: t_k per row buffer, and the fold's scratch for them
@@ -953,14 +953,14 @@ struct TileRotation {
 // for phase B.
 template <int MODE, int W, bool ENT>
 __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0, int first) {
-    // Forward with row_skip: a warp with no tile in the row (ntl < NW) skips
-    // it: it writes nothing, and rowdone counts only the min(NW, ntl) warps
-    // that have tiles.  Each of those waits for partfree of row n - rbufs
-    // first, and the planner allows the skip only where that parity wait
-    // stays within one phase (row_skip_safe).  The fused modes keep every
-    // warp in every row: the LSE of row n must outlive phase B of row n in
-    // every warp.
-    if (MODE == kModeFwd && p.row_skip && first >= x.ntl) return true;
+    // With row_skip (the forward and the L2 fused schedule) a warp with no
+    // tile in the row (ntl < NW) skips it: it writes nothing, and rowdone
+    // counts only the min(NW, ntl) warps that have tiles.  Each of those
+    // waits for partfree of row n - rbufs first; the planner allows the skip
+    // only where that parity wait stays within one phase and, fused, where
+    // the row's LSE outlives every phase B that reads it (row_skip_safe).
+    // The resident fused schedule keeps every warp in every row.
+    if ((MODE == kModeFwd || MODE == kModeFusedL2) && p.row_skip && first >= x.ntl) return true;
     const int lane = x.lane;
     const int b = row_buf(p, n);
     bool ok = true;
@@ -1067,11 +1067,13 @@ __device__ void consumer(const Params& p, const Ctx& x) {
         for (int64_t n = 0; n < R; ++n) {
             if (n + S < R) phase_a<MODE, NW, ENT>(p, x, n + S, item_a(n + S), rot_a.next(x.warp));
             const int b = row_buf(p, n);
+            const int first_b = rot_b.next(x.warp);
+            // row_skip: no tile in this row, so neither its LSE nor phase B
+            if (MODE == kModeFusedL2 && p.row_skip && first_b >= x.ntl) continue;
             const bool ready = x.wt.warp_wait(x.lseready0 + 8u * b, row_par(p, n));
             // A failed wait anywhere sets the abort flag; the slot headers may
             // then be stale, so skip the writes (the status word already says
             // RLK_ERR_TIMEOUT).
-            const int first_b = rot_b.next(x.warp);
             if (ready && !*x.wt.abort_flag) phase_b<MODE, NW>(p, x, n, item_b(n), x.rows[b].lse, first_b);
         }
     }
@@ -1124,7 +1126,8 @@ __global__ void __launch_bounds__(threads_for(MODE, PER_SM), PER_SM)
             x.seq[s] = 0xFFFFFFFFu;
         }
         for (int b = 0; b < p.rbufs; ++b) {
-            mbar_init(x.rowdone0 + 8u * b, (uint32_t)(MODE == kModeFwd && p.row_skip ? min(NW, x.ntl) : NW));
+            mbar_init(x.rowdone0 + 8u * b,
+                      (uint32_t)((MODE == kModeFwd || MODE == kModeFusedL2) && p.row_skip ? min(NW, x.ntl) : NW));
             mbar_init(x.lseready0 + 8u * b, 1);
             mbar_init(x.partfree0 + 8u * b, 1);
             mbar_init(x.xbar0 + 8u * b, 1);    // the local arrival (with expect-tx on the folder)
@@ -1221,22 +1224,31 @@ FastDiv make_fastdiv(uint32_t d) {
     return f;
 }
 
-// Whether forward consumer warps may skip the rows in which they have no
-// tile.  A warp still waits for the release of row n - rbufs (a parity wait
-// on partfree) before each row it works on, and a parity wait is right only
-// while the barrier is within one phase of it: row n - 2*rbufs must already
-// be released.  That holds when every warp's first row is below 2*rbufs and
-// its consecutive rows are at most rbufs apart (its previous wait then
-// covered row n - 2*rbufs); the tile rotation repeats within NW rows.
-bool row_skip_safe(int NW, int ntl, int rbufs) {
-    if (ntl >= NW) return false;  // every warp has a tile in every row
+// Whether consumer warps may skip the rows in which they have no tile:
+// every warp's first row below first_lim and its consecutive rows at most
+// span apart (the tile rotation repeats within NW rows).
+//  * Forward (span rbufs, first_lim 2*rbufs).  A warp still waits for the
+//    release of row n - rbufs (a parity wait on partfree) before each row it
+//    works on, and a parity wait is right only while the barrier is within
+//    one phase of it: row n - 2*rbufs must already be released, which the
+//    warp's previous wait covered.
+//  * L2 fused schedule with skew S (span rbufs - S, first_lim rbufs).  Also
+//    a warp in phase B of row n reads rows[b].lse, which the fold of row
+//    n + rbufs overwrites.  That fold needs phase A of every row up to
+//    n + rbufs in every warp with a tile there (the pushes go in row order);
+//    a warp's phase A of rows above n + S comes after its phase B of row n,
+//    and rows at most rbufs - S apart put one of them in (n + S, n + rbufs].
+//    The first row below rbufs keeps the first lseready parity wait within
+//    one phase.
+bool row_skip_safe(int NW, int ntl, int span, int first_lim) {
+    if (ntl >= NW || span < 1) return false;  // every warp has a tile in every row
     const int step = ntl % NW;
     for (int w = 0; w < NW; ++w) {
         int last = -1, r = 0;
-        for (int n = 0; n < 2 * NW + 2 * rbufs; ++n) {
+        for (int n = 0; n < 2 * NW + 2 * first_lim; ++n) {
             const int f = ((w - r) % NW + NW) % NW;
             if (f < ntl) {
-                if (last < 0 ? n >= 2 * rbufs : n - last > rbufs) return false;
+                if (last < 0 ? n >= first_lim : n - last > span) return false;
                 last = n;
             }
             r = (r + step) % NW;
@@ -1528,7 +1540,13 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     if (clusters <= 0) return RLK_ERR_CUDA;
     void (*kfn)(Params) = pick(ctas_per_sm);
     cfg.blockDim = dim3(threads_for(mode, ctas_per_sm), 1, 1);
-    p.row_skip = (mode == kModeFwd && row_skip_safe(consumers_for(mode, ctas_per_sm), ntl_cta, p.rbufs)) ? 1 : 0;
+    {
+        const int nw = consumers_for(mode, ctas_per_sm);
+        p.row_skip = (mode == kModeFwd && row_skip_safe(nw, ntl_cta, p.rbufs, 2 * p.rbufs)) ||
+                             (mode == kModeFusedL2 && row_skip_safe(nw, ntl_cta, p.rbufs - p.skew, p.rbufs))
+                         ? 1
+                         : 0;
+    }
     p.NS = NS;
     p.ns_div = make_fastdiv((uint32_t)NS);
     smem = layout(p, NS);
