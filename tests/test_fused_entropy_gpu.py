@@ -43,17 +43,22 @@ def test_fused_entropy_small_cases(case):
 def test_fused_entropy_qwen3_shape_and_special_rows(monkeypatch):
     from synth import workloads as W
     v_real, v_padded, nt = 1000, 1024, 64
-    bits = synth.logits_host(0, 4, v_padded, v_padded, v_real, seed=9, sigma=2.0)
+    bits = synth.logits_host(0, 5, v_padded, v_padded, v_real, seed=9, sigma=2.0)
     bits[1, :v_real] = 0xFF80          # all -inf: NaN entropy
     bits[2, :v_real] = 0xFF80
     bits[2, 500] = 0x3F80              # one finite column: entropy 0
-    c = contract(4, v_real, v_padded, nt, 2, rlk.MASK_IGNORE_INDEX, validate=0)
-    tg = torch.full((4,), -100, dtype=torch.int64).cuda()
-    _, _, _, ent = rlk.logp_fwd_bwd_entropy(c, to_dev(bits), tg, None, torch.zeros(4).cuda())
-    torch.cuda.synchronize()
-    e = ent.cpu().numpy()
-    assert np.isnan(e[1]) and e[2] == 0.0
-    check_entropy(bits, v_real, e)
+    bits[3, 3:v_real:7] = 0xFF80       # -inf logits scattered among finite ones, in every tile
+    bits[4, 640:656] = 0xFF80          # one whole tile -inf beside finite tiles
+    tg = torch.full((5,), -100, dtype=torch.int64).cuda()
+    for vtp in (1, 2, 8):
+        c = contract(5, v_real, v_padded, nt, vtp, rlk.MASK_IGNORE_INDEX, validate=0)
+        _, _, lse, ent = rlk.logp_fwd_bwd_entropy(c, to_dev(bits), tg, None, torch.zeros(5).cuda())
+        _, _, e0 = rlk.logp_fwd_entropy(c, to_dev(bits), tg)
+        torch.cuda.synchronize()
+        e = ent.cpu().numpy()
+        assert np.isnan(e[1]) and e[2] == 0.0 and np.all(np.isfinite(e[[0, 3, 4]]))
+        check_entropy(bits, v_real, e)
+        assert np.array_equal(e.view(np.uint32), e0.cpu().numpy().view(np.uint32)), vtp
 
     w = W.QWEN3
     qbits = W.logits_host(w)

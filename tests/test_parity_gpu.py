@@ -242,20 +242,29 @@ def test_entropy_small_cases(case):
 
 
 def test_entropy_special_rows_and_qwen3_shape(monkeypatch):
-    """Rows with one finite column (entropy 0) and no finite column (NaN);
-    then the Qwen3-shaped batch, every 13th row against the oracle, at one
-    and two CTAs per SM and every virtual TP, bitwise equal."""
+    """Rows with one finite column (entropy 0), no finite column (NaN) and
+    -inf logits scattered among finite ones (a -inf term adds 0, which the
+    tile sum takes from its clamped redo); then the Qwen3-shaped batch, every
+    13th row against the oracle, at one and two CTAs per SM and every virtual
+    TP, bitwise equal."""
     v_real, v_padded, nt = 1000, 1024, 64
-    bits = synth.logits_host(0, 4, v_padded, v_padded, v_real, seed=9, sigma=2.0)
+    bits = synth.logits_host(0, 5, v_padded, v_padded, v_real, seed=9, sigma=2.0)
     bits[1, :v_real] = 0xFF80          # all -inf
     bits[2, :v_real] = 0xFF80
     bits[2, 500] = 0x3F80              # one finite column (1.0)
-    c = contract(4, v_real, v_padded, nt, 2, rlk.MASK_IGNORE_INDEX, validate=0)
-    _, lse, ent = rlk.logp_fwd_entropy(c, to_dev(bits), torch.full((4,), -100, dtype=torch.int64).cuda())
+    bits[3, 3:v_real:7] = 0xFF80       # every 7th column -inf, in every tile
+    bits[4, 640:656] = 0xFF80          # one whole tile -inf (identity partial) beside finite tiles
+    c = contract(5, v_real, v_padded, nt, 2, rlk.MASK_IGNORE_INDEX, validate=0)
+    dbits = to_dev(bits)
+    tgt5 = torch.full((5,), -100, dtype=torch.int64).cuda()
+    _, lse, ent = rlk.logp_fwd_entropy(c, dbits, tgt5)
     torch.cuda.synchronize()
     e = ent.cpu().numpy()
     assert np.isnan(e[1]) and e[2] == 0.0
+    assert np.all(np.isfinite(e[[0, 3, 4]]))
     check_entropy(bits, v_real, e)
+    _, lse_plain = rlk.logp_fwd(c, dbits, tgt5)
+    assert torch.equal(lse, lse_plain)  # the clamped redo leaves the LSE bitwise that of the plain forward
 
     from synth import workloads as W
     w = W.QWEN3

@@ -353,15 +353,18 @@ __device__ __forceinline__ void sum8(float2 (&s)[4], const uint4& v, float nmL) 
 
 // sum8 plus t[j] += e x for the same terms (the tile's sum_c e^(x_c - m) x_c).
 // A -inf column (padding, masked edges, or a -inf logit) must add 0 to t, not
-// 0 * -inf: the pair is first clamped to the largest finite negative BF16
-// (max.NaN keeps a NaN).  Its term e stays exactly 0 (x log2e overflows to
-// -inf), so s is bitwise that of sum8.
+// 0 * -inf.  CLAMP: the pair is first clamped to the largest finite negative
+// BF16 (max.NaN keeps a NaN); its term e stays exactly 0 (x log2e overflows
+// to -inf), so s is bitwise that of sum8.  Without CLAMP a finite pair gives
+// the same bits, and a -inf one makes t NaN (tile_partial then redoes the
+// tile with CLAMP).
+template <bool CLAMP>
 __device__ __forceinline__ void sum8_ent(float2 (&s)[4], float2 (&t)[4], const uint4& v, float nmL) {
     const float2 c = make_float2(nmL, nmL);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float2 x = bf16x2_to_f32x2(bf16x2_max_nan(w[j], 0xFF7FFF7Fu));
+        const float2 x = bf16x2_to_f32x2(CLAMP ? bf16x2_max_nan(w[j], 0xFF7FFF7Fu) : w[j]);
         const float2 e = exp_terms2(x, c);
         s[j] = fadd2(s[j], e);
         t[j] = ffma2(e, x, t[j]);
@@ -378,7 +381,13 @@ __device__ __forceinline__ float combine8(const float2 (&a)[4]) {
 // tile maximum is exact, the sum uses 8 accumulators combined pairwise, then
 // a fixed xor butterfly across lanes.  ENT: also t_k = sum_c e^(x_c - m_k) x_c
 // into *t_out, accumulated beside s in the same order (s is unchanged).
-template <bool ENT>
+//
+// ENT_CLAMP (ENT only): clamp every pair, interior groups too.  Otherwise
+// interior groups skip the clamp and the rare tile whose t comes out NaN is
+// redone clamped; both give the same bits.  Measured on GB300: skipping it
+// speeds the forward with entropy by 2-3.5% and slows the fused schedule's
+// larger kernel by 4-6%, so the fused schedule clamps everywhere.
+template <bool ENT, bool ENT_CLAMP = true>
 __device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const TileGeom& t, const GroupRange& gr,
                                int lane, float* t_out) {
     if (ENT) *t_out = 0.f;
@@ -401,12 +410,27 @@ __device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const
             sum8(sm, load_group(slot, grow, t.a + 8 * edge_group(gr, e), t), nmL);
         return make_float2(m, warp_sum(combine8(sm)));
     } else {
+        // Without ENT_CLAMP interior groups (real logits only) skip the
+        // clamp, which only a -inf logit needs.  Edge groups (masked columns
+        // read as -inf) always clamp.
         float2 tm[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll 4
-        for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) sum8_ent(sm, tm, s4[gi], nmL);
+        for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) sum8_ent<ENT_CLAMP>(sm, tm, s4[gi], nmL);
         for (int e = lane; e < ne; e += 32)
-            sum8_ent(sm, tm, load_group(slot, grow, t.a + 8 * edge_group(gr, e), t), nmL);
-        *t_out = warp_sum(combine8(tm));
+            sum8_ent<true>(sm, tm, load_group(slot, grow, t.a + 8 * edge_group(gr, e), t), nmL);
+        float tk = warp_sum(combine8(tm));
+        if (!ENT_CLAMP && __builtin_expect(isnan(tk), 0) && !isnan(m)) {
+            // t is NaN but no logit is: a -inf logit met 0 * -inf.  Redo the
+            // tile with every pair clamped (the same operations in the same
+            // order as the fast path wherever a pair is finite).
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sm[j] = tm[j] = make_float2(0.f, 0.f);
+            for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) sum8_ent<true>(sm, tm, s4[gi], nmL);
+            for (int e = lane; e < ne; e += 32)
+                sum8_ent<true>(sm, tm, load_group(slot, grow, t.a + 8 * edge_group(gr, e), t), nmL);
+            tk = warp_sum(combine8(tm));
+        }
+        *t_out = tk;
         return make_float2(m, warp_sum(combine8(sm)));
     }
 }
@@ -985,7 +1009,7 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
         const TileGeom& tg = m.g;
         const uint16_t* sl = slots + (size_t)it.slot * slot_elems + m.soff;
         float tk = 0.f;
-        const float2 pr = tile_partial<ENT>(sl, grow, tg, m.ga, lane, &tk);
+        const float2 pr = tile_partial<ENT, MODE != kModeFwd>(sl, grow, tg, m.ga, lane, &tk);
         if (lane == 0) {
             RowShared& rs = x.rows[b];
             if (l == 0) {
