@@ -1577,6 +1577,14 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
     cfg.dynamicSmemBytes = smem;
     cudaError_t e = cudaSuccess;
     if (clusters > p.T) clusters = p.T;
+    {
+        // Ring items are numbered in 32 bits per CTA (two blocks of nch
+        // chunks per row in the fused schedules); no wrap is allowed.
+        const int64_t rows_cta = (p.T + clusters - 1) / clusters;
+        const int64_t nch_cta = (ntl_cta + p.tps - 1) / p.tps;
+        if (rows_cta * 2 * nch_cta >= ((int64_t)1 << 31))
+            return fail(RLK_ERR_UNSUPPORTED, "too many rows per CTA for the slot ring's 32-bit item numbers");
+    }
     cfg.gridDim = dim3((unsigned)(clusters * p.C), 1, 1);
     if (env_int("RLK_VERBOSE", 0))
         std::fprintf(stderr,
