@@ -196,6 +196,36 @@ rlk_status rlk_grpo_loss(int64_t T, const float* logp, const float* advantage, c
                          rlk_stream_t stream);
 
 /*
+ * The GRPO training step of the logits in one pass over them: logp, LSE,
+ * the GRPO loss, its gradient g and dlogits = g (onehot - softmax), with or
+ * without the KL term.  rlk_grpo_loss's g depends on logp, so composed from
+ * the calls above the step needs rlk_logp_fwd, rlk_grpo_loss, then
+ * rlk_logp_bwd with lse_in (the logits read twice).  Here each row's g is
+ * formed on chip as soon as the fused pass has the row's logp, by exactly
+ * the operations rlk_grpo_loss uses, and the row's dlogits follow at once.
+ * The loss, g, logp, LSE and dlogits are bitwise those of that composition.
+ *   contract      as for rlk_logp_bwd (either mask mode); runs the L2 fused
+ *                 schedule (RLK_FUSED_SCHEDULE=resident: RLK_ERR_UNSUPPORTED).
+ *   advantage     [T] FP32, per row (broadcast per-sequence values).
+ *   ref_logp      [T] FP32, or NULL for no KL term; beta >= 0 as for
+ *                 rlk_grpo_loss.  N = the contract's active rows.
+ *   dlogits_bf16  [T, row_stride] out, as for rlk_logp_bwd; may be the
+ *                 logits themselves (in place).
+ *   logp_out, lse_out, grad_out  [T] FP32 out (grad_out: g of every row).
+ *   entropy_out   [T] FP32 out, or NULL: the entropy of each row's softmax
+ *                 (bitwise rlk_logp_fwd_entropy's).
+ *   loss          one FP32 out; active_count NULL or one FP32 out (N).
+ *   workspace     rlk_grpo_fused_workspace_size bytes.
+ * T = 0 writes loss = 0 (and N = 0).  Status as for rlk_logp_bwd.
+ */
+size_t rlk_grpo_fused_workspace_size(const rlk_logp_contract* contract);
+rlk_status rlk_grpo_fused_step(const rlk_logp_contract* contract, const void* logits_bf16, const int64_t* targets,
+                               const uint8_t* active_mask, const float* advantage, const float* ref_logp,
+                               float beta, void* dlogits_bf16, float* logp_out, float* lse_out, float* grad_out,
+                               float* entropy_out, float* loss, float* active_count, void* workspace,
+                               rlk_stream_t stream);
+
+/*
  * Backward (and, with lse_in == NULL, the fused single-pass forward+backward).
  *   grad_logp    [T] FP32: upstream gradient g_r of logp_r (used on active rows).
  *   dlogits_bf16 [T, row_stride] BF16 out, 16-byte aligned: columns

@@ -208,3 +208,29 @@ def test_dlogits_may_alias_logits_only_exactly(built):
     assert "overlaps logits" in rlk.rlk_last_error_message()
     rlk.rlk_logp_shard_bwd(cs, 0, base, 0x2000, 0x3000, 0x4000, 0x5000, base + sspan, 0x6000, None)
     assert "overlaps" not in rlk.rlk_last_error_message()
+
+
+def test_grpo_fused_step_fails_closed_on_the_host(built):
+    """The fused GRPO step checks its arguments before any CUDA call: a missing loss, a bad beta, a missing
+    advantage or output, a misaligned or partly overlapping dlogits."""
+    c = ok_contract(T=8)
+    assert rlk.rlk_grpo_fused_workspace_size(c) >= 256 + 256 + 256
+    assert rlk.rlk_grpo_fused_workspace_size(ok_contract(num_tiles=63)) == 0
+    base = 0x10000000
+
+    def call(**kw):
+        a = dict(logits=base, targets=0x2000, mask=0x3000, adv=0x4000, ref=None, beta=0.01, dl=0x20000000,
+                 logp=0x5000, lse=0x6000, grad=0x7000, ent=None, loss=0x8000, count=None, ws=0x9000)
+        a.update(kw)
+        return rlk.rlk_grpo_fused_step(c, a["logits"], a["targets"], a["mask"], a["adv"], a["ref"], a["beta"], a["dl"],
+                                       a["logp"], a["lse"], a["grad"], a["ent"], a["loss"], a["count"], a["ws"], None)
+    assert call(loss=None) == rlk.RLK_ERR_INVALID_ARG and "loss" in rlk.rlk_last_error_message()
+    assert call(beta=-1.0) == rlk.RLK_ERR_INVALID_ARG and "beta" in rlk.rlk_last_error_message()
+    assert call(beta=float("nan")) == rlk.RLK_ERR_INVALID_ARG
+    assert call(adv=None) == rlk.RLK_ERR_INVALID_ARG and "advantage" in rlk.rlk_last_error_message()
+    assert call(grad=None) == rlk.RLK_ERR_INVALID_ARG
+    assert call(dl=0x20000008) == rlk.RLK_ERR_MISALIGNED
+    assert call(dl=base + 16) == rlk.RLK_ERR_INVALID_ARG and "overlaps" in rlk.rlk_last_error_message()
+    assert call(mask=None) == rlk.RLK_ERR_INVALID_ARG  # explicit mode needs the mask
+    # everything well-formed: the call gets as far as the device check (no GPU here)
+    assert call() == rlk.RLK_ERR_INVALID_ARG and "CUDA pointer" in rlk.rlk_last_error_message()

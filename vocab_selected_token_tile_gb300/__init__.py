@@ -34,6 +34,8 @@ EXPORTED = (
     "rlk_logp_fwd_entropy",
     "rlk_logp_fwd_bwd_entropy",
     "rlk_grpo_loss",
+    "rlk_grpo_fused_workspace_size",
+    "rlk_grpo_fused_step",
     "rlk_logp_lmhead_workspace_size",
     "rlk_logp_fused_lmhead",
     "rlk_logp_fused_lmhead_bwd",
@@ -115,6 +117,10 @@ def library():
         lib.rlk_logp_fwd_bwd_entropy.restype = i
         lib.rlk_grpo_loss.argtypes = [ctypes.c_int64, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp]
         lib.rlk_grpo_loss.restype = i
+        lib.rlk_grpo_fused_workspace_size.argtypes = [P]
+        lib.rlk_grpo_fused_workspace_size.restype = ctypes.c_size_t
+        lib.rlk_grpo_fused_step.argtypes = [P, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.rlk_grpo_fused_step.restype = i
         lib.rlk_logp_check_shard_contract.argtypes = [P, ctypes.c_int32]
         lib.rlk_logp_check_shard_contract.restype = i
         lib.rlk_logp_shard_workspace_size.argtypes = [P]
@@ -190,6 +196,17 @@ def rlk_logp_fwd_bwd_entropy(contract, logits, targets, active_mask, grad_logp, 
 def rlk_grpo_loss(T, logp, advantage, active_mask, ref_logp, beta, loss, grad_logp, active_count, stream):
     return library().rlk_grpo_loss(T, logp, advantage, active_mask, ref_logp, beta, loss, grad_logp, active_count,
                                    stream)
+
+
+def rlk_grpo_fused_workspace_size(contract):
+    return library().rlk_grpo_fused_workspace_size(ctypes.byref(contract))
+
+
+def rlk_grpo_fused_step(contract, logits, targets, active_mask, advantage, ref_logp, beta, dlogits, logp_out, lse_out,
+                        grad_out, entropy_out, loss, active_count, workspace, stream):
+    return library().rlk_grpo_fused_step(ctypes.byref(contract), logits, targets, active_mask, advantage, ref_logp,
+                                         beta, dlogits, logp_out, lse_out, grad_out, entropy_out, loss, active_count,
+                                         workspace, stream)
 
 
 def rlk_logp_fwd_noalloc(contract, logits, targets, active_mask, logp, lse, partials, stream):
@@ -319,6 +336,30 @@ def grpo_loss(logp, advantage, mask, ref_logp=None, beta=0.0, stream=None):
     check(rlk_grpo_loss(T, _ptr(logp), _ptr(advantage), _ptr(mask), _ptr(ref_logp), float(beta), _ptr(loss),
                         _ptr(g), _ptr(count), _stream(stream)))
     return loss, g, count
+
+
+def grpo_fused_step(contract, logits, targets, mask, advantage, ref_logp=None, beta=0.0, dlogits=None,
+                    entropy=False, stream=None, workspace=None):
+    """The GRPO step in one pass over the logits: a dict of dlogits, logp, lse, grad (g), loss and active_count
+    (1-element), and entropy if asked; bitwise logp_fwd -> grpo_loss -> logp_bwd(lse, g)."""
+    import torch
+    dev = logits.device
+    T = contract.T
+    if dlogits is None:
+        dlogits = torch.empty_like(logits)
+    out = {"dlogits": dlogits}
+    for k in ("logp", "lse", "grad"):
+        out[k] = torch.empty(T, dtype=torch.float32, device=dev)
+    out["entropy"] = torch.empty(T, dtype=torch.float32, device=dev) if entropy else None
+    out["loss"] = torch.empty(1, dtype=torch.float32, device=dev)
+    out["active_count"] = torch.empty(1, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(rlk_grpo_fused_workspace_size(contract), 256), dtype=torch.uint8, device=dev)
+    check(rlk_grpo_fused_step(contract, _ptr(logits), _ptr(targets), _ptr(mask), _ptr(advantage), _ptr(ref_logp),
+                              float(beta), _ptr(dlogits), _ptr(out["logp"]), _ptr(out["lse"]), _ptr(out["grad"]),
+                              _ptr(out["entropy"]), _ptr(out["loss"]), _ptr(out["active_count"]), _ptr(workspace),
+                              _stream(stream)))
+    return out
 
 
 def logp_fwd_bwd(contract, logits, targets, mask, grad, dlogits=None, stream=None, out=None):

@@ -112,7 +112,7 @@ __global__ void __cluster_dims__(kLossCtas, 1, 1) __launch_bounds__(kLossThreads
                 acc += (double)term;
                 ++n_act;
             }
-            if (r < T) grad[r] = act[u] ? dterm : 0.f;
+            if (grad && r < T) grad[r] = act[u] ? dterm : 0.f;
         }
     }
 
@@ -150,7 +150,7 @@ __global__ void __cluster_dims__(kLossCtas, 1, 1) __launch_bounds__(kLossThreads
 
     // pass 2: g_r = (unnormalised gradient) / N on this thread's own rows
     const float inv_nf = (float)inv_n;
-    for (int64_t base = t0; base < T; base += kLossUnroll * kLossStride) {
+    for (int64_t base = t0; grad && base < T; base += kLossUnroll * kLossStride) {
         float v[kLossUnroll];
 #pragma unroll
         for (int u = 0; u < kLossUnroll; ++u) {
@@ -165,7 +165,39 @@ __global__ void __cluster_dims__(kLossCtas, 1, 1) __launch_bounds__(kLossThreads
     }
 }
 
+// N of the fused GRPO step: the active rows of the contract (explicit mask,
+// or target != ignore_index), counted with integer atomics (exact in any
+// order).  In ignore_index mode each row's activity is also written to
+// mask_out for the loss kernel.
+__global__ void __launch_bounds__(256) grpo_count_kernel(int64_t T, const int64_t* __restrict__ targets,
+                                                         const uint8_t* __restrict__ mask, int64_t ignore_index,
+                                                         uint8_t* __restrict__ mask_out,
+                                                         unsigned long long* __restrict__ n_active) {
+    unsigned long long n = 0;
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < T; r += (int64_t)gridDim.x * blockDim.x) {
+        const bool act = mask ? mask[r] != 0 : targets[r] != ignore_index;
+        if (mask_out) mask_out[r] = act ? 1 : 0;
+        n += act ? 1 : 0;
+    }
+    n = warp_sum(n);
+    if ((threadIdx.x & 31) == 0 && n) atomicAdd(n_active, n);
+}
+
 }  // namespace
+
+rlk_status launch_grpo_count(int64_t T, const int64_t* targets, const uint8_t* mask, int64_t ignore_index,
+                             uint8_t* mask_out, unsigned long long* n_active, int sm_count, cudaStream_t stream) {
+    cudaError_t e = cudaMemsetAsync(n_active, 0, sizeof(unsigned long long), stream);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("clearing the active count: ") + cudaGetErrorString(e));
+    if (T > 0) {
+        const int64_t want = (T + 255) / 256;
+        const int blocks = (int)(want < 4 * (int64_t)sm_count ? want : 4 * (int64_t)sm_count);
+        grpo_count_kernel<<<blocks, 256, 0, stream>>>(T, targets, mask, ignore_index, mask_out, n_active);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("active count launch: ") + cudaGetErrorString(e));
+    }
+    return RLK_OK;
+}
 
 rlk_status launch_grpo_loss(int64_t T, const float* logp, const float* adv, const uint8_t* mask, const float* ref,
                             float beta, float* loss, float* grad, float* count, cudaStream_t stream) {

@@ -48,6 +48,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <cstddef>
 #include <cstdio>
 #include <cstdlib>
 #include <initializer_list>
@@ -84,6 +85,11 @@ constexpr int kMaxSkew = 2;  // measured at virtual TP 8: skew 1-2 beat 3-4
 constexpr int kMinSlotsShared = 4;  // fewest ring slots worth running two CTAs per SM
 constexpr int64_t kFusedChunkCols = 16384;
 
+// Variants of a kernel, as template flags so that a launch without them runs
+// none of their code (each adds code the fused kernel measured slower with).
+constexpr int kFlagEnt = 1;   // the entropy of each row's softmax
+constexpr int kFlagGrpo = 2;  // the fused GRPO step: g formed on chip (kModeFusedL2)
+
 struct SlotHdr {  // row metadata the producer writes beside each slot
     int64_t target;
     float g;
@@ -94,16 +100,19 @@ struct SlotHdr {  // row metadata the producer writes beside each slot
 };
 static_assert(sizeof(SlotHdr) == 32, "SlotHdr layout");
 
-struct RowShared {  // per-row state of the fold, double-buffered by row parity
+struct RowShared {  // per-row state of the fold, one per row buffer
     int64_t target;
-    float g;
-    int32_t active;
-    float xt;       // f32(logit[row, target]) when this CTA owns the target's tile
-    int32_t has_xt;
-    float lse;
-    int32_t pad;
+    float g;         // the header's g (the advantage A_r in the GRPO step)
+    int16_t active;  // (written by the warp of the row's first tile ...
+    int16_t has_xt;  //  ... and by the warp of the target's tile: separate halves of one word)
+    float xt;        // f32(logit[row, target]) when this CTA owns the target's tile
+    float ref;       // GRPO step: the row's reference logp (the header's lse_in)
+    float lse;       // from the fold: the row's LSE ...
+    float gf;        // ... and, in the GRPO step, its g (one 8-byte remote store with lse)
 };
 static_assert(sizeof(RowShared) == 32, "RowShared layout");
+static_assert(offsetof(RowShared, gf) == offsetof(RowShared, lse) + 4 && offsetof(RowShared, lse) % 8 == 0,
+              "lse and gf travel as one 8-byte store");
 
 // Division by a divisor fixed for the launch (Granlund and Montgomery,
 // "Division by invariant integers using multiplication", 1994): with
@@ -126,7 +135,7 @@ struct Params {
     FastDiv ns_div;  // division by NS
     int32_t rbufs, rb_shift;  // row buffers of the fold (a power of two) and its log2
     int32_t skew;             // kModeFusedL2: phase A runs `skew` rows ahead of phase B (< rbufs)
-    int32_t ent;  // the launch computes the entropy (stream_kernel's ENT)
+    int32_t ent;  // the launch computes the entropy (stream_kernel's kFlagEnt)
     int32_t row_skip;  // kModeFwd, kModeFusedL2: consumer warps skip the rows in which they have no tile (row_skip_safe)
     uint32_t off_full, off_empty, off_hdr, off_seq, off_part, off_fold, off_rows, off_xtin, off_bars, off_flag;
     uint32_t off_meta;  // TileMeta of each of the CTA's tiles
@@ -616,8 +625,9 @@ struct MetaWindow {
 // holds item i - NS: with several producers the slot's previous item may
 // belong to another one, and a parity wait while that item is not yet
 // issued could pass two phases ahead and overwrite a slot still in use.
-template <int MODE, int NP>
+template <int MODE, int NP, int F>
 __device__ void producer(const Params& p, const Ctx& x, int pid) {
+    constexpr bool GRPO = (F & kFlagGrpo) != 0;
     const int lane = x.lane;
     const uint64_t pol_first = l2_policy_evict_first();
     const uint64_t pol_last = l2_policy_evict_last();
@@ -631,8 +641,13 @@ __device__ void producer(const Params& p, const Ctx& x, int pid) {
             const int64_t r = x.q + n * x.G;
             cur.t = p.a.targets[r];
             cur.act = (p.mask_mode == RLK_MASK_EXPLICIT) ? (p.a.mask[r] != 0) : (cur.t != p.ignore_index);
-            cur.g = (MODE != kModeFwd) ? p.a.grad[r] : 0.f;
-            cur.lin = (MODE == kModeBwd) ? p.a.lse_in[r] : 0.f;
+            if (GRPO) {  // the GRPO step: A_r and ref_r ride in g and lse_in
+                cur.g = p.a.adv[r];
+                cur.lin = p.a.ref ? p.a.ref[r] : 0.f;
+            } else {
+                cur.g = (MODE != kModeFwd) ? p.a.grad[r] : 0.f;
+                cur.lin = (MODE == kModeBwd) ? p.a.lse_in[r] : 0.f;
+            }
         }
     };
     load_meta(0);
@@ -758,8 +773,9 @@ __device__ __forceinline__ bool warp_test(uint32_t bar, uint32_t parity, bool cl
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
-template <bool ENT>
+template <int F>
 __device__ void push_row(const Params& p, const Ctx& x, int64_t n) {
+    constexpr bool ENT = (F & kFlagEnt) != 0, GRPO = (F & kFlagGrpo) != 0;
     if (p.C == 1) return;
     const int lane = x.lane;
     const int b = row_buf(p, n);
@@ -789,12 +805,27 @@ __device__ void push_row(const Params& p, const Ctx& x, int64_t n) {
                        __int_as_float(rs.has_xt), fxb);
         rs.has_xt = 0;
         mbar_arrive(xb);
-        mbar_arrive_expect_tx(lb, 4u);  // the folder's LSE
+        mbar_arrive_expect_tx(lb, GRPO ? 8u : 4u);  // the folder's LSE (and, GRPO, the row's g)
     }
 }
 
-template <bool ENT>
-__device__ void fold_row(const Params& p, const Ctx& x, int64_t n) {
+// g of a row in the fused GRPO step, in the GRPO loss kernel's FP32
+// operations and order (so the two give the same bits): the row's advantage
+// a, reference logp rf, logp lp and 1/N as FP32.
+__device__ __forceinline__ float grpo_row_grad(const Params& p, bool active, float a, float rf, float lp,
+                                               float inv_nf) {
+    float dterm = -a;
+    if (p.a.ref) {
+        const float d = rf - lp;
+        const float e = expf(d);
+        dterm = fmaf(p.a.beta, 1.f - e, dterm);
+    }
+    return (active ? dterm : 0.f) * inv_nf;
+}
+
+template <int F>
+__device__ void fold_row(const Params& p, const Ctx& x, int64_t n, float inv_nf) {
+    constexpr bool ENT = (F & kFlagEnt) != 0, GRPO = (F & kFlagGrpo) != 0;
     const int lane = x.lane;
     const int b = row_buf(p, n);
     float2* part = x.part + (size_t)b * p.NT;
@@ -824,33 +855,53 @@ __device__ void fold_row(const Params& p, const Ctx& x, int64_t n) {
             xt = __shfl_sync(0xFFFFFFFFu, r.x, __ffs(from) - 1);
         }
         // the LSE to every other CTA of the cluster
-        if (lane < p.C && (uint32_t)lane != x.rank)
+        if (!GRPO && lane < p.C && (uint32_t)lane != x.rank)
             st_async_f32(mapa_shared(smem_u32(&rs.lse), (uint32_t)lane), lse_v,
                          mapa_shared(x.lsebar0 + 8u * b, (uint32_t)lane));
     }
+    const bool active = rs.active != 0;
+    const int64_t t = rs.target;
+    const bool in_range = t >= 0 && t < p.Vr;
+    float gv = 0.f;
+    if constexpr (GRPO) {
+        // the row's logp and g (every lane), then the LSE and g to every other CTA
+        const float lp = !active ? 0.f : (in_range && has) ? __fsub_rn(xt, lse_v) : __int_as_float(0x7FC00000);
+        gv = grpo_row_grad(p, active, rs.g, rs.ref, lp, inv_nf);
+        if (p.C > 1 && lane < p.C && (uint32_t)lane != x.rank)
+            st_async_f32x2(mapa_shared(smem_u32(&rs.lse), (uint32_t)lane), lse_v, gv,
+                           mapa_shared(x.lsebar0 + 8u * b, (uint32_t)lane));
+    }
     __syncwarp();
     if (lane == 0) {
-        const bool active = rs.active != 0;
-        const int64_t t = rs.target;
         p.a.lse[row] = lse_v;
         if (ENT) p.a.entropy[row] = ent_v;
         if (!active) {
             p.a.logp[row] = 0.f;
-        } else if (t < 0 || t >= p.Vr) {
+        } else if (!in_range) {
             p.a.logp[row] = __int_as_float(0x7FC00000);
             atomicOr(p.a.status, kStatusTargetRange);
         } else if (has) {
             p.a.logp[row] = __fsub_rn(xt, lse_v);
         }
         if (active && !isfinite(lse_v)) atomicOr(p.a.status, kStatusNonFinite);
+        if (GRPO) {
+            p.a.grad_out[row] = gv;
+            rs.gf = gv;
+        }
         rs.has_xt = 0;
         rs.lse = lse_v;
     }
     __syncwarp();
 }
 
-template <int MODE, bool ENT>
+template <int MODE, int F>
 __device__ void fold_warp(const Params& p, const Ctx& x) {
+    // GRPO step: 1/N as FP32, formed as the GRPO loss kernel forms it
+    float inv_nf = 0.f;
+    if constexpr ((F & kFlagGrpo) != 0) {
+        const unsigned long long n_act = *p.a.n_active;
+        inv_nf = (float)(n_act > 0 ? 1.0 / (double)n_act : 0.0);
+    }
     const int64_t R = x.nrows;
     int64_t np = 0, nr = 0;                         // next row to push, to release
     int64_t nf = p.C > 1 ? (int64_t)x.rank : 0;     // next row this CTA folds
@@ -860,13 +911,13 @@ __device__ void fold_warp(const Params& p, const Ctx& x) {
     while (nr < R) {
         bool progressed = false;
         if (np < R && warp_test(x.rowdone0 + 8u * row_buf(p, np), row_par(p, np), false)) {
-            push_row<ENT>(p, x, np);
+            push_row<F>(p, x, np);
             ++np;
             progressed = true;
         }
         if (nf < R && nf < np &&
             (p.C == 1 || warp_test(x.xbar0 + 8u * row_buf(p, nf), row_par(p, nf), true))) {
-            fold_row<ENT>(p, x, nf);
+            fold_row<F>(p, x, nf, inv_nf);
             nf += fstep;
             progressed = true;
         }
@@ -975,8 +1026,9 @@ struct TileRotation {
 // row metadata (tile 0) and the target logit (the tile that holds it).
 // FWD releases each tile's share of its slot at once; FUSED keeps the slots
 // for phase B.
-template <int MODE, int W, bool ENT>
+template <int MODE, int W, int F>
 __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0, int first) {
+    constexpr bool ENT = (F & kFlagEnt) != 0, GRPO = (F & kFlagGrpo) != 0;
     // With row_skip (the forward and the L2 fused schedule) a warp with no
     // tile in the row (ntl < NW) skips it: it writes nothing, and rowdone
     // counts only the min(NW, ntl) warps that have tiles.  Each of those
@@ -1014,8 +1066,9 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
             RowShared& rs = x.rows[b];
             if (l == 0) {
                 rs.target = h.target;
-                rs.active = h.active;
+                rs.active = (int16_t)(h.active != 0);
                 rs.g = h.g;
+                if (GRPO) rs.ref = h.lse_in;
             }
             x.part[(size_t)b * p.NT + k] = pr;
             if (ENT) x.tpart[(size_t)b * p.NT + k] = tk;
@@ -1040,8 +1093,10 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
 // lse_v is the fold's LSE.  FUSED_L2: the tile waits for the second copy of
 // its chunk; lse_v is the fold's LSE.  BWD: the tile waits for its chunk and
 // reads the row's LSE (lse_in) from the slot header.
-template <int MODE, int W>
-__device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0, float lse_v, int first) {
+template <int MODE, int W, int F>
+__device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0, float lse_v, float g_fold,
+                        int first) {
+    constexpr bool GRPO = (F & kFlagGrpo) != 0;
     constexpr bool kWaits = MODE == kModeBwd || MODE == kModeFusedL2;
     const int lane = x.lane;
     uint16_t* slots = reinterpret_cast<uint16_t*>(x.smem);
@@ -1061,14 +1116,14 @@ __device__ bool phase_b(const Params& p, const Ctx& x, int64_t n, uint32_t item0
         }
         tile_grad(slots + (size_t)it.slot * slot_elems + m.soff, p.a.logits + h.row * p.stride,
                   p.a.dlogits + h.row * p.stride, tg, GroupRange{m.ga.lo, m.ga.hi, m.nb}, (int)p.Vr,
-                  h.active != 0, h.target, h.g, lse, lane);
+                  h.active != 0, h.target, GRPO ? g_fold : h.g, lse, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive_n(x.empty0 + 8u * it.slot, (uint32_t)m.share);
     }
     return true;
 }
 
-template <int MODE, int NW, bool ENT>
+template <int MODE, int NW, int F>
 __device__ void consumer(const Params& p, const Ctx& x) {
     const int64_t R = x.nrows;
     const uint32_t nch = (uint32_t)x.nch;
@@ -1078,18 +1133,18 @@ __device__ void consumer(const Params& p, const Ctx& x) {
     TileRotation<NW> rot_a(x.ntl), rot_b(x.ntl);  // phase A and phase B each visit rows in order
     if constexpr (MODE == kModeBwd) {
         for (int64_t n = 0; n < R; ++n)
-            if (!phase_b<MODE, NW>(p, x, n, item_b(n), 0.f, rot_b.next(x.warp))) break;
+            if (!phase_b<MODE, NW, F>(p, x, n, item_b(n), 0.f, 0.f, rot_b.next(x.warp))) break;
     } else if constexpr (MODE == kModeFwd) {
-        for (int64_t n = 0; n < R; ++n) phase_a<MODE, NW, ENT>(p, x, n, item_a(n), rot_a.next(x.warp));
+        for (int64_t n = 0; n < R; ++n) phase_a<MODE, NW, F>(p, x, n, item_a(n), rot_a.next(x.warp));
     } else {
         // Skewed order A(0), ..., A(S-1), then A(n+S), B(n): the fold of row
         // n overlaps phase A of rows n+1..n+S.  kModeFused (S = 1) keeps two
         // rows of slots resident; kModeFusedL2 copies each row a second time
         // for phase B.  rbufs > S keeps rows[b].lse of row n until every warp
         // has read it: row n + rbufs comes after B(n) in every warp's order.
-        for (int64_t n = 0; n < S && n < R; ++n) phase_a<MODE, NW, ENT>(p, x, n, item_a(n), rot_a.next(x.warp));
+        for (int64_t n = 0; n < S && n < R; ++n) phase_a<MODE, NW, F>(p, x, n, item_a(n), rot_a.next(x.warp));
         for (int64_t n = 0; n < R; ++n) {
-            if (n + S < R) phase_a<MODE, NW, ENT>(p, x, n + S, item_a(n + S), rot_a.next(x.warp));
+            if (n + S < R) phase_a<MODE, NW, F>(p, x, n + S, item_a(n + S), rot_a.next(x.warp));
             const int b = row_buf(p, n);
             const int first_b = rot_b.next(x.warp);
             // row_skip: no tile in this row, so neither its LSE nor phase B
@@ -1098,14 +1153,17 @@ __device__ void consumer(const Params& p, const Ctx& x) {
             // A failed wait anywhere sets the abort flag; the slot headers may
             // then be stale, so skip the writes (the status word already says
             // RLK_ERR_TIMEOUT).
-            if (ready && !*x.wt.abort_flag) phase_b<MODE, NW>(p, x, n, item_b(n), x.rows[b].lse, first_b);
+            if (ready && !*x.wt.abort_flag)
+                phase_b<MODE, NW, F>(p, x, n, item_b(n), x.rows[b].lse, (F & kFlagGrpo) ? x.rows[b].gf : 0.f,
+                                     first_b);
         }
     }
 }
 
 // PER_SM: CTAs resident per SM (1 or 2); the register budget follows from it.
-// ENT (the forward and the fused L2 schedule): also the entropy of each row's softmax.
-template <int MODE, int PER_SM, bool ENT>
+// F: kFlagEnt (the forward and the fused L2 schedule) also forms the entropy of
+// each row's softmax; kFlagGrpo (the fused L2 schedule) is the GRPO step.
+template <int MODE, int PER_SM, int F>
 __global__ void __launch_bounds__(threads_for(MODE, PER_SM), PER_SM)
     stream_kernel(const __grid_constant__ Params p) {
     constexpr int NW = consumers_for(MODE, PER_SM);
@@ -1165,11 +1223,11 @@ __global__ void __launch_bounds__(threads_for(MODE, PER_SM), PER_SM)
     if (p.C > 1) cluster_sync_all(); else __syncthreads();
 
     if (x.warp > NW) {
-        producer<MODE, producers_for(PER_SM)>(p, x, x.warp - NW - 1);
+        producer<MODE, producers_for(PER_SM), F>(p, x, x.warp - NW - 1);
     } else if (x.warp == NW) {
-        if (MODE != kModeBwd) fold_warp<MODE, ENT>(p, x);
+        if (MODE != kModeBwd) fold_warp<MODE, F>(p, x);
     } else {
-        consumer<MODE, NW, ENT>(p, x);
+        consumer<MODE, NW, F>(p, x);
     }
 
     __syncthreads();
@@ -1379,7 +1437,10 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
         if (s != "resident") mode = kModeFusedL2;
         if (p.ent && mode != kModeFusedL2)
             return fail(RLK_ERR_UNSUPPORTED, "the entropy is computed by the L2 fused schedule, not the resident one");
+        if (a.grpo && mode != kModeFusedL2)
+            return fail(RLK_ERR_UNSUPPORTED, "the fused GRPO step runs the L2 fused schedule, not the resident one");
     }
+    if (a.grpo && mode != kModeFusedL2) return fail(RLK_ERR_UNSUPPORTED, "the fused GRPO step is a fused mode");
     int C = (mode == kModeBwd) ? 1 : c.virtual_tp;
     // The L2 fused schedule at virtual TP 1 splits each row over a cluster of
     // two CTAs, as the resident schedule does when a row does not fit: every
@@ -1501,18 +1562,25 @@ rlk_status launch_stream(const rlk_logp_contract& c, int mode, const StreamArgs&
 
     const int ntl_cta = (c.num_tiles + p.C - 1) / p.C;
     auto pick = [&](int per_sm) -> void (*)(Params) {
+        const bool two = per_sm == 2;
+        if (a.grpo) {  // kModeFusedL2 only (checked above)
+            if (p.ent)
+                return two ? stream_kernel<kModeFusedL2, 2, kFlagGrpo | kFlagEnt>
+                           : stream_kernel<kModeFusedL2, 1, kFlagGrpo | kFlagEnt>;
+            return two ? stream_kernel<kModeFusedL2, 2, kFlagGrpo> : stream_kernel<kModeFusedL2, 1, kFlagGrpo>;
+        }
         if (p.ent && mode == kModeFusedL2)
-            return per_sm == 2 ? stream_kernel<kModeFusedL2, 2, true> : stream_kernel<kModeFusedL2, 1, true>;
-        if (p.ent) return per_sm == 2 ? stream_kernel<kModeFwd, 2, true> : stream_kernel<kModeFwd, 1, true>;
-        if (per_sm == 2)
-            return (mode == kModeFwd)     ? stream_kernel<kModeFwd, 2, false>
-                 : (mode == kModeBwd)     ? stream_kernel<kModeBwd, 2, false>
-                 : (mode == kModeFusedL2) ? stream_kernel<kModeFusedL2, 2, false>
-                                          : stream_kernel<kModeFused, 2, false>;
-        return (mode == kModeFwd)     ? stream_kernel<kModeFwd, 1, false>
-             : (mode == kModeBwd)     ? stream_kernel<kModeBwd, 1, false>
-             : (mode == kModeFusedL2) ? stream_kernel<kModeFusedL2, 1, false>
-                                      : stream_kernel<kModeFused, 1, false>;
+            return two ? stream_kernel<kModeFusedL2, 2, kFlagEnt> : stream_kernel<kModeFusedL2, 1, kFlagEnt>;
+        if (p.ent) return two ? stream_kernel<kModeFwd, 2, kFlagEnt> : stream_kernel<kModeFwd, 1, kFlagEnt>;
+        if (two)
+            return (mode == kModeFwd)     ? stream_kernel<kModeFwd, 2, 0>
+                 : (mode == kModeBwd)     ? stream_kernel<kModeBwd, 2, 0>
+                 : (mode == kModeFusedL2) ? stream_kernel<kModeFusedL2, 2, 0>
+                                          : stream_kernel<kModeFused, 2, 0>;
+        return (mode == kModeFwd)     ? stream_kernel<kModeFwd, 1, 0>
+             : (mode == kModeBwd)     ? stream_kernel<kModeBwd, 1, 0>
+             : (mode == kModeFusedL2) ? stream_kernel<kModeFusedL2, 1, 0>
+                                      : stream_kernel<kModeFused, 1, 0>;
     };
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];

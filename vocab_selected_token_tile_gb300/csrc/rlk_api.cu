@@ -282,6 +282,84 @@ RLK_EXPORT rlk_status rlk_grpo_loss(int64_t T, const float* logp, const float* a
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace rlk {
+namespace {
+// Workspace of the fused GRPO step: the status word, N (8 bytes in 256), and
+// in ignore_index mode each row's activity for the loss (one byte a row).
+constexpr size_t kGrpoCountBytes = 256;
+size_t grpo_workspace(const rlk_logp_contract& c) {
+    return kWorkspaceBytes + kGrpoCountBytes + ((size_t)c.T + 255) / 256 * 256;
+}
+}  // namespace
+}  // namespace rlk
+
+RLK_EXPORT size_t rlk_grpo_fused_workspace_size(const rlk_logp_contract* c) {
+    return check_contract(c) == RLK_OK ? grpo_workspace(*c) : 0;
+}
+
+RLK_EXPORT rlk_status rlk_grpo_fused_step(const rlk_logp_contract* c, const void* logits_bf16,
+                                          const int64_t* targets, const uint8_t* active_mask, const float* advantage,
+                                          const float* ref_logp, float beta, void* dlogits_bf16, float* logp_out,
+                                          float* lse_out, float* grad_out, float* entropy_out, float* loss,
+                                          float* active_count, void* workspace, rlk_stream_t stream) {
+    rlk_status s = check_contract(c);
+    if (s != RLK_OK) return s;
+    if (!loss) return fail(RLK_ERR_INVALID_ARG, "loss output is required");
+    if (!(beta >= 0.f) || !isfinite(beta)) return fail(RLK_ERR_INVALID_ARG, "beta must be finite and >= 0");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (c->T == 0) {  // no rows: loss 0 (and N = 0)
+        if ((s = select_device(loss)) != RLK_OK) return s;
+        if ((s = check_device_ptrs({{active_count, "active_count"}})) != RLK_OK) return s;
+        return launch_grpo_loss(0, nullptr, nullptr, nullptr, nullptr, beta, loss, nullptr, active_count, st);
+    }
+    if ((s = check_common(c, logits_bf16, targets, active_mask, workspace)) != RLK_OK) return s;
+    if (!advantage) return fail(RLK_ERR_INVALID_ARG, "advantage is NULL");
+    if (!dlogits_bf16) return fail(RLK_ERR_INVALID_ARG, "dlogits is NULL");
+    if (!aligned16(dlogits_bf16)) return fail(RLK_ERR_MISALIGNED, "dlogits must be 16-byte aligned");
+    if ((s = check_dlogits_overlap(logits_bf16, dlogits_bf16, c->T, c->row_stride ? c->row_stride : c->V_padded)) !=
+        RLK_OK)
+        return s;
+    if (!logp_out || !lse_out || !grad_out)
+        return fail(RLK_ERR_INVALID_ARG, "logp_out, lse_out and grad_out are required");
+    if ((s = select_device(logits_bf16)) != RLK_OK) return s;
+    if ((s = check_device_ptrs({{targets, "targets"}, {active_mask, "active_mask"}, {advantage, "advantage"},
+                                {ref_logp, "ref_logp"}, {dlogits_bf16, "dlogits"}, {logp_out, "logp_out"},
+                                {lse_out, "lse_out"}, {grad_out, "grad_out"}, {entropy_out, "entropy_out"},
+                                {loss, "loss"}, {active_count, "active_count"}, {workspace, "workspace"}})) != RLK_OK)
+        return s;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("querying the device: ") + cudaGetErrorString(e));
+    if ((s = begin(workspace, st)) != RLK_OK) return s;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    auto* n_active = reinterpret_cast<unsigned long long*>(ws + kWorkspaceBytes);
+    uint8_t* mask_ws = (c->mask_mode == RLK_MASK_IGNORE_INDEX) ? ws + kWorkspaceBytes + kGrpoCountBytes : nullptr;
+    if ((s = launch_grpo_count(c->T, targets, active_mask, c->ignore_index, mask_ws, n_active, sms, st)) != RLK_OK)
+        return s;
+    StreamArgs a{};
+    a.logits = static_cast<const uint16_t*>(logits_bf16);
+    a.dlogits = static_cast<uint16_t*>(dlogits_bf16);
+    a.targets = targets;
+    a.mask = active_mask;
+    a.logp = logp_out;
+    a.lse = lse_out;
+    a.entropy = entropy_out;
+    a.status = static_cast<uint32_t*>(workspace);
+    a.grpo = 1;
+    a.adv = advantage;
+    a.ref = ref_logp;
+    a.beta = beta;
+    a.n_active = n_active;
+    a.grad_out = grad_out;
+    if ((s = launch_stream(*c, kModeFused, a, st)) != RLK_OK) return s;
+    // the loss from this step's logp, in the GRPO loss kernel's fixed order (g is already written)
+    if ((s = launch_grpo_loss(c->T, logp_out, advantage, active_mask ? active_mask : mask_ws, ref_logp, beta, loss,
+                              nullptr, active_count, st)) != RLK_OK)
+        return s;
+    return c->validate ? read_status(workspace, st) : RLK_OK;
+}
+
 RLK_EXPORT rlk_status rlk_logp_bwd(const rlk_logp_contract* c, const void* logits_bf16, const int64_t* targets,
                                    const uint8_t* active_mask, const float* lse_in, const float* grad_logp,
                                    void* dlogits_bf16, float* logp_out, float* lse_out, void* workspace,

@@ -45,6 +45,17 @@ struct StreamArgs {
     // another shard (any value outside [0, V_real) of this launch); it then
     // takes no one-hot term here and is not an error.
     int32_t foreign_targets;
+    // The fused GRPO step (kModeFusedL2): instead of reading g, each row's g
+    // is formed on chip from its logp once the fold has it,
+    //   g_r = mask_r (-A_r + beta (1 - exp(ref_r - logp_r))) / N
+    // (no KL term without ref), in the same FP32 operations as the GRPO loss
+    // kernel, and written to grad_out.  n_active holds N.
+    int32_t grpo;
+    const float* adv;
+    const float* ref;
+    float beta;
+    const unsigned long long* n_active;
+    float* grad_out;
 };
 
 // Records a failure reason for rlk_last_error_message() and returns `s`.
@@ -96,9 +107,15 @@ rlk_status launch_shard_bwd(const rlk_logp_contract& c, int32_t shard, const uin
                             const uint8_t* mask, const float* lse_in, const float* grad, uint16_t* dlogits,
                             void* workspace, uint32_t* status, cudaStream_t stream);
 
-// Token-mean GRPO loss and its gradient (grpo_loss.cu); one CTA, fixed order.
+// Token-mean GRPO loss and its gradient (grpo_loss.cu); one cluster, fixed
+// order.  grad may be NULL (the loss alone).
 rlk_status launch_grpo_loss(int64_t T, const float* logp, const float* adv, const uint8_t* mask, const float* ref,
                             float beta, float* loss, float* grad, float* count, cudaStream_t stream);
+
+// N of the fused GRPO step into *n_active (cleared first); in ignore_index
+// mode (mask NULL) each row's activity also goes to mask_out.
+rlk_status launch_grpo_count(int64_t T, const int64_t* targets, const uint8_t* mask, int64_t ignore_index,
+                             uint8_t* mask_out, unsigned long long* n_active, int sm_count, cudaStream_t stream);
 
 // Launches the bounded-wait self-test kernel (one warp waiting on an mbarrier
 // that nothing arrives at).
