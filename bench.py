@@ -10,8 +10,11 @@ so no flush is needed between steps.
 Prints ONE JSON line on rank 0.  Beside the headline it carries, under
 ``extra``, the other paths timed the same way, each with its own clock
 record: the forward at virtual TP 1 and 8 (rollout), the fused step at
-virtual TP 1 and 8, and the fused lm_head (hidden [8192, 4096] x W
-[152576, 4096]) forward and forward+backward (``--no-extra`` skips them).
+virtual TP 1, 4 and 8, the forward and the fused step with the entropy, the
+fused GRPO step (loss, g and dlogits in one pass), the GRPO loss, the split
+path, one rank of the vocabulary-parallel step, and the fused lm_head
+(hidden [8192, 4096] x W [152576, 4096]) forward and forward+backward
+(``--no-extra`` skips them).
 ``--impl reference`` times the FP64 CPU oracle instead, on a bounded sample
 of the same workload, across the host's cores.
 
@@ -530,6 +533,7 @@ def lmhead_bench(rlk, args, dev, clock_index, steps=10, warmup=3, rows=0, bwd=Tr
 def extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, Vp, args, clock_index):
     """The other paths on the same batch, each timed like the headline (events on the launching stream,
     warm-up first, a clock record of its own)."""
+    import numpy as np
     import torch
     out = {}
     stream = torch.cuda.current_stream()
@@ -571,6 +575,26 @@ def extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, T, Vr, V
                                                ent.data_ptr(), ws_f.data_ptr(), stream.cuda_stream))
     _, ms, clk = timed(fused_ent, args.steps, 3, stream, clock_index)
     out["fused_entropy_vtp2"] = entry(ms, T * (2 * Vr + 2 * Vp + 25), clk, "stream_kernel<kModeFusedL2, ENT>")
+    # the fused GRPO step with the KL term: logp, LSE, loss, g and dlogits in one pass (per row also targets,
+    # mask, A, ref, logp, LSE, g: 29 B, and the count and loss kernels' 14 B)
+    rng = np.random.default_rng(1)
+    adv = torch.from_numpy(np.repeat(rng.standard_normal(T // 2048 or 1), 2048)[:T].astype(np.float32)).to(
+        logits.device)
+    refp = torch.from_numpy((-6.0 * rng.random(T)).astype(np.float32)).to(logits.device)
+    ws_g = torch.empty(rlk.rlk_grpo_fused_workspace_size(c2), dtype=torch.uint8, device=logits.device)
+    gout = {"grad": torch.empty(T, dtype=torch.float32, device=logits.device)}
+    loss_g = torch.empty(1, dtype=torch.float32, device=logits.device)
+
+    def grpo_step():
+        rlk.check(rlk.rlk_grpo_fused_step(c2, logits.data_ptr(), targets.data_ptr(), dmask.data_ptr(), adv.data_ptr(),
+                                          refp.data_ptr(), 0.01, dlogits.data_ptr(), logp.data_ptr(), lse.data_ptr(),
+                                          gout["grad"].data_ptr(), None, loss_g.data_ptr(), None, ws_g.data_ptr(),
+                                          stream.cuda_stream))
+    _, ms, clk = timed(grpo_step, args.steps, 3, stream, clock_index, per_launch=False)
+    out["grpo_fused_step_vtp2"] = entry(ms, T * (2 * Vr + 2 * Vp + 43), clk,
+                                        "grpo_count_kernel + stream_kernel<kModeFusedL2, GRPO> + grpo_loss_kernel")
+    out["grpo_fused_step_vtp2"]["note"] = ("beta 0.01 with a reference logp; the same step composed (forward, loss, "
+                                           "backward from the LSE) is split_fwd_then_bwd_vtp1 plus grpo_loss")
     # the GRPO loss and g from this batch's logp (reads logp, A, mask, ref; writes g: 17 B per row)
     ref = logp + 0.01
     loss, gl, cnt = (torch.empty(1, dtype=torch.float32, device=logits.device),
