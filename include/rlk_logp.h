@@ -216,7 +216,11 @@ rlk_status rlk_grpo_loss(int64_t T, const float* logp, const float* advantage, c
  *                 (bitwise rlk_logp_fwd_entropy's).
  *   loss          one FP32 out; active_count NULL or one FP32 out (N).
  *   workspace     rlk_grpo_fused_workspace_size bytes.
- * T = 0 writes loss = 0 (and N = 0).  Status as for rlk_logp_bwd.
+ * The loss convention and its sources on the pages are rlk_grpo_loss's
+ * (above).  T = 0 writes loss = 0 (and N = 0).  Host checks return
+ * RLK_ERR_INVALID_ARG for a missing pointer, a negative or non-finite beta,
+ * or dlogits overlapping the logits other than exactly; device status as for
+ * rlk_logp_bwd.  The workspace belongs to one call at a time.
  */
 size_t rlk_grpo_fused_workspace_size(const rlk_logp_contract* contract);
 rlk_status rlk_grpo_fused_step(const rlk_logp_contract* contract, const void* logits_bf16, const int64_t* targets,
