@@ -76,3 +76,42 @@ def test_lmhead_forward_backward_replays_from_a_graph(built):
         torch.cuda.synchronize()
         assert torch.equal(logp, ref[0]) and torch.equal(lse, ref[1])
         assert torch.equal(dh, ref[2]) and torch.equal(dw, ref[3])
+
+
+def test_grpo_step_replays_from_a_graph(built):
+    """The fused GRPO step (two memsets, the count, the fused pass, the loss) captured once, replayed with
+    the eager call's bits, then replayed on a new advantage in the same buffer."""
+    T, vr, vp, nt = 200, 3001, 3072, 64
+    bits = synth.logits_host(0, T, vp, vp, vr, seed=4, sigma=3.0, nspikes=2, garbage=True)
+    tgt = synth.targets(T, vr, seed=4)
+    mask = (np.arange(T) % 3 != 0).astype(np.uint8)
+    rng = np.random.default_rng(4)
+    adv_h = rng.standard_normal(T).astype(np.float32)
+    logits = torch.from_numpy(bits.view(np.int16)).cuda()
+    dt, dm, adv = (torch.from_numpy(a).cuda() for a in (tgt, mask, adv_h))
+    c = rlk.Contract(T=T, V_real=vr, V_padded=vp, num_tiles=nt, virtual_tp=2, validate=0)
+    ref_lp = rlk.logp_fwd(c, logits, dt, dm)[0] + 0.03
+    want = rlk.grpo_fused_step(c, logits, dt, dm, adv, ref_lp, 0.01)  # eager
+    bufs = {k: torch.empty(T, device="cuda") for k in ("logp", "lse", "grad")}
+    dl = torch.empty_like(logits)
+    loss = torch.empty(1, device="cuda")
+    n = torch.empty(1, device="cuda")
+    ws = torch.zeros(rlk.rlk_grpo_fused_workspace_size(c), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        rlk.check(rlk.rlk_grpo_fused_step(c, logits.data_ptr(), dt.data_ptr(), dm.data_ptr(), adv.data_ptr(),
+                                          ref_lp.data_ptr(), 0.01, dl.data_ptr(), bufs["logp"].data_ptr(),
+                                          bufs["lse"].data_ptr(), bufs["grad"].data_ptr(), None, loss.data_ptr(),
+                                          n.data_ptr(), ws.data_ptr(), torch.cuda.current_stream().cuda_stream))
+    graph.replay()
+    torch.cuda.synchronize()
+    for k in ("logp", "lse", "grad"):
+        assert torch.equal(bufs[k], want[k]), k
+    assert torch.equal(dl, want["dlogits"]) and torch.equal(loss, want["loss"]) and torch.equal(n, want["active_count"])
+    adv.copy_(torch.flip(adv, dims=[0]))
+    want2 = rlk.grpo_fused_step(c, logits, dt, dm, adv, ref_lp, 0.01)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(bufs["grad"], want2["grad"]) and torch.equal(loss, want2["loss"])
+    assert torch.equal(dl, want2["dlogits"]) and not torch.equal(want2["grad"], want["grad"])
