@@ -64,7 +64,8 @@ def parse():
     ap.add_argument("--no-extra", action="store_true", help="skip the other paths' timings")
     ap.add_argument("--rows", type=int, default=0,
                     help="profiling only: shrink the batch to this many rows (not a bench number)")
-    ap.add_argument("--path", default="fused", choices=["fused", "fwd", "split", "lmhead", "lmhead_bwd", "vocab_rank"],
+    ap.add_argument("--path", default="fused",
+                    choices=["fused", "fwd", "split", "grpo", "lmhead", "lmhead_bwd", "vocab_rank"],
                     help="profiling only: time another kernel instead of the fused step")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="--impl reference: oracle seconds per core spread over the warm-up and timed steps")
@@ -313,6 +314,13 @@ def run_ours(args, ws, rank, local):
                      mask_mode=rlk.MASK_EXPLICIT, validate=0)
     stream = torch.cuda.current_stream()
     ws_buf = rlk.workspace_for(c, dev, stream)
+    if args.path == "grpo":  # the fused GRPO step: one advantage per sequence, a reference logp, beta 0.01
+        rng = np.random.default_rng(w.seed)
+        adv = torch.from_numpy(np.repeat(rng.standard_normal(w.batch), w.seq)[r0:r1].astype(np.float32)).to(dev)
+        refp = torch.from_numpy((-6.0 * rng.random(T))[r0:r1].astype(np.float32)).to(dev)
+        gout = torch.empty(Tl, dtype=torch.float32, device=dev)
+        loss_buf = torch.empty(1, dtype=torch.float32, device=dev)
+        ws_buf = torch.zeros(rlk.rlk_grpo_fused_workspace_size(c), dtype=torch.uint8, device=dev)
 
     def step():
         if args.path in ("fwd", "split"):
@@ -326,6 +334,11 @@ def run_ours(args, ws, rank, local):
             rlk.check(rlk.rlk_logp_bwd(c, logits.data_ptr(), targets.data_ptr(), dmask.data_ptr(), None,
                                        dg.data_ptr(), dlogits.data_ptr(), logp.data_ptr(), lse.data_ptr(),
                                        ws_buf.data_ptr(), stream.cuda_stream))
+        if args.path == "grpo":
+            rlk.check(rlk.rlk_grpo_fused_step(c, logits.data_ptr(), targets.data_ptr(), dmask.data_ptr(),
+                                              adv.data_ptr(), refp.data_ptr(), 0.01, dlogits.data_ptr(),
+                                              logp.data_ptr(), lse.data_ptr(), gout.data_ptr(), None,
+                                              loss_buf.data_ptr(), None, ws_buf.data_ptr(), stream.cuda_stream))
 
     for _ in range(args.warmup):
         step()
@@ -348,10 +361,12 @@ def run_ours(args, ws, rank, local):
     fwd_bytes = Tl * 2 * Vr + Tl * (8 + 1 + 4 + 4)              # logits, targets, mask, logp, LSE
     bwd_bytes = n_active * 2 * Vr + Tl * 2 * Vp + Tl * (8 + 1 + 4 + 4)  # logits of active rows, dlogits, g, LSE
     alg_bytes = {"fused": Tl * (2 * Vr + 2 * Vp) + Tl * (8 + 1 + 4 + 4 + 4),
+                 "grpo": Tl * (2 * Vr + 2 * Vp + 43),  # + A, ref, g; the count and loss kernels' 14 B
                  "fwd": fwd_bytes, "split": fwd_bytes + bwd_bytes}[args.path]
     kernel = {"fused": "stream_kernel<kModeFusedL2>", "fwd": "stream_kernel<kModeFwd>",
+              "grpo": "grpo_count_kernel + stream_kernel<kModeFusedL2, GRPO> + grpo_loss_kernel",
               "split": "stream_kernel<kModeFwd> + stream_kernel<kModeBwd>"}[args.path]
-    launches_per_step = 2 if args.path == "split" else 1
+    launches_per_step = {"split": 2, "grpo": 3}.get(args.path, 1)
     achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
     rows_split = args.split == "rows" and ws > 1
     result = {
