@@ -175,6 +175,19 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu), or the machine type when lscpu gives none."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
+
 def cpu_threads():
     try:
         return len(os.sched_getaffinity(0))
@@ -227,9 +240,10 @@ def time_oracle(pool, budget_s, cores, max_rows_per_core=4096):
 
 # --------------------------------------------------------------------------- timing helpers
 
-def timed(fn, steps, warmup, stream, clock_index, per_launch=True):
+def timed(fn, steps, warmup, stream, clock_index, per_launch=True, stats=None):
     """Runs fn() warmup times, then steps times between CUDA events on `stream` with a clock record;
-    returns (total ms, mean per-call ms, clocks)."""
+    returns (total ms, mean per-call ms, clocks).  With per_launch, `stats` (a dict, if given) gets the
+    median per-call ms too."""
     import torch
     for _ in range(warmup):
         fn()
@@ -250,6 +264,8 @@ def timed(fn, steps, warmup, stream, clock_index, per_launch=True):
     clk = clocks.stop()
     total = a.elapsed_time(b)
     per = statistics.mean(x.elapsed_time(y) for x, y in ev) if per_launch else total / steps
+    if stats is not None and per_launch:
+        stats["median"] = statistics.median(x.elapsed_time(y) for x, y in ev)
     return total, per, clk
 
 
@@ -350,7 +366,8 @@ def run_ours(args, ws, rank, local):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    total_ms, per_launch_ms, clk = timed(step, args.steps, 0, stream, local)
+    launch_stats = {}
+    total_ms, per_launch_ms, clk = timed(step, args.steps, 0, stream, local, stats=launch_stats)
     if ws > 1:
         torch.distributed.barrier()
         total_ms = max_over_ranks(total_ms, dev)
@@ -392,6 +409,8 @@ def run_ours(args, ws, rank, local):
             "alg_bytes_per_step": alg_bytes,
         },
         "achieved_gbs": achieved,
+        "ms_median_launch": launch_stats.get("median"),
+        "active_tokens_per_s": (int(active.sum()) if rows_split else ws * n_active) / (ms_per_step * 1e-3),
         "roofline": {
             "bound": "hbm",
             "achieved": achieved,
@@ -405,6 +424,9 @@ def run_ours(args, ws, rank, local):
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
     }
+    tr = result["roofline"]["traffic"]
+    # ncu's DRAM bytes of one launch over the launch's measured time, beside the algorithmic rate
+    result["roofline"]["traffic_gbs"] = tr / (per_launch_ms * 1e-3) / 1e9 if tr else None
     if not args.no_extra and rank == 0 and not args.rows:
         try:
             result["extra"] = extra_paths(rlk, c, logits, targets, dmask, dg, dlogits, logp, lse, Tl, Vr, Vp, args,
@@ -746,7 +768,8 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded counter-based generator)",
             "config": {"workload": "grpo: fused fwd+bwd, T=65536 x V_padded=152576 (V_real=151936), 64 tiles"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample_desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample_desc,
+                             "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": time.perf_counter() - t0,
         }
@@ -758,7 +781,7 @@ def main():
         # the oracle's pool is spawned before the first CUDA call of this process
         with oracle_pool(cores) as pool:
             tps, rows, secs = time_oracle(pool, args.cpu_seconds, cores)
-        cpu = {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle",
+        cpu = {"value": tps, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
                "sample": f"{rows} seeded rows of the grpo workload, FP64 numpy oracle (fwd LSE/logp + dlogits), "
                          f"one spawned process per core, {secs:.1f} s of oracle time each"}
     import torch
