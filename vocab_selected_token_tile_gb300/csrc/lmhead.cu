@@ -599,16 +599,18 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                     const uint32_t fb = smem_u32(&bars->full[stage]);
                     const uint32_t a = smem_u32(sA + stage * kStageA);
                     const uint32_t b = smem_u32(sB + stage * kStageB);
-                    mbar_arrive_expect_tx(fb, kStageA + (uint32_t)t.nbox * kMnBlock);
+                    // B: the four 64-wide blocks of the stage in one 3-D box (blocks past H read as
+                    // zero and still count their bytes)
+                    mbar_arrive_expect_tx(fb, kStageA + 4u * kMnBlock);
                     if (t.prob == 0) {
                         // dlogits rows m0.., columns (K) kb*64..; W rows (K) kb*64.., columns h
                         tma_load_2d(a, &tmA0, kb * kBK, m0, fb);
-                        for (int j = 0; j < t.nbox; ++j) tma_load_2d(b + j * kMnBlock, &tmB0, h0 + 64 * j, kb * kBK, fb);
+                        tma_load_3d(b, &tmB0, 0, kb * kBK, h0 / 64, fb);
                     } else {
                         // dlogits columns (M) m0.., rows (K) kb*64..; hidden rows (K) kb*64.., columns h
                         tma_load_2d(a, &tmA1, m0, kb * kBK, fb);
                         tma_load_2d(a + kMnBlock, &tmA1, m0 + 64, kb * kBK, fb);
-                        for (int j = 0; j < t.nbox; ++j) tma_load_2d(b + j * kMnBlock, &tmB1, h0 + 64 * j, kb * kBK, fb);
+                        tma_load_3d(b, &tmB1, 0, kb * kBK, h0 / 64, fb);
                     }
                     ++issued;
                     if (++stage == kStages) {
@@ -761,6 +763,24 @@ bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows, int
     const cuuint32_t box[2] = {box_inner, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A BF16 matrix whose contiguous dimension `inner` (a multiple of 64) is read
+// in 64-element blocks: dims {64, rows, inner/64}, the blocks 128 bytes apart,
+// so one box {64, box_rows, box_blocks} lands as box_blocks consecutive
+// 64 x box_rows blocks of the 128-byte swizzle -- the layout of as many 2-D
+// boxes {64, box_rows}.  Blocks past inner/64 read as zero.
+bool make_map_mn3(CUtensorMap* m, const void* base, int64_t inner, int64_t rows, int64_t stride, uint32_t box_rows,
+                  uint32_t box_blocks) {
+    EncodeTiled enc = encode_fn();
+    if (!enc || inner % 64 != 0) return false;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(inner / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)stride * 2, 128};
+    const cuuint32_t box[3] = {64, box_rows, box_blocks};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -928,9 +948,9 @@ rlk_status launch_lmhead_bwd_given_lse(const rlk_logp_contract& c, const void* h
     // come out exactly 0.
     CUtensorMap tmA0, tmB0, tmA1, tmB1;
     if (!make_map(&tmA0, dlogits, c.V_real, c.T, c.V_padded, kBK, kBM) ||
-        !make_map(&tmB0, weight, H, c.V_real, H, 64, kBK) ||
+        !make_map_mn3(&tmB0, weight, H, c.V_real, H, kBK, 4) ||
         !make_map(&tmA1, dlogits, c.V_real, c.T, c.V_padded, 64, kBK) ||
-        !make_map(&tmB1, hidden, H, c.T, H, 64, kBK))
+        !make_map_mn3(&tmB1, hidden, H, c.T, H, kBK, 4))
         return fail(RLK_ERR_CUDA, "cuTensorMapEncodeTiled failed for a gradient operand");
     GradParams g{};
     g.dhidden = static_cast<uint16_t*>(dhidden);
