@@ -33,7 +33,9 @@
 //   dHidden[T, H]  = dlogits[:, :V_real] W[:V_real]      (A K-major, B MN-major)
 //   dW[V_padded, H] = dlogits[:, :V_real]^T hidden       (A and B MN-major)
 // Each output tile accumulates its whole K range in one fixed order on one
-// CTA: no split-K, no atomics on data.
+// CTA: no split-K, no atomics on data.  An MN-major B operand (W, hidden)
+// arrives as four 64-wide swizzled blocks per stage in one 3-D TMA box
+// (make_map_mn3): four 2-D boxes a stage measured latency-bound.
 //
 // Every wait is bounded; on expiry the CTA records RLK_ERR_TIMEOUT, stops
 // issuing, waits (bounded) for its issued copies and MMAs, frees its tensor
