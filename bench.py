@@ -29,6 +29,7 @@ Multi-GPU (torchrun), ``--split``:
 The time is the max over ranks.
 """
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -407,6 +408,7 @@ def run_ours(args, ws, rank, local):
                             f"dp{ws} (independent rows, no collective)" if ws > 1 else "single GPU"),
             "l2": "inputs (20.0 GB logits) larger than L2; no flush",
             "alg_bytes_per_step": alg_bytes,
+            "contract_sha256": hashlib.sha256(ctypes.string_at(ctypes.addressof(c), ctypes.sizeof(c))).hexdigest(),
         },
         "achieved_gbs": achieved,
         "ms_median_launch": launch_stats.get("median"),

@@ -15,6 +15,8 @@ host check.  What is tested is the layer's logic:
   can strand the other TP ranks) -- whether the layer's own check, the C
   library's contract check or the shard call's host checks reject it, in
   the forward or in the backward;
+* ranks whose contracts are each valid but differ (the pages' preflight
+  compares a contract fingerprint) all raise before any data moves;
 * the backward returns each rank's own shard;
 * token rows split over ranks cover every row once.
 """
@@ -134,6 +136,8 @@ def _rank_main(rank, world, port, case, out_dir):
             c = c.replace(num_tiles=6)  # 6 does not divide 1024: this rank's host check fails
         if case == "bad_shape" and rank == 0:
             shard = shard[:, :-8].contiguous()
+        if case == "contract_mismatch" and rank == 1:
+            c = c.replace(V_real=V_REAL - 1)  # valid on its own, but not the group's contract
         ops = OracleOps(vp.KernelOps())
         if case == "fwd_call_fails":
             ops = FailingOps(vp.KernelOps(), failing_rank=1, failing_call="fwd")
@@ -196,7 +200,7 @@ def test_gather_order_and_fold_give_the_whole_row(built, tmp_path, world):
 
 
 @pytest.mark.parametrize("case", ["bad_contract", "bad_shape", "fwd_call_fails", "bad_bwd", "bad_bwd_dtype",
-                                  "bwd_call_fails"])
+                                  "bwd_call_fails", "contract_mismatch"])
 def test_an_invalid_call_on_one_rank_fails_closed_on_every_rank(built, tmp_path, case):
     """A host check that fails on one rank -- the layer's own, the contract check, or the shard call's
     pointer checks -- makes every rank raise the same status, and no rank is left inside a collective
@@ -212,6 +216,9 @@ def test_an_invalid_call_on_one_rank_fails_closed_on_every_rank(built, tmp_path,
         assert "another rank" not in res[bad]["bwd_message"]
         return
     assert all(not r["ok"] for r in res)
+    if case == "contract_mismatch":  # both contracts are valid: every rank names the mismatch
+        assert all(r["status"] == rlk.RLK_ERR_INVALID_ARG and "different contracts" in r["message"] for r in res)
+        return
     bad = 0 if case == "bad_shape" else 1
     want = rlk.RLK_ERR_NON_TILEABLE if case == "bad_contract" else rlk.RLK_ERR_INVALID_ARG
     assert res[bad]["status"] == want

@@ -12,11 +12,14 @@ Forward, on every rank:
 
 1. the rank checks its own call on the host (the C library's contract check,
    shapes and dtypes) -- no device work;
-2. the ranks agree: an all-reduce (MAX) of the status codes.  If any rank's
-   call is invalid, every rank raises the same error before any data moves,
-   so a rank-local failure never leaves the others waiting inside a
-   collective (the pages' review of the vocab-parallel entry point raises
-   exactly this);
+2. the ranks agree: one all-reduce (MAX) of the status codes and of a
+   fingerprint of the contract (every field, and T) taken with both signs, so
+   that MAX gives both ends of the fingerprints' range.  If any rank's call
+   is invalid, or the ranks' contracts differ, every rank raises the same
+   error before any data moves, so a rank-local failure never leaves the
+   others waiting inside a collective (the pages' review of the
+   vocab-parallel entry point raises exactly this, and their preflight
+   compares a rank-independent contract fingerprint across the TP group);
 3. ``rlk_logp_shard_fwd`` on the rank's columns: partials [T, NT/tp, 2] and
    the target logits it owns [T].  The call's own host-side status (its
    pointer and device checks) is agreed on the same way before the
@@ -36,6 +39,9 @@ Every computation is a call into the CUDA library; this module only checks,
 agrees and moves buffers.  ``ops`` lets a test substitute the per-rank
 computations to exercise the agreement and gather logic on CPU ranks.
 """
+import ctypes
+import hashlib
+
 import torch
 import torch.distributed as dist
 
@@ -58,6 +64,12 @@ class KernelOps:
 
     def shard_bwd(self, contract, shard, logits_shard, targets, mask, lse, grad):
         return shard_bwd(contract, shard, logits_shard, targets, mask, lse, grad)
+
+
+def contract_fingerprint(contract):
+    """A rank-independent identity of a contract: the first 62 bits of the SHA-256 of its 64 bytes."""
+    raw = ctypes.string_at(ctypes.addressof(contract), ctypes.sizeof(contract))
+    return int.from_bytes(hashlib.sha256(raw).digest()[:8], "little") >> 2
 
 
 def split_rows(T, world, rank):
@@ -111,14 +123,19 @@ class VocabParallelLogp:
             return e.status, str(e), None
 
     def _agree(self, status, message, device):
-        """All-reduce (MAX) of the ranks' status codes; every rank raises if any rank's call is invalid."""
-        t = torch.tensor([int(status)], dtype=torch.int32, device=device)
+        """One all-reduce (MAX) of the ranks' status codes and of the contract fingerprint with both signs;
+        every rank raises if any rank's call is invalid or the contracts differ."""
+        fp = contract_fingerprint(self.contract)
+        t = torch.tensor([int(status), fp, -fp], dtype=torch.int64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX, group=self.group)
-        worst = int(t.item())
+        worst, fp_max, fp_min = int(t[0].item()), int(t[1].item()), -int(t[2].item())
         if worst != RLK_OK:
             if status != RLK_OK:
                 raise RlkError(status, message)
             raise RlkError(worst, f"another rank of the group rejected its call ({rlk_status_string(worst)})")
+        if fp_max != fp_min:
+            raise RlkError(RLK_ERR_INVALID_ARG, "the ranks of the group hold different contracts "
+                                                "(T, vocabulary, tiles, virtual_tp, mask mode or stride differ)")
 
     def _all_gather(self, out, x):
         """out[r] = rank r's x, shard-major (out has a leading dimension of tp)."""
