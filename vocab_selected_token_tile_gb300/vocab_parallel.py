@@ -12,18 +12,18 @@ Forward, on every rank:
 
 1. the rank checks its own call on the host (the C library's contract check,
    shapes and dtypes) -- no device work;
-2. the ranks agree: one all-reduce (MAX) of the status codes and of a
-   fingerprint of the contract (every field, and T) taken with both signs, so
-   that MAX gives both ends of the fingerprints' range.  If any rank's call
-   is invalid, or the ranks' contracts differ, every rank raises the same
-   error before any data moves, so a rank-local failure never leaves the
-   others waiting inside a collective (the pages' review of the
-   vocab-parallel entry point raises exactly this, and their preflight
-   compares a rank-independent contract fingerprint across the TP group);
-3. ``rlk_logp_shard_fwd`` on the rank's columns: partials [T, NT/tp, 2] and
-   the target logits it owns [T].  The call's own host-side status (its
-   pointer and device checks) is agreed on the same way before the
-   exchange, so a call that fails on one rank fails on every rank;
+2. ``rlk_logp_shard_fwd`` on the rank's columns, unless step 1 failed:
+   partials [T, NT/tp, 2] and the target logits it owns [T];
+3. the ranks agree, before any data moves: one all-reduce (MAX) of the
+   status codes of steps 1 and 2 (the call's host-side pointer and device
+   checks) and of a fingerprint of the contract (every field, and T) taken
+   with both signs, so that MAX gives both ends of the fingerprints' range.
+   If any rank's call failed, or the ranks' contracts differ, every rank
+   raises the same error, so a rank-local failure never leaves the others
+   waiting inside a collective (the pages' review of the vocab-parallel entry
+   point raises exactly this, and their preflight compares a rank-independent
+   contract fingerprint across the TP group).  One all-reduce and one host
+   synchronisation per call;
 4. one all-gather of each (plain device buffers);
 5. ``rlk_logp_fold`` on the gathered partials, in global tile order: logp and
    LSE, replicated on every rank and bitwise those of ``rlk_logp_fwd`` on one
@@ -149,9 +149,10 @@ class VocabParallelLogp:
     def forward(self, logits_shard, targets, mask=None):
         """(logp, lse) of every row, replicated on every rank."""
         st, msg = self._local_check(logits_shard, targets, mask)
-        self._agree(st, msg, targets.device)
-        st, msg, out = self._call(self.ops.shard_fwd, self.contract, self.rank, logits_shard, targets, mask)
-        self._agree(st, msg, targets.device)
+        out = None
+        if st == RLK_OK:  # a rank whose own checks fail skips its call and still joins the agreement
+            st, msg, out = self._call(self.ops.shard_fwd, self.contract, self.rank, logits_shard, targets, mask)
+        self._agree(st, msg, targets.device)  # one host synchronisation per call
         part, xt = out
         gathered = torch.empty((self.tp,) + tuple(part.shape), dtype=part.dtype, device=part.device)
         gathered_xt = torch.empty((self.tp,) + tuple(xt.shape), dtype=xt.dtype, device=xt.device)
@@ -165,8 +166,10 @@ class VocabParallelLogp:
         if st == RLK_OK and any(t.dtype != torch.float32 or t.numel() != self.contract.T or
                                 t.device != logits_shard.device for t in (lse, grad)):
             st, msg = RLK_ERR_INVALID_ARG, "lse and grad must be FP32 [T] on the logits' device"
-        self._agree(st, msg, targets.device)
+        out = None
+        if st == RLK_OK:
+            st, msg, out = self._call(self.ops.shard_bwd, self.contract, self.rank, logits_shard, targets, mask, lse,
+                                      grad)
         # no collective follows, but every rank still returns or raises together
-        st, msg, out = self._call(self.ops.shard_bwd, self.contract, self.rank, logits_shard, targets, mask, lse, grad)
         self._agree(st, msg, targets.device)
         return out
