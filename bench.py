@@ -744,7 +744,20 @@ def e2e(rlk, c, w, logits_dev, tgt, mask, g, dev, args):
                     "LSE; dlogits stay on the device for the model's backward"}
 
 
+_RESULT_FD = 1
+
+
+def emit(line):
+    """Writes the result line to the process's original stdout, where nothing else goes (main points fd 1 at
+    stderr, so libraries' own prints -- NCCL's version banner, say -- cannot mix with the line)."""
+    os.write(_RESULT_FD, (json.dumps(line) + "\n").encode())
+
+
 def main():
+    global _RESULT_FD
+    sys.stdout.flush()
+    _RESULT_FD = os.dup(1)
+    os.dup2(2, 1)
     args = parse()
     ws, rank, local = dist_env()
     cores = cpu_threads()
@@ -775,7 +788,7 @@ def main():
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": time.perf_counter() - t0,
         }
-        print(json.dumps(line))
+        emit(line)
         return
 
     cpu = None
@@ -799,7 +812,7 @@ def main():
     if cpu is not None:
         result["cpu_baseline"] = cpu
     if rank == 0:
-        print(json.dumps(result))
+        emit(result)
     if torch.distributed.is_initialized():
         torch.distributed.destroy_process_group()
 
