@@ -16,21 +16,27 @@
 //              sees one read of the logits; the default for rlk_logp_bwd
 //              without lse_in (RLK_FUSED_SCHEDULE=resident selects kModeFused)
 //
+// Template flags add variants without putting their code in the others: the
+// entropy of each row's softmax (kFlagEnt: rlk_logp_fwd_entropy,
+// rlk_logp_fwd_bwd_entropy) and the GRPO step's on-chip g (kFlagGrpo:
+// rlk_grpo_fused_step).
+//
 // Method (PR #289 "[WS2][PR4][Logp] feat: add distributed TP/CP logprob drift
 // report": the PR-1 contract commit, the global-tile commit and the typed
 // contract commit): padded columns are -inf; the vocabulary is cut into
 // num_tiles global tiles; each tile gives an FP32 (max, sumexp) partial, the
 // identity (-inf, 0) when it has no finite column; partials are merged in
 // fixed global tile order.  Virtual TP (the H100 matrix document, "Fixes
-// exercised": fixed virtual TP8) is a cluster of virtual_tp CTAs: CTA j owns
-// the tile-aligned shard j and computes its tiles' partials; each row's
+// exercised": fixed virtual TP8) is a cluster of virtual_tp CTAs (two at
+// virtual TP 1 in kModeFusedL2): CTA j owns the tile-aligned shard j and
+// computes its tiles' partials; each row's
 // shards meet in the shared memory of one CTA, the row's folder, which folds
 // all num_tiles partials in index order and returns the LSE to the others
 // (the on-chip analogue of the pages' gather), so the result does not depend
 // on virtual_tp.
 //
 // Layout of work.  Cluster q handles rows q, q + G, q + 2G, ... (G clusters).
-// Within a CTA, 8-16 consumer warps reduce tiles (one warp per tile), one warp
+// Within a CTA, 12 or 16 consumer warps reduce tiles (one warp per tile), one warp
 // runs the exchange and fold, and one or two producer warps stream each item
 // (one row's chunk of consecutive tiles, its 16-byte-aligned column span)
 // into a ring slot with a 1-D bulk copy (cp.async.bulk, completion on the
