@@ -5,27 +5,28 @@
 // The optional fused kernel of issue #323 ("[WS2][Logprob] H100 validation
 // and reproduction guide", "Validation Boundary": "the optional PR6 fused
 // kernel") is the prior art; its design is not on the pages.  Here each
-// (128-token block, global vocabulary tile) unit runs a tcgen05 GEMM over the
-// tile's columns in chunks of up to 256 vocabulary rows (accumulators in
-// tensor memory, operands staged by TMA with the 128-byte swizzle), and the
-// epilogue turns each chunk into the running (max, sumexp) partial of the
-// tile -- the same per-tile partials as the streaming path, but of FP32
-// logits that are never rounded or written.  A fold kernel then merges the
-// tiles in fixed index order (rlk_fold.cuh) and forms logp.
+// (128-token block, 256-row chunk of a global vocabulary tile) unit runs a
+// tcgen05 GEMM (accumulators in tensor memory, operands staged by TMA with
+// the 128-byte swizzle), and the epilogue turns the chunk into its (max,
+// sumexp) partial -- of FP32 logits that are never rounded or written.  A
+// fold kernel merges each tile's chunks in chunk order into the tile's
+// partial, then the tiles in fixed index order (rlk_fold.cuh), and forms
+// logp.
 //
 // Roles (192 threads, one CTA per SM): warp 0 issues the TMA loads, warp 1
 // allocates tensor memory and issues the MMAs, warps 2-5 run the epilogue
 // (warp w reads TMEM lanes 32*(w%4)..+31, one token row per thread).
-// Units are handed out by an atomic ticket in tile-major order: the units in
-// flight at any moment are a window of consecutive units, so the token blocks
-// that share a weight tile run together and the tile is read from HBM about
-// once.  The producer's lane takes the ticket and passes the unit to the
-// other roles through a small queue in shared memory.
+// Units are handed out by an atomic ticket in chunk-major order within bands
+// of token blocks: the units in flight at any moment are a window of
+// consecutive units, so the token blocks that share a weight chunk run
+// together and the weight is read from HBM once per band.  The producer's
+// lane takes the ticket and passes the unit to the other roles through a
+// small queue in shared memory.
 // Virtual TP: the CTAs are split into virtual_tp groups; group j takes
-// tickets only for the tiles of shard j.  A tile's partial is computed by one
-// thread in one fixed order (chunks, then 32-column blocks, then columns),
-// whatever the grouping or the CTA that runs it, so outputs do not depend on
-// virtual_tp.
+// tickets only for the tiles of shard j.  A chunk's partial is computed by
+// one thread in one fixed order (32-column blocks, then columns) and a tile's
+// chunks are merged in chunk order, whatever the grouping or the CTA that
+// runs them, so outputs do not depend on virtual_tp.
 //
 // Backward: the same GEMM re-runs with an epilogue that writes
 // dlogits = g (onehot - exp(x - LSE)) in BF16, then one persistent launch
@@ -67,12 +68,17 @@ constexpr uint32_t kStageB = kBN * kBK * 2;
 constexpr uint32_t kMnBlock = 64 * kBK * 2;  // one 64-wide block of an MN-major stage: 64 K rows x 128 B
 constexpr uint64_t kDrainNsLm = 1000000000ull;
 constexpr int kMaxGroups = 8;
-// Unit order of the logits GEMMs: bands of 32 token blocks (32 MB of hidden at H = 4096), tile-major
-// within a band, hidden loaded with an L2 evict-last policy.  Measured at 8192 x 4096 x 152576
-// (DRAM reads of the forward GEMM, its time): one band of 64 blocks 8.9 GB, 6.03 ms; bands of 32
-// 3.9 GB, 5.88 ms; of 16 6.0 GB, 6.00 ms; of 8 10.6 GB, 6.19 ms; 32 with the hint 3.75 GB,
-// 5.88 ms and the recompute GEMM 6.19 ms against 6.60.
-constexpr int kBandBlocks = 32;  // token blocks per band of the logits GEMMs' unit order
+// Unit order of the logits GEMMs: a unit is one 256-row weight chunk of one token block; units
+// come in bands of token blocks whose hidden spans at most kBandHiddenBytes, chunk-major within a
+// band, hidden loaded with an L2 evict-last policy.  The units in flight then share about two
+// weight chunks (a few MB) and one band of hidden, so L2 holds both and the weight is read from
+// HBM once per band.  Measured at 8192 x 4096 x 152576 (time, DRAM reads of the forward GEMM):
+// bands of 64 MB 6.43 ms, 13.9 GB (hidden no longer stays in L2); 32 MB 5.77 ms, 2.57 GB (the
+// weight twice); 16 MB 6.06 ms; an evict-first hint on the weight loads made every band size
+// slower (64 MB 6.25 ms, 10.3 GB; 32 MB 5.92 ms).  Whole-tile units in bands of 32 blocks had
+// measured 5.88 ms and 3.75 GB: the ten chunks of a tile ran on one CTA, so the units in flight
+// spanned about 47 MB of weight.
+constexpr int64_t kBandHiddenBytes = (int64_t)32 << 20;
 constexpr int kKeepHidden = 1;   // 1: the logits GEMMs load hidden with an L2 evict-last policy
 // Tile order of the gradient GEMMs: bands of kBandN 256-wide H blocks, M-major within a band.
 // Measured at 8192 x 4096 x 152576 (DRAM reads, time of the gradient launch): bands of 16 (no
@@ -177,7 +183,7 @@ __device__ void drain_copies(Bars* bars, int64_t issued, const WaitCtl& w) {
 struct LmParams {
     const int64_t* targets;
     const uint8_t* mask;
-    float2* partials;  // [T, NT]                     (kEpiPartials)
+    float2* partials;  // [T, NT * nchunk] chunk partials (kEpiPartials)
     float* xt;         // [T] target logits          (kEpiPartials)
     const float* lse_in;  // [T]                      (kEpiGrad)
     const float* grad;    // [T] upstream g of logp   (kEpiGrad)
@@ -191,9 +197,8 @@ struct LmParams {
     int32_t keep_hidden;  // hidden tiles loaded with an L2 evict-last policy
 };
 
-// Virtual-TP group of this CTA: group j takes tickets for units
-// [0, NT/vtp * MB) of shard j, tile-major (unit u = tile j*NT/vtp + u / MB,
-// token block u % MB).
+// Virtual-TP group of this CTA: group j takes tickets for the units
+// [0, NT/vtp * nchunk * MB) of shard j (unit_coords).
 struct Group {
     int j, tile0, ntl;
     int64_t end;
@@ -205,27 +210,32 @@ __device__ Group group_of(const LmParams& p) {
     g.j = (int)blockIdx.x / Gj;
     g.ntl = p.NT / p.vtp;
     g.tile0 = g.j * g.ntl;
-    g.end = (int64_t)g.ntl * p.MB;
+    g.end = (int64_t)g.ntl * p.nchunk * p.MB;
     return g;
 }
 
-// Unit u of a group: token blocks are taken in bands of p.MBg blocks; within
-// a band the order is tile-major, so the units in flight share few weight
-// tiles (the band's blocks of one tile run together) and few hidden blocks
-// (one band).  The last band may be narrower.
-__device__ __forceinline__ void unit_coords(const LmParams& p, const Group& g, int64_t u, int& tile, int& mb) {
-    const int64_t band_units = (int64_t)g.ntl * p.MBg;
+// Unit u of a group is (weight chunk ch of tile, token block mb).  Token
+// blocks are taken in bands of p.MBg blocks; within a band the order is
+// chunk-major over the shard's tiles, so the units in flight share about two
+// weight chunks (the band's blocks of one chunk run together) and one band of
+// hidden.  The last band may be narrower.
+__device__ __forceinline__ void unit_coords(const LmParams& p, const Group& g, int64_t u, int& tile, int& ch,
+                                            int& mb) {
+    const int64_t band_units = (int64_t)g.ntl * p.nchunk * p.MBg;
     const int64_t full = p.MB / p.MBg;
+    int64_t gc;
     if (u < full * band_units) {
         const int64_t b = u / band_units, r = u % band_units;
-        tile = g.tile0 + (int)(r / p.MBg);
+        gc = r / p.MBg;
         mb = (int)(b * p.MBg + r % p.MBg);
     } else {
         const int64_t r = u - full * band_units;
         const int w = p.MB - (int)full * p.MBg;
-        tile = g.tile0 + (int)(r / w);
+        gc = r / w;
         mb = (int)(full * p.MBg + r % w);
     }
+    tile = g.tile0 + (int)(gc / p.nchunk);
+    ch = (int)(gc % p.nchunk);
 }
 
 // One 32-column block of a row's logits into the running partial of its
@@ -317,29 +327,27 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                 int64_t u = (int64_t)atomicAdd(&p.tickets[grp.j], 1ull);
                 if (u >= grp.end) u = -1;
                 if (!unit_put(bars, n++, u, p.w) || u < 0) break;
-                int tile, mb;
-                unit_coords(p, grp, u, tile, mb);
-                for (int ch = 0; ch < p.nchunk && !aborted; ++ch) {
-                    const bool last_rem = (ch == p.nchunk - 1) && p.rem;
-                    const int nrows = last_rem ? p.rem : kBN;
-                    const int n0 = tile * p.W + ch * kBN;
-                    for (int kb = 0; kb < KB; ++kb) {
-                        if (!lm_wait(bars, smem_u32(&bars->empty[stage]), phase ^ 1u, p.w)) {
-                            aborted = true;
-                            break;
-                        }
-                        const uint32_t fb = smem_u32(&bars->full[stage]);
-                        mbar_arrive_expect_tx(fb, kStageA + (uint32_t)nrows * kBK * 2);
-                        if (p.keep_hidden)
-                            tma_load_2d_hint(smem_u32(sA + stage * kStageA), &tmH, kb * kBK, mb * kBM, fb, keep);
-                        else
-                            tma_load_2d(smem_u32(sA + stage * kStageA), &tmH, kb * kBK, mb * kBM, fb);
-                        tma_load_2d(smem_u32(sB + stage * kStageB), last_rem ? &tmWr : &tmW, kb * kBK, n0, fb);
-                        ++issued;
-                        if (++stage == kStages) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                int tile, ch, mb;
+                unit_coords(p, grp, u, tile, ch, mb);
+                const bool last_rem = (ch == p.nchunk - 1) && p.rem;
+                const int nrows = last_rem ? p.rem : kBN;
+                const int n0 = tile * p.W + ch * kBN;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!lm_wait(bars, smem_u32(&bars->empty[stage]), phase ^ 1u, p.w)) {
+                        aborted = true;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&bars->full[stage]);
+                    mbar_arrive_expect_tx(fb, kStageA + (uint32_t)nrows * kBK * 2);
+                    if (p.keep_hidden)
+                        tma_load_2d_hint(smem_u32(sA + stage * kStageA), &tmH, kb * kBK, mb * kBM, fb, keep);
+                    else
+                        tma_load_2d(smem_u32(sA + stage * kStageA), &tmH, kb * kBK, mb * kBM, fb);
+                    tma_load_2d(smem_u32(sB + stage * kStageB), last_rem ? &tmWr : &tmW, kb * kBK, n0, fb);
+                    ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
                 }
             }
@@ -357,37 +365,35 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                 if (!unit_get(bars, n, u, p.w)) break;
                 unit_done(bars, n++);
                 if (u < 0) break;
-                for (int ch = 0; ch < p.nchunk && !aborted; ++ch, ++chunk) {
-                    const int acc = (int)(chunk & 1);
-                    const uint32_t accph = (uint32_t)((chunk >> 1) & 1);
-                    if (!lm_wait(bars, smem_u32(&bars->tempty[acc]), accph ^ 1u, p.w)) {
+                int tile, ch, mb;
+                unit_coords(p, grp, u, tile, ch, mb);
+                const int acc = (int)(chunk & 1);
+                const uint32_t accph = (uint32_t)((chunk >> 1) & 1);
+                ++chunk;
+                if (!lm_wait(bars, smem_u32(&bars->tempty[acc]), accph ^ 1u, p.w)) break;
+                tc_fence_after();
+                const bool last_rem = (ch == p.nchunk - 1) && p.rem;
+                const uint32_t idesc = idesc_bf16_f32(kBM, last_rem ? (uint32_t)p.rem : (uint32_t)kBN);
+                const uint32_t d = tmem + (uint32_t)(acc * kBN);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!lm_wait(bars, smem_u32(&bars->full[stage]), phase, p.w)) {
                         aborted = true;
                         break;
                     }
                     tc_fence_after();
-                    const bool last_rem = (ch == p.nchunk - 1) && p.rem;
-                    const uint32_t idesc = idesc_bf16_f32(kBM, last_rem ? (uint32_t)p.rem : (uint32_t)kBN);
-                    const uint32_t d = tmem + (uint32_t)(acc * kBN);
-                    for (int kb = 0; kb < KB; ++kb) {
-                        if (!lm_wait(bars, smem_u32(&bars->full[stage]), phase, p.w)) {
-                            aborted = true;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t a0 = smem_u32(sA + stage * kStageA);
-                        const uint32_t b0 = smem_u32(sB + stage * kStageB);
+                    const uint32_t a0 = smem_u32(sA + stage * kStageA);
+                    const uint32_t b0 = smem_u32(sB + stage * kStageB);
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk)
-                            umma_bf16(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
-                                      (kb | kk) != 0);
-                        umma_commit(smem_u32(&bars->empty[stage]));  // frees the stage when these MMAs finish
-                        if (++stage == kStages) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        umma_bf16(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
+                                  (kb | kk) != 0);
+                    umma_commit(smem_u32(&bars->empty[stage]));  // frees the stage when these MMAs finish
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
-                    if (!aborted) umma_commit(smem_u32(&bars->tfull[acc]));
                 }
+                if (!aborted) umma_commit(smem_u32(&bars->tfull[acc]));
             }
             // Every issued MMA completes before tensor memory is freed.
             umma_commit(smem_u32(&bars->drain));
@@ -399,8 +405,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
         const int r_in = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         int64_t chunk = 0, n = 0;
-        bool aborted = false;
-        while (!aborted) {
+        for (;;) {
             int64_t u = -1;
             const bool got = unit_get(bars, n, u, p.w);
             if (!__all_sync(0xFFFFFFFFu, got)) break;
@@ -408,8 +413,8 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             if (lane == 0) unit_done(bars, n);
             ++n;
             if (u < 0) break;
-            int tile, mb;
-            unit_coords(p, grp, u, tile, mb);
+            int tile, ch, mb;
+            unit_coords(p, grp, u, tile, ch, mb);
             const int64_t row = (int64_t)mb * kBM + r_in;
             const bool valid = row < p.T;
             int64_t target = -1;
@@ -428,46 +433,43 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                 nlL = -__fmul_rn(l, kLog2e);
                 drow = p.dlogits + row * p.Vp;
                 // the device conditions of a backward given the LSE, reported once per row
-                if (active && tile == grp.tile0 && grp.j == 0) {
+                if (active && tile == grp.tile0 && ch == 0 && grp.j == 0) {
                     if (target < 0 || target >= p.Vr) atomicOr(p.w.status, kStatusTargetRange);
                     if (!isfinite(l)) atomicOr(p.w.status, kStatusNonFinite);
                 }
             }
-            for (int ch = 0; ch < p.nchunk; ++ch, ++chunk) {
-                const int acc = (int)(chunk & 1);
-                const uint32_t accph = (uint32_t)((chunk >> 1) & 1);
-                const bool ok = lm_wait(bars, smem_u32(&bars->tfull[acc]), accph, p.w);
-                if (!__all_sync(0xFFFFFFFFu, ok)) {
-                    aborted = true;
-                    break;
+            const int acc = (int)(chunk & 1);
+            const uint32_t accph = (uint32_t)((chunk >> 1) & 1);
+            ++chunk;
+            const bool ok = lm_wait(bars, smem_u32(&bars->tfull[acc]), accph, p.w);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after();
+            const int ncols = ((ch == p.nchunk - 1) && p.rem) ? p.rem : kBN;
+            const int64_t cbase = (int64_t)tile * p.W + (int64_t)ch * kBN;
+            for (int sub = 0; sub * 32 < ncols; ++sub) {
+                float v[32];
+                tmem_ld32(tmem + lane_base + (uint32_t)(acc * kBN + sub * 32), v);
+                const int nv = min(32, ncols - sub * 32);
+                const int64_t col0 = cbase + sub * 32;
+                if (EPI == kEpiGrad) {
+                    if (valid) grad_block(v, nv, col0, p.Vr, active, target, g, nlL, drow);
+                    continue;
                 }
-                tc_fence_after();
-                const int ncols = ((ch == p.nchunk - 1) && p.rem) ? p.rem : kBN;
-                const int64_t cbase = (int64_t)tile * p.W + (int64_t)ch * kBN;
-                for (int sub = 0; sub * 32 < ncols; ++sub) {
-                    float v[32];
-                    tmem_ld32(tmem + lane_base + (uint32_t)(acc * kBN + sub * 32), v);
-                    const int nv = min(32, ncols - sub * 32);
-                    const int64_t col0 = cbase + sub * 32;
-                    if (EPI == kEpiGrad) {
-                        if (valid) grad_block(v, nv, col0, p.Vr, active, target, g, nlL, drow);
-                        continue;
-                    }
-                    online_block(v, nv, col0, p.Vr, m_run, s_run);
-                    if (active && target >= col0 && target < col0 + nv && target < p.Vr) {
-                        const int idx = (int)(target - col0);
+                online_block(v, nv, col0, p.Vr, m_run, s_run);
+                if (active && target >= col0 && target < col0 + nv && target < p.Vr) {
+                    const int idx = (int)(target - col0);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (i == idx) xt = v[i];
-                        have_xt = true;
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        if (i == idx) xt = v[i];
+                    have_xt = true;
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bars->tempty[acc]));
             }
-            if (EPI == kEpiPartials && !aborted && valid) {
-                p.partials[row * p.NT + tile] = make_float2(m_run, s_run);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars->tempty[acc]));
+            if (EPI == kEpiPartials && valid) {
+                const int64_t k = (int64_t)tile * p.nchunk + ch;
+                p.partials[row * (int64_t)p.NT * p.nchunk + k] = make_float2(m_run, s_run);
                 if (have_xt) p.xt[row] = xt;
             }
         }
@@ -480,16 +482,39 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
     }
 }
 
-// LSE and logp of each row from its tile partials (one warp per row).
+// A tile's partial from its chunk partials, merged in chunk order: the
+// running maximum, the sum rescaled when the maximum grows, then the chunk's
+// sum scaled to it.  An all -inf chunk is the identity; a NaN maximum stays.
+__device__ __forceinline__ float2 merge_chunks(const float2* c, int nchunk) {
+    float m = -INFINITY, s = 0.f;
+    for (int k = 0; k < nchunk; ++k) {
+        const float2 q = c[k];
+        if (q.x == -INFINITY) continue;
+        const float M = fmax_nan(m, q.x);
+        if (M != m) s = __fmul_rn(s, ex2_approx(__fmul_rn(__fsub_rn(m, M), kLog2e)));
+        s = __fadd_rn(s, __fmul_rn(q.y, ex2_approx(__fmul_rn(__fsub_rn(q.x, M), kLog2e))));
+        m = M;
+    }
+    return make_float2(m, s);
+}
+
+// LSE and logp of each row from its chunk partials (one warp per row): each
+// lane merges the chunks of its tiles, then the tiles are folded in index
+// order as in the streaming path.
 __global__ void lmhead_fold_kernel(const float2* partials, const float* xt, const int64_t* targets,
                                    const uint8_t* mask, int mask_mode, int64_t ignore_index, int64_t T, int64_t Vr,
-                                   int NT, float* logp, float* lse, uint32_t* status) {
+                                   int NT, int nchunk, float* logp, float* lse, uint32_t* status) {
     extern __shared__ float2 scratch[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     float2* sc = scratch + (size_t)warp * NT;
     for (int64_t row = (int64_t)blockIdx.x * wpb + warp; row < T; row += (int64_t)gridDim.x * wpb) {
-        const float l = fold_tiles(partials + row * NT, NT, sc, lane);
+        const float2* pr = partials + row * (int64_t)NT * nchunk;
+        for (int t = lane; t < NT; t += 32) sc[t] = merge_chunks(pr + (int64_t)t * nchunk, nchunk);
+        __syncwarp();
+        // fold_tiles reads each tile's entry before it writes that index of its scratch, so the
+        // merged tiles may serve as both
+        const float l = fold_tiles(sc, NT, sc, lane);
         if (lane == 0) {
             const int64_t t = targets[row];
             const bool active = (mask_mode == RLK_MASK_EXPLICIT) ? (mask[row] != 0) : (t != ignore_index);
@@ -791,12 +816,20 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
 constexpr size_t kGemmSmem = 1024 + (size_t)kStages * (kStageA + kStageB) + sizeof(Bars);
 
+// Chunks of kBN weight rows per tile (the last one may be narrower).
+int64_t chunks_per_tile(const rlk_logp_contract& c) { return (c.V_padded / c.num_tiles + kBN - 1) / kBN; }
+
+size_t partial_bytes(const rlk_logp_contract& c) {
+    return round256((size_t)c.T * c.num_tiles * chunks_per_tile(c) * 8);
+}
+
 }  // namespace
 
-// Workspace beyond the status word: tickets, FP32 partials [T, NT, 2], target
-// logits [T]; the backward adds BF16 dlogits [T, V_padded].
+// Workspace beyond the status word: tickets, FP32 chunk partials
+// [T, NT * chunks, 2], target logits [T]; the backward adds BF16 dlogits
+// [T, V_padded].
 size_t lmhead_fwd_workspace(const rlk_logp_contract& c) {
-    return kTicketBytes + round256((size_t)c.T * c.num_tiles * 8) + round256((size_t)c.T * 4);
+    return kTicketBytes + partial_bytes(c) + round256((size_t)c.T * 4);
 }
 
 size_t lmhead_bwd_workspace(const rlk_logp_contract& c) {
@@ -852,13 +885,16 @@ rlk_status prepare(LmLaunch& L, const rlk_logp_contract& c, const void* hidden, 
     p.rem = p.W % kBN;
     p.mask_mode = c.mask_mode;
     p.MB = (int32_t)((c.T + kBM - 1) / kBM);
-    p.MBg = p.MB < kBandBlocks ? p.MB : kBandBlocks;
+    {
+        const int64_t band = kBandHiddenBytes / ((int64_t)kBM * H * 2);
+        p.MBg = (int32_t)(band < 1 ? 1 : band < p.MB ? band : p.MB);
+    }
     p.keep_hidden = kKeepHidden;
     const uint32_t rrows = p.rem ? (uint32_t)p.rem : (uint32_t)kBN;
     if (!make_map(&L.tmH, hidden, H, c.T, H, kBK, kBM) || !make_map(&L.tmW, weight, H, c.V_padded, H, kBK, kBN) ||
         !make_map(&L.tmWr, weight, H, c.V_padded, H, kBK, rrows))
         return fail(RLK_ERR_CUDA, "cuTensorMapEncodeTiled failed for the hidden or weight tensor");
-    const int64_t units_per_shard = (int64_t)(c.num_tiles / c.virtual_tp) * p.MB;
+    const int64_t units_per_shard = (int64_t)(c.num_tiles / c.virtual_tp) * p.nchunk * p.MB;
     int64_t per_group = sms / c.virtual_tp;  // CTAs per virtual-TP group
     if (per_group > units_per_shard) per_group = units_per_shard;
     if (per_group < 1) per_group = 1;
@@ -896,7 +932,7 @@ rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int
     if ((st = prepare(L, c, hidden, H, weight, targets, mask, status, tickets)) != RLK_OK) return st;
     LmParams& p = L.p;
     p.partials = reinterpret_cast<float2*>(ws + kTicketBytes);
-    p.xt = reinterpret_cast<float*>(ws + kTicketBytes + round256((size_t)c.T * c.num_tiles * 8));
+    p.xt = reinterpret_cast<float*>(ws + kTicketBytes + partial_bytes(c));
     if ((st = launch_gemm(lmhead_kernel<kEpiPartials>, L.grid, stream, "lm_head GEMM", L.tmH, L.tmW, L.tmWr, p)) !=
         RLK_OK)
         return st;
@@ -908,7 +944,8 @@ rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int
     int64_t fold_grid = (c.T + 7) / 8;
     if (fold_grid > (int64_t)L.sms * 8) fold_grid = (int64_t)L.sms * 8;
     lmhead_fold_kernel<<<(unsigned)fold_grid, fold_threads, fold_smem, stream>>>(
-        p.partials, p.xt, targets, mask, c.mask_mode, c.ignore_index, c.T, c.V_real, c.num_tiles, logp, lse, status);
+        p.partials, p.xt, targets, mask, c.mask_mode, c.ignore_index, c.T, c.V_real, c.num_tiles, p.nchunk, logp, lse,
+        status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("lm_head fold launch: ") + cudaGetErrorString(e));
     return RLK_OK;
