@@ -257,10 +257,13 @@ rlk_status rlk_logp_bwd(const rlk_logp_contract* contract, const void* logits_bf
                         float* logp_out, float* lse_out, void* workspace, rlk_stream_t stream);
 
 /*
- * Bytes of device workspace rlk_logp_fused_lmhead needs for hidden size H
- * (the status word, 256 bytes of work tickets, FP32 partials
- * [T, num_tiles, 2], target logits [T], and for the backward the BF16 dlogits
- * [T, V_padded]); 0 for an unsupported contract.
+ * Bytes of device workspace rlk_logp_fused_lmhead and rlk_logp_fused_lmhead_bwd
+ * need for hidden size H: the status word, 256 bytes of work tickets, FP32
+ * partials [T, num_tiles * ceil(V_padded / num_tiles / 256), 2] (one per
+ * 256-row weight chunk), target logits [T], and for the backward the BF16
+ * dlogits [T, V_padded] and the forward's FP32 logits [T, V_padded] (about
+ * T * V_padded * 6 bytes in all: 7.5 GB for 8192 x 152576); 0 for an
+ * unsupported contract.
  */
 size_t rlk_logp_lmhead_workspace_size(const rlk_logp_contract* contract, int64_t H);
 
@@ -268,16 +271,18 @@ size_t rlk_logp_lmhead_workspace_size(const rlk_logp_contract* contract, int64_t
  * Fused lm_head: logp and LSE of logits = hidden @ weight^T without
  * materialising the logits (the optional fused kernel of issue #323,
  * "Validation Boundary").  A tcgen05 GEMM (FP32 accumulators in tensor
- * memory) feeds each (128-token block, vocabulary tile) into the tile's
- * (max, sumexp) partial in its epilogue; the partials are folded in fixed
- * tile order.  The logits stay FP32 (never rounded to BF16).
+ * memory) turns each (128-token block, 256-row weight chunk) into the chunk's
+ * (max, sumexp) partial in its epilogue; a tile's chunks are merged in chunk
+ * order and the tiles folded in fixed tile order.  The logits stay FP32
+ * (never rounded to BF16).
  *   hidden_bf16  [T, H] BF16 row-major, 16-byte aligned; H a multiple of 64.
  *   weight_bf16  [V_padded, H] BF16 row-major; rows >= V_real are padding
  *                and are never read.
  *   targets, active_mask, logp, lse: as for rlk_logp_fwd.
  *   grad_logp    NULL (forward only) or [T] FP32 upstream gradient of logp.
- *                With it the backward runs too: dlogits = g (onehot - softmax)
- *                are recomputed from a second pass of the GEMM and the LSE just
+ *                With it the backward runs too: the forward also writes its
+ *                FP32 logits to the workspace, an elementwise pass forms
+ *                dlogits = g (onehot - softmax) from them and the LSE just
  *                formed (BF16, in the workspace), then two more tcgen05 GEMMs
  *                with FP32 accumulation give
  *   dhidden_bf16 [T, H] BF16 out = dlogits[:, :V_real] @ weight[:V_real], and
@@ -287,8 +292,9 @@ size_t rlk_logp_lmhead_workspace_size(const rlk_logp_contract* contract, int64_t
  *                Each output element is accumulated over its whole K range in
  *                one fixed order by one CTA (no split-K, no atomics), so the
  *                gradients are deterministic.  All three NULL without grad_logp.
- *   workspace    rlk_logp_lmhead_workspace_size(contract, H) bytes (it holds
- *                the BF16 dlogits, T * V_padded * 2 bytes, for the backward).
+ *   workspace    rlk_logp_lmhead_workspace_size(contract, H) bytes (for the
+ *                backward it holds the FP32 logits and the BF16 dlogits,
+ *                T * V_padded * 6 bytes).
  * The tile width V_padded / num_tiles must be a multiple of 16.  row_stride
  * is not used.  Outputs are bitwise identical for every virtual_tp.
  */

@@ -28,9 +28,14 @@
 // chunks are merged in chunk order, whatever the grouping or the CTA that
 // runs them, so outputs do not depend on virtual_tp.
 //
-// Backward: the same GEMM re-runs with an epilogue that writes
-// dlogits = g (onehot - exp(x - LSE)) in BF16, then one persistent launch
-// runs the two gradient contractions as tcgen05 GEMMs with FP32 accumulators:
+// Backward: dlogits = g (onehot - exp(x - LSE)) in BF16.  In the forward +
+// backward call the forward also stores its FP32 logits (staged through
+// shared memory so that each store writes a 128-byte row segment) and an
+// elementwise pass forms dlogits once the fold has the LSE; the backward from
+// a given LSE re-runs the GEMM with an epilogue that writes dlogits.  The
+// logits are the same accumulators either way, so dlogits are bitwise equal.
+// Then one persistent launch runs the two gradient contractions as tcgen05
+// GEMMs with FP32 accumulators:
 //   dHidden[T, H]  = dlogits[:, :V_real] W[:V_real]      (A K-major, B MN-major)
 //   dW[V_padded, H] = dlogits[:, :V_real]^T hidden       (A and B MN-major)
 // Each output tile accumulates its whole K range in one fixed order on one
@@ -88,7 +93,9 @@ constexpr int kBandN = 8;
 // Workspace: 256 bytes of tickets (three launches x kMaxGroups 64-bit counters).
 constexpr size_t kTicketBytes = 256;
 
-enum : int { kEpiPartials = 0, kEpiGrad = 1 };
+// kEpiPartials: chunk partials and target logits; kEpiPartialsStore: the same,
+// and the FP32 logits written to a [T, V_padded] buffer; kEpiGrad: dlogits.
+enum : int { kEpiPartials = 0, kEpiGrad = 1, kEpiPartialsStore = 2 };
 
 struct Bars {
     uint64_t full[kStages];
@@ -102,6 +109,12 @@ struct Bars {
     uint32_t tmem_addr;
     int abort_flag;
 };
+
+// Shared memory of the logits GEMMs past the 1024-byte alignment slack: the
+// operand stages, then the barriers (then, for kEpiPartialsStore, the staging
+// blocks of the logits store).
+constexpr size_t kGemmSmemCore = (size_t)kStages * (kStageA + kStageB) + (sizeof(Bars) + 15) / 16 * 16;
+constexpr int kStoreStage = 32 * 33;  // floats per epilogue warp: 32 rows, pitch 33
 
 struct WaitCtl {
     uint32_t* status;
@@ -185,6 +198,7 @@ struct LmParams {
     const uint8_t* mask;
     float2* partials;  // [T, NT * nchunk] chunk partials (kEpiPartials)
     float* xt;         // [T] target logits          (kEpiPartials)
+    float* xlog;       // [T, Vp] FP32 logits out     (kEpiPartialsStore)
     const float* lse_in;  // [T]                      (kEpiGrad)
     const float* grad;    // [T] upstream g of logp   (kEpiGrad)
     uint16_t* dlogits;    // [T, Vp] BF16 out         (kEpiGrad)
@@ -404,6 +418,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
         const int quarter = warp & 3;
         const int r_in = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        float* xst = reinterpret_cast<float*>(smem + kGemmSmemCore) + quarter * kStoreStage;
         int64_t chunk = 0, n = 0;
         for (;;) {
             int64_t u = -1;
@@ -455,6 +470,19 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                     if (valid) grad_block(v, nv, col0, p.Vr, active, target, g, nlL, drow);
                     continue;
                 }
+                if (EPI == kEpiPartialsStore) {
+                    // The warp's 32 rows x nv columns through shared memory (row pitch 33:
+                    // conflict-free both ways), then one 128-byte row segment per store.
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (i < nv) xst[lane * 33 + i] = v[i];
+                    __syncwarp();
+                    const int64_t row0 = (int64_t)mb * kBM + quarter * 32;
+                    for (int rr = 0; rr < 32; ++rr)
+                        if (row0 + rr < p.T && lane < nv)
+                            p.xlog[(row0 + rr) * p.Vp + col0 + lane] = xst[rr * 33 + lane];
+                    __syncwarp();
+                }
                 online_block(v, nv, col0, p.Vr, m_run, s_run);
                 if (active && target >= col0 && target < col0 + nv && target < p.Vr) {
                     const int idx = (int)(target - col0);
@@ -467,7 +495,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bars->tempty[acc]));
-            if (EPI == kEpiPartials && valid) {
+            if (EPI != kEpiGrad && valid) {
                 const int64_t k = (int64_t)tile * p.nchunk + ch;
                 p.partials[row * (int64_t)p.NT * p.nchunk + k] = make_float2(m_run, s_run);
                 if (have_xt) p.xt[row] = xt;
@@ -530,6 +558,55 @@ __global__ void lmhead_fold_kernel(const float2* partials, const float* xt, cons
             if (active && !isfinite(l)) atomicOr(status, kStatusNonFinite);
         }
         __syncwarp();
+    }
+}
+
+// dlogits from the FP32 logits the forward stored: g * ([c == t] - exp(x - LSE))
+// on the real columns of an active row, exactly 0 elsewhere, BF16 -- the
+// operations of grad_block on the same FP32 values, so the result is bitwise
+// that of the recompute GEMM's epilogue.  One CTA a row (a grid-stride loop
+// past 2^31 - 1 rows), 8 columns (two 16-byte loads, one 16-byte store) a
+// thread per step; both streams are read or written once, with the
+// cache-streaming hint.
+__global__ void __launch_bounds__(256) lmhead_dlogits_kernel(const float* xlog, const float* lse,
+                                                             const float* grad, const int64_t* targets,
+                                                             const uint8_t* mask, int mask_mode,
+                                                             int64_t ignore_index, int64_t T, int64_t Vr,
+                                                             int64_t Vp, uint16_t* dlogits) {
+    const int64_t groups = Vp / 8;
+    for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
+        const int64_t t = targets[row];
+        const bool active = (mask_mode == RLK_MASK_EXPLICIT) ? (mask[row] != 0) : (t != ignore_index);
+        const float g = grad[row];
+        const float nlL = -__fmul_rn(lse[row], kLog2e);
+        const float4* xr = reinterpret_cast<const float4*>(xlog + row * Vp);
+        uint4* dr = reinterpret_cast<uint4*>(dlogits + row * Vp);
+        for (int64_t q = threadIdx.x; q < groups; q += blockDim.x) {
+            const int64_t c0 = q * 8;
+            uint4 o = make_uint4(0u, 0u, 0u, 0u);
+            if (active && c0 < Vr) {
+                const float4 a = __ldcs(&xr[2 * q]), b = __ldcs(&xr[2 * q + 1]);
+                const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                    float d[2];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int64_t c = c0 + i + j;
+                        float dj = 0.f;
+                        if (c < Vr) {
+                            const float pr = ex2_approx(__fmaf_rn(x[i + j], kLog2e, nlL));
+                            dj = (c == t) ? __fmul_rn(g, __fsub_rn(1.f, pr)) : __fmul_rn(-g, pr);
+                        }
+                        d[j] = dj;
+                    }
+                    w[i >> 1] = pack_bf16x2_rn(d[0], d[1]);
+                }
+                o = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            __stcs(&dr[q], o);
+        }
     }
 }
 
@@ -814,7 +891,9 @@ bool make_map_mn3(CUtensorMap* m, const void* base, int64_t inner, int64_t rows,
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
-constexpr size_t kGemmSmem = 1024 + (size_t)kStages * (kStageA + kStageB) + sizeof(Bars);
+constexpr size_t kGemmSmem = 1024 + kGemmSmemCore;
+// kEpiPartialsStore adds one 32 x 33 FP32 staging block per epilogue warp.
+constexpr size_t kGemmSmemStore = kGemmSmem + 4 * kStoreStage * sizeof(float);
 
 // Chunks of kBN weight rows per tile (the last one may be narrower).
 int64_t chunks_per_tile(const rlk_logp_contract& c) { return (c.V_padded / c.num_tiles + kBN - 1) / kBN; }
@@ -823,17 +902,20 @@ size_t partial_bytes(const rlk_logp_contract& c) {
     return round256((size_t)c.T * c.num_tiles * chunks_per_tile(c) * 8);
 }
 
+size_t dlogits_bytes(const rlk_logp_contract& c) { return round256((size_t)c.T * c.V_padded * 2); }
+
 }  // namespace
 
 // Workspace beyond the status word: tickets, FP32 chunk partials
 // [T, NT * chunks, 2], target logits [T]; the backward adds BF16 dlogits
-// [T, V_padded].
+// [T, V_padded] and, for the forward+backward in one call, the forward's FP32
+// logits [T, V_padded].
 size_t lmhead_fwd_workspace(const rlk_logp_contract& c) {
     return kTicketBytes + partial_bytes(c) + round256((size_t)c.T * 4);
 }
 
 size_t lmhead_bwd_workspace(const rlk_logp_contract& c) {
-    return lmhead_fwd_workspace(c) + round256((size_t)c.T * c.V_padded * 2);
+    return lmhead_fwd_workspace(c) + dlogits_bytes(c) + round256((size_t)c.T * c.V_padded * 4);
 }
 
 rlk_status lmhead_check(const rlk_logp_contract& c, int64_t H) {
@@ -904,13 +986,18 @@ rlk_status prepare(LmLaunch& L, const rlk_logp_contract& c, const void* hidden, 
 }
 
 template <class K, class... Args>
-rlk_status launch_gemm(K kernel, int grid, cudaStream_t stream, const char* what, Args... args) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+rlk_status launch_gemm_smem(K kernel, int grid, size_t smem, cudaStream_t stream, const char* what, Args... args) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-    kernel<<<(unsigned)grid, kThreadsLm, kGemmSmem, stream>>>(args...);
+    kernel<<<(unsigned)grid, kThreadsLm, smem, stream>>>(args...);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string(what) + " launch: " + cudaGetErrorString(e));
     return RLK_OK;
+}
+
+template <class K, class... Args>
+rlk_status launch_gemm(K kernel, int grid, cudaStream_t stream, const char* what, Args... args) {
+    return launch_gemm_smem(kernel, grid, kGemmSmem, stream, what, args...);
 }
 
 rlk_status clear_tickets(void* tickets, cudaStream_t stream) {
@@ -919,11 +1006,11 @@ rlk_status clear_tickets(void* tickets, cudaStream_t stream) {
     return RLK_OK;
 }
 
-}  // namespace
-
-rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
-                             const int64_t* targets, const uint8_t* mask, float* logp, float* lse, void* workspace,
-                             uint32_t* status, cudaStream_t stream) {
+// The forward: the logits GEMM with the partials epilogue (and, with xlog,
+// the FP32 logits stored), then the fold.
+rlk_status forward(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                   const int64_t* targets, const uint8_t* mask, float* logp, float* lse, void* workspace,
+                   float* xlog, uint32_t* status, cudaStream_t stream) {
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     unsigned long long* tickets = reinterpret_cast<unsigned long long*>(ws);
     rlk_status st = clear_tickets(tickets, stream);
@@ -933,9 +1020,11 @@ rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int
     LmParams& p = L.p;
     p.partials = reinterpret_cast<float2*>(ws + kTicketBytes);
     p.xt = reinterpret_cast<float*>(ws + kTicketBytes + partial_bytes(c));
-    if ((st = launch_gemm(lmhead_kernel<kEpiPartials>, L.grid, stream, "lm_head GEMM", L.tmH, L.tmW, L.tmWr, p)) !=
-        RLK_OK)
-        return st;
+    p.xlog = xlog;
+    st = xlog ? launch_gemm_smem(lmhead_kernel<kEpiPartialsStore>, L.grid, kGemmSmemStore, stream, "lm_head GEMM",
+                                 L.tmH, L.tmW, L.tmWr, p)
+              : launch_gemm(lmhead_kernel<kEpiPartials>, L.grid, stream, "lm_head GEMM", L.tmH, L.tmW, L.tmWr, p);
+    if (st != RLK_OK) return st;
     const int fold_threads = 256;
     const size_t fold_smem = (size_t)(fold_threads / 32) * c.num_tiles * sizeof(float2);
     cudaError_t e =
@@ -951,40 +1040,16 @@ rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int
     return RLK_OK;
 }
 
-rlk_status launch_lmhead_bwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
-                             const int64_t* targets, const uint8_t* mask, const float* grad, float* logp, float* lse,
-                             void* dhidden, float* dweight_f32, void* dweight_bf16, void* workspace, uint32_t* status,
-                             cudaStream_t stream) {
-    // 1. forward: LSE and logp
-    rlk_status st = launch_lmhead_fwd(c, hidden, H, weight, targets, mask, logp, lse, workspace, status, stream);
+// dHidden = dlogits[:, :V_real] W[:V_real] and dW = dlogits[:, :V_real]^T hidden in one launch.
+// The maps stop at V_real (and at T), so padded columns of dlogits, padded
+// rows of W and rows past T read as zero; rows [V_real, V_padded) of dW come
+// out exactly 0.
+rlk_status grad_gemms(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                      const uint16_t* dlogits, void* dhidden, float* dweight_f32, void* dweight_bf16,
+                      unsigned long long* ticket, uint32_t* status, cudaStream_t stream) {
+    int sms = 0;
+    rlk_status st = sm_count(&sms);
     if (st != RLK_OK) return st;
-    // 2.-3. the backward from that LSE
-    return launch_lmhead_bwd_given_lse(c, hidden, H, weight, targets, mask, grad, lse, dhidden, dweight_f32,
-                                       dweight_bf16, workspace, status, stream);
-}
-
-rlk_status launch_lmhead_bwd_given_lse(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
-                                       const int64_t* targets, const uint8_t* mask, const float* grad,
-                                       const float* lse, void* dhidden, float* dweight_f32, void* dweight_bf16,
-                                       void* workspace, uint32_t* status, cudaStream_t stream) {
-    unsigned char* ws = static_cast<unsigned char*>(workspace);
-    unsigned long long* tickets = reinterpret_cast<unsigned long long*>(ws);
-    rlk_status st = clear_tickets(tickets, stream);
-    if (st != RLK_OK) return st;
-    uint16_t* dlogits = reinterpret_cast<uint16_t*>(ws + lmhead_fwd_workspace(c));
-    // 2. dlogits = g * (onehot - exp(x - LSE)) from the recomputed logits (BF16 [T, V_padded])
-    LmLaunch L;
-    if ((st = prepare(L, c, hidden, H, weight, targets, mask, status, tickets + kMaxGroups)) != RLK_OK) return st;
-    L.p.lse_in = lse;
-    L.p.grad = grad;
-    L.p.dlogits = dlogits;
-    if ((st = launch_gemm(lmhead_kernel<kEpiGrad>, L.grid, stream, "lm_head recompute GEMM", L.tmH, L.tmW, L.tmWr,
-                          L.p)) != RLK_OK)
-        return st;
-    // 3. dHidden = dlogits[:, :V_real] W[:V_real] and dW = dlogits[:, :V_real]^T hidden in one launch.
-    // The maps stop at V_real (and at T), so padded columns of dlogits, padded
-    // rows of W and rows past T read as zero; rows [V_real, V_padded) of dW
-    // come out exactly 0.
     CUtensorMap tmA0, tmB0, tmA1, tmB1;
     if (!make_map(&tmA0, dlogits, c.V_real, c.T, c.V_padded, kBK, kBM) ||
         !make_map_mn3(&tmB0, weight, H, c.V_real, H, kBK, 4) ||
@@ -995,8 +1060,9 @@ rlk_status launch_lmhead_bwd_given_lse(const rlk_logp_contract& c, const void* h
     g.dhidden = static_cast<uint16_t*>(dhidden);
     g.dw_bf16 = static_cast<uint16_t*>(dweight_bf16);
     g.dw_f32 = dweight_f32;
-    g.ticket = tickets + 2 * kMaxGroups;
-    g.w = L.p.w;
+    g.ticket = ticket;
+    g.w.status = status;
+    g.w.wait_ns = c.wait_timeout_ns > 0 ? (uint64_t)c.wait_timeout_ns : kDefaultWaitNs;
     g.T = c.T;
     g.Vr = c.V_real;
     g.Vp = c.V_padded;
@@ -1008,8 +1074,66 @@ rlk_status launch_lmhead_bwd_given_lse(const rlk_logp_contract& c, const void* h
     g.n0 = ((c.T + kBM - 1) / kBM) * g.NB;
     g.n1 = ((c.V_padded + kBM - 1) / kBM) * g.NB;
     const int64_t total = g.n0 + g.n1;
-    const int grid = (int)(total < L.sms ? total : L.sms);
+    const int grid = (int)(total < sms ? total : sms);
     return launch_gemm(lmhead_grad_kernel, grid, stream, "lm_head gradient GEMM", tmA0, tmB0, tmA1, tmB1, g);
+}
+
+}  // namespace
+
+rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                             const int64_t* targets, const uint8_t* mask, float* logp, float* lse, void* workspace,
+                             uint32_t* status, cudaStream_t stream) {
+    return forward(c, hidden, H, weight, targets, mask, logp, lse, workspace, nullptr, status, stream);
+}
+
+// Forward and backward in one call: the forward stores its FP32 logits (the
+// accumulators the recompute GEMM would form again, bitwise), an elementwise
+// pass turns them into dlogits with the forward's LSE, then the gradient GEMMs.
+rlk_status launch_lmhead_bwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                             const int64_t* targets, const uint8_t* mask, const float* grad, float* logp, float* lse,
+                             void* dhidden, float* dweight_f32, void* dweight_bf16, void* workspace, uint32_t* status,
+                             cudaStream_t stream) {
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    uint16_t* dlogits = reinterpret_cast<uint16_t*>(ws + lmhead_fwd_workspace(c));
+    float* xlog = reinterpret_cast<float*>(ws + lmhead_fwd_workspace(c) + dlogits_bytes(c));
+    // 1. forward: LSE and logp, the logits kept
+    rlk_status st = forward(c, hidden, H, weight, targets, mask, logp, lse, workspace, xlog, status, stream);
+    if (st != RLK_OK) return st;
+    // 2. dlogits = g * (onehot - exp(x - LSE)) (BF16 [T, V_padded])
+    // one block a row (the hardware balances the tail), at most 2^31 - 1 blocks
+    const int64_t grid = c.T < 0x7FFFFFFF ? c.T : 0x7FFFFFFF;
+    lmhead_dlogits_kernel<<<(unsigned)grid, 256, 0, stream>>>(xlog, lse, grad, targets, mask, c.mask_mode,
+                                                              c.ignore_index, c.T, c.V_real, c.V_padded, dlogits);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("lm_head dlogits launch: ") + cudaGetErrorString(e));
+    // 3. dHidden and dW
+    unsigned long long* tickets = reinterpret_cast<unsigned long long*>(ws);
+    return grad_gemms(c, hidden, H, weight, dlogits, dhidden, dweight_f32, dweight_bf16, tickets + 2 * kMaxGroups,
+                      status, stream);
+}
+
+// The backward alone, from a given LSE: the recompute GEMM's epilogue forms
+// dlogits, then the gradient GEMMs.
+rlk_status launch_lmhead_bwd_given_lse(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                                       const int64_t* targets, const uint8_t* mask, const float* grad,
+                                       const float* lse, void* dhidden, float* dweight_f32, void* dweight_bf16,
+                                       void* workspace, uint32_t* status, cudaStream_t stream) {
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    unsigned long long* tickets = reinterpret_cast<unsigned long long*>(ws);
+    rlk_status st = clear_tickets(tickets, stream);
+    if (st != RLK_OK) return st;
+    uint16_t* dlogits = reinterpret_cast<uint16_t*>(ws + lmhead_fwd_workspace(c));
+    // dlogits = g * (onehot - exp(x - LSE)) from the recomputed logits (BF16 [T, V_padded])
+    LmLaunch L;
+    if ((st = prepare(L, c, hidden, H, weight, targets, mask, status, tickets + kMaxGroups)) != RLK_OK) return st;
+    L.p.lse_in = lse;
+    L.p.grad = grad;
+    L.p.dlogits = dlogits;
+    if ((st = launch_gemm(lmhead_kernel<kEpiGrad>, L.grid, stream, "lm_head recompute GEMM", L.tmH, L.tmW, L.tmWr,
+                          L.p)) != RLK_OK)
+        return st;
+    return grad_gemms(c, hidden, H, weight, dlogits, dhidden, dweight_f32, dweight_bf16, tickets + 2 * kMaxGroups,
+                      status, stream);
 }
 
 }  // namespace rlk
