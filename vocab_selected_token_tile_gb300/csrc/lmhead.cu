@@ -29,9 +29,10 @@
 // runs them, so outputs do not depend on virtual_tp.
 //
 // Backward: dlogits = g (onehot - exp(x - LSE)) in BF16.  In the forward +
-// backward call the forward also stores its FP32 logits (staged through
-// shared memory so that each store writes a 128-byte row segment) and an
-// elementwise pass forms dlogits once the fold has the LSE; the backward from
+// backward call the forward also stores its FP32 logits (each epilogue warp
+// stages 32 rows x 32 columns in shared memory with the 128-byte swizzle and
+// issues one TMA tile store) and an elementwise pass forms dlogits once the
+// fold has the LSE; the backward from
 // a given LSE re-runs the GEMM with an epilogue that writes dlogits.  The
 // logits are the same accumulators either way, so dlogits are bitwise equal.
 // Then one persistent launch runs the two gradient contractions as tcgen05
@@ -60,6 +61,22 @@
 
 namespace rlk {
 namespace {
+
+// TMA tile store from shared memory (bulk group); the writing threads fence
+// the async proxy first.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t c0, int32_t c1, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap), "r"(c0),
+                 "r"(c1), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The source of every committed store has been read (the buffer may be rewritten).
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Every committed store has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 constexpr int kBM = 128;  // token rows per unit (TMEM lanes)
 constexpr int kBN = 256;  // vocabulary rows per chunk (accumulator columns)
@@ -113,8 +130,10 @@ struct Bars {
 // Shared memory of the logits GEMMs past the 1024-byte alignment slack: the
 // operand stages, then the barriers (then, for kEpiPartialsStore, the staging
 // blocks of the logits store).
-constexpr size_t kGemmSmemCore = (size_t)kStages * (kStageA + kStageB) + (sizeof(Bars) + 15) / 16 * 16;
-constexpr int kStoreStage = 32 * 33;  // floats per epilogue warp: 32 rows, pitch 33
+constexpr size_t kGemmSmemCore = ((size_t)kStages * (kStageA + kStageB) + sizeof(Bars) + 1023) / 1024 * 1024;
+// Per epilogue warp: 32 rows x 32 FP32 columns with the 128-byte swizzle (the
+// TMA store's source), or 32 rows at pitch 33 (the 16-column remainder).
+constexpr int kStoreStage = 1280;  // floats (5 KB, a multiple of 1024 bytes)
 
 struct WaitCtl {
     uint32_t* status;
@@ -307,7 +326,8 @@ __device__ __forceinline__ void grad_block(const float (&v)[32], int nv, int64_t
 template <int EPI>
 __global__ void __launch_bounds__(kThreadsLm, 1)
     lmhead_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW,
-                  const __grid_constant__ CUtensorMap tmWr, const __grid_constant__ LmParams p) {
+                  const __grid_constant__ CUtensorMap tmWr, const __grid_constant__ CUtensorMap tmX,
+                  const __grid_constant__ LmParams p) {
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzled operand tiles.
     unsigned char* smem =
@@ -419,6 +439,7 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
         const int r_in = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         float* xst = reinterpret_cast<float*>(smem + kGemmSmemCore) + quarter * kStoreStage;
+        bool store_pending = false;
         int64_t chunk = 0, n = 0;
         for (;;) {
             int64_t u = -1;
@@ -471,17 +492,39 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                     continue;
                 }
                 if (EPI == kEpiPartialsStore) {
-                    // The warp's 32 rows x nv columns through shared memory (row pitch 33:
-                    // conflict-free both ways), then one 128-byte row segment per store.
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (i < nv) xst[lane * 33 + i] = v[i];
-                    __syncwarp();
                     const int64_t row0 = (int64_t)mb * kBM + quarter * 32;
-                    for (int rr = 0; rr < 32; ++rr)
-                        if (row0 + rr < p.T && lane < nv)
-                            p.xlog[(row0 + rr) * p.Vp + col0 + lane] = xst[rr * 33 + lane];
-                    __syncwarp();
+                    // the warp's previous TMA store has read the staging block
+                    if (store_pending) {
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+                    }
+                    if (nv == 32) {
+                        // 32 rows x 128 bytes with the 128-byte swizzle (16-byte chunk j of row r
+                        // at chunk j ^ (r mod 8)), then one TMA tile store; rows past T are clipped
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<float4*>(xst + lane * 32 + ((j ^ (lane & 7)) * 4)) =
+                                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmX, (int32_t)col0, (int32_t)row0, smem_u32(xst));
+                            bulk_commit();
+                        }
+                        store_pending = true;
+                    } else {
+                        // a 16-column remainder: through shared memory at pitch 33 (conflict-free
+                        // both ways), then one 64-byte row segment per store
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i < nv) xst[lane * 33 + i] = v[i];
+                        __syncwarp();
+                        for (int rr = 0; rr < 32; ++rr)
+                            if (row0 + rr < p.T && lane < nv)
+                                p.xlog[(row0 + rr) * p.Vp + col0 + lane] = xst[rr * 33 + lane];
+                        __syncwarp();
+                        store_pending = false;
+                    }
                 }
                 online_block(v, nv, col0, p.Vr, m_run, s_run);
                 if (active && target >= col0 && target < col0 + nv && target < p.Vr) {
@@ -501,6 +544,9 @@ __global__ void __launch_bounds__(kThreadsLm, 1)
                 if (have_xt) p.xt[row] = xt;
             }
         }
+        // the warp's TMA stores complete before the CTA exits
+        if (EPI == kEpiPartialsStore && lane == 0) bulk_wait_all();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -871,6 +917,22 @@ bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows, int
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An FP32 matrix [rows, inner] (row-major, inner * 4 bytes a row, a multiple
+// of 16) in boxes of box_inner x box_rows with the 128-byte swizzle: the
+// stored logits, written by TMA tile stores.
+bool make_map_f32(CUtensorMap* m, const void* base, int64_t inner, int64_t rows, uint32_t box_inner,
+                  uint32_t box_rows) {
+    EncodeTiled enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)inner * 4};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A BF16 matrix whose contiguous dimension `inner` (a multiple of 64) is read
 // in 64-element blocks: dims {64, rows, inner/64}, the blocks 128 bytes apart,
 // so one box {64, box_rows, box_blocks} lands as box_blocks consecutive
@@ -894,6 +956,7 @@ size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 constexpr size_t kGemmSmem = 1024 + kGemmSmemCore;
 // kEpiPartialsStore adds one 32 x 33 FP32 staging block per epilogue warp.
 constexpr size_t kGemmSmemStore = kGemmSmem + 4 * kStoreStage * sizeof(float);
+static_assert(kStoreStage * sizeof(float) % 1024 == 0 && kStoreStage >= 32 * 33, "staging block per warp");
 
 // Chunks of kBN weight rows per tile (the last one may be narrower).
 int64_t chunks_per_tile(const rlk_logp_contract& c) { return (c.V_padded / c.num_tiles + kBN - 1) / kBN; }
@@ -1021,9 +1084,16 @@ rlk_status forward(const rlk_logp_contract& c, const void* hidden, int64_t H, co
     p.partials = reinterpret_cast<float2*>(ws + kTicketBytes);
     p.xt = reinterpret_cast<float*>(ws + kTicketBytes + partial_bytes(c));
     p.xlog = xlog;
-    st = xlog ? launch_gemm_smem(lmhead_kernel<kEpiPartialsStore>, L.grid, kGemmSmemStore, stream, "lm_head GEMM",
-                                 L.tmH, L.tmW, L.tmWr, p)
-              : launch_gemm(lmhead_kernel<kEpiPartials>, L.grid, stream, "lm_head GEMM", L.tmH, L.tmW, L.tmWr, p);
+    if (xlog) {
+        // the FP32 logits [T, V_padded]: 32 x 32 boxes with the 128-byte swizzle
+        CUtensorMap tmX;
+        if (!make_map_f32(&tmX, xlog, c.V_padded, c.T, 32, 32))
+            return fail(RLK_ERR_CUDA, "cuTensorMapEncodeTiled failed for the stored logits");
+        st = launch_gemm_smem(lmhead_kernel<kEpiPartialsStore>, L.grid, kGemmSmemStore, stream, "lm_head GEMM", L.tmH,
+                              L.tmW, L.tmWr, tmX, p);
+    } else {
+        st = launch_gemm(lmhead_kernel<kEpiPartials>, L.grid, stream, "lm_head GEMM", L.tmH, L.tmW, L.tmWr, L.tmH, p);
+    }
     if (st != RLK_OK) return st;
     const int fold_threads = 256;
     const size_t fold_smem = (size_t)(fold_threads / 32) * c.num_tiles * sizeof(float2);
@@ -1130,7 +1200,7 @@ rlk_status launch_lmhead_bwd_given_lse(const rlk_logp_contract& c, const void* h
     L.p.grad = grad;
     L.p.dlogits = dlogits;
     if ((st = launch_gemm(lmhead_kernel<kEpiGrad>, L.grid, stream, "lm_head recompute GEMM", L.tmH, L.tmW, L.tmWr,
-                          L.p)) != RLK_OK)
+                          L.tmH, L.p)) != RLK_OK)
         return st;
     return grad_gemms(c, hidden, H, weight, dlogits, dhidden, dweight_f32, dweight_bf16, tickets + 2 * kMaxGroups,
                       status, stream);
