@@ -257,8 +257,8 @@ rlk_status rlk_logp_bwd(const rlk_logp_contract* contract, const void* logits_bf
                         float* logp_out, float* lse_out, void* workspace, rlk_stream_t stream);
 
 /*
- * Bytes of device workspace rlk_logp_fused_lmhead and rlk_logp_fused_lmhead_bwd
- * need for hidden size H: the status word, 256 bytes of work tickets, FP32
+ * Bytes of device workspace every fused lm_head call (rlk_logp_fused_lmhead
+ * and the _bwd, _keep and _bwd_kept forms) needs for hidden size H: the status word, 256 bytes of work tickets, FP32
  * partials [T, num_tiles * ceil(V_padded / num_tiles / 256), 2] (one per
  * 256-row weight chunk), target logits [T], and for the backward the BF16
  * dlogits [T, V_padded] and the forward's FP32 logits [T, V_padded] (about
@@ -319,6 +319,40 @@ rlk_status rlk_logp_fused_lmhead_bwd(const rlk_logp_contract* contract, const vo
                                      const void* weight_bf16, const int64_t* targets, const uint8_t* active_mask,
                                      const float* lse_in, const float* grad_logp, void* dhidden_bf16,
                                      float* dweight_f32, void* dweight_bf16, void* workspace, rlk_stream_t stream);
+
+/*
+ * The fused lm_head forward that also keeps its FP32 logits for a later
+ * backward, for an autograd forward that trades T * V_padded * 4 bytes, held
+ * until the backward, for the backward's recompute GEMM (the split form of
+ * what rlk_logp_fused_lmhead with grad_logp does inside one call).
+ *   logits_f32  [T, V_padded] FP32 out, 16-byte aligned, written in full:
+ *               hidden @ weight^T as the GEMM accumulated it (columns >= V_real
+ *               hold products with the padding rows and are never used).
+ *   the other arguments and outputs as for rlk_logp_fused_lmhead without
+ *   grad_logp; logp and lse are bitwise those of that call.
+ */
+rlk_status rlk_logp_fused_lmhead_keep(const rlk_logp_contract* contract, const void* hidden_bf16, int64_t H,
+                                      const void* weight_bf16, const int64_t* targets, const uint8_t* active_mask,
+                                      float* logp, float* lse, float* logits_f32, void* workspace,
+                                      rlk_stream_t stream);
+
+/*
+ * The fused lm_head backward from the logits rlk_logp_fused_lmhead_keep kept
+ * and its LSE: an HBM-bound pass writes dlogits = g (onehot - exp(x - lse_in))
+ * in BF16, then the dHidden and dW GEMMs run.  The outputs are bitwise those
+ * of rlk_logp_fused_lmhead_bwd with the same lse_in, and of
+ * rlk_logp_fused_lmhead with grad_logp.
+ *   logits_f32  [T, V_padded] FP32 in, 16-byte aligned, as the forward wrote
+ *               it; not modified.
+ *   the other arguments and outputs as for rlk_logp_fused_lmhead_bwd; no
+ *   output may overlap an input.
+ * Device status (validate == 1): as for rlk_logp_fused_lmhead_bwd.
+ */
+rlk_status rlk_logp_fused_lmhead_bwd_kept(const rlk_logp_contract* contract, const void* hidden_bf16, int64_t H,
+                                          const void* weight_bf16, const int64_t* targets,
+                                          const uint8_t* active_mask, const float* lse_in, const float* logits_f32,
+                                          const float* grad_logp, void* dhidden_bf16, float* dweight_f32,
+                                          void* dweight_bf16, void* workspace, rlk_stream_t stream);
 
 /*
  * Vocabulary-parallel tensor parallelism across GPUs (PR #289 "[WS2][PR4]

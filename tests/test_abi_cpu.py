@@ -179,6 +179,25 @@ def test_new_entry_points_fail_closed_on_the_host(built):
                                          None, 0x9000, None) == rlk.RLK_ERR_INVALID_ARG  # no dweight output
     assert rlk.rlk_logp_fused_lmhead(cl, 0x1000, 128, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000,
                                      0x9008, None, 0xA000, None) == rlk.RLK_ERR_MISALIGNED  # FP32 dweight
+    # the lm_head forward keeping its logits, and the backward from them
+    assert rlk.rlk_logp_fused_lmhead_keep(ok_contract(T=0), None, 128, None, None, None, None, None, None, None,
+                                          None) == rlk.RLK_OK
+    assert rlk.rlk_logp_fused_lmhead_keep(cl, 0x1000, 128, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, None, 0xA000,
+                                          None) == rlk.RLK_ERR_INVALID_ARG  # no logits_f32
+    assert rlk.rlk_logp_fused_lmhead_keep(cl, 0x1000, 128, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7008, 0xA000,
+                                          None) == rlk.RLK_ERR_MISALIGNED
+    assert rlk.rlk_logp_fused_lmhead_keep(cl, 0x1000, 192, 0x2000, 0x3000, None, 0x5000, 0x6000, 0x7000, 0xA000,
+                                          None) == rlk.RLK_ERR_INVALID_ARG  # explicit mask mode, no mask
+    assert rlk.rlk_logp_fused_lmhead_bwd_kept(ok_contract(T=0), None, 128, None, None, None, None, None, None, None,
+                                              None, None, None, None) == rlk.RLK_OK
+    assert rlk.rlk_logp_fused_lmhead_bwd_kept(cl, 0x1000, 128, 0x2000, 0x3000, 0x4000, 0x5000, None, 0x6000, 0x7000,
+                                              None, 0x9000, 0xA000, None) == rlk.RLK_ERR_INVALID_ARG  # no logits_f32
+    assert rlk.rlk_logp_fused_lmhead_bwd_kept(cl, 0x1000, 128, 0x2000, 0x3000, 0x4000, 0x5000, 0x5008, 0x6000,
+                                              0x7000, None, 0x9000, 0xA000, None) == rlk.RLK_ERR_MISALIGNED
+    assert rlk.rlk_logp_fused_lmhead_bwd_kept(cl, 0x1000, 128, 0x2000, 0x3000, 0x4000, None, 0x5000, 0x6000, 0x7000,
+                                              None, 0x9000, 0xA000, None) == rlk.RLK_ERR_INVALID_ARG  # no lse_in
+    assert rlk.rlk_logp_fused_lmhead_bwd_kept(cl, 0x1000, 128, 0x2000, 0x3000, 0x4000, 0x5000, 0x5800, 0x6000,
+                                              0x7000, None, None, 0xA000, None) == rlk.RLK_ERR_INVALID_ARG  # no dW
 
 
 def test_dlogits_may_alias_logits_only_exactly(built):

@@ -91,3 +91,25 @@ def test_lmhead_autograd_matches_the_c_entry_points_and_the_oracle():
     got_dw = W.grad.float().cpu().numpy().astype(np.float64)
     assert np.all(np.abs(got_dw[:v_real] - dw_ref[:v_real]) <= 2.0 ** -8 * (np.abs(dw_ref[:v_real]) + sc_dw) + 1e-30)
     assert np.all(got_dw[v_real:] == 0.0)
+
+
+def test_lmhead_autograd_keep_logits_is_bitwise_the_recompute_path():
+    """keep_logits=True (the forward keeps its FP32 logits, the backward forms dlogits from them) gives
+    bitwise the logp, LSE and gradients of keep_logits=False (the backward re-runs the GEMM)."""
+    from vocab_selected_token_tile_gb300.autograd import lmhead_logprob
+    T, H, v_real, v_padded, nt = 259, 192, 1000, 1024, 4
+    hb = synth.normal_bf16_host(0, T, H, 43, synth.STREAM_HIDDEN, 1.0)
+    wb = synth.normal_bf16_host(0, v_padded, H, 43, synth.STREAM_WEIGHT, 0.3)
+    tgt = synth.targets(T, v_real, seed=43, ignore_frac=0.25)
+    w = torch.from_numpy(np.random.default_rng(43).standard_normal(T).astype(np.float32)).cuda()
+    dt = torch.from_numpy(tgt).cuda()
+    out = []
+    for keep in (False, True):
+        h = torch.from_numpy(hb.view(np.int16)).cuda().view(torch.bfloat16).requires_grad_(True)
+        W = torch.from_numpy(wb.view(np.int16)).cuda().view(torch.bfloat16).requires_grad_(True)
+        logp, lse = lmhead_logprob(h, W, dt, None, v_real=v_real, num_tiles=nt, keep_logits=keep)
+        (logp * w).sum().backward()
+        torch.cuda.synchronize()
+        out.append((logp.detach(), lse, h.grad, W.grad))
+    for a, b in zip(*out):
+        assert torch.equal(a, b)

@@ -324,3 +324,52 @@ def test_lmhead_degenerate_sizes(case):
         assert np.all(within(dwb[:v_real], ref_dw, sc_dw)) and np.all(dwb[v_real:] == 0)
         outs.add((logp.cpu().numpy().tobytes(), lse.cpu().numpy().tobytes(), dhb.tobytes(), dwb.tobytes()))
     assert len(outs) == 1
+
+
+@pytest.mark.parametrize("case", [CASES[1], CASES[4], (129, 64, 300, 320, 5)], ids=lambda c: "T%d_H%d_V%d_P%d_NT%d" % c)
+def test_lmhead_kept_logits_forward_and_backward(case):
+    """rlk_logp_fused_lmhead_keep: logp and LSE bitwise the plain forward's; the kept FP32 logits within
+    FP32 accumulation of the FP64 oracle's on the real columns, bitwise the same at every virtual TP.
+    rlk_logp_fused_lmhead_bwd_kept: dHidden and dW bitwise those of the backward from the LSE and of
+    the fused call, the kept logits untouched; an active target outside [0, V_real) and a non-finite
+    LSE are reported."""
+    T, H, v_real, v_padded, nt = case
+    hb, wb = make(T, H, v_real, v_padded, seed=5 * T + H)
+    tgt = synth.targets(T, v_real, seed=T + 3)
+    mask = (np.arange(T) % 6 != 2).astype(np.uint8)
+    g = np.where(mask != 0, np.random.default_rng(T).standard_normal(T), 0.0).astype(np.float32)
+    dh_, dw_, dt, dm, dg = dev(hb), dev(wb), torch.from_numpy(tgt).cuda(), torch.from_numpy(mask).cuda(), \
+        torch.from_numpy(g).cuda()
+    c = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=nt, virtual_tp=1, validate=1)
+    logp, lse = rlk.logp_fused_lmhead(c, dh_, dw_, dt, dm)
+    logp_k, lse_k, logits = rlk.logp_fused_lmhead_keep(c, dh_, dw_, dt, dm)
+    torch.cuda.synchronize()
+    assert torch.equal(logp, logp_k) and torch.equal(lse, lse_k)
+    x = logits.cpu().numpy().astype(np.float64)[:, :v_real]
+    ref = oracle.lmhead_logits(hb, wb, v_real)
+    scale = np.abs(oracle.bf16_bits_to_f64(hb)) @ np.abs(oracle.bf16_bits_to_f64(wb[:v_real])).T
+    # a tensor-core FP32 accumulation: a few units of 2^-24 per addition at most (2^-22 taken)
+    assert np.all(np.abs(x - ref) <= H * 2.0 ** -22 * scale + 1e-30), "kept logits outside FP32 accumulation"
+    for vtp in (v for v in (2, 4, 8) if nt % v == 0):
+        cv = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=nt, virtual_tp=vtp, validate=1)
+        _, _, lv = rlk.logp_fused_lmhead_keep(cv, dh_, dw_, dt, dm)
+        torch.cuda.synchronize()
+        assert torch.equal(lv[:, :v_real], logits[:, :v_real]), vtp
+    before = logits.clone()
+    dh1, dw1 = rlk.logp_fused_lmhead_bwd(c, dh_, dw_, dt, dm, lse, dg, dweight_dtype="both")
+    dh2, dw2 = rlk.logp_fused_lmhead_bwd_kept(c, dh_, dw_, dt, dm, lse_k, logits, dg, dweight_dtype="both")
+    _, _, dh3, dw3 = rlk.logp_fused_lmhead(c, dh_, dw_, dt, dm, grad=dg, dweight_dtype="both")
+    torch.cuda.synchronize()
+    assert torch.equal(logits.view(torch.int32), before.view(torch.int32))  # bits: padded columns may hold NaN
+    for a, b in ((dh1, dh2), (dw1[0], dw2[0]), (dw1[1], dw2[1]), (dh3, dh2), (dw3[0], dw2[0]), (dw3[1], dw2[1])):
+        assert torch.equal(a, b)
+    bad = tgt.copy()
+    bad[int(np.nonzero(mask)[0][0])] = v_real + 1
+    with pytest.raises(rlk.RlkError) as ei:
+        rlk.logp_fused_lmhead_bwd_kept(c, dh_, dw_, torch.from_numpy(bad).cuda(), dm, lse_k, logits, dg)
+    assert ei.value.status == rlk.RLK_ERR_TARGET_RANGE
+    l2 = lse_k.clone()
+    l2[int(np.nonzero(mask)[0][1])] = float("nan")
+    with pytest.raises(rlk.RlkError) as ei:
+        rlk.logp_fused_lmhead_bwd_kept(c, dh_, dw_, dt, dm, l2, logits, dg)
+    assert ei.value.status == rlk.RLK_ERR_NONFINITE_LSE

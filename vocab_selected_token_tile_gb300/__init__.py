@@ -39,6 +39,8 @@ EXPORTED = (
     "rlk_logp_lmhead_workspace_size",
     "rlk_logp_fused_lmhead",
     "rlk_logp_fused_lmhead_bwd",
+    "rlk_logp_fused_lmhead_keep",
+    "rlk_logp_fused_lmhead_bwd_kept",
     "rlk_logp_check_shard_contract",
     "rlk_logp_shard_workspace_size",
     "rlk_logp_shard_fwd",
@@ -109,6 +111,11 @@ def library():
         lib.rlk_logp_fused_lmhead.restype = i
         lib.rlk_logp_fused_lmhead_bwd.argtypes = [P, vp, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.rlk_logp_fused_lmhead_bwd.restype = i
+        lib.rlk_logp_fused_lmhead_keep.argtypes = [P, vp, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.rlk_logp_fused_lmhead_keep.restype = i
+        lib.rlk_logp_fused_lmhead_bwd_kept.argtypes = [P, vp, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                       vp, vp]
+        lib.rlk_logp_fused_lmhead_bwd_kept.restype = i
         lib.rlk_logp_fwd_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp]
         lib.rlk_logp_fwd_noalloc.restype = i
         lib.rlk_logp_fwd_entropy.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -180,6 +187,19 @@ def rlk_logp_fused_lmhead_bwd(contract, hidden, H, weight, targets, active_mask,
     return library().rlk_logp_fused_lmhead_bwd(ctypes.byref(contract), hidden, H, weight, targets, active_mask,
                                                lse_in, grad_logp, dhidden, dweight_f32, dweight_bf16, workspace,
                                                stream)
+
+
+def rlk_logp_fused_lmhead_keep(contract, hidden, H, weight, targets, active_mask, logp, lse, logits_f32, workspace,
+                               stream):
+    return library().rlk_logp_fused_lmhead_keep(ctypes.byref(contract), hidden, H, weight, targets, active_mask,
+                                                logp, lse, logits_f32, workspace, stream)
+
+
+def rlk_logp_fused_lmhead_bwd_kept(contract, hidden, H, weight, targets, active_mask, lse_in, logits_f32, grad_logp,
+                                   dhidden, dweight_f32, dweight_bf16, workspace, stream):
+    return library().rlk_logp_fused_lmhead_bwd_kept(ctypes.byref(contract), hidden, H, weight, targets, active_mask,
+                                                    lse_in, logits_f32, grad_logp, dhidden, dweight_f32,
+                                                    dweight_bf16, workspace, stream)
 
 
 def rlk_logp_fwd_entropy(contract, logits, targets, active_mask, logp, lse, entropy, workspace, stream):
@@ -500,6 +520,45 @@ def logp_fused_lmhead_bwd(contract, hidden, weight, targets, mask, lse, grad, st
     ws = workspace if workspace is not None else torch.empty(n, dtype=torch.uint8, device=dev)
     check(rlk_logp_fused_lmhead_bwd(contract, _ptr(hidden), H, _ptr(weight), _ptr(targets), _ptr(mask), _ptr(lse),
                                     _ptr(grad), _ptr(dh), _ptr(dwf), _ptr(dwb), _ptr(ws), _stream(stream)))
+    return dh, {"bf16": dwb, "f32": dwf, "both": (dwf, dwb)}[dweight_dtype]
+
+
+def logp_fused_lmhead_keep(contract, hidden, weight, targets, mask=None, stream=None, workspace=None):
+    """(logp, lse, logits): the fused lm_head forward that also keeps its FP32 logits [T, V_padded] for
+    logp_fused_lmhead_bwd_kept (T * V_padded * 4 bytes)."""
+    import torch
+    dev = hidden.device
+    T, H = hidden.shape
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    logits = torch.empty((T, weight.shape[0]), dtype=torch.float32, device=dev)
+    n = rlk_logp_lmhead_workspace_size(contract, H)
+    if n == 0:
+        check(rlk_logp_check_contract(contract) or RLK_ERR_UNSUPPORTED)
+    ws = workspace if workspace is not None else torch.empty(n, dtype=torch.uint8, device=dev)
+    check(rlk_logp_fused_lmhead_keep(contract, _ptr(hidden), H, _ptr(weight), _ptr(targets), _ptr(mask), _ptr(logp),
+                                     _ptr(lse), _ptr(logits), _ptr(ws), _stream(stream)))
+    return logp, lse, logits
+
+
+def logp_fused_lmhead_bwd_kept(contract, hidden, weight, targets, mask, lse, logits, grad, stream=None, workspace=None,
+                               dweight_dtype="bf16"):
+    """(dhidden, dweight) from the logits and LSE of logp_fused_lmhead_keep; bitwise logp_fused_lmhead_bwd's."""
+    import torch
+    dev = hidden.device
+    T, H = hidden.shape
+    if dweight_dtype not in ("bf16", "f32", "both"):
+        raise ValueError("dweight_dtype must be bf16, f32 or both")
+    dh = torch.empty_like(hidden)
+    dwf = torch.empty(weight.shape, dtype=torch.float32, device=dev) if dweight_dtype in ("f32", "both") else None
+    dwb = torch.empty_like(weight) if dweight_dtype in ("bf16", "both") else None
+    n = rlk_logp_lmhead_workspace_size(contract, H)
+    if n == 0:
+        check(rlk_logp_check_contract(contract) or RLK_ERR_UNSUPPORTED)
+    ws = workspace if workspace is not None else torch.empty(n, dtype=torch.uint8, device=dev)
+    check(rlk_logp_fused_lmhead_bwd_kept(contract, _ptr(hidden), H, _ptr(weight), _ptr(targets), _ptr(mask),
+                                         _ptr(lse), _ptr(logits), _ptr(grad), _ptr(dh), _ptr(dwf), _ptr(dwb), _ptr(ws),
+                                         _stream(stream)))
     return dh, {"bf16": dwb, "f32": dwf, "both": (dwf, dwb)}[dweight_dtype]
 
 

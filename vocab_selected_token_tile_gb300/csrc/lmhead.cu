@@ -618,13 +618,20 @@ __global__ void __launch_bounds__(256) lmhead_dlogits_kernel(const float* xlog, 
                                                              const float* grad, const int64_t* targets,
                                                              const uint8_t* mask, int mask_mode,
                                                              int64_t ignore_index, int64_t T, int64_t Vr,
-                                                             int64_t Vp, uint16_t* dlogits) {
+                                                             int64_t Vp, uint16_t* dlogits, uint32_t* status) {
     const int64_t groups = Vp / 8;
     for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
         const int64_t t = targets[row];
         const bool active = (mask_mode == RLK_MASK_EXPLICIT) ? (mask[row] != 0) : (t != ignore_index);
         const float g = grad[row];
-        const float nlL = -__fmul_rn(lse[row], kLog2e);
+        const float l = lse[row];
+        const float nlL = -__fmul_rn(l, kLog2e);
+        // the device conditions of a backward given the LSE, once per row (the target is
+        // only compared with column indices, never used as one)
+        if (threadIdx.x == 0 && active) {
+            if (t < 0 || t >= Vr) atomicOr(status, kStatusTargetRange);
+            if (!isfinite(l)) atomicOr(status, kStatusNonFinite);
+        }
         const float4* xr = reinterpret_cast<const float4*>(xlog + row * Vp);
         uint4* dr = reinterpret_cast<uint4*>(dlogits + row * Vp);
         for (int64_t q = threadIdx.x; q < groups; q += blockDim.x) {
@@ -1148,6 +1155,27 @@ rlk_status grad_gemms(const rlk_logp_contract& c, const void* hidden, int64_t H,
     return launch_gemm(lmhead_grad_kernel, grid, stream, "lm_head gradient GEMM", tmA0, tmB0, tmA1, tmB1, g);
 }
 
+// dlogits = g * (onehot - exp(x - LSE)) from FP32 logits (BF16 [T, V_padded]
+// in the workspace), then dHidden and dW.  The gradient GEMM's ticket must be
+// zero at entry.
+rlk_status backward_from_logits(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                                const int64_t* targets, const uint8_t* mask, const float* grad, const float* lse,
+                                const float* xlog, void* dhidden, float* dweight_f32, void* dweight_bf16,
+                                void* workspace, uint32_t* status, cudaStream_t stream) {
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    uint16_t* dlogits = reinterpret_cast<uint16_t*>(ws + lmhead_fwd_workspace(c));
+    // one block a row (the hardware balances the tail), at most 2^31 - 1 blocks
+    const int64_t grid = c.T < 0x7FFFFFFF ? c.T : 0x7FFFFFFF;
+    lmhead_dlogits_kernel<<<(unsigned)grid, 256, 0, stream>>>(xlog, lse, grad, targets, mask, c.mask_mode,
+                                                              c.ignore_index, c.T, c.V_real, c.V_padded, dlogits,
+                                                              status);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("lm_head dlogits launch: ") + cudaGetErrorString(e));
+    unsigned long long* tickets = reinterpret_cast<unsigned long long*>(ws);
+    return grad_gemms(c, hidden, H, weight, dlogits, dhidden, dweight_f32, dweight_bf16, tickets + 2 * kMaxGroups,
+                      status, stream);
+}
+
 }  // namespace
 
 rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
@@ -1156,30 +1184,37 @@ rlk_status launch_lmhead_fwd(const rlk_logp_contract& c, const void* hidden, int
     return forward(c, hidden, H, weight, targets, mask, logp, lse, workspace, nullptr, status, stream);
 }
 
-// Forward and backward in one call: the forward stores its FP32 logits (the
-// accumulators the recompute GEMM would form again, bitwise), an elementwise
-// pass turns them into dlogits with the forward's LSE, then the gradient GEMMs.
+// Forward and backward in one call: the forward stores its FP32 logits in the
+// workspace (the accumulators the recompute GEMM would form again, bitwise),
+// an elementwise pass turns them into dlogits with the forward's LSE, then the
+// gradient GEMMs.
 rlk_status launch_lmhead_bwd(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
                              const int64_t* targets, const uint8_t* mask, const float* grad, float* logp, float* lse,
                              void* dhidden, float* dweight_f32, void* dweight_bf16, void* workspace, uint32_t* status,
                              cudaStream_t stream) {
     unsigned char* ws = static_cast<unsigned char*>(workspace);
-    uint16_t* dlogits = reinterpret_cast<uint16_t*>(ws + lmhead_fwd_workspace(c));
     float* xlog = reinterpret_cast<float*>(ws + lmhead_fwd_workspace(c) + dlogits_bytes(c));
-    // 1. forward: LSE and logp, the logits kept
+    // the forward clears every ticket, the gradient GEMM's among them
     rlk_status st = forward(c, hidden, H, weight, targets, mask, logp, lse, workspace, xlog, status, stream);
     if (st != RLK_OK) return st;
-    // 2. dlogits = g * (onehot - exp(x - LSE)) (BF16 [T, V_padded])
-    // one block a row (the hardware balances the tail), at most 2^31 - 1 blocks
-    const int64_t grid = c.T < 0x7FFFFFFF ? c.T : 0x7FFFFFFF;
-    lmhead_dlogits_kernel<<<(unsigned)grid, 256, 0, stream>>>(xlog, lse, grad, targets, mask, c.mask_mode,
-                                                              c.ignore_index, c.T, c.V_real, c.V_padded, dlogits);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(RLK_ERR_CUDA, std::string("lm_head dlogits launch: ") + cudaGetErrorString(e));
-    // 3. dHidden and dW
-    unsigned long long* tickets = reinterpret_cast<unsigned long long*>(ws);
-    return grad_gemms(c, hidden, H, weight, dlogits, dhidden, dweight_f32, dweight_bf16, tickets + 2 * kMaxGroups,
-                      status, stream);
+    return backward_from_logits(c, hidden, H, weight, targets, mask, grad, lse, xlog, dhidden, dweight_f32,
+                                dweight_bf16, workspace, status, stream);
+}
+
+rlk_status launch_lmhead_fwd_keep(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                                  const int64_t* targets, const uint8_t* mask, float* logp, float* lse,
+                                  float* logits_f32, void* workspace, uint32_t* status, cudaStream_t stream) {
+    return forward(c, hidden, H, weight, targets, mask, logp, lse, workspace, logits_f32, status, stream);
+}
+
+rlk_status launch_lmhead_bwd_kept(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                                  const int64_t* targets, const uint8_t* mask, const float* grad, const float* lse,
+                                  const float* logits_f32, void* dhidden, float* dweight_f32, void* dweight_bf16,
+                                  void* workspace, uint32_t* status, cudaStream_t stream) {
+    rlk_status st = clear_tickets(workspace, stream);
+    if (st != RLK_OK) return st;
+    return backward_from_logits(c, hidden, H, weight, targets, mask, grad, lse, logits_f32, dhidden, dweight_f32,
+                                dweight_bf16, workspace, status, stream);
 }
 
 // The backward alone, from a given LSE: the recompute GEMM's epilogue forms

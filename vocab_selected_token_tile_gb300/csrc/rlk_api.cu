@@ -490,6 +490,82 @@ RLK_EXPORT rlk_status rlk_logp_fused_lmhead_bwd(const rlk_logp_contract* c, cons
     return c->validate ? read_status(workspace, st) : RLK_OK;
 }
 
+RLK_EXPORT rlk_status rlk_logp_fused_lmhead_keep(const rlk_logp_contract* c, const void* hidden_bf16, int64_t H,
+                                                 const void* weight_bf16, const int64_t* targets,
+                                                 const uint8_t* active_mask, float* logp, float* lse,
+                                                 float* logits_f32, void* workspace, rlk_stream_t stream) {
+    rlk_status s = check_contract(c);
+    if (s != RLK_OK) return s;
+    if ((s = lmhead_check(*c, H)) != RLK_OK) return s;
+    if (c->T == 0) return RLK_OK;
+    if (!hidden_bf16 || !weight_bf16) return fail(RLK_ERR_INVALID_ARG, "hidden and weight are required");
+    if (!aligned16(hidden_bf16) || !aligned16(weight_bf16))
+        return fail(RLK_ERR_MISALIGNED, "hidden and weight must be 16-byte aligned");
+    if (!targets) return fail(RLK_ERR_INVALID_ARG, "targets is NULL");
+    if (c->mask_mode == RLK_MASK_EXPLICIT && !active_mask)
+        return fail(RLK_ERR_INVALID_ARG, "explicit mask mode needs active_mask");
+    if (c->mask_mode == RLK_MASK_IGNORE_INDEX && active_mask)
+        return fail(RLK_ERR_INVALID_ARG, "ignore_index mode takes no active_mask (pass NULL)");
+    if (!logp || !lse) return fail(RLK_ERR_INVALID_ARG, "logp and lse outputs are required");
+    if (!logits_f32) return fail(RLK_ERR_INVALID_ARG, "logits_f32 is NULL");
+    if (!aligned16(logits_f32)) return fail(RLK_ERR_MISALIGNED, "logits_f32 must be 16-byte aligned");
+    if (!workspace || !aligned16(workspace)) return fail(RLK_ERR_INVALID_ARG, "workspace must be non-NULL and 16-byte aligned");
+    if ((s = select_device(hidden_bf16)) != RLK_OK) return s;
+    if ((s = check_device_ptrs({{weight_bf16, "weight"}, {targets, "targets"}, {active_mask, "active_mask"},
+                                {logp, "logp"}, {lse, "lse"}, {logits_f32, "logits_f32"},
+                                {workspace, "workspace"}})) != RLK_OK)
+        return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = begin(workspace, st)) != RLK_OK) return s;
+    if ((s = launch_lmhead_fwd_keep(*c, hidden_bf16, H, weight_bf16, targets, active_mask, logp, lse, logits_f32,
+                                    static_cast<unsigned char*>(workspace) + kWorkspaceBytes,
+                                    static_cast<uint32_t*>(workspace), st)) != RLK_OK)
+        return s;
+    return c->validate ? read_status(workspace, st) : RLK_OK;
+}
+
+RLK_EXPORT rlk_status rlk_logp_fused_lmhead_bwd_kept(const rlk_logp_contract* c, const void* hidden_bf16, int64_t H,
+                                                     const void* weight_bf16, const int64_t* targets,
+                                                     const uint8_t* active_mask, const float* lse_in,
+                                                     const float* logits_f32, const float* grad_logp,
+                                                     void* dhidden_bf16, float* dweight_f32, void* dweight_bf16,
+                                                     void* workspace, rlk_stream_t stream) {
+    rlk_status s = check_contract(c);
+    if (s != RLK_OK) return s;
+    if ((s = lmhead_check(*c, H)) != RLK_OK) return s;
+    if (c->T == 0) return RLK_OK;
+    if (!hidden_bf16 || !weight_bf16) return fail(RLK_ERR_INVALID_ARG, "hidden and weight are required");
+    if (!aligned16(hidden_bf16) || !aligned16(weight_bf16))
+        return fail(RLK_ERR_MISALIGNED, "hidden and weight must be 16-byte aligned");
+    if (!targets) return fail(RLK_ERR_INVALID_ARG, "targets is NULL");
+    if (c->mask_mode == RLK_MASK_EXPLICIT && !active_mask)
+        return fail(RLK_ERR_INVALID_ARG, "explicit mask mode needs active_mask");
+    if (c->mask_mode == RLK_MASK_IGNORE_INDEX && active_mask)
+        return fail(RLK_ERR_INVALID_ARG, "ignore_index mode takes no active_mask (pass NULL)");
+    if (!lse_in || !grad_logp) return fail(RLK_ERR_INVALID_ARG, "lse_in and grad_logp are required");
+    if (!logits_f32) return fail(RLK_ERR_INVALID_ARG, "logits_f32 is NULL");
+    if (!aligned16(logits_f32)) return fail(RLK_ERR_MISALIGNED, "logits_f32 must be 16-byte aligned");
+    if (!dhidden_bf16 || (!dweight_f32 && !dweight_bf16))
+        return fail(RLK_ERR_INVALID_ARG, "dhidden and at least one dweight output are required");
+    if (!aligned16(dhidden_bf16) || !aligned16(dweight_f32) || !aligned16(dweight_bf16))
+        return fail(RLK_ERR_MISALIGNED, "dhidden and dweight must be 16-byte aligned");
+    if (!workspace || !aligned16(workspace)) return fail(RLK_ERR_INVALID_ARG, "workspace must be non-NULL and 16-byte aligned");
+    if ((s = select_device(hidden_bf16)) != RLK_OK) return s;
+    if ((s = check_device_ptrs({{weight_bf16, "weight"}, {targets, "targets"}, {active_mask, "active_mask"},
+                                {lse_in, "lse_in"}, {logits_f32, "logits_f32"}, {grad_logp, "grad_logp"},
+                                {dhidden_bf16, "dhidden"}, {dweight_f32, "dweight_f32"},
+                                {dweight_bf16, "dweight_bf16"}, {workspace, "workspace"}})) != RLK_OK)
+        return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = begin(workspace, st)) != RLK_OK) return s;
+    if ((s = launch_lmhead_bwd_kept(*c, hidden_bf16, H, weight_bf16, targets, active_mask, grad_logp, lse_in,
+                                    logits_f32, dhidden_bf16, dweight_f32, dweight_bf16,
+                                    static_cast<unsigned char*>(workspace) + kWorkspaceBytes,
+                                    static_cast<uint32_t*>(workspace), st)) != RLK_OK)
+        return s;
+    return c->validate ? read_status(workspace, st) : RLK_OK;
+}
+
 // ---------------------------------------------------------------- vocabulary-parallel shards
 
 namespace rlk {

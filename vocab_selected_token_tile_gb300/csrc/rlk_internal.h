@@ -83,6 +83,15 @@ rlk_status launch_lmhead_bwd(const rlk_logp_contract& c, const void* hidden, int
                              const int64_t* targets, const uint8_t* mask, const float* grad, float* logp, float* lse,
                              void* dhidden, float* dweight_f32, void* dweight_bf16, void* workspace, uint32_t* status,
                              cudaStream_t stream);
+// The forward that also writes its FP32 logits [T, V_padded] to logits_f32.
+rlk_status launch_lmhead_fwd_keep(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                                  const int64_t* targets, const uint8_t* mask, float* logp, float* lse,
+                                  float* logits_f32, void* workspace, uint32_t* status, cudaStream_t stream);
+// The backward from kept FP32 logits and the LSE: dlogits pass, then dHidden and dW.
+rlk_status launch_lmhead_bwd_kept(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
+                                  const int64_t* targets, const uint8_t* mask, const float* grad, const float* lse,
+                                  const float* logits_f32, void* dhidden, float* dweight_f32, void* dweight_bf16,
+                                  void* workspace, uint32_t* status, cudaStream_t stream);
 // The backward alone, from a given LSE: recompute GEMM (dlogits), then dHidden and dW.
 rlk_status launch_lmhead_bwd_given_lse(const rlk_logp_contract& c, const void* hidden, int64_t H, const void* weight,
                                        const int64_t* targets, const uint8_t* mask, const float* grad,
