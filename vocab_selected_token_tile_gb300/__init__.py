@@ -287,6 +287,95 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+_BF16 = ("bfloat16", "int16", "uint16")  # BF16 logits, or their bits as 16-bit integers
+_I64 = ("int64",)
+_U8 = ("uint8", "bool")
+_F32 = ("float32",)
+
+
+def _need(t, name, nbytes, kinds, optional=False):
+    """Fails before any launch when ``t`` cannot be what the call reads or writes through its pointer:
+    a CUDA tensor of one of ``kinds`` whose storage holds ``nbytes`` from its first element on (so no
+    access leaves it) and, when it is contiguous, whose own elements cover them (a short view of a
+    larger buffer is a mistake too).  The C entry points check pointers, alignment and the device;
+    only the caller knows the sizes."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    kind = str(t.dtype).replace("torch.", "")
+    if kind not in kinds:
+        raise TypeError(f"{name} must be {' or '.join(kinds)}, not {kind}")
+    have = t.untyped_storage().nbytes() - t.storage_offset() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{name} holds {have} bytes from its first element; the call touches {nbytes}")
+    if t.is_contiguous() and t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name} has {t.numel()} elements; the call touches {nbytes} bytes")
+
+
+def _need_rows(t, name, T, stride, width, kinds):
+    """A [T, stride] row buffer of 16-bit elements of which the call touches ``width`` a row; a 2-D
+    view must also have those rows and that row stride (a shard read in place from the whole row
+    buffer is such a view)."""
+    _need(t, name, _rows(T, stride, width, 2), kinds)
+    if t.dim() == 2 and T > 0 and (t.shape[0] < T or t.shape[1] < width or t.stride(1) != 1 or
+                                   (T > 1 and t.stride(0) != stride)):
+        raise ValueError(f"{name} is a {list(t.shape)} view with strides {list(t.stride())}; the call reads {T} "
+                         f"rows of {width} elements, {stride} apart")
+
+
+def _rows(T, stride, width, esize):
+    """Bytes from the first element of a [T, stride] row-major buffer to the end of row T-1's width."""
+    return 0 if T <= 0 else ((T - 1) * stride + width) * esize
+
+
+def _dlogits_out(contract, logits, dlogits, stride=None, width=None):
+    """The dlogits buffer: the given one, checked, or a new [T, row stride] one like the logits."""
+    import torch
+    stride = stride or contract.row_stride or contract.V_padded
+    width = width or contract.V_padded
+    if dlogits is None:
+        return torch.empty((contract.T, stride), dtype=logits.dtype, device=logits.device)
+    _need_rows(dlogits, "dlogits", contract.T, stride, width, _BF16)
+    return dlogits
+
+
+def _lmhead_operands(contract, hidden, weight):
+    """hidden [T, H] and weight [V_padded, H], BF16, contiguous; returns H."""
+    if hidden.dim() != 2 or hidden.shape[0] != contract.T:
+        raise ValueError(f"hidden must be [T = {contract.T}, H], not {list(hidden.shape)}")
+    H = hidden.shape[1]
+    if weight.dim() != 2 or weight.shape[0] != contract.V_padded or weight.shape[1] != H:
+        raise ValueError(f"weight must be [V_padded = {contract.V_padded}, H = {H}], not {list(weight.shape)}")
+    for name, t in (("hidden", hidden), ("weight", weight)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        _need(t, name, 2 * t.numel(), _BF16)
+    return H
+
+
+def _lmhead_workspace(contract, H, dev, workspace):
+    import torch
+    n = rlk_logp_lmhead_workspace_size(contract, H)
+    if n == 0:
+        check(rlk_logp_check_contract(contract) or RLK_ERR_UNSUPPORTED)
+    if workspace is None:
+        return torch.empty(n, dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", n, ("uint8",))
+    return workspace
+
+
+def _rowwise(contract, targets, mask, **f32):
+    """targets int64 [T], mask uint8/bool [T] (None in ignore_index mode) and FP32 [T] vectors."""
+    T = contract.T
+    _need(targets, "targets", 8 * T, _I64)
+    _need(mask, "mask", T, _U8, optional=True)
+    for name, t in f32.items():
+        _need(t, name, 4 * T, _F32)
+
+
 def _stream(stream):
     import torch
     return (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
@@ -312,8 +401,10 @@ def logp_fwd(contract, logits, targets, mask=None, partials=False, stream=None, 
     import torch
     dev = logits.device
     T = contract.T
+    _need_rows(logits, "logits", contract.T, contract.row_stride or contract.V_padded, contract.V_padded, _BF16)
     logp, lse = out if out is not None else (torch.empty(T, dtype=torch.float32, device=dev),
                                              torch.empty(T, dtype=torch.float32, device=dev))
+    _rowwise(contract, targets, mask, logp=logp, lse=lse)
     part = torch.empty((T, contract.num_tiles, 2), dtype=torch.float32, device=dev) if partials else None
     ws = workspace_for(contract, dev, stream)
     check(rlk_logp_fwd(contract, _ptr(logits), _ptr(targets), _ptr(mask), _ptr(logp), _ptr(lse), _ptr(part),
@@ -323,10 +414,10 @@ def logp_fwd(contract, logits, targets, mask=None, partials=False, stream=None, 
 
 def logp_bwd(contract, logits, targets, mask, lse, grad, dlogits=None, stream=None):
     """BF16 dlogits [T, row_stride] from the forward's LSE (the logits are re-read)."""
-    import torch
     dev = logits.device
-    if dlogits is None:
-        dlogits = torch.empty_like(logits)
+    _need_rows(logits, "logits", contract.T, contract.row_stride or contract.V_padded, contract.V_padded, _BF16)
+    _rowwise(contract, targets, mask, lse=lse, grad=grad)
+    dlogits = _dlogits_out(contract, logits, dlogits)
     ws = workspace_for(contract, dev, stream)
     check(rlk_logp_bwd(contract, _ptr(logits), _ptr(targets), _ptr(mask), _ptr(lse), _ptr(grad),
                        _ptr(dlogits), None, None, _ptr(ws), _stream(stream)))
@@ -338,6 +429,8 @@ def logp_fwd_entropy(contract, logits, targets, mask=None, stream=None):
     import torch
     dev = logits.device
     T = contract.T
+    _need_rows(logits, "logits", contract.T, contract.row_stride or contract.V_padded, contract.V_padded, _BF16)
+    _rowwise(contract, targets, mask)
     logp, lse, ent = (torch.empty(T, dtype=torch.float32, device=dev) for _ in range(3))
     ws = workspace_for(contract, dev, stream)
     check(rlk_logp_fwd_entropy(contract, _ptr(logits), _ptr(targets), _ptr(mask), _ptr(logp), _ptr(lse), _ptr(ent),
@@ -350,6 +443,10 @@ def grpo_loss(logp, advantage, mask, ref_logp=None, beta=0.0, stream=None):
     import torch
     dev = logp.device
     T = logp.numel()
+    _need(logp, "logp", 4 * T, _F32)
+    _need(advantage, "advantage", 4 * T, _F32)
+    _need(mask, "mask", T, _U8, optional=True)
+    _need(ref_logp, "ref_logp", 4 * T, _F32, optional=True)
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     count = torch.empty(1, dtype=torch.float32, device=dev)
     g = torch.empty(T, dtype=torch.float32, device=dev)
@@ -365,8 +462,10 @@ def grpo_fused_step(contract, logits, targets, mask, advantage, ref_logp=None, b
     import torch
     dev = logits.device
     T = contract.T
-    if dlogits is None:
-        dlogits = torch.empty_like(logits)
+    _need_rows(logits, "logits", contract.T, contract.row_stride or contract.V_padded, contract.V_padded, _BF16)
+    _rowwise(contract, targets, mask, advantage=advantage)
+    _need(ref_logp, "ref_logp", 4 * T, _F32, optional=True)
+    dlogits = _dlogits_out(contract, logits, dlogits)
     out = {"dlogits": dlogits}
     for k in ("logp", "lse", "grad"):
         out[k] = torch.empty(T, dtype=torch.float32, device=dev)
@@ -375,6 +474,8 @@ def grpo_fused_step(contract, logits, targets, mask, advantage, ref_logp=None, b
     out["active_count"] = torch.empty(1, dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = torch.empty(max(rlk_grpo_fused_workspace_size(contract), 256), dtype=torch.uint8, device=dev)
+    else:
+        _need(workspace, "workspace", rlk_grpo_fused_workspace_size(contract), ("uint8",))
     check(rlk_grpo_fused_step(contract, _ptr(logits), _ptr(targets), _ptr(mask), _ptr(advantage), _ptr(ref_logp),
                               float(beta), _ptr(dlogits), _ptr(out["logp"]), _ptr(out["lse"]), _ptr(out["grad"]),
                               _ptr(out["entropy"]), _ptr(out["loss"]), _ptr(out["active_count"]), _ptr(workspace),
@@ -387,10 +488,11 @@ def logp_fwd_bwd(contract, logits, targets, mask, grad, dlogits=None, stream=Non
     import torch
     dev = logits.device
     T = contract.T
-    if dlogits is None:
-        dlogits = torch.empty_like(logits)
+    _need_rows(logits, "logits", contract.T, contract.row_stride or contract.V_padded, contract.V_padded, _BF16)
+    dlogits = _dlogits_out(contract, logits, dlogits)
     logp, lse = out if out is not None else (torch.empty(T, dtype=torch.float32, device=dev),
                                              torch.empty(T, dtype=torch.float32, device=dev))
+    _rowwise(contract, targets, mask, grad=grad, logp=logp, lse=lse)
     ws = workspace_for(contract, dev, stream)
     check(rlk_logp_bwd(contract, _ptr(logits), _ptr(targets), _ptr(mask), None, _ptr(grad), _ptr(dlogits),
                        _ptr(logp), _ptr(lse), _ptr(ws), _stream(stream)))
@@ -402,8 +504,9 @@ def logp_fwd_bwd_entropy(contract, logits, targets, mask, grad, dlogits=None, st
     import torch
     dev = logits.device
     T = contract.T
-    if dlogits is None:
-        dlogits = torch.empty_like(logits)
+    _need_rows(logits, "logits", contract.T, contract.row_stride or contract.V_padded, contract.V_padded, _BF16)
+    _rowwise(contract, targets, mask, grad=grad)
+    dlogits = _dlogits_out(contract, logits, dlogits)
     logp, lse, ent = (torch.empty(T, dtype=torch.float32, device=dev) for _ in range(3))
     ws = workspace_for(contract, dev, stream)
     check(rlk_logp_fwd_bwd_entropy(contract, _ptr(logits), _ptr(targets), _ptr(mask), _ptr(grad), _ptr(dlogits),
@@ -428,6 +531,12 @@ def logp_fwd_bwd_host(contract, logits, targets, mask, grad, device, chunk_rows=
     """
     import torch
     T = contract.T
+    stride = contract.row_stride or contract.V_padded
+    if logits.dim() != 2 or logits.shape[0] < T or logits.shape[1] < stride:
+        raise ValueError(f"logits must be [T >= {T}, row_stride >= {stride}], not {list(logits.shape)}")
+    for name, t in (("targets", targets), ("mask", mask), ("grad", grad)):
+        if t is not None and t.numel() < T:
+            raise ValueError(f"{name} must hold T = {T} values")
     comp = torch.cuda.current_stream(device)
     copy = torch.cuda.Stream(device)
     d_logits = staging if staging is not None else torch.empty(logits.shape, dtype=logits.dtype, device=device)
@@ -478,7 +587,10 @@ def logp_fused_lmhead(contract, hidden, weight, targets, mask=None, grad=None, s
     """
     import torch
     dev = hidden.device
-    T, H = hidden.shape
+    H = _lmhead_operands(contract, hidden, weight)
+    T = contract.T
+    _rowwise(contract, targets, mask)
+    _need(grad, "grad", 4 * T, _F32, optional=True)
     logp = torch.empty(T, dtype=torch.float32, device=dev)
     lse = torch.empty(T, dtype=torch.float32, device=dev)
     dh = dwf = dwb = None
@@ -490,10 +602,7 @@ def logp_fused_lmhead(contract, hidden, weight, targets, mask=None, grad=None, s
             dwf = torch.empty(weight.shape, dtype=torch.float32, device=dev)
         if dweight_dtype in ("bf16", "both"):
             dwb = torch.empty_like(weight)
-    n = rlk_logp_lmhead_workspace_size(contract, H)
-    if n == 0:
-        check(rlk_logp_check_contract(contract) or RLK_ERR_UNSUPPORTED)
-    ws = workspace if workspace is not None else torch.empty(n, dtype=torch.uint8, device=dev)
+    ws = _lmhead_workspace(contract, H, dev, workspace)
     check(rlk_logp_fused_lmhead(contract, _ptr(hidden), H, _ptr(weight), _ptr(targets), _ptr(mask), _ptr(grad),
                                 _ptr(logp), _ptr(lse), _ptr(dh), _ptr(dwf), _ptr(dwb), _ptr(ws), _stream(stream)))
     if grad is None:
@@ -508,16 +617,14 @@ def logp_fused_lmhead_bwd(contract, hidden, weight, targets, mask, lse, grad, st
     logp_fused_lmhead."""
     import torch
     dev = hidden.device
-    T, H = hidden.shape
+    H = _lmhead_operands(contract, hidden, weight)
+    _rowwise(contract, targets, mask, lse=lse, grad=grad)
     if dweight_dtype not in ("bf16", "f32", "both"):
         raise ValueError("dweight_dtype must be bf16, f32 or both")
     dh = torch.empty_like(hidden)
     dwf = torch.empty(weight.shape, dtype=torch.float32, device=dev) if dweight_dtype in ("f32", "both") else None
     dwb = torch.empty_like(weight) if dweight_dtype in ("bf16", "both") else None
-    n = rlk_logp_lmhead_workspace_size(contract, H)
-    if n == 0:
-        check(rlk_logp_check_contract(contract) or RLK_ERR_UNSUPPORTED)
-    ws = workspace if workspace is not None else torch.empty(n, dtype=torch.uint8, device=dev)
+    ws = _lmhead_workspace(contract, H, dev, workspace)
     check(rlk_logp_fused_lmhead_bwd(contract, _ptr(hidden), H, _ptr(weight), _ptr(targets), _ptr(mask), _ptr(lse),
                                     _ptr(grad), _ptr(dh), _ptr(dwf), _ptr(dwb), _ptr(ws), _stream(stream)))
     return dh, {"bf16": dwb, "f32": dwf, "both": (dwf, dwb)}[dweight_dtype]
@@ -528,14 +635,13 @@ def logp_fused_lmhead_keep(contract, hidden, weight, targets, mask=None, stream=
     logp_fused_lmhead_bwd_kept (T * V_padded * 4 bytes)."""
     import torch
     dev = hidden.device
-    T, H = hidden.shape
+    H = _lmhead_operands(contract, hidden, weight)
+    T = contract.T
+    _rowwise(contract, targets, mask)
     logp = torch.empty(T, dtype=torch.float32, device=dev)
     lse = torch.empty(T, dtype=torch.float32, device=dev)
     logits = torch.empty((T, weight.shape[0]), dtype=torch.float32, device=dev)
-    n = rlk_logp_lmhead_workspace_size(contract, H)
-    if n == 0:
-        check(rlk_logp_check_contract(contract) or RLK_ERR_UNSUPPORTED)
-    ws = workspace if workspace is not None else torch.empty(n, dtype=torch.uint8, device=dev)
+    ws = _lmhead_workspace(contract, H, dev, workspace)
     check(rlk_logp_fused_lmhead_keep(contract, _ptr(hidden), H, _ptr(weight), _ptr(targets), _ptr(mask), _ptr(logp),
                                      _ptr(lse), _ptr(logits), _ptr(ws), _stream(stream)))
     return logp, lse, logits
@@ -546,16 +652,15 @@ def logp_fused_lmhead_bwd_kept(contract, hidden, weight, targets, mask, lse, log
     """(dhidden, dweight) from the logits and LSE of logp_fused_lmhead_keep; bitwise logp_fused_lmhead_bwd's."""
     import torch
     dev = hidden.device
-    T, H = hidden.shape
+    H = _lmhead_operands(contract, hidden, weight)
+    _rowwise(contract, targets, mask, lse=lse, grad=grad)
+    _need(logits, "logits", 4 * contract.T * contract.V_padded, _F32)
     if dweight_dtype not in ("bf16", "f32", "both"):
         raise ValueError("dweight_dtype must be bf16, f32 or both")
     dh = torch.empty_like(hidden)
     dwf = torch.empty(weight.shape, dtype=torch.float32, device=dev) if dweight_dtype in ("f32", "both") else None
     dwb = torch.empty_like(weight) if dweight_dtype in ("bf16", "both") else None
-    n = rlk_logp_lmhead_workspace_size(contract, H)
-    if n == 0:
-        check(rlk_logp_check_contract(contract) or RLK_ERR_UNSUPPORTED)
-    ws = workspace if workspace is not None else torch.empty(n, dtype=torch.uint8, device=dev)
+    ws = _lmhead_workspace(contract, H, dev, workspace)
     check(rlk_logp_fused_lmhead_bwd_kept(contract, _ptr(hidden), H, _ptr(weight), _ptr(targets), _ptr(mask),
                                          _ptr(lse), _ptr(logits), _ptr(grad), _ptr(dh), _ptr(dwf), _ptr(dwb), _ptr(ws),
                                          _stream(stream)))
@@ -577,6 +682,9 @@ def shard_fwd(contract, shard, logits_shard, targets, mask=None, stream=None, wo
     import torch
     dev = logits_shard.device
     T = contract.T
+    vs = contract.V_padded // contract.virtual_tp
+    _need_rows(logits_shard, "logits_shard", T, contract.row_stride or vs, vs, _BF16)
+    _rowwise(contract, targets, mask)
     part = torch.empty((T, contract.num_tiles // contract.virtual_tp, 2), dtype=torch.float32, device=dev)
     xt = torch.empty(T, dtype=torch.float32, device=dev)
     ws = workspace if workspace is not None else shard_workspace(contract, dev)
@@ -591,6 +699,9 @@ def fold_gathered(contract, gathered_partials, gathered_target_logit, targets, m
     import torch
     dev = gathered_partials.device
     T = contract.T
+    _need(gathered_partials, "gathered_partials", 8 * T * contract.num_tiles, _F32)
+    _need(gathered_target_logit, "gathered_target_logit", 4 * T * contract.virtual_tp, _F32)
+    _rowwise(contract, targets, mask)
     logp = torch.empty(T, dtype=torch.float32, device=dev)
     lse = torch.empty(T, dtype=torch.float32, device=dev)
     ws = workspace if workspace is not None else shard_workspace(contract, dev)
@@ -601,10 +712,12 @@ def fold_gathered(contract, gathered_partials, gathered_target_logit, targets, m
 
 def shard_bwd(contract, shard, logits_shard, targets, mask, lse, grad, dlogits=None, stream=None, workspace=None):
     """BF16 dlogits of one vocabulary shard [T, row_stride] (columns [0, V_padded/tp) written)."""
-    import torch
     dev = logits_shard.device
-    if dlogits is None:
-        dlogits = torch.empty_like(logits_shard)
+    vs = contract.V_padded // contract.virtual_tp
+    stride = contract.row_stride or vs
+    _need_rows(logits_shard, "logits_shard", contract.T, stride, vs, _BF16)
+    _rowwise(contract, targets, mask, lse=lse, grad=grad)
+    dlogits = _dlogits_out(contract, logits_shard, dlogits, stride=stride, width=vs)
     ws = workspace if workspace is not None else shard_workspace(contract, dev)
     check(rlk_logp_shard_bwd(contract, shard, _ptr(logits_shard), _ptr(targets), _ptr(mask), _ptr(lse), _ptr(grad),
                              _ptr(dlogits), _ptr(ws), _stream(stream)))
