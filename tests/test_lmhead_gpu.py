@@ -373,3 +373,36 @@ def test_lmhead_kept_logits_forward_and_backward(case):
     with pytest.raises(rlk.RlkError) as ei:
         rlk.logp_fused_lmhead_bwd_kept(c, dh_, dw_, dt, dm, l2, logits, dg)
     assert ei.value.status == rlk.RLK_ERR_NONFINITE_LSE
+
+
+def test_lmhead_ragged_last_band_of_token_blocks():
+    """At H = 4096 a band of the logits GEMMs' unit order is 32 token blocks (32 MB of hidden); 5000
+    rows are 40 blocks, a full band and a ragged one of 8.  Forward and backward against the oracle,
+    bitwise across virtual TP, in both the one-call form and the split form that keeps the logits."""
+    T, H, v_real, v_padded, nt = 5000, 4096, 600, 608, 2
+    hb, wb = make(T, H, v_real, v_padded, seed=61, w_sigma=0.05)
+    tgt = synth.targets(T, v_real, seed=61)
+    mask = (np.arange(T) % 9 != 4).astype(np.uint8)
+    g = np.where(mask != 0, np.random.default_rng(61).standard_normal(T), 0.0).astype(np.float32)
+    act = mask != 0
+    ref_logp, ref_lse, _ = oracle.lmhead_forward(hb, wb, tgt, act, v_real)
+    ref_dh, ref_dw, sc_dh, sc_dw = grad_bounds(hb, wb, tgt, act, g, v_real)
+    dh_, dw_, dt, dm, dg = dev(hb), dev(wb), torch.from_numpy(tgt).cuda(), torch.from_numpy(mask).cuda(), \
+        torch.from_numpy(g).cuda()
+    outs = set()
+    for vtp in (1, 2):
+        c = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=nt, virtual_tp=vtp, validate=1)
+        logp, lse, dh, dw = rlk.logp_fused_lmhead(c, dh_, dw_, dt, dm, grad=dg)
+        _, lse_k, logits = rlk.logp_fused_lmhead_keep(c, dh_, dw_, dt, dm)
+        dh2, dw2 = rlk.logp_fused_lmhead_bwd_kept(c, dh_, dw_, dt, dm, lse_k, logits, dg)
+        dh3, dw3 = rlk.logp_fused_lmhead_bwd(c, dh_, dw_, dt, dm, lse, dg)
+        torch.cuda.synchronize()
+        close("lse", lse.cpu().numpy(), ref_lse)
+        close("logp", logp.cpu().numpy()[act], ref_logp[act])
+        dhb, dwb = dh.cpu().numpy().view(np.uint16), dw.cpu().numpy().view(np.uint16)
+        assert np.all(within(dhb, ref_dh, sc_dh))
+        assert np.all(within(dwb[:v_real], ref_dw, sc_dw)) and np.all(dwb[v_real:] == 0)
+        for a, b in ((dh, dh2), (dw, dw2), (dh, dh3), (dw, dw3), (lse, lse_k)):
+            assert torch.equal(a, b), vtp
+        outs.add((logp.cpu().numpy().tobytes(), lse.cpu().numpy().tobytes(), dhb.tobytes(), dwb.tobytes()))
+    assert len(outs) == 1
