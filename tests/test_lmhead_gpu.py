@@ -406,3 +406,30 @@ def test_lmhead_ragged_last_band_of_token_blocks():
             assert torch.equal(a, b), vtp
         outs.add((logp.cpu().numpy().tobytes(), lse.cpu().numpy().tobytes(), dhb.tobytes(), dwb.tobytes()))
     assert len(outs) == 1
+
+
+def test_lmhead_gradient_ragged_band_of_h_blocks():
+    """The gradient GEMMs take their 256-wide H blocks in bands of 8; H = 2368 is 10 blocks (the last
+    64 wide), a full band and a ragged one of 2.  dHidden and dW against the oracle, bitwise across
+    virtual TP."""
+    T, H, v_real, v_padded, nt = 300, 2368, 1000, 1024, 4
+    hb, wb = make(T, H, v_real, v_padded, seed=67, w_sigma=0.05)
+    tgt = synth.targets(T, v_real, seed=67)
+    mask = (np.arange(T) % 7 != 2).astype(np.uint8)
+    g = np.where(mask != 0, np.random.default_rng(67).standard_normal(T), 0.0).astype(np.float32)
+    act = mask != 0
+    ref_dh, ref_dw, sc_dh, sc_dw = grad_bounds(hb, wb, tgt, act, g, v_real)
+    dh_, dw_, dt, dm, dg = dev(hb), dev(wb), torch.from_numpy(tgt).cuda(), torch.from_numpy(mask).cuda(), \
+        torch.from_numpy(g).cuda()
+    outs = set()
+    for vtp in (1, 4):
+        c = rlk.Contract(T=T, V_real=v_real, V_padded=v_padded, num_tiles=nt, virtual_tp=vtp, validate=1)
+        _, _, dh, dw = rlk.logp_fused_lmhead(c, dh_, dw_, dt, dm, grad=dg, dweight_dtype="f32")
+        torch.cuda.synchronize()
+        dhb, dwf = dh.cpu().numpy().view(np.uint16), dw.cpu().numpy().astype(np.float64)
+        assert np.all(within(dhb, ref_dh, sc_dh))
+        # FP32 dW: the BF16 dlogits' rounding (2^-9) and the FP32 sum, no output rounding
+        assert np.all(np.abs(dwf[:v_real] - ref_dw) <= 2.0 ** -8 * (np.abs(ref_dw) + sc_dw) + 1e-30)
+        assert np.all(dwf[v_real:] == 0.0)
+        outs.add((dhb.tobytes(), dwf.tobytes()))
+    assert len(outs) == 1
