@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import vocab_selected_token_tile_gb300 as rlk
-from parity import check_dlogits, check_fwd, contract
+from parity import check_dlogits, check_entropy, check_fwd, contract
 from synth import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -104,6 +104,50 @@ def test_grpo_fused_full_size_in_bench_configuration(batch):
     ref = oracle.dlogits(batch["bits"][:8], batch["tgt"][rows[:8]], batch["active"][rows[:8]],
                          batch["g"][rows[:8]], w.v_real, w.v_padded)
     assert np.all(np.abs(ref.sum(axis=1)) <= 1e-9 * (np.abs(batch["g"][rows[:8]]) + 1e-30) * w.v_real)
+
+
+def test_grpo_step_and_entropy_full_size(batch):
+    """Two more of the bench's lines at full size, virtual TP 2.  The fused GRPO step (beta 0.01, a
+    reference logp, one advantage per 2048-token sequence, as bench.py draws them) is bitwise the
+    composition forward -> rlk_grpo_loss -> backward from the LSE, and its loss and g are the oracle's
+    on the step's own logp within FP32 rounding.  The fused forward+backward with the entropy gives the
+    fused step's bits and the oracle's entropy on the sampled rows."""
+    w, rows = batch["w"], batch["rows"]
+    T = w.T
+    c = contract(T, w.v_real, w.v_padded, w.num_tiles, BENCH_VTP, validate=0)
+    rng = np.random.default_rng(1)
+    adv = np.repeat(rng.standard_normal(T // 2048 or 1), 2048)[:T].astype(np.float32)
+    ref = (-6.0 * rng.random(T)).astype(np.float32)
+    dadv, dref = torch.from_numpy(adv).cuda(), torch.from_numpy(ref).cuda()
+    dl_a, dl_b = torch.empty_like(batch["logits"]), torch.empty_like(batch["logits"])
+    st = rlk.grpo_fused_step(c, batch["logits"], batch["dt"], batch["dm"], dadv, dref, 0.01, dlogits=dl_a)
+    logp, lse = rlk.logp_fwd(c, batch["logits"], batch["dt"], batch["dm"])
+    loss, g, n = rlk.grpo_loss(logp, dadv, batch["dm"], dref, 0.01)
+    rlk.logp_bwd(c, batch["logits"], batch["dt"], batch["dm"], lse, g, dlogits=dl_b)
+    torch.cuda.synchronize()
+    for k, want in (("logp", logp), ("lse", lse), ("grad", g), ("loss", loss), ("active_count", n)):
+        assert torch.equal(st[k], want), k
+    assert torch.equal(dl_a, dl_b)
+    act = batch["active"]
+    lp = logp.cpu().numpy()
+    ol, og, on = oracle.grpo_loss(lp, adv, act, ref, 0.01)
+    assert float(n.item()) == on
+    eps = 2.0 ** -24
+    d = np.abs(ref.astype(np.float64) - lp)
+    e = np.exp(ref.astype(np.float64) - lp)
+    assert np.all(np.abs(g.cpu().numpy() - og) <= 8 * eps * (np.abs(adv) + 0.01 * (1.0 + e * (1.0 + d))) / on)
+    terms = np.abs(adv * lp) + 0.01 * e * (1.0 + d)
+    assert abs(float(loss.item()) - ol) <= 8 * eps * float(terms[act].sum()) / on + 2 * eps * abs(ol)
+    # the entropy in the fused pass
+    dl_e, lp_e, ls_e, ent = rlk.logp_fwd_bwd_entropy(c, batch["logits"], batch["dt"], batch["dm"], batch["dg"],
+                                                     dlogits=dl_a)
+    dl_f, lp_f, ls_f = rlk.logp_fwd_bwd(c, batch["logits"], batch["dt"], batch["dm"], batch["dg"], dlogits=dl_b)
+    torch.cuda.synchronize()
+    assert torch.equal(lp_e, lp_f) and torch.equal(ls_e, ls_f) and torch.equal(dl_e, dl_f)
+    assert torch.isfinite(ent).all() and (ent >= -1e-4).all()
+    check_entropy(batch["bits"], w.v_real, ent.cpu().numpy()[rows])
+    del dl_a, dl_b, dl_e, dl_f, st
+    torch.cuda.empty_cache()
 
 
 def test_vocabulary_shards_full_size(batch):
