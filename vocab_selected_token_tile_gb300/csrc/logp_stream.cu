@@ -95,6 +95,12 @@ constexpr int64_t kFusedChunkCols = 16384;
 // none of their code (each adds code the fused kernel measured slower with).
 constexpr int kFlagEnt = 1;   // the entropy of each row's softmax
 constexpr int kFlagGrpo = 2;  // the fused GRPO step: g formed on chip (kModeFusedL2)
+// Unrolling of the tile loops in the GRPO instantiations (4 elsewhere).  Their
+// larger code stalls on instruction fetch at two CTAs per SM; measured at
+// virtual TP 8 (65536 x 152576): unroll 2 6.45 ms against 6.76 with 4, while
+// unroll 2 made the plain kernels slower (forward TP 1 2.80 against 2.72 ms,
+// TP 8 3.38 against 3.17, fused TP 8 6.42 against 6.39).
+constexpr int kTileUnrollGrpo = 2;
 
 struct SlotHdr {  // row metadata the producer writes beside each slot
     int64_t target;
@@ -402,7 +408,11 @@ __device__ __forceinline__ float combine8(const float2 (&a)[4]) {
 // redone clamped; both give the same bits.  Measured on GB300: skipping it
 // speeds the forward with entropy by 2-3.5% and slows the fused schedule's
 // larger kernel by 4-6%, so the fused schedule clamps everywhere.
-template <bool ENT, bool ENT_CLAMP = true>
+//
+// UNROLL: of the interior loops.  Each lane adds its groups in the same order
+// whatever the unrolling, so the bits do not depend on it; it trades loop
+// overhead against code size (see kTileUnrollGrpo).
+template <bool ENT, bool ENT_CLAMP = true, int UNROLL = 4>
 __device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const TileGeom& t, const GroupRange& gr,
                                int lane, float* t_out) {
     if (ENT) *t_out = 0.f;
@@ -410,7 +420,7 @@ __device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const
     const int ne = gr.lo + (gr.n - gr.hi);
     const uint4* s4 = reinterpret_cast<const uint4*>(slot);
     uint32_t acc[4] = {0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u};
-#pragma unroll 4
+#pragma unroll UNROLL
     for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) max4(acc, s4[gi]);
     for (int e = lane; e < ne; e += 32) max4(acc, load_group(slot, grow, t.a + 8 * edge_group(gr, e), t));
     acc[0] = bf16x2_max_nan(bf16x2_max_nan(acc[0], acc[1]), bf16x2_max_nan(acc[2], acc[3]));
@@ -419,7 +429,7 @@ __device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const
     const float nmL = -__fmul_rn(m, kLog2e);
     float2 sm[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     if constexpr (!ENT) {
-#pragma unroll 4
+#pragma unroll UNROLL
         for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) sum8(sm, s4[gi], nmL);
         for (int e = lane; e < ne; e += 32)
             sum8(sm, load_group(slot, grow, t.a + 8 * edge_group(gr, e), t), nmL);
@@ -429,7 +439,7 @@ __device__ float2 tile_partial(const uint16_t* slot, const uint16_t* grow, const
         // clamp, which only a -inf logit needs.  Edge groups (masked columns
         // read as -inf) always clamp.
         float2 tm[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll 4
+#pragma unroll UNROLL
         for (int gi = gr.lo + lane; gi < gr.hi; gi += 32) sum8_ent<ENT_CLAMP>(sm, tm, s4[gi], nmL);
         for (int e = lane; e < ne; e += 32)
             sum8_ent<true>(sm, tm, load_group(slot, grow, t.a + 8 * edge_group(gr, e), t), nmL);
@@ -1068,7 +1078,8 @@ __device__ bool phase_a(const Params& p, const Ctx& x, int64_t n, uint32_t item0
         const TileGeom& tg = m.g;
         const uint16_t* sl = slots + (size_t)it.slot * slot_elems + m.soff;
         float tk = 0.f;
-        const float2 pr = tile_partial<ENT, MODE != kModeFwd>(sl, grow, tg, m.ga, lane, &tk);
+        const float2 pr =
+            tile_partial<ENT, MODE != kModeFwd, GRPO ? kTileUnrollGrpo : 4>(sl, grow, tg, m.ga, lane, &tk);
         if (lane == 0) {
             RowShared& rs = x.rows[b];
             if (l == 0) {
