@@ -101,6 +101,13 @@ constexpr int kFlagGrpo = 2;  // the fused GRPO step: g formed on chip (kModeFus
 // unroll 2 made the plain kernels slower (forward TP 1 2.80 against 2.72 ms,
 // TP 8 3.38 against 3.17, fused TP 8 6.42 against 6.39).
 constexpr int kTileUnrollGrpo = 2;
+// Unrolling of the fold's 64-step recurrence in the fused L2 schedule without
+// the entropy (64 elsewhere).  The same bits; measured at 65536 x 152576 (same
+// box): fused TP 8 6.33 ms against 6.39 fully unrolled, TP 4 6.16 against
+// 6.14, TP 1-2 unchanged; the forward at TP 8 (3.30 against 3.17 ms) and the
+// entropy paths got slower with 8, and choosing by cluster size at run time
+// (both folds in the kernel) made the GRPO step at TP 8 slower (6.51 ms).
+constexpr int kFoldUnrollFusedL2 = 8;
 
 struct SlotHdr {  // row metadata the producer writes beside each slot
     int64_t target;
@@ -840,7 +847,7 @@ __device__ __noinline__ float grpo_row_grad(const Params& p, bool active, float 
     return (active ? dterm : 0.f) * inv_nf;
 }
 
-template <int F>
+template <int MODE, int F>
 __device__ void fold_row(const Params& p, const Ctx& x, int64_t n, float inv_nf) {
     constexpr bool ENT = (F & kFlagEnt) != 0, GRPO = (F & kFlagGrpo) != 0;
     const int lane = x.lane;
@@ -853,7 +860,7 @@ __device__ void fold_row(const Params& p, const Ctx& x, int64_t n, float inv_nf)
         lse_v = r.x;
         ent_v = r.y;
     } else {
-        lse_v = fold_tiles(part, p.NT, x.fold, lane);
+        lse_v = fold_tiles<MODE == kModeFusedL2 ? kFoldUnrollFusedL2 : 64>(part, p.NT, x.fold, lane);
     }
     const int64_t row = x.q + n * x.G;
     if (p.a.partials) {
@@ -934,7 +941,7 @@ __device__ void fold_warp(const Params& p, const Ctx& x) {
         }
         if (nf < R && nf < np &&
             (p.C == 1 || warp_test(x.xbar0 + 8u * row_buf(p, nf), row_par(p, nf), true))) {
-            fold_row<F>(p, x, nf, inv_nf);
+            fold_row<MODE, F>(p, x, nf, inv_nf);
             nf += fstep;
             progressed = true;
         }

@@ -73,17 +73,34 @@ __device__ __forceinline__ void load_parts64(const float2* part, int NT, int lan
 // and the terms b_k = s_k exp(m_k - M_k) are formed lane-parallel (beyond 64
 // tiles into scratch[0..NT)); the sum recurrence S_k = S_{k-1} f_k + b_k then
 // runs in index order.
+//
+// UNROLL: of the 64-step recurrence when NT <= 64 (64: fully unrolled).  The
+// steps run in index order either way, so the bits do not depend on it.
+template <int UNROLL = 64>
 __device__ __forceinline__ float fold_tiles(const float2* part, int NT, float2* scratch, int lane) {
     if (NT <= 64) {
         float2 p[2];
         load_parts64(part, NT, lane, p);
         const FoldTerms t = fold_terms64(p, lane);
         float S = 0.f;
+        if constexpr (UNROLL >= 64) {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-            const float f = __shfl_sync(0xFFFFFFFFu, t.f[k >> 5], k & 31);
-            const float b = __shfl_sync(0xFFFFFFFFu, t.b[k >> 5], k & 31);
-            if (k < NT) S = __fmaf_rn(S, f, b);
+            for (int k = 0; k < 64; ++k) {
+                const float f = __shfl_sync(0xFFFFFFFFu, t.f[k >> 5], k & 31);
+                const float b = __shfl_sync(0xFFFFFFFFu, t.b[k >> 5], k & 31);
+                if (k < NT) S = __fmaf_rn(S, f, b);
+            }
+        } else {
+            // k = 32 h + j; h fixed per half keeps t.f[h] and t.b[h] in registers
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll UNROLL
+                for (int j = 0; j < 32; ++j) {
+                    const float f = __shfl_sync(0xFFFFFFFFu, t.f[h], j);
+                    const float b = __shfl_sync(0xFFFFFFFFu, t.b[h], j);
+                    if (32 * h + j < NT) S = __fmaf_rn(S, f, b);
+                }
+            }
         }
         return (t.M == -INFINITY) ? -INFINITY : __fadd_rn(t.M, logf(S));
     }
