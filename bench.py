@@ -565,6 +565,35 @@ def lmhead_bench(rlk, args, dev, clock_index, steps=10, warmup=3, rows=0, bwd=Tr
                        "T*V_padded*10 bytes for the stored FP32 logits and the BF16 dlogits (an HBM-bound pass "
                        "between the GEMMs), which this tensor figure leaves out"}
     if rows == 0 and args.path == "fused":
+        # The split forms an autograd forward and backward use: the forward keeping its FP32 logits,
+        # then the backward from them (lmhead_logprob(keep_logits=True)); and the forward, then the
+        # backward from the saved LSE, which re-runs the GEMM (the default).
+        xl = torch.empty((T, Vp), dtype=torch.float32, device=dev)
+
+        def split_keep():
+            rlk.check(rlk.rlk_logp_fused_lmhead_keep(c, hd.data_ptr(), H, wd.data_ptr(), tgt.data_ptr(),
+                                                     mask.data_ptr(), logp.data_ptr(), lse.data_ptr(), xl.data_ptr(),
+                                                     wsb.data_ptr(), stream.cuda_stream))
+            rlk.check(rlk.rlk_logp_fused_lmhead_bwd_kept(c, hd.data_ptr(), H, wd.data_ptr(), tgt.data_ptr(),
+                                                         mask.data_ptr(), lse.data_ptr(), xl.data_ptr(), g.data_ptr(),
+                                                         dh.data_ptr(), None, dw.data_ptr(), wsb.data_ptr(),
+                                                         stream.cuda_stream))
+
+        def split_recompute():
+            rlk.check(rlk.rlk_logp_fused_lmhead(c, hd.data_ptr(), H, wd.data_ptr(), tgt.data_ptr(), mask.data_ptr(),
+                                                None, logp.data_ptr(), lse.data_ptr(), None, None, None,
+                                                wsb.data_ptr(), stream.cuda_stream))
+            rlk.check(rlk.rlk_logp_fused_lmhead_bwd(c, hd.data_ptr(), H, wd.data_ptr(), tgt.data_ptr(),
+                                                    mask.data_ptr(), lse.data_ptr(), g.data_ptr(), dh.data_ptr(),
+                                                    None, dw.data_ptr(), wsb.data_ptr(), stream.cuda_stream))
+        _, ms_k, clk_k = timed(split_keep, steps, warmup, stream, clock_index, per_launch=False)
+        _, ms_r, clk_r = timed(split_recompute, steps, warmup, stream, clock_index, per_launch=False)
+        del xl
+        bwd_res["split"] = {"keep_logits_ms": ms_k, "recompute_ms": ms_r, "clocks_keep_logits": clk_k,
+                            "clocks_recompute": clk_r,
+                            "note": "forward then backward as two calls, as autograd runs them: keeping the FP32 "
+                                    "logits (T*V_padded*4 bytes held between them) or re-running the GEMM from "
+                                    "the saved LSE"}
         out["fwd_bwd"] = bwd_res
         return out
     return {**bwd_res, "workload": out["workload"].replace("lmhead fwd", "lmhead fwd+bwd"),
